@@ -1,0 +1,365 @@
+#!/usr/bin/env python
+"""Benchmark of the DFlash 2 drafter hot path on GB300.
+
+One step = the whole path once: a context append of `block` new target rows
+(taps -> FC -> hidden_norm -> every layer's K/V, written at the end of the
+context) and one block of `block` rows anchored after them (draft layers,
+head, draft tokens).  Default workload: the Qwen3-8B-shaped drafter, one
+sequence, context 2048 (the context is prefilled with 2048 - block rows; each
+step re-appends the last `block` rows at the same positions, so every step
+sees 2048 context rows).
+
+value: draft tokens/s with inputs and outputs resident in HBM (CUDA events on
+the launching stream).  e2e: the same through the host-buffer API (pinned
+host taps and anchors in, logits and tokens out, copies inside the timed
+region).  roofline: the kernel with the largest device time in a profiled
+pass of the same steps.  cpu_baseline / --impl reference: the CPU oracle.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "DFlash block latency ms & draft tokens/s; achieved HBM GB/s vs GB300 peak"
+UNIT = "draft tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "block_speculative_drafting_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(d, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or
+    None when there is none for this workload or the kernels changed since."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d[workload][kernel]
+        if e.get("source_hash") != kernel_source_hash():
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.idx = device_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        inside = [r for r in rows if t0 - 0.15 <= r[0] <= t1 + 0.15] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in inside for n, v in zip(names, r[3]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside)}
+
+
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def oracle_step_timer(wl, weights, steps_wanted, budget_s):
+    """Time the CPU oracle on steps of the workload.  Returns (seconds per
+    step, steps timed, cores).  The oracle model build and the context
+    prefill are not timed."""
+    from oracle import OracleModel, OracleSeq, block
+
+    g = wl.geom
+    om = OracleModel(g, weights)
+    osq = OracleSeq(om)
+    pre = wl.ctx - g.block
+    osq.append(0, W.make_taps(g, pre, call_id=0))
+    taps = W.make_taps(g, g.block, call_id=1)
+    anchor = int(W.make_anchors(g, 1)[0])
+    times = []
+    t_start = time.perf_counter()
+    while len(times) < steps_wanted:
+        t0 = time.perf_counter()
+        osq.append(pre, taps)
+        block(om, osq, anchor, wl.ctx, g.block)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_start + times[-1] > budget_s:
+            break
+    return statistics.median(times), len(times), cpu_threads()
+
+
+def run_reference(args, wl):
+    rank = env_int("RANK", 0)
+    if rank != 0:
+        return
+    g = wl.geom
+    weights = W.make_weights(g)
+    # the reference arm's step: one full oracle step (append + block); the
+    # warm-up and timed counts are bounded so the run ends in a few minutes
+    sec, n, cores = oracle_step_timer(wl, weights, max(1, args.steps), budget_s=args.cpu_budget)
+    value = g.block - 1 if False else (g.block - 1) / sec
+    sample = (f"{n} full step(s) (append {g.block} rows + one {g.block}-row block) of {wl.name} on the CPU oracle; "
+              "oracle build and context prefill untimed")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": n,
+        "warmup": 0, "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded Gaussian weights and taps)",
+        "config": {"workload": wl.name, "n_seqs": wl.n_seqs, "ctx": wl.ctx, "block": g.block},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, wl):
+    import torch
+
+    import block_speculative_drafting_gb300 as dfl
+
+    rank, world, local = env_int("RANK", 0), env_int("WORLD_SIZE", 1), env_int("LOCAL_RANK", 0)
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist = dist_mod
+        dist.init_process_group("nccl")
+    g = wl.geom
+    B = g.block
+    t_setup = time.perf_counter()
+    weights = W.make_weights(g)
+    model = dfl.Model(g, weights)
+    seq = model.new_sequence(wl.ctx + 2 * B)
+    pre = wl.ctx - B
+    model.ctx_append(seq, 0, W.make_taps(g, pre, call_id=0))
+    taps_h = W.make_taps(g, B, call_id=1)
+    anchor = int(W.make_anchors(g, 1)[0])
+    dev = torch.device("cuda", local)
+    taps_d = torch.from_numpy(taps_h).to(dev)
+    anchor_d = torch.tensor([anchor], dtype=torch.int32, device=dev)
+    logits_d = torch.empty((1, B - 1, g.vocab), dtype=torch.float32, device=dev)
+    tok_d = torch.empty((1, B - 1), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    setup_s = time.perf_counter() - t_setup
+
+    def step():
+        model.ctx_append(seq, pre, taps_d)
+        model.block([seq], anchor_d, [wl.ctx], B, logits=logits_d, tokens=tok_d)
+
+    def barrier():
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    n0 = model.launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    barrier()
+    t_wall1 = time.time()
+    launches = model.launch_count() - n0
+    ms = e0.elapsed_time(e1) / args.steps
+    clocks.stop()
+    clk = clocks.summary(t_wall0, t_wall1)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * (B - 1) / (ms * 1e-3)
+
+    # profiled pass: the same steps with every launch bracketed by events
+    model.profile_start()
+    pe0, pe1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pe0.record(stream)
+    for _ in range(args.steps):
+        step()
+    pe1.record(stream)
+    torch.cuda.synchronize()
+    prof = model.profile_stop()
+    prof_ms = pe0.elapsed_time(pe1) / args.steps
+    top = max(prof.items(), key=lambda kv: kv[1][1])
+    name, (nl, tms, tbytes) = top
+    achieved = tbytes / (tms * 1e-3) / 1e9  # GB/s, algorithmic bytes over device time
+    peak, peak_kind = measured_peaks()
+    step_bytes = sum(v[2] for v in prof.values()) / args.steps
+    traffic = ncu_traffic(name, wl.name)
+    roofline = {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_kind == "measured" else "fallback 6800 GB/s",
+                "traffic": traffic, "algorithmic_bytes_per_launch": tbytes / nl,
+                "avg_launch_us": tms / nl * 1e3, "launches_per_step": nl / args.steps}
+    kernels = {k: {"launches_per_step": v[0] / args.steps, "ms_per_step": v[1] / args.steps,
+                   "share": v[1] / sum(x[1] for x in prof.values()), "GBps": v[2] / (v[1] * 1e-3) / 1e9}
+               for k, v in sorted(prof.items(), key=lambda kv: -kv[1][1])}
+
+    # end to end through the host-buffer API: pinned host taps and anchor in,
+    # logits and tokens out, every copy inside the timed region
+    taps_p = torch.from_numpy(taps_h).pin_memory().numpy()
+    logits_p = torch.empty((1, B - 1, g.vocab), dtype=torch.float32).pin_memory().numpy()
+    tok_p = torch.empty((1, B - 1), dtype=torch.int32).pin_memory().numpy().view(np.uint32)
+    anchors_p = np.array([anchor], dtype=np.uint32)
+
+    def step_host():
+        model.ctx_append(seq, pre, taps_p)
+        model.block([seq], anchors_p, [wl.ctx], B, logits=logits_p, tokens=tok_p)
+
+    for _ in range(max(1, args.warmup // 2)):
+        step_host()
+    barrier()
+    k_e2e = args.steps
+    t0 = time.perf_counter()
+    for _ in range(k_e2e):
+        step_host()
+    barrier()
+    e2e_s = (time.perf_counter() - t0) / k_e2e
+    if dist:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e = {"value": world * (B - 1) / e2e_s, "unit": UNIT, "ms_per_step": e2e_s * 1e3,
+           "h2d_bytes_per_step": int(taps_p.nbytes + anchors_p.nbytes),
+           "d2h_bytes_per_step": int(logits_p.nbytes + tok_p.nbytes)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sec, n, cores = oracle_step_timer(wl, weights, 3, budget_s=args.cpu_budget)
+        cpu = {"value": (B - 1) / sec, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"median of {n} full step(s) (append {B} rows + one {B}-row block) of {wl.name}; "
+                         "oracle build and context prefill untimed"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int4xint8 (f32 accumulate)",
+            "data": "synthetic (seeded Gaussian weights N(0,0.02), taps N(0,1))",
+            "config": {"workload": wl.name, "n_seqs": wl.n_seqs, "ctx": wl.ctx, "block": B,
+                       "step": f"ctx_append({B} rows) + block({B} rows)", "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (1.3 GB of weights streamed each step)"},
+            "block_latency_ms": ms, "hbm_gbs_step": step_bytes / (ms * 1e-3) / 1e9,
+            "algorithmic_bytes_per_step": step_bytes, "profiled_ms_per_step": prof_ms,
+            "roofline": roofline, "kernels": kernels, "e2e": e2e, "cpu_baseline": cpu,
+            "gpu_launches": launches, "clocks": clk, "setup_s": setup_s,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="qwen3_8b_ctx2048", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=60.0, help="seconds of CPU oracle steps at most")
+    args = ap.parse_args()
+    wl = W.WORKLOADS[args.workload]
+    if wl.n_seqs != 1 or wl.prefill:
+        raise SystemExit("bench.py times the single-sequence decode workloads")
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

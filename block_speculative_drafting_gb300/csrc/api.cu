@@ -1,0 +1,935 @@
+// The C ABI of include/dflash.h: model and sequence state, weight upload and
+// packing, and the order of kernels of a context append and of a block.
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/dflash.h"
+#include "common.cuh"
+#include "kernels.cuh"
+
+using namespace dflash;
+
+namespace {
+
+thread_local std::string g_init_error;
+
+// Context rows projected per pass of an append (bounds the scratch buffers).
+constexpr int64_t kAppendRows = 1024;
+
+struct DevBuf {
+    void* p = nullptr;
+    size_t bytes = 0;
+};
+
+struct Layer {
+    float *in_norm = nullptr, *post_norm = nullptr, *q_norm = nullptr, *k_norm = nullptr;
+    uint8_t *qkv_p = nullptr, *o_p = nullptr, *gu_p = nullptr, *down_p = nullptr;  // 4-bit packed
+    float *qkv_f = nullptr, *o_f = nullptr, *gu_f = nullptr, *down_f = nullptr;    // f32
+};
+
+struct MatView {
+    const uint8_t* packed;
+    const float* f32;
+    int tile0, N, K, ksteps;
+};
+
+}  // namespace
+
+struct dflash_model {
+    dflash_geometry g{};
+    int device = 0, num_sms = kSMs;
+    bool poisoned = false;
+    std::string err;
+    std::vector<void*> owned;  // device allocations freed with the model
+    int live_seqs = 0;
+
+    float *embed = nullptr, *hidden_norm = nullptr, *norm = nullptr, *inv_freq = nullptr;
+    uint8_t *fc_p = nullptr, *kvctx_p = nullptr;
+    float *fc_f = nullptr, *kvctx_f = nullptr, *head_f = nullptr;
+    int8_t* head_p = nullptr;
+    float* head_scale = nullptr;
+    std::vector<Layer> layers;
+    const float** k_norm_dev = nullptr;  // [L] device pointers to k_norm
+
+    int qd = 0, kd = 0, qkv_w = 0, tap_w = 0, kvctx_w = 0;
+    int ks_h = 0, ks_i = 0, ks_q = 0, ks_tap = 0;
+
+    // launch accounting and the optional per-launch event profile
+    int64_t launches = 0;  // kernels of this library launched since init
+    bool profiling = false;
+    struct ProfRec {
+        const char* name;
+        cudaEvent_t e0, e1;
+        double bytes;
+        int kernels;
+    };
+    std::vector<ProfRec> prof_open;
+    std::vector<cudaEvent_t> ev_pool;
+    struct ProfSum {
+        const char* name;
+        int64_t launches = 0;
+        double ms = 0, bytes = 0;
+    };
+    std::vector<ProfSum> prof_sum;
+
+    // scratch, grown on demand (a call that needs more memory than any call
+    // before it allocates; calls of the same sizes allocate nothing)
+    DevBuf h, xq, xs, qkv, y, gu, logits, keys, toks, part, anchors, pos0, aseqs;
+    DevBuf a_taps, a_codes, a_scale, a_t, a_kv;
+};
+
+struct dflash_seq {
+    dflash_model* m = nullptr;
+    int64_t cap = 0, first = 0, len = 0;
+    std::vector<float*> k, v;          // per layer [nkv][cap][hd]
+    float** k_dev = nullptr;           // device arrays of the per-layer pointers
+    float** v_dev = nullptr;
+};
+
+namespace {
+
+int set_err(dflash_model* m, int code, const std::string& msg) {
+    if (m)
+        m->err = msg;
+    else
+        g_init_error = msg;
+    return code;
+}
+
+int cuda_fail(dflash_model* m, int e, const char* what) {
+    std::string msg = std::string(what) + ": " + cudaGetErrorString((cudaError_t)e);
+    if (m) m->poisoned = true;
+    return set_err(m, (e == cudaErrorMemoryAllocation) ? DFLASH_ENOMEM : DFLASH_ECUDA, msg);
+}
+
+#define CK(m, expr)                                                      \
+    do {                                                                 \
+        int e__ = (int)(expr);                                           \
+        if (e__ != 0) return cuda_fail((m), e__, #expr);                 \
+    } while (0)
+
+cudaEvent_t pool_event(dflash_model* m) {
+    if (!m->ev_pool.empty()) {
+        cudaEvent_t e = m->ev_pool.back();
+        m->ev_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+// Launch `expr` (a launcher returning a cudaError_t as int) that starts
+// `nk` kernels moving `bytes` algorithmic bytes; with profiling on, bracket
+// it with a pair of events on `st`.
+#define KL(m, name, nk, bytes, st, expr)                                       \
+    do {                                                                       \
+        cudaEvent_t e0__ = nullptr;                                            \
+        if ((m)->profiling) {                                                  \
+            e0__ = pool_event(m);                                              \
+            cudaEventRecord(e0__, (st));                                       \
+        }                                                                      \
+        int e__ = (int)(expr);                                                 \
+        if (e__ != 0) return cuda_fail((m), e__, #expr);                       \
+        (m)->launches += (nk);                                                 \
+        if ((m)->profiling) {                                                  \
+            cudaEvent_t e1__ = pool_event(m);                                  \
+            cudaEventRecord(e1__, (st));                                       \
+            (m)->prof_open.push_back({(name), e0__, e1__, (double)(bytes), (nk)}); \
+        }                                                                      \
+    } while (0)
+
+template <class T>
+int dalloc(dflash_model* m, T** p, size_t count) {
+    void* q = nullptr;
+    cudaError_t e = cudaMalloc(&q, std::max<size_t>(count * sizeof(T), 16));
+    if (e != cudaSuccess) return (int)e;
+    m->owned.push_back(q);
+    *p = static_cast<T*>(q);
+    return 0;
+}
+
+int ensure(DevBuf& b, size_t bytes) {
+    if (b.bytes >= bytes) return 0;
+    if (b.p) cudaFree(b.p);
+    b.p = nullptr;
+    b.bytes = 0;
+    cudaError_t e = cudaMalloc(&b.p, std::max<size_t>(bytes, 256));
+    if (e != cudaSuccess) return (int)e;
+    b.bytes = std::max<size_t>(bytes, 256);
+    return 0;
+}
+
+void free_buf(DevBuf& b) {
+    if (b.p) cudaFree(b.p);
+    b.p = nullptr;
+    b.bytes = 0;
+}
+
+template <class T>
+T* P(const DevBuf& b) {
+    return static_cast<T*>(b.p);
+}
+
+std::string geometry_problem(const dflash_geometry& g) {
+    char buf[256];
+    if (g.layers < 1) return "layers < 1";
+    if (g.block < 2) return "block < 2";
+    if (g.n_taps < 1) return "n_taps < 1";
+    if (g.kv_heads < 1 || g.heads < 1 || g.heads % g.kv_heads) return "heads must be a multiple of kv_heads >= 1";
+    if (g.head_dim != 64 && g.head_dim != 128) return "head_dim must be 64 or 128";
+    if (g.hidden < 64 || g.hidden % 64) return "hidden must be a positive multiple of 64";
+    if (g.intermediate < 64 || g.intermediate % 64) return "intermediate must be a positive multiple of 64";
+    if (g.vocab < 1) return "vocab < 1";
+    if (g.mask_token < 0 || g.mask_token >= g.vocab) return "mask_token outside [0, vocab)";
+    if (g.window != 0) return "window != 0 (per-layer windows are not supported)";
+    if (!(g.eps > 0.f)) return "eps must be > 0";
+    if (!(g.rope_theta > 0.0)) return "rope_theta must be > 0";
+    if (g.quant != DFLASH_QUANT_F32 && g.quant != DFLASH_QUANT_Q4G32) return "unknown quant";
+    if ((int64_t)g.vocab * g.hidden > ((int64_t)1 << 40)) {
+        snprintf(buf, sizeof buf, "vocab * hidden too large");
+        return buf;
+    }
+    return "";
+}
+
+// A weight tensor as a device pointer: `src` itself when the caller's
+// weights are on the device, else copied into `stage`.
+int to_device(dflash_model* m, const float* src, size_t count, bool on_device, float* stage, const float** out) {
+    if (on_device) {
+        *out = src;
+        return 0;
+    }
+    cudaError_t e = cudaMemcpy(stage, src, count * sizeof(float), cudaMemcpyHostToDevice);
+    *out = stage;
+    return (int)e;
+}
+
+int copy_f32(dflash_model* m, float* dst, const float* src, size_t count, bool on_device) {
+    return (int)cudaMemcpy(dst, src, count * sizeof(float), on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice);
+}
+
+MatView mat_view(const dflash_model* m, int id) {
+    const dflash_geometry& g = m->g;
+    MatView v{nullptr, nullptr, 0, 0, 0, 0};
+    if (id == DFLASH_MAT_FC) return MatView{m->fc_p, m->fc_f, 0, g.hidden, m->tap_w, m->ks_tap};
+    if (id == DFLASH_MAT_HEAD) return MatView{nullptr, m->head_f, 0, g.vocab, g.hidden, g.hidden / kI8KStep};
+    int rel = id - 2;
+    if (rel < 0 || rel >= 7 * g.layers) return v;
+    const Layer& L = m->layers[rel / 7];
+    switch (rel % 7) {
+        case DFLASH_Q: return MatView{L.qkv_p, L.qkv_f, 0, m->qd, g.hidden, m->ks_h};
+        case DFLASH_K: return MatView{L.qkv_p, L.qkv_f ? L.qkv_f + (size_t)m->qd * g.hidden : nullptr, m->qd / 16, m->kd, g.hidden, m->ks_h};
+        case DFLASH_V: return MatView{L.qkv_p, L.qkv_f ? L.qkv_f + (size_t)(m->qd + m->kd) * g.hidden : nullptr, (m->qd + m->kd) / 16, m->kd, g.hidden, m->ks_h};
+        case DFLASH_O: return MatView{L.o_p, L.o_f, 0, g.hidden, m->qd, m->ks_q};
+        case DFLASH_GATE: return MatView{L.gu_p, L.gu_f, 0, g.intermediate, g.hidden, m->ks_h};
+        case DFLASH_UP: return MatView{L.gu_p, L.gu_f ? L.gu_f + (size_t)g.intermediate * g.hidden : nullptr, g.intermediate / 16, g.intermediate, g.hidden, m->ks_h};
+        case DFLASH_DOWN: return MatView{L.down_p, L.down_f, 0, g.hidden, g.intermediate, m->ks_i};
+    }
+    return v;
+}
+
+int check_model(dflash_model* m) {
+    if (!m) return DFLASH_EINVAL;
+    if (m->poisoned) return set_err(m, DFLASH_ECUDA, "model poisoned by an earlier CUDA error");
+    cudaError_t e = cudaSetDevice(m->device);
+    if (e != cudaSuccess) return cuda_fail(m, (int)e, "cudaSetDevice");
+    return 0;
+}
+
+int build_model(dflash_model* m, const dflash_weights* w, bool on_dev, cudaStream_t st) {
+    const dflash_geometry& g = m->g;
+    const int H = g.hidden, I = g.intermediate, L = g.layers, hd = g.head_dim;
+    m->qd = g.heads * hd;
+    m->kd = g.kv_heads * hd;
+    m->qkv_w = m->qd + 2 * m->kd;
+    m->tap_w = g.n_taps * H;
+    m->kvctx_w = L * 2 * m->kd;
+    m->ks_h = H / kQ4KStep;
+    m->ks_i = I / kQ4KStep;
+    m->ks_q = m->qd / kQ4KStep;
+    m->ks_tap = m->tap_w / kQ4KStep;
+    const bool quant = g.quant == DFLASH_QUANT_Q4G32;
+
+    // staging buffer for host weights: the largest tensor
+    size_t biggest = std::max({(size_t)H * m->tap_w, (size_t)g.vocab * H, (size_t)I * H, (size_t)m->qd * H});
+    float* stage = nullptr;
+    if (!on_dev) CK(m, dalloc(m, &stage, biggest));
+    __half* sc_scratch = nullptr;
+    if (quant) {
+        size_t most = std::max({(size_t)H * (m->tap_w / 32), (size_t)I * (H / 32), (size_t)H * (I / 32),
+                                (size_t)(m->qd + 16) * (H / 32), (size_t)H * (m->qd / 32)});
+        CK(m, dalloc(m, &sc_scratch, most + 64));
+    }
+
+    // small f32 vectors
+    CK(m, dalloc(m, &m->hidden_norm, H));
+    CK(m, copy_f32(m, m->hidden_norm, w->hidden_norm, H, on_dev));
+    CK(m, dalloc(m, &m->norm, H));
+    CK(m, copy_f32(m, m->norm, w->norm, H, on_dev));
+    CK(m, dalloc(m, &m->embed, (size_t)g.vocab * H));
+    CK(m, copy_f32(m, m->embed, w->embed, (size_t)g.vocab * H, on_dev));
+    std::vector<float> invf(hd / 2);
+    for (int i = 0; i < hd / 2; ++i) invf[i] = (float)std::pow(g.rope_theta, -(2.0 * i) / (double)hd);
+    CK(m, dalloc(m, &m->inv_freq, hd / 2));
+    CK(m, cudaMemcpy(m->inv_freq, invf.data(), invf.size() * sizeof(float), cudaMemcpyHostToDevice));
+
+    const float* d = nullptr;
+    auto pack = [&](const float* src, int N, int K, uint8_t* dst, int tile0, int ksteps) -> int {
+        int e = to_device(m, src, (size_t)N * K, on_dev, stage, &d);
+        if (e) return e;
+        e = q4_quantize_pack(d, N, K, dst, tile0, ksteps, sc_scratch, st);
+        if (e) return e;
+        return (int)cudaStreamSynchronize(st);  // the stage is reused by the next tensor
+    };
+    auto q4_bytes = [](int rows, int ksteps) { return (size_t)((rows + 15) / 16) * ksteps * kQ4Chunk; };
+
+    // fc and the all-layer Wk||Wv of the context projection
+    if (quant) {
+        CK(m, dalloc(m, &m->fc_p, q4_bytes(H, m->ks_tap)));
+        CK(m, pack(w->fc, H, m->tap_w, m->fc_p, 0, m->ks_tap));
+        CK(m, dalloc(m, &m->kvctx_p, q4_bytes(m->kvctx_w, m->ks_h)));
+        for (int l = 0; l < L; ++l) {
+            CK(m, pack(w->k[l], m->kd, H, m->kvctx_p, (l * 2 * m->kd) / 16, m->ks_h));
+            CK(m, pack(w->v[l], m->kd, H, m->kvctx_p, (l * 2 * m->kd + m->kd) / 16, m->ks_h));
+        }
+    } else {
+        CK(m, dalloc(m, &m->fc_f, (size_t)H * m->tap_w));
+        CK(m, copy_f32(m, m->fc_f, w->fc, (size_t)H * m->tap_w, on_dev));
+        CK(m, dalloc(m, &m->kvctx_f, (size_t)m->kvctx_w * H));
+        for (int l = 0; l < L; ++l) {
+            CK(m, copy_f32(m, m->kvctx_f + (size_t)l * 2 * m->kd * H, w->k[l], (size_t)m->kd * H, on_dev));
+            CK(m, copy_f32(m, m->kvctx_f + (size_t)(l * 2 + 1) * m->kd * H, w->v[l], (size_t)m->kd * H, on_dev));
+        }
+    }
+    // head
+    if (quant) {
+        const int vpad = (g.vocab + 15) / 16 * 16;
+        CK(m, dalloc(m, &m->head_p, (size_t)vpad * H));
+        CK(m, dalloc(m, &m->head_scale, vpad));
+        CK(m, to_device(m, w->head, (size_t)g.vocab * H, on_dev, stage, &d));
+        CK(m, i8_rows_quantize_pack(d, g.vocab, H, vpad, H / kI8KStep, m->head_p, m->head_scale, st));
+        CK(m, cudaStreamSynchronize(st));
+    } else {
+        CK(m, dalloc(m, &m->head_f, (size_t)g.vocab * H));
+        CK(m, copy_f32(m, m->head_f, w->head, (size_t)g.vocab * H, on_dev));
+    }
+    // layers
+    m->layers.resize(L);
+    std::vector<const float*> knorm_ptrs(L);
+    for (int l = 0; l < L; ++l) {
+        Layer& Ly = m->layers[l];
+        CK(m, dalloc(m, &Ly.in_norm, H));
+        CK(m, copy_f32(m, Ly.in_norm, w->in_norm[l], H, on_dev));
+        CK(m, dalloc(m, &Ly.post_norm, H));
+        CK(m, copy_f32(m, Ly.post_norm, w->post_norm[l], H, on_dev));
+        CK(m, dalloc(m, &Ly.q_norm, hd));
+        CK(m, copy_f32(m, Ly.q_norm, w->q_norm[l], hd, on_dev));
+        CK(m, dalloc(m, &Ly.k_norm, hd));
+        CK(m, copy_f32(m, Ly.k_norm, w->k_norm[l], hd, on_dev));
+        knorm_ptrs[l] = Ly.k_norm;
+        if (quant) {
+            CK(m, dalloc(m, &Ly.qkv_p, q4_bytes(m->qkv_w, m->ks_h)));
+            CK(m, pack(w->q[l], m->qd, H, Ly.qkv_p, 0, m->ks_h));
+            CK(m, pack(w->k[l], m->kd, H, Ly.qkv_p, m->qd / 16, m->ks_h));
+            CK(m, pack(w->v[l], m->kd, H, Ly.qkv_p, (m->qd + m->kd) / 16, m->ks_h));
+            CK(m, dalloc(m, &Ly.o_p, q4_bytes(H, m->ks_q)));
+            CK(m, pack(w->o[l], H, m->qd, Ly.o_p, 0, m->ks_q));
+            CK(m, dalloc(m, &Ly.gu_p, q4_bytes(2 * I, m->ks_h)));
+            CK(m, pack(w->gate[l], I, H, Ly.gu_p, 0, m->ks_h));
+            CK(m, pack(w->up[l], I, H, Ly.gu_p, I / 16, m->ks_h));
+            CK(m, dalloc(m, &Ly.down_p, q4_bytes(H, m->ks_i)));
+            CK(m, pack(w->down[l], H, I, Ly.down_p, 0, m->ks_i));
+        } else {
+            CK(m, dalloc(m, &Ly.qkv_f, (size_t)m->qkv_w * H));
+            CK(m, copy_f32(m, Ly.qkv_f, w->q[l], (size_t)m->qd * H, on_dev));
+            CK(m, copy_f32(m, Ly.qkv_f + (size_t)m->qd * H, w->k[l], (size_t)m->kd * H, on_dev));
+            CK(m, copy_f32(m, Ly.qkv_f + (size_t)(m->qd + m->kd) * H, w->v[l], (size_t)m->kd * H, on_dev));
+            CK(m, dalloc(m, &Ly.o_f, (size_t)H * m->qd));
+            CK(m, copy_f32(m, Ly.o_f, w->o[l], (size_t)H * m->qd, on_dev));
+            CK(m, dalloc(m, &Ly.gu_f, (size_t)2 * I * H));
+            CK(m, copy_f32(m, Ly.gu_f, w->gate[l], (size_t)I * H, on_dev));
+            CK(m, copy_f32(m, Ly.gu_f + (size_t)I * H, w->up[l], (size_t)I * H, on_dev));
+            CK(m, dalloc(m, &Ly.down_f, (size_t)H * I));
+            CK(m, copy_f32(m, Ly.down_f, w->down[l], (size_t)H * I, on_dev));
+        }
+    }
+    CK(m, dalloc(m, &m->k_norm_dev, L));
+    CK(m, cudaMemcpy(m->k_norm_dev, knorm_ptrs.data(), L * sizeof(float*), cudaMemcpyHostToDevice));
+    CK(m, cudaStreamSynchronize(st));
+    // the staging buffers are not needed after init
+    auto drop = [&](void* p) {
+        if (!p) return;
+        cudaFree(p);
+        m->owned.erase(std::remove(m->owned.begin(), m->owned.end(), p), m->owned.end());
+    };
+    drop(stage);
+    drop(sc_scratch);
+    return DFLASH_OK;
+}
+
+bool weights_complete(const dflash_weights* w, int L) {
+    if (!w->fc || !w->hidden_norm || !w->norm || !w->embed || !w->head) return false;
+    const float* const* per[] = {w->in_norm, w->post_norm, w->q_norm, w->k_norm, w->q, w->k,
+                                 w->v,       w->o,         w->gate,   w->up,     w->down};
+    for (auto a : per) {
+        if (!a) return false;
+        for (int l = 0; l < L; ++l)
+            if (!a[l]) return false;
+    }
+    return true;
+}
+
+// Apply one matrix (4-bit or f32) to activations: quantised formats take the
+// int8 codes in m->xq / m->xs, the f32 format the f32 rows `xf`.
+#define APPLY(expr)                 \
+    do {                            \
+        int rc__ = (expr);          \
+        if (rc__) return rc__;      \
+    } while (0)
+
+double q4_bytes_of(int N, int K, int T, bool accumulate) {
+    // 4-bit weights (0.5 B a weight, 2 B per 32) + int8 activations + f32 outputs
+    return (double)N * K * 0.5 + (double)N * (K / 32) * 2 + (double)T * (K + 4) + (double)T * N * 4 * (accumulate ? 2 : 1);
+}
+double f32_bytes_of(int N, int K, int T, bool accumulate) {
+    return (double)N * K * 4 + (double)T * K * 4 + (double)T * N * 4 * (accumulate ? 2 : 1);
+}
+
+int apply(dflash_model* m, const uint8_t* packed, const float* f32w, int tile0, int N, int K, int ksteps,
+          const float* xf, int ldxf, int T, float* y, int ldy, bool accumulate, int ldq, cudaStream_t st) {
+    if (m->g.quant == DFLASH_QUANT_Q4G32) {
+        QAct x{P<__half>(m->xq), P<float>(m->xs), ldq};
+        KL(m, "q4_gemm", 1, q4_bytes_of(N, K, T, accumulate), st,
+           q4_gemm(packed, tile0, N, ksteps, x, T, y, ldy, accumulate, m->num_sms, st));
+        return 0;
+    }
+    KL(m, "linear_f32", 1, f32_bytes_of(N, K, T, accumulate), st,
+       linear_f32(f32w, N, K, xf, ldxf, T, y, ldy, accumulate, st));
+    return 0;
+}
+
+// Project `n` context rows (device taps) at positions pos0.. into the store.
+int append_rows(dflash_model* m, dflash_seq* s, const float* taps_dev, int64_t n, int64_t pos0, int64_t idx0,
+                cudaStream_t st) {
+    const dflash_geometry& g = m->g;
+    const int H = g.hidden;
+    const bool quant = g.quant == DFLASH_QUANT_Q4G32;
+    const int rows = (int)n;
+    RowMap ident{1, 1, 0};
+    float* t = P<float>(m->a_t);
+    float* kv = P<float>(m->a_kv);
+    if (quant) {
+        // taps -> int8 rows; t = FC . Q(taps); x = Q(rms(t, hidden_norm)); kv = [Wk;Wv]_all . x
+        KL(m, "rms_quant", 1, (double)rows * m->tap_w * 5, st,
+           rms_rows(taps_dev, m->tap_w, ident, rows, m->tap_w, nullptr, g.eps, nullptr, 0, P<__half>(m->a_codes),
+                    P<float>(m->a_scale), m->tap_w, st));
+        QAct xt{P<__half>(m->a_codes), P<float>(m->a_scale), m->tap_w};
+        KL(m, "q4_gemm", 1, q4_bytes_of(H, m->tap_w, rows, false), st,
+           q4_gemm(m->fc_p, 0, H, m->ks_tap, xt, rows, t, H, false, m->num_sms, st));
+        KL(m, "rms_quant", 1, (double)rows * H * 5, st,
+           rms_rows(t, H, ident, rows, H, m->hidden_norm, g.eps, nullptr, 0, P<__half>(m->a_codes),
+                    P<float>(m->a_scale), H, st));
+        QAct xh{P<__half>(m->a_codes), P<float>(m->a_scale), H};
+        KL(m, "q4_gemm", 1, q4_bytes_of(m->kvctx_w, H, rows, false), st,
+           q4_gemm(m->kvctx_p, 0, m->kvctx_w, m->ks_h, xh, rows, kv, m->kvctx_w, false, m->num_sms, st));
+    } else {
+        KL(m, "linear_f32", 1, f32_bytes_of(H, m->tap_w, rows, false), st,
+           linear_f32(m->fc_f, H, m->tap_w, taps_dev, m->tap_w, rows, t, H, false, st));
+        float* tn = P<float>(m->a_codes);  // reuse as f32 rows
+        KL(m, "rms_f32", 1, (double)rows * H * 8, st,
+           rms_rows(t, H, ident, rows, H, m->hidden_norm, g.eps, tn, H, nullptr, nullptr, 0, st));
+        KL(m, "linear_f32", 1, f32_bytes_of(m->kvctx_w, H, rows, false), st,
+           linear_f32(m->kvctx_f, m->kvctx_w, H, tn, H, rows, kv, m->kvctx_w, false, st));
+    }
+    KL(m, "kv_append", 1, (double)rows * m->kvctx_w * 8, st,
+       kv_append(kv, rows, g.layers, g.kv_heads, g.head_dim, m->k_norm_dev, m->inv_freq, g.eps, pos0, idx0, s->k_dev,
+                 s->v_dev, s->cap, st));
+    return DFLASH_OK;
+}
+
+int ensure_append_scratch(dflash_model* m, int64_t rows) {
+    const bool quant = m->g.quant == DFLASH_QUANT_Q4G32;
+    const size_t r = (size_t)rows;
+    CK(m, ensure(m->a_taps, r * m->tap_w * sizeof(float)));
+    CK(m, ensure(m->a_codes, quant ? r * m->tap_w * sizeof(__half) : r * m->g.hidden * sizeof(float)));
+    CK(m, ensure(m->a_scale, r * sizeof(float)));
+    CK(m, ensure(m->a_t, r * m->g.hidden * sizeof(float)));
+    CK(m, ensure(m->a_kv, r * m->kvctx_w * sizeof(float)));
+    return 0;
+}
+
+}  // namespace
+
+// ============================================================================
+extern "C" {
+
+int dflash_init(const dflash_geometry* geom, const dflash_weights* weights, int weights_on_device, void* stream,
+                dflash_model** out) {
+    g_init_error.clear();
+    if (!out) return set_err(nullptr, DFLASH_EINVAL, "out is NULL");
+    *out = nullptr;
+    if (!geom || !weights) return set_err(nullptr, DFLASH_EINVAL, "geometry or weights is NULL");
+    std::string why = geometry_problem(*geom);
+    if (!why.empty()) return set_err(nullptr, DFLASH_EGEOM, "unsupported geometry: " + why);
+    if (!weights_complete(weights, geom->layers)) return set_err(nullptr, DFLASH_EINVAL, "a weight pointer is NULL");
+    dflash_model* m = new (std::nothrow) dflash_model();
+    if (!m) return set_err(nullptr, DFLASH_ENOMEM, "host allocation failed");
+    m->g = *geom;
+    cudaStream_t st = (cudaStream_t)stream;
+    int rc = DFLASH_OK;
+    cudaError_t e = cudaGetDevice(&m->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device);
+    if (e != cudaSuccess) {
+        rc = cuda_fail(m, (int)e, "cudaGetDevice");
+    } else {
+        rc = build_model(m, weights, weights_on_device != 0, st);
+    }
+    if (rc != DFLASH_OK) {
+        g_init_error = m->err;
+        dflash_free(m);
+        return rc;
+    }
+    *out = m;
+    return DFLASH_OK;
+}
+
+void dflash_free(dflash_model* m) {
+    if (!m) return;
+    cudaSetDevice(m->device);
+    for (auto& r : m->prof_open) {
+        cudaEventDestroy(r.e0);
+        cudaEventDestroy(r.e1);
+    }
+    for (cudaEvent_t e : m->ev_pool) cudaEventDestroy(e);
+    for (void* p : m->owned) cudaFree(p);
+    for (DevBuf* b : {&m->h, &m->xq, &m->xs, &m->qkv, &m->y, &m->gu, &m->logits, &m->keys, &m->toks, &m->part,
+                      &m->anchors, &m->pos0, &m->aseqs, &m->a_taps, &m->a_codes, &m->a_scale, &m->a_t, &m->a_kv})
+        free_buf(*b);
+    delete m;
+}
+
+const char* dflash_last_error(const dflash_model* m) { return m ? m->err.c_str() : g_init_error.c_str(); }
+
+int dflash_geometry_of(const dflash_model* m, dflash_geometry* out) {
+    if (!m || !out) return DFLASH_EINVAL;
+    *out = m->g;
+    return DFLASH_OK;
+}
+
+int dflash_seq_new(dflash_model* m, int64_t max_ctx_rows, dflash_seq** out) {
+    if (!m || !out) return DFLASH_EINVAL;
+    *out = nullptr;
+    int rc = check_model(m);
+    if (rc) return rc;
+    if (max_ctx_rows < 1) return set_err(m, DFLASH_EINVAL, "max_ctx_rows < 1");
+    dflash_seq* s = new (std::nothrow) dflash_seq();
+    if (!s) return set_err(m, DFLASH_ENOMEM, "host allocation failed");
+    s->m = m;
+    s->cap = max_ctx_rows;
+    const int L = m->g.layers;
+    const size_t per = (size_t)m->g.kv_heads * (size_t)max_ctx_rows * m->g.head_dim;
+    s->k.assign(L, nullptr);
+    s->v.assign(L, nullptr);
+    cudaError_t e = cudaSuccess;
+    for (int l = 0; l < L && e == cudaSuccess; ++l) {
+        e = cudaMalloc(&s->k[l], per * sizeof(float));
+        if (e == cudaSuccess) e = cudaMalloc(&s->v[l], per * sizeof(float));
+    }
+    if (e == cudaSuccess) e = cudaMalloc(&s->k_dev, L * sizeof(float*));
+    if (e == cudaSuccess) e = cudaMalloc(&s->v_dev, L * sizeof(float*));
+    if (e == cudaSuccess) e = cudaMemcpy(s->k_dev, s->k.data(), L * sizeof(float*), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(s->v_dev, s->v.data(), L * sizeof(float*), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        dflash_seq_free(s);
+        return set_err(m, e == cudaErrorMemoryAllocation ? DFLASH_ENOMEM : DFLASH_ECUDA,
+                       std::string("sequence allocation: ") + cudaGetErrorString(e));
+    }
+    m->live_seqs++;
+    *out = s;
+    return DFLASH_OK;
+}
+
+void dflash_seq_free(dflash_seq* s) {
+    if (!s) return;
+    if (s->m) cudaSetDevice(s->m->device);
+    for (float* p : s->k) if (p) cudaFree(p);
+    for (float* p : s->v) if (p) cudaFree(p);
+    if (s->k_dev) cudaFree(s->k_dev);
+    if (s->v_dev) cudaFree(s->v_dev);
+    if (s->m && s->m->live_seqs > 0) s->m->live_seqs--;
+    delete s;
+}
+
+int dflash_seq_span(const dflash_seq* s, int64_t* first, int64_t* next) {
+    if (!s || !first || !next) return DFLASH_EINVAL;
+    *first = s->first;
+    *next = s->first + s->len;
+    return DFLASH_OK;
+}
+
+int dflash_truncate(dflash_seq* s, int64_t pos) {
+    if (!s) return DFLASH_EINVAL;
+    int64_t keep = std::min(std::max<int64_t>(pos - s->first, 0), s->len);
+    s->len = keep;
+    return DFLASH_OK;
+}
+
+int dflash_reset(dflash_seq* s) {
+    if (!s) return DFLASH_EINVAL;
+    s->len = 0;
+    s->first = 0;
+    return DFLASH_OK;
+}
+
+int dflash_ctx_append(dflash_model* m, dflash_seq* s, int64_t pos, const float* taps, int64_t n_rows,
+                      int taps_on_device, void* stream) {
+    int rc = check_model(m);
+    if (rc) return rc;
+    if (!s || s->m != m) return set_err(m, DFLASH_EINVAL, "sequence is NULL or belongs to another model");
+    if (n_rows < 0 || pos < 0) return set_err(m, DFLASH_EINVAL, "n_rows < 0 or pos < 0");
+    if (n_rows > 0 && !taps) return set_err(m, DFLASH_EINVAL, "taps is NULL");
+    cudaStream_t st = (cudaStream_t)stream;
+    // position rule: replace from pos, or start over at pos
+    int64_t first = s->first, len = s->len;
+    if (pos > first + len || pos < first) {
+        first = pos;
+        len = 0;
+    } else {
+        len = pos - first;
+    }
+    if (len + n_rows > s->cap)
+        return set_err(m, DFLASH_ECAPACITY, "context of " + std::to_string(len + n_rows) + " rows exceeds capacity " +
+                                                std::to_string(s->cap));
+    s->first = first;
+    s->len = len;
+    if (n_rows == 0) return DFLASH_OK;
+    const int64_t chunk = std::min<int64_t>(n_rows, kAppendRows);
+    rc = ensure_append_scratch(m, chunk);
+    if (rc) return rc;
+    for (int64_t r0 = 0; r0 < n_rows; r0 += chunk) {
+        const int64_t n = std::min(chunk, n_rows - r0);
+        const float* src = taps + r0 * m->tap_w;
+        if (!taps_on_device) {
+            CK(m, cudaMemcpyAsync(m->a_taps.p, src, (size_t)n * m->tap_w * sizeof(float), cudaMemcpyHostToDevice, st));
+            src = P<float>(m->a_taps);
+        }
+        rc = append_rows(m, s, src, n, first + len + r0, len + r0, st);
+        if (rc) return rc;
+        if (!taps_on_device && r0 + chunk < n_rows) CK(m, cudaStreamSynchronize(st));  // staging reused
+    }
+    if (!taps_on_device) CK(m, cudaStreamSynchronize(st));
+    s->len = len + n_rows;
+    return DFLASH_OK;
+}
+
+int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const uint32_t* anchor_tok,
+                 const int64_t* anchor_pos, int32_t block_len, float* logits, uint32_t* draft_tok, int io_on_device,
+                 void* stream) {
+    int rc = check_model(m);
+    if (rc) return rc;
+    const dflash_geometry& g = m->g;
+    if (!seqs || !anchor_tok || !anchor_pos || n_seqs < 1)
+        return set_err(m, DFLASH_EINVAL, "seqs / anchor_tok / anchor_pos NULL or n_seqs < 1");
+    if (block_len < 2 || block_len > g.block)
+        return set_err(m, DFLASH_ERANGE, "block_len " + std::to_string(block_len) + " outside [2, block]");
+    for (int s = 0; s < n_seqs; ++s) {
+        if (!seqs[s] || seqs[s]->m != m) return set_err(m, DFLASH_EINVAL, "a sequence is NULL or of another model");
+        if (anchor_pos[s] < 0) return set_err(m, DFLASH_EINVAL, "anchor_pos < 0");
+        if (!io_on_device && anchor_tok[s] >= (uint32_t)g.vocab)
+            return set_err(m, DFLASH_EINVAL, "anchor token outside the vocabulary");
+    }
+    cudaStream_t st = (cudaStream_t)stream;
+    const bool quant = g.quant == DFLASH_QUANT_Q4G32;
+    const int H = g.hidden, I = g.intermediate, hd = g.head_dim, B = block_len;
+    const int R = n_seqs * B, D = n_seqs * (B - 1);
+    const int maxK = std::max({H, I, m->qd});
+
+    // context rows each sequence reads: [first, min(anchor, first + len))
+    std::vector<AttnSeq> as(n_seqs);
+    std::vector<int64_t> p0(anchor_pos, anchor_pos + n_seqs);
+    int max_ctx = 0;
+    for (int s = 0; s < n_seqs; ++s) {
+        const dflash_seq* q = seqs[s];
+        const int64_t hi = std::max(std::min(anchor_pos[s], q->first + q->len), q->first);
+        as[s].cap = q->cap;
+        as[s].lo = 0;
+        as[s].n = (int)(hi - q->first);
+        max_ctx = std::max(max_ctx, as[s].n);
+    }
+    double attn_bytes = (double)R * m->qkv_w * 4 + (double)R * m->qd * 4;
+    for (int s = 0; s < n_seqs; ++s) attn_bytes += (double)as[s].n * m->kd * 8;
+    const int64_t part_floats = attn_scratch_floats(n_seqs, B, max_ctx, g.heads, g.kv_heads, hd, m->num_sms);
+    CK(m, ensure(m->h, (size_t)R * H * sizeof(float)));
+    CK(m, ensure(m->xq, (size_t)R * (quant ? maxK * sizeof(__half) : maxK * sizeof(float))));
+    CK(m, ensure(m->xs, (size_t)R * sizeof(float)));
+    CK(m, ensure(m->qkv, (size_t)R * m->qkv_w * sizeof(float)));
+    CK(m, ensure(m->y, (size_t)R * m->qd * sizeof(float)));
+    CK(m, ensure(m->gu, (size_t)R * 2 * I * sizeof(float)));
+    CK(m, ensure(m->part, (size_t)part_floats * sizeof(float)));
+    CK(m, ensure(m->keys, (size_t)D * sizeof(unsigned long long)));
+    CK(m, ensure(m->toks, (size_t)D * sizeof(uint32_t)));
+    CK(m, ensure(m->anchors, (size_t)n_seqs * sizeof(uint32_t)));
+    CK(m, ensure(m->pos0, (size_t)n_seqs * sizeof(int64_t)));
+    CK(m, ensure(m->aseqs, (size_t)g.layers * n_seqs * sizeof(AttnSeq)));
+    float* logit_out = io_on_device ? logits : nullptr;
+    if (!io_on_device && logits) {
+        CK(m, ensure(m->logits, (size_t)D * g.vocab * sizeof(float)));
+        logit_out = P<float>(m->logits);
+    }
+    if (!quant && !logit_out) {  // the f32 head needs its logits for the argmax
+        CK(m, ensure(m->logits, (size_t)D * g.vocab * sizeof(float)));
+        logit_out = P<float>(m->logits);
+    }
+    // per-call vectors (pageable sources: the driver copies them before returning)
+    const uint32_t* anchors_dev = anchor_tok;
+    if (!io_on_device) {
+        CK(m, cudaMemcpyAsync(m->anchors.p, anchor_tok, n_seqs * sizeof(uint32_t), cudaMemcpyHostToDevice, st));
+        anchors_dev = P<uint32_t>(m->anchors);
+    }
+    CK(m, cudaMemcpyAsync(m->pos0.p, p0.data(), n_seqs * sizeof(int64_t), cudaMemcpyHostToDevice, st));
+    // every layer's context views in one upload: [layer][sequence]
+    std::vector<AttnSeq> as_all((size_t)g.layers * n_seqs);
+    for (int l = 0; l < g.layers; ++l)
+        for (int s = 0; s < n_seqs; ++s) {
+            AttnSeq a = as[s];
+            a.kc = seqs[s]->k[l];
+            a.vc = seqs[s]->v[l];
+            as_all[(size_t)l * n_seqs + s] = a;
+        }
+    CK(m, cudaMemcpyAsync(m->aseqs.p, as_all.data(), as_all.size() * sizeof(AttnSeq), cudaMemcpyHostToDevice, st));
+
+    float* h = P<float>(m->h);
+    float* qkv = P<float>(m->qkv);
+    float* y = P<float>(m->y);
+    float* gu = P<float>(m->gu);
+    float* xf = P<float>(m->xq);  // the f32 path's normed rows
+    __half* xq = P<__half>(m->xq);
+    float* xs = P<float>(m->xs);
+    RowMap ident{1, 1, 0};
+    const float scale = 1.0f / sqrtf((float)hd);
+
+    KL(m, "embed_rows", 1, (double)R * H * 8, st, embed_rows(m->embed, H, g.vocab, anchors_dev, g.mask_token, n_seqs, B, h, st));
+    for (int l = 0; l < g.layers; ++l) {
+        const Layer& Ly = m->layers[l];
+        // attention half: x = rms(h, in_norm); q, k, v; norms and rotation; attention; h += O y
+        if (quant) {
+            KL(m, "rms_quant", 1, (double)R * H * 5, st, rms_rows(h, H, ident, R, H, Ly.in_norm, g.eps, nullptr, 0, xq, xs, maxK, st));
+            APPLY(apply(m, Ly.qkv_p, nullptr, 0, m->qkv_w, H, m->ks_h, nullptr, 0, R, qkv, m->qkv_w, false, maxK, st));
+        } else {
+            KL(m, "rms_f32", 1, (double)R * H * 8, st, rms_rows(h, H, ident, R, H, Ly.in_norm, g.eps, xf, maxK, nullptr, nullptr, 0, st));
+            APPLY(apply(m, nullptr, Ly.qkv_f, 0, m->qkv_w, H, 0, xf, maxK, R, qkv, m->qkv_w, false, 0, st));
+        }
+        KL(m, "qk_norm_rope", 1, (double)R * (m->qd + m->kd) * 8, st,
+           qk_norm_rope(qkv, m->qkv_w, R, B, P<int64_t>(m->pos0), g.heads, g.kv_heads, hd, Ly.q_norm, Ly.k_norm,
+                        m->inv_freq, g.eps, st));
+        const AttnSeq* aseq_dev = P<AttnSeq>(m->aseqs) + (size_t)l * n_seqs;
+        KL(m, "attention", 2, attn_bytes, st,
+           attention(qkv, m->qkv_w, n_seqs, B, aseq_dev, max_ctx, g.heads, g.kv_heads, hd, scale, P<float>(m->part),
+                     part_floats, y, m->num_sms, st));
+        if (quant) {
+            KL(m, "rms_quant", 1, (double)R * m->qd * 5, st, rms_rows(y, m->qd, ident, R, m->qd, nullptr, g.eps, nullptr, 0, xq, xs, maxK, st));
+            APPLY(apply(m, Ly.o_p, nullptr, 0, H, m->qd, m->ks_q, nullptr, 0, R, h, H, true, maxK, st));
+        } else {
+            APPLY(apply(m, nullptr, Ly.o_f, 0, H, m->qd, 0, y, m->qd, R, h, H, true, 0, st));
+        }
+        // MLP half: x = rms(h, post_norm); h += down (silu(gate x) * up x)
+        if (quant) {
+            KL(m, "rms_quant", 1, (double)R * H * 5, st, rms_rows(h, H, ident, R, H, Ly.post_norm, g.eps, nullptr, 0, xq, xs, maxK, st));
+            APPLY(apply(m, Ly.gu_p, nullptr, 0, 2 * I, H, m->ks_h, nullptr, 0, R, gu, 2 * I, false, maxK, st));
+            KL(m, "silu_quant", 1, (double)R * I * 9, st, silu_mul(gu, 2 * I, R, I, nullptr, 0, xq, xs, maxK, st));
+            APPLY(apply(m, Ly.down_p, nullptr, 0, H, I, m->ks_i, nullptr, 0, R, h, H, true, maxK, st));
+        } else {
+            KL(m, "rms_f32", 1, (double)R * H * 8, st, rms_rows(h, H, ident, R, H, Ly.post_norm, g.eps, xf, maxK, nullptr, nullptr, 0, st));
+            APPLY(apply(m, nullptr, Ly.gu_f, 0, 2 * I, H, 0, xf, maxK, R, gu, 2 * I, false, 0, st));
+            KL(m, "silu_f32", 1, (double)R * I * 12, st, silu_mul(gu, 2 * I, R, I, xf, maxK, nullptr, nullptr, 0, st));
+            APPLY(apply(m, nullptr, Ly.down_f, 0, H, I, 0, xf, maxK, R, h, H, true, 0, st));
+        }
+    }
+    // head over the rows after each anchor: row i of the output is row
+    // (i / (B-1)) * B + 1 + i % (B-1) of h
+    RowMap drafts{B - 1, B, 1};
+    unsigned long long* keys = P<unsigned long long>(m->keys);
+    uint32_t* tok_out = (io_on_device && draft_tok) ? draft_tok : P<uint32_t>(m->toks);
+    if (quant) {
+        KL(m, "rms_quant", 1, (double)D * H * 5, st, rms_rows(h, H, drafts, D, H, m->norm, g.eps, nullptr, 0, xq, xs, maxK, st));
+        CK(m, cudaMemsetAsync(keys, 0, (size_t)D * sizeof(unsigned long long), st));
+        QAct xh{xq, xs, maxK};
+        const double hb = (double)g.vocab * H + (double)g.vocab * 4 + (double)D * H + (logit_out ? (double)D * g.vocab * 4 : 0.0);
+        KL(m, "head_i8", 1, hb, st,
+           head_i8(m->head_p, m->head_scale, g.vocab, H / kI8KStep, xh, D, logit_out, g.vocab, keys, m->num_sms, st));
+    } else {
+        KL(m, "rms_f32", 1, (double)D * H * 8, st, rms_rows(h, H, drafts, D, H, m->norm, g.eps, xf, maxK, nullptr, nullptr, 0, st));
+        KL(m, "linear_f32", 1, f32_bytes_of(g.vocab, H, D, false), st,
+           linear_f32(m->head_f, g.vocab, H, xf, maxK, D, logit_out, g.vocab, false, st));
+        KL(m, "argmax_rows", 1, (double)D * g.vocab * 4, st, argmax_rows(logit_out, g.vocab, g.vocab, D, keys, st));
+    }
+    KL(m, "keys_to_tokens", 1, (double)D * 12, st, keys_to_tokens(keys, D, tok_out, st));
+    if (!io_on_device) {
+        if (logits)
+            CK(m, cudaMemcpyAsync(logits, logit_out, (size_t)D * g.vocab * sizeof(float), cudaMemcpyDeviceToHost, st));
+        if (draft_tok)
+            CK(m, cudaMemcpyAsync(draft_tok, tok_out, (size_t)D * sizeof(uint32_t), cudaMemcpyDeviceToHost, st));
+        CK(m, cudaStreamSynchronize(st));
+    }
+    return DFLASH_OK;
+}
+
+// ------------------------------------------------------------------ tracing
+int dflash_profile_start(dflash_model* m) {
+    if (!m) return DFLASH_EINVAL;
+    for (auto& r : m->prof_open) {
+        m->ev_pool.push_back(r.e0);
+        m->ev_pool.push_back(r.e1);
+    }
+    m->prof_open.clear();
+    m->prof_sum.clear();
+    m->profiling = true;
+    return DFLASH_OK;
+}
+
+int dflash_profile_stop(dflash_model* m) {
+    if (!m) return DFLASH_EINVAL;
+    m->profiling = false;
+    int rc = DFLASH_OK;
+    for (auto& r : m->prof_open) {
+        float ms = 0.f;
+        cudaError_t e = cudaEventSynchronize(r.e1);
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.e0, r.e1);
+        if (e != cudaSuccess && rc == DFLASH_OK) rc = cuda_fail(m, (int)e, "profile events");
+        auto it = std::find_if(m->prof_sum.begin(), m->prof_sum.end(),
+                               [&](const dflash_model::ProfSum& p) { return std::strcmp(p.name, r.name) == 0; });
+        if (it == m->prof_sum.end()) {
+            m->prof_sum.push_back(dflash_model::ProfSum{r.name});
+            it = m->prof_sum.end() - 1;
+        }
+        it->launches += r.kernels;
+        it->ms += ms;
+        it->bytes += r.bytes;
+        m->ev_pool.push_back(r.e0);
+        m->ev_pool.push_back(r.e1);
+    }
+    m->prof_open.clear();
+    return rc;
+}
+
+int dflash_profile_entry(const dflash_model* m, int32_t i, const char** name, int64_t* launches, double* total_ms,
+                         double* total_bytes) {
+    if (!m) return DFLASH_EINVAL;
+    if (i < 0 || i >= (int32_t)m->prof_sum.size()) return DFLASH_ERANGE;
+    const auto& p = m->prof_sum[i];
+    if (name) *name = p.name;
+    if (launches) *launches = p.launches;
+    if (total_ms) *total_ms = p.ms;
+    if (total_bytes) *total_bytes = p.bytes;
+    return DFLASH_OK;
+}
+
+int64_t dflash_launch_count(const dflash_model* m) { return m ? m->launches : -1; }
+
+// ------------------------------------------------------------------ test hooks
+int dflash_debug_q4_codes(dflash_model* m, int32_t id, int8_t* codes, uint16_t* scales, void* stream) {
+    int rc = check_model(m);
+    if (rc) return rc;
+    if (m->g.quant != DFLASH_QUANT_Q4G32 || id == DFLASH_MAT_HEAD || !codes || !scales)
+        return set_err(m, DFLASH_EINVAL, "not a 4-bit matrix, or NULL output");
+    MatView v = mat_view(m, id);
+    if (!v.packed) return set_err(m, DFLASH_EINVAL, "bad matrix id");
+    cudaStream_t st = (cudaStream_t)stream;
+    int8_t* dc = nullptr;
+    uint16_t* ds = nullptr;
+    CK(m, cudaMalloc(&dc, (size_t)v.N * v.K));
+    CK(m, cudaMalloc(&ds, (size_t)v.N * (v.K / 32) * 2));
+    int e = q4_unpack(v.packed, v.tile0, v.N, v.K, v.ksteps, dc, ds, st);
+    if (!e) e = (int)cudaMemcpyAsync(codes, dc, (size_t)v.N * v.K, cudaMemcpyDeviceToHost, st);
+    if (!e) e = (int)cudaMemcpyAsync(scales, ds, (size_t)v.N * (v.K / 32) * 2, cudaMemcpyDeviceToHost, st);
+    if (!e) e = (int)cudaStreamSynchronize(st);
+    cudaFree(dc);
+    cudaFree(ds);
+    CK(m, e);
+    return DFLASH_OK;
+}
+
+int dflash_debug_head_codes(dflash_model* m, int8_t* codes, float* scales, void* stream) {
+    int rc = check_model(m);
+    if (rc) return rc;
+    if (m->g.quant != DFLASH_QUANT_Q4G32 || !codes || !scales) return set_err(m, DFLASH_EINVAL, "f32 model or NULL");
+    cudaStream_t st = (cudaStream_t)stream;
+    const int V = m->g.vocab, H = m->g.hidden;
+    int8_t* dc = nullptr;
+    CK(m, cudaMalloc(&dc, (size_t)V * H));
+    int e = i8_unpack(m->head_p, V, H, H / kI8KStep, dc, st);
+    if (!e) e = (int)cudaMemcpyAsync(codes, dc, (size_t)V * H, cudaMemcpyDeviceToHost, st);
+    if (!e) e = (int)cudaMemcpyAsync(scales, m->head_scale, (size_t)V * sizeof(float), cudaMemcpyDeviceToHost, st);
+    if (!e) e = (int)cudaStreamSynchronize(st);
+    cudaFree(dc);
+    CK(m, e);
+    return DFLASH_OK;
+}
+
+int dflash_debug_q4_groupsums(dflash_model* m, int32_t id, const int8_t* x, int32_t rows, int32_t* out, void* stream) {
+    int rc = check_model(m);
+    if (rc) return rc;
+    if (m->g.quant != DFLASH_QUANT_Q4G32 || id == DFLASH_MAT_HEAD || !x || !out || rows < 1 || rows > 16)
+        return set_err(m, DFLASH_EINVAL, "bad arguments");
+    MatView v = mat_view(m, id);
+    if (!v.packed) return set_err(m, DFLASH_EINVAL, "bad matrix id");
+    cudaStream_t st = (cudaStream_t)stream;
+    const int ldk = v.ksteps * kQ4KStep;
+    std::vector<__half> hx((size_t)rows * ldk, __float2half(0.f));
+    for (int r = 0; r < rows; ++r)
+        for (int k = 0; k < v.K; ++k) {
+            int xv = x[(size_t)r * v.K + k];
+            if (xv < -127) return set_err(m, DFLASH_EINVAL, "activation code -128");
+            hx[(size_t)r * ldk + k] = __float2half((float)xv);
+        }
+    std::vector<float> ones(rows, 1.f);
+    __half* dx = nullptr;
+    float* dsc = nullptr;
+    int32_t* dout = nullptr;
+    const size_t outn = (size_t)rows * v.N * (v.K / 32);
+    CK(m, cudaMalloc(&dx, hx.size() * sizeof(__half)));
+    CK(m, cudaMalloc(&dsc, rows * sizeof(float)));
+    CK(m, cudaMalloc(&dout, outn * sizeof(int32_t)));
+    int e = (int)cudaMemcpyAsync(dx, hx.data(), hx.size() * sizeof(__half), cudaMemcpyHostToDevice, st);
+    if (!e) e = (int)cudaMemcpyAsync(dsc, ones.data(), rows * sizeof(float), cudaMemcpyHostToDevice, st);
+    QAct qa{dx, dsc, ldk};
+    if (!e) e = q4_groupsums(v.packed, v.tile0, v.N, v.ksteps, qa, rows, dout, st);
+    if (!e) e = (int)cudaMemcpyAsync(out, dout, outn * sizeof(int32_t), cudaMemcpyDeviceToHost, st);
+    if (!e) e = (int)cudaStreamSynchronize(st);
+    cudaFree(dx);
+    cudaFree(dsc);
+    cudaFree(dout);
+    CK(m, e);
+    return DFLASH_OK;
+}
+
+int dflash_debug_read_kv(dflash_model* m, const dflash_seq* s, int32_t layer, int64_t pos, int64_t n, float* k,
+                         float* v, void* stream) {
+    int rc = check_model(m);
+    if (rc) return rc;
+    if (!s || s->m != m || layer < 0 || layer >= m->g.layers || n < 0)
+        return set_err(m, DFLASH_EINVAL, "bad arguments");
+    if (pos < s->first || pos + n > s->first + s->len) return set_err(m, DFLASH_ERANGE, "positions not held");
+    cudaStream_t st = (cudaStream_t)stream;
+    const int hd = m->g.head_dim, kv = m->g.kv_heads;
+    const int64_t idx = pos - s->first;
+    for (int which = 0; which < 2; ++which) {
+        float* dst = which ? v : k;
+        const float* src = which ? s->v[layer] : s->k[layer];
+        if (!dst || n == 0) continue;
+        for (int gq = 0; gq < kv; ++gq)
+            CK(m, cudaMemcpy2DAsync(dst + (size_t)gq * hd, (size_t)kv * hd * sizeof(float),
+                                    src + ((size_t)gq * s->cap + idx) * hd, (size_t)hd * sizeof(float),
+                                    (size_t)hd * sizeof(float), (size_t)n, cudaMemcpyDeviceToHost, st));
+    }
+    CK(m, cudaStreamSynchronize(st));
+    return DFLASH_OK;
+}
+
+}  // extern "C"

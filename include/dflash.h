@@ -1,0 +1,291 @@
+/*
+ * dflash.h — C ABI of the GB300 (sm_103a) DFlash 2 block drafter.
+ *
+ * The drafter (page "cortiq-engine 0.8.71 — src/dflash.rs", module
+ * documentation) is a few Qwen3-shaped layers beside a target model:
+ *
+ *   context  t = norm(FC . [target layer outputs of a row])
+ *            K_l = rot(norm(Wk_l . t)),  V_l = Wv_l . t     kept per position
+ *   block    rows [anchor, MASK, ..., MASK] at positions a, a+1, ...
+ *            x = norm(h); q,k,v = W . x; attention over K_l, V_l before a and
+ *            the block's own rows (not causal); h += O . y; the MLP likewise
+ *   tokens   logits = head . norm(h); row j >= 1 drafts the token at a + j
+ *
+ * The DFlash 2 row convolution is bypassed (x and the sub-layer outputs pass
+ * unchanged): the workloads this library serves fix no convolution geometry.
+ *
+ * Conventions for every call:
+ *  - Return 0 (DFLASH_OK) on success, a negative DFLASH_E* code otherwise;
+ *    dflash_last_error() gives a human-readable reason.  No C++ exception
+ *    crosses the ABI and there is no CPU fallback: every step of the path
+ *    runs in this library's CUDA kernels.
+ *  - After DFLASH_ECUDA the model is poisoned: every later call on it (and
+ *    on its sequences) returns DFLASH_ECUDA until dflash_free().
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *    queued on it.  Calls on one model (and its sequences) must not overlap:
+ *    the model's scratch buffers are shared by its calls.
+ *  - Matrices are row-major [out][in] float32, as the page's tensors are.
+ *  - Weights and context K/V live in device memory the library allocates and
+ *    owns; inputs and outputs are owned by the caller.
+ */
+#ifndef DFLASH_H
+#define DFLASH_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DFLASH_API __attribute__((visibility("default")))
+#else
+#define DFLASH_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define DFLASH_OK 0
+#define DFLASH_EINVAL (-1)    /* a null pointer, a bad size or shape */
+#define DFLASH_EGEOM (-2)     /* a geometry the page or the kernels reject */
+#define DFLASH_ECAPACITY (-3) /* context rows beyond the sequence's capacity */
+#define DFLASH_ERANGE (-4)    /* block_len or a position outside its range */
+#define DFLASH_ECUDA (-5)     /* a CUDA call failed; the model is poisoned */
+#define DFLASH_ENOMEM (-6)    /* a device or host allocation failed */
+
+/* number formats (dflash_geometry.quant) */
+#define DFLASH_QUANT_F32 0   /* every matrix, activation and the head in f32 */
+#define DFLASH_QUANT_Q4G32 1 /* draft-layer matrices, fc, Wk/Wv: 4-bit, groups of
+                                32 along K with f16 scales; head: int8 per row
+                                with an f32 row scale; every matrix input row:
+                                int8 per row with an f32 scale; the rest f32 */
+
+typedef struct dflash_model dflash_model; /* weights, geometry, scratch */
+typedef struct dflash_seq dflash_seq;     /* one sequence's context K/V */
+
+/*
+ * What a DFlash 2 checkpoint fixes (page "cortiq-engine 0.8.71 —
+ * src/dflash.rs", `Geometry` and `Geometry::of`).
+ * Rules (DFLASH_EGEOM otherwise): layers >= 1; block >= 2; n_taps >= 1;
+ * kv_heads >= 1; heads % kv_heads == 0 (the page's rules); and the kernels'
+ * limits: head_dim 64 or 128; hidden and intermediate multiples of 64;
+ * 0 <= mask_token < vocab; window == 0 (every layer reads its whole
+ * context); eps > 0; rope_theta > 0; quant one of DFLASH_QUANT_*.
+ */
+typedef struct {
+    int32_t hidden;       /* H */
+    int32_t intermediate; /* I, the SwiGLU width */
+    int32_t layers;       /* L */
+    int32_t heads;        /* query heads */
+    int32_t kv_heads;     /* key/value heads; query head h reads kv head h / (heads / kv_heads) */
+    int32_t head_dim;     /* hd */
+    int32_t vocab;        /* V, rows of the target's embedding and head */
+    int32_t block;        /* rows of a block: the anchor and block - 1 drafts */
+    int32_t n_taps;       /* target layers a context row joins; a row is n_taps * H wide */
+    int32_t mask_token;   /* token whose embedding fills rows 1.. of a block */
+    int32_t window;       /* positions a block row sees back; 0 = all (the only value accepted) */
+    int32_t quant;        /* DFLASH_QUANT_F32 or DFLASH_QUANT_Q4G32 */
+    float eps;            /* RMSNorm epsilon */
+    double rope_theta;    /* RoPE base: inv_freq[i] = theta^(-2i/hd) */
+} dflash_geometry;
+
+/*
+ * The drafter's weights (page "cortiq-engine 0.8.71 — src/dflash.rs",
+ * `Drafter::new`: the sidecar's tensor names and shapes), float32 row-major.
+ * Per-layer fields point to arrays of `layers` pointers.
+ *   fc [H][n_taps*H]   hidden_norm [H]   norm [H]
+ *   embed [V][H] (the target's embedding)   head [V][H] (the target's head)
+ *   in_norm, post_norm [H];  q_norm, k_norm [hd]
+ *   q [heads*hd][H];  k, v [kv_heads*hd][H];  o [H][heads*hd]
+ *   gate, up [I][H];  down [H][I]
+ * The pointers are host pointers, or device pointers when dflash_init's
+ * weights_on_device is 1.  They are read during dflash_init only; the library
+ * keeps its own (quantised and packed) copies.
+ */
+typedef struct {
+    const float* fc;
+    const float* hidden_norm;
+    const float* norm;
+    const float* embed;
+    const float* head;
+    const float* const* in_norm;
+    const float* const* post_norm;
+    const float* const* q_norm;
+    const float* const* k_norm;
+    const float* const* q;
+    const float* const* k;
+    const float* const* v;
+    const float* const* o;
+    const float* const* gate;
+    const float* const* up;
+    const float* const* down;
+} dflash_weights;
+
+/*
+ * Build a model on the current CUDA device: check the geometry, upload the
+ * weights and, for DFLASH_QUANT_Q4G32, quantise and pack them on the device
+ * (the page's sidecar arrives quantised; this library quantises float32
+ * weights itself by the format above).  Blocks until the weights are ready
+ * (page "cortiq-engine 0.8.75 — src/gpu_wgpu/dflash_dev.rs", `Dev::new`: the
+ * weights are resident before the first block).
+ * Errors: EINVAL (null), EGEOM, ENOMEM, ECUDA.  On error *out is NULL and
+ * dflash_last_error(NULL) gives the reason.
+ */
+DFLASH_API int dflash_init(const dflash_geometry* geom, const dflash_weights* weights, int weights_on_device, void* stream,
+                dflash_model** out);
+
+/* Free a model and its device memory (sequences must be freed first). NULL is a no-op. */
+DFLASH_API void dflash_free(dflash_model* model);
+
+/* The reason of the last failed call on `model` (NULL: the last failed
+ * dflash_init of this thread).  Never NULL; "" when nothing failed. */
+DFLASH_API const char* dflash_last_error(const dflash_model* model);
+
+/* Copy the geometry a model was built with into *out. */
+DFLASH_API int dflash_geometry_of(const dflash_model* model, dflash_geometry* out);
+
+/*
+ * A sequence: device K/V storage for up to `max_ctx_rows` context positions
+ * in every layer, f32, laid out per layer [kv_heads][max_ctx_rows][head_dim]
+ * for keys and the same for values (page "cortiq-engine 0.8.71 —
+ * src/dflash.rs", `Ctx`: per layer, per KV head, a row of head_dim per
+ * position).  The context starts empty at position 0.
+ * Errors: EINVAL (null, max_ctx_rows < 1), ENOMEM, ECUDA.
+ */
+DFLASH_API int dflash_seq_new(dflash_model* model, int64_t max_ctx_rows, dflash_seq** out);
+
+/* Free a sequence. NULL is a no-op. */
+DFLASH_API void dflash_seq_free(dflash_seq* seq);
+
+/* The positions the context covers: [*first, *next) (`Drafter::span`). */
+DFLASH_API int dflash_seq_span(const dflash_seq* seq, int64_t* first, int64_t* next);
+
+/*
+ * Add the target's rows of positions pos, pos+1, ... to the context
+ * (page "cortiq-engine 0.8.71 — src/dflash.rs", `Drafter::push_context`,
+ * `queue_context` and `settle_rows`):
+ *   t = rms(FC . Q(taps_r), hidden_norm); for every layer
+ *   K_l[p] = rot_p(rms_head(Wk_l . Q(t), k_norm_l)),  V_l[p] = Wv_l . Q(t)
+ * where Q is the int8 row quantiser in DFLASH_QUANT_Q4G32 and the identity in
+ * DFLASH_QUANT_F32.  `taps` is [n_rows][n_taps*hidden] f32, the tapped
+ * layers' outputs joined in tap order; a host pointer, or a device pointer
+ * when taps_on_device is 1.  Positions: with first <= pos <= next the rows
+ * replace position pos and everything after it; pos < first or pos > next
+ * starts the context over at pos.  The rows are settled at once (no queue).
+ * n_rows == 0 applies only the position rule.  Host taps: the call returns
+ * after the rows are copied; device taps: the work is queued on `stream`.
+ * Errors: EINVAL (null taps with n_rows > 0, n_rows < 0, pos < 0),
+ * ECAPACITY (the context would exceed max_ctx_rows), ECUDA.
+ */
+DFLASH_API int dflash_ctx_append(dflash_model* model, dflash_seq* seq, int64_t pos, const float* taps, int64_t n_rows,
+                      int taps_on_device, void* stream);
+
+/* Forget the context from position `pos` on (`Drafter::truncate`). */
+DFLASH_API int dflash_truncate(dflash_seq* seq, int64_t pos);
+
+/* Empty the context and move its start back to position 0 (`Drafter::reset`). */
+DFLASH_API int dflash_reset(dflash_seq* seq);
+
+/*
+ * One block per sequence (page "cortiq-engine 0.8.71 — src/dflash.rs",
+ * `Drafter::block` and `block_dev`; page "cortiq-engine 0.8.75 —
+ * src/gpu_wgpu/dflash_dev.rs", `Dev::block`): for sequence s the rows
+ * [anchor_tok[s], mask, ..., mask] (block_len rows) at positions
+ * anchor_pos[s], anchor_pos[s]+1, ... run through every draft layer,
+ * attending to context positions [first, min(anchor_pos[s], next)) and to
+ * the block's own rows (not causal); then
+ *   logits[s][j-1] = head . Q(rms(h_j, norm))  for j = 1 .. block_len-1
+ *   draft_tok[s][j-1] = argmax of that row, the lowest index among equals
+ *                       (`top_k` with k = 1), decided on the f32 logits.
+ * Layout: logits [n_seqs][block_len-1][vocab] f32, draft_tok
+ * [n_seqs][block_len-1] u32; either may be NULL (not written).  anchor_tok
+ * [n_seqs] and the outputs are host pointers, or device pointers when
+ * io_on_device is 1; anchor_pos [n_seqs] is always a host pointer (the
+ * positions decide which context rows are read).  Host outputs: the call
+ * returns after one device-to-host copy of the results (one round trip);
+ * device outputs: the work is queued on `stream`.
+ * Errors: EINVAL (null seqs/anchor_tok/anchor_pos, n_seqs < 1, a sequence of
+ * another model, anchor_pos < 0), ERANGE (block_len < 2 or > block), ECUDA.
+ */
+DFLASH_API int dflash_block(dflash_model* model, dflash_seq* const* seqs, int32_t n_seqs, const uint32_t* anchor_tok,
+                 const int64_t* anchor_pos, int32_t block_len, float* logits, uint32_t* draft_tok, int io_on_device,
+                 void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Tracing (the device-side counterpart of the page's stage timers:
+ * page "cortiq-engine 0.8.71 — src/dflash.rs", `stage` / `stage_report`, and
+ * page "cortiq-engine 0.8.75 — src/gpu_wgpu/dflash_dev.rs", the timestamp
+ * queries of `Dev::block`).  While a profile is open, every kernel launch of
+ * the library is bracketed by a pair of CUDA events on the launch's stream and
+ * tagged with the kernel's name and its algorithmic bytes.
+ * ------------------------------------------------------------------------- */
+
+/* Open a profile (clears the previous one).  Errors: EINVAL. */
+DFLASH_API int dflash_profile_start(dflash_model* model);
+
+/* Close the profile: waits for the recorded events, then sums device time,
+ * launches and algorithmic bytes per kernel name.  Errors: EINVAL, ECUDA. */
+DFLASH_API int dflash_profile_stop(dflash_model* model);
+
+/* Entry `index` (0-based) of the closed profile: the kernel's name (a static
+ * string), its launches, total device milliseconds between its event pairs
+ * and total algorithmic bytes.  Returns ERANGE past the last entry. */
+DFLASH_API int dflash_profile_entry(const dflash_model* model, int32_t index, const char** name, int64_t* launches,
+                                    double* total_ms, double* total_bytes);
+
+/* Kernels of this library launched on behalf of `model` since dflash_init
+ * (-1 for NULL). */
+DFLASH_API int64_t dflash_launch_count(const dflash_model* model);
+
+/* ---------------------------------------------------------------------------
+ * Test hooks: views of the library's internal state, for parity checks.
+ * All pointers are host pointers; each call synchronises `stream`.
+ * ------------------------------------------------------------------------- */
+
+/* Matrix ids for the hooks below: DFLASH_MAT_FC, DFLASH_MAT_HEAD, and for
+ * layer l: DFLASH_MAT_LAYER(l, DFLASH_Q) ... DFLASH_MAT_LAYER(l, DFLASH_DOWN). */
+#define DFLASH_MAT_FC 0
+#define DFLASH_MAT_HEAD 1
+#define DFLASH_Q 0
+#define DFLASH_K 1
+#define DFLASH_V 2
+#define DFLASH_O 3
+#define DFLASH_GATE 4
+#define DFLASH_UP 5
+#define DFLASH_DOWN 6
+#define DFLASH_MAT_LAYER(l, which) (2 + 7 * (l) + (which))
+
+/*
+ * The 4-bit codes and f16 scales the library holds for a matrix, unpacked
+ * from its device layout: codes [rows][cols] int8 in [-8, 7] and scales
+ * [rows][cols/32] as f16 bit patterns (the quantiser of
+ * DFLASH_QUANT_Q4G32).  DFLASH_MAT_HEAD is not a 4-bit matrix: use
+ * dflash_debug_head_codes.  Errors: EINVAL (f32 model, bad id), ECUDA.
+ */
+DFLASH_API int dflash_debug_q4_codes(dflash_model* model, int32_t matrix_id, int8_t* codes, uint16_t* scales, void* stream);
+
+/* The head's int8 codes [vocab][hidden] and f32 row scales [vocab]. */
+DFLASH_API int dflash_debug_head_codes(dflash_model* model, int8_t* codes, float* scales, void* stream);
+
+/*
+ * The exact integer group sums of the 4-bit matvec kernel for given int8
+ * activation codes: out[r][n][g] = sum_{k in group g} x[r][k] * q[n][k],
+ * x [rows][cols] int8 (|x| <= 127), out [rows][rows_of_matrix][cols/32]
+ * int32, computed by the same tensor-core inner loop the matmuls run.
+ * Errors: EINVAL (f32 model, bad id, rows < 1 or > 16), ECUDA.
+ */
+DFLASH_API int dflash_debug_q4_groupsums(dflash_model* model, int32_t matrix_id, const int8_t* x, int32_t rows, int32_t* out,
+                              void* stream);
+
+/*
+ * The stored keys and values of context positions [pos, pos + n) of one
+ * layer: k and v [n][kv_heads][head_dim] f32 (either may be NULL).
+ * Errors: EINVAL, ERANGE (positions not held), ECUDA.
+ */
+DFLASH_API int dflash_debug_read_kv(dflash_model* model, const dflash_seq* seq, int32_t layer, int64_t pos, int64_t n, float* k,
+                         float* v, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFLASH_H */

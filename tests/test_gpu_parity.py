@@ -1,0 +1,285 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle on
+the same seeded inputs, at sizes the oracle finishes in seconds (several
+tiles, ragged vocabulary and context tails).
+
+Bars: integer work bit-exact (4-bit and int8 codes, f16 and f32 scales, the
+int32 group sums); f32 config logits within 1e-4 * max|logit|; quantised
+logits within 2e-3 * max|logit|; draft tokens equal wherever the oracle's
+top two logits are further apart than the logits' tolerance.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import workloads as W
+from oracle import OracleModel, OracleSeq, block
+from oracle import quant as Q
+
+pytestmark = pytest.mark.gpu
+
+TOL = {0: 1e-4, 1: 2e-3}  # relative to max|oracle logit|, by geometry.quant
+
+
+def _dfl():
+    import block_speculative_drafting_gb300 as dfl
+    return dfl
+
+
+class Pair:
+    """A GPU model and an oracle model on the same weights."""
+
+    def __init__(self, name, **changes):
+        wl = W.WORKLOADS[name]
+        self.wl = wl
+        self.g = dataclasses.replace(wl.geom, **changes) if changes else wl.geom
+        self.w = W.make_weights(self.g)
+        self.gpu = _dfl().Model(self.g, self.w)
+        self.ora = OracleModel(self.g, self.w)
+
+
+_pairs = {}
+
+
+def pair(name):
+    if name not in _pairs:
+        _pairs[name] = Pair(name)
+    return _pairs[name]
+
+
+def check_logits(g, got, ref, tol_scale=1.0):
+    """max |got - ref| <= tol * max|ref|; tokens equal unless a near tie."""
+    got = np.asarray(got, dtype=np.float64).reshape(ref.shape)
+    scale = float(np.max(np.abs(ref)))
+    err = float(np.max(np.abs(got - ref)))
+    tol = TOL[g.quant] * tol_scale * scale
+    assert err <= tol, f"max|dlogit| {err:.3e} > {tol:.3e}"
+    return err / scale
+
+
+def check_tokens(got_tok, ref_logits, tol_abs):
+    ref32 = ref_logits.astype(np.float32)
+    ref_tok = np.argmax(ref32, axis=-1)
+    srt = np.sort(ref32, axis=-1)
+    margin = srt[..., -1] - srt[..., -2]
+    decided = margin > 2 * tol_abs
+    got_tok = np.asarray(got_tok).reshape(ref_tok.shape)
+    assert (got_tok[decided] == ref_tok[decided]).all()
+    return float(np.mean(got_tok == ref_tok))
+
+
+# ---------------------------------------------------------------- integer work
+@pytest.mark.parametrize("name", ["small_q4", "small_q4_hd64"])
+def test_q4_codes_and_scales_bit_exact(name):
+    dfl = _dfl()
+    p = pair(name)
+    g = p.g
+    mats = [(dfl.MAT_FC, p.w["fc"])]
+    for l in range(g.layers):
+        for which in dfl._abi.MAT_NAMES:
+            mats.append((dfl.mat_layer(l, which), p.w["layers"][l][which]))
+    for mid, w in mats:
+        codes, scales = p.gpu.q4_codes(mid, *w.shape)
+        rq, rs = Q.quantize_q4g32(w)
+        np.testing.assert_array_equal(codes, rq)
+        np.testing.assert_array_equal(scales.view(np.uint16), rs.view(np.uint16))
+
+
+@pytest.mark.parametrize("name", ["small_q4", "small_q4_hd64"])
+def test_head_codes_bit_exact(name):
+    p = pair(name)
+    codes, scales = p.gpu.head_codes()
+    rq, rs = Q.quantize_rows_i8(p.w["head"])
+    np.testing.assert_array_equal(codes, rq)
+    np.testing.assert_array_equal(scales.view(np.uint32), rs.view(np.uint32))
+
+
+@pytest.mark.parametrize("rows", [16, 5, 1])
+def test_group_sums_bit_exact(rows):
+    dfl = _dfl()
+    p = pair("small_q4")
+    rng = np.random.default_rng(rows)
+    for mid, w in [(dfl.MAT_FC, p.w["fc"]), (dfl.mat_layer(1, "down"), p.w["layers"][1]["down"]),
+                   (dfl.mat_layer(0, "k"), p.w["layers"][0]["k"])]:
+        x = rng.integers(-127, 128, size=(rows, w.shape[1]), dtype=np.int8)
+        x[0, :7] = 127
+        x[-1, -9:] = -127
+        got = p.gpu.q4_groupsums(mid, x, w.shape[0])
+        rq, _ = Q.quantize_q4g32(w)
+        np.testing.assert_array_equal(got, Q.q4_group_sums(x, rq).astype(np.int32))
+
+
+# ---------------------------------------------------------------- context append
+@pytest.mark.parametrize("name", ["tiny_f32", "small_q4", "small_q4_hd64"])
+def test_kv_append_matches_oracle(name):
+    p = pair(name)
+    g, n = p.g, p.wl.ctx
+    taps = W.make_taps(g, n, call_id=3)
+    seq = p.gpu.new_sequence(n + 8)
+    p.gpu.ctx_append(seq, 5, taps)
+    assert seq.span() == (5, 5 + n)
+    osq = OracleSeq(p.ora)
+    osq.append(5, taps)
+    tol = 1e-5 if g.quant == 0 else 2e-3
+    for l in range(g.layers):
+        k, v = p.gpu.read_kv(seq, l, 5, n)
+        rk, rv = osq.k[l].transpose(1, 0, 2), osq.v[l].transpose(1, 0, 2)
+        assert np.max(np.abs(k - rk)) <= tol * np.max(np.abs(rk))
+        assert np.max(np.abs(v - rv)) <= tol * np.max(np.abs(rv))
+    seq.close()
+
+
+def test_append_in_chunks_equals_at_once():
+    p = pair("small_q4")
+    g = p.g
+    taps = W.make_taps(g, 40, call_id=4)
+    a = p.gpu.new_sequence(64)
+    p.gpu.ctx_append(a, 0, taps)
+    b = p.gpu.new_sequence(64)
+    for r0, step in [(0, 1), (1, 7), (8, 13), (21, 19)]:
+        p.gpu.ctx_append(b, r0, taps[r0:r0 + step])
+    assert b.span() == (0, 40)
+    for l in range(g.layers):
+        ka, va = p.gpu.read_kv(a, l, 0, 40)
+        kb, vb = p.gpu.read_kv(b, l, 0, 40)
+        np.testing.assert_allclose(kb, ka, rtol=0, atol=2e-3 * np.max(np.abs(ka)))
+        np.testing.assert_allclose(vb, va, rtol=0, atol=2e-3 * np.max(np.abs(va)))
+
+
+# ---------------------------------------------------------------- the block
+@pytest.mark.parametrize("name", ["tiny_f32", "small_q4", "small_q4_hd64"])
+def test_block_matches_oracle(name):
+    p = pair(name)
+    g, n = p.g, p.wl.ctx
+    taps = W.make_taps(g, n)
+    anchor = int(W.make_anchors(g, 1)[0])
+    seq = p.gpu.new_sequence(n + 16)
+    p.gpu.ctx_append(seq, 0, taps)
+    logits, toks = p.gpu.block([seq], [anchor], [n], g.block)
+    osq = OracleSeq(p.ora)
+    osq.append(0, taps)
+    ref, _ = block(p.ora, osq, anchor, n, g.block)
+    check_logits(g, logits[0], ref)
+    check_tokens(toks[0], ref, TOL[g.quant] * np.max(np.abs(ref)))
+    seq.close()
+
+
+@pytest.mark.parametrize("name", ["tiny_f32", "small_q4"])
+def test_block_edge_cases(name):
+    """Shorter blocks, an empty context, an anchor inside the held context, a
+    block reading a context that starts past position 0."""
+    p = pair(name)
+    g = p.g
+    taps = W.make_taps(g, 50, call_id=5)
+    seq = p.gpu.new_sequence(80)
+    osq = OracleSeq(p.ora)
+    cases = [
+        # (append pos, rows, anchor pos, anchor token, block_len)
+        (0, 0, 0, 3, 2),            # empty context, two rows
+        (0, 33, 33, 17, g.block),   # ragged context
+        (0, 50, 20, 9, 3),          # anchor inside the context: reads positions < 20 only
+        (100, 50, 150, 0, g.block), # context starting at position 100
+    ]
+    for pos, rows, apos, atok, bl in cases:
+        p.gpu.ctx_append(seq, pos, taps[:rows])
+        osq.append(pos, taps[:rows])
+        logits, toks = p.gpu.block([seq], [atok], [apos], bl)
+        ref, _ = block(p.ora, osq, atok, apos, bl)
+        assert logits.shape == (1, bl - 1, g.vocab)
+        check_logits(g, logits[0], ref)
+        check_tokens(toks[0], ref, TOL[g.quant] * np.max(np.abs(ref)))
+    seq.close()
+
+
+@pytest.mark.parametrize("name", ["tiny_f32", "small_q4"])
+def test_batched_sequences(name):
+    """Several sequences in one call, each with its own context and anchor."""
+    p = pair(name)
+    g = p.g
+    lens = [7, 0, 61]
+    seqs, oseqs = [], []
+    for i, n in enumerate(lens):
+        s = p.gpu.new_sequence(72)
+        o = OracleSeq(p.ora)
+        t = W.make_taps(g, n, call_id=10 + i)
+        p.gpu.ctx_append(s, 0, t)
+        o.append(0, t)
+        seqs.append(s)
+        oseqs.append(o)
+    anchors = [11, 12, 13]
+    logits, toks = p.gpu.block(seqs, anchors, lens, g.block)
+    for i in range(3):
+        ref, _ = block(p.ora, oseqs[i], anchors[i], lens[i], g.block)
+        check_logits(g, logits[i], ref)
+        check_tokens(toks[i], ref, TOL[g.quant] * np.max(np.abs(ref)))
+    for s in seqs:
+        s.close()
+
+
+def test_truncate_and_reappend():
+    p = pair("small_q4")
+    g = p.g
+    t1 = W.make_taps(g, 40, call_id=20)
+    t2 = W.make_taps(g, 40, call_id=21)
+    seq = p.gpu.new_sequence(64)
+    p.gpu.ctx_append(seq, 0, t1)
+    seq.truncate(25)
+    assert seq.span() == (0, 25)
+    p.gpu.ctx_append(seq, 25, t2[25:])
+    p.gpu.ctx_append(seq, 30, t2[30:35])  # replaces 30.. : context ends at 35
+    assert seq.span() == (0, 35)
+    osq = OracleSeq(p.ora)
+    osq.append(0, np.concatenate([t1[:25], t2[25:35]]))
+    logits, toks = p.gpu.block([seq], [5], [35], g.block)
+    ref, _ = block(p.ora, osq, 5, 35, g.block)
+    check_logits(g, logits[0], ref)
+    seq.reset()
+    assert seq.span() == (0, 0)
+    seq.close()
+
+
+def test_device_io_matches_host_io():
+    import torch
+    p = pair("small_q4")
+    g = p.g
+    taps = W.make_taps(g, 30, call_id=30)
+    seq = p.gpu.new_sequence(40)
+    p.gpu.ctx_append(seq, 0, torch.from_numpy(taps).cuda())
+    lh, th = p.gpu.block([seq], [7], [30], g.block)
+    ld = torch.empty((1, g.block - 1, g.vocab), dtype=torch.float32, device="cuda")
+    td = torch.empty((1, g.block - 1), dtype=torch.int32, device="cuda")
+    p.gpu.block([seq], torch.tensor([7], dtype=torch.int32, device="cuda"), [30], g.block, logits=ld, tokens=td)
+    torch.cuda.synchronize()
+    ref = lh.astype(np.float64)
+    assert np.max(np.abs(ld.cpu().numpy() - ref)) <= 1e-4 * np.max(np.abs(ref))
+    # tokens-only host call
+    _, t2 = p.gpu.block([seq], [7], [30], g.block, want_logits=False)
+    np.testing.assert_array_equal(t2, th)
+    seq.close()
+
+
+def test_error_codes():
+    dfl = _dfl()
+    p = pair("tiny_f32")
+    g = p.g
+    seq = p.gpu.new_sequence(10)
+    with pytest.raises(dfl.DFlashError) as e:
+        p.gpu.ctx_append(seq, 0, W.make_taps(g, 11))
+    assert e.value.code == dfl._abi.DFLASH_ECAPACITY
+    assert seq.span() == (0, 0)
+    p.gpu.ctx_append(seq, 0, W.make_taps(g, 4))
+    for bl in (1, g.block + 1):
+        with pytest.raises(dfl.DFlashError) as e:
+            p.gpu.block([seq], [1], [4], bl)
+        assert e.value.code == dfl._abi.DFLASH_ERANGE
+    with pytest.raises(dfl.DFlashError) as e:
+        p.gpu.block([seq], [g.vocab], [4], 2)
+    assert e.value.code == dfl._abi.DFLASH_EINVAL
+    other = pair("small_q4")
+    with pytest.raises(dfl.DFlashError) as e:
+        other.gpu.block([seq], [1], [4], 2)
+    assert e.value.code == dfl._abi.DFLASH_EINVAL
+    # the model still works after rejected calls
+    logits, _ = p.gpu.block([seq], [1], [4], 2)
+    assert np.isfinite(logits).all()
+    seq.close()
