@@ -237,3 +237,14 @@ class Model:
         self._check(lib().dflash_debug_read_kv(self.handle, seq.handle, layer, int(pos), int(n), _ptr(k), _ptr(v),
                                                _stream(stream)))
         return k, v
+
+    def attention(self, seqs, layer: int, anchor_pos, qkv, y, stream=None):
+        """The block's attention alone (torch CUDA tensors): qkv [rows][(heads+2kv)*hd]
+        with q, k normed and rotated; writes y [rows][heads*hd]."""
+        n = len(seqs)
+        handles = (C.c_void_p * n)(*[s.handle for s in seqs])
+        pos = (C.c_int64 * n)(*[int(p) for p in anchor_pos])
+        bl = int(qkv.shape[0]) // n
+        self._check(lib().dflash_debug_attention(self.handle, handles, n, int(layer), pos, bl, _ptr(qkv), _ptr(y),
+                                                 _stream(stream)))
+        return y

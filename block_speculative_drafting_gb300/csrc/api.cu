@@ -780,6 +780,57 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
     return DFLASH_OK;
 }
 
+// ------------------------------------------------------------------ attention alone
+namespace {
+
+// Checks of an attention call and the per-sequence context views of one layer.
+int attention_views(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, int32_t layer,
+                    const int64_t* anchor_pos, int32_t block_len, const float* qkv, const float* y,
+                    std::vector<AttnSeq>& views, int* max_ctx) {
+    const dflash_geometry& g = m->g;
+    if (!seqs || !anchor_pos || !qkv || !y || n_seqs < 1 || layer < 0 || layer >= g.layers)
+        return set_err(m, DFLASH_EINVAL, "attention: null pointer, n_seqs < 1 or bad layer");
+    if (block_len < 2 || block_len > g.block) return set_err(m, DFLASH_ERANGE, "attention: block_len outside [2, block]");
+    views.assign(n_seqs, AttnSeq{});
+    *max_ctx = 0;
+    for (int s = 0; s < n_seqs; ++s) {
+        const dflash_seq* q = seqs[s];
+        if (!q || q->m != m) return set_err(m, DFLASH_EINVAL, "attention: a sequence is NULL or of another model");
+        if (anchor_pos[s] < 0) return set_err(m, DFLASH_EINVAL, "attention: anchor_pos < 0");
+        const int64_t hi = std::max(std::min(anchor_pos[s], q->first + q->len), q->first);
+        views[s].kc = q->k[layer];
+        views[s].vc = q->v[layer];
+        views[s].cap = q->cap;
+        views[s].lo = 0;
+        views[s].n = (int)(hi - q->first);
+        *max_ctx = std::max(*max_ctx, views[s].n);
+    }
+    return DFLASH_OK;
+}
+
+}  // namespace
+
+int dflash_debug_attention(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, int32_t layer,
+                           const int64_t* anchor_pos, int32_t block_len, const float* qkv, float* y, void* stream) {
+    int rc = check_model(m);
+    if (rc) return rc;
+    std::vector<AttnSeq> views;
+    int max_ctx = 0;
+    rc = attention_views(m, seqs, n_seqs, layer, anchor_pos, block_len, qkv, y, views, &max_ctx);
+    if (rc) return rc;
+    const dflash_geometry& g = m->g;
+    cudaStream_t st = (cudaStream_t)stream;
+    const int64_t part_floats =
+        attn_scratch_floats(n_seqs, block_len, max_ctx, g.heads, g.kv_heads, g.head_dim, m->num_sms);
+    CK(m, ensure(m->part, (size_t)part_floats * sizeof(float)));
+    CK(m, ensure(m->aseqs, (size_t)n_seqs * sizeof(AttnSeq)));
+    CK(m, cudaMemcpyAsync(m->aseqs.p, views.data(), views.size() * sizeof(AttnSeq), cudaMemcpyHostToDevice, st));
+    KL(m, "attention", 2, 0.0, st,
+       attention(qkv, m->qkv_w, n_seqs, block_len, P<AttnSeq>(m->aseqs), max_ctx, g.heads, g.kv_heads, g.head_dim,
+                 1.0f / sqrtf((float)g.head_dim), P<float>(m->part), part_floats, y, m->num_sms, st));
+    return DFLASH_OK;
+}
+
 // ------------------------------------------------------------------ tracing
 int dflash_profile_start(dflash_model* m) {
     if (!m) return DFLASH_EINVAL;

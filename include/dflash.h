@@ -284,6 +284,22 @@ DFLASH_API int dflash_debug_q4_groupsums(dflash_model* model, int32_t matrix_id,
 DFLASH_API int dflash_debug_read_kv(dflash_model* model, const dflash_seq* seq, int32_t layer, int64_t pos, int64_t n, float* k,
                          float* v, void* stream);
 
+/*
+ * The block's attention alone (row b4 of the path; page "cortiq-engine 0.8.71
+ * — src/dflash.rs", `Drafter::block`: scores of every (head, row) over the
+ * context before the anchor and the block's own rows, not causal, softmax,
+ * values).  qkv: device [n_seqs*block_len][(heads + 2*kv_heads)*head_dim] f32,
+ * each row its q heads, then k heads, then v heads, q and k already normed and
+ * rotated; sequence s reads its layer-`layer` context positions
+ * [first, min(anchor_pos[s], next)) and rows s*block_len .. of qkv.  y: device
+ * [n_seqs*block_len][heads*head_dim] f32.  anchor_pos is a host array.  Uses
+ * the model's scratch (allocated on first need).  Work is queued on `stream`.
+ * Errors: EINVAL (null, bad layer or sizes), ERANGE (block_len), ECUDA.
+ */
+DFLASH_API int dflash_debug_attention(dflash_model* model, dflash_seq* const* seqs, int32_t n_seqs, int32_t layer,
+                                      const int64_t* anchor_pos, int32_t block_len, const float* qkv, float* y,
+                                      void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -283,3 +283,43 @@ def test_error_codes():
     logits, _ = p.gpu.block([seq], [1], [4], 2)
     assert np.isfinite(logits).all()
     seq.close()
+
+
+@pytest.mark.parametrize("name", ["tiny_f32", "small_q4", "small_q4_hd64"])
+def test_attention_matches_oracle(name):
+    """Row b4 alone: the block's attention over each sequence's context and
+    its own rows, for seeded q/k/v block rows."""
+    import math
+
+    import torch
+    from oracle import attention as oattn
+    p = pair(name)
+    g = p.g
+    hd, nh, kv, B = g.head_dim, g.heads, g.kv_heads, g.block
+    ctx = [p.wl.ctx, 3]
+    seqs, oseqs = [], []
+    for i, n in enumerate(ctx):
+        s = p.gpu.new_sequence(n + 4)
+        o = OracleSeq(p.ora)
+        t = W.make_taps(g, n, call_id=40 + i)
+        p.gpu.ctx_append(s, 0, t)
+        o.append(0, t)
+        seqs.append(s)
+        oseqs.append(o)
+    width = (nh + 2 * kv) * hd
+    qkv = W.normal(7, 100, (len(ctx) * B, width))
+    y = torch.empty((len(ctx) * B, nh * hd), dtype=torch.float32, device="cuda")
+    layer = g.layers - 1
+    p.gpu.attention(seqs, layer, ctx, torch.from_numpy(qkv).cuda(), y)
+    got = y.cpu().numpy()
+    tol = 1e-4 if g.quant == 0 else 2e-3
+    for s in range(len(ctx)):
+        rows = qkv[s * B:(s + 1) * B].astype(np.float64)
+        q = rows[:, :nh * hd].reshape(B, nh, hd)
+        kb = rows[:, nh * hd:(nh + kv) * hd].reshape(B, kv, hd)
+        vb = rows[:, (nh + kv) * hd:].reshape(B, kv, hd)
+        ref = oattn(q, kb, vb, oseqs[s].k[layer], oseqs[s].v[layer], g.rep, 1 / math.sqrt(hd))
+        out = got[s * B:(s + 1) * B].reshape(B, nh, hd)
+        assert np.max(np.abs(out - ref)) <= tol * np.max(np.abs(ref))
+    for s in seqs:
+        s.close()
