@@ -248,3 +248,16 @@ class Model:
         self._check(lib().dflash_debug_attention(self.handle, handles, n, int(layer), pos, bl, _ptr(qkv), _ptr(y),
                                                  _stream(stream)))
         return y
+
+    def attention_noalloc(self, seqs, layer: int, anchor_pos, qkv, y, stream=None):
+        """`attention` for callers that cannot allocate device memory: its
+        scratch is a fixed array inside the library (see include/dflash.h,
+        dflash_attention_noalloc); calls on one GPU must not overlap."""
+        n = len(seqs)
+        handles = (C.c_void_p * n)(*[s.handle for s in seqs])
+        pos = (C.c_int64 * n)(*[int(p) for p in anchor_pos])
+        bl = int(qkv.shape[0]) // n
+        self._check(lib().dflash_attention_noalloc(self.handle, handles, n, int(layer), pos, bl, _ptr(qkv), _ptr(y),
+                                                   _stream(stream)))
+        return y
+

@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -984,3 +985,83 @@ int dflash_debug_read_kv(dflash_model* m, const dflash_seq* s, int32_t layer, in
 }
 
 }  // extern "C"
+
+// ============================================================================
+// The block's attention without any allocation.
+//
+// Some callers cannot allocate device memory at the moment they need the
+// attention: code running while another component captures a CUDA graph
+// (an allocation would break or be recorded into the capture), processes in
+// which a host framework owns every device byte through its own pool, or
+// latency-critical loops that must never block in the allocator.  For them,
+// dflash_attention_noalloc runs the same attention kernels as
+// dflash_debug_attention, but its scratch (the split partials and the
+// per-sequence context views) lives in the fixed array below, which is part of
+// this library's device image: every GPU that loads the library holds these
+// 16 MiB until the process exits.
+// ============================================================================
+namespace {
+
+constexpr int64_t kNoAllocFloats = int64_t(4) << 20;  // 16 MiB of f32 scratch
+constexpr int64_t kNoAllocViewFloats = 4096;           // the first 16 KiB hold the context views
+constexpr int kNoAllocMaxSeqs = 256;                   // 256 views * 40 B fit in those 16 KiB
+constexpr int kNoAllocMaxDevices = 64;
+
+std::mutex g_noalloc_mutex;
+float* g_noalloc_base[kNoAllocMaxDevices] = {};
+
+}  // namespace
+
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocFloats];
+
+namespace {
+
+// The device address of the fixed array on `device` (which must be current):
+// looked up once per device, then reused.  In host code the array's name is
+// only a host-side stand-in, so kernels must be given this address.
+int noalloc_base(int device, float** out) {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (device < 0 || device >= kNoAllocMaxDevices) return (int)cudaErrorInvalidDevice;
+    if (!g_noalloc_base[device]) {
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return (int)e;
+        g_noalloc_base[device] = static_cast<float*>(p);
+    }
+    *out = g_noalloc_base[device];
+    return 0;
+}
+
+}  // namespace
+
+int dflash_attention_noalloc(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, int32_t layer,
+                             const int64_t* anchor_pos, int32_t block_len, const float* qkv, float* y, void* stream) {
+    int rc = check_model(m);
+    if (rc) return rc;
+    std::vector<AttnSeq> views;
+    int max_ctx = 0;
+    rc = attention_views(m, seqs, n_seqs, layer, anchor_pos, block_len, qkv, y, views, &max_ctx);
+    if (rc) return rc;
+    if (n_seqs > kNoAllocMaxSeqs)
+        return set_err(m, DFLASH_ERANGE, "attention without allocation: " + std::to_string(n_seqs) +
+                                             " sequences, at most " + std::to_string(kNoAllocMaxSeqs));
+    const dflash_geometry& g = m->g;
+    const int64_t part_floats =
+        attn_scratch_floats(n_seqs, block_len, max_ctx, g.heads, g.kv_heads, g.head_dim, m->num_sms);
+    if (part_floats > kNoAllocFloats - kNoAllocViewFloats)
+        return set_err(m, DFLASH_ERANGE, "attention without allocation needs " + std::to_string(part_floats) +
+                                             " floats of scratch; the fixed array holds " +
+                                             std::to_string(kNoAllocFloats - kNoAllocViewFloats));
+    float* base = nullptr;
+    CK(m, noalloc_base(m->device, &base));
+    cudaStream_t st = (cudaStream_t)stream;
+    AttnSeq* views_dev = reinterpret_cast<AttnSeq*>(base);
+    // every partial slot is written by the split kernel before the combine
+    // reads it, so nothing in the array needs to start at zero
+    CK(m, cudaMemcpyAsync(views_dev, views.data(), views.size() * sizeof(AttnSeq), cudaMemcpyHostToDevice, st));
+    CK(m, attention(qkv, m->qkv_w, n_seqs, block_len, views_dev, max_ctx, g.heads, g.kv_heads, g.head_dim,
+                    1.0f / sqrtf((float)g.head_dim), base + kNoAllocViewFloats, part_floats, y, m->num_sms, st));
+    m->launches += 2;
+    return DFLASH_OK;
+}
+
