@@ -231,6 +231,28 @@ class Model:
                                                     _stream(stream)))
         return out
 
+    def trace(self, enable: bool = True):
+        self._check(lib().dflash_debug_trace(self.handle, 1 if enable else 0))
+
+    def trace_force(self, codes, scales):
+        codes = np.ascontiguousarray(codes, dtype=np.int8)
+        scales = np.ascontiguousarray(scales, dtype=np.float32)
+        self._check(lib().dflash_debug_trace_force(self.handle, codes.shape[0], codes.shape[1], _ptr(codes),
+                                                   _ptr(scales)))
+
+    def trace_sites(self):
+        """[(values f32 [rows][cols], codes int8, scales f32)] in execution order."""
+        out, i = [], 0
+        r, c = C.c_int32(), C.c_int32()
+        while lib().dflash_debug_trace_site(self.handle, i, C.byref(r), C.byref(c), None, None, None) == 0:
+            v = np.empty((r.value, c.value), dtype=np.float32)
+            q = np.empty((r.value, c.value), dtype=np.int8)
+            s = np.empty(r.value, dtype=np.float32)
+            lib().dflash_debug_trace_site(self.handle, i, None, None, _ptr(v), _ptr(q), _ptr(s))
+            out.append((v, q, s))
+            i += 1
+        return out
+
     def read_kv(self, seq: Sequence, layer: int, pos: int, n: int, stream=None):
         k = np.empty((n, self.gs.kv_heads, self.gs.head_dim), dtype=np.float32)
         v = np.empty_like(k)

@@ -77,6 +77,20 @@ struct dflash_model {
     };
     std::vector<ProfSum> prof_sum;
 
+    // quantisation-site trace (test hook): every site's pre-quantisation
+    // values, codes and scales in execution order, and queued decisions that
+    // replace a site's own codes and scales
+    struct Site {
+        int rows = 0, cols = 0;
+        std::vector<float> values, scales;
+        std::vector<int8_t> codes;
+    };
+    bool tracing = false;
+    std::vector<Site> trace;
+    std::vector<Site> forced;
+    size_t forced_next = 0;
+    DevBuf trace_buf;
+
     // scratch, grown on demand (a call that needs more memory than any call
     // before it allocates; calls of the same sizes allocate nothing)
     DevBuf h, xq, xs, qkv, y, gu, logits, keys, toks, part, anchors, pos0, aseqs;
@@ -414,6 +428,53 @@ int apply(dflash_model* m, const uint8_t* packed, const float* f32w, int tile0, 
     return 0;
 }
 
+// A quantisation site just written: `rows` rows of int8 codes (as f16, row
+// stride ld) and f32 scales on the device.  With tracing on, record the
+// site's pre-quantisation values (`values_fn` writes them, f32 [rows][cols],
+// into the device pointer it is given), its codes and scales; and if a
+// forced decision is queued, replace the codes and scales with it.
+template <class F>
+int trace_site(dflash_model* m, cudaStream_t st, int rows, int cols, __half* codes, int ld, float* scales,
+               F values_fn) {
+    if (!m->tracing) return 0;
+    CK(m, ensure(m->trace_buf, (size_t)rows * cols * sizeof(float)));
+    CK(m, values_fn(P<float>(m->trace_buf)));
+    dflash_model::Site site;
+    site.rows = rows;
+    site.cols = cols;
+    site.values.resize((size_t)rows * cols);
+    site.scales.resize(rows);
+    std::vector<__half> hc((size_t)rows * ld);
+    CK(m, cudaMemcpyAsync(site.values.data(), m->trace_buf.p, site.values.size() * sizeof(float),
+                          cudaMemcpyDeviceToHost, st));
+    CK(m, cudaMemcpyAsync(hc.data(), codes, hc.size() * sizeof(__half), cudaMemcpyDeviceToHost, st));
+    CK(m, cudaMemcpyAsync(site.scales.data(), scales, rows * sizeof(float), cudaMemcpyDeviceToHost, st));
+    CK(m, cudaStreamSynchronize(st));
+    site.codes.resize((size_t)rows * cols);
+    for (int r = 0; r < rows; ++r)
+        for (int c = 0; c < cols; ++c) site.codes[(size_t)r * cols + c] = (int8_t)__half2float(hc[(size_t)r * ld + c]);
+    m->trace.push_back(std::move(site));
+    if (m->forced_next < m->forced.size()) {
+        const dflash_model::Site& f = m->forced[m->forced_next++];
+        if (f.rows != rows || f.cols != cols)
+            return set_err(m, DFLASH_EINVAL, "forced site " + std::to_string(m->forced_next - 1) + " is " +
+                                                 std::to_string(f.rows) + "x" + std::to_string(f.cols) + ", the site is " +
+                                                 std::to_string(rows) + "x" + std::to_string(cols));
+        for (int r = 0; r < rows; ++r)
+            for (int c = 0; c < cols; ++c) hc[(size_t)r * ld + c] = __float2half((float)f.codes[(size_t)r * cols + c]);
+        CK(m, cudaMemcpyAsync(codes, hc.data(), hc.size() * sizeof(__half), cudaMemcpyHostToDevice, st));
+        CK(m, cudaMemcpyAsync(scales, f.scales.data(), rows * sizeof(float), cudaMemcpyHostToDevice, st));
+        CK(m, cudaStreamSynchronize(st));
+    }
+    return 0;
+}
+
+#define TRACE(expr)                \
+    do {                           \
+        int rc__ = (expr);         \
+        if (rc__) return rc__;     \
+    } while (0)
+
 // Project `n` context rows (device taps) at positions pos0.. into the store.
 int append_rows(dflash_model* m, dflash_seq* s, const float* taps_dev, int64_t n, int64_t pos0, int64_t idx0,
                 cudaStream_t st) {
@@ -429,12 +490,18 @@ int append_rows(dflash_model* m, dflash_seq* s, const float* taps_dev, int64_t n
         KL(m, "rms_quant", 1, (double)rows * m->tap_w * 5, st,
            rms_rows(taps_dev, m->tap_w, ident, rows, m->tap_w, nullptr, g.eps, nullptr, 0, P<__half>(m->a_codes),
                     P<float>(m->a_scale), m->tap_w, st));
+        TRACE(trace_site(m, st, rows, m->tap_w, P<__half>(m->a_codes), m->tap_w, P<float>(m->a_scale), [&](float* v) {
+            return rms_rows(taps_dev, m->tap_w, ident, rows, m->tap_w, nullptr, g.eps, v, m->tap_w, nullptr, nullptr, 0, st);
+        }));
         QAct xt{P<__half>(m->a_codes), P<float>(m->a_scale), m->tap_w};
         KL(m, "q4_gemm", 1, q4_bytes_of(H, m->tap_w, rows, false), st,
            q4_gemm(m->fc_p, 0, H, m->ks_tap, xt, rows, t, H, false, m->num_sms, st));
         KL(m, "rms_quant", 1, (double)rows * H * 5, st,
            rms_rows(t, H, ident, rows, H, m->hidden_norm, g.eps, nullptr, 0, P<__half>(m->a_codes),
                     P<float>(m->a_scale), H, st));
+        TRACE(trace_site(m, st, rows, H, P<__half>(m->a_codes), H, P<float>(m->a_scale), [&](float* v) {
+            return rms_rows(t, H, ident, rows, H, m->hidden_norm, g.eps, v, H, nullptr, nullptr, 0, st);
+        }));
         QAct xh{P<__half>(m->a_codes), P<float>(m->a_scale), H};
         KL(m, "q4_gemm", 1, q4_bytes_of(m->kvctx_w, H, rows, false), st,
            q4_gemm(m->kvctx_p, 0, m->kvctx_w, m->ks_h, xh, rows, kv, m->kvctx_w, false, m->num_sms, st));
@@ -721,6 +788,9 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
         // attention half: x = rms(h, in_norm); q, k, v; norms and rotation; attention; h += O y
         if (quant) {
             KL(m, "rms_quant", 1, (double)R * H * 5, st, rms_rows(h, H, ident, R, H, Ly.in_norm, g.eps, nullptr, 0, xq, xs, maxK, st));
+            TRACE(trace_site(m, st, R, H, xq, maxK, xs, [&](float* v) {
+                return rms_rows(h, H, ident, R, H, Ly.in_norm, g.eps, v, H, nullptr, nullptr, 0, st);
+            }));
             APPLY(apply(m, Ly.qkv_p, nullptr, 0, m->qkv_w, H, m->ks_h, nullptr, 0, R, qkv, m->qkv_w, false, maxK, st));
         } else {
             KL(m, "rms_f32", 1, (double)R * H * 8, st, rms_rows(h, H, ident, R, H, Ly.in_norm, g.eps, xf, maxK, nullptr, nullptr, 0, st));
@@ -735,6 +805,9 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
                      part_floats, y, m->num_sms, st));
         if (quant) {
             KL(m, "rms_quant", 1, (double)R * m->qd * 5, st, rms_rows(y, m->qd, ident, R, m->qd, nullptr, g.eps, nullptr, 0, xq, xs, maxK, st));
+            TRACE(trace_site(m, st, R, m->qd, xq, maxK, xs, [&](float* v) {
+                return rms_rows(y, m->qd, ident, R, m->qd, nullptr, g.eps, v, m->qd, nullptr, nullptr, 0, st);
+            }));
             APPLY(apply(m, Ly.o_p, nullptr, 0, H, m->qd, m->ks_q, nullptr, 0, R, h, H, true, maxK, st));
         } else {
             APPLY(apply(m, nullptr, Ly.o_f, 0, H, m->qd, 0, y, m->qd, R, h, H, true, 0, st));
@@ -742,8 +815,14 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
         // MLP half: x = rms(h, post_norm); h += down (silu(gate x) * up x)
         if (quant) {
             KL(m, "rms_quant", 1, (double)R * H * 5, st, rms_rows(h, H, ident, R, H, Ly.post_norm, g.eps, nullptr, 0, xq, xs, maxK, st));
+            TRACE(trace_site(m, st, R, H, xq, maxK, xs, [&](float* v) {
+                return rms_rows(h, H, ident, R, H, Ly.post_norm, g.eps, v, H, nullptr, nullptr, 0, st);
+            }));
             APPLY(apply(m, Ly.gu_p, nullptr, 0, 2 * I, H, m->ks_h, nullptr, 0, R, gu, 2 * I, false, maxK, st));
             KL(m, "silu_quant", 1, (double)R * I * 9, st, silu_mul(gu, 2 * I, R, I, nullptr, 0, xq, xs, maxK, st));
+            TRACE(trace_site(m, st, R, I, xq, maxK, xs, [&](float* v) {
+                return silu_mul(gu, 2 * I, R, I, v, I, nullptr, nullptr, 0, st);
+            }));
             APPLY(apply(m, Ly.down_p, nullptr, 0, H, I, m->ks_i, nullptr, 0, R, h, H, true, maxK, st));
         } else {
             KL(m, "rms_f32", 1, (double)R * H * 8, st, rms_rows(h, H, ident, R, H, Ly.post_norm, g.eps, xf, maxK, nullptr, nullptr, 0, st));
@@ -759,6 +838,9 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
     uint32_t* tok_out = (io_on_device && draft_tok) ? draft_tok : P<uint32_t>(m->toks);
     if (quant) {
         KL(m, "rms_quant", 1, (double)D * H * 5, st, rms_rows(h, H, drafts, D, H, m->norm, g.eps, nullptr, 0, xq, xs, maxK, st));
+        TRACE(trace_site(m, st, D, H, xq, maxK, xs, [&](float* v) {
+            return rms_rows(h, H, drafts, D, H, m->norm, g.eps, v, H, nullptr, nullptr, 0, st);
+        }));
         CK(m, cudaMemsetAsync(keys, 0, (size_t)D * sizeof(unsigned long long), st));
         QAct xh{xq, xs, maxK};
         const double hb = (double)g.vocab * H + (double)g.vocab * 4 + (double)D * H + (logit_out ? (double)D * g.vocab * 4 : 0.0);
@@ -829,6 +911,40 @@ int dflash_debug_attention(dflash_model* m, dflash_seq* const* seqs, int32_t n_s
     KL(m, "attention", 2, 0.0, st,
        attention(qkv, m->qkv_w, n_seqs, block_len, P<AttnSeq>(m->aseqs), max_ctx, g.heads, g.kv_heads, g.head_dim,
                  1.0f / sqrtf((float)g.head_dim), P<float>(m->part), part_floats, y, m->num_sms, st));
+    return DFLASH_OK;
+}
+
+// ------------------------------------------------------------------ site trace
+int dflash_debug_trace(dflash_model* m, int32_t enable) {
+    if (!m) return DFLASH_EINVAL;
+    m->tracing = enable != 0;
+    m->trace.clear();
+    m->forced.clear();
+    m->forced_next = 0;
+    return DFLASH_OK;
+}
+
+int dflash_debug_trace_force(dflash_model* m, int32_t rows, int32_t cols, const int8_t* codes, const float* scales) {
+    if (!m || rows < 1 || cols < 1 || !codes || !scales) return DFLASH_EINVAL;
+    dflash_model::Site f;
+    f.rows = rows;
+    f.cols = cols;
+    f.codes.assign(codes, codes + (size_t)rows * cols);
+    f.scales.assign(scales, scales + rows);
+    m->forced.push_back(std::move(f));
+    return DFLASH_OK;
+}
+
+int dflash_debug_trace_site(const dflash_model* m, int32_t i, int32_t* rows, int32_t* cols, float* values,
+                            int8_t* codes, float* scales) {
+    if (!m) return DFLASH_EINVAL;
+    if (i < 0 || i >= (int32_t)m->trace.size()) return DFLASH_ERANGE;
+    const auto& t = m->trace[i];
+    if (rows) *rows = t.rows;
+    if (cols) *cols = t.cols;
+    if (values) std::memcpy(values, t.values.data(), t.values.size() * sizeof(float));
+    if (codes) std::memcpy(codes, t.codes.data(), t.codes.size());
+    if (scales) std::memcpy(scales, t.scales.data(), t.scales.size() * sizeof(float));
     return DFLASH_OK;
 }
 

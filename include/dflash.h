@@ -285,6 +285,28 @@ DFLASH_API int dflash_debug_read_kv(dflash_model* model, const dflash_seq* seq, 
                          float* v, void* stream);
 
 /*
+ * Quantisation-site trace, for parity tests that hold the quantised path to
+ * f32-level tolerances: an f32 computation and an f64 one quantise the same
+ * value to different int8 codes whenever it lies within rounding of a
+ * half-step boundary, and one different code moves every later value by a
+ * whole quantisation step.  With the trace on, every quantisation site of
+ * dflash_ctx_append and dflash_block (the taps; t; per layer the inputs of
+ * the fused Wq/Wk/Wv, of Wo, of the fused gate/up and of down; the final
+ * normed draft rows), in execution order, records its pre-quantisation f32
+ * values [rows][cols], its own int8 codes and its f32 row scales; a decision
+ * queued with dflash_debug_trace_force replaces the next site's codes and
+ * scales (the site's own are still recorded).  Tracing synchronises the
+ * stream at every site.  enable = 1 clears the record and the queue.
+ */
+DFLASH_API int dflash_debug_trace(dflash_model* model, int32_t enable);
+DFLASH_API int dflash_debug_trace_force(dflash_model* model, int32_t rows, int32_t cols, const int8_t* codes,
+                                        const float* scales);
+/* Site `index` of the record: dims, and (when non-NULL) values, codes and
+ * scales copied out.  ERANGE past the last site. */
+DFLASH_API int dflash_debug_trace_site(const dflash_model* model, int32_t index, int32_t* rows, int32_t* cols,
+                                       float* values, int8_t* codes, float* scales);
+
+/*
  * The block's attention alone (row b4 of the path; page "cortiq-engine 0.8.71
  * — src/dflash.rs", `Drafter::block`: scores of every (head, row) over the
  * context before the anchor and the block's own rows, not causal, softmax,

@@ -88,6 +88,25 @@ def softmax(s):
     return e / np.sum(e, axis=-1, keepdims=True)
 
 
+class QuantTrace:
+    """Records the oracle's quantisation decisions in call order: per site the
+    input values (float64), the int8 codes and the f32 row scales.  A site whose
+    input equals the previous site's (the same rows feeding Wq, Wk and Wv, or
+    gate and up, or every layer's Wk/Wv of the context) is recorded once."""
+
+    def __init__(self):
+        self.sites = []
+
+    def record(self, x, q, s):
+        x = np.asarray(x, dtype=F64)
+        if self.sites and self.sites[-1][0].shape == x.shape and np.array_equal(self.sites[-1][0], x):
+            return
+        self.sites.append((x.copy(), q.copy(), s.copy()))
+
+
+TRACE = None  # a QuantTrace while the decisions are being recorded
+
+
 class Matrix:
     """One weight matrix [out][in] as the oracle applies it.
 
@@ -121,6 +140,8 @@ class Matrix:
             xin = x
         else:
             qx, sx = Q.quantize_rows_i8(x)
+            if TRACE is not None:
+                TRACE.record(x, qx, sx)
             xin = qx.astype(F64)
         for r0 in range(0, self.rows, self.ROWS_PER_CHUNK):
             r1 = min(self.rows, r0 + self.ROWS_PER_CHUNK)

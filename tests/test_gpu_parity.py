@@ -47,12 +47,36 @@ def pair(name):
     return _pairs[name]
 
 
-def check_logits(g, got, ref, tol_scale=1.0):
-    """max |got - ref| <= tol * max|ref|; tokens equal unless a near tie."""
+def decision_noise(om, osq, anchor, anchor_pos, bl, ref, runs=2):
+    """max |logits - ref| / max|ref| of the oracle against itself when the
+    values it quantises carry f32-level noise (1e-7 relative): the spread
+    that differing rounding-boundary decisions alone produce."""
+    from oracle import quant as Q
+    orig = Q.quantize_rows_i8
+    rng = np.random.default_rng(123)
+    devs = []
+    try:
+        Q.quantize_rows_i8 = lambda x: orig(np.asarray(x, np.float64) * (1 + 1e-7 * rng.standard_normal(np.shape(x))))
+        for _ in range(runs):
+            lp, _ = block(om, osq, anchor, anchor_pos, bl)
+            devs.append(float(np.max(np.abs(lp - ref))) / float(np.max(np.abs(ref))))
+    finally:
+        Q.quantize_rows_i8 = orig
+    return max(devs)
+
+
+def check_logits(g, got, ref, tol_scale=1.0, noise=None):
+    """f32 format: max |got - ref| <= 1e-4 * max|ref|.  Quantised format: the
+    same with 2e-3, or, where the two sides' own quantisation decisions differ
+    at rounding boundaries (free running), within three times the oracle's own
+    decision-noise spread (`noise()` computes it when needed); the
+    identical-decision tests hold the quantised path to 1e-5."""
     got = np.asarray(got, dtype=np.float64).reshape(ref.shape)
     scale = float(np.max(np.abs(ref)))
     err = float(np.max(np.abs(got - ref)))
     tol = TOL[g.quant] * tol_scale * scale
+    if err > tol and g.quant and noise is not None:
+        tol = max(tol, 3 * noise() * scale + tol)
     assert err <= tol, f"max|dlogit| {err:.3e} > {tol:.3e}"
     return err / scale
 
@@ -159,8 +183,9 @@ def test_block_matches_oracle(name):
     osq = OracleSeq(p.ora)
     osq.append(0, taps)
     ref, _ = block(p.ora, osq, anchor, n, g.block)
-    check_logits(g, logits[0], ref)
-    check_tokens(toks[0], ref, TOL[g.quant] * np.max(np.abs(ref)))
+    check_logits(g, logits[0], ref, noise=lambda: decision_noise(p.ora, osq, anchor, n, g.block, ref))
+    if g.quant == 0:
+        check_tokens(toks[0], ref, TOL[g.quant] * np.max(np.abs(ref)))
     seq.close()
 
 
@@ -186,8 +211,9 @@ def test_block_edge_cases(name):
         logits, toks = p.gpu.block([seq], [atok], [apos], bl)
         ref, _ = block(p.ora, osq, atok, apos, bl)
         assert logits.shape == (1, bl - 1, g.vocab)
-        check_logits(g, logits[0], ref)
-        check_tokens(toks[0], ref, TOL[g.quant] * np.max(np.abs(ref)))
+        check_logits(g, logits[0], ref, noise=lambda: decision_noise(p.ora, osq, atok, apos, bl, ref))
+        if g.quant == 0:
+            check_tokens(toks[0], ref, TOL[g.quant] * np.max(np.abs(ref)))
     seq.close()
 
 
@@ -210,8 +236,13 @@ def test_batched_sequences(name):
     logits, toks = p.gpu.block(seqs, anchors, lens, g.block)
     for i in range(3):
         ref, _ = block(p.ora, oseqs[i], anchors[i], lens[i], g.block)
-        check_logits(g, logits[i], ref)
-        check_tokens(toks[i], ref, TOL[g.quant] * np.max(np.abs(ref)))
+        check_logits(g, logits[i], ref, noise=lambda: decision_noise(p.ora, oseqs[i], anchors[i], lens[i], g.block, ref))
+        if g.quant == 0:
+            check_tokens(toks[i], ref, TOL[g.quant] * np.max(np.abs(ref)))
+        # a sequence in a batch computes what it computes alone
+        single, _ = p.gpu.block([seqs[i]], [anchors[i]], [lens[i]], g.block)
+        check_logits(g, logits[i], single[0].astype(np.float64), tol_scale=0.5,
+                     noise=lambda: decision_noise(p.ora, oseqs[i], anchors[i], lens[i], g.block, ref))
     for s in seqs:
         s.close()
 
@@ -232,7 +263,7 @@ def test_truncate_and_reappend():
     osq.append(0, np.concatenate([t1[:25], t2[25:35]]))
     logits, toks = p.gpu.block([seq], [5], [35], g.block)
     ref, _ = block(p.ora, osq, 5, 35, g.block)
-    check_logits(g, logits[0], ref)
+    check_logits(g, logits[0], ref, noise=lambda: decision_noise(p.ora, osq, 5, 35, g.block, ref))
     seq.reset()
     assert seq.span() == (0, 0)
     seq.close()
@@ -323,3 +354,75 @@ def test_attention_matches_oracle(name):
         assert np.max(np.abs(out - ref)) <= tol * np.max(np.abs(ref))
     for s in seqs:
         s.close()
+
+
+# ---------------------------------------------------------------- identical decisions
+def forced_run(p, ctx, anchor, taps, pos=0):
+    """Run the oracle recording its quantisation decisions, then the GPU with
+    every site's codes and scales replaced by the oracle's.  Returns the
+    oracle's sites, the GPU's own sites, both logits and the GPU sequence."""
+    import oracle.drafter as D
+    g = p.g
+    D.TRACE = D.QuantTrace()
+    try:
+        osq = OracleSeq(p.ora)
+        osq.append(pos, taps)
+        ref, ref_tok = block(p.ora, osq, anchor, pos + ctx, g.block)
+        sites = D.TRACE.sites
+    finally:
+        D.TRACE = None
+    seq = p.gpu.new_sequence(ctx + 8)
+    p.gpu.trace(True)
+    for x, q, s in sites:
+        p.gpu.trace_force(q, s)
+    try:
+        p.gpu.ctx_append(seq, pos, taps)
+        logits, toks = p.gpu.block([seq], [anchor], [pos + ctx], g.block)
+        own = p.gpu.trace_sites()
+    finally:
+        p.gpu.trace(False)
+    return sites, own, ref, ref_tok, logits[0], toks[0], seq, osq
+
+
+def check_sites(sites, own, value_tol):
+    """Per site: values agree to value_tol * max|x|, scales likewise, and the
+    GPU's own codes equal the oracle's except where the oracle's value lies
+    within rounding of a half-step boundary.  Returns the flipped-code count."""
+    assert len(own) == len(sites), (len(own), len(sites))
+    flips = 0
+    for i, ((x, q, s), (v, qg, sg)) in enumerate(zip(sites, own)):
+        assert v.shape == x.shape, (i, v.shape, x.shape)
+        err = np.max(np.abs(v - x))
+        assert err <= value_tol * np.max(np.abs(x)), f"site {i}: values differ by {err:.3e}"
+        np.testing.assert_allclose(sg, s, rtol=value_tol, atol=0, err_msg=f"site {i} scales")
+        diff = qg != q
+        if diff.any():
+            r = np.asarray(x, np.float32) / np.where(s > 0, s, 1)[:, None]
+            dist = np.abs(np.abs(r - np.floor(r)) - 0.5)
+            near = dist <= value_tol * np.maximum(np.abs(r), 1.0) * 4
+            assert (near[diff]).all(), f"site {i}: code differs away from a rounding boundary"
+            assert (np.abs(qg.astype(int) - q)[diff] == 1).all()
+            flips += int(diff.sum())
+    return flips
+
+
+@pytest.mark.parametrize("name", ["small_q4", "small_q4_hd64"])
+def test_identical_decisions_parity(name):
+    """With the oracle's quantisation decisions at every site, the GPU's
+    continuous values at every site agree to f32 level (1e-5 relative), and so
+    do the logits; its own decisions differ only at rounding boundaries."""
+    p = pair(name)
+    g, n = p.g, p.wl.ctx
+    taps = W.make_taps(g, n, call_id=50)
+    for anchor in (11, 4000 % g.vocab):
+        sites, own, ref, ref_tok, logits, toks, seq, osq = forced_run(p, n, anchor, taps)
+        assert len(sites) == 2 + 4 * g.layers + 1
+        check_sites(sites, own, 1e-5)
+        scale = np.max(np.abs(ref))
+        assert np.max(np.abs(logits - ref)) <= 1e-5 * scale
+        assert (toks == ref_tok).all()
+        for l in range(g.layers):
+            k, v = p.gpu.read_kv(seq, l, 0, n)
+            assert np.max(np.abs(k - osq.k[l].transpose(1, 0, 2))) <= 1e-5 * np.max(np.abs(osq.k[l]))
+            assert np.max(np.abs(v - osq.v[l].transpose(1, 0, 2))) <= 1e-5 * np.max(np.abs(osq.v[l]))
+        seq.close()
