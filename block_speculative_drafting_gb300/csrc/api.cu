@@ -35,8 +35,17 @@ struct Layer {
 struct MatView {
     const uint8_t* packed;
     const float* f32;
-    int tile0, N, K, ksteps;
+    int tile0, N, K;
+    Q4Layout L;
 };
+
+Q4Layout make_layout(int rows, int K) {
+    Q4Layout L;
+    L.ngroups = rows / 64;
+    L.ksteps = K / kQ4KStep;
+    L.kb = q4_kblock_steps(L.ksteps);
+    return L;
+}
 
 }  // namespace
 
@@ -57,7 +66,10 @@ struct dflash_model {
     const float** k_norm_dev = nullptr;  // [L] device pointers to k_norm
 
     int qd = 0, kd = 0, qkv_w = 0, tap_w = 0, kvctx_w = 0;
-    int ks_h = 0, ks_i = 0, ks_q = 0, ks_tap = 0;
+    // layouts of the packed 4-bit matrices (the same for every layer)
+    Q4Layout L_fc{}, L_kvctx{}, L_qkv{}, L_o{}, L_gu{}, L_down{};
+    int* err_dev = nullptr;   // raised by a kernel whose bounded wait expired
+    int* err_host = nullptr;  // pinned copy, read after a synchronising call
 
     // launch accounting and the optional per-launch event profile
     int64_t launches = 0;  // kernels of this library launched since init
@@ -94,7 +106,20 @@ struct dflash_model {
     // scratch, grown on demand (a call that needs more memory than any call
     // before it allocates; calls of the same sizes allocate nothing)
     DevBuf h, xq, xs, qkv, y, gu, logits, keys, toks, part, anchors, pos0, aseqs;
-    DevBuf a_taps, a_codes, a_scale, a_t, a_kv;
+    DevBuf a_taps, a_codes, a_scale, a_t, a_kv, a_pos;
+    bool grown = false;  // a scratch buffer moved since the graphs were captured
+
+    // CUDA graphs of the kernel sequences of a block and of a short append,
+    // captured once per shape (and buffer set) on cap_stream, replayed on
+    // the caller's stream
+    struct GraphEntry {
+        std::vector<int64_t> key;
+        cudaGraphExec_t exec;
+        int64_t kernels;
+    };
+    std::vector<GraphEntry> graphs;
+    cudaStream_t cap_stream = nullptr;
+    bool use_graphs = true;
 };
 
 struct dflash_seq {
@@ -168,8 +193,9 @@ int dalloc(dflash_model* m, T** p, size_t count) {
     return 0;
 }
 
-int ensure(DevBuf& b, size_t bytes) {
+int ensure(DevBuf& b, size_t bytes, bool* grown = nullptr) {
     if (b.bytes >= bytes) return 0;
+    if (grown) *grown = true;
     if (b.p) cudaFree(b.p);
     b.p = nullptr;
     b.bytes = 0;
@@ -183,6 +209,20 @@ void free_buf(DevBuf& b) {
     if (b.p) cudaFree(b.p);
     b.p = nullptr;
     b.bytes = 0;
+}
+
+void clear_graphs(dflash_model* m) {
+    for (auto& e : m->graphs) cudaGraphExecDestroy(e.exec);
+    m->graphs.clear();
+}
+
+// A model's scratch buffer of at least `bytes`; growing it drops the
+// captured graphs (they hold the old address).
+int ensure_m(dflash_model* m, DevBuf& b, size_t bytes) {
+    bool grown = false;
+    int e = ensure(b, bytes, &grown);
+    if (grown) clear_graphs(m);
+    return e;
 }
 
 template <class T>
@@ -230,22 +270,30 @@ int copy_f32(dflash_model* m, float* dst, const float* src, size_t count, bool o
 
 MatView mat_view(const dflash_model* m, int id) {
     const dflash_geometry& g = m->g;
-    MatView v{nullptr, nullptr, 0, 0, 0, 0};
-    if (id == DFLASH_MAT_FC) return MatView{m->fc_p, m->fc_f, 0, g.hidden, m->tap_w, m->ks_tap};
-    if (id == DFLASH_MAT_HEAD) return MatView{nullptr, m->head_f, 0, g.vocab, g.hidden, g.hidden / kI8KStep};
+    MatView v{nullptr, nullptr, 0, 0, 0, Q4Layout{}};
+    if (id == DFLASH_MAT_FC) return MatView{m->fc_p, m->fc_f, 0, g.hidden, m->tap_w, m->L_fc};
+    if (id == DFLASH_MAT_HEAD) return MatView{nullptr, m->head_f, 0, g.vocab, g.hidden, Q4Layout{}};
     int rel = id - 2;
     if (rel < 0 || rel >= 7 * g.layers) return v;
     const Layer& L = m->layers[rel / 7];
+    const size_t H = g.hidden, I = g.intermediate;
     switch (rel % 7) {
-        case DFLASH_Q: return MatView{L.qkv_p, L.qkv_f, 0, m->qd, g.hidden, m->ks_h};
-        case DFLASH_K: return MatView{L.qkv_p, L.qkv_f ? L.qkv_f + (size_t)m->qd * g.hidden : nullptr, m->qd / 16, m->kd, g.hidden, m->ks_h};
-        case DFLASH_V: return MatView{L.qkv_p, L.qkv_f ? L.qkv_f + (size_t)(m->qd + m->kd) * g.hidden : nullptr, (m->qd + m->kd) / 16, m->kd, g.hidden, m->ks_h};
-        case DFLASH_O: return MatView{L.o_p, L.o_f, 0, g.hidden, m->qd, m->ks_q};
-        case DFLASH_GATE: return MatView{L.gu_p, L.gu_f, 0, g.intermediate, g.hidden, m->ks_h};
-        case DFLASH_UP: return MatView{L.gu_p, L.gu_f ? L.gu_f + (size_t)g.intermediate * g.hidden : nullptr, g.intermediate / 16, g.intermediate, g.hidden, m->ks_h};
-        case DFLASH_DOWN: return MatView{L.down_p, L.down_f, 0, g.hidden, g.intermediate, m->ks_i};
+        case DFLASH_Q: return MatView{L.qkv_p, L.qkv_f, 0, m->qd, g.hidden, m->L_qkv};
+        case DFLASH_K: return MatView{L.qkv_p, L.qkv_f ? L.qkv_f + (size_t)m->qd * H : nullptr, m->qd / 16, m->kd, g.hidden, m->L_qkv};
+        case DFLASH_V: return MatView{L.qkv_p, L.qkv_f ? L.qkv_f + (size_t)(m->qd + m->kd) * H : nullptr, (m->qd + m->kd) / 16, m->kd, g.hidden, m->L_qkv};
+        case DFLASH_O: return MatView{L.o_p, L.o_f, 0, g.hidden, m->qd, m->L_o};
+        case DFLASH_GATE: return MatView{L.gu_p, L.gu_f, 0, g.intermediate, g.hidden, m->L_gu};
+        case DFLASH_UP: return MatView{L.gu_p, L.gu_f ? L.gu_f + I * H : nullptr, g.intermediate / 16, g.intermediate, g.hidden, m->L_gu};
+        case DFLASH_DOWN: return MatView{L.down_p, L.down_f, 0, g.hidden, g.intermediate, m->L_down};
     }
     return v;
+}
+
+// A kernel gave up a bounded wait (its data never arrived): the results of
+// the call are incomplete and the model is not trusted any more.
+int device_wait_expired(dflash_model* m) {
+    m->poisoned = true;
+    return set_err(m, DFLASH_ECUDA, "a kernel's bounded wait for its data expired; results are incomplete");
 }
 
 int check_model(dflash_model* m) {
@@ -264,10 +312,16 @@ int build_model(dflash_model* m, const dflash_weights* w, bool on_dev, cudaStrea
     m->qkv_w = m->qd + 2 * m->kd;
     m->tap_w = g.n_taps * H;
     m->kvctx_w = L * 2 * m->kd;
-    m->ks_h = H / kQ4KStep;
-    m->ks_i = I / kQ4KStep;
-    m->ks_q = m->qd / kQ4KStep;
-    m->ks_tap = m->tap_w / kQ4KStep;
+    m->L_fc = make_layout(H, m->tap_w);
+    m->L_kvctx = make_layout(m->kvctx_w, H);
+    m->L_qkv = make_layout(m->qkv_w, H);
+    m->L_o = make_layout(H, m->qd);
+    m->L_gu = make_layout(2 * I, H);
+    m->L_down = make_layout(H, I);
+    CK(m, dalloc(m, &m->err_dev, 1));
+    CK(m, cudaMemset(m->err_dev, 0, sizeof(int)));
+    CK(m, cudaMallocHost(&m->err_host, sizeof(int)));
+    *m->err_host = 0;
     const bool quant = g.quant == DFLASH_QUANT_Q4G32;
 
     // staging buffer for host weights: the largest tensor
@@ -294,23 +348,23 @@ int build_model(dflash_model* m, const dflash_weights* w, bool on_dev, cudaStrea
     CK(m, cudaMemcpy(m->inv_freq, invf.data(), invf.size() * sizeof(float), cudaMemcpyHostToDevice));
 
     const float* d = nullptr;
-    auto pack = [&](const float* src, int N, int K, uint8_t* dst, int tile0, int ksteps) -> int {
+    auto pack = [&](const float* src, int N, int K, uint8_t* dst, int tile0, Q4Layout Lo) -> int {
         int e = to_device(m, src, (size_t)N * K, on_dev, stage, &d);
         if (e) return e;
-        e = q4_quantize_pack(d, N, K, dst, tile0, ksteps, sc_scratch, st);
+        e = q4_quantize_pack(d, N, K, dst, Lo, tile0, sc_scratch, st);
         if (e) return e;
         return (int)cudaStreamSynchronize(st);  // the stage is reused by the next tensor
     };
-    auto q4_bytes = [](int rows, int ksteps) { return (size_t)((rows + 15) / 16) * ksteps * kQ4Chunk; };
+    auto q4_bytes = [](Q4Layout Lo) { return (size_t)Lo.ngroups * Lo.ksteps * 4 * kQ4Chunk; };
 
     // fc and the all-layer Wk||Wv of the context projection
     if (quant) {
-        CK(m, dalloc(m, &m->fc_p, q4_bytes(H, m->ks_tap)));
-        CK(m, pack(w->fc, H, m->tap_w, m->fc_p, 0, m->ks_tap));
-        CK(m, dalloc(m, &m->kvctx_p, q4_bytes(m->kvctx_w, m->ks_h)));
+        CK(m, dalloc(m, &m->fc_p, q4_bytes(m->L_fc)));
+        CK(m, pack(w->fc, H, m->tap_w, m->fc_p, 0, m->L_fc));
+        CK(m, dalloc(m, &m->kvctx_p, q4_bytes(m->L_kvctx)));
         for (int l = 0; l < L; ++l) {
-            CK(m, pack(w->k[l], m->kd, H, m->kvctx_p, (l * 2 * m->kd) / 16, m->ks_h));
-            CK(m, pack(w->v[l], m->kd, H, m->kvctx_p, (l * 2 * m->kd + m->kd) / 16, m->ks_h));
+            CK(m, pack(w->k[l], m->kd, H, m->kvctx_p, (l * 2 * m->kd) / 16, m->L_kvctx));
+            CK(m, pack(w->v[l], m->kd, H, m->kvctx_p, (l * 2 * m->kd + m->kd) / 16, m->L_kvctx));
         }
     } else {
         CK(m, dalloc(m, &m->fc_f, (size_t)H * m->tap_w));
@@ -323,7 +377,7 @@ int build_model(dflash_model* m, const dflash_weights* w, bool on_dev, cudaStrea
     }
     // head
     if (quant) {
-        const int vpad = (g.vocab + 15) / 16 * 16;
+        const int vpad = (g.vocab + 63) / 64 * 64;
         CK(m, dalloc(m, &m->head_p, (size_t)vpad * H));
         CK(m, dalloc(m, &m->head_scale, vpad));
         CK(m, to_device(m, w->head, (size_t)g.vocab * H, on_dev, stage, &d));
@@ -348,17 +402,17 @@ int build_model(dflash_model* m, const dflash_weights* w, bool on_dev, cudaStrea
         CK(m, copy_f32(m, Ly.k_norm, w->k_norm[l], hd, on_dev));
         knorm_ptrs[l] = Ly.k_norm;
         if (quant) {
-            CK(m, dalloc(m, &Ly.qkv_p, q4_bytes(m->qkv_w, m->ks_h)));
-            CK(m, pack(w->q[l], m->qd, H, Ly.qkv_p, 0, m->ks_h));
-            CK(m, pack(w->k[l], m->kd, H, Ly.qkv_p, m->qd / 16, m->ks_h));
-            CK(m, pack(w->v[l], m->kd, H, Ly.qkv_p, (m->qd + m->kd) / 16, m->ks_h));
-            CK(m, dalloc(m, &Ly.o_p, q4_bytes(H, m->ks_q)));
-            CK(m, pack(w->o[l], H, m->qd, Ly.o_p, 0, m->ks_q));
-            CK(m, dalloc(m, &Ly.gu_p, q4_bytes(2 * I, m->ks_h)));
-            CK(m, pack(w->gate[l], I, H, Ly.gu_p, 0, m->ks_h));
-            CK(m, pack(w->up[l], I, H, Ly.gu_p, I / 16, m->ks_h));
-            CK(m, dalloc(m, &Ly.down_p, q4_bytes(H, m->ks_i)));
-            CK(m, pack(w->down[l], H, I, Ly.down_p, 0, m->ks_i));
+            CK(m, dalloc(m, &Ly.qkv_p, q4_bytes(m->L_qkv)));
+            CK(m, pack(w->q[l], m->qd, H, Ly.qkv_p, 0, m->L_qkv));
+            CK(m, pack(w->k[l], m->kd, H, Ly.qkv_p, m->qd / 16, m->L_qkv));
+            CK(m, pack(w->v[l], m->kd, H, Ly.qkv_p, (m->qd + m->kd) / 16, m->L_qkv));
+            CK(m, dalloc(m, &Ly.o_p, q4_bytes(m->L_o)));
+            CK(m, pack(w->o[l], H, m->qd, Ly.o_p, 0, m->L_o));
+            CK(m, dalloc(m, &Ly.gu_p, q4_bytes(m->L_gu)));
+            CK(m, pack(w->gate[l], I, H, Ly.gu_p, 0, m->L_gu));
+            CK(m, pack(w->up[l], I, H, Ly.gu_p, I / 16, m->L_gu));
+            CK(m, dalloc(m, &Ly.down_p, q4_bytes(m->L_down)));
+            CK(m, pack(w->down[l], H, I, Ly.down_p, 0, m->L_down));
         } else {
             CK(m, dalloc(m, &Ly.qkv_f, (size_t)m->qkv_w * H));
             CK(m, copy_f32(m, Ly.qkv_f, w->q[l], (size_t)m->qd * H, on_dev));
@@ -415,13 +469,30 @@ double f32_bytes_of(int N, int K, int T, bool accumulate) {
     return (double)N * K * 4 + (double)T * K * 4 + (double)T * N * 4 * (accumulate ? 2 : 1);
 }
 
-int apply(dflash_model* m, const uint8_t* packed, const float* f32w, int tile0, int N, int K, int ksteps,
+// A 4-bit matmul on int8 codes: the streaming kernel for up to 16 rows (it
+// ADDS into y, which an earlier kernel cleared or which holds the residual),
+// the general one beyond.
+int q4_mm(dflash_model* m, const uint8_t* packed, Q4Layout L, int tile0, int N, int K, QAct x, int T, float* y,
+          int ldy, bool accumulate, cudaStream_t st) {
+    if (T <= 16) {
+        KL(m, "q4_stream", 1, q4_bytes_of(N, K, T, true), st,
+           q4_stream(packed, L, tile0, N, x, T, y, ldy, m->num_sms, m->err_dev, st));
+    } else {
+        KL(m, "q4_gemm", 1, q4_bytes_of(N, K, T, accumulate), st,
+           q4_gemm(packed, L, tile0, N, x, T, y, ldy, accumulate, m->num_sms, st));
+    }
+    return 0;
+}
+
+// Apply one matrix to the block's rows.  Quantised format: the int8 codes in
+// m->xq / m->xs.  Up to 16 rows take the streaming kernel, which ADDS into y:
+// a fresh output must have been cleared by an earlier kernel (the zeroing
+// side duty of the row kernel before it).  f32 format: the f32 rows `xf`.
+int apply(dflash_model* m, const uint8_t* packed, const float* f32w, Q4Layout L, int tile0, int N, int K,
           const float* xf, int ldxf, int T, float* y, int ldy, bool accumulate, int ldq, cudaStream_t st) {
     if (m->g.quant == DFLASH_QUANT_Q4G32) {
-        QAct x{P<__half>(m->xq), P<float>(m->xs), ldq};
-        KL(m, "q4_gemm", 1, q4_bytes_of(N, K, T, accumulate), st,
-           q4_gemm(packed, tile0, N, ksteps, x, T, y, ldy, accumulate, m->num_sms, st));
-        return 0;
+        QAct x{P<int8_t>(m->xq), P<float>(m->xs), ldq};
+        return q4_mm(m, packed, L, tile0, N, K, x, T, y, ldy, accumulate, st);
     }
     KL(m, "linear_f32", 1, f32_bytes_of(N, K, T, accumulate), st,
        linear_f32(f32w, N, K, xf, ldxf, T, y, ldy, accumulate, st));
@@ -434,25 +505,25 @@ int apply(dflash_model* m, const uint8_t* packed, const float* f32w, int tile0, 
 // into the device pointer it is given), its codes and scales; and if a
 // forced decision is queued, replace the codes and scales with it.
 template <class F>
-int trace_site(dflash_model* m, cudaStream_t st, int rows, int cols, __half* codes, int ld, float* scales,
+int trace_site(dflash_model* m, cudaStream_t st, int rows, int cols, int8_t* codes, int ld, float* scales,
                F values_fn) {
     if (!m->tracing) return 0;
-    CK(m, ensure(m->trace_buf, (size_t)rows * cols * sizeof(float)));
+    CK(m, ensure_m(m, m->trace_buf, (size_t)rows * cols * sizeof(float)));
     CK(m, values_fn(P<float>(m->trace_buf)));
     dflash_model::Site site;
     site.rows = rows;
     site.cols = cols;
     site.values.resize((size_t)rows * cols);
     site.scales.resize(rows);
-    std::vector<__half> hc((size_t)rows * ld);
+    std::vector<int8_t> hc((size_t)rows * ld);
     CK(m, cudaMemcpyAsync(site.values.data(), m->trace_buf.p, site.values.size() * sizeof(float),
                           cudaMemcpyDeviceToHost, st));
-    CK(m, cudaMemcpyAsync(hc.data(), codes, hc.size() * sizeof(__half), cudaMemcpyDeviceToHost, st));
+    CK(m, cudaMemcpyAsync(hc.data(), codes, hc.size(), cudaMemcpyDeviceToHost, st));
     CK(m, cudaMemcpyAsync(site.scales.data(), scales, rows * sizeof(float), cudaMemcpyDeviceToHost, st));
     CK(m, cudaStreamSynchronize(st));
     site.codes.resize((size_t)rows * cols);
     for (int r = 0; r < rows; ++r)
-        for (int c = 0; c < cols; ++c) site.codes[(size_t)r * cols + c] = (int8_t)__half2float(hc[(size_t)r * ld + c]);
+        for (int c = 0; c < cols; ++c) site.codes[(size_t)r * cols + c] = hc[(size_t)r * ld + c];
     m->trace.push_back(std::move(site));
     if (m->forced_next < m->forced.size()) {
         const dflash_model::Site& f = m->forced[m->forced_next++];
@@ -461,8 +532,8 @@ int trace_site(dflash_model* m, cudaStream_t st, int rows, int cols, __half* cod
                                                  std::to_string(f.rows) + "x" + std::to_string(f.cols) + ", the site is " +
                                                  std::to_string(rows) + "x" + std::to_string(cols));
         for (int r = 0; r < rows; ++r)
-            for (int c = 0; c < cols; ++c) hc[(size_t)r * ld + c] = __float2half((float)f.codes[(size_t)r * cols + c]);
-        CK(m, cudaMemcpyAsync(codes, hc.data(), hc.size() * sizeof(__half), cudaMemcpyHostToDevice, st));
+            for (int c = 0; c < cols; ++c) hc[(size_t)r * ld + c] = f.codes[(size_t)r * cols + c];
+        CK(m, cudaMemcpyAsync(codes, hc.data(), hc.size(), cudaMemcpyHostToDevice, st));
         CK(m, cudaMemcpyAsync(scales, f.scales.data(), rows * sizeof(float), cudaMemcpyHostToDevice, st));
         CK(m, cudaStreamSynchronize(st));
     }
@@ -475,9 +546,51 @@ int trace_site(dflash_model* m, cudaStream_t st, int rows, int cols, __half* cod
         if (rc__) return rc__;     \
     } while (0)
 
+// Run `enqueue(stream)` (a fixed kernel sequence) on `st`: replayed from a
+// graph captured once per key, or directly when graphs are off (profiling,
+// tracing, or a stream capture of the caller's own in progress).
+template <class F>
+int run_enqueue(dflash_model* m, const std::vector<int64_t>& key, cudaStream_t st, F enqueue) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (!m->use_graphs || m->profiling || m->tracing || cudaStreamIsCapturing(st, &cs) != cudaSuccess ||
+        cs != cudaStreamCaptureStatusNone)
+        return enqueue(st);
+    for (auto& e : m->graphs)
+        if (e.key == key) {
+            CK(m, cudaGraphLaunch(e.exec, st));
+            m->launches += e.kernels;
+            return DFLASH_OK;
+        }
+    if (!m->cap_stream) CK(m, cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking));
+    const int64_t before = m->launches;
+    CK(m, cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeThreadLocal));
+    int rc = enqueue(m->cap_stream);
+    cudaGraph_t graph = nullptr;
+    cudaError_t e2 = cudaStreamEndCapture(m->cap_stream, &graph);
+    const int64_t kernels = m->launches - before;
+    m->launches = before;
+    if (rc != DFLASH_OK) {
+        if (graph) cudaGraphDestroy(graph);
+        return rc;
+    }
+    CK(m, e2);
+    cudaGraphExec_t exec = nullptr;
+    cudaError_t e3 = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    CK(m, e3);
+    if (m->graphs.size() >= 16) {
+        cudaGraphExecDestroy(m->graphs.front().exec);
+        m->graphs.erase(m->graphs.begin());
+    }
+    m->graphs.push_back(dflash_model::GraphEntry{key, exec, kernels});
+    CK(m, cudaGraphLaunch(exec, st));
+    m->launches += kernels;
+    return DFLASH_OK;
+}
+
 // Project `n` context rows (device taps) at positions pos0.. into the store.
-int append_rows(dflash_model* m, dflash_seq* s, const float* taps_dev, int64_t n, int64_t pos0, int64_t idx0,
-                cudaStream_t st) {
+// {pos0, idx0} of the rows are in m->a_pos (device).
+int append_rows(dflash_model* m, dflash_seq* s, const float* taps_dev, int64_t n, cudaStream_t st) {
     const dflash_geometry& g = m->g;
     const int H = g.hidden;
     const bool quant = g.quant == DFLASH_QUANT_Q4G32;
@@ -486,25 +599,26 @@ int append_rows(dflash_model* m, dflash_seq* s, const float* taps_dev, int64_t n
     float* t = P<float>(m->a_t);
     float* kv = P<float>(m->a_kv);
     if (quant) {
-        // taps -> int8 rows; t = FC . Q(taps); x = Q(rms(t, hidden_norm)); kv = [Wk;Wv]_all . x
+        // taps -> int8 rows (t cleared on the side); t = FC . Q(taps);
+        // x = Q(rms(t, hidden_norm)) (kv cleared on the side); kv = [Wk;Wv]_all . x
+        int8_t* codes = P<int8_t>(m->a_codes);
+        float* sc = P<float>(m->a_scale);
         KL(m, "rms_quant", 1, (double)rows * m->tap_w * 5, st,
-           rms_rows(taps_dev, m->tap_w, ident, rows, m->tap_w, nullptr, g.eps, nullptr, 0, P<__half>(m->a_codes),
-                    P<float>(m->a_scale), m->tap_w, st));
-        TRACE(trace_site(m, st, rows, m->tap_w, P<__half>(m->a_codes), m->tap_w, P<float>(m->a_scale), [&](float* v) {
+           rms_rows(taps_dev, m->tap_w, ident, rows, m->tap_w, nullptr, g.eps, nullptr, 0, codes, sc, m->tap_w, st, t,
+                    (int64_t)rows * H));
+        TRACE(trace_site(m, st, rows, m->tap_w, codes, m->tap_w, sc, [&](float* v) {
             return rms_rows(taps_dev, m->tap_w, ident, rows, m->tap_w, nullptr, g.eps, v, m->tap_w, nullptr, nullptr, 0, st);
         }));
-        QAct xt{P<__half>(m->a_codes), P<float>(m->a_scale), m->tap_w};
-        KL(m, "q4_gemm", 1, q4_bytes_of(H, m->tap_w, rows, false), st,
-           q4_gemm(m->fc_p, 0, H, m->ks_tap, xt, rows, t, H, false, m->num_sms, st));
+        QAct xt{codes, sc, m->tap_w};
+        APPLY(q4_mm(m, m->fc_p, m->L_fc, 0, H, m->tap_w, xt, rows, t, H, false, st));
         KL(m, "rms_quant", 1, (double)rows * H * 5, st,
-           rms_rows(t, H, ident, rows, H, m->hidden_norm, g.eps, nullptr, 0, P<__half>(m->a_codes),
-                    P<float>(m->a_scale), H, st));
-        TRACE(trace_site(m, st, rows, H, P<__half>(m->a_codes), H, P<float>(m->a_scale), [&](float* v) {
+           rms_rows(t, H, ident, rows, H, m->hidden_norm, g.eps, nullptr, 0, codes, sc, H, st, kv,
+                    (int64_t)rows * m->kvctx_w));
+        TRACE(trace_site(m, st, rows, H, codes, H, sc, [&](float* v) {
             return rms_rows(t, H, ident, rows, H, m->hidden_norm, g.eps, v, H, nullptr, nullptr, 0, st);
         }));
-        QAct xh{P<__half>(m->a_codes), P<float>(m->a_scale), H};
-        KL(m, "q4_gemm", 1, q4_bytes_of(m->kvctx_w, H, rows, false), st,
-           q4_gemm(m->kvctx_p, 0, m->kvctx_w, m->ks_h, xh, rows, kv, m->kvctx_w, false, m->num_sms, st));
+        QAct xh{codes, sc, H};
+        APPLY(q4_mm(m, m->kvctx_p, m->L_kvctx, 0, m->kvctx_w, H, xh, rows, kv, m->kvctx_w, false, st));
     } else {
         KL(m, "linear_f32", 1, f32_bytes_of(H, m->tap_w, rows, false), st,
            linear_f32(m->fc_f, H, m->tap_w, taps_dev, m->tap_w, rows, t, H, false, st));
@@ -515,19 +629,20 @@ int append_rows(dflash_model* m, dflash_seq* s, const float* taps_dev, int64_t n
            linear_f32(m->kvctx_f, m->kvctx_w, H, tn, H, rows, kv, m->kvctx_w, false, st));
     }
     KL(m, "kv_append", 1, (double)rows * m->kvctx_w * 8, st,
-       kv_append(kv, rows, g.layers, g.kv_heads, g.head_dim, m->k_norm_dev, m->inv_freq, g.eps, pos0, idx0, s->k_dev,
-                 s->v_dev, s->cap, st));
+       kv_append(kv, rows, g.layers, g.kv_heads, g.head_dim, m->k_norm_dev, m->inv_freq, g.eps, P<int64_t>(m->a_pos),
+                 s->k_dev, s->v_dev, s->cap, st));
     return DFLASH_OK;
 }
 
 int ensure_append_scratch(dflash_model* m, int64_t rows) {
     const bool quant = m->g.quant == DFLASH_QUANT_Q4G32;
     const size_t r = (size_t)rows;
-    CK(m, ensure(m->a_taps, r * m->tap_w * sizeof(float)));
-    CK(m, ensure(m->a_codes, quant ? r * m->tap_w * sizeof(__half) : r * m->g.hidden * sizeof(float)));
-    CK(m, ensure(m->a_scale, r * sizeof(float)));
-    CK(m, ensure(m->a_t, r * m->g.hidden * sizeof(float)));
-    CK(m, ensure(m->a_kv, r * m->kvctx_w * sizeof(float)));
+    CK(m, ensure_m(m, m->a_taps, r * m->tap_w * sizeof(float)));
+    CK(m, ensure_m(m, m->a_codes, quant ? r * m->tap_w : r * m->g.hidden * sizeof(float)));
+    CK(m, ensure_m(m, m->a_scale, r * sizeof(float)));
+    CK(m, ensure_m(m, m->a_t, r * m->g.hidden * sizeof(float)));
+    CK(m, ensure_m(m, m->a_kv, r * m->kvctx_w * sizeof(float)));
+    CK(m, ensure_m(m, m->a_pos, 2 * sizeof(int64_t)));
     return 0;
 }
 
@@ -574,6 +689,9 @@ void dflash_free(dflash_model* m) {
         cudaEventDestroy(r.e1);
     }
     for (cudaEvent_t e : m->ev_pool) cudaEventDestroy(e);
+    if (m->err_host) cudaFreeHost(m->err_host);
+    clear_graphs(m);
+    if (m->cap_stream) cudaStreamDestroy(m->cap_stream);
     for (void* p : m->owned) cudaFree(p);
     for (DevBuf* b : {&m->h, &m->xq, &m->xs, &m->qkv, &m->y, &m->gu, &m->logits, &m->keys, &m->toks, &m->part,
                       &m->anchors, &m->pos0, &m->aseqs, &m->a_taps, &m->a_codes, &m->a_scale, &m->a_t, &m->a_kv})
@@ -687,12 +805,20 @@ int dflash_ctx_append(dflash_model* m, dflash_seq* s, int64_t pos, const float* 
             CK(m, cudaMemcpyAsync(m->a_taps.p, src, (size_t)n * m->tap_w * sizeof(float), cudaMemcpyHostToDevice, st));
             src = P<float>(m->a_taps);
         }
-        rc = append_rows(m, s, src, n, first + len + r0, len + r0, st);
+        const int64_t pos2[2] = {first + len + r0, len + r0};
+        CK(m, cudaMemcpyAsync(m->a_pos.p, pos2, sizeof(pos2), cudaMemcpyHostToDevice, st));
+        const std::vector<int64_t> key = {1, (int64_t)(intptr_t)s, (int64_t)(intptr_t)s->k_dev, n,
+                                          (int64_t)(intptr_t)src};
+        rc = run_enqueue(m, key, st, [&](cudaStream_t q) { return append_rows(m, s, src, n, q); });
         if (rc) return rc;
         if (!taps_on_device && r0 + chunk < n_rows) CK(m, cudaStreamSynchronize(st));  // staging reused
     }
-    if (!taps_on_device) CK(m, cudaStreamSynchronize(st));
     s->len = len + n_rows;
+    if (!taps_on_device) {
+        CK(m, cudaMemcpyAsync(m->err_host, m->err_dev, sizeof(int), cudaMemcpyDeviceToHost, st));
+        CK(m, cudaStreamSynchronize(st));
+        if (*m->err_host) return device_wait_expired(m);
+    }
     return DFLASH_OK;
 }
 
@@ -721,37 +847,37 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
     // context rows each sequence reads: [first, min(anchor, first + len))
     std::vector<AttnSeq> as(n_seqs);
     std::vector<int64_t> p0(anchor_pos, anchor_pos + n_seqs);
-    int max_ctx = 0;
+    int max_ctx = 0;  // the launch is planned for the largest capacity, so that it stays as contexts grow
     for (int s = 0; s < n_seqs; ++s) {
         const dflash_seq* q = seqs[s];
         const int64_t hi = std::max(std::min(anchor_pos[s], q->first + q->len), q->first);
         as[s].cap = q->cap;
         as[s].lo = 0;
         as[s].n = (int)(hi - q->first);
-        max_ctx = std::max(max_ctx, as[s].n);
+        max_ctx = (int)std::max<int64_t>(max_ctx, q->cap);
     }
     double attn_bytes = (double)R * m->qkv_w * 4 + (double)R * m->qd * 4;
     for (int s = 0; s < n_seqs; ++s) attn_bytes += (double)as[s].n * m->kd * 8;
     const int64_t part_floats = attn_scratch_floats(n_seqs, B, max_ctx, g.heads, g.kv_heads, hd, m->num_sms);
-    CK(m, ensure(m->h, (size_t)R * H * sizeof(float)));
-    CK(m, ensure(m->xq, (size_t)R * (quant ? maxK * sizeof(__half) : maxK * sizeof(float))));
-    CK(m, ensure(m->xs, (size_t)R * sizeof(float)));
-    CK(m, ensure(m->qkv, (size_t)R * m->qkv_w * sizeof(float)));
-    CK(m, ensure(m->y, (size_t)R * m->qd * sizeof(float)));
-    CK(m, ensure(m->gu, (size_t)R * 2 * I * sizeof(float)));
-    CK(m, ensure(m->part, (size_t)part_floats * sizeof(float)));
-    CK(m, ensure(m->keys, (size_t)D * sizeof(unsigned long long)));
-    CK(m, ensure(m->toks, (size_t)D * sizeof(uint32_t)));
-    CK(m, ensure(m->anchors, (size_t)n_seqs * sizeof(uint32_t)));
-    CK(m, ensure(m->pos0, (size_t)n_seqs * sizeof(int64_t)));
-    CK(m, ensure(m->aseqs, (size_t)g.layers * n_seqs * sizeof(AttnSeq)));
+    CK(m, ensure_m(m, m->h, (size_t)R * H * sizeof(float)));
+    CK(m, ensure_m(m, m->xq, (size_t)R * (quant ? maxK : maxK * sizeof(float))));
+    CK(m, ensure_m(m, m->xs, (size_t)R * sizeof(float)));
+    CK(m, ensure_m(m, m->qkv, (size_t)R * m->qkv_w * sizeof(float)));
+    CK(m, ensure_m(m, m->y, (size_t)R * m->qd * sizeof(float)));
+    CK(m, ensure_m(m, m->gu, (size_t)R * 2 * I * sizeof(float)));
+    CK(m, ensure_m(m, m->part, (size_t)part_floats * sizeof(float)));
+    CK(m, ensure_m(m, m->keys, (size_t)D * sizeof(unsigned long long)));
+    CK(m, ensure_m(m, m->toks, (size_t)D * sizeof(uint32_t)));
+    CK(m, ensure_m(m, m->anchors, (size_t)n_seqs * sizeof(uint32_t)));
+    CK(m, ensure_m(m, m->pos0, (size_t)n_seqs * sizeof(int64_t)));
+    CK(m, ensure_m(m, m->aseqs, (size_t)g.layers * n_seqs * sizeof(AttnSeq)));
     float* logit_out = io_on_device ? logits : nullptr;
     if (!io_on_device && logits) {
-        CK(m, ensure(m->logits, (size_t)D * g.vocab * sizeof(float)));
+        CK(m, ensure_m(m, m->logits, (size_t)D * g.vocab * sizeof(float)));
         logit_out = P<float>(m->logits);
     }
     if (!quant && !logit_out) {  // the f32 head needs its logits for the argmax
-        CK(m, ensure(m->logits, (size_t)D * g.vocab * sizeof(float)));
+        CK(m, ensure_m(m, m->logits, (size_t)D * g.vocab * sizeof(float)));
         logit_out = P<float>(m->logits);
     }
     // per-call vectors (pageable sources: the driver copies them before returning)
@@ -772,12 +898,13 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
         }
     CK(m, cudaMemcpyAsync(m->aseqs.p, as_all.data(), as_all.size() * sizeof(AttnSeq), cudaMemcpyHostToDevice, st));
 
+    auto enqueue = [&](cudaStream_t st) -> int {
     float* h = P<float>(m->h);
     float* qkv = P<float>(m->qkv);
     float* y = P<float>(m->y);
     float* gu = P<float>(m->gu);
     float* xf = P<float>(m->xq);  // the f32 path's normed rows
-    __half* xq = P<__half>(m->xq);
+    int8_t* xq = P<int8_t>(m->xq);
     float* xs = P<float>(m->xs);
     RowMap ident{1, 1, 0};
     const float scale = 1.0f / sqrtf((float)hd);
@@ -787,14 +914,15 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
         const Layer& Ly = m->layers[l];
         // attention half: x = rms(h, in_norm); q, k, v; norms and rotation; attention; h += O y
         if (quant) {
-            KL(m, "rms_quant", 1, (double)R * H * 5, st, rms_rows(h, H, ident, R, H, Ly.in_norm, g.eps, nullptr, 0, xq, xs, maxK, st));
+            KL(m, "rms_quant", 1, (double)R * H * 5, st,
+               rms_rows(h, H, ident, R, H, Ly.in_norm, g.eps, nullptr, 0, xq, xs, maxK, st, qkv, (int64_t)R * m->qkv_w));
             TRACE(trace_site(m, st, R, H, xq, maxK, xs, [&](float* v) {
                 return rms_rows(h, H, ident, R, H, Ly.in_norm, g.eps, v, H, nullptr, nullptr, 0, st);
             }));
-            APPLY(apply(m, Ly.qkv_p, nullptr, 0, m->qkv_w, H, m->ks_h, nullptr, 0, R, qkv, m->qkv_w, false, maxK, st));
+            APPLY(apply(m, Ly.qkv_p, nullptr, m->L_qkv, 0, m->qkv_w, H, nullptr, 0, R, qkv, m->qkv_w, false, maxK, st));
         } else {
             KL(m, "rms_f32", 1, (double)R * H * 8, st, rms_rows(h, H, ident, R, H, Ly.in_norm, g.eps, xf, maxK, nullptr, nullptr, 0, st));
-            APPLY(apply(m, nullptr, Ly.qkv_f, 0, m->qkv_w, H, 0, xf, maxK, R, qkv, m->qkv_w, false, 0, st));
+            APPLY(apply(m, nullptr, Ly.qkv_f, Q4Layout{}, 0, m->qkv_w, H, xf, maxK, R, qkv, m->qkv_w, false, 0, st));
         }
         KL(m, "qk_norm_rope", 1, (double)R * (m->qd + m->kd) * 8, st,
            qk_norm_rope(qkv, m->qkv_w, R, B, P<int64_t>(m->pos0), g.heads, g.kv_heads, hd, Ly.q_norm, Ly.k_norm,
@@ -808,27 +936,28 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
             TRACE(trace_site(m, st, R, m->qd, xq, maxK, xs, [&](float* v) {
                 return rms_rows(y, m->qd, ident, R, m->qd, nullptr, g.eps, v, m->qd, nullptr, nullptr, 0, st);
             }));
-            APPLY(apply(m, Ly.o_p, nullptr, 0, H, m->qd, m->ks_q, nullptr, 0, R, h, H, true, maxK, st));
+            APPLY(apply(m, Ly.o_p, nullptr, m->L_o, 0, H, m->qd, nullptr, 0, R, h, H, true, maxK, st));
         } else {
-            APPLY(apply(m, nullptr, Ly.o_f, 0, H, m->qd, 0, y, m->qd, R, h, H, true, 0, st));
+            APPLY(apply(m, nullptr, Ly.o_f, Q4Layout{}, 0, H, m->qd, y, m->qd, R, h, H, true, 0, st));
         }
         // MLP half: x = rms(h, post_norm); h += down (silu(gate x) * up x)
         if (quant) {
-            KL(m, "rms_quant", 1, (double)R * H * 5, st, rms_rows(h, H, ident, R, H, Ly.post_norm, g.eps, nullptr, 0, xq, xs, maxK, st));
+            KL(m, "rms_quant", 1, (double)R * H * 5, st,
+               rms_rows(h, H, ident, R, H, Ly.post_norm, g.eps, nullptr, 0, xq, xs, maxK, st, gu, (int64_t)R * 2 * I));
             TRACE(trace_site(m, st, R, H, xq, maxK, xs, [&](float* v) {
                 return rms_rows(h, H, ident, R, H, Ly.post_norm, g.eps, v, H, nullptr, nullptr, 0, st);
             }));
-            APPLY(apply(m, Ly.gu_p, nullptr, 0, 2 * I, H, m->ks_h, nullptr, 0, R, gu, 2 * I, false, maxK, st));
+            APPLY(apply(m, Ly.gu_p, nullptr, m->L_gu, 0, 2 * I, H, nullptr, 0, R, gu, 2 * I, false, maxK, st));
             KL(m, "silu_quant", 1, (double)R * I * 9, st, silu_mul(gu, 2 * I, R, I, nullptr, 0, xq, xs, maxK, st));
             TRACE(trace_site(m, st, R, I, xq, maxK, xs, [&](float* v) {
                 return silu_mul(gu, 2 * I, R, I, v, I, nullptr, nullptr, 0, st);
             }));
-            APPLY(apply(m, Ly.down_p, nullptr, 0, H, I, m->ks_i, nullptr, 0, R, h, H, true, maxK, st));
+            APPLY(apply(m, Ly.down_p, nullptr, m->L_down, 0, H, I, nullptr, 0, R, h, H, true, maxK, st));
         } else {
             KL(m, "rms_f32", 1, (double)R * H * 8, st, rms_rows(h, H, ident, R, H, Ly.post_norm, g.eps, xf, maxK, nullptr, nullptr, 0, st));
-            APPLY(apply(m, nullptr, Ly.gu_f, 0, 2 * I, H, 0, xf, maxK, R, gu, 2 * I, false, 0, st));
+            APPLY(apply(m, nullptr, Ly.gu_f, Q4Layout{}, 0, 2 * I, H, xf, maxK, R, gu, 2 * I, false, 0, st));
             KL(m, "silu_f32", 1, (double)R * I * 12, st, silu_mul(gu, 2 * I, R, I, xf, maxK, nullptr, nullptr, 0, st));
-            APPLY(apply(m, nullptr, Ly.down_f, 0, H, I, 0, xf, maxK, R, h, H, true, 0, st));
+            APPLY(apply(m, nullptr, Ly.down_f, Q4Layout{}, 0, H, I, xf, maxK, R, h, H, true, 0, st));
         }
     }
     // head over the rows after each anchor: row i of the output is row
@@ -837,28 +966,40 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
     unsigned long long* keys = P<unsigned long long>(m->keys);
     uint32_t* tok_out = (io_on_device && draft_tok) ? draft_tok : P<uint32_t>(m->toks);
     if (quant) {
-        KL(m, "rms_quant", 1, (double)D * H * 5, st, rms_rows(h, H, drafts, D, H, m->norm, g.eps, nullptr, 0, xq, xs, maxK, st));
+        KL(m, "rms_quant", 1, (double)D * H * 5, st,
+           rms_rows(h, H, drafts, D, H, m->norm, g.eps, nullptr, 0, xq, xs, maxK, st, reinterpret_cast<float*>(keys),
+                    (int64_t)D * 2));
         TRACE(trace_site(m, st, D, H, xq, maxK, xs, [&](float* v) {
             return rms_rows(h, H, drafts, D, H, m->norm, g.eps, v, H, nullptr, nullptr, 0, st);
         }));
-        CK(m, cudaMemsetAsync(keys, 0, (size_t)D * sizeof(unsigned long long), st));
         QAct xh{xq, xs, maxK};
         const double hb = (double)g.vocab * H + (double)g.vocab * 4 + (double)D * H + (logit_out ? (double)D * g.vocab * 4 : 0.0);
-        KL(m, "head_i8", 1, hb, st,
-           head_i8(m->head_p, m->head_scale, g.vocab, H / kI8KStep, xh, D, logit_out, g.vocab, keys, m->num_sms, st));
+        KL(m, "head_stream", 1, hb, st,
+           head_stream(m->head_p, m->head_scale, g.vocab, H / kI8KStep, xh, D, logit_out, g.vocab, keys, m->num_sms,
+                       m->err_dev, st));
     } else {
-        KL(m, "rms_f32", 1, (double)D * H * 8, st, rms_rows(h, H, drafts, D, H, m->norm, g.eps, xf, maxK, nullptr, nullptr, 0, st));
+        KL(m, "rms_f32", 1, (double)D * H * 8, st, rms_rows(h, H, drafts, D, H, m->norm, g.eps, xf, maxK, nullptr, nullptr, 0, st,
+                                                         reinterpret_cast<float*>(keys), (int64_t)D * 2));
         KL(m, "linear_f32", 1, f32_bytes_of(g.vocab, H, D, false), st,
            linear_f32(m->head_f, g.vocab, H, xf, maxK, D, logit_out, g.vocab, false, st));
         KL(m, "argmax_rows", 1, (double)D * g.vocab * 4, st, argmax_rows(logit_out, g.vocab, g.vocab, D, keys, st));
     }
     KL(m, "keys_to_tokens", 1, (double)D * 12, st, keys_to_tokens(keys, D, tok_out, st));
+    return DFLASH_OK;
+    };
+    uint32_t* tok_out = (io_on_device && draft_tok) ? draft_tok : P<uint32_t>(m->toks);
+    const std::vector<int64_t> key = {2, n_seqs, B, max_ctx, (int64_t)(intptr_t)logit_out, (int64_t)(intptr_t)tok_out,
+                                      (int64_t)(intptr_t)anchors_dev};
+    rc = run_enqueue(m, key, st, enqueue);
+    if (rc) return rc;
     if (!io_on_device) {
         if (logits)
             CK(m, cudaMemcpyAsync(logits, logit_out, (size_t)D * g.vocab * sizeof(float), cudaMemcpyDeviceToHost, st));
         if (draft_tok)
             CK(m, cudaMemcpyAsync(draft_tok, tok_out, (size_t)D * sizeof(uint32_t), cudaMemcpyDeviceToHost, st));
+        CK(m, cudaMemcpyAsync(m->err_host, m->err_dev, sizeof(int), cudaMemcpyDeviceToHost, st));
         CK(m, cudaStreamSynchronize(st));
+        if (*m->err_host) return device_wait_expired(m);
     }
     return DFLASH_OK;
 }
@@ -874,6 +1015,8 @@ int attention_views(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, in
     if (!seqs || !anchor_pos || !qkv || !y || n_seqs < 1 || layer < 0 || layer >= g.layers)
         return set_err(m, DFLASH_EINVAL, "attention: null pointer, n_seqs < 1 or bad layer");
     if (block_len < 2 || block_len > g.block) return set_err(m, DFLASH_ERANGE, "attention: block_len outside [2, block]");
+    if (reinterpret_cast<uintptr_t>(qkv) % 16 != 0)
+        return set_err(m, DFLASH_EINVAL, "attention: qkv must be 16-byte aligned");
     views.assign(n_seqs, AttnSeq{});
     *max_ctx = 0;
     for (int s = 0; s < n_seqs; ++s) {
@@ -905,8 +1048,8 @@ int dflash_debug_attention(dflash_model* m, dflash_seq* const* seqs, int32_t n_s
     cudaStream_t st = (cudaStream_t)stream;
     const int64_t part_floats =
         attn_scratch_floats(n_seqs, block_len, max_ctx, g.heads, g.kv_heads, g.head_dim, m->num_sms);
-    CK(m, ensure(m->part, (size_t)part_floats * sizeof(float)));
-    CK(m, ensure(m->aseqs, (size_t)n_seqs * sizeof(AttnSeq)));
+    CK(m, ensure_m(m, m->part, (size_t)part_floats * sizeof(float)));
+    CK(m, ensure_m(m, m->aseqs, (size_t)n_seqs * sizeof(AttnSeq)));
     CK(m, cudaMemcpyAsync(m->aseqs.p, views.data(), views.size() * sizeof(AttnSeq), cudaMemcpyHostToDevice, st));
     KL(m, "attention", 2, 0.0, st,
        attention(qkv, m->qkv_w, n_seqs, block_len, P<AttnSeq>(m->aseqs), max_ctx, g.heads, g.kv_heads, g.head_dim,
@@ -1013,7 +1156,7 @@ int dflash_debug_q4_codes(dflash_model* m, int32_t id, int8_t* codes, uint16_t* 
     uint16_t* ds = nullptr;
     CK(m, cudaMalloc(&dc, (size_t)v.N * v.K));
     CK(m, cudaMalloc(&ds, (size_t)v.N * (v.K / 32) * 2));
-    int e = q4_unpack(v.packed, v.tile0, v.N, v.K, v.ksteps, dc, ds, st);
+    int e = q4_unpack(v.packed, v.L, v.tile0, v.N, v.K, dc, ds, st);
     if (!e) e = (int)cudaMemcpyAsync(codes, dc, (size_t)v.N * v.K, cudaMemcpyDeviceToHost, st);
     if (!e) e = (int)cudaMemcpyAsync(scales, ds, (size_t)v.N * (v.K / 32) * 2, cudaMemcpyDeviceToHost, st);
     if (!e) e = (int)cudaStreamSynchronize(st);
@@ -1048,26 +1191,26 @@ int dflash_debug_q4_groupsums(dflash_model* m, int32_t id, const int8_t* x, int3
     MatView v = mat_view(m, id);
     if (!v.packed) return set_err(m, DFLASH_EINVAL, "bad matrix id");
     cudaStream_t st = (cudaStream_t)stream;
-    const int ldk = v.ksteps * kQ4KStep;
-    std::vector<__half> hx((size_t)rows * ldk, __float2half(0.f));
+    const int ldk = v.L.ksteps * kQ4KStep;
+    std::vector<int8_t> hx((size_t)rows * ldk, 0);
     for (int r = 0; r < rows; ++r)
         for (int k = 0; k < v.K; ++k) {
             int xv = x[(size_t)r * v.K + k];
             if (xv < -127) return set_err(m, DFLASH_EINVAL, "activation code -128");
-            hx[(size_t)r * ldk + k] = __float2half((float)xv);
+            hx[(size_t)r * ldk + k] = (int8_t)xv;
         }
     std::vector<float> ones(rows, 1.f);
-    __half* dx = nullptr;
+    int8_t* dx = nullptr;
     float* dsc = nullptr;
     int32_t* dout = nullptr;
     const size_t outn = (size_t)rows * v.N * (v.K / 32);
-    CK(m, cudaMalloc(&dx, hx.size() * sizeof(__half)));
+    CK(m, cudaMalloc(&dx, hx.size()));
     CK(m, cudaMalloc(&dsc, rows * sizeof(float)));
     CK(m, cudaMalloc(&dout, outn * sizeof(int32_t)));
-    int e = (int)cudaMemcpyAsync(dx, hx.data(), hx.size() * sizeof(__half), cudaMemcpyHostToDevice, st);
+    int e = (int)cudaMemcpyAsync(dx, hx.data(), hx.size(), cudaMemcpyHostToDevice, st);
     if (!e) e = (int)cudaMemcpyAsync(dsc, ones.data(), rows * sizeof(float), cudaMemcpyHostToDevice, st);
     QAct qa{dx, dsc, ldk};
-    if (!e) e = q4_groupsums(v.packed, v.tile0, v.N, v.ksteps, qa, rows, dout, st);
+    if (!e) e = q4_groupsums(v.packed, v.L, v.tile0, v.N, qa, rows, dout, st);
     if (!e) e = (int)cudaMemcpyAsync(out, dout, outn * sizeof(int32_t), cudaMemcpyDeviceToHost, st);
     if (!e) e = (int)cudaStreamSynchronize(st);
     cudaFree(dx);

@@ -12,7 +12,38 @@ namespace dflash {
 constexpr int kSMs = 152;  // GB300: 2 dies x 76 SMs (grids are sized from the device's count at run time)
 
 // ---------------------------------------------------------------------------
-// 4-bit g32 packed layout ("q4 tile").
+// Order of the 576-byte chunks of a 4-bit matrix in memory.  Four 16-row tiles
+// form a 64-row group; a (group, k-step) "super-chunk" is the group's four
+// chunks of that k-step, 2304 contiguous bytes.  K is cut into K-blocks of KB
+// k-steps (KB the largest divisor of the k-step count not above 32, i.e. at
+// most 2048 columns), and super-chunks are stored [K-block][group][k-step in
+// block]: a contiguous slice of the matrix needs the activations of one
+// K-block only, and one group's k-steps inside a K-block are contiguous.
+// ---------------------------------------------------------------------------
+struct Q4Layout {
+    int ngroups;  // 64-row groups of the whole (fused) matrix
+    int ksteps;   // 64-column k-steps
+    int kb;       // k-steps per K-block
+};
+
+__host__ __device__ __forceinline__ int q4_kblock_steps(int ksteps) {
+    int best = 1;
+    for (int d = 1; d <= 32 && d <= ksteps; ++d)
+        if (ksteps % d == 0) best = d;
+    return best;
+}
+
+// byte offset of the chunk of tile `tile` (16-row tile of the whole matrix)
+// and k-step `ks`
+__host__ __device__ __forceinline__ int64_t q4_chunk_offset(const Q4Layout& L, int tile, int ks) {
+    const int g = tile >> 2, r = tile & 3;
+    const int kblk = ks / L.kb, ksl = ks - kblk * L.kb;
+    const int64_t sc = ((int64_t)kblk * L.ngroups + g) * L.kb + ksl;
+    return sc * (4 * 576) + r * 576;
+}
+
+// ---------------------------------------------------------------------------
+// Within a chunk ("q4 tile").
 // A matrix [N][K] (N padded to a multiple of 16, K to a multiple of 64) is cut
 // into 16-row tiles and 64-column k-steps (two 32-column quantisation
 // groups).  Chunk (tile, kstep) is 576 bytes, tile-major:
@@ -36,18 +67,96 @@ constexpr int kSMs = 152;  // GB300: 2 dies x 76 SMs (grids are sized from the d
 constexpr int kQ4Chunk = 576;
 constexpr int kQ4KStep = 64;
 
-// int8 head layout ("i8 tile"): rows padded to 16; per (tile, 32-column
-// k-step) 512 bytes, lane-major 16 bytes per lane l = 4*gq + tq:
-//   [row gq cols 8tq..8tq+3][row gq+8 cols 8tq..+3][row gq cols 8tq+4..+7][row gq+8 cols 8tq+4..+7]
-// = the m16n8k32 s8 A fragment {a0,a1,a2,a3} with k slot 4tq+{0..3} <-> column
-// 8tq+{0..3} and slot 16+4tq+{0..3} <-> column 8tq+4+{0..3}.
-constexpr int kI8Chunk = 512;
-constexpr int kI8KStep = 32;
+// int8 head layout: rows padded to 64; per (64-row group, 64-column k-step)
+// a 4096-byte super-chunk of four 1024-byte tile chunks, group-major
+// ([group][k-step][tile]).  In a tile chunk lane l = 4*gq + tq holds 32 bytes:
+// for group-half gi in {0,1} and half s in {0,1} of it, 4 bytes of row gq then
+// 4 bytes of row gq + 8, at columns 32*gi + 8*tq + 4*s + {0,1,2,3} -- the
+// m16n8k16 A fragment order of the 4-bit layout, as bytes.
+constexpr int kI8Chunk = 1024;
+constexpr int kI8Super = 4 * kI8Chunk;
+constexpr int kI8KStep = 64;
+
+// byte offset of the head code at row n, column c (K = ksteps * 64)
+__host__ __device__ __forceinline__ int64_t i8_byte_offset(int n, int c, int ksteps) {
+    const int g = n >> 6, r = (n >> 4) & 3, rr = n & 15, gq = rr & 7, up = rr >> 3;
+    const int ks = c >> 6, w = c & 63, gi = w >> 5, wc = w & 31, tq = wc >> 3, s = (wc >> 2) & 1, cc = wc & 3;
+    return (((int64_t)g * ksteps + ks) * 4 + r) * kI8Chunk + (4 * gq + tq) * 32 + (gi * 2 + s) * 8 + up * 4 + cc;
+}
+
+// Four int8 (a u32) -> two half2 of exact integers: bytes (0,1) and (2,3).
+DF_DEV void i8x4_to_half2x2(uint32_t v, uint32_t& lo, uint32_t& hi) {
+    const uint32_t u = v ^ 0x80808080u;  // offset binary: b + 128
+    uint32_t a, b;
+    asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(u), "r"(0x64646464u));
+    asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(u), "r"(0x64646464u));
+    const uint32_t k1152 = 0x64806480u;  // 1152.0h = 1024 + 128
+    __half2 ra = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<const __half2*>(&k1152));
+    __half2 rb = __hsub2(*reinterpret_cast<__half2*>(&b), *reinterpret_cast<const __half2*>(&k1152));
+    lo = *reinterpret_cast<uint32_t*>(&ra);
+    hi = *reinterpret_cast<uint32_t*>(&rb);
+}
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialisation attribute may start while its predecessor runs; it
+// reads or writes nothing the predecessor touches before pdl_wait().
+DF_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+DF_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
+// mbarrier and bulk-copy (TMA, non-tensor) helpers.
+DF_DEV uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+DF_DEV void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+DF_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+DF_DEV void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+DF_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+DF_DEV uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+// Bounded wait: gives up once `limit_ns` nanoseconds have passed, returning false.
+DF_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > limit_ns) return false;
+    }
+}
+DF_DEV void bulk_g2s(void* dst_smem, const void* src_gmem, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst_smem)),
+        "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+DF_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+DF_DEV void red_add_v4(float* gaddr, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(gaddr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
 
 DF_DEV uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
     // (a & b) | c
     uint32_t d;
-    asm volatile("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
 }
 
@@ -76,7 +185,7 @@ DF_DEV void unpack_q4_word(uint32_t w, uint32_t (&a)[4]) {
 
 // D = A(16x16 f16) * B(16x8 f16) + C, f32 accumulate (warp-level tensor-core MMA).
 DF_DEV void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1, const float (&c)[4]) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%10,%11,%12,%13};"
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
@@ -86,7 +195,7 @@ DF_DEV void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, ui
 
 // D = A(16x32 s8) * B(32x8 s8) + C, s32 accumulate.
 DF_DEV void mma_s8_16832(int (&d)[4], const uint4& a, uint32_t b0, uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};"
         : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])

@@ -16,68 +16,82 @@
 
 namespace dflash {
 
-// Block-wide sum / max over 256 threads (deterministic tree order).
+// int8 code of v under scale sx (sx > 0)
+DF_DEV int8_t code_of(float v, float sx) {
+    float q = rintf(__fdiv_rn(v, sx));
+    q = fminf(fmaxf(q, -127.f), 127.f);
+    return (int8_t)(int)q;
+}
+
+constexpr int kRowThreads = 1024;
+
+// Block-wide sum / max over kRowThreads threads.
 template <bool kMax>
-DF_DEV float block_reduce_256(float v, float* red) {
+DF_DEV float row_reduce(float v, float* red) {
     v = kMax ? warp_max(v) : warp_sum(v);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
     __syncthreads();
     if (threadIdx.x < 32) {
-        float u = threadIdx.x < 8 ? red[threadIdx.x] : (kMax ? 0.f : 0.f);
+        float u = red[threadIdx.x];
         u = kMax ? warp_max(u) : warp_sum(u);
-        if (threadIdx.x == 0) red[8] = u;
+        if (threadIdx.x == 0) red[32] = u;
     }
     __syncthreads();
-    float r = red[8];
+    float r = red[32];
     __syncthreads();
     return r;
 }
 
-// int8 code of v under scale sx (sx > 0), as an exact f16 integer
-DF_DEV __half code_of(float v, float sx) {
-    float q = rintf(__fdiv_rn(v, sx));
-    q = fminf(fmaxf(q, -127.f), 127.f);
-    return __float2half_rn(q);
+// Zero `n` floats at `p`, spread over the grid (a side duty that clears the
+// buffer a later kernel accumulates into).
+DF_DEV void zero_side(float* p, int64_t n) {
+    if (!p) return;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) p[i] = 0.f;
 }
 
-__global__ void __launch_bounds__(256) rms_rows_kernel(const float* __restrict__ src, int ld_src, RowMap map, int n,
-                                                       const float* __restrict__ w, float eps,
-                                                       float* __restrict__ out_f32, int ld_out,
-                                                       __half* __restrict__ out_codes, float* __restrict__ out_scale,
-                                                       int ld_codes) {
-    __shared__ float red[16];
+__global__ void __launch_bounds__(kRowThreads) rms_rows_kernel(const float* __restrict__ src, int ld_src, RowMap map,
+                                                               int n, const float* __restrict__ w, float eps,
+                                                               float* __restrict__ out_f32, int ld_out,
+                                                               int8_t* __restrict__ out_codes,
+                                                               float* __restrict__ out_scale, int ld_codes,
+                                                               float* zero_buf, int64_t zero_n) {
+    __shared__ float red[33];
+    pdl_trigger();
+    pdl_wait();
+    zero_side(zero_buf, zero_n);
     const int i = blockIdx.x;
     const int srow = (i / map.per) * map.stride + map.skip + (i % map.per);
     const float* x = src + (int64_t)srow * ld_src;
     float s = 1.f;
     if (w) {
         float ss = 0.f;
-        for (int c = threadIdx.x; c < n; c += 256) ss = fmaf(x[c], x[c], ss);
-        ss = block_reduce_256<false>(ss, red);
+        for (int c = threadIdx.x; c < n; c += kRowThreads) ss = fmaf(x[c], x[c], ss);
+        ss = row_reduce<false>(ss, red);
         s = 1.0f / sqrtf(ss / (float)n + eps);
     }
     if (out_f32) {
-        for (int c = threadIdx.x; c < n; c += 256) out_f32[(int64_t)i * ld_out + c] = w ? x[c] * s * w[c] : x[c];
+        for (int c = threadIdx.x; c < n; c += kRowThreads) out_f32[(int64_t)i * ld_out + c] = w ? x[c] * s * w[c] : x[c];
         return;
     }
     float amax = 0.f;
-    for (int c = threadIdx.x; c < n; c += 256) amax = fmaxf(amax, fabsf(w ? x[c] * s * w[c] : x[c]));
-    amax = block_reduce_256<true>(amax, red);
+    for (int c = threadIdx.x; c < n; c += kRowThreads) amax = fmaxf(amax, fabsf(w ? x[c] * s * w[c] : x[c]));
+    amax = row_reduce<true>(amax, red);
     const float sx = __fdiv_rn(amax, 127.0f);
-    __half* q = out_codes + (int64_t)i * ld_codes;
-    for (int c = threadIdx.x; c < n; c += 256) {
+    int8_t* q = out_codes + (int64_t)i * ld_codes;
+    for (int c = threadIdx.x; c < n; c += kRowThreads) {
         const float v = w ? x[c] * s * w[c] : x[c];
-        q[c] = sx > 0.f ? code_of(v, sx) : __float2half_rn(0.f);
+        q[c] = sx > 0.f ? code_of(v, sx) : (int8_t)0;
     }
     if (threadIdx.x == 0) out_scale[i] = sx;
 }
 
 int rms_rows(const float* src, int ld_src, RowMap map, int rows, int n, const float* w, float eps, float* out_f32,
-             int ld_out, __half* out_codes, float* out_scale, int ld_codes, cudaStream_t st) {
+             int ld_out, int8_t* out_codes, float* out_scale, int ld_codes, cudaStream_t st, float* zero_buf,
+             int64_t zero_n) {
     if (rows <= 0) return 0;
-    rms_rows_kernel<<<rows, 256, 0, st>>>(src, ld_src, map, n, w, eps, out_f32, ld_out, out_codes, out_scale,
-                                          ld_codes);
-    return (int)cudaGetLastError();
+    return (int)launch(rms_rows_kernel, dim3(rows), dim3(kRowThreads), 0, st, src, ld_src, map, n, w, eps, out_f32,
+                       ld_out, out_codes, out_scale, ld_codes, zero_buf, zero_n);
 }
 
 // A token outside [0, vocab) (only possible for anchors already on the
@@ -86,6 +100,8 @@ __global__ void embed_rows_kernel(const float* __restrict__ embed, int H, int vo
                                   const uint32_t* __restrict__ anchor_tok, int mask_token, int block_len,
                                   float* __restrict__ h) {
     const int r = blockIdx.x;
+    pdl_trigger();
+    pdl_wait();
     const uint32_t tok = (r % block_len == 0) ? anchor_tok[r / block_len] : (uint32_t)mask_token;
     float4* d = reinterpret_cast<float4*>(h + (int64_t)r * H);
     if (tok >= (uint32_t)vocab) {
@@ -98,8 +114,8 @@ __global__ void embed_rows_kernel(const float* __restrict__ embed, int H, int vo
 
 int embed_rows(const float* embed, int H, int vocab, const uint32_t* anchor_tok, int mask_token, int n_seqs,
                int block_len, float* h, cudaStream_t st) {
-    embed_rows_kernel<<<n_seqs * block_len, 256, 0, st>>>(embed, H, vocab, anchor_tok, mask_token, block_len, h);
-    return (int)cudaGetLastError();
+    return (int)launch(embed_rows_kernel, dim3(n_seqs * block_len), dim3(256), 0, st, embed, H, vocab, anchor_tok,
+                       mask_token, block_len, h);
 }
 
 // RMSNorm of one head (hd = 32 * E elements, lane holds lane + 32 j) and its
@@ -137,6 +153,8 @@ __global__ void qk_norm_rope_kernel(float* __restrict__ qkv, int ld, int rows, i
     constexpr int HD = 32 * E;
     const int wid = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
     const int heads = nq + nkv;
+    pdl_trigger();
+    pdl_wait();
     if (wid >= rows * heads) return;
     const int r = wid / heads, hh = wid % heads, lane = threadIdx.x & 31;
     float* p = qkv + (int64_t)r * ld + hh * HD;  // q heads then k heads are contiguous
@@ -154,21 +172,22 @@ int qk_norm_rope(float* qkv, int ld, int rows, int block_len, const int64_t* pos
     const int64_t warps = (int64_t)rows * (nq + nkv);
     const unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
     if (hd == 128)
-        qk_norm_rope_kernel<4><<<blocks, 256, 0, st>>>(qkv, ld, rows, block_len, pos0_dev, nq, nkv, q_norm, k_norm,
-                                                       inv_freq, eps);
-    else
-        qk_norm_rope_kernel<2><<<blocks, 256, 0, st>>>(qkv, ld, rows, block_len, pos0_dev, nq, nkv, q_norm, k_norm,
-                                                       inv_freq, eps);
-    return (int)cudaGetLastError();
+        return (int)launch(qk_norm_rope_kernel<4>, dim3(blocks), dim3(256), 0, st, qkv, ld, rows, block_len, pos0_dev,
+                           nq, nkv, q_norm, k_norm, inv_freq, eps);
+    return (int)launch(qk_norm_rope_kernel<2>, dim3(blocks), dim3(256), 0, st, qkv, ld, rows, block_len, pos0_dev, nq,
+                       nkv, q_norm, k_norm, inv_freq, eps);
 }
 
 template <int E>
 __global__ void kv_append_kernel(const float* __restrict__ kv, int n, int L, int nkv,
                                  const float* const* __restrict__ k_norm, const float* __restrict__ inv_freq,
-                                 float eps, int64_t pos0, int64_t idx0, float* const* __restrict__ kstore,
+                                 float eps, const int64_t* __restrict__ pos, float* const* __restrict__ kstore,
                                  float* const* __restrict__ vstore, int64_t cap) {
     constexpr int HD = 32 * E;
     const int64_t wid = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+    pdl_trigger();
+    pdl_wait();
+    const int64_t pos0 = pos[0], idx0 = pos[1];
     if (wid >= (int64_t)n * L * nkv) return;
     const int lane = threadIdx.x & 31;
     const int g = (int)(wid % nkv), l = (int)((wid / nkv) % L);
@@ -191,51 +210,51 @@ __global__ void kv_append_kernel(const float* __restrict__ kv, int n, int L, int
 }
 
 int kv_append(const float* kv, int n, int L, int nkv, int hd, const float* const* k_norm_dev, const float* inv_freq,
-              float eps, int64_t pos0, int64_t idx0, float* const* kstore_dev, float* const* vstore_dev, int64_t cap,
+              float eps, const int64_t* pos_dev, float* const* kstore_dev, float* const* vstore_dev, int64_t cap,
               cudaStream_t st) {
     if (n <= 0) return 0;
     const int64_t warps = (int64_t)n * L * nkv;
     const unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
     if (hd == 128)
-        kv_append_kernel<4><<<blocks, 256, 0, st>>>(kv, n, L, nkv, k_norm_dev, inv_freq, eps, pos0, idx0, kstore_dev,
-                                                    vstore_dev, cap);
-    else
-        kv_append_kernel<2><<<blocks, 256, 0, st>>>(kv, n, L, nkv, k_norm_dev, inv_freq, eps, pos0, idx0, kstore_dev,
-                                                    vstore_dev, cap);
-    return (int)cudaGetLastError();
+        return (int)launch(kv_append_kernel<4>, dim3(blocks), dim3(256), 0, st, kv, n, L, nkv, k_norm_dev, inv_freq,
+                           eps, pos_dev, kstore_dev, vstore_dev, cap);
+    return (int)launch(kv_append_kernel<2>, dim3(blocks), dim3(256), 0, st, kv, n, L, nkv, k_norm_dev, inv_freq, eps,
+                       pos_dev, kstore_dev, vstore_dev, cap);
 }
 
 DF_DEV float silu_f(float a) { return a / (1.0f + expf(-a)); }
 
-__global__ void __launch_bounds__(256) silu_mul_kernel(const float* __restrict__ gu, int ld_gu, int I,
-                                                       float* __restrict__ out_f32, int ld_out,
-                                                       __half* __restrict__ out_codes, float* __restrict__ out_scale,
-                                                       int ld_codes) {
-    __shared__ float red[16];
+__global__ void __launch_bounds__(kRowThreads) silu_mul_kernel(const float* __restrict__ gu, int ld_gu, int I,
+                                                               float* __restrict__ out_f32, int ld_out,
+                                                               int8_t* __restrict__ out_codes,
+                                                               float* __restrict__ out_scale, int ld_codes) {
+    __shared__ float red[33];
+    pdl_trigger();
+    pdl_wait();
     const int r = blockIdx.x;
     const float* g = gu + (int64_t)r * ld_gu;
     const float* u = g + I;
     if (out_f32) {
-        for (int c = threadIdx.x; c < I; c += 256) out_f32[(int64_t)r * ld_out + c] = silu_f(g[c]) * u[c];
+        for (int c = threadIdx.x; c < I; c += kRowThreads) out_f32[(int64_t)r * ld_out + c] = silu_f(g[c]) * u[c];
         return;
     }
     float amax = 0.f;
-    for (int c = threadIdx.x; c < I; c += 256) amax = fmaxf(amax, fabsf(silu_f(g[c]) * u[c]));
-    amax = block_reduce_256<true>(amax, red);
+    for (int c = threadIdx.x; c < I; c += kRowThreads) amax = fmaxf(amax, fabsf(silu_f(g[c]) * u[c]));
+    amax = row_reduce<true>(amax, red);
     const float sx = __fdiv_rn(amax, 127.0f);
-    __half* q = out_codes + (int64_t)r * ld_codes;
-    for (int c = threadIdx.x; c < I; c += 256) {
+    int8_t* q = out_codes + (int64_t)r * ld_codes;
+    for (int c = threadIdx.x; c < I; c += kRowThreads) {
         const float a = silu_f(g[c]) * u[c];
-        q[c] = sx > 0.f ? code_of(a, sx) : __float2half_rn(0.f);
+        q[c] = sx > 0.f ? code_of(a, sx) : (int8_t)0;
     }
     if (threadIdx.x == 0) out_scale[r] = sx;
 }
 
-int silu_mul(const float* gu, int ld_gu, int rows, int I, float* out_f32, int ld_out, __half* out_codes,
+int silu_mul(const float* gu, int ld_gu, int rows, int I, float* out_f32, int ld_out, int8_t* out_codes,
              float* out_scale, int ld_codes, cudaStream_t st) {
     if (rows <= 0) return 0;
-    silu_mul_kernel<<<rows, 256, 0, st>>>(gu, ld_gu, I, out_f32, ld_out, out_codes, out_scale, ld_codes);
-    return (int)cudaGetLastError();
+    return (int)launch(silu_mul_kernel, dim3(rows), dim3(kRowThreads), 0, st, gu, ld_gu, I, out_f32, ld_out,
+                       out_codes, out_scale, ld_codes);
 }
 
 // ------------------------------------------------------------------ attention
@@ -244,133 +263,268 @@ int silu_mul(const float* gu, int ld_gu, int rows, int I, float* out_f32, int ld
 // [lo, lo + n) then the block's rows; a split keeps an online softmax (running
 // max in the log2 domain, running sum, unnormalised output) and writes it to
 // `part`; attn_combine merges the splits.
-constexpr int kAttnQ = 64;
-constexpr int kAttnK = 32;
+constexpr int kAttnQ = 64;   // query vectors of a CTA: 4 warps x 16
+constexpr int kAttnK = 32;   // keys per tile
+constexpr int kAttnWarps = 4;
+
+// f32 -> (hi, lo) f16 pair with hi + lo = x to about 2^-22 relative
+DF_DEV void split_f16(float x, __half& hi, __half& lo) {
+    hi = __float2half_rn(x);
+    lo = __float2half_rn(x - __half2float(hi));
+}
+
+DF_DEV void ldsm_x4(uint32_t (&r)[4], const __half* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_addr(p)));
+}
+DF_DEV void ldsm_x4_t(uint32_t (&r)[4], const __half* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_addr(p)));
+}
+DF_DEV uint32_t pack_half2(__half a, __half b) {
+    __half2 h = __halves2half2(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// four consecutive f32 values as hi/lo f16 halves, one 8-byte store each
+DF_DEV void split_store4(float4 v, __half* hi, __half* lo) {
+    __half h0, l0, h1, l1, h2, l2, h3, l3;
+    split_f16(v.x, h0, l0);
+    split_f16(v.y, h1, l1);
+    split_f16(v.z, h2, l2);
+    split_f16(v.w, h3, l3);
+    *reinterpret_cast<uint2*>(hi) = make_uint2(pack_half2(h0, h1), pack_half2(h2, h3));
+    *reinterpret_cast<uint2*>(lo) = make_uint2(pack_half2(l0, l1), pack_half2(l2, l3));
+}
 
 template <int HD>
 struct AttnSmem {
-    float q[kAttnQ][HD + 4];
-    float k[kAttnK][HD + 4];
-    float v[kAttnK][HD];
-    float p[kAttnQ][kAttnK + 1];
+    static constexpr int LD = HD + 8;  // halves: 16-byte row pad, conflict-free ldmatrix
+    __half qh[kAttnQ][LD], ql[kAttnQ][LD];
+    __half kh[kAttnK][LD], kl[kAttnK][LD];
+    __half vh[kAttnK][LD], vl[kAttnK][LD];
 };
 
+// One CTA per (key split, kv head x query tile, sequence).  The query tile is
+// up to 64 (q head of the group, block row) pairs, 16 per warp; keys are the
+// context rows [lo, lo + n) then the block's rows.  Scores and values go
+// through f16 tensor-core MMAs as hi/lo splits (q.k = qh.kh + qh.kl + ql.kh,
+// likewise p.v), which keeps f32-level accuracy; the softmax is online in f32
+// (running max in the log2 domain, running sum, unnormalised output), written
+// per split to `part` for attn_combine.
 template <int HD>
-__global__ void __launch_bounds__(256) attn_split_kernel(const float* __restrict__ qkv, int ld, int block_len,
-                                                         const AttnSeq* __restrict__ seqs, int nq, int nkv, int qtiles,
-                                                         int nsplit, int keys_per_split, float scale_log2,
-                                                         float* __restrict__ part) {
+__global__ void __launch_bounds__(kAttnWarps * 32) attn_split_kernel(const float* __restrict__ qkv, int ld,
+                                                                     int block_len, const AttnSeq* __restrict__ seqs,
+                                                                     int nq, int nkv, int qtiles, int nsplit,
+                                                                     float scale_log2, float* __restrict__ part) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     AttnSmem<HD>& sm = *reinterpret_cast<AttnSmem<HD>*>(smem_raw);
-    constexpr int DV = HD / 16;  // float4 groups of the output a thread keeps
+    constexpr int LD = AttnSmem<HD>::LD;
+    constexpr int NT = HD / 8;   // n8 tiles of the output
+    constexpr int KS = HD / 16;  // k16 steps of the scores
     const int sp = blockIdx.x, g = blockIdx.y / qtiles, qt = blockIdx.y % qtiles, s = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
+    pdl_trigger();
+    pdl_wait();
     const AttnSeq sq = seqs[s];
     const int rep = nq / nkv, mq = rep * block_len;
     const int total = sq.n + block_len;
+    // this sequence's keys in nsplit splits of a multiple of the key tile
+    const int keys_per_split = ((total + nsplit - 1) / nsplit + kAttnK - 1) / kAttnK * kAttnK;
     const int j0 = sp * keys_per_split, j1 = min(total, j0 + keys_per_split);
-    const int tid = threadIdx.x, qrow = tid >> 2, sub = tid & 3;
     const int64_t row0 = (int64_t)s * block_len;
 
-    // queries of this tile: query ii = qt*64 + qrow is head g*rep + ii / block_len at row ii % block_len
-    for (int i = tid; i < kAttnQ * (HD / 4); i += 256) {
-        const int qr = i / (HD / 4), c4 = i % (HD / 4), ii = qt * kAttnQ + qr;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (ii < mq) {
-            const int head = g * rep + ii / block_len, r = ii % block_len;
-            v = *reinterpret_cast<const float4*>(qkv + (row0 + r) * ld + (int64_t)head * HD + c4 * 4);
-        }
-        *reinterpret_cast<float4*>(&sm.q[qr][c4 * 4]) = v;
-    }
-    float m_run = -INFINITY, l_run = 0.f;
-    float4 acc[DV];
+    // Operands move as float4: the query tile and each key/value tile are read
+    // with all of a thread's loads in flight at once, and the next key tile is
+    // fetched into registers while the current one is multiplied.
+    constexpr int D4 = HD / 4;
+    constexpr int NQ4 = kAttnQ * D4 / (kAttnWarps * 32), NK4 = kAttnK * D4 / (kAttnWarps * 32);
+    static_assert(NQ4 * kAttnWarps * 32 == kAttnQ * D4 && NK4 * kAttnWarps * 32 == kAttnK * D4, "tile split");
+    float4 pk[NK4], pv[NK4];
+    auto load_kv = [&](int jt) {
 #pragma unroll
-    for (int d = 0; d < DV; ++d) acc[d] = make_float4(0.f, 0.f, 0.f, 0.f);
-
-    for (int jt = j0; jt < j1; jt += kAttnK) {
-        __syncthreads();  // previous tile's k/v/p no longer read
-        for (int i = tid; i < kAttnK * (HD / 4); i += 256) {
-            const int kr = i / (HD / 4), c4 = i % (HD / 4), j = jt + kr;
+        for (int u = 0; u < NK4; ++u) {
+            const int i = tid + u * kAttnWarps * 32, kr = i / D4, d = (i % D4) * 4, j = jt + kr;
             float4 kk = make_float4(0.f, 0.f, 0.f, 0.f), vv = kk;
             if (j < j1) {
                 if (j < sq.n) {
-                    const int64_t off = ((int64_t)g * sq.cap + sq.lo + j) * HD + c4 * 4;
+                    const int64_t off = ((int64_t)g * sq.cap + sq.lo + j) * HD + d;
                     kk = *reinterpret_cast<const float4*>(sq.kc + off);
                     vv = *reinterpret_cast<const float4*>(sq.vc + off);
                 } else {
-                    const int64_t off = (row0 + (j - sq.n)) * ld + c4 * 4;
+                    const int64_t off = (row0 + (j - sq.n)) * ld + d;
                     kk = *reinterpret_cast<const float4*>(qkv + off + (int64_t)(nq + g) * HD);
                     vv = *reinterpret_cast<const float4*>(qkv + off + (int64_t)(nq + nkv + g) * HD);
                 }
             }
-            *reinterpret_cast<float4*>(&sm.k[kr][c4 * 4]) = kk;
-            *reinterpret_cast<float4*>(&sm.v[kr][c4 * 4]) = vv;
+            pk[u] = kk;
+            pv[u] = vv;
+        }
+    };
+    {
+        float4 qv[NQ4];
+#pragma unroll
+        for (int u = 0; u < NQ4; ++u) {
+            const int i = tid + u * kAttnWarps * 32, qr = i / D4, d = (i % D4) * 4, ii = qt * kAttnQ + qr;
+            qv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (ii < mq) {
+                const int head = g * rep + ii / block_len, r = ii % block_len;
+                qv[u] = *reinterpret_cast<const float4*>(qkv + (row0 + r) * ld + (int64_t)head * HD + d);
+            }
+        }
+        if (j0 < j1) load_kv(j0);
+#pragma unroll
+        for (int u = 0; u < NQ4; ++u) {
+            const int i = tid + u * kAttnWarps * 32, qr = i / D4, d = (i % D4) * 4;
+            split_store4(qv[u], &sm.qh[qr][d], &sm.ql[qr][d]);
+        }
+    }
+
+    float o[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+    const int qbase = warp * 16;
+    // ldmatrix row addresses: A (queries x dims) and B (keys x dims) operands
+    const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8, lcol = (lane >> 4) * 8;
+
+    for (int jt = j0; jt < j1; jt += kAttnK) {
+        __syncthreads();  // the previous tile's keys and values are no longer read
+#pragma unroll
+        for (int u = 0; u < NK4; ++u) {
+            const int i = tid + u * kAttnWarps * 32, kr = i / D4, d = (i % D4) * 4;
+            split_store4(pk[u], &sm.kh[kr][d], &sm.kl[kr][d]);
+            split_store4(pv[u], &sm.vh[kr][d], &sm.vl[kr][d]);
         }
         __syncthreads();
-        // scores of keys sub + 4m
-        float sc[8];
+        if (jt + kAttnK < j1) load_kv(jt + kAttnK);
+        // scores: 16 queries x 32 keys per warp
+        float sc[4][4];
 #pragma unroll
-        for (int m = 0; m < 8; ++m) sc[m] = 0.f;
-#pragma unroll 4
-        for (int d = 0; d < HD; d += 4) {
-            const float4 qv = *reinterpret_cast<const float4*>(&sm.q[qrow][d]);
+        for (int n = 0; n < 4; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
 #pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                const float4 kv4 = *reinterpret_cast<const float4*>(&sm.k[sub + 4 * m][d]);
-                sc[m] = fmaf(qv.x, kv4.x, fmaf(qv.y, kv4.y, fmaf(qv.z, kv4.z, fmaf(qv.w, kv4.w, sc[m]))));
+        for (int k = 0; k < KS; ++k) {
+            uint32_t ah[4], al[4];
+            ldsm_x4(ah, &sm.qh[qbase + lrow][k * 16 + lcol]);
+            ldsm_x4(al, &sm.ql[qbase + lrow][k * 16 + lcol]);
+#pragma unroll
+            for (int nb = 0; nb < 2; ++nb) {  // keys 16 nb .. 16 nb + 15
+                uint32_t bh[4], bl[4];
+                // matrices: (keys +0..7, dims +0..7), (keys +0..7, dims +8..15), (keys +8..15, ...), ...
+                const int brow = nb * 16 + (lane & 7) + (lane >> 4) * 8, bcol = k * 16 + ((lane >> 3) & 1) * 8;
+                ldsm_x4(bh, &sm.kh[brow][bcol]);
+                ldsm_x4(bl, &sm.kl[brow][bcol]);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    float* c = sc[nb * 2 + h];
+                    float cc[4] = {c[0], c[1], c[2], c[3]};
+                    mma_f16_16816(cc, ah, bh[h * 2], bh[h * 2 + 1], cc);
+                    mma_f16_16816(cc, ah, bl[h * 2], bl[h * 2 + 1], cc);
+                    mma_f16_16816(cc, al, bh[h * 2], bh[h * 2 + 1], cc);
+                    c[0] = cc[0];
+                    c[1] = cc[1];
+                    c[2] = cc[2];
+                    c[3] = cc[3];
+                }
             }
         }
-        float tmax = -INFINITY;
+        // online softmax over the tile; rows gq and gq + 8 of the warp's 16
+        float tmax[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
-            sc[m] = (jt + sub + 4 * m < j1) ? sc[m] * scale_log2 : -INFINITY;
-            tmax = fmaxf(tmax, sc[m]);
+        for (int n = 0; n < 4; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int key = jt + n * 8 + 2 * tq + (e & 1);
+                const float v = key < j1 ? sc[n][e] * scale_log2 : -INFINITY;
+                sc[n][e] = v;
+                tmax[e >> 1] = fmaxf(tmax[e >> 1], v);
+            }
+        float corr[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            tmax[h] = fmaxf(tmax[h], __shfl_xor_sync(0xffffffffu, tmax[h], 1));
+            tmax[h] = fmaxf(tmax[h], __shfl_xor_sync(0xffffffffu, tmax[h], 2));
+            const float m_new = fmaxf(m_run[h], tmax[h]);
+            corr[h] = (m_run[h] == -INFINITY) ? 0.f : exp2f(m_run[h] - m_new);
+            m_run[h] = m_new;
         }
-        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
-        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
-        const float m_new = fmaxf(m_run, tmax);
-        const float corr = (m_run == -INFINITY) ? 0.f : exp2f(m_run - m_new);
-        float psum = 0.f;
+        float psum[2] = {0.f, 0.f};
+        uint32_t ph[2][4], pl[2][4];  // A fragments of P for the two k16 steps (keys 0..15, 16..31)
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
-            const float p = (sc[m] == -INFINITY) ? 0.f : exp2f(sc[m] - m_new);
-            sm.p[qrow][sub + 4 * m] = p;
-            psum += p;
+        for (int n = 0; n < 4; ++n) {
+            float p[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                p[e] = (sc[n][e] == -INFINITY) ? 0.f : exp2f(sc[n][e] - m_run[e >> 1]);
+                psum[e >> 1] += p[e];
+            }
+            __half h0, l0, h1, l1, h2, l2, h3, l3;
+            split_f16(p[0], h0, l0);
+            split_f16(p[1], h1, l1);
+            split_f16(p[2], h2, l2);
+            split_f16(p[3], h3, l3);
+            const int kstep = n >> 1, half = n & 1;  // keys 8n..8n+7 -> k16 step n/2, column half n%2
+            ph[kstep][half * 2 + 0] = pack_half2(h0, h1);  // row gq
+            ph[kstep][half * 2 + 1] = pack_half2(h2, h3);  // row gq + 8
+            pl[kstep][half * 2 + 0] = pack_half2(l0, l1);
+            pl[kstep][half * 2 + 1] = pack_half2(l2, l3);
         }
-        psum += __shfl_xor_sync(0xffffffffu, psum, 1);
-        psum += __shfl_xor_sync(0xffffffffu, psum, 2);
-        l_run = l_run * corr + psum;
-        m_run = m_new;
 #pragma unroll
-        for (int d = 0; d < DV; ++d) {
-            acc[d].x *= corr;
-            acc[d].y *= corr;
-            acc[d].z *= corr;
-            acc[d].w *= corr;
+        for (int h = 0; h < 2; ++h) {
+            psum[h] += __shfl_xor_sync(0xffffffffu, psum[h], 1);
+            psum[h] += __shfl_xor_sync(0xffffffffu, psum[h], 2);
+            l_run[h] = l_run[h] * corr[h] + psum[h];
         }
-        __syncwarp();
-        // the 4 threads of a query row wrote its 32 probabilities; they are in one warp
-#pragma unroll 4
-        for (int kk = 0; kk < kAttnK; ++kk) {
-            const float p = sm.p[qrow][kk];
 #pragma unroll
-            for (int d = 0; d < DV; ++d) {
-                const float4 vv = *reinterpret_cast<const float4*>(&sm.v[kk][4 * (sub + 4 * d)]);
-                acc[d].x = fmaf(p, vv.x, acc[d].x);
-                acc[d].y = fmaf(p, vv.y, acc[d].y);
-                acc[d].z = fmaf(p, vv.z, acc[d].z);
-                acc[d].w = fmaf(p, vv.w, acc[d].w);
+        for (int j = 0; j < NT; ++j) {
+            o[j][0] *= corr[0];
+            o[j][1] *= corr[0];
+            o[j][2] *= corr[1];
+            o[j][3] *= corr[1];
+        }
+        // o += p . v over the tile's 32 keys
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+            // A fragment order: {row gq keys 2t.., row gq+8 keys 2t.., row gq keys 8+2t.., row gq+8 keys 8+2t..}
+            const uint32_t ahp[4] = {ph[ks][0], ph[ks][1], ph[ks][2], ph[ks][3]};
+            const uint32_t alp[4] = {pl[ks][0], pl[ks][1], pl[ks][2], pl[ks][3]};
+#pragma unroll
+            for (int jb = 0; jb < NT / 2; ++jb) {  // dims 16 jb .. 16 jb + 15
+                uint32_t bh[4], bl[4];
+                // .trans matrices: (keys +0..7, dims +0..7), (keys +8..15, dims +0..7), (keys +0..7, dims +8..15), ...
+                const int vrow = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, vcol = jb * 16 + (lane >> 4) * 8;
+                ldsm_x4_t(bh, &sm.vh[vrow][vcol]);
+                ldsm_x4_t(bl, &sm.vl[vrow][vcol]);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    float* c = o[jb * 2 + h];
+                    float cc[4] = {c[0], c[1], c[2], c[3]};
+                    mma_f16_16816(cc, ahp, bh[h * 2], bh[h * 2 + 1], cc);
+                    mma_f16_16816(cc, ahp, bl[h * 2], bl[h * 2 + 1], cc);
+                    mma_f16_16816(cc, alp, bh[h * 2], bh[h * 2 + 1], cc);
+                    c[0] = cc[0];
+                    c[1] = cc[1];
+                    c[2] = cc[2];
+                    c[3] = cc[3];
+                }
             }
         }
     }
-    // partial: [s][g][qt][sp][qrow] -> {m, l, -, -, acc[HD]} (16-byte aligned)
-    const int64_t e = ((((int64_t)s * nkv + g) * qtiles + qt) * nsplit + sp) * kAttnQ + qrow;
-    float* out = part + e * (HD + 4);
-    if (sub == 0) {
-        out[0] = m_run;
-        out[1] = l_run;
-    }
+    // partial: [s][g][qt][sp][query row] -> {m, l, -, -, acc[HD]} (16-byte aligned)
+    const int64_t e0 = (((int64_t)s * nkv + g) * qtiles + qt) * nsplit + sp;
 #pragma unroll
-    for (int d = 0; d < DV; ++d) *reinterpret_cast<float4*>(out + 4 + 4 * (sub + 4 * d)) = acc[d];
+    for (int h = 0; h < 2; ++h) {
+        const int qrow = qbase + gq + 8 * h;
+        float* out = part + (e0 * kAttnQ + qrow) * (HD + 4);
+        if (tq == 0) {
+            out[0] = m_run[h];
+            out[1] = l_run[h];
+        }
+#pragma unroll
+        for (int j = 0; j < NT; ++j) *reinterpret_cast<float2*>(out + 4 + j * 8 + 2 * tq) = make_float2(o[j][2 * h], o[j][2 * h + 1]);
+    }
 }
 
 // One warp per (sequence, block row, q head): merge the splits, divide by the sum.
@@ -378,6 +532,8 @@ template <int HD>
 __global__ void attn_combine_kernel(const float* __restrict__ part, int n_seqs, int block_len, int nq, int nkv,
                                     int qtiles, int nsplit, float* __restrict__ y) {
     const int64_t wid = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+    pdl_trigger();
+    pdl_wait();
     if (wid >= (int64_t)n_seqs * block_len * nq) return;
     const int lane = threadIdx.x & 31;
     const int h = (int)(wid % nq), r = (int)((wid / nq) % block_len), s = (int)(wid / ((int64_t)nq * block_len));
@@ -405,23 +561,21 @@ __global__ void attn_combine_kernel(const float* __restrict__ part, int n_seqs, 
     for (int j = 0; j < E; ++j) dst[lane + 32 * j] = o[j] / L;
 }
 
-static void attn_plan(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int num_sms, int* qtiles, int* nsplit,
-                      int* kps) {
+// Splits of the keys: enough CTAs to cover the SMs twice, no more splits than
+// key tiles of the longest context `max_ctx` can have (callers pass the
+// sequences' capacity, so that the launch does not change as contexts grow).
+static void attn_plan(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int num_sms, int* qtiles, int* nsplit) {
     const int mq = (nq / nkv) * block_len;
     *qtiles = (mq + kAttnQ - 1) / kAttnQ;
     const int total = max_ctx + block_len;
     const int max_split = (total + kAttnK - 1) / kAttnK;
     const int units = nkv * *qtiles * n_seqs;
-    int ns = std::max(1, std::min(max_split, (2 * num_sms + units - 1) / units));
-    int k = (total + ns - 1) / ns;
-    k = (k + kAttnK - 1) / kAttnK * kAttnK;
-    *kps = k;
-    *nsplit = (total + k - 1) / k;
+    *nsplit = std::max(1, std::min(max_split, (2 * num_sms + units - 1) / units));
 }
 
 int64_t attn_scratch_floats(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int hd, int num_sms) {
-    int qt, ns, kps;
-    attn_plan(n_seqs, block_len, max_ctx, nq, nkv, num_sms, &qt, &ns, &kps);
+    int qt, ns;
+    attn_plan(n_seqs, block_len, max_ctx, nq, nkv, num_sms, &qt, &ns);
     return (int64_t)n_seqs * nkv * qt * ns * kAttnQ * (hd + 4);
 }
 
@@ -429,8 +583,8 @@ template <int HD>
 static int attention_hd(const float* qkv, int ld, int n_seqs, int block_len, const AttnSeq* seqs_dev, int max_ctx,
                         int nq, int nkv, float scale, float* part, int64_t part_floats, float* y, int num_sms,
                         cudaStream_t st) {
-    int qtiles, nsplit, kps;
-    attn_plan(n_seqs, block_len, max_ctx, nq, nkv, num_sms, &qtiles, &nsplit, &kps);
+    int qtiles, nsplit;
+    attn_plan(n_seqs, block_len, max_ctx, nq, nkv, num_sms, &qtiles, &nsplit);
     if ((int64_t)n_seqs * nkv * qtiles * nsplit * kAttnQ * (HD + 4) > part_floats) return (int)cudaErrorInvalidValue;
     static bool attr = false;
     if (!attr) {
@@ -440,14 +594,12 @@ static int attention_hd(const float* qkv, int ld, int n_seqs, int block_len, con
     }
     const float scale_log2 = scale * 1.4426950408889634f;
     dim3 grid(nsplit, nkv * qtiles, n_seqs);
-    attn_split_kernel<HD><<<grid, 256, sizeof(AttnSmem<HD>), st>>>(qkv, ld, block_len, seqs_dev, nq, nkv, qtiles,
-                                                                   nsplit, kps, scale_log2, part);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch(attn_split_kernel<HD>, grid, dim3(kAttnWarps * 32), sizeof(AttnSmem<HD>), st, qkv, ld, block_len,
+                           seqs_dev, nq, nkv, qtiles, nsplit, scale_log2, part);
     if (e != cudaSuccess) return (int)e;
     const int64_t warps = (int64_t)n_seqs * block_len * nq;
-    attn_combine_kernel<HD><<<(unsigned)((warps * 32 + 255) / 256), 256, 0, st>>>(part, n_seqs, block_len, nq, nkv,
-                                                                                  qtiles, nsplit, y);
-    return (int)cudaGetLastError();
+    return (int)launch(attn_combine_kernel<HD>, dim3((unsigned)((warps * 32 + 255) / 256)), dim3(256), 0, st, part,
+                       n_seqs, block_len, nq, nkv, qtiles, nsplit, y);
 }
 
 int attention(const float* qkv, int ld, int n_seqs, int block_len, const AttnSeq* seqs_dev, int max_ctx, int nq,

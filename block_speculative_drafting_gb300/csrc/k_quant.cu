@@ -36,10 +36,12 @@ DF_DEV uint32_t q4_nibble(const float* __restrict__ w, int N, int K, int n, int 
     return (uint32_t)((int)q + 8);
 }
 
-// One thread per (tile, kstep, lane): the lane's 16 bytes, and (tq == 0) its 8 scale bytes.
+// One thread per (tile, kstep, lane): the lane's 16 bytes, and (tq == 0) its
+// 8 scale bytes, at the chunk of tile tile0 + tile in layout L.
 __global__ void q4_pack_kernel(const float* __restrict__ w, int N, int K, const __half* __restrict__ scales,
-                               int Gpad, int ntiles, int ksteps, uint8_t* __restrict__ out) {
+                               int Gpad, int ntiles, Q4Layout L, int tile0, uint8_t* __restrict__ out) {
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int ksteps = L.ksteps;
     if (i >= (int64_t)ntiles * ksteps * 32) return;
     int lane = (int)(i % 32);
     int64_t chunk = i / 32;
@@ -67,7 +69,7 @@ __global__ void q4_pack_kernel(const float* __restrict__ w, int N, int K, const 
             words[gi * 2 + s] = wd;
         }
     }
-    uint8_t* base = out + chunk * kQ4Chunk;
+    uint8_t* base = out + q4_chunk_offset(L, tile0 + tile, ks);
     *reinterpret_cast<uint4*>(base + lane * 16) = make_uint4(words[0], words[1], words[2], words[3]);
     if (tq == 0) {
         __half sc[4] = {scales[(int64_t)r0 * Gpad + 2 * ks], scales[(int64_t)r1 * Gpad + 2 * ks],
@@ -76,28 +78,27 @@ __global__ void q4_pack_kernel(const float* __restrict__ w, int N, int K, const 
     }
 }
 
-int q4_quantize_pack(const float* w_dev, int N, int K, uint8_t* packed, int tile0, int ksteps, __half* scratch,
+int q4_quantize_pack(const float* w_dev, int N, int K, uint8_t* packed, Q4Layout L, int tile0, __half* scratch,
                      cudaStream_t st) {
-    int Npad = (N + 15) / 16 * 16, Gpad = ksteps * 2;
+    int Npad = (N + 15) / 16 * 16, Gpad = L.ksteps * 2;
     int64_t ns = (int64_t)Npad * Gpad;
     q4_scales_kernel<<<(unsigned)((ns + 255) / 256), 256, 0, st>>>(w_dev, N, K, Npad, Gpad, scratch);
     int ntiles = Npad / 16;
-    int64_t nt = (int64_t)ntiles * ksteps * 32;
-    q4_pack_kernel<<<(unsigned)((nt + 255) / 256), 256, 0, st>>>(w_dev, N, K, scratch, Gpad, ntiles, ksteps,
-                                                                 packed + (int64_t)tile0 * ksteps * kQ4Chunk);
+    int64_t nt = (int64_t)ntiles * L.ksteps * 32;
+    q4_pack_kernel<<<(unsigned)((nt + 255) / 256), 256, 0, st>>>(w_dev, N, K, scratch, Gpad, ntiles, L, tile0, packed);
     return (int)cudaGetLastError();
 }
 
 // Inverse of the packing: codes [N][K] and scale bits [N][K/32] of rows
 // [tile0*16, tile0*16 + N).
-__global__ void q4_unpack_kernel(const uint8_t* __restrict__ packed, int tile0, int N, int K, int ksteps,
+__global__ void q4_unpack_kernel(const uint8_t* __restrict__ packed, Q4Layout L, int tile0, int N, int K,
                                  int8_t* __restrict__ codes, uint16_t* __restrict__ scales) {
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= (int64_t)N * K) return;
     int n = (int)(i / K), c = (int)(i % K);
     int tile = tile0 + n / 16, rr = n % 16, gq = rr % 8, up = rr / 8;
     int ks = c / 64, gi = (c % 64) / 32, wc = c % 32, tq = wc / 8, s = (wc % 8) / 4, cc = wc % 4;
-    const uint8_t* base = packed + ((int64_t)tile * ksteps + ks) * kQ4Chunk;
+    const uint8_t* base = packed + q4_chunk_offset(L, tile, ks);
     uint32_t word = reinterpret_cast<const uint32_t*>(base + (4 * gq + tq) * 16)[gi * 2 + s];
     // bit position of (row half `up`, column offset cc) inside the word
     int pos = (cc & 1 ? 16 : 0) + (cc & 2 ? 8 : 0) + (up ? 4 : 0);
@@ -108,20 +109,14 @@ __global__ void q4_unpack_kernel(const uint8_t* __restrict__ packed, int tile0, 
     }
 }
 
-int q4_unpack(const uint8_t* packed, int tile0, int N, int K, int ksteps, int8_t* codes, uint16_t* scales,
+int q4_unpack(const uint8_t* packed, Q4Layout L, int tile0, int N, int K, int8_t* codes, uint16_t* scales,
               cudaStream_t st) {
     int64_t n = (int64_t)N * K;
-    q4_unpack_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(packed, tile0, N, K, ksteps, codes, scales);
+    q4_unpack_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(packed, L, tile0, N, K, codes, scales);
     return (int)cudaGetLastError();
 }
 
 // --------------------------------------------------------------- int8 rows
-DF_DEV int64_t i8_byte_offset(int n, int c, int ksteps) {
-    int tile = n / 16, rr = n % 16, gq = rr % 8, up = rr / 8;
-    int ks = c / 32, wc = c % 32, tq = wc / 8, cc = wc % 8;
-    return ((int64_t)tile * ksteps + ks) * kI8Chunk + (4 * gq + tq) * 16 + (cc / 4) * 8 + up * 4 + (cc % 4);
-}
-
 // One CTA per row (rows >= N: zero codes and scale).
 __global__ void i8_rows_pack_kernel(const float* __restrict__ w, int N, int K, int ksteps, int8_t* __restrict__ packed,
                                     float* __restrict__ row_scale) {
@@ -141,7 +136,7 @@ __global__ void i8_rows_pack_kernel(const float* __restrict__ w, int N, int K, i
     __syncthreads();
     float s = __fdiv_rn(red[0], 127.0f);
     if (threadIdx.x == 0) row_scale[n] = s;
-    for (int c = threadIdx.x; c < ksteps * 32; c += blockDim.x) {
+    for (int c = threadIdx.x; c < ksteps * kI8KStep; c += blockDim.x) {
         int q = 0;
         if (n < N && c < K && s > 0.f) {
             float v = rintf(__fdiv_rn(w[(int64_t)n * K + c], s));

@@ -6,38 +6,70 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "common.cuh"
+
 namespace dflash {
 
 // ---- init-time quantisers / packers (k_quant.cu)
-int q4_quantize_pack(const float* w_dev, int N, int K, uint8_t* packed, int tile0, int ksteps, __half* scale_scratch,
+// 4-bit matrices in layout L (common.cuh); tile0: first 16-row tile of the
+// sub-matrix inside the fused matrix.
+int q4_quantize_pack(const float* w_dev, int N, int K, uint8_t* packed, Q4Layout L, int tile0, __half* scale_scratch,
                      cudaStream_t st);
-int q4_unpack(const uint8_t* packed, int tile0, int N, int K, int ksteps, int8_t* codes, uint16_t* scales,
+int q4_unpack(const uint8_t* packed, Q4Layout L, int tile0, int N, int K, int8_t* codes, uint16_t* scales,
               cudaStream_t st);
 int i8_rows_quantize_pack(const float* w_dev, int N, int K, int Npad, int ksteps, int8_t* packed, float* row_scale,
                           cudaStream_t st);
 int i8_unpack(const int8_t* packed, int N, int K, int ksteps, int8_t* codes, cudaStream_t st);
 
-// ---- matmuls (k_gemm.cu)
-// Activation operand of the quantised matmuls: int8 codes held as exact f16
-// integers, [rows][ld] with ld >= K (K a multiple of 64), one f32 scale a row.
+// ---- launching: every kernel of the library goes out with the programmatic
+// stream-serialisation attribute (programmatic dependent launch), so that it
+// may start -- and stream its weights -- while the previous kernel on the
+// stream finishes; each kernel waits (pdl_wait) before it touches what its
+// predecessors write.  Without a predecessor kernel the attribute is inert.
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// ---- matmuls (k_gemm.cu, k_stream.cu)
+// Activation operand of the quantised matmuls: int8 codes [rows][ld]
+// (ld >= K, a multiple of 16), one f32 scale a row.
 struct QAct {
-    const __half* codes;
+    const int8_t* codes;
     const float* scale;
     int ld;
 };
 
 // y[t][n] (+)= xs[t] * sum_g s[n][g] * sum_{k in g} q[n][k] x[t][k] for n < N,
-// t < T.  accumulate: add into y (atomically); otherwise y is overwritten.
-int q4_gemm(const uint8_t* packed, int tile0, int N, int ksteps, QAct x, int T, float* y, int ldy, bool accumulate,
+// t < T, any T (16 rows per CTA).  accumulate: add into y (atomically);
+// otherwise y is overwritten.
+int q4_gemm(const uint8_t* packed, Q4Layout L, int tile0, int N, QAct x, int T, float* y, int ldy, bool accumulate,
             int num_sms, cudaStream_t st);
 // The int32 group sums of the same inner loop (T <= 16): out[t][n][g].
-int q4_groupsums(const uint8_t* packed, int tile0, int N, int ksteps, QAct x, int T, int32_t* out, cudaStream_t st);
+int q4_groupsums(const uint8_t* packed, Q4Layout L, int tile0, int N, QAct x, int T, int32_t* out, cudaStream_t st);
 
-// The head: logits[t][n] = xs[t] * sw[n] * sum_k q[n][k] x[t][k] (int32 sums),
-// and, if keys != nullptr, keys[t] = max over n of argmax_key(logits[t][n], n)
-// (keys must be zeroed before).
-int head_i8(const int8_t* packed, const float* row_scale, int V, int ksteps, QAct x, int T, float* logits, int ldl,
-            unsigned long long* keys, int num_sms, cudaStream_t st);
+// The streaming form for up to 16 rows: every CTA streams a contiguous slice
+// of the matrix (tile0 and N multiples of 64 rows) through a bulk-copy ring
+// and ADDS its partial sums into y (which must hold zeros or the residual).
+int q4_stream(const uint8_t* packed, Q4Layout L, int tile0, int N, QAct x, int T, float* y, int ldy, int num_sms,
+              int* err_flag, cudaStream_t st);
+size_t q4_stream_smem_bytes(Q4Layout L, int N, int num_sms);
+
+// The head: logits[t][n] = xs[t] * sw[n] * sum_k q[n][k] x[t][k] (exact int32
+// sums on f16 tensor cores), and keys[t] = max over n of argmax_key(logit, n)
+// (keys zeroed before).  logits may be nullptr.  Any T (16 rows per pass).
+int head_stream(const int8_t* packed, const float* row_scale, int V, int ksteps, QAct x, int T, float* logits,
+                int ldl, unsigned long long* keys, int num_sms, int* err_flag, cudaStream_t st);
 
 // y[t][n] (+)= sum_k W[n][k] x[t][k]; W f32 [N][K] (K % 4 == 0).
 int linear_f32(const float* W, int N, int K, const float* x, int ldx, int T, float* y, int ldy, bool accumulate,
@@ -53,9 +85,11 @@ struct RowMap {
     int per, stride, skip;
 };
 // x = rms(src, w) (w == nullptr: no norm, x = src); then either f32 out
-// (out_f32 != nullptr) or int8 codes as f16 + scale (out_q).
+// (out_f32 != nullptr) or int8 codes + an f32 scale per row.
+// zero_buf / zero_n: a buffer the kernel clears on the side (nullptr: none).
 int rms_rows(const float* src, int ld_src, RowMap map, int rows, int n, const float* w, float eps, float* out_f32,
-             int ld_out, __half* out_codes, float* out_scale, int ld_codes, cudaStream_t st);
+             int ld_out, int8_t* out_codes, float* out_scale, int ld_codes, cudaStream_t st,
+             float* zero_buf = nullptr, int64_t zero_n = 0);
 // h[r] = embed[tok(r)]: row r of sequence s = r / block_len is the anchor
 // (anchor_tok[s]) for r % block_len == 0, the mask token otherwise.
 int embed_rows(const float* embed, int H, int vocab, const uint32_t* anchor_tok, int mask_token, int n_seqs,
@@ -67,12 +101,13 @@ int qk_norm_rope(float* qkv, int ld, int rows, int block_len, const int64_t* pos
                  const float* q_norm, const float* k_norm, const float* inv_freq, float eps, cudaStream_t st);
 // Context rows: kv [n][L * 2 * nkv * hd] (per layer k then v) -> the
 // sequence's store: K rows normed (k_norm_l) and rotated at position
-// pos0 + r, V rows as they are; stored at index (pos0 - first) + r.
+// pos0 + r, V rows as they are; stored at index idx0 + r, where
+// pos_dev = {pos0, idx0} lives in device memory (set per call).
 int kv_append(const float* kv, int n, int L, int nkv, int hd, const float* const* k_norm_dev, const float* inv_freq,
-              float eps, int64_t pos0, int64_t idx0, float* const* kstore_dev, float* const* vstore_dev, int64_t cap,
+              float eps, const int64_t* pos_dev, float* const* kstore_dev, float* const* vstore_dev, int64_t cap,
               cudaStream_t st);
 // a = silu(g) * u for gu [rows][2I] (gate then up); f32 out or int8 codes.
-int silu_mul(const float* gu, int ld_gu, int rows, int I, float* out_f32, int ld_out, __half* out_codes,
+int silu_mul(const float* gu, int ld_gu, int rows, int I, float* out_f32, int ld_out, int8_t* out_codes,
              float* out_scale, int ld_codes, cudaStream_t st);
 
 // Attention of a block over its sequence's context and its own rows.
@@ -85,6 +120,8 @@ struct AttnSeq {
 };
 // qkv [n_seqs*block_len][ld] (q, k, v of the block after norm and RoPE);
 // y [n_seqs*block_len][nq*hd].  `part` is scratch of attn_scratch_floats().
+// max_ctx: the largest context any sequence of the call may hold (its
+// capacity); the launch depends on it, each CTA's key range on the actual n.
 int attention(const float* qkv, int ld, int n_seqs, int block_len, const AttnSeq* seqs_dev, int max_ctx, int nq,
               int nkv, int hd, float scale, float* part, int64_t part_floats, float* y, int num_sms, cudaStream_t st);
 int64_t attn_scratch_floats(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int hd, int num_sms);

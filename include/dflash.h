@@ -312,7 +312,8 @@ DFLASH_API int dflash_debug_trace_site(const dflash_model* model, int32_t index,
  * context before the anchor and the block's own rows, not causal, softmax,
  * values).  qkv: device [n_seqs*block_len][(heads + 2*kv_heads)*head_dim] f32,
  * each row its q heads, then k heads, then v heads, q and k already normed and
- * rotated; sequence s reads its layer-`layer` context positions
+ * rotated, the pointer 16-byte aligned (EINVAL otherwise: the kernel reads
+ * it as float4); sequence s reads its layer-`layer` context positions
  * [first, min(anchor_pos[s], next)) and rows s*block_len .. of qkv.  y: device
  * [n_seqs*block_len][heads*head_dim] f32.  anchor_pos is a host array.  Uses
  * the model's scratch (allocated on first need).  Work is queued on `stream`.
