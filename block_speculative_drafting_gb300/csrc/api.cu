@@ -928,7 +928,7 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
            qk_norm_rope(qkv, m->qkv_w, R, B, P<int64_t>(m->pos0), g.heads, g.kv_heads, hd, Ly.q_norm, Ly.k_norm,
                         m->inv_freq, g.eps, st));
         const AttnSeq* aseq_dev = P<AttnSeq>(m->aseqs) + (size_t)l * n_seqs;
-        KL(m, "attention", 2, attn_bytes, st,
+        KL(m, "attention", 1, attn_bytes, st,
            attention(qkv, m->qkv_w, n_seqs, B, aseq_dev, max_ctx, g.heads, g.kv_heads, hd, scale, P<float>(m->part),
                      part_floats, y, m->num_sms, st));
         if (quant) {
@@ -1051,7 +1051,7 @@ int dflash_debug_attention(dflash_model* m, dflash_seq* const* seqs, int32_t n_s
     CK(m, ensure_m(m, m->part, (size_t)part_floats * sizeof(float)));
     CK(m, ensure_m(m, m->aseqs, (size_t)n_seqs * sizeof(AttnSeq)));
     CK(m, cudaMemcpyAsync(m->aseqs.p, views.data(), views.size() * sizeof(AttnSeq), cudaMemcpyHostToDevice, st));
-    KL(m, "attention", 2, 0.0, st,
+    KL(m, "attention", 1, 0.0, st,
        attention(qkv, m->qkv_w, n_seqs, block_len, P<AttnSeq>(m->aseqs), max_ctx, g.heads, g.kv_heads, g.head_dim,
                  1.0f / sqrtf((float)g.head_dim), P<float>(m->part), part_floats, y, m->num_sms, st));
     return DFLASH_OK;
@@ -1315,12 +1315,14 @@ int dflash_attention_noalloc(dflash_model* m, dflash_seq* const* seqs, int32_t n
     CK(m, noalloc_base(m->device, &base));
     cudaStream_t st = (cudaStream_t)stream;
     AttnSeq* views_dev = reinterpret_cast<AttnSeq*>(base);
-    // every partial slot is written by the split kernel before the combine
-    // reads it, so nothing in the array needs to start at zero
+    // the array's head holds the context views; the key splits merge their
+    // partial results in distributed shared memory, so the rest of the array
+    // (kept for kernels that need scratch) is not read, and nothing in it
+    // needs to start at zero
     CK(m, cudaMemcpyAsync(views_dev, views.data(), views.size() * sizeof(AttnSeq), cudaMemcpyHostToDevice, st));
     CK(m, attention(qkv, m->qkv_w, n_seqs, block_len, views_dev, max_ctx, g.heads, g.kv_heads, g.head_dim,
                     1.0f / sqrtf((float)g.head_dim), base + kNoAllocViewFloats, part_floats, y, m->num_sms, st));
-    m->launches += 2;
+    m->launches += 1;
     return DFLASH_OK;
 }
 

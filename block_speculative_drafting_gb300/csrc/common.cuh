@@ -160,7 +160,11 @@ DF_DEV uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
     return d;
 }
 
-// Eight offset nibbles -> four half2 of exact integers (code = nibble - 8).
+// Eight offset nibbles -> four half2 of exact integers (code = nibble - 8):
+// a nibble n ORed into the mantissa of 1024.0h reads 1024 + n (low nibbles)
+// or 1024 + 16 n (high nibbles), and one subtraction (or multiply-add) per
+// half2 removes the offset.  The mask-and-insert is one explicit LOP3 each
+// (measured: fewer integer instructions than the compiler's own lowering).
 DF_DEV void unpack_q4_word(uint32_t w, uint32_t (&a)[4]) {
     const uint32_t kLo = 0x000F000Fu, kHi = 0x00F000F0u, kMagic = 0x64006400u;  // 0x6400 = 1024.0h
     const uint32_t kSub = 0x64086408u;                                        // 1032.0h: 1024 + 8

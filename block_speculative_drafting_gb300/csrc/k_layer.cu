@@ -9,12 +9,16 @@
 // max-subtract / exp / divide).  Page "cortiq-engine 0.8.75 —
 // src/gpu_wgpu/dflash_dev.rs": the same steps as the kernels `dflash_rms`,
 // `dflash_qk`, `dflash_attn`, `dflash_silu`.
+#include <cooperative_groups.h>
+
 #include <algorithm>
 
 #include "common.cuh"
 #include "kernels.cuh"
 
 namespace dflash {
+
+namespace cg = cooperative_groups;
 
 // int8 code of v under scale sx (sx > 0)
 DF_DEV int8_t code_of(float v, float sx) {
@@ -86,10 +90,103 @@ __global__ void __launch_bounds__(kRowThreads) rms_rows_kernel(const float* __re
     if (threadIdx.x == 0) out_scale[i] = sx;
 }
 
+// The same in one read: the row sits in registers (NV float4 per thread) from
+// the load to the codes.  Rows must be 16-byte aligned, n % 4 == 0 and
+// n <= 4 * NV * kRowThreads.
+DF_DEV bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+DF_DEV float amax4(float4 v) { return fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))); }
+DF_DEV uint32_t codes4(float4 v, float sx) {
+    if (!(sx > 0.f)) return 0u;
+    const uint32_t a = (uint8_t)code_of(v.x, sx), b = (uint8_t)code_of(v.y, sx);
+    const uint32_t c = (uint8_t)code_of(v.z, sx), d = (uint8_t)code_of(v.w, sx);
+    return a | (b << 8) | (c << 16) | (d << 24);
+}
+
+template <int NV>
+__global__ void __launch_bounds__(kRowThreads) rms_rows_reg_kernel(const float* __restrict__ src, int ld_src, RowMap map,
+                                                                   int n, const float* __restrict__ w, float eps,
+                                                                   float* __restrict__ out_f32, int ld_out,
+                                                                   int8_t* __restrict__ out_codes,
+                                                                   float* __restrict__ out_scale, int ld_codes,
+                                                                   float* zero_buf, int64_t zero_n) {
+    __shared__ float red[33];
+    pdl_trigger();
+    pdl_wait();
+    zero_side(zero_buf, zero_n);
+    const int i = blockIdx.x;
+    const int srow = (i / map.per) * map.stride + map.skip + (i % map.per);
+    const float4* x4 = reinterpret_cast<const float4*>(src + (int64_t)srow * ld_src);
+    const int n4 = n / 4;
+    float4 v[NV];
+    float ss = 0.f;
+#pragma unroll
+    for (int u = 0; u < NV; ++u) {
+        const int c = threadIdx.x + u * kRowThreads;
+        v[u] = c < n4 ? x4[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+        ss = fmaf(v[u].x, v[u].x, ss);
+        ss = fmaf(v[u].y, v[u].y, ss);
+        ss = fmaf(v[u].z, v[u].z, ss);
+        ss = fmaf(v[u].w, v[u].w, ss);
+    }
+    if (w) {
+        ss = row_reduce<false>(ss, red);
+        const float s = 1.f / sqrtf(ss / (float)n + eps);
+        const float4* w4 = reinterpret_cast<const float4*>(w);
+#pragma unroll
+        for (int u = 0; u < NV; ++u) {
+            const int c = threadIdx.x + u * kRowThreads;
+            if (c < n4) {
+                const float4 g = w4[c];
+                v[u] = make_float4(v[u].x * s * g.x, v[u].y * s * g.y, v[u].z * s * g.z, v[u].w * s * g.w);
+            }
+        }
+    }
+    if (out_f32) {
+        float4* o4 = reinterpret_cast<float4*>(out_f32 + (int64_t)i * ld_out);
+#pragma unroll
+        for (int u = 0; u < NV; ++u) {
+            const int c = threadIdx.x + u * kRowThreads;
+            if (c < n4) o4[c] = v[u];
+        }
+        return;
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int u = 0; u < NV; ++u) amax = fmaxf(amax, amax4(v[u]));  // lanes past n hold zeros
+    amax = row_reduce<true>(amax, red);
+    const float sx = __fdiv_rn(amax, 127.0f);
+    uint32_t* q4 = reinterpret_cast<uint32_t*>(out_codes + (int64_t)i * ld_codes);
+#pragma unroll
+    for (int u = 0; u < NV; ++u) {
+        const int c = threadIdx.x + u * kRowThreads;
+        if (c < n4) q4[c] = codes4(v[u], sx);
+    }
+    if (threadIdx.x == 0) out_scale[i] = sx;
+}
+
+static bool rows_fit_reg(int n, const void* src, int ld_src, const void* out_f32, int ld_out, const void* codes,
+                         int ld_codes, int max_n) {
+    auto al = [](const void* p, int a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; };
+    return n % 4 == 0 && n <= max_n && ld_src % 4 == 0 && al(src, 16) && (!out_f32 || (ld_out % 4 == 0 && al(out_f32, 16))) &&
+           (!codes || (ld_codes % 4 == 0 && al(codes, 4)));
+}
+
 int rms_rows(const float* src, int ld_src, RowMap map, int rows, int n, const float* w, float eps, float* out_f32,
              int ld_out, int8_t* out_codes, float* out_scale, int ld_codes, cudaStream_t st, float* zero_buf,
              int64_t zero_n) {
     if (rows <= 0) return 0;
+    const bool wal = !w || (reinterpret_cast<uintptr_t>(w) % 16) == 0;
+    if (wal && rows_fit_reg(n, src, ld_src, out_f32, ld_out, out_codes, ld_codes, 8 * 4 * kRowThreads)) {
+        const int nv = (n + 4 * kRowThreads - 1) / (4 * kRowThreads);
+        auto go = [&](auto kern) {
+            return (int)launch(kern, dim3(rows), dim3(kRowThreads), 0, st, src, ld_src, map, n, w, eps, out_f32, ld_out,
+                               out_codes, out_scale, ld_codes, zero_buf, zero_n);
+        };
+        if (nv <= 1) return go(rms_rows_reg_kernel<1>);
+        if (nv <= 2) return go(rms_rows_reg_kernel<2>);
+        if (nv <= 4) return go(rms_rows_reg_kernel<4>);
+        return go(rms_rows_reg_kernel<8>);
+    }
     return (int)launch(rms_rows_kernel, dim3(rows), dim3(kRowThreads), 0, st, src, ld_src, map, n, w, eps, out_f32,
                        ld_out, out_codes, out_scale, ld_codes, zero_buf, zero_n);
 }
@@ -250,22 +347,81 @@ __global__ void __launch_bounds__(kRowThreads) silu_mul_kernel(const float* __re
     if (threadIdx.x == 0) out_scale[r] = sx;
 }
 
+// The same in one read, the products kept in registers (NV float4 per thread).
+template <int NV>
+__global__ void __launch_bounds__(kRowThreads) silu_mul_reg_kernel(const float* __restrict__ gu, int ld_gu, int I,
+                                                                   float* __restrict__ out_f32, int ld_out,
+                                                                   int8_t* __restrict__ out_codes,
+                                                                   float* __restrict__ out_scale, int ld_codes) {
+    __shared__ float red[33];
+    pdl_trigger();
+    pdl_wait();
+    const int r = blockIdx.x;
+    const float4* g4 = reinterpret_cast<const float4*>(gu + (int64_t)r * ld_gu);
+    const float4* u4 = reinterpret_cast<const float4*>(gu + (int64_t)r * ld_gu + I);
+    const int n4 = I / 4;
+    float4 gv[NV], uv[NV];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int c = threadIdx.x + k * kRowThreads;
+        gv[k] = c < n4 ? g4[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+        uv[k] = c < n4 ? u4[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float4 a[NV];
+    float amax = 0.f;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        a[k] = make_float4(silu_f(gv[k].x) * uv[k].x, silu_f(gv[k].y) * uv[k].y, silu_f(gv[k].z) * uv[k].z,
+                           silu_f(gv[k].w) * uv[k].w);
+        amax = fmaxf(amax, amax4(a[k]));  // lanes past I: silu(0) * 0 = 0
+    }
+    if (out_f32) {
+        float4* o4 = reinterpret_cast<float4*>(out_f32 + (int64_t)r * ld_out);
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int c = threadIdx.x + k * kRowThreads;
+            if (c < n4) o4[c] = a[k];
+        }
+        return;
+    }
+    amax = row_reduce<true>(amax, red);
+    const float sx = __fdiv_rn(amax, 127.0f);
+    uint32_t* q4 = reinterpret_cast<uint32_t*>(out_codes + (int64_t)r * ld_codes);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int c = threadIdx.x + k * kRowThreads;
+        if (c < n4) q4[c] = codes4(a[k], sx);
+    }
+    if (threadIdx.x == 0) out_scale[r] = sx;
+}
+
 int silu_mul(const float* gu, int ld_gu, int rows, int I, float* out_f32, int ld_out, int8_t* out_codes,
              float* out_scale, int ld_codes, cudaStream_t st) {
     if (rows <= 0) return 0;
+    if (rows_fit_reg(I, gu, ld_gu, out_f32, ld_out, out_codes, ld_codes, 4 * 4 * kRowThreads) &&
+        (reinterpret_cast<uintptr_t>(gu + I) % 16) == 0) {
+        const int nv = (I + 4 * kRowThreads - 1) / (4 * kRowThreads);
+        auto go = [&](auto kern) {
+            return (int)launch(kern, dim3(rows), dim3(kRowThreads), 0, st, gu, ld_gu, I, out_f32, ld_out, out_codes,
+                               out_scale, ld_codes);
+        };
+        if (nv <= 1) return go(silu_mul_reg_kernel<1>);
+        if (nv <= 2) return go(silu_mul_reg_kernel<2>);
+        return go(silu_mul_reg_kernel<4>);
+    }
     return (int)launch(silu_mul_kernel, dim3(rows), dim3(kRowThreads), 0, st, gu, ld_gu, I, out_f32, ld_out,
                        out_codes, out_scale, ld_codes);
 }
 
 // ------------------------------------------------------------------ attention
-// One CTA per (key split, kv head x query tile, sequence).  The query tile is
-// up to 64 (q head of the group, block row) pairs; keys are the context rows
-// [lo, lo + n) then the block's rows; a split keeps an online softmax (running
-// max in the log2 domain, running sum, unnormalised output) and writes it to
-// `part`; attn_combine merges the splits.
-constexpr int kAttnQ = 64;   // query vectors of a CTA: 4 warps x 16
-constexpr int kAttnK = 32;   // keys per tile
-constexpr int kAttnWarps = 4;
+// The key range of one (sequence, kv head, query tile) is split over the CTAs
+// of a thread-block cluster; each CTA runs an online softmax over its keys
+// and the cluster merges the CTAs' partial results through distributed
+// shared memory, so that nothing but y is written to global memory.
+constexpr int kAttnQ = 64;           // query vectors of a CTA: 4 query warps x 16
+constexpr int kAttnK = 32;           // keys of a tile; the CTA's two key halves take a tile each
+constexpr int kAttnWarps = 8;        // 4 query warps x 2 key halves
+constexpr int kAttnMaxCluster = 16;  // CTAs of a cluster (non-portable above 8)
 
 // f32 -> (hi, lo) f16 pair with hi + lo = x to about 2^-22 relative
 DF_DEV void split_f16(float x, __half& hi, __half& lo) {
@@ -302,51 +458,61 @@ DF_DEV void split_store4(float4 v, __half* hi, __half* lo) {
 template <int HD>
 struct AttnSmem {
     static constexpr int LD = HD + 8;  // halves: 16-byte row pad, conflict-free ldmatrix
+    static constexpr int PART = HD + 4;  // floats of a partial row: m, l, -, -, acc[HD]
     __half qh[kAttnQ][LD], ql[kAttnQ][LD];
-    __half kh[kAttnK][LD], kl[kAttnK][LD];
-    __half vh[kAttnK][LD], vl[kAttnK][LD];
+    // [key half][key][dim]; after the key loop this area holds the partial
+    // rows [key half][query][PART] that the cluster merges
+    __half kh[2][kAttnK][LD], kl[2][kAttnK][LD];
+    __half vh[2][kAttnK][LD], vl[2][kAttnK][LD];
+    DF_DEV float* part() { return reinterpret_cast<float*>(&kh[0][0][0]); }
 };
 
-// One CTA per (key split, kv head x query tile, sequence).  The query tile is
-// up to 64 (q head of the group, block row) pairs, 16 per warp; keys are the
-// context rows [lo, lo + n) then the block's rows.  Scores and values go
-// through f16 tensor-core MMAs as hi/lo splits (q.k = qh.kh + qh.kl + ql.kh,
-// likewise p.v), which keeps f32-level accuracy; the softmax is online in f32
-// (running max in the log2 domain, running sum, unnormalised output), written
-// per split to `part` for attn_combine.
+// CTA (split sp of the cluster, kv head x query tile, sequence).  The query
+// tile is up to 64 (q head of the group, block row) pairs, 16 per query warp;
+// the CTA's keys (context rows [lo, lo + n) then the block's rows, its share
+// of them) go by in 64-key steps, keys 0..31 of a step to key half 0 and keys
+// 32..63 to key half 1.  Scores and values go through f16 tensor-core MMAs as
+// hi/lo splits (q.k = qh.kh + qh.kl + ql.kh, likewise p.v), which keeps
+// f32-level accuracy; the softmax is online in f32 (running max in the log2
+// domain, running sum, unnormalised output).  At the end every query row has
+// 2 x nsplit partial results in the cluster's shared memory; CTA sp merges
+// rows sp, sp + nsplit, ... and writes them to y.
 template <int HD>
-__global__ void __launch_bounds__(kAttnWarps * 32) attn_split_kernel(const float* __restrict__ qkv, int ld,
-                                                                     int block_len, const AttnSeq* __restrict__ seqs,
-                                                                     int nq, int nkv, int qtiles, int nsplit,
-                                                                     float scale_log2, float* __restrict__ part) {
+__global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const float* __restrict__ qkv, int ld,
+                                                                       int block_len, const AttnSeq* __restrict__ seqs,
+                                                                       int nq, int nkv, int qtiles, int nsplit,
+                                                                       float scale_log2, float* __restrict__ y) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     AttnSmem<HD>& sm = *reinterpret_cast<AttnSmem<HD>*>(smem_raw);
-    constexpr int LD = AttnSmem<HD>::LD;
+    constexpr int PART = AttnSmem<HD>::PART;
     constexpr int NT = HD / 8;   // n8 tiles of the output
     constexpr int KS = HD / 16;  // k16 steps of the scores
-    const int sp = blockIdx.x, g = blockIdx.y / qtiles, qt = blockIdx.y % qtiles, s = blockIdx.z;
+    constexpr int kThreads = kAttnWarps * 32;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int sp = (int)cluster.block_rank(), g = blockIdx.y / qtiles, qt = blockIdx.y % qtiles, s = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
+    const int qw = warp & 3, half = warp >> 2;
     pdl_trigger();
     pdl_wait();
     const AttnSeq sq = seqs[s];
     const int rep = nq / nkv, mq = rep * block_len;
     const int total = sq.n + block_len;
-    // this sequence's keys in nsplit splits of a multiple of the key tile
-    const int keys_per_split = ((total + nsplit - 1) / nsplit + kAttnK - 1) / kAttnK * kAttnK;
-    const int j0 = sp * keys_per_split, j1 = min(total, j0 + keys_per_split);
+    // this sequence's keys in nsplit equal shares (the last step of a share may be partial)
+    const int kps = (total + nsplit - 1) / nsplit;
+    const int j0 = sp * kps, j1 = min(total, j0 + kps);
     const int64_t row0 = (int64_t)s * block_len;
 
-    // Operands move as float4: the query tile and each key/value tile are read
-    // with all of a thread's loads in flight at once, and the next key tile is
+    // Operands move as float4: the query tile and each 64-key step are read
+    // with all of a thread's loads in flight at once, and the next step is
     // fetched into registers while the current one is multiplied.
     constexpr int D4 = HD / 4;
-    constexpr int NQ4 = kAttnQ * D4 / (kAttnWarps * 32), NK4 = kAttnK * D4 / (kAttnWarps * 32);
-    static_assert(NQ4 * kAttnWarps * 32 == kAttnQ * D4 && NK4 * kAttnWarps * 32 == kAttnK * D4, "tile split");
+    constexpr int NQ4 = kAttnQ * D4 / kThreads, NK4 = 2 * kAttnK * D4 / kThreads;
+    static_assert(NQ4 * kThreads == kAttnQ * D4 && NK4 * kThreads == 2 * kAttnK * D4, "tile split");
     float4 pk[NK4], pv[NK4];
     auto load_kv = [&](int jt) {
 #pragma unroll
         for (int u = 0; u < NK4; ++u) {
-            const int i = tid + u * kAttnWarps * 32, kr = i / D4, d = (i % D4) * 4, j = jt + kr;
+            const int i = tid + u * kThreads, kr = i / D4, d = (i % D4) * 4, j = jt + kr;
             float4 kk = make_float4(0.f, 0.f, 0.f, 0.f), vv = kk;
             if (j < j1) {
                 if (j < sq.n) {
@@ -367,7 +533,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_split_kernel(const float
         float4 qv[NQ4];
 #pragma unroll
         for (int u = 0; u < NQ4; ++u) {
-            const int i = tid + u * kAttnWarps * 32, qr = i / D4, d = (i % D4) * 4, ii = qt * kAttnQ + qr;
+            const int i = tid + u * kThreads, qr = i / D4, d = (i % D4) * 4, ii = qt * kAttnQ + qr;
             qv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (ii < mq) {
                 const int head = g * rep + ii / block_len, r = ii % block_len;
@@ -377,7 +543,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_split_kernel(const float
         if (j0 < j1) load_kv(j0);
 #pragma unroll
         for (int u = 0; u < NQ4; ++u) {
-            const int i = tid + u * kAttnWarps * 32, qr = i / D4, d = (i % D4) * 4;
+            const int i = tid + u * kThreads, qr = i / D4, d = (i % D4) * 4;
             split_store4(qv[u], &sm.qh[qr][d], &sm.ql[qr][d]);
         }
     }
@@ -386,20 +552,23 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_split_kernel(const float
 #pragma unroll
     for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-    const int qbase = warp * 16;
+    const int qbase = qw * 16;
     // ldmatrix row addresses: A (queries x dims) and B (keys x dims) operands
     const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8, lcol = (lane >> 4) * 8;
 
-    for (int jt = j0; jt < j1; jt += kAttnK) {
-        __syncthreads();  // the previous tile's keys and values are no longer read
+    for (int jt = j0; jt < j1; jt += 2 * kAttnK) {
+        __syncthreads();  // the previous step's keys and values are no longer read
 #pragma unroll
         for (int u = 0; u < NK4; ++u) {
-            const int i = tid + u * kAttnWarps * 32, kr = i / D4, d = (i % D4) * 4;
-            split_store4(pk[u], &sm.kh[kr][d], &sm.kl[kr][d]);
-            split_store4(pv[u], &sm.vh[kr][d], &sm.vl[kr][d]);
+            const int i = tid + u * kThreads, kr = i / D4, d = (i % D4) * 4;
+            const int hf = kr / kAttnK, k = kr % kAttnK;
+            split_store4(pk[u], &sm.kh[hf][k][d], &sm.kl[hf][k][d]);
+            split_store4(pv[u], &sm.vh[hf][k][d], &sm.vl[hf][k][d]);
         }
         __syncthreads();
-        if (jt + kAttnK < j1) load_kv(jt + kAttnK);
+        if (jt + 2 * kAttnK < j1) load_kv(jt + 2 * kAttnK);
+        const int kt = jt + half * kAttnK;  // first key of this warp's tile
+        if (kt >= j1) continue;              // warp-uniform: nothing of this half in the last step
         // scores: 16 queries x 32 keys per warp
         float sc[4][4];
 #pragma unroll
@@ -414,8 +583,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_split_kernel(const float
                 uint32_t bh[4], bl[4];
                 // matrices: (keys +0..7, dims +0..7), (keys +0..7, dims +8..15), (keys +8..15, ...), ...
                 const int brow = nb * 16 + (lane & 7) + (lane >> 4) * 8, bcol = k * 16 + ((lane >> 3) & 1) * 8;
-                ldsm_x4(bh, &sm.kh[brow][bcol]);
-                ldsm_x4(bl, &sm.kl[brow][bcol]);
+                ldsm_x4(bh, &sm.kh[half][brow][bcol]);
+                ldsm_x4(bl, &sm.kl[half][brow][bcol]);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     float* c = sc[nb * 2 + h];
@@ -436,7 +605,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_split_kernel(const float
         for (int n = 0; n < 4; ++n)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int key = jt + n * 8 + 2 * tq + (e & 1);
+                const int key = kt + n * 8 + 2 * tq + (e & 1);
                 const float v = key < j1 ? sc[n][e] * scale_log2 : -INFINITY;
                 sc[n][e] = v;
                 tmax[e >> 1] = fmaxf(tmax[e >> 1], v);
@@ -465,11 +634,11 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_split_kernel(const float
             split_f16(p[1], h1, l1);
             split_f16(p[2], h2, l2);
             split_f16(p[3], h3, l3);
-            const int kstep = n >> 1, half = n & 1;  // keys 8n..8n+7 -> k16 step n/2, column half n%2
-            ph[kstep][half * 2 + 0] = pack_half2(h0, h1);  // row gq
-            ph[kstep][half * 2 + 1] = pack_half2(h2, h3);  // row gq + 8
-            pl[kstep][half * 2 + 0] = pack_half2(l0, l1);
-            pl[kstep][half * 2 + 1] = pack_half2(l2, l3);
+            const int kstep = n >> 1, hcol = n & 1;  // keys 8n..8n+7 -> k16 step n/2, column half n%2
+            ph[kstep][hcol * 2 + 0] = pack_half2(h0, h1);  // row gq
+            ph[kstep][hcol * 2 + 1] = pack_half2(h2, h3);  // row gq + 8
+            pl[kstep][hcol * 2 + 0] = pack_half2(l0, l1);
+            pl[kstep][hcol * 2 + 1] = pack_half2(l2, l3);
         }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -495,8 +664,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_split_kernel(const float
                 uint32_t bh[4], bl[4];
                 // .trans matrices: (keys +0..7, dims +0..7), (keys +8..15, dims +0..7), (keys +0..7, dims +8..15), ...
                 const int vrow = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, vcol = jb * 16 + (lane >> 4) * 8;
-                ldsm_x4_t(bh, &sm.vh[vrow][vcol]);
-                ldsm_x4_t(bl, &sm.vl[vrow][vcol]);
+                ldsm_x4_t(bh, &sm.vh[half][vrow][vcol]);
+                ldsm_x4_t(bl, &sm.vl[half][vrow][vcol]);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     float* c = o[jb * 2 + h];
@@ -512,12 +681,11 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_split_kernel(const float
             }
         }
     }
-    // partial: [s][g][qt][sp][query row] -> {m, l, -, -, acc[HD]} (16-byte aligned)
-    const int64_t e0 = (((int64_t)s * nkv + g) * qtiles + qt) * nsplit + sp;
+    __syncthreads();  // every warp is done with the key/value tiles: their area takes the partial rows
+    float* part = sm.part();
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-        const int qrow = qbase + gq + 8 * h;
-        float* out = part + (e0 * kAttnQ + qrow) * (HD + 4);
+        float* out = part + (half * kAttnQ + qbase + gq + 8 * h) * PART;
         if (tq == 0) {
             out[0] = m_run[h];
             out[1] = l_run[h];
@@ -525,90 +693,126 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_split_kernel(const float
 #pragma unroll
         for (int j = 0; j < NT; ++j) *reinterpret_cast<float2*>(out + 4 + j * 8 + 2 * tq) = make_float2(o[j][2 * h], o[j][2 * h + 1]);
     }
-}
+    cluster.sync();  // every CTA's partial rows are written
 
-// One warp per (sequence, block row, q head): merge the splits, divide by the sum.
-template <int HD>
-__global__ void attn_combine_kernel(const float* __restrict__ part, int n_seqs, int block_len, int nq, int nkv,
-                                    int qtiles, int nsplit, float* __restrict__ y) {
-    const int64_t wid = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
-    pdl_trigger();
-    pdl_wait();
-    if (wid >= (int64_t)n_seqs * block_len * nq) return;
-    const int lane = threadIdx.x & 31;
-    const int h = (int)(wid % nq), r = (int)((wid / nq) % block_len), s = (int)(wid / ((int64_t)nq * block_len));
-    const int rep = nq / nkv, g = h / rep, ii = (h % rep) * block_len + r;
-    const int qt = ii / kAttnQ, qrow = ii % kAttnQ;
-    const int64_t base = (((int64_t)s * nkv + g) * qtiles + qt) * nsplit;
-    float M = -INFINITY;
-    for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, part[((base + sp) * kAttnQ + qrow) * (HD + 4)]);
-    constexpr int E = HD / 32;
-    float o[E];
+    // merge: one warp per query row; lane k < 2 nsplit reads partial k's
+    // running max and sum (CTA k / 2, key half k % 2), then every lane sums
+    // its VEC dims over the partials
+    constexpr int VEC = HD / 32;
+    const int nparts = 2 * nsplit;
+    for (int qr = sp + warp * nsplit; qr < kAttnQ; qr += kAttnWarps * nsplit) {
+        const int ii = qt * kAttnQ + qr;
+        if (ii >= mq) break;  // rows grow with qr: none further (warp-uniform)
+        float mk = -INFINITY, lk = 0.f;
+        if (lane < nparts) {
+            const float* src = cluster.map_shared_rank(part, lane >> 1) + ((lane & 1) * kAttnQ + qr) * PART;
+            mk = src[0];
+            lk = src[1];
+        }
+        const float M = warp_max(mk);
+        const float wk = (mk == -INFINITY) ? 0.f : exp2f(mk - M);
+        const float L = warp_sum(lk * wk);
+        float acc[VEC];
 #pragma unroll
-    for (int j = 0; j < E; ++j) o[j] = 0.f;
-    float L = 0.f;
-    for (int sp = 0; sp < nsplit; ++sp) {
-        const float* pp = part + ((base + sp) * kAttnQ + qrow) * (HD + 4);
-        const float m = pp[0];
-        if (m == -INFINITY) continue;
-        const float w = exp2f(m - M);
-        L = fmaf(pp[1], w, L);
+        for (int j = 0; j < VEC; ++j) acc[j] = 0.f;
+#pragma unroll 8
+        for (int k = 0; k < nparts; ++k) {
+            const float w = __shfl_sync(0xffffffffu, wk, k);
+            const float* src = cluster.map_shared_rank(part, k >> 1) + ((k & 1) * kAttnQ + qr) * PART + 4 + VEC * lane;
+            if constexpr (VEC == 4) {
+                const float4 a = *reinterpret_cast<const float4*>(src);
+                acc[0] = fmaf(a.x, w, acc[0]);
+                acc[1] = fmaf(a.y, w, acc[1]);
+                acc[2] = fmaf(a.z, w, acc[2]);
+                acc[3] = fmaf(a.w, w, acc[3]);
+            } else {
+                const float2 a = *reinterpret_cast<const float2*>(src);
+                acc[0] = fmaf(a.x, w, acc[0]);
+                acc[1] = fmaf(a.y, w, acc[1]);
+            }
+        }
+        const int head = g * rep + ii / block_len, r = ii % block_len;
+        float* dst = y + (row0 + r) * ((int64_t)nq * HD) + (int64_t)head * HD + VEC * lane;
 #pragma unroll
-        for (int j = 0; j < E; ++j) o[j] = fmaf(pp[4 + lane + 32 * j], w, o[j]);
+        for (int j = 0; j < VEC; ++j) dst[j] = acc[j] / L;
     }
-    float* dst = y + ((int64_t)s * block_len + r) * ((int64_t)nq * HD) + (int64_t)h * HD;
-#pragma unroll
-    for (int j = 0; j < E; ++j) dst[lane + 32 * j] = o[j] / L;
+    cluster.sync();  // no CTA leaves while another may still read its partial rows
 }
 
-// Splits of the keys: enough CTAs to cover the SMs twice, no more splits than
-// key tiles of the longest context `max_ctx` can have (callers pass the
-// sequences' capacity, so that the launch does not change as contexts grow).
-static void attn_plan(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int num_sms, int* qtiles, int* nsplit) {
+// Cluster size (the key splits).  max_active[c]: clusters of c CTAs the
+// device holds at once.  With few (sequence, kv head, query tile) units the
+// largest cluster whose units all run in one wave, capped by the 64-key steps
+// of the longest context `max_ctx` (callers pass the sequences' capacity, so
+// that the launch does not change as contexts grow); with many units, enough
+// splits to cover the SMs.
+static void attn_plan(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int num_sms, const int* max_active,
+                      int* qtiles, int* nsplit) {
     const int mq = (nq / nkv) * block_len;
     *qtiles = (mq + kAttnQ - 1) / kAttnQ;
     const int total = max_ctx + block_len;
-    const int max_split = (total + kAttnK - 1) / kAttnK;
+    const int max_split = std::max(1, (total + 2 * kAttnK - 1) / (2 * kAttnK));
     const int units = nkv * *qtiles * n_seqs;
-    *nsplit = std::max(1, std::min(max_split, (2 * num_sms + units - 1) / units));
+    const int want = std::min(max_split, std::max(1, (num_sms + units - 1) / units));
+    int best = 1;
+    for (int c = 1; c <= std::min(want, kAttnMaxCluster); ++c)
+        if (max_active[c] >= std::min(units, max_active[1])) best = c;
+    *nsplit = best;
 }
 
-int64_t attn_scratch_floats(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int hd, int num_sms) {
-    int qt, ns;
-    attn_plan(n_seqs, block_len, max_ctx, nq, nkv, num_sms, &qt, &ns);
-    return (int64_t)n_seqs * nkv * qt * ns * kAttnQ * (hd + 4);
+int64_t attn_scratch_floats(int, int, int, int, int, int, int) { return 0; }
+
+// How many clusters of c = 1..16 CTAs of attn_cluster_kernel<HD> the device
+// holds at once (0 where it cannot place one), found once per process.
+template <int HD>
+static const int* attn_cluster_table(cudaStream_t st) {
+    static int table[kAttnMaxCluster + 1] = {0};
+    static bool done = false;
+    if (done) return table;
+    cudaFuncSetAttribute(attn_cluster_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)sizeof(AttnSmem<HD>));
+    cudaFuncSetAttribute(attn_cluster_kernel<HD>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    for (int c = 1; c <= kAttnMaxCluster; ++c) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(c, 1, 1);
+        cfg.blockDim = dim3(kAttnWarps * 32);
+        cfg.dynamicSmemBytes = sizeof(AttnSmem<HD>);
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = c;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, attn_cluster_kernel<HD>, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+        table[c] = n;
+    }
+    if (table[1] < 1) table[1] = 1;
+    done = true;
+    return table;
 }
 
 template <int HD>
 static int attention_hd(const float* qkv, int ld, int n_seqs, int block_len, const AttnSeq* seqs_dev, int max_ctx,
-                        int nq, int nkv, float scale, float* part, int64_t part_floats, float* y, int num_sms,
-                        cudaStream_t st) {
+                        int nq, int nkv, float scale, float* y, int num_sms, cudaStream_t st) {
+    const int* table = attn_cluster_table<HD>(st);
     int qtiles, nsplit;
-    attn_plan(n_seqs, block_len, max_ctx, nq, nkv, num_sms, &qtiles, &nsplit);
-    if ((int64_t)n_seqs * nkv * qtiles * nsplit * kAttnQ * (HD + 4) > part_floats) return (int)cudaErrorInvalidValue;
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(attn_split_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)sizeof(AttnSmem<HD>));
-        attr = true;
-    }
+    attn_plan(n_seqs, block_len, max_ctx, nq, nkv, num_sms, table, &qtiles, &nsplit);
     const float scale_log2 = scale * 1.4426950408889634f;
     dim3 grid(nsplit, nkv * qtiles, n_seqs);
-    cudaError_t e = launch(attn_split_kernel<HD>, grid, dim3(kAttnWarps * 32), sizeof(AttnSmem<HD>), st, qkv, ld, block_len,
-                           seqs_dev, nq, nkv, qtiles, nsplit, scale_log2, part);
-    if (e != cudaSuccess) return (int)e;
-    const int64_t warps = (int64_t)n_seqs * block_len * nq;
-    return (int)launch(attn_combine_kernel<HD>, dim3((unsigned)((warps * 32 + 255) / 256)), dim3(256), 0, st, part,
-                       n_seqs, block_len, nq, nkv, qtiles, nsplit, y);
+    return (int)launch_cluster(attn_cluster_kernel<HD>, grid, dim3(kAttnWarps * 32), sizeof(AttnSmem<HD>), st, nsplit,
+                               qkv, ld, block_len, seqs_dev, nq, nkv, qtiles, nsplit, scale_log2, y);
 }
 
 int attention(const float* qkv, int ld, int n_seqs, int block_len, const AttnSeq* seqs_dev, int max_ctx, int nq,
-              int nkv, int hd, float scale, float* part, int64_t part_floats, float* y, int num_sms, cudaStream_t st) {
+              int nkv, int hd, float scale, float*, int64_t, float* y, int num_sms, cudaStream_t st) {
     if (hd == 128)
-        return attention_hd<128>(qkv, ld, n_seqs, block_len, seqs_dev, max_ctx, nq, nkv, scale, part, part_floats, y,
-                                 num_sms, st);
-    return attention_hd<64>(qkv, ld, n_seqs, block_len, seqs_dev, max_ctx, nq, nkv, scale, part, part_floats, y,
-                            num_sms, st);
+        return attention_hd<128>(qkv, ld, n_seqs, block_len, seqs_dev, max_ctx, nq, nkv, scale, y, num_sms, st);
+    return attention_hd<64>(qkv, ld, n_seqs, block_len, seqs_dev, max_ctx, nq, nkv, scale, y, num_sms, st);
 }
 
 }  // namespace dflash

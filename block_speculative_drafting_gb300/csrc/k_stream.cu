@@ -24,7 +24,7 @@ constexpr uint64_t kWaitLimit = 1000000000ull;  // ns an mbarrier wait may take 
 
 // ------------------------------------------------------------------ 4-bit
 // Each warp streams its own contiguous share of the CTA's span through a
-// private ring of one-super-chunk slots (its lane 0 issues the bulk copies and
+// private ring of two-super-chunk slots (its lane 0 issues the bulk copies and
 // refills a slot as soon as the warp has read it), accumulates consecutive
 // k-steps of a 64-row group in registers, and adds a group's 16 x 64 partial
 // sums, times the rows' activation scales, straight into y when it moves to
@@ -33,7 +33,8 @@ constexpr uint64_t kWaitLimit = 1000000000ull;  // ns an mbarrier wait may take 
 constexpr int kQ4Warps = 16;
 constexpr int kQ4Threads = kQ4Warps * 32;
 constexpr int kQ4SC = 4 * kQ4Chunk;  // super-chunk: 4 tiles x one k-step
-constexpr int kQ4WarpSlots = 4;      // ring slots per warp, one super-chunk each
+constexpr int kQ4SlotSC = 2;         // super-chunks per ring slot (one bulk copy)
+constexpr int kQ4WarpSlots = 2;      // ring slots per warp
 constexpr int kQ4ActPad = 32;        // halves of row pad: conflict-free 16-byte B-fragment loads
 constexpr int kQ4BarBytes = 1024;    // the warps' mbarriers, ahead of the ring
 
@@ -79,8 +80,8 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
     extern __shared__ __align__(128) unsigned char sm[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint64_t* full = reinterpret_cast<uint64_t*>(sm) + warp * kQ4WarpSlots;
-    unsigned char* ring = sm + kQ4BarBytes + warp * kQ4WarpSlots * kQ4SC;
-    __half* act = reinterpret_cast<__half*>(sm + kQ4BarBytes + kQ4Warps * kQ4WarpSlots * kQ4SC);
+    unsigned char* ring = sm + kQ4BarBytes + warp * (kQ4WarpSlots * kQ4SlotSC * kQ4SC);
+    __half* act = reinterpret_cast<__half*>(sm + kQ4BarBytes + kQ4Warps * (kQ4WarpSlots * kQ4SlotSC * kQ4SC));
     const int kbc = L.kb * kQ4KStep;  // columns of a K-block
     const int ldact = kbc + kQ4ActPad;
 
@@ -88,20 +89,22 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
     const int64_t span = sg.hi - sg.lo;
     const int64_t wlo = sg.lo + span * warp / kQ4Warps;
     const int n = (int)(sg.lo + span * (warp + 1) / kQ4Warps - wlo);  // this warp's super-chunks
+    const int nslots = (n + kQ4SlotSC - 1) / kQ4SlotSC;
     const uint8_t* src = wp + (sg.base + wlo) * kQ4SC;
 
     pdl_trigger();
     // the first slots go out before the previous kernel has finished: weights do not depend on it
     int issued = 0;
-    auto issue = [&](int i) {
-        const int slot = i % kQ4WarpSlots;
-        mbar_arrive_expect_tx(&full[slot], kQ4SC);
-        bulk_g2s(ring + slot * kQ4SC, src + (int64_t)i * kQ4SC, kQ4SC, &full[slot]);
+    auto issue = [&](int j) {
+        const int slot = j % kQ4WarpSlots;
+        const uint32_t bytes = (uint32_t)min(kQ4SlotSC, n - j * kQ4SlotSC) * kQ4SC;
+        mbar_arrive_expect_tx(&full[slot], bytes);
+        bulk_g2s(ring + slot * (kQ4SlotSC * kQ4SC), src + (int64_t)j * (kQ4SlotSC * kQ4SC), bytes, &full[slot]);
     };
     if (lane == 0) {
         for (int i = 0; i < kQ4WarpSlots; ++i) mbar_init(&full[i], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        for (; issued < min(kQ4WarpSlots, n); ++issued) issue(issued);
+        for (; issued < min(kQ4WarpSlots, nslots); ++issued) issue(issued);
     }
 
     pdl_wait();
@@ -157,32 +160,14 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
                 }
     };
 
-    const int kb = L.kb;
-    int ks = (int)(wlo % kb), grp = (int)(wlo / kb), cur = grp;
-    int i = 0;
-    bool ok = true;
-    for (; i < n; ++i) {
-        const int slot = i % kQ4WarpSlots;
-        // ok is warp-uniform after the vote, so the warp leaves the loop whole
-        ok = __all_sync(0xffffffffu, mbar_wait(&full[slot], (i / kQ4WarpSlots) & 1, kWaitLimit));
-        if (!ok) break;
-        if (grp != cur) {
-            dump(cur);
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) acc[r][h][e] = 0.f;
-            cur = grp;
-        }
+    // one super-chunk at scp: k-step ks of group grp
+    auto sc_step = [&](const unsigned char* scp, int ks) {
         uint4 bq[2][2];  // [group][row half]: 8 halves = the two k16 B fragments
 #pragma unroll
         for (int gi = 0; gi < 2; ++gi) {
             bq[gi][0] = *reinterpret_cast<const uint4*>(a_lo + ks * kQ4KStep + gi * 32);
             bq[gi][1] = *reinterpret_cast<const uint4*>(a_hi + ks * kQ4KStep + gi * 32);
         }
-        const unsigned char* scp = ring + slot * kQ4SC;
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const uint4 wv = *reinterpret_cast<const uint4*>(scp + r * kQ4Chunk + lane * 16);
@@ -211,15 +196,42 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
                 acc[r][1][3] = fmaf(sc.y, d1[3], acc[r][1][3]);
             }
         }
-        // every lane has read the slot: refill it with the super-chunk S ahead
+    };
+
+    const int kb = L.kb;
+    int ks = (int)(wlo % kb), grp = (int)(wlo / kb), cur = grp;
+    int j = 0;
+    bool ok = true;
+    for (; j < nslots; ++j) {
+        const int slot = j % kQ4WarpSlots;
+        // ok is warp-uniform after the vote, so the warp leaves the loop whole
+        ok = __all_sync(0xffffffffu, mbar_wait(&full[slot], (j / kQ4WarpSlots) & 1, kWaitLimit));
+        if (!ok) break;
+        const unsigned char* sb = ring + slot * (kQ4SlotSC * kQ4SC);
+#pragma unroll
+        for (int u = 0; u < kQ4SlotSC; ++u) {
+            if (u > 0 && j * kQ4SlotSC + u >= n) break;  // the warp's last slot may be short (uniform)
+            if (grp != cur) {
+                dump(cur);
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc[r][h][e] = 0.f;
+                cur = grp;
+            }
+            sc_step(sb + u * kQ4SC, ks);
+            if (++ks == kb) {
+                ks = 0;
+                ++grp;
+            }
+        }
+        // every lane has read the slot: refill it with the slot kQ4WarpSlots ahead
         __syncwarp();
-        if (lane == 0 && issued < n) {
+        if (lane == 0 && issued < nslots) {
             fence_proxy_async_smem();
             issue(issued++);
-        }
-        if (++ks == kb) {
-            ks = 0;
-            ++grp;
         }
     }
     if (ok) {
@@ -228,14 +240,14 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
         // a wait gave up: record it, and let no copy still land in this CTA's memory after it exits
         if (lane == 0) {
             atomicExch(err, 1);
-            for (int j = i; j < issued; ++j)
-                mbar_wait(&full[j % kQ4WarpSlots], (j / kQ4WarpSlots) & 1, kWaitLimit);
+            for (int k = j; k < issued; ++k)
+                mbar_wait(&full[k % kQ4WarpSlots], (k / kQ4WarpSlots) & 1, kWaitLimit);
         }
     }
 }
 
 static size_t q4_stream_bytes(Q4Layout L) {
-    return (size_t)kQ4BarBytes + (size_t)kQ4Warps * kQ4WarpSlots * kQ4SC +
+    return (size_t)kQ4BarBytes + (size_t)kQ4Warps * kQ4WarpSlots * kQ4SlotSC * kQ4SC +
            (size_t)16 * (L.kb * kQ4KStep + kQ4ActPad) * sizeof(__half);
 }
 
@@ -260,7 +272,7 @@ int q4_stream(const uint8_t* packed, Q4Layout L, int tile0, int N, QAct x, int T
 // ------------------------------------------------------------------ head
 constexpr int kActPad = 32;     // bytes of row pad of the head's staged int8 codes
 constexpr int kHeadSlotSC = 8;  // super-chunks (k-steps of one group) per slot
-constexpr int kHeadSlots = 2;
+constexpr int kHeadSlots = 4;  // 4 x 32 KB of weights in flight per SM
 
 __global__ void __launch_bounds__(kStreamThreads, 1)
     head_stream_kernel(const int8_t* __restrict__ wp, const float* __restrict__ sw, int ngroups, int ksteps, int V,

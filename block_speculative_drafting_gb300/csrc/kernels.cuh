@@ -107,6 +107,27 @@ int kv_append(const float* kv, int n, int L, int nkv, int hd, const float* const
               float eps, const int64_t* pos_dev, float* const* kstore_dev, float* const* vstore_dev, int64_t cap,
               cudaStream_t st);
 // a = silu(g) * u for gu [rows][2I] (gate then up); f32 out or int8 codes.
+// The same with the grid in clusters of cluster_x CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                           int cluster_x, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)cluster_x;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 int silu_mul(const float* gu, int ld_gu, int rows, int I, float* out_f32, int ld_out, int8_t* out_codes,
              float* out_scale, int ld_codes, cudaStream_t st);
 
@@ -119,7 +140,9 @@ struct AttnSeq {
     int n;       // context rows read
 };
 // qkv [n_seqs*block_len][ld] (q, k, v of the block after norm and RoPE);
-// y [n_seqs*block_len][nq*hd].  `part` is scratch of attn_scratch_floats().
+// y [n_seqs*block_len][nq*hd].  `part` / part_floats: scratch of
+// attn_scratch_floats() floats (none at present: the key splits merge in
+// distributed shared memory).
 // max_ctx: the largest context any sequence of the call may hold (its
 // capacity); the launch depends on it, each CTA's key range on the actual n.
 int attention(const float* qkv, int ld, int n_seqs, int block_len, const AttnSeq* seqs_dev, int max_ctx, int nq,

@@ -330,7 +330,8 @@ DFLASH_API int dflash_debug_attention(dflash_model* model, dflash_seq* const* se
  * capture, under a framework that owns all device memory through its own
  * pool, or in a loop that must never block in the allocator).
  * Same arguments, layouts and result as dflash_debug_attention.  Its scratch
- * (the split partials and the context views) is a fixed 16 MiB device array
+ * (the context views; the key splits merge in distributed shared memory and
+ * need no partials in global memory) is a fixed 16 MiB device array
  * inside this library, held by every GPU that loads the library until the
  * process exits; the call makes no cudaMalloc / cudaFree.  The first call on
  * a device looks up that array's device address (cudaGetSymbolAddress) and
@@ -338,8 +339,8 @@ DFLASH_API int dflash_debug_attention(dflash_model* model, dflash_seq* const* se
  * the one array and overwrites what the previous call left there, so calls
  * whose work overlaps on the GPU (other streams, other threads) race: order
  * them on one stream.  Errors: as dflash_debug_attention, and ERANGE when the
- * call needs more scratch than the array holds (more than 256 sequences, or
- * more than 4 Mi - 4096 floats of partials) -- nothing is launched then.
+ * call needs more scratch than the array holds (more than 256 sequences) --
+ * nothing is launched then.
  */
 DFLASH_API int dflash_attention_noalloc(dflash_model* model, dflash_seq* const* seqs, int32_t n_seqs, int32_t layer,
                                         const int64_t* anchor_pos, int32_t block_len, const float* qkv, float* y,
