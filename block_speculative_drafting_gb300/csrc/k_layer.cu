@@ -418,10 +418,13 @@ int silu_mul(const float* gu, int ld_gu, int rows, int I, float* out_f32, int ld
 // of a thread-block cluster; each CTA runs an online softmax over its keys
 // and the cluster merges the CTAs' partial results through distributed
 // shared memory, so that nothing but y is written to global memory.
-constexpr int kAttnQ = 64;           // query vectors of a CTA: 4 query warps x 16
-constexpr int kAttnK = 32;           // keys of a tile; the CTA's two key halves take a tile each
-constexpr int kAttnWarps = 8;        // 4 query warps x 2 key halves
-constexpr int kAttnMaxCluster = 16;  // CTAs of a cluster (non-portable above 8)
+constexpr int kAttnQW = 4;                     // query warps of a CTA, 16 query vectors each
+constexpr int kAttnKH = 2;                     // key lanes: warps that share a query warp's rows
+constexpr int kAttnQ = 16 * kAttnQW;           // query vectors of a CTA
+constexpr int kAttnK = 32;                     // keys of a tile; each key lane takes one tile per step
+constexpr int kAttnStep = kAttnKH * kAttnK;    // keys per step of the CTA
+constexpr int kAttnWarps = kAttnQW * kAttnKH;
+constexpr int kAttnMaxCluster = 32 / kAttnKH < 16 ? 32 / kAttnKH : 16;  // CTAs of a cluster (non-portable above 8)
 
 // f32 -> (hi, lo) f16 pair with hi + lo = x to about 2^-22 relative
 DF_DEV void split_f16(float x, __half& hi, __half& lo) {
@@ -460,22 +463,23 @@ struct AttnSmem {
     static constexpr int LD = HD + 8;  // halves: 16-byte row pad, conflict-free ldmatrix
     static constexpr int PART = HD + 4;  // floats of a partial row: m, l, -, -, acc[HD]
     __half qh[kAttnQ][LD], ql[kAttnQ][LD];
-    // [key half][key][dim]; after the key loop this area holds the partial
-    // rows [key half][query][PART] that the cluster merges
-    __half kh[2][kAttnK][LD], kl[2][kAttnK][LD];
-    __half vh[2][kAttnK][LD], vl[2][kAttnK][LD];
+    // [key lane][key][dim]; after the key loop this area holds the partial
+    // rows [key lane][query][PART] that the cluster merges
+    __half kh[kAttnKH][kAttnK][LD], kl[kAttnKH][kAttnK][LD];
+    __half vh[kAttnKH][kAttnK][LD], vl[kAttnKH][kAttnK][LD];
     DF_DEV float* part() { return reinterpret_cast<float*>(&kh[0][0][0]); }
 };
+static_assert(kAttnQW <= 4, "the partial rows must fit the key/value area");
 
 // CTA (split sp of the cluster, kv head x query tile, sequence).  The query
-// tile is up to 64 (q head of the group, block row) pairs, 16 per query warp;
-// the CTA's keys (context rows [lo, lo + n) then the block's rows, its share
-// of them) go by in 64-key steps, keys 0..31 of a step to key half 0 and keys
-// 32..63 to key half 1.  Scores and values go through f16 tensor-core MMAs as
+// tile is up to kAttnQ (q head of the group, block row) pairs, 16 per query
+// warp; the CTA's keys (context rows [lo, lo + n) then the block's rows, its
+// share of them) go by in steps of kAttnKH tiles of 32 keys, tile k of a step
+// to the warps of key lane k.  Scores and values go through f16 tensor-core MMAs as
 // hi/lo splits (q.k = qh.kh + qh.kl + ql.kh, likewise p.v), which keeps
 // f32-level accuracy; the softmax is online in f32 (running max in the log2
 // domain, running sum, unnormalised output).  At the end every query row has
-// 2 x nsplit partial results in the cluster's shared memory; CTA sp merges
+// kAttnKH x nsplit partial results in the cluster's shared memory; CTA sp merges
 // rows sp, sp + nsplit, ... and writes them to y.
 template <int HD>
 __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const float* __restrict__ qkv, int ld,
@@ -491,7 +495,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const flo
     cg::cluster_group cluster = cg::this_cluster();
     const int sp = (int)cluster.block_rank(), g = blockIdx.y / qtiles, qt = blockIdx.y % qtiles, s = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
-    const int qw = warp & 3, half = warp >> 2;
+    const int qw = warp % kAttnQW, half = warp / kAttnQW;  // query warp, key lane
     pdl_trigger();
     pdl_wait();
     const AttnSeq sq = seqs[s];
@@ -502,12 +506,12 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const flo
     const int j0 = sp * kps, j1 = min(total, j0 + kps);
     const int64_t row0 = (int64_t)s * block_len;
 
-    // Operands move as float4: the query tile and each 64-key step are read
+    // Operands move as float4: the query tile and each key step are read
     // with all of a thread's loads in flight at once, and the next step is
     // fetched into registers while the current one is multiplied.
     constexpr int D4 = HD / 4;
-    constexpr int NQ4 = kAttnQ * D4 / kThreads, NK4 = 2 * kAttnK * D4 / kThreads;
-    static_assert(NQ4 * kThreads == kAttnQ * D4 && NK4 * kThreads == 2 * kAttnK * D4, "tile split");
+    constexpr int NQ4 = kAttnQ * D4 / kThreads, NK4 = kAttnStep * D4 / kThreads;
+    static_assert(NQ4 * kThreads == kAttnQ * D4 && NK4 * kThreads == kAttnStep * D4, "tile split");
     float4 pk[NK4], pv[NK4];
     auto load_kv = [&](int jt) {
 #pragma unroll
@@ -556,7 +560,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const flo
     // ldmatrix row addresses: A (queries x dims) and B (keys x dims) operands
     const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8, lcol = (lane >> 4) * 8;
 
-    for (int jt = j0; jt < j1; jt += 2 * kAttnK) {
+    for (int jt = j0; jt < j1; jt += kAttnStep) {
         __syncthreads();  // the previous step's keys and values are no longer read
 #pragma unroll
         for (int u = 0; u < NK4; ++u) {
@@ -566,9 +570,9 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const flo
             split_store4(pv[u], &sm.vh[hf][k][d], &sm.vl[hf][k][d]);
         }
         __syncthreads();
-        if (jt + 2 * kAttnK < j1) load_kv(jt + 2 * kAttnK);
+        if (jt + kAttnStep < j1) load_kv(jt + kAttnStep);
         const int kt = jt + half * kAttnK;  // first key of this warp's tile
-        if (kt >= j1) continue;              // warp-uniform: nothing of this half in the last step
+        if (kt >= j1) continue;              // warp-uniform: nothing of this lane in the last step
         // scores: 16 queries x 32 keys per warp
         float sc[4][4];
 #pragma unroll
@@ -695,17 +699,18 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const flo
     }
     cluster.sync();  // every CTA's partial rows are written
 
-    // merge: one warp per query row; lane k < 2 nsplit reads partial k's
-    // running max and sum (CTA k / 2, key half k % 2), then every lane sums
-    // its VEC dims over the partials
+    // merge: one warp per query row; lane k < kAttnKH nsplit reads partial
+    // k's running max and sum (CTA k / kAttnKH, key lane k % kAttnKH), then
+    // every lane sums its VEC dims over the partials
     constexpr int VEC = HD / 32;
-    const int nparts = 2 * nsplit;
+    const int nparts = kAttnKH * nsplit;
     for (int qr = sp + warp * nsplit; qr < kAttnQ; qr += kAttnWarps * nsplit) {
         const int ii = qt * kAttnQ + qr;
         if (ii >= mq) break;  // rows grow with qr: none further (warp-uniform)
         float mk = -INFINITY, lk = 0.f;
         if (lane < nparts) {
-            const float* src = cluster.map_shared_rank(part, lane >> 1) + ((lane & 1) * kAttnQ + qr) * PART;
+            const float* src =
+                cluster.map_shared_rank(part, lane / kAttnKH) + ((lane % kAttnKH) * kAttnQ + qr) * PART;
             mk = src[0];
             lk = src[1];
         }
@@ -718,7 +723,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const flo
 #pragma unroll 8
         for (int k = 0; k < nparts; ++k) {
             const float w = __shfl_sync(0xffffffffu, wk, k);
-            const float* src = cluster.map_shared_rank(part, k >> 1) + ((k & 1) * kAttnQ + qr) * PART + 4 + VEC * lane;
+            const float* src =
+                cluster.map_shared_rank(part, k / kAttnKH) + ((k % kAttnKH) * kAttnQ + qr) * PART + 4 + VEC * lane;
             if constexpr (VEC == 4) {
                 const float4 a = *reinterpret_cast<const float4*>(src);
                 acc[0] = fmaf(a.x, w, acc[0]);
@@ -741,7 +747,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const flo
 
 // Cluster size (the key splits).  max_active[c]: clusters of c CTAs the
 // device holds at once.  With few (sequence, kv head, query tile) units the
-// largest cluster whose units all run in one wave, capped by the 64-key steps
+// largest cluster whose units all run in one wave, capped by the key steps
 // of the longest context `max_ctx` (callers pass the sequences' capacity, so
 // that the launch does not change as contexts grow); with many units, enough
 // splits to cover the SMs.
@@ -750,9 +756,10 @@ static void attn_plan(int n_seqs, int block_len, int max_ctx, int nq, int nkv, i
     const int mq = (nq / nkv) * block_len;
     *qtiles = (mq + kAttnQ - 1) / kAttnQ;
     const int total = max_ctx + block_len;
-    const int max_split = std::max(1, (total + 2 * kAttnK - 1) / (2 * kAttnK));
+    const int max_split = std::max(1, (total + kAttnStep - 1) / kAttnStep);
     const int units = nkv * *qtiles * n_seqs;
-    const int want = std::min(max_split, std::max(1, (num_sms + units - 1) / units));
+    const int slots = std::max(max_active[1], num_sms);  // CTAs the device holds at once
+    const int want = std::min(max_split, std::max(1, (slots + units - 1) / units));
     int best = 1;
     for (int c = 1; c <= std::min(want, kAttnMaxCluster); ++c)
         if (max_active[c] >= std::min(units, max_active[1])) best = c;

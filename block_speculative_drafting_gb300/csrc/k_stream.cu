@@ -109,16 +109,29 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
 
     pdl_wait();
     {
-        // the K-block's codes of the 16 rows as exact f16 (rows past T are zero)
-        const int vec = kbc / 8;
-        for (int i = threadIdx.x; i < 16 * vec; i += kQ4Threads) {
-            const int r = i / vec, c = i - r * vec;
-            uint2 v = make_uint2(0u, 0u);
-            if (r < T) v = *reinterpret_cast<const uint2*>(x.codes + (int64_t)r * x.ld + sg.kblk * kbc + c * 8);
-            uint4 h;
-            i8x4_to_half2x2(v.x, h.x, h.y);
-            i8x4_to_half2x2(v.y, h.z, h.w);
-            *reinterpret_cast<uint4*>(act + r * ldact + c * 8) = h;
+        // the K-block's codes of the 16 rows as exact f16 (rows past T are
+        // zero), eight loads of a thread in flight at once
+        const int vec = kbc / 8, total = 16 * vec;
+        constexpr int kBatch = 8;
+        for (int base = threadIdx.x; base < total; base += kBatch * kQ4Threads) {
+            uint2 v[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int i = base + u * kQ4Threads, r = i / vec, c = i - r * vec;
+                v[u] = make_uint2(0u, 0u);
+                if (i < total && r < T)
+                    v[u] = *reinterpret_cast<const uint2*>(x.codes + (int64_t)r * x.ld + sg.kblk * kbc + c * 8);
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int i = base + u * kQ4Threads, r = i / vec, c = i - r * vec;
+                if (i < total) {
+                    uint4 h;
+                    i8x4_to_half2x2(v[u].x, h.x, h.y);
+                    i8x4_to_half2x2(v[u].y, h.z, h.w);
+                    *reinterpret_cast<uint4*>(act + r * ldact + c * 8) = h;
+                }
+            }
         }
         __syncthreads();
     }
@@ -328,12 +341,23 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
 
     pdl_wait();
     {
-        const int vec = K / 16;
-        for (int i = threadIdx.x; i < 16 * vec; i += kConsumers * 32) {
-            const int r = i / vec, cc = i - r * vec;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (tok0 + r < T) v = *reinterpret_cast<const uint4*>(x.codes + (int64_t)(tok0 + r) * x.ld + cc * 16);
-            *reinterpret_cast<uint4*>(act + r * ldact + cc * 16) = v;
+        // eight loads of a thread in flight at once
+        const int vec = K / 16, total = 16 * vec;
+        constexpr int kBatch = 8, kN = kConsumers * 32;
+        for (int base = threadIdx.x; base < total; base += kBatch * kN) {
+            uint4 v[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int i = base + u * kN, r = i / vec, cc = i - r * vec;
+                v[u] = make_uint4(0u, 0u, 0u, 0u);
+                if (i < total && tok0 + r < T)
+                    v[u] = *reinterpret_cast<const uint4*>(x.codes + (int64_t)(tok0 + r) * x.ld + cc * 16);
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int i = base + u * kN, r = i / vec, cc = i - r * vec;
+                if (i < total) *reinterpret_cast<uint4*>(act + r * ldact + cc * 16) = v[u];
+            }
         }
         asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");
     }
