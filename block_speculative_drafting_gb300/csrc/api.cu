@@ -105,7 +105,7 @@ struct dflash_model {
 
     // scratch, grown on demand (a call that needs more memory than any call
     // before it allocates; calls of the same sizes allocate nothing)
-    DevBuf h, xq, xs, qkv, y, gu, logits, keys, toks, part, anchors, pos0, aseqs;
+    DevBuf h, xq, xs, qkv, y, gu, logits, keys, toks, part, anchors, pos0, aseqs, rope;
     DevBuf a_taps, a_codes, a_scale, a_t, a_kv, a_pos;
     bool grown = false;  // a scratch buffer moved since the graphs were captured
 
@@ -870,6 +870,7 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
     CK(m, ensure_m(m, m->toks, (size_t)D * sizeof(uint32_t)));
     CK(m, ensure_m(m, m->anchors, (size_t)n_seqs * sizeof(uint32_t)));
     CK(m, ensure_m(m, m->pos0, (size_t)n_seqs * sizeof(int64_t)));
+    CK(m, ensure_m(m, m->rope, (size_t)R * (hd / 2) * sizeof(float2)));
     CK(m, ensure_m(m, m->aseqs, (size_t)g.layers * n_seqs * sizeof(AttnSeq)));
     float* logit_out = io_on_device ? logits : nullptr;
     if (!io_on_device && logits) {
@@ -909,7 +910,12 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
     RowMap ident{1, 1, 0};
     const float scale = 1.0f / sqrtf((float)hd);
 
-    KL(m, "embed_rows", 1, (double)R * H * 8, st, embed_rows(m->embed, H, g.vocab, anchors_dev, g.mask_token, n_seqs, B, h, st));
+    // the embedding also writes the block rows' rotation table (cos, sin per
+    // position and frequency) that the attention applies as it loads q and k
+    float2* rope = P<float2>(m->rope);
+    KL(m, "embed_rows", 1, (double)R * H * 8, st,
+       embed_rows(m->embed, H, g.vocab, anchors_dev, g.mask_token, n_seqs, B, h, st, P<int64_t>(m->pos0),
+                  m->inv_freq, hd, rope));
     for (int l = 0; l < g.layers; ++l) {
         const Layer& Ly = m->layers[l];
         // attention half: x = rms(h, in_norm); q, k, v; norms and rotation; attention; h += O y
@@ -924,13 +930,11 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
             KL(m, "rms_f32", 1, (double)R * H * 8, st, rms_rows(h, H, ident, R, H, Ly.in_norm, g.eps, xf, maxK, nullptr, nullptr, 0, st));
             APPLY(apply(m, nullptr, Ly.qkv_f, Q4Layout{}, 0, m->qkv_w, H, xf, maxK, R, qkv, m->qkv_w, false, 0, st));
         }
-        KL(m, "qk_norm_rope", 1, (double)R * (m->qd + m->kd) * 8, st,
-           qk_norm_rope(qkv, m->qkv_w, R, B, P<int64_t>(m->pos0), g.heads, g.kv_heads, hd, Ly.q_norm, Ly.k_norm,
-                        m->inv_freq, g.eps, st));
+        // q/k norms and rotation run inside the attention, as it loads them
         const AttnSeq* aseq_dev = P<AttnSeq>(m->aseqs) + (size_t)l * n_seqs;
         KL(m, "attention", 1, attn_bytes, st,
            attention(qkv, m->qkv_w, n_seqs, B, aseq_dev, max_ctx, g.heads, g.kv_heads, hd, scale, P<float>(m->part),
-                     part_floats, y, m->num_sms, st));
+                     part_floats, y, m->num_sms, st, Ly.q_norm, Ly.k_norm, rope, g.eps));
         if (quant) {
             KL(m, "rms_quant", 1, (double)R * m->qd * 5, st, rms_rows(y, m->qd, ident, R, m->qd, nullptr, g.eps, nullptr, 0, xq, xs, maxK, st));
             TRACE(trace_site(m, st, R, m->qd, xq, maxK, xs, [&](float* v) {

@@ -108,11 +108,19 @@ __global__ void __launch_bounds__(kRowThreads) rms_rows_reg_kernel(const float* 
                                                                    float* __restrict__ out_f32, int ld_out,
                                                                    int8_t* __restrict__ out_codes,
                                                                    float* __restrict__ out_scale, int ld_codes,
-                                                                   float* zero_buf, int64_t zero_n) {
+                                                                   float* zero_buf, int64_t zero_n, int rows) {
     __shared__ float red[33];
     pdl_trigger();
     pdl_wait();
-    zero_side(zero_buf, zero_n);
+    if ((int)blockIdx.x >= rows) {
+        // the CTAs past the rows clear the side buffer, float4 at a time
+        const int64_t stride = (int64_t)(gridDim.x - rows) * blockDim.x;
+        const int64_t first = (int64_t)(blockIdx.x - rows) * blockDim.x + threadIdx.x;
+        float4* p4 = reinterpret_cast<float4*>(zero_buf);
+        for (int64_t k = first; k < zero_n / 4; k += stride) p4[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (first < zero_n % 4) zero_buf[zero_n / 4 * 4 + first] = 0.f;
+        return;
+    }
     const int i = blockIdx.x;
     const int srow = (i / map.per) * map.stride + map.skip + (i % map.per);
     const float4* x4 = reinterpret_cast<const float4*>(src + (int64_t)srow * ld_src);
@@ -176,11 +184,15 @@ int rms_rows(const float* src, int ld_src, RowMap map, int rows, int n, const fl
              int64_t zero_n) {
     if (rows <= 0) return 0;
     const bool wal = !w || (reinterpret_cast<uintptr_t>(w) % 16) == 0;
-    if (wal && rows_fit_reg(n, src, ld_src, out_f32, ld_out, out_codes, ld_codes, 8 * 4 * kRowThreads)) {
+    const bool zal = !zero_buf || (reinterpret_cast<uintptr_t>(zero_buf) % 16) == 0;
+    if (wal && zal && rows_fit_reg(n, src, ld_src, out_f32, ld_out, out_codes, ld_codes, 8 * 4 * kRowThreads)) {
         const int nv = (n + 4 * kRowThreads - 1) / (4 * kRowThreads);
+        // extra CTAs clear the side buffer (about four float4 stores a thread, at most 128 CTAs)
+        const int extra =
+            zero_buf && zero_n > 0 ? (int)std::min<int64_t>(128, zero_n / 4 / (kRowThreads * 4) + 1) : 0;
         auto go = [&](auto kern) {
-            return (int)launch(kern, dim3(rows), dim3(kRowThreads), 0, st, src, ld_src, map, n, w, eps, out_f32, ld_out,
-                               out_codes, out_scale, ld_codes, zero_buf, zero_n);
+            return (int)launch(kern, dim3(rows + extra), dim3(kRowThreads), 0, st, src, ld_src, map, n, w, eps, out_f32,
+                               ld_out, out_codes, out_scale, ld_codes, zero_buf, zero_n, rows);
         };
         if (nv <= 1) return go(rms_rows_reg_kernel<1>);
         if (nv <= 2) return go(rms_rows_reg_kernel<2>);
@@ -195,10 +207,20 @@ int rms_rows(const float* src, int ld_src, RowMap map, int rows, int n, const fl
 // device, which the host cannot check) embeds as a row of zeros.
 __global__ void embed_rows_kernel(const float* __restrict__ embed, int H, int vocab,
                                   const uint32_t* __restrict__ anchor_tok, int mask_token, int block_len,
-                                  float* __restrict__ h) {
+                                  float* __restrict__ h, const int64_t* __restrict__ pos0,
+                                  const float* __restrict__ inv_freq, int half_hd, float2* __restrict__ rope) {
     const int r = blockIdx.x;
     pdl_trigger();
     pdl_wait();
+    if (rope != nullptr) {
+        // the same angle and sincosf as the context keys' rotation
+        const float p = (float)(pos0[r / block_len] + r % block_len);
+        for (int i = threadIdx.x; i < half_hd; i += blockDim.x) {
+            float sn, cs;
+            sincosf(__fmul_rn(p, inv_freq[i]), &sn, &cs);
+            rope[(int64_t)r * half_hd + i] = make_float2(cs, sn);
+        }
+    }
     const uint32_t tok = (r % block_len == 0) ? anchor_tok[r / block_len] : (uint32_t)mask_token;
     float4* d = reinterpret_cast<float4*>(h + (int64_t)r * H);
     if (tok >= (uint32_t)vocab) {
@@ -210,9 +232,10 @@ __global__ void embed_rows_kernel(const float* __restrict__ embed, int H, int vo
 }
 
 int embed_rows(const float* embed, int H, int vocab, const uint32_t* anchor_tok, int mask_token, int n_seqs,
-               int block_len, float* h, cudaStream_t st) {
+               int block_len, float* h, cudaStream_t st, const int64_t* pos0, const float* inv_freq, int hd,
+               float2* rope) {
     return (int)launch(embed_rows_kernel, dim3(n_seqs * block_len), dim3(256), 0, st, embed, H, vocab, anchor_tok,
-                       mask_token, block_len, h);
+                       mask_token, block_len, h, pos0, inv_freq, hd / 2, rope);
 }
 
 // RMSNorm of one head (hd = 32 * E elements, lane holds lane + 32 j) and its
@@ -240,39 +263,6 @@ DF_DEV void norm_rope_head(float (&v)[E], const float* __restrict__ gain, const 
         v[j] = lo * cs - hi * sn;
         v[j + E / 2] = hi * cs + lo * sn;
     }
-}
-
-template <int E>
-__global__ void qk_norm_rope_kernel(float* __restrict__ qkv, int ld, int rows, int block_len,
-                                    const int64_t* __restrict__ pos0, int nq, int nkv,
-                                    const float* __restrict__ q_norm, const float* __restrict__ k_norm,
-                                    const float* __restrict__ inv_freq, float eps) {
-    constexpr int HD = 32 * E;
-    const int wid = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
-    const int heads = nq + nkv;
-    pdl_trigger();
-    pdl_wait();
-    if (wid >= rows * heads) return;
-    const int r = wid / heads, hh = wid % heads, lane = threadIdx.x & 31;
-    float* p = qkv + (int64_t)r * ld + hh * HD;  // q heads then k heads are contiguous
-    float v[E];
-#pragma unroll
-    for (int j = 0; j < E; ++j) v[j] = p[lane + 32 * j];
-    const int64_t pos = pos0[r / block_len] + r % block_len;
-    norm_rope_head<E>(v, hh < nq ? q_norm : k_norm, inv_freq, eps, pos, true);
-#pragma unroll
-    for (int j = 0; j < E; ++j) p[lane + 32 * j] = v[j];
-}
-
-int qk_norm_rope(float* qkv, int ld, int rows, int block_len, const int64_t* pos0_dev, int nq, int nkv, int hd,
-                 const float* q_norm, const float* k_norm, const float* inv_freq, float eps, cudaStream_t st) {
-    const int64_t warps = (int64_t)rows * (nq + nkv);
-    const unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
-    if (hd == 128)
-        return (int)launch(qk_norm_rope_kernel<4>, dim3(blocks), dim3(256), 0, st, qkv, ld, rows, block_len, pos0_dev,
-                           nq, nkv, q_norm, k_norm, inv_freq, eps);
-    return (int)launch(qk_norm_rope_kernel<2>, dim3(blocks), dim3(256), 0, st, qkv, ld, rows, block_len, pos0_dev, nq,
-                       nkv, q_norm, k_norm, inv_freq, eps);
 }
 
 template <int E>
@@ -395,9 +385,51 @@ __global__ void __launch_bounds__(kRowThreads) silu_mul_reg_kernel(const float* 
     if (threadIdx.x == 0) out_scale[r] = sx;
 }
 
+// The same with a row split over the kSiluSplit CTAs of a cluster (one float4
+// of the row per thread): each CTA reduces its share's max|a|, the cluster
+// takes the row's max through distributed shared memory.
+constexpr int kSiluSplit = 4;
+__global__ void __launch_bounds__(kRowThreads) silu_mul_cluster_kernel(const float* __restrict__ gu, int ld_gu, int I,
+                                                                       float* __restrict__ out_f32, int ld_out,
+                                                                       int8_t* __restrict__ out_codes,
+                                                                       float* __restrict__ out_scale, int ld_codes) {
+    __shared__ float red[33];
+    cg::cluster_group cluster = cg::this_cluster();
+    pdl_trigger();
+    pdl_wait();
+    const int r = blockIdx.y, part = (int)cluster.block_rank();
+    const int share4 = I / 4 / kSiluSplit;  // float4 of the row per CTA
+    const int c = part * share4 + threadIdx.x;
+    const bool in = threadIdx.x < share4;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (in) {
+        const float4 gv = reinterpret_cast<const float4*>(gu + (int64_t)r * ld_gu)[c];
+        const float4 uv = reinterpret_cast<const float4*>(gu + (int64_t)r * ld_gu + I)[c];
+        a = make_float4(silu_f(gv.x) * uv.x, silu_f(gv.y) * uv.y, silu_f(gv.z) * uv.z, silu_f(gv.w) * uv.w);
+    }
+    if (out_f32) {
+        if (in) reinterpret_cast<float4*>(out_f32 + (int64_t)r * ld_out)[c] = a;
+        return;  // no cluster-wide step on this path: every CTA leaves here
+    }
+    const float local = row_reduce<true>(amax4(a), red);  // red[32] holds this CTA's max
+    cluster.sync();
+    float amax = local;
+#pragma unroll
+    for (int k = 0; k < kSiluSplit; ++k) amax = fmaxf(amax, cluster.map_shared_rank(red, k)[32]);
+    cluster.sync();  // no CTA leaves while another may still read its max
+    const float sx = __fdiv_rn(amax, 127.0f);
+    if (in) reinterpret_cast<uint32_t*>(out_codes + (int64_t)r * ld_codes)[c] = codes4(a, sx);
+    if (part == 0 && threadIdx.x == 0) out_scale[r] = sx;
+}
+
 int silu_mul(const float* gu, int ld_gu, int rows, int I, float* out_f32, int ld_out, int8_t* out_codes,
              float* out_scale, int ld_codes, cudaStream_t st) {
     if (rows <= 0) return 0;
+    if (I % (4 * kSiluSplit) == 0 && I / 4 / kSiluSplit <= kRowThreads &&
+        rows_fit_reg(I, gu, ld_gu, out_f32, ld_out, out_codes, ld_codes, 4 * kSiluSplit * kRowThreads) &&
+        (reinterpret_cast<uintptr_t>(gu + I) % 16) == 0)
+        return (int)launch_cluster(silu_mul_cluster_kernel, dim3(kSiluSplit, rows), dim3(kRowThreads), 0, st,
+                                   kSiluSplit, gu, ld_gu, I, out_f32, ld_out, out_codes, out_scale, ld_codes);
     if (rows_fit_reg(I, gu, ld_gu, out_f32, ld_out, out_codes, ld_codes, 4 * 4 * kRowThreads) &&
         (reinterpret_cast<uintptr_t>(gu + I) % 16) == 0) {
         const int nv = (I + 4 * kRowThreads - 1) / (4 * kRowThreads);
@@ -458,6 +490,42 @@ DF_DEV void split_store4(float4 v, __half* hi, __half* lo) {
     *reinterpret_cast<uint2*>(lo) = make_uint2(pack_half2(l0, l1), pack_half2(l2, l3));
 }
 
+// Per-head RMSNorm and half-split rotation of a row held as float4 by HD/4
+// consecutive lanes (lane d4 holds dims 4 d4 .. 4 d4 + 3; the partner dims
+// i +- HD/2 sit at lane d4 ^ HD/8).  Every lane runs the shuffles; the result
+// replaces v where `apply`.  tab: the row's (cos, sin) per i < HD/2.
+template <int HD>
+DF_DEV void norm_rope4(float4& v, bool apply, const float* __restrict__ gain, const float2* __restrict__ tab,
+                       int d4, float eps) {
+    constexpr int D4 = HD / 4;
+    float ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, v.w * v.w)));
+#pragma unroll
+    for (int o = D4 / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float s = 1.0f / sqrtf(ss / (float)HD + eps);
+    float4 g = make_float4(1.f, 1.f, 1.f, 1.f);
+    if (apply) g = *reinterpret_cast<const float4*>(gain + 4 * d4);
+    const float4 n = make_float4(v.x * s * g.x, v.y * s * g.y, v.z * s * g.z, v.w * s * g.w);
+    float4 pn;  // the partner lane's normed dims
+    pn.x = __shfl_xor_sync(0xffffffffu, n.x, D4 / 2);
+    pn.y = __shfl_xor_sync(0xffffffffu, n.y, D4 / 2);
+    pn.z = __shfl_xor_sync(0xffffffffu, n.z, D4 / 2);
+    pn.w = __shfl_xor_sync(0xffffffffu, n.w, D4 / 2);
+    if (!apply) return;
+    const bool lo_half = d4 < D4 / 2;
+    const int i0 = (4 * d4) % (HD / 2);
+    const float4 t01 = *reinterpret_cast<const float4*>(tab + i0);      // (cos, sin) of i0, i0 + 1
+    const float4 t23 = *reinterpret_cast<const float4*>(tab + i0 + 2);  // of i0 + 2, i0 + 3
+    const float cs[4] = {t01.x, t01.z, t23.x, t23.z}, sn[4] = {t01.y, t01.w, t23.y, t23.w};
+    const float me[4] = {n.x, n.y, n.z, n.w}, other[4] = {pn.x, pn.y, pn.z, pn.w};
+    float r[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        // lo' = lo cos - hi sin; hi' = hi cos + lo sin
+        r[c] = lo_half ? me[c] * cs[c] - other[c] * sn[c] : me[c] * cs[c] + other[c] * sn[c];
+    }
+    v = make_float4(r[0], r[1], r[2], r[3]);
+}
+
 template <int HD>
 struct AttnSmem {
     static constexpr int LD = HD + 8;  // halves: 16-byte row pad, conflict-free ldmatrix
@@ -485,7 +553,10 @@ template <int HD>
 __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const float* __restrict__ qkv, int ld,
                                                                        int block_len, const AttnSeq* __restrict__ seqs,
                                                                        int nq, int nkv, int qtiles, int nsplit,
-                                                                       float scale_log2, float* __restrict__ y) {
+                                                                       float scale_log2, float* __restrict__ y,
+                                                                       const float* __restrict__ q_norm,
+                                                                       const float* __restrict__ k_norm,
+                                                                       const float2* __restrict__ rope, float eps) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     AttnSmem<HD>& sm = *reinterpret_cast<AttnSmem<HD>*>(smem_raw);
     constexpr int PART = AttnSmem<HD>::PART;
@@ -529,6 +600,10 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const flo
                     vv = *reinterpret_cast<const float4*>(qkv + off + (int64_t)(nq + nkv + g) * HD);
                 }
             }
+            if (k_norm != nullptr) {  // the block's own keys: norm and rotate (all lanes run the shuffles)
+                const int r = min(max(j - sq.n, 0), block_len - 1);
+                norm_rope4<HD>(kk, j < j1 && j >= sq.n, k_norm, rope + (row0 + r) * (HD / 2), i % D4, eps);
+            }
             pk[u] = kk;
             pv[u] = vv;
         }
@@ -543,6 +618,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const flo
                 const int head = g * rep + ii / block_len, r = ii % block_len;
                 qv[u] = *reinterpret_cast<const float4*>(qkv + (row0 + r) * ld + (int64_t)head * HD + d);
             }
+            if (q_norm != nullptr)
+                norm_rope4<HD>(qv[u], ii < mq, q_norm, rope + (row0 + ii % block_len) * (HD / 2), i % D4, eps);
         }
         if (j0 < j1) load_kv(j0);
 #pragma unroll
@@ -805,21 +882,28 @@ static const int* attn_cluster_table(cudaStream_t st) {
 
 template <int HD>
 static int attention_hd(const float* qkv, int ld, int n_seqs, int block_len, const AttnSeq* seqs_dev, int max_ctx,
-                        int nq, int nkv, float scale, float* y, int num_sms, cudaStream_t st) {
+                        int nq, int nkv, float scale, float* y, int num_sms, cudaStream_t st, const float* q_norm,
+                        const float* k_norm, const float2* rope, float eps) {
     const int* table = attn_cluster_table<HD>(st);
     int qtiles, nsplit;
     attn_plan(n_seqs, block_len, max_ctx, nq, nkv, num_sms, table, &qtiles, &nsplit);
     const float scale_log2 = scale * 1.4426950408889634f;
     dim3 grid(nsplit, nkv * qtiles, n_seqs);
     return (int)launch_cluster(attn_cluster_kernel<HD>, grid, dim3(kAttnWarps * 32), sizeof(AttnSmem<HD>), st, nsplit,
-                               qkv, ld, block_len, seqs_dev, nq, nkv, qtiles, nsplit, scale_log2, y);
+                               qkv, ld, block_len, seqs_dev, nq, nkv, qtiles, nsplit, scale_log2, y, q_norm, k_norm,
+                               rope, eps);
 }
 
 int attention(const float* qkv, int ld, int n_seqs, int block_len, const AttnSeq* seqs_dev, int max_ctx, int nq,
-              int nkv, int hd, float scale, float*, int64_t, float* y, int num_sms, cudaStream_t st) {
+              int nkv, int hd, float scale, float*, int64_t, float* y, int num_sms, cudaStream_t st,
+              const float* q_norm, const float* k_norm, const float2* rope, float eps) {
+    if ((q_norm == nullptr) != (k_norm == nullptr) || (q_norm != nullptr && rope == nullptr))
+        return (int)cudaErrorInvalidValue;
     if (hd == 128)
-        return attention_hd<128>(qkv, ld, n_seqs, block_len, seqs_dev, max_ctx, nq, nkv, scale, y, num_sms, st);
-    return attention_hd<64>(qkv, ld, n_seqs, block_len, seqs_dev, max_ctx, nq, nkv, scale, y, num_sms, st);
+        return attention_hd<128>(qkv, ld, n_seqs, block_len, seqs_dev, max_ctx, nq, nkv, scale, y, num_sms, st, q_norm,
+                                 k_norm, rope, eps);
+    return attention_hd<64>(qkv, ld, n_seqs, block_len, seqs_dev, max_ctx, nq, nkv, scale, y, num_sms, st, q_norm,
+                            k_norm, rope, eps);
 }
 
 }  // namespace dflash

@@ -91,14 +91,12 @@ int rms_rows(const float* src, int ld_src, RowMap map, int rows, int n, const fl
              int ld_out, int8_t* out_codes, float* out_scale, int ld_codes, cudaStream_t st,
              float* zero_buf = nullptr, int64_t zero_n = 0);
 // h[r] = embed[tok(r)]: row r of sequence s = r / block_len is the anchor
-// (anchor_tok[s]) for r % block_len == 0, the mask token otherwise.
+// (anchor_tok[s]) for r % block_len == 0, the mask token otherwise.  Side
+// duty (rope != nullptr): the block rows' rotation table rope[r][i] =
+// (cos, sin) of f32(pos0[s] + r % block_len) * inv_freq[i], i < hd / 2.
 int embed_rows(const float* embed, int H, int vocab, const uint32_t* anchor_tok, int mask_token, int n_seqs,
-               int block_len, float* h, cudaStream_t st);
-// In-place per-head RMSNorm (q_norm / k_norm) and half-split RoPE of the
-// block's q and k: qkv [rows][(nq + 2 nkv) hd]; row r sits at position
-// pos0[r / block_len] + r % block_len.
-int qk_norm_rope(float* qkv, int ld, int rows, int block_len, const int64_t* pos0_dev, int nq, int nkv, int hd,
-                 const float* q_norm, const float* k_norm, const float* inv_freq, float eps, cudaStream_t st);
+               int block_len, float* h, cudaStream_t st, const int64_t* pos0 = nullptr,
+               const float* inv_freq = nullptr, int hd = 0, float2* rope = nullptr);
 // Context rows: kv [n][L * 2 * nkv * hd] (per layer k then v) -> the
 // sequence's store: K rows normed (k_norm_l) and rotated at position
 // pos0 + r, V rows as they are; stored at index idx0 + r, where
@@ -139,14 +137,18 @@ struct AttnSeq {
     int64_t lo;  // first context index read (position - first)
     int n;       // context rows read
 };
-// qkv [n_seqs*block_len][ld] (q, k, v of the block after norm and RoPE);
-// y [n_seqs*block_len][nq*hd].  `part` / part_floats: scratch of
+// qkv [n_seqs*block_len][ld] (q, k, v of the block); with q_norm != nullptr
+// the kernel applies the per-head RMSNorm (q_norm / k_norm) and the rotation
+// (table `rope` of embed_rows) to q and to the block's k as it loads them,
+// otherwise q and k arrive normed and rotated.  y [n_seqs*block_len][nq*hd].  `part` / part_floats: scratch of
 // attn_scratch_floats() floats (none at present: the key splits merge in
 // distributed shared memory).
 // max_ctx: the largest context any sequence of the call may hold (its
 // capacity); the launch depends on it, each CTA's key range on the actual n.
 int attention(const float* qkv, int ld, int n_seqs, int block_len, const AttnSeq* seqs_dev, int max_ctx, int nq,
-              int nkv, int hd, float scale, float* part, int64_t part_floats, float* y, int num_sms, cudaStream_t st);
+              int nkv, int hd, float scale, float* part, int64_t part_floats, float* y, int num_sms, cudaStream_t st,
+              const float* q_norm = nullptr, const float* k_norm = nullptr, const float2* rope = nullptr,
+              float eps = 0.f);
 int64_t attn_scratch_floats(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int hd, int num_sms);
 
 }  // namespace dflash

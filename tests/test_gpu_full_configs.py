@@ -12,11 +12,15 @@ afford one by one:
   32 sequences whole and the GPU's logits for those two must match;
 * long context: the oracle runs the whole sequence.
 
-Each side takes its own quantisation decisions here (an f32 value within
-rounding of a half-step boundary can round either way), so a row or a block
-is compared with the bound the identical-decision tests justify where no
-decision differs, and with the spread that f32-level noise on the oracle's
-own decisions produces where one does.
+Free running, each side takes its own quantisation decisions (an f32 value
+within rounding of a half-step boundary can round either way), so a row or a
+block is compared with the bound the identical-decision tests justify where
+no decision differs, and with the spread that f32-level noise on the
+oracle's own decisions produces where one does.  The blocks are then run
+again with the oracle's decisions at every quantisation site of the block
+and must agree at f32 level (the appended context keeps each side's own
+decisions: a context row with a code at a boundary moves the attention by
+about its 1/n weight times a code step).
 """
 import numpy as np
 import pytest
@@ -56,6 +60,30 @@ def _noise_bound(om, osq, anchor, anchor_pos, B, ref, runs=2):
     finally:
         Q.quantize_rows_i8 = orig
     return max(devs)
+
+
+def _oracle_block_sites(om, osq, anchor, anchor_pos, B):
+    """The oracle's block with its quantisation sites recorded."""
+    import oracle.drafter as D
+    D.TRACE = D.QuantTrace()
+    try:
+        ref, ref_tok = block(om, osq, anchor, anchor_pos, B)
+        return ref, ref_tok, D.TRACE.sites
+    finally:
+        D.TRACE = None
+
+
+def _forced_block(model, seqs, anchors, positions, B, sites):
+    """The GPU block with every site's codes and scales replaced by `sites`."""
+    model.trace(True)
+    for _, q, sc in sites:
+        model.trace_force(q, sc)
+    try:
+        out = model.block(seqs, anchors, positions, B)
+        own = model.trace_sites()
+    finally:
+        model.trace(False)
+    return out, own
 
 
 def test_prefill_8192_rows_sampled(qwen):
@@ -104,11 +132,22 @@ def test_batch32_ctx4096_sampled_sequences(qwen):
         seqs.append(seq)
     logits, toks = model.block(seqs, anchors, [ctx] * S, B)
     assert logits.shape == (S, B - 1, g.vocab) and toks.shape == (S, B - 1)
+    # the GPU's own decisions of one more run, for the identical-decision pass
+    model.trace(True)
+    try:
+        model.block(seqs, anchors, [ctx] * S, B)
+        own = model.trace_sites()
+    finally:
+        model.trace(False)
+    assert len(own) == 4 * g.layers + 1
+    forced = [(None, q.copy(), sc.copy()) for _, q, sc in own]
+    refs = {}
     for s in (0, S - 1):
         osq = OracleSeq(om)
         for r0 in range(0, ctx, APPEND_CHUNK):
             osq.append(r0, W.make_taps(g, min(APPEND_CHUNK, ctx - r0), call_id=1000 + 64 * s + r0 // APPEND_CHUNK))
-        ref, ref_tok = block(om, osq, int(anchors[s]), ctx, B)
+        # free running: each side its own decisions
+        ref, ref_tok, sites = _oracle_block_sites(om, osq, int(anchors[s]), ctx, B)
         scale = float(np.max(np.abs(ref)))
         dev = float(np.max(np.abs(logits[s] - ref))) / scale
         noise = _noise_bound(om, osq, int(anchors[s]), ctx, B, ref)
@@ -116,6 +155,21 @@ def test_batch32_ctx4096_sampled_sequences(qwen):
         print(f"batch32 sequence {s}: GPU vs oracle {dev:.2e} of max|logit|, oracle noise {noise:.2e}, "
               f"token agreement {agree:.3f}")
         assert dev <= 3 * noise + 2e-3
+        # this sequence's rows of every site take the oracle's decisions; the
+        # other sequences keep the GPU's own (sequences are independent: those
+        # decisions move only their own sequences' outputs)
+        assert len(sites) == len(own)
+        for i, (_, q, sc) in enumerate(sites):
+            rb = q.shape[0]  # B rows (layer sites) or B - 1 (the head's)
+            forced[i][1][s * rb:(s + 1) * rb] = q
+            forced[i][2][s * rb:(s + 1) * rb] = sc
+        refs[s] = (ref, ref_tok)
+    (logits_f, toks_f), _ = _forced_block(model, seqs, anchors, [ctx] * S, B, forced)
+    for s, (ref, ref_tok) in refs.items():
+        err = float(np.max(np.abs(logits_f[s] - ref))) / float(np.max(np.abs(ref)))
+        print(f"batch32 sequence {s}, identical decisions: {err:.2e} of max|logit|")
+        assert err <= 1e-4
+        assert (toks_f[s] == ref_tok).all()
     for seq in seqs:
         seq.close()
 
@@ -141,6 +195,15 @@ def test_ctx32768_block(qwen):
     agree = float(np.mean(toks[0] == ref_tok))
     print(f"ctx 32768: GPU vs oracle {dev:.2e} of max|logit|, oracle noise {noise:.2e}, token agreement {agree:.3f}")
     assert dev <= 3 * noise + 2e-3
+    # identical decisions in the block (the context's own decisions on each
+    # side: a context row with a code at a boundary moves the attention by
+    # about its 1/32768 weight times a code step)
+    ref_f, ref_tok_f, sites = _oracle_block_sites(om, osq, anchor, ctx, B)
+    (logits_f, toks_f), own = _forced_block(model, [seq], [anchor], [ctx], B, sites)
+    err = float(np.max(np.abs(logits_f[0] - ref_f))) / float(np.max(np.abs(ref_f)))
+    print(f"ctx 32768, identical decisions in the block: {err:.2e} of max|logit|")
+    assert err <= 1e-4
+    assert (toks_f[0] == ref_tok_f).all()
     # stored context rows near both ends and in the middle
     for p0 in (0, ctx // 2 + 7, ctx - B):
         k, v = model.read_kv(seq, g.layers - 1, p0, B)
