@@ -493,28 +493,23 @@ DF_DEV void split_store4(float4 v, __half* hi, __half* lo) {
 // Per-head RMSNorm and half-split rotation of a row held as float4 by HD/4
 // consecutive lanes (lane d4 holds dims 4 d4 .. 4 d4 + 3; the partner dims
 // i +- HD/2 sit at lane d4 ^ HD/8).  Every lane runs the shuffles; the result
-// replaces v where `apply`.  tab: the row's (cos, sin) per i < HD/2.
+// replaces v where `apply`.  g: the gains of the lane's dims; t01 / t23: the
+// (cos, sin) pairs of its frequencies i0 .. i0 + 3, i0 = 4 d4 mod HD/2
+// (loaded by the caller, ahead of time).
 template <int HD>
-DF_DEV void norm_rope4(float4& v, bool apply, const float* __restrict__ gain, const float2* __restrict__ tab,
-                       int d4, float eps) {
+DF_DEV void norm_rope4(float4& v, bool apply, float4 g, float4 t01, float4 t23, int d4, float eps) {
     constexpr int D4 = HD / 4;
     float ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, v.w * v.w)));
 #pragma unroll
     for (int o = D4 / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     const float s = 1.0f / sqrtf(ss / (float)HD + eps);
-    float4 g = make_float4(1.f, 1.f, 1.f, 1.f);
-    if (apply) g = *reinterpret_cast<const float4*>(gain + 4 * d4);
     const float4 n = make_float4(v.x * s * g.x, v.y * s * g.y, v.z * s * g.z, v.w * s * g.w);
     float4 pn;  // the partner lane's normed dims
     pn.x = __shfl_xor_sync(0xffffffffu, n.x, D4 / 2);
     pn.y = __shfl_xor_sync(0xffffffffu, n.y, D4 / 2);
     pn.z = __shfl_xor_sync(0xffffffffu, n.z, D4 / 2);
     pn.w = __shfl_xor_sync(0xffffffffu, n.w, D4 / 2);
-    if (!apply) return;
     const bool lo_half = d4 < D4 / 2;
-    const int i0 = (4 * d4) % (HD / 2);
-    const float4 t01 = *reinterpret_cast<const float4*>(tab + i0);      // (cos, sin) of i0, i0 + 1
-    const float4 t23 = *reinterpret_cast<const float4*>(tab + i0 + 2);  // of i0 + 2, i0 + 3
     const float cs[4] = {t01.x, t01.z, t23.x, t23.z}, sn[4] = {t01.y, t01.w, t23.y, t23.w};
     const float me[4] = {n.x, n.y, n.z, n.w}, other[4] = {pn.x, pn.y, pn.z, pn.w};
     float r[4];
@@ -523,7 +518,15 @@ DF_DEV void norm_rope4(float4& v, bool apply, const float* __restrict__ gain, co
         // lo' = lo cos - hi sin; hi' = hi cos + lo sin
         r[c] = lo_half ? me[c] * cs[c] - other[c] * sn[c] : me[c] * cs[c] + other[c] * sn[c];
     }
-    v = make_float4(r[0], r[1], r[2], r[3]);
+    if (apply) v = make_float4(r[0], r[1], r[2], r[3]);
+}
+
+// the (cos, sin) pairs a lane needs for row `row` of the rotation table
+template <int HD>
+DF_DEV void rope_pairs(const float2* __restrict__ rope, int64_t row, int d4, float4& t01, float4& t23) {
+    const float4* t = reinterpret_cast<const float4*>(rope + row * (HD / 2) + (4 * d4) % (HD / 2));
+    t01 = t[0];
+    t23 = t[1];
 }
 
 template <int HD>
@@ -600,10 +603,6 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const flo
                     vv = *reinterpret_cast<const float4*>(qkv + off + (int64_t)(nq + nkv + g) * HD);
                 }
             }
-            if (k_norm != nullptr) {  // the block's own keys: norm and rotate (all lanes run the shuffles)
-                const int r = min(max(j - sq.n, 0), block_len - 1);
-                norm_rope4<HD>(kk, j < j1 && j >= sq.n, k_norm, rope + (row0 + r) * (HD / 2), i % D4, eps);
-            }
             pk[u] = kk;
             pv[u] = vv;
         }
@@ -618,10 +617,26 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const flo
                 const int head = g * rep + ii / block_len, r = ii % block_len;
                 qv[u] = *reinterpret_cast<const float4*>(qkv + (row0 + r) * ld + (int64_t)head * HD + d);
             }
-            if (q_norm != nullptr)
-                norm_rope4<HD>(qv[u], ii < mq, q_norm, rope + (row0 + ii % block_len) * (HD / 2), i % D4, eps);
         }
-        if (j0 < j1) load_kv(j0);
+        if (q_norm != nullptr) {
+            // gains and rotation pairs in flight with the loads above and below
+            const int d4 = tid % D4;
+            const float4 gq = *reinterpret_cast<const float4*>(q_norm + 4 * d4);
+            float4 tq[NQ4][2];
+#pragma unroll
+            for (int u = 0; u < NQ4; ++u) {
+                const int ii = qt * kAttnQ + (tid + u * kThreads) / D4;
+                rope_pairs<HD>(rope, row0 + ii % block_len, d4, tq[u][0], tq[u][1]);
+            }
+            if (j0 < j1) load_kv(j0);
+#pragma unroll
+            for (int u = 0; u < NQ4; ++u) {
+                const int ii = qt * kAttnQ + (tid + u * kThreads) / D4;
+                norm_rope4<HD>(qv[u], ii < mq, gq, tq[u][0], tq[u][1], d4, eps);
+            }
+        } else if (j0 < j1) {
+            load_kv(j0);
+        }
 #pragma unroll
         for (int u = 0; u < NQ4; ++u) {
             const int i = tid + u * kThreads, qr = i / D4, d = (i % D4) * 4;
@@ -639,6 +654,24 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const flo
 
     for (int jt = j0; jt < j1; jt += kAttnStep) {
         __syncthreads();  // the previous step's keys and values are no longer read
+        if (k_norm != nullptr && jt + kAttnStep > sq.n) {
+            // this step holds block rows (j >= n): their keys get the norm and
+            // rotation here, as they go to shared memory (uniform over the
+            // CTA; all lanes run the shuffles)
+            const int d4 = tid % D4;
+            const float4 gk = *reinterpret_cast<const float4*>(k_norm + 4 * d4);
+            float4 tk[NK4][2];
+#pragma unroll
+            for (int u = 0; u < NK4; ++u) {
+                const int j = jt + (tid + u * kThreads) / D4;
+                rope_pairs<HD>(rope, row0 + min(max(j - sq.n, 0), block_len - 1), d4, tk[u][0], tk[u][1]);
+            }
+#pragma unroll
+            for (int u = 0; u < NK4; ++u) {
+                const int j = jt + (tid + u * kThreads) / D4;
+                norm_rope4<HD>(pk[u], j < j1 && j >= sq.n, gk, tk[u][0], tk[u][1], d4, eps);
+            }
+        }
 #pragma unroll
         for (int u = 0; u < NK4; ++u) {
             const int i = tid + u * kThreads, kr = i / D4, d = (i % D4) * 4;

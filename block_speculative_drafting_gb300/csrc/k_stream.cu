@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
             xs[h][e] = t < T ? x.scale[t] : 0.f;
         }
     const float zero[4] = {0.f, 0.f, 0.f, 0.f};
-    float acc[4][2][4];
+    __align__(8) float acc[4][2][4];
 #pragma unroll
     for (int r = 0; r < 4; ++r)
 #pragma unroll
@@ -197,16 +197,20 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
                 mma_f16_16816(d0, a1, bq[gi][0].z, bq[gi][0].w, d0);
                 mma_f16_16816(d1, a0, bq[gi][1].x, bq[gi][1].y, zero);
                 mma_f16_16816(d1, a1, bq[gi][1].z, bq[gi][1].w, d1);
+                // the group's f16 scales of rows gq and gq + 8, each as an f32
+                // pair, for packed f32x2 fused multiply-adds (same rounding as
+                // two fmaf)
                 uint32_t sbits = svs[gi];
-                const float2 sc = __half22float2(*reinterpret_cast<const __half2*>(&sbits));
-                acc[r][0][0] = fmaf(sc.x, d0[0], acc[r][0][0]);
-                acc[r][0][1] = fmaf(sc.x, d0[1], acc[r][0][1]);
-                acc[r][0][2] = fmaf(sc.y, d0[2], acc[r][0][2]);
-                acc[r][0][3] = fmaf(sc.y, d0[3], acc[r][0][3]);
-                acc[r][1][0] = fmaf(sc.x, d1[0], acc[r][1][0]);
-                acc[r][1][1] = fmaf(sc.x, d1[1], acc[r][1][1]);
-                acc[r][1][2] = fmaf(sc.y, d1[2], acc[r][1][2]);
-                acc[r][1][3] = fmaf(sc.y, d1[3], acc[r][1][3]);
+                const __half2 sh = *reinterpret_cast<const __half2*>(&sbits);
+                const float2 s0 = __half22float2(__low2half2(sh)), s1 = __half22float2(__high2half2(sh));
+                float2* a00 = reinterpret_cast<float2*>(&acc[r][0][0]);
+                float2* a01 = reinterpret_cast<float2*>(&acc[r][0][2]);
+                float2* a10 = reinterpret_cast<float2*>(&acc[r][1][0]);
+                float2* a11 = reinterpret_cast<float2*>(&acc[r][1][2]);
+                *a00 = __ffma2_rn(s0, make_float2(d0[0], d0[1]), *a00);
+                *a01 = __ffma2_rn(s1, make_float2(d0[2], d0[3]), *a01);
+                *a10 = __ffma2_rn(s0, make_float2(d1[0], d1[1]), *a10);
+                *a11 = __ffma2_rn(s1, make_float2(d1[2], d1[3]), *a11);
             }
         }
     };
