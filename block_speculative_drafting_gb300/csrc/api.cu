@@ -3,7 +3,9 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
+#include <functional>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -69,6 +71,8 @@ struct dflash_model {
     // layouts of the packed 4-bit matrices (the same for every layer)
     Q4Layout L_fc{}, L_kvctx{}, L_qkv{}, L_o{}, L_gu{}, L_down{};
     int* err_dev = nullptr;   // raised by a kernel whose bounded wait expired
+    unsigned* chain_bar = nullptr;  // the chain kernel's barrier counter (zero between launches)
+    bool use_chain = false;         // run a block's (and a short append's) steps as chain programs
     int* err_host = nullptr;  // pinned copy, read after a synchronising call
 
     // launch accounting and the optional per-launch event profile
@@ -320,6 +324,15 @@ int build_model(dflash_model* m, const dflash_weights* w, bool on_dev, cudaStrea
     m->L_down = make_layout(H, I);
     CK(m, dalloc(m, &m->err_dev, 1));
     CK(m, cudaMemset(m->err_dev, 0, sizeof(int)));
+    CK(m, dalloc(m, &m->chain_bar, 1));
+    CK(m, cudaMemset(m->chain_bar, 0, sizeof(unsigned)));
+    {
+        // DFLASH_CHAIN=1 runs the steps between two attentions as one persistent
+        // chain kernel each (measured slower than one kernel per step on the
+        // context-2048 block: kept as an option for comparisons)
+        const char* ev = getenv("DFLASH_CHAIN");
+        m->use_chain = ev && ev[0] == '1';
+    }
     CK(m, cudaMallocHost(&m->err_host, sizeof(int)));
     *m->err_host = 0;
     const bool quant = g.quant == DFLASH_QUANT_Q4G32;
@@ -546,6 +559,96 @@ int trace_site(dflash_model* m, cudaStream_t st, int rows, int cols, int8_t* cod
         if (rc__) return rc__;     \
     } while (0)
 
+// ------------------------------------------------------------------ chain programs
+// A matvec stage over the whole (fused) matrix of N rows (N % 64 == 0).
+ChainStage mv_stage(const uint8_t* wp, Q4Layout L, int N, const int8_t* xc, const float* xs, int ldx, int T, float* y,
+                    int ldy) {
+    ChainStage c = {};
+    c.op = kChainMatvec;
+    c.wp = wp;
+    c.L = L;
+    c.g0 = 0;
+    c.ng = N / 64;
+    c.xc = xc;
+    c.xs = xs;
+    c.ldx = ldx;
+    c.T = T;
+    c.y = y;
+    c.ldy = ldy;
+    return c;
+}
+// A row stage (kChainRows: codes of rms(row, w), or of the row itself when
+// w is null; kChainSilu: codes of silu(g) * u of [g | u] rows of 2n).
+ChainStage row_stage(int op, const float* src, int ld_src, RowMap map, int rows, int n, const float* w, float eps,
+                     int8_t* codes, float* scale, int ld_codes, float* zero = nullptr, int64_t zero_n = 0) {
+    ChainStage c = {};
+    c.op = op;
+    c.src = src;
+    c.ld_src = ld_src;
+    c.map = map;
+    c.rows = rows;
+    c.n = n;
+    c.w = w;
+    c.eps = eps;
+    c.codes = codes;
+    c.scale = scale;
+    c.ld_codes = ld_codes;
+    c.zero = zero;
+    c.zero_n = zero_n;
+    return c;
+}
+
+// A chain program being built, with a hook after each stage (tracing: the
+// record of the quantisation site the stage wrote, and a forced decision).
+struct ChainBuild {
+    ChainProgram p{};
+    std::vector<std::function<int()>> hooks;
+    double bytes = 0;
+    void add(const ChainStage& st, double b, std::function<int()> hook = nullptr) {
+        p.s[p.n++] = st;
+        hooks.push_back(std::move(hook));
+        bytes += b;
+    }
+    void clear() {
+        p.n = 0;
+        hooks.clear();
+        bytes = 0;
+    }
+};
+
+// Launch a built program as one chain kernel; with tracing on, one launch
+// per stage with the stage's hook after it (the same device code).
+int run_chain(dflash_model* m, cudaStream_t st, ChainBuild& c) {
+    if (c.p.n == 0) return 0;
+    if (!m->tracing) {
+        KL(m, "chain", 1, c.bytes, st, chain_run(c.p, m->num_sms, m->chain_bar, m->err_dev, st));
+    } else {
+        for (int i = 0; i < c.p.n; ++i) {
+            ChainProgram one{};
+            one.n = 1;
+            one.s[0] = c.p.s[i];
+            KL(m, "chain", 1, 0.0, st, chain_run(one, m->num_sms, m->chain_bar, m->err_dev, st));
+            if (c.hooks[i]) {
+                const int rc = c.hooks[i]();
+                if (rc) return rc;
+            }
+        }
+    }
+    c.clear();
+    return 0;
+}
+
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Whether rows of the block (or of an append) go through chain programs.
+bool chain_ok(const dflash_model* m, int rows) {
+    const dflash_geometry& g = m->g;
+    return m->use_chain && g.quant == DFLASH_QUANT_Q4G32 && rows >= 1 && rows <= 16 && rows < m->num_sms &&
+           m->num_sms >= 16 && g.hidden % 64 == 0 && m->qkv_w % 64 == 0 && (2 * g.intermediate) % 64 == 0 &&
+           m->kvctx_w % 64 == 0 && m->tap_w % 4 == 0 && m->tap_w <= kChainRowMax && g.hidden <= kChainRowMax &&
+           g.intermediate <= kChainRowMax && m->qd <= kChainRowMax && m->qd % 4 == 0 && g.intermediate % 4 == 0;
+}
+
 // Run `enqueue(stream)` (a fixed kernel sequence) on `st`: replayed from a
 // graph captured once per key, or directly when graphs are off (profiling,
 // tracing, or a stream capture of the caller's own in progress).
@@ -598,7 +701,31 @@ int append_rows(dflash_model* m, dflash_seq* s, const float* taps_dev, int64_t n
     RowMap ident{1, 1, 0};
     float* t = P<float>(m->a_t);
     float* kv = P<float>(m->a_kv);
-    if (quant) {
+    if (quant && chain_ok(m, rows) && al16(taps_dev)) {
+        // the same four steps as one chain program
+        int8_t* codes = P<int8_t>(m->a_codes);
+        float* sc = P<float>(m->a_scale);
+        ChainBuild c;
+        c.add(row_stage(kChainRows, taps_dev, m->tap_w, ident, rows, m->tap_w, nullptr, g.eps, codes, sc, m->tap_w, t,
+                        (int64_t)rows * H),
+              (double)rows * m->tap_w * 5, [&]() {
+                  return trace_site(m, st, rows, m->tap_w, codes, m->tap_w, sc, [&](float* v) {
+                      return rms_rows(taps_dev, m->tap_w, ident, rows, m->tap_w, nullptr, g.eps, v, m->tap_w, nullptr,
+                                      nullptr, 0, st);
+                  });
+              });
+        c.add(mv_stage(m->fc_p, m->L_fc, H, codes, sc, m->tap_w, rows, t, H), q4_bytes_of(H, m->tap_w, rows, true));
+        c.add(row_stage(kChainRows, t, H, ident, rows, H, m->hidden_norm, g.eps, codes, sc, H, kv,
+                        (int64_t)rows * m->kvctx_w),
+              (double)rows * H * 5, [&]() {
+                  return trace_site(m, st, rows, H, codes, H, sc, [&](float* v) {
+                      return rms_rows(t, H, ident, rows, H, m->hidden_norm, g.eps, v, H, nullptr, nullptr, 0, st);
+                  });
+              });
+        c.add(mv_stage(m->kvctx_p, m->L_kvctx, m->kvctx_w, codes, sc, H, rows, kv, m->kvctx_w),
+              q4_bytes_of(m->kvctx_w, H, rows, true));
+        APPLY(run_chain(m, st, c));
+    } else if (quant) {
         // taps -> int8 rows (t cleared on the side); t = FC . Q(taps);
         // x = Q(rms(t, hidden_norm)) (kv cleared on the side); kv = [Wk;Wv]_all . x
         int8_t* codes = P<int8_t>(m->a_codes);
@@ -916,6 +1043,76 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
     KL(m, "embed_rows", 1, (double)R * H * 8, st,
        embed_rows(m->embed, H, g.vocab, anchors_dev, g.mask_token, n_seqs, B, h, st, P<int64_t>(m->pos0),
                   m->inv_freq, hd, rope));
+    RowMap drafts{B - 1, B, 1};
+    unsigned long long* keys = P<unsigned long long>(m->keys);
+    uint32_t* tok_out = (io_on_device && draft_tok) ? draft_tok : P<uint32_t>(m->toks);
+    if (quant && chain_ok(m, R)) {
+        // the steps between two attentions as one chain program each:
+        // [x = Q(rms(h, in_norm)); qkv = W x] before the first attention, then per
+        // layer [Q(y); h += O y; x = Q(rms(h, post_norm)); gu = [G; U] x;
+        // a = Q(silu(g) u); h += D a; then the next layer's x and qkv, or the
+        // head's Q(rms(h, norm)) of the draft rows]
+        ChainBuild c;
+        auto add_in = [&](int l) {
+            const Layer& Ly = m->layers[l];
+            c.add(row_stage(kChainRows, h, H, ident, R, H, Ly.in_norm, g.eps, xq, xs, maxK, qkv, (int64_t)R * m->qkv_w),
+                  (double)R * H * 5, [&, l]() {
+                      return trace_site(m, st, R, H, xq, maxK, xs, [&, l](float* v) {
+                          return rms_rows(h, H, ident, R, H, m->layers[l].in_norm, g.eps, v, H, nullptr, nullptr, 0, st);
+                      });
+                  });
+            c.add(mv_stage(Ly.qkv_p, m->L_qkv, m->qkv_w, xq, xs, maxK, R, qkv, m->qkv_w),
+                  q4_bytes_of(m->qkv_w, H, R, true));
+        };
+        add_in(0);
+        APPLY(run_chain(m, st, c));
+        for (int l = 0; l < g.layers; ++l) {
+            const Layer& Ly = m->layers[l];
+            const AttnSeq* aseq_dev = P<AttnSeq>(m->aseqs) + (size_t)l * n_seqs;
+            KL(m, "attention", 1, attn_bytes, st,
+               attention(qkv, m->qkv_w, n_seqs, B, aseq_dev, max_ctx, g.heads, g.kv_heads, hd, scale, P<float>(m->part),
+                         part_floats, y, m->num_sms, st, Ly.q_norm, Ly.k_norm, rope, g.eps));
+            c.add(row_stage(kChainRows, y, m->qd, ident, R, m->qd, nullptr, g.eps, xq, xs, maxK), (double)R * m->qd * 5,
+                  [&]() {
+                      return trace_site(m, st, R, m->qd, xq, maxK, xs, [&](float* v) {
+                          return rms_rows(y, m->qd, ident, R, m->qd, nullptr, g.eps, v, m->qd, nullptr, nullptr, 0, st);
+                      });
+                  });
+            c.add(mv_stage(Ly.o_p, m->L_o, H, xq, xs, maxK, R, h, H), q4_bytes_of(H, m->qd, R, true));
+            c.add(row_stage(kChainRows, h, H, ident, R, H, Ly.post_norm, g.eps, xq, xs, maxK, gu, (int64_t)R * 2 * I),
+                  (double)R * H * 5, [&]() {
+                      return trace_site(m, st, R, H, xq, maxK, xs, [&](float* v) {
+                          return rms_rows(h, H, ident, R, H, Ly.post_norm, g.eps, v, H, nullptr, nullptr, 0, st);
+                      });
+                  });
+            c.add(mv_stage(Ly.gu_p, m->L_gu, 2 * I, xq, xs, maxK, R, gu, 2 * I), q4_bytes_of(2 * I, H, R, true));
+            c.add(row_stage(kChainSilu, gu, 2 * I, ident, R, I, nullptr, g.eps, xq, xs, maxK), (double)R * I * 9, [&]() {
+                return trace_site(m, st, R, I, xq, maxK, xs, [&](float* v) {
+                    return silu_mul(gu, 2 * I, R, I, v, I, nullptr, nullptr, 0, st);
+                });
+            });
+            c.add(mv_stage(Ly.down_p, m->L_down, H, xq, xs, maxK, R, h, H), q4_bytes_of(H, I, R, true));
+            if (l + 1 < g.layers) {
+                add_in(l + 1);
+            } else {
+                c.add(row_stage(kChainRows, h, H, drafts, D, H, m->norm, g.eps, xq, xs, maxK,
+                                reinterpret_cast<float*>(keys), (int64_t)D * 2),
+                      (double)D * H * 5, [&]() {
+                          return trace_site(m, st, D, H, xq, maxK, xs, [&](float* v) {
+                              return rms_rows(h, H, drafts, D, H, m->norm, g.eps, v, H, nullptr, nullptr, 0, st);
+                          });
+                      });
+            }
+            APPLY(run_chain(m, st, c));
+        }
+        QAct xh{xq, xs, maxK};
+        const double hb = (double)g.vocab * H + (double)g.vocab * 4 + (double)D * H + (logit_out ? (double)D * g.vocab * 4 : 0.0);
+        KL(m, "head_stream", 1, hb, st,
+           head_stream(m->head_p, m->head_scale, g.vocab, H / kI8KStep, xh, D, logit_out, g.vocab, keys, m->num_sms,
+                       m->err_dev, st));
+        KL(m, "keys_to_tokens", 1, (double)D * 12, st, keys_to_tokens(keys, D, tok_out, st));
+        return DFLASH_OK;
+    }
     for (int l = 0; l < g.layers; ++l) {
         const Layer& Ly = m->layers[l];
         // attention half: x = rms(h, in_norm); q, k, v; norms and rotation; attention; h += O y
@@ -966,9 +1163,6 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
     }
     // head over the rows after each anchor: row i of the output is row
     // (i / (B-1)) * B + 1 + i % (B-1) of h
-    RowMap drafts{B - 1, B, 1};
-    unsigned long long* keys = P<unsigned long long>(m->keys);
-    uint32_t* tok_out = (io_on_device && draft_tok) ? draft_tok : P<uint32_t>(m->toks);
     if (quant) {
         KL(m, "rms_quant", 1, (double)D * H * 5, st,
            rms_rows(h, H, drafts, D, H, m->norm, g.eps, nullptr, 0, xq, xs, maxK, st, reinterpret_cast<float*>(keys),

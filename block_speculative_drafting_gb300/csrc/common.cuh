@@ -42,6 +42,32 @@ __host__ __device__ __forceinline__ int64_t q4_chunk_offset(const Q4Layout& L, i
     return sc * (4 * 576) + r * 576;
 }
 
+// The share of a streaming CTA: the CTAs of the grid are dealt out to the
+// K-blocks in order (as evenly as they go), and the CTAs of one K-block split
+// its span of super-chunks (groups g0 .. g0 + ng, every k-step of the block)
+// into equal contiguous parts.
+struct StreamGeom {
+    int64_t lo, hi;  // super-chunks of this CTA inside its K-block's span
+    int64_t base;    // global super-chunk index of the span's start
+    int kblk;
+};
+
+__device__ __forceinline__ StreamGeom stream_geom(const Q4Layout& L, int g0, int ng) {
+    const int nkb = L.ksteps / L.kb;
+    const int G = gridDim.x, c = blockIdx.x;
+    const int kblk = (int)((int64_t)c * nkb / G);
+    const int first = (int)(((int64_t)kblk * G + nkb - 1) / nkb);
+    const int nxt = (int)(((int64_t)(kblk + 1) * G + nkb - 1) / nkb);
+    const int cnt = nxt - first, lc = c - first;
+    const int64_t span = (int64_t)ng * L.kb;
+    StreamGeom s;
+    s.lo = span * lc / cnt;
+    s.hi = span * (lc + 1) / cnt;
+    s.base = ((int64_t)kblk * L.ngroups + g0) * L.kb;
+    s.kblk = kblk;
+    return s;
+}
+
 // ---------------------------------------------------------------------------
 // Within a chunk ("q4 tile").
 // A matrix [N][K] (N padded to a multiple of 16, K to a multiple of 64) is cut
@@ -153,6 +179,34 @@ DF_DEV void red_add_v4(float* gaddr, float a, float b, float c, float d) {
                  : "memory");
 }
 
+// Add a warp's partial sums of one 64-row group -- the m16n8k16 C fragments
+// acc[r][h][e] of its four 16-row tiles r and two 8-token halves h (lane
+// 4 gq + tq holds rows gq / gq + 8 of tokens h*8 + 2tq + {0,1}) -- each times
+// its token's activation scale xs[h][e & 1], into y[t][row0 + ...] for
+// tokens t < T.  The fragments of one (tile, half) go through a 512-byte
+// per-warp shared scratch, so that each lane adds four consecutive rows of
+// one token with a single 16-byte vector reduction (y and ldy 16-byte
+// aligned): a quarter of the reductions of one add per value.
+DF_DEV void dump_group_v4(const float (&acc)[4][2][4], const float (&xs)[2][2], float* y, int ldy, int row0, int T,
+                          float* scratch, int lane) {
+    const int gq = lane >> 2, tq = lane & 3;
+    const int t = lane >> 2, q = lane & 3;  // the reading view: token t of the half, rows 4q .. 4q + 3
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            scratch[(2 * tq) * 16 + gq] = acc[r][h][0] * xs[h][0];
+            scratch[(2 * tq + 1) * 16 + gq] = acc[r][h][1] * xs[h][1];
+            scratch[(2 * tq) * 16 + gq + 8] = acc[r][h][2] * xs[h][0];
+            scratch[(2 * tq + 1) * 16 + gq + 8] = acc[r][h][3] * xs[h][1];
+            __syncwarp();
+            const float4 v = *reinterpret_cast<const float4*>(scratch + t * 16 + 4 * q);
+            const int tok = h * 8 + t;
+            if (tok < T) red_add_v4(y + (int64_t)tok * ldy + row0 + r * 16 + 4 * q, v.x, v.y, v.z, v.w);
+            __syncwarp();
+        }
+}
+
 DF_DEV uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
     // (a & b) | c
     uint32_t d;
@@ -230,6 +284,24 @@ DF_DEV float warp_max(float v) {
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
 }
+
+// int8 code of v under scale sx (sx > 0): round half to even of the IEEE
+// quotient, clamped to [-127, 127]
+DF_DEV int8_t code_of(float v, float sx) {
+    float q = rintf(__fdiv_rn(v, sx));
+    q = fminf(fmaxf(q, -127.f), 127.f);
+    return (int8_t)(int)q;
+}
+DF_DEV float amax4(float4 v) { return fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))); }
+// four codes in one word (all zero when sx is 0: a row of zeros)
+DF_DEV uint32_t codes4(float4 v, float sx) {
+    if (!(sx > 0.f)) return 0u;
+    const uint32_t a = (uint8_t)code_of(v.x, sx), b = (uint8_t)code_of(v.y, sx);
+    const uint32_t c = (uint8_t)code_of(v.z, sx), d = (uint8_t)code_of(v.w, sx);
+    return a | (b << 8) | (c << 16) | (d << 24);
+}
+// silu(a) = a / (1 + exp(-a))
+DF_DEV float silu_f(float a) { return a / (1.0f + expf(-a)); }
 
 // Float -> u32 key whose unsigned order is the float order (no NaNs expected).
 DF_DEV uint32_t float_order_key(float f) {

@@ -20,13 +20,6 @@ namespace dflash {
 
 namespace cg = cooperative_groups;
 
-// int8 code of v under scale sx (sx > 0)
-DF_DEV int8_t code_of(float v, float sx) {
-    float q = rintf(__fdiv_rn(v, sx));
-    q = fminf(fmaxf(q, -127.f), 127.f);
-    return (int8_t)(int)q;
-}
-
 constexpr int kRowThreads = 1024;
 
 // Block-wide sum / max over kRowThreads threads.
@@ -94,13 +87,6 @@ __global__ void __launch_bounds__(kRowThreads) rms_rows_kernel(const float* __re
 // the load to the codes.  Rows must be 16-byte aligned, n % 4 == 0 and
 // n <= 4 * NV * kRowThreads.
 DF_DEV bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
-DF_DEV float amax4(float4 v) { return fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))); }
-DF_DEV uint32_t codes4(float4 v, float sx) {
-    if (!(sx > 0.f)) return 0u;
-    const uint32_t a = (uint8_t)code_of(v.x, sx), b = (uint8_t)code_of(v.y, sx);
-    const uint32_t c = (uint8_t)code_of(v.z, sx), d = (uint8_t)code_of(v.w, sx);
-    return a | (b << 8) | (c << 16) | (d << 24);
-}
 
 template <int NV>
 __global__ void __launch_bounds__(kRowThreads) rms_rows_reg_kernel(const float* __restrict__ src, int ld_src, RowMap map,
@@ -309,7 +295,6 @@ int kv_append(const float* kv, int n, int L, int nkv, int hd, const float* const
                        pos_dev, kstore_dev, vstore_dev, cap);
 }
 
-DF_DEV float silu_f(float a) { return a / (1.0f + expf(-a)); }
 
 __global__ void __launch_bounds__(kRowThreads) silu_mul_kernel(const float* __restrict__ gu, int ld_gu, int I,
                                                                float* __restrict__ out_f32, int ld_out,

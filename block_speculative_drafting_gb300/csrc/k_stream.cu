@@ -37,28 +37,7 @@ constexpr int kQ4SlotSC = 2;         // super-chunks per ring slot (one bulk cop
 constexpr int kQ4WarpSlots = 2;      // ring slots per warp
 constexpr int kQ4ActPad = 32;        // halves of row pad: conflict-free 16-byte B-fragment loads
 constexpr int kQ4BarBytes = 1024;    // the warps' mbarriers, ahead of the ring
-
-struct StreamGeom {
-    int64_t lo, hi;  // super-chunks of this CTA inside its K-block's span
-    int64_t base;    // global super-chunk index of the span's start
-    int kblk;
-};
-
-__device__ __forceinline__ StreamGeom stream_geom(const Q4Layout& L, int g0, int ng) {
-    const int nkb = L.ksteps / L.kb;
-    const int G = gridDim.x, c = blockIdx.x;
-    const int kblk = (int)((int64_t)c * nkb / G);
-    const int first = (int)(((int64_t)kblk * G + nkb - 1) / nkb);
-    const int nxt = (int)(((int64_t)(kblk + 1) * G + nkb - 1) / nkb);
-    const int cnt = nxt - first, lc = c - first;
-    const int64_t span = (int64_t)ng * L.kb;
-    StreamGeom s;
-    s.lo = span * lc / cnt;
-    s.hi = span * (lc + 1) / cnt;
-    s.base = ((int64_t)kblk * L.ngroups + g0) * L.kb;
-    s.kblk = kblk;
-    return s;
-}
+constexpr int kQ4DumpBytes = 512;    // a warp's scratch for the vector reductions of a group
 
 // B fragments of one k-step (two 32-column groups, block rows gq and gq + 8)
 // from int8 codes in shared memory: 8 codes per (group, row half) -> 4 half2.
@@ -84,6 +63,9 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
     __half* act = reinterpret_cast<__half*>(sm + kQ4BarBytes + kQ4Warps * (kQ4WarpSlots * kQ4SlotSC * kQ4SC));
     const int kbc = L.kb * kQ4KStep;  // columns of a K-block
     const int ldact = kbc + kQ4ActPad;
+    float* dscr = reinterpret_cast<float*>(sm + kQ4BarBytes + kQ4Warps * (kQ4WarpSlots * kQ4SlotSC * kQ4SC) +
+                                           (size_t)16 * ldact * sizeof(__half)) +
+                  warp * (kQ4DumpBytes / 4);
 
     const StreamGeom sg = stream_geom(L, g0, ng);
     const int64_t span = sg.hi - sg.lo;
@@ -157,21 +139,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
             for (int e = 0; e < 4; ++e) acc[r][h][e] = 0.f;
 
     // a group's partial sums into y (rows >= T are not written)
-    auto dump = [&](int grp) {
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int t = h * 8 + 2 * tq + e;
-                    if (t < T) {
-                        float* yr = y + (int64_t)t * ldy + grp * 64 + r * 16 + gq;
-                        atomicAdd(yr, acc[r][h][e] * xs[h][e]);
-                        atomicAdd(yr + 8, acc[r][h][e + 2] * xs[h][e]);
-                    }
-                }
-    };
+    auto dump = [&](int grp) { dump_group_v4(acc, xs, y, ldy, grp * 64, T, dscr, lane); };
 
     // one super-chunk at scp: k-step ks of group grp
     auto sc_step = [&](const unsigned char* scp, int ks) {
@@ -265,7 +233,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
 
 static size_t q4_stream_bytes(Q4Layout L) {
     return (size_t)kQ4BarBytes + (size_t)kQ4Warps * kQ4WarpSlots * kQ4SlotSC * kQ4SC +
-           (size_t)16 * (L.kb * kQ4KStep + kQ4ActPad) * sizeof(__half);
+           (size_t)16 * (L.kb * kQ4KStep + kQ4ActPad) * sizeof(__half) + (size_t)kQ4Warps * kQ4DumpBytes;
 }
 
 size_t q4_stream_smem_bytes(Q4Layout L, int, int) { return q4_stream_bytes(L); }
@@ -273,7 +241,8 @@ size_t q4_stream_smem_bytes(Q4Layout L, int, int) { return q4_stream_bytes(L); }
 int q4_stream(const uint8_t* packed, Q4Layout L, int tile0, int N, QAct x, int T, float* y, int ldy, int num_sms,
               int* err_flag, cudaStream_t st) {
     if (T <= 0 || N <= 0) return 0;
-    if (T > 16 || N % 64 || tile0 % 4 || L.ksteps / L.kb > num_sms) return (int)cudaErrorInvalidValue;
+    if (T > 16 || N % 64 || tile0 % 4 || L.ksteps / L.kb > num_sms || ldy % 4 || (reinterpret_cast<uintptr_t>(y) & 15))
+        return (int)cudaErrorInvalidValue;
     const size_t smem = q4_stream_bytes(L);
     if (smem > 227 * 1024) return (int)cudaErrorInvalidValue;
     static size_t limit = 0;

@@ -41,6 +41,11 @@ cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// Row maps: output row i reads source row  (i / per) * stride + skip + i % per.
+struct RowMap {
+    int per, stride, skip;
+};
+
 // ---- matmuls (k_gemm.cu, k_stream.cu)
 // Activation operand of the quantised matmuls: int8 codes [rows][ld]
 // (ld >= K, a multiple of 16), one f32 scale a row.
@@ -79,11 +84,53 @@ int argmax_rows(const float* logits, int ldl, int V, int T, unsigned long long* 
 // tokens[t] = index encoded in keys[t].
 int keys_to_tokens(const unsigned long long* keys, int T, uint32_t* tokens, cudaStream_t st);
 
-// ---- layer pieces (k_layer.cu)
-// Row maps: output row i reads source row  (i / per) * stride + skip + i % per.
-struct RowMap {
-    int per, stride, skip;
+// ---- the chain: a persistent kernel (one CTA per SM) that runs a short
+// program of dependent stages of the block's rows, with a grid-wide barrier
+// between stages, and whose warps stream the 4-bit weights of every matvec
+// stage of the program through their rings in program order -- a stage's
+// first weights arrive while earlier stages still run (k_chain.cu).
+enum ChainOp : int {
+    kChainMatvec = 0,  // y[t][n] += xs[t] * sum_g s[n][g] * sum_k q[n][k] x[t][k] (t < T <= 16), as q4_stream
+    kChainRows = 1,    // codes of rms(src row, w) (w == nullptr: of the row itself), one f32 scale a row
+    kChainSilu = 2,    // codes of silu(g) * u, src rows [g (n) | u (n)]
 };
+struct ChainStage {
+    int op;
+    // matvec
+    const uint8_t* wp;
+    Q4Layout L;
+    int g0, ng;  // 64-row groups of the (fused) matrix
+    const int8_t* xc;
+    const float* xs;
+    int ldx, T;
+    float* y;
+    int ldy;
+    // row stages: `rows` rows (row i reads source row map(i)) of n columns
+    const float* src;
+    int ld_src;
+    RowMap map;
+    int rows, n;
+    const float* w;
+    float eps;
+    int8_t* codes;
+    float* scale;
+    int ld_codes;
+    float* zero;  // side duty of a row stage: clear zero_n floats here
+    int64_t zero_n;
+};
+constexpr int kChainMaxStages = 12;
+struct ChainProgram {
+    int n;
+    ChainStage s[kChainMaxStages];
+};
+// Launch a program on num_sms CTAs; bar: a device counter the launch resets
+// and uses for its barriers; err: the model's error flag (raised when a
+// bounded wait expires).  Row stages need rows <= num_sms, n % 4 == 0 and
+// n <= kChainRowMax, 16-byte aligned rows.
+constexpr int kChainRowMax = 4 * 12 * 512;
+int chain_run(const ChainProgram& p, int num_sms, unsigned* bar, int* err, cudaStream_t st);
+
+// ---- layer pieces (k_layer.cu)
 // x = rms(src, w) (w == nullptr: no norm, x = src); then either f32 out
 // (out_f32 != nullptr) or int8 codes + an f32 scale per row.
 // zero_buf / zero_n: a buffer the kernel clears on the side (nullptr: none).

@@ -502,3 +502,20 @@ def test_identical_decisions_parity(name):
             assert np.max(np.abs(k - osq.k[l].transpose(1, 0, 2))) <= 1e-5 * np.max(np.abs(osq.k[l]))
             assert np.max(np.abs(v - osq.v[l].transpose(1, 0, 2))) <= 1e-5 * np.max(np.abs(osq.v[l]))
         seq.close()
+
+
+# ---------------------------------------------------------------- chain programs
+@pytest.mark.parametrize("forced", [True, False])
+def test_chain_programs_match_oracle(forced, monkeypatch):
+    """The same checks with the steps between two attentions run as persistent
+    chain kernels (DFLASH_CHAIN=1 at model creation): whole programs when free
+    running, one launch per stage when the decisions are forced (tracing)."""
+    monkeypatch.setenv("DFLASH_CHAIN", "1")
+    p = Pair("small_q4")
+    g, n = p.g, p.wl.ctx
+    sc = Script(p, 1, n + 16)
+    sc.append(0, 0, W.make_taps(g, n))
+    sc.block([0], [int(W.make_anchors(g, 1)[0])], [n], g.block)
+    sc.append(0, n, W.make_taps(g, 9, call_id=7))   # a short append: one chain program
+    sc.block([0], [5], [n + 9], g.block - 3)
+    sc.run(forced).check(forced)
