@@ -231,6 +231,16 @@ class Model:
                                                     _stream(stream)))
         return out
 
+    def q4_matmul(self, matrix_id: int, x_codes, x_scales, n_rows_out: int, stream=None):
+        """y[r][n] = xs[r] * sum_g s[n][g] sum_k q[n][k] x[r][k] by the library's kernels (the
+        streaming kernel for up to 16 rows, the tensor-core kernel beyond)."""
+        x = np.ascontiguousarray(x_codes, dtype=np.int8)
+        xs = np.ascontiguousarray(x_scales, dtype=np.float32)
+        out = np.empty((x.shape[0], n_rows_out), dtype=np.float32)
+        self._check(lib().dflash_debug_q4_matmul(self.handle, matrix_id, _ptr(x), _ptr(xs), x.shape[0], _ptr(out),
+                                                 _stream(stream)))
+        return out
+
     def trace(self, enable: bool = True):
         self._check(lib().dflash_debug_trace(self.handle, 1 if enable else 0))
 

@@ -21,7 +21,7 @@ namespace {
 thread_local std::string g_init_error;
 
 // Context rows projected per pass of an append (bounds the scratch buffers).
-constexpr int64_t kAppendRows = 1024;
+constexpr int64_t kAppendRows = 8192;
 
 struct DevBuf {
     void* p = nullptr;
@@ -73,6 +73,7 @@ struct dflash_model {
     int* err_dev = nullptr;   // raised by a kernel whose bounded wait expired
     unsigned* chain_bar = nullptr;  // the chain kernel's barrier counter (zero between launches)
     bool use_chain = false;         // run a block's (and a short append's) steps as chain programs
+    bool use_tc = true;             // matmuls of more than 16 rows on the tcgen05 kernel (DFLASH_TC=0: mma.sync)
     int* err_host = nullptr;  // pinned copy, read after a synchronising call
 
     // launch accounting and the optional per-launch event profile
@@ -332,6 +333,8 @@ int build_model(dflash_model* m, const dflash_weights* w, bool on_dev, cudaStrea
         // context-2048 block: kept as an option for comparisons)
         const char* ev = getenv("DFLASH_CHAIN");
         m->use_chain = ev && ev[0] == '1';
+        const char* tv = getenv("DFLASH_TC");
+        m->use_tc = !(tv && tv[0] == '0');
     }
     CK(m, cudaMallocHost(&m->err_host, sizeof(int)));
     *m->err_host = 0;
@@ -490,11 +493,31 @@ int q4_mm(dflash_model* m, const uint8_t* packed, Q4Layout L, int tile0, int N, 
     if (T <= 16) {
         KL(m, "q4_stream", 1, q4_bytes_of(N, K, T, true), st,
            q4_stream(packed, L, tile0, N, x, T, y, ldy, m->num_sms, m->err_dev, st));
+    } else if (m->use_tc && q4_tc_supported(L, tile0, N, K, x) && ldy % 4 == 0 &&
+               (reinterpret_cast<uintptr_t>(y) & 15) == 0) {
+        KL(m, "q4_tc", 1, q4_bytes_of(N, K, T, accumulate), st,
+           q4_tc(packed, L, tile0, N, x, T, y, ldy, accumulate, m->num_sms, m->err_dev, st));
     } else {
         KL(m, "q4_gemm", 1, q4_bytes_of(N, K, T, accumulate), st,
            q4_gemm(packed, L, tile0, N, x, T, y, ldy, accumulate, m->num_sms, st));
     }
     return 0;
+}
+
+// The head over D rows: the streaming kernel (one pass over the head per 16
+// rows) for a single block, the tcgen05 kernel for many rows.
+int run_head(dflash_model* m, QAct xh, int D, float* logit_out, unsigned long long* keys, double hb, cudaStream_t st) {
+    const dflash_geometry& g = m->g;
+    const int H = g.hidden;
+    if (D > 16 && m->use_tc && head_tc_supported(H / kI8KStep, xh)) {
+        KL(m, "head_tc", 1, hb, st,
+           head_tc(m->head_p, m->head_scale, g.vocab, H / kI8KStep, xh, D, logit_out, g.vocab, keys, m->err_dev, st));
+    } else {
+        KL(m, "head_stream", 1, hb, st,
+           head_stream(m->head_p, m->head_scale, g.vocab, H / kI8KStep, xh, D, logit_out, g.vocab, keys, m->num_sms,
+                       m->err_dev, st));
+    }
+    return DFLASH_OK;
 }
 
 // Apply one matrix to the block's rows.  Quantised format: the int8 codes in
@@ -1107,9 +1130,7 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
         }
         QAct xh{xq, xs, maxK};
         const double hb = (double)g.vocab * H + (double)g.vocab * 4 + (double)D * H + (logit_out ? (double)D * g.vocab * 4 : 0.0);
-        KL(m, "head_stream", 1, hb, st,
-           head_stream(m->head_p, m->head_scale, g.vocab, H / kI8KStep, xh, D, logit_out, g.vocab, keys, m->num_sms,
-                       m->err_dev, st));
+        APPLY(run_head(m, xh, D, logit_out, keys, hb, st));
         KL(m, "keys_to_tokens", 1, (double)D * 12, st, keys_to_tokens(keys, D, tok_out, st));
         return DFLASH_OK;
     }
@@ -1172,9 +1193,7 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
         }));
         QAct xh{xq, xs, maxK};
         const double hb = (double)g.vocab * H + (double)g.vocab * 4 + (double)D * H + (logit_out ? (double)D * g.vocab * 4 : 0.0);
-        KL(m, "head_stream", 1, hb, st,
-           head_stream(m->head_p, m->head_scale, g.vocab, H / kI8KStep, xh, D, logit_out, g.vocab, keys, m->num_sms,
-                       m->err_dev, st));
+        APPLY(run_head(m, xh, D, logit_out, keys, hb, st));
     } else {
         KL(m, "rms_f32", 1, (double)D * H * 8, st, rms_rows(h, H, drafts, D, H, m->norm, g.eps, xf, maxK, nullptr, nullptr, 0, st,
                                                          reinterpret_cast<float*>(keys), (int64_t)D * 2));
@@ -1415,6 +1434,50 @@ int dflash_debug_q4_groupsums(dflash_model* m, int32_t id, const int8_t* x, int3
     cudaFree(dsc);
     cudaFree(dout);
     CK(m, e);
+    return DFLASH_OK;
+}
+
+int dflash_debug_q4_matmul(dflash_model* m, int32_t id, const int8_t* x, const float* xs, int32_t rows, float* y,
+                           void* stream) {
+    int rc = check_model(m);
+    if (rc) return rc;
+    if (m->g.quant != DFLASH_QUANT_Q4G32 || id == DFLASH_MAT_HEAD || !x || !xs || !y || rows < 1)
+        return set_err(m, DFLASH_EINVAL, "bad arguments");
+    MatView v = mat_view(m, id);
+    if (!v.packed) return set_err(m, DFLASH_EINVAL, "bad matrix id");
+    cudaStream_t st = (cudaStream_t)stream;
+    const int ldk = v.L.ksteps * kQ4KStep;
+    std::vector<int8_t> hx((size_t)rows * ldk, 0);
+    for (int r = 0; r < rows; ++r)
+        for (int k = 0; k < v.K; ++k) {
+            int xv = x[(size_t)r * v.K + k];
+            if (xv < -127) return set_err(m, DFLASH_EINVAL, "activation code -128");
+            hx[(size_t)r * ldk + k] = (int8_t)xv;
+        }
+    int8_t* dx = nullptr;
+    float* dsc = nullptr;
+    float* dy = nullptr;
+    const size_t outn = (size_t)rows * v.N;
+    CK(m, cudaMalloc(&dx, hx.size()));
+    CK(m, cudaMalloc(&dsc, rows * sizeof(float)));
+    CK(m, cudaMalloc(&dy, outn * sizeof(float)));
+    int e = (int)cudaMemcpyAsync(dx, hx.data(), hx.size(), cudaMemcpyHostToDevice, st);
+    if (!e) e = (int)cudaMemcpyAsync(dsc, xs, rows * sizeof(float), cudaMemcpyHostToDevice, st);
+    // the streaming kernel adds into y: start from zeros on every path
+    if (!e) e = (int)cudaMemsetAsync(dy, 0, outn * sizeof(float), st);
+    QAct qa{dx, dsc, ldk};
+    int lib_rc = DFLASH_OK;
+    if (!e) lib_rc = q4_mm(m, v.packed, v.L, v.tile0, v.N, v.K, qa, rows, dy, v.N, false, st);
+    if (!e && lib_rc == DFLASH_OK) e = (int)cudaMemcpyAsync(y, dy, outn * sizeof(float), cudaMemcpyDeviceToHost, st);
+    if (!e && lib_rc == DFLASH_OK)
+        e = (int)cudaMemcpyAsync(m->err_host, m->err_dev, sizeof(int), cudaMemcpyDeviceToHost, st);
+    if (!e) e = (int)cudaStreamSynchronize(st);
+    cudaFree(dx);
+    cudaFree(dsc);
+    cudaFree(dy);
+    if (lib_rc != DFLASH_OK) return lib_rc;
+    CK(m, (cudaError_t)e);
+    if (*m->err_host) return device_wait_expired(m);
     return DFLASH_OK;
 }
 

@@ -38,6 +38,28 @@ constexpr int kQ4WarpSlots = 2;      // ring slots per warp
 constexpr int kQ4ActPad = 32;        // halves of row pad: conflict-free 16-byte B-fragment loads
 constexpr int kQ4BarBytes = 1024;    // the warps' mbarriers, ahead of the ring
 constexpr int kQ4DumpBytes = 512;    // a warp's scratch for the vector reductions of a group
+// The offsets the unpacking leaves in the weights are taken out by the MMA's
+// C input: per 32-column group g of the K-block and 8-row half h of the
+// block's rows, lane quad tq reads {-1032 X[t0], -1032 X[t1], -72 X[t0],
+// -72 X[t1]} (t0 = 8 h + 2 tq, t1 = t0 + 1; X[t] the group's sum of row t's
+// activation codes) -- the m16n8k16 C fragment of weight rows gq (offset
+// 1032) and gq + 8 (offset 72).
+constexpr int kQ4OffBytes = (32 * kQ4KStep / 32) * 2 * 4 * 16;  // 64 groups x 2 halves x 4 quads x 16 B
+
+// Eight offset nibbles (code + 8) -> four half2 of the m16n8k16 A fragment
+// with the offsets left in: the low nibbles (rows gq) ORed into the mantissa
+// of 1024.0h read 1024 + nibble = 1032 + code, the high nibbles (rows gq + 8)
+// ORed into that of 64.0h (unit 1/16) read 64 + nibble = 72 + code.  One LOP3
+// per half2.
+DF_DEV void unpack_q4_word_biased(uint32_t w, uint32_t (&a)[4]) {
+    const uint32_t kLo = 0x000F000Fu, kHi = 0x00F000F0u;
+    const uint32_t kM1024 = 0x64006400u, kM64 = 0x54005400u;
+    a[0] = lop3_and_or(w, kLo, kM1024);
+    a[1] = lop3_and_or(w, kHi, kM64);
+    const uint32_t w8 = w >> 8;
+    a[2] = lop3_and_or(w8, kLo, kM1024);
+    a[3] = lop3_and_or(w8, kHi, kM64);
+}
 
 // B fragments of one k-step (two 32-column groups, block rows gq and gq + 8)
 // from int8 codes in shared memory: 8 codes per (group, row half) -> 4 half2.
@@ -66,6 +88,8 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
     float* dscr = reinterpret_cast<float*>(sm + kQ4BarBytes + kQ4Warps * (kQ4WarpSlots * kQ4SlotSC * kQ4SC) +
                                            (size_t)16 * ldact * sizeof(__half)) +
                   warp * (kQ4DumpBytes / 4);
+    float4* offs = reinterpret_cast<float4*>(sm + kQ4BarBytes + kQ4Warps * (kQ4WarpSlots * kQ4SlotSC * kQ4SC) +
+                                             (size_t)16 * ldact * sizeof(__half) + (size_t)kQ4Warps * kQ4DumpBytes);
 
     const StreamGeom sg = stream_geom(L, g0, ng);
     const int64_t span = sg.hi - sg.lo;
@@ -94,6 +118,9 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
         // the K-block's codes of the 16 rows as exact f16 (rows past T are
         // zero), eight loads of a thread in flight at once
         const int vec = kbc / 8, total = 16 * vec;
+        // X[t][g]: the sums of each row's codes over each 32-column group,
+        // gathered first as integers in the offset area
+        int* xsum = reinterpret_cast<int*>(offs) + (kQ4OffBytes / 4) / 2;  // [16][64], the area's upper half
         constexpr int kBatch = 8;
         for (int base = threadIdx.x; base < total; base += kBatch * kQ4Threads) {
             uint2 v[kBatch];
@@ -107,14 +134,34 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
 #pragma unroll
             for (int u = 0; u < kBatch; ++u) {
                 const int i = base + u * kQ4Threads, r = i / vec, c = i - r * vec;
+                // four consecutive vectors (threads) make a group: vec and the
+                // thread count are multiples of 4, so a quad never straddles rows
+                int gs = __dp4a((int)v[u].x, 0x01010101, __dp4a((int)v[u].y, 0x01010101, 0));
+                gs += __shfl_xor_sync(0xffffffffu, gs, 1);
+                gs += __shfl_xor_sync(0xffffffffu, gs, 2);
                 if (i < total) {
                     uint4 h;
                     i8x4_to_half2x2(v[u].x, h.x, h.y);
                     i8x4_to_half2x2(v[u].y, h.z, h.w);
                     *reinterpret_cast<uint4*>(act + r * ldact + c * 8) = h;
+                    if ((c & 3) == 0) xsum[r * 64 + (c >> 2)] = gs;
                 }
             }
         }
+        __syncthreads();
+        // the C-fragment table from the sums: entry j = (g, h, tq), at most
+        // (kbc / 32) * 8 <= 512 entries, one a thread; the table overwrites
+        // the sums, so every thread reads before any writes
+        const int j = threadIdx.x;
+        const bool has = j < (kbc / 32) * 8;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (has) {
+            const int g = j >> 3, h = (j >> 2) & 1, tq = j & 3, t0 = 8 * h + 2 * tq;
+            const float x0 = (float)xsum[t0 * 64 + g], x1 = (float)xsum[(t0 + 1) * 64 + g];
+            o = make_float4(-1032.f * x0, -1032.f * x1, -72.f * x0, -72.f * x1);
+        }
+        __syncthreads();
+        if (has) offs[j] = o;
         __syncthreads();
     }
     const int gq = lane >> 2, tq = lane & 3;
@@ -149,6 +196,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
             bq[gi][0] = *reinterpret_cast<const uint4*>(a_lo + ks * kQ4KStep + gi * 32);
             bq[gi][1] = *reinterpret_cast<const uint4*>(a_hi + ks * kQ4KStep + gi * 32);
         }
+        const float4* ok = offs + (2 * ks) * 8 + tq;  // entries (group 2 ks + gi, half h) at ok[gi * 8 + h * 4]
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const uint4 wv = *reinterpret_cast<const uint4*>(scp + r * kQ4Chunk + lane * 16);
@@ -158,12 +206,16 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
 #pragma unroll
             for (int gi = 0; gi < 2; ++gi) {
                 uint32_t a0[4], a1[4];
-                unpack_q4_word(wds[gi * 2 + 0], a0);
-                unpack_q4_word(wds[gi * 2 + 1], a1);
+                unpack_q4_word_biased(wds[gi * 2 + 0], a0);
+                unpack_q4_word_biased(wds[gi * 2 + 1], a1);
+                // the offsets' C fragments (re-read per tile: registers are short)
+                const float4 o0 = ok[gi * 8], o1 = ok[gi * 8 + 4];
+                const float c0[4] = {o0.x, o0.y, o0.z, o0.w}, c1[4] = {o1.x, o1.y, o1.z, o1.w};
                 float d0[4], d1[4];
-                mma_f16_16816(d0, a0, bq[gi][0].x, bq[gi][0].y, zero);
+                // group sums are exact integers below 2^23 at every step
+                mma_f16_16816(d0, a0, bq[gi][0].x, bq[gi][0].y, c0);
                 mma_f16_16816(d0, a1, bq[gi][0].z, bq[gi][0].w, d0);
-                mma_f16_16816(d1, a0, bq[gi][1].x, bq[gi][1].y, zero);
+                mma_f16_16816(d1, a0, bq[gi][1].x, bq[gi][1].y, c1);
                 mma_f16_16816(d1, a1, bq[gi][1].z, bq[gi][1].w, d1);
                 // the group's f16 scales of rows gq and gq + 8, each as an f32
                 // pair, for packed f32x2 fused multiply-adds (same rounding as
@@ -233,7 +285,8 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
 
 static size_t q4_stream_bytes(Q4Layout L) {
     return (size_t)kQ4BarBytes + (size_t)kQ4Warps * kQ4WarpSlots * kQ4SlotSC * kQ4SC +
-           (size_t)16 * (L.kb * kQ4KStep + kQ4ActPad) * sizeof(__half) + (size_t)kQ4Warps * kQ4DumpBytes;
+           (size_t)16 * (L.kb * kQ4KStep + kQ4ActPad) * sizeof(__half) + (size_t)kQ4Warps * kQ4DumpBytes +
+           (size_t)kQ4OffBytes;
 }
 
 size_t q4_stream_smem_bytes(Q4Layout L, int, int) { return q4_stream_bytes(L); }

@@ -1,0 +1,587 @@
+// Dense contractions of many rows on the fifth-generation tensor cores
+// (tcgen05): the 4-bit g32 matrices of page "cortiq-engine 0.8.75 —
+// src/gpu_wgpu/dflash_dev.rs" (`Dev::q4`: four-bit codes with one scale per
+// 32 columns against int8 activations) and the int8 head (`Dev::q8`, the
+// head of page "cortiq-engine 0.8.71 — src/dflash.rs", `block_dev`) applied
+// to a batch of rows: the prefill of many context rows
+// (`Drafter::settle_rows`) and the blocks of many sequences at once.
+//
+// 4-bit: y[t][n] = xs[t] * sum_k (s[n][k/32] q[n][k]) x[t][k], the quantised
+// matvec with the group scale folded into the weight.  s (f16) times q
+// (-8..7) needs up to 14 significant bits, so the weight goes to the tensor
+// core as the exact sum of two f16 values, hi = f16(s q) and
+// lo = f16(s q - hi) (an fma; the remainder is representable), and every k
+// slice runs two MMAs (x . hi + x . lo).  The int8 codes of x are exact in
+// f16, so every product is exact.
+// Head: logits[t][n] = xs[t] * sw[n] * sum_k q[n][k] x[t][k], one MMA a k
+// slice on exact f16 integers, and the draft token's argmax (lowest index
+// among equal values) folded into the epilogue.
+//
+// Accumulation.  The tensor core's f32 accumulation truncates, which over
+// long K shrinks sums measurably; so tensor memory only ever holds a chunk of
+// kTcChunk k-blocks (512 columns), in two alternating accumulators, and the
+// converter warps drain each finished chunk into registers: round-to-nearest
+// f32 adds for the 4-bit matrices, exact int32 adds for the head (a chunk's
+// integer sum is below 512 * 127 * 127 < 2^24, so the f32 chunk value is the
+// exact integer).
+//
+// One CTA computes a 128-row x 128-output tile, D[t][n], in tensor memory
+// (128 lanes x 128 f32 columns per accumulator).  Roles:
+//   warp 8 (one lane): TMA -- the int8 activation tile of each 64-column
+//     k-block (cp.async.bulk.tensor over a tensor map of the codes) and the
+//     packed weights of the k-block's two 64-row groups (cp.async.bulk), into
+//     a ring of raw stages;
+//   warps 0-7: convert a raw stage into a converted stage (activations to
+//     f16; weights to f16, or to the hi and lo f16 tiles) in the K-major
+//     128-byte-swizzled layout the MMA descriptors name; drain finished
+//     chunks; run the epilogue (warp w reads tensor-memory lanes
+//     32 (w % 4) .., columns 64 (w / 4) ..);
+//   warp 9: allocates the tensor memory; one lane issues the MMAs
+//     (tcgen05.mma kind::f16, M 128, N 128, K 16) and commits every converted
+//     stage and every finished chunk.
+// Every wait is bounded (1 s of %globaltimer): on expiry the kernel raises the
+// error flag, the roles stop, copies and MMAs in flight are waited for
+// (bounded), and the tensor memory is freed.
+#include <cuda.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace dflash {
+
+constexpr int kTcM = 128;    // rows of a tile: MMA M, tensor-memory lanes
+constexpr int kTcN = 128;    // outputs of a tile: MMA N, tensor-memory columns of one accumulator
+constexpr int kTcKB = 64;    // columns of a k-block: one 128-byte swizzle row of f16
+constexpr int kTcChunk = 8;  // k-blocks accumulated in tensor memory before a drain
+constexpr int kTcCvt = 2;    // converted stages
+constexpr int kTcCvtWarps = 8;
+constexpr int kTcThreads = (kTcCvtWarps + 2) * 32;
+constexpr int kTcTmaWarp = kTcCvtWarps, kTcMmaWarp = kTcCvtWarps + 1;
+constexpr int kTcCols = 64;  // accumulator columns a converter thread drains
+constexpr uint64_t kTcWait = 1000000000ull;  // ns a wait may take before the kernel gives up
+static_assert(kTcChunk >= 3, "a chunk is drained at the third k-block of the next one");
+static_assert(kTcCvtWarps * 32 * kTcCols == kTcM * kTcN, "drain split");
+
+constexpr int kTcMaxRaw = 9;  // raw stages at most (the control block's barrier arrays)
+// Raw stages are compact (int8 activations, packed weights), so the ring is
+// deep: enough bytes in flight to cover the load latency at the tensor cores'
+// pace; converted stages (f16) are double-buffered.
+template <bool kHead>
+struct TcShape {
+    static constexpr int kWRaw = kHead ? 2 * kI8Super : 2 * 4 * kQ4Chunk;  // two 64-row groups of one k-block
+    static constexpr int kRawBytes = kTcM * kTcKB + kWRaw;                   // + the int8 activation tile
+    static constexpr int kA = kTcM * kTcKB * 2;                              // f16 activation tile, swizzled
+    static constexpr int kB = kTcN * kTcKB * 2;                              // f16 weight tile, swizzled
+    static constexpr int kCvtBytes = kA + (kHead ? 1 : 2) * kB;
+    static constexpr int kRaw = kHead ? 9 : 8;                               // raw stages
+    static constexpr size_t kSmem = 1024 /*alignment slack*/ + 1024 /*control*/ + (size_t)kTcCvt * kCvtBytes +
+                                    (size_t)kRaw * kRawBytes;
+    static_assert(kCvtBytes % 1024 == 0 && kRawBytes % 128 == 0, "stage alignment");
+    static_assert(kRaw <= kTcMaxRaw && kSmem <= 227 * 1024, "shared memory");
+};
+
+// Instruction descriptor of tcgen05.mma kind::f16: D f32 (bits 4-5 = 1), A and
+// B f16 (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 at bits
+// 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t kTcIdesc = (1u << 4) | ((uint32_t)(kTcN >> 3) << 17) | ((uint32_t)(kTcM >> 4) << 24);
+
+// Shared-memory matrix descriptor: a K-major tile with 128-byte rows in the
+// 128-byte swizzle (eight-row atoms of 1024 bytes, stride 1024 bytes between
+// atoms), base 1024-aligned; the k16 slice j starts 32 j bytes into the rows.
+DF_DEV uint64_t tc_desc_sw128(uint32_t saddr) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// byte offset of the 16-byte chunk c (columns 8c .. 8c+7) of row r in such a tile
+DF_DEV uint32_t tc_swz(int r, int c) { return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4)); }
+
+DF_DEV void tc_mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(kTcIdesc), "r"(accumulate)
+        : "memory");
+}
+DF_DEV void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+DF_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+DF_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 16 consecutive f32 columns of this thread's tensor-memory lane (whole warp)
+DF_DEV void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+DF_DEV void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+DF_DEV void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(smem_addr(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// hi / lo of s * q for four half2 of codes q
+DF_DEV void split_scaled(const uint32_t (&q)[4], uint32_t s2, uint4& hi, uint4& lo) {
+    const __half2 s = *reinterpret_cast<const __half2*>(&s2);
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __half2 qi = *reinterpret_cast<const __half2*>(&q[i]);
+        const __half2 hh = __hmul2(qi, s);
+        const __half2 ll = __hfma2(qi, s, __hneg2(hh));
+        h[i] = *reinterpret_cast<const uint32_t*>(&hh);
+        l[i] = *reinterpret_cast<const uint32_t*>(&ll);
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+struct TcCtl {
+    uint64_t raw_full[kTcMaxRaw], raw_empty[kTcMaxRaw], cvt_full[kTcCvt], cvt_empty[kTcCvt], dfull[2], dempty[2], fin;
+    uint32_t tmem;
+    int abort;
+};
+static_assert(sizeof(TcCtl) <= 1024, "control block");
+
+struct TcArgs {
+    const uint8_t* w;          // 4-bit: packed matrix; head: int8 super-chunks
+    Q4Layout L;                // 4-bit layout (head: ksteps only)
+    int g0;                    // first 64-row group of the sub-matrix (4-bit)
+    int N;                     // outputs (4-bit: multiple of 64; head: vocab)
+    const float* xscale;       // [T]
+    int T;
+    float* y;                  // [T][ldy] (head: logits, may be null)
+    int ldy;
+    int accumulate;            // 4-bit: add into y
+    int kb_per_split;          // k-blocks per CTA along grid z
+    const float* wscale;       // head: row scales [>= N]
+    unsigned long long* keys;  // head: argmax keys [T]
+    int* err;
+};
+
+template <bool kHead>
+__global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_constant__ CUtensorMap xmap, TcArgs a) {
+    using S = TcShape<kHead>;
+    extern __shared__ __align__(1024) unsigned char sm_raw[];
+    // 1024-aligned base (the swizzled tiles need it)
+    unsigned char* sm = sm_raw + ((1024 - (smem_addr(sm_raw) & 1023)) & 1023);
+    TcCtl& ctl = *reinterpret_cast<TcCtl*>(sm);
+    unsigned char* cvt = sm + 1024;
+    unsigned char* raw = cvt + kTcCvt * S::kCvtBytes;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * kTcM, nt = blockIdx.y;
+    const int ksteps = a.L.ksteps;
+    const int kb_lo = blockIdx.z * a.kb_per_split, kb_hi = min(ksteps, kb_lo + a.kb_per_split);
+    const int nkb = kb_hi - kb_lo;
+    const int nchunks = (nkb + kTcChunk - 1) / kTcChunk;
+    const int ngroups_n = (a.N + 63) / 64;  // 64-row groups of the outputs
+
+    constexpr int kTcRaw = S::kRaw;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kTcRaw; ++i) {
+            mbar_init(&ctl.raw_full[i], 1);
+            mbar_init(&ctl.raw_empty[i], kTcCvtWarps);
+        }
+        for (int i = 0; i < kTcCvt; ++i) {
+            mbar_init(&ctl.cvt_full[i], kTcCvtWarps);
+            mbar_init(&ctl.cvt_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ctl.dfull[i], 1);
+            mbar_init(&ctl.dempty[i], kTcCvtWarps);
+        }
+        mbar_init(&ctl.fin, 1);
+        ctl.abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kTcMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&ctl.tmem)),
+                     "r"(2 * kTcN)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl.tmem;
+    pdl_trigger();
+    pdl_wait();
+
+    auto give_up = [&]() {
+        atomicExch(a.err, 1);
+        *reinterpret_cast<volatile int*>(&ctl.abort) = 1;
+    };
+    auto aborted = [&]() { return *reinterpret_cast<volatile int*>(&ctl.abort) != 0; };
+
+    if (warp == kTcTmaWarp) {
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&xmap) : "memory");
+            int issued = 0;
+            int ng = 0;  // valid 64-row groups of this tile
+            for (int gg = 0; gg < kTcN / 64; ++gg) ng += (nt * (kTcN / 64) + gg < ngroups_n) ? 1 : 0;
+            const int wbytes = kHead ? kI8Super : 4 * kQ4Chunk;
+            for (int i = 0; i < nkb; ++i) {
+                const int r = i % kTcRaw;
+                if (i >= kTcRaw && !mbar_wait(&ctl.raw_empty[r], ((i / kTcRaw) - 1) & 1, kTcWait)) {
+                    give_up();
+                    break;
+                }
+                if (aborted()) break;
+                fence_proxy_async_smem();
+                const int kb = kb_lo + i;
+                unsigned char* dst = raw + r * S::kRawBytes;
+                mbar_arrive_expect_tx(&ctl.raw_full[r], (uint32_t)(kTcM * kTcKB + ng * wbytes));
+                tma_load_2d(dst, &xmap, kb * kTcKB, m0, &ctl.raw_full[r]);
+                for (int gg = 0; gg < ng; ++gg) {
+                    const int grp = nt * (kTcN / 64) + gg;
+                    const uint8_t* src = kHead ? a.w + ((int64_t)grp * ksteps + kb) * kI8Super
+                                               : a.w + q4_chunk_offset(a.L, 4 * (a.g0 + grp), kb);
+                    bulk_g2s(dst + kTcM * kTcKB + gg * wbytes, src, (uint32_t)wbytes, &ctl.raw_full[r]);
+                }
+                issued = i + 1;
+            }
+            // copies still in flight land before the CTA can leave
+            for (int i = max(0, issued - kTcRaw); i < issued; ++i)
+                mbar_wait(&ctl.raw_full[i % kTcRaw], (i / kTcRaw) & 1, kTcWait);
+        }
+    } else if (warp == kTcMmaWarp) {
+        if (lane == 0) {
+            for (int i = 0; i < nkb; ++i) {
+                const int st = i % kTcCvt, ch = i / kTcChunk, buf = ch & 1;
+                const bool first = i % kTcChunk == 0;
+                bool ok = true;
+                if (first && ch >= 2) ok = mbar_wait(&ctl.dempty[buf], ((ch >> 1) - 1) & 1, kTcWait);
+                if (ok) ok = mbar_wait(&ctl.cvt_full[st], (i / kTcCvt) & 1, kTcWait);
+                if (!ok) give_up();
+                if (!ok || aborted()) break;
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(buf * kTcN);
+                const uint32_t sa = smem_addr(cvt + st * S::kCvtBytes);
+                const uint32_t sb = sa + S::kA;
+#pragma unroll
+                for (int j = 0; j < kTcKB / 16; ++j) {
+                    tc_mma(d, tc_desc_sw128(sa + 32 * j), tc_desc_sw128(sb + 32 * j), (first && j == 0) ? 0u : 1u);
+                    if (!kHead) tc_mma(d, tc_desc_sw128(sa + 32 * j), tc_desc_sw128(sb + S::kB + 32 * j), 1u);
+                }
+                tc_commit(&ctl.cvt_empty[st]);
+                if (i % kTcChunk == kTcChunk - 1 || i == nkb - 1) tc_commit(&ctl.dfull[buf]);
+            }
+            // arrives once every MMA issued so far has completed (the memory is freed after it)
+            tc_commit(&ctl.fin);
+            mbar_wait(&ctl.fin, 0, kTcWait);
+        }
+    } else {
+        // ---------------------------------------------------------------- converters
+        const int tid = threadIdx.x;  // 0 .. 255
+        const int sub = warp & 3, half = warp >> 2;
+        const uint32_t lane_base = (uint32_t)(32 * sub) << 16;
+        float facc[kTcCols];
+        int32_t iacc[kTcCols];
+#pragma unroll
+        for (int j = 0; j < kTcCols; ++j) {
+            facc[j] = 0.f;
+            iacc[j] = 0;
+        }
+        bool ok = true;
+        int drained = 0;
+        // add finished chunk `ch` (tensor-memory accumulator ch & 1) into the registers
+        auto drain = [&](int ch) {
+            const int buf = ch & 1;
+            const bool w = mbar_wait(&ctl.dfull[buf], (ch >> 1) & 1, kTcWait);
+            if (!w) give_up();
+            if (__any_sync(0xffffffffu, !w || aborted())) {
+                ok = false;
+                return;
+            }
+            tc_fence_after();
+            const uint32_t base = tmem + lane_base + (uint32_t)(buf * kTcN + half * kTcCols);
+#pragma unroll
+            for (int c = 0; c < kTcCols; c += 16) {
+                uint32_t r[16];
+                tc_ld16(base + (uint32_t)c, r);
+                tc_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    if (kHead)
+                        iacc[c + q] += (int32_t)__uint_as_float(r[q]);
+                    else
+                        facc[c + q] += __uint_as_float(r[q]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl.dempty[buf]);
+        };
+
+        for (int i = 0; i < nkb && ok; ++i) {
+            const int r = i % kTcRaw, c = i % kTcCvt;
+            bool w = mbar_wait(&ctl.raw_full[r], (i / kTcRaw) & 1, kTcWait);
+            if (w && i >= kTcCvt) w = mbar_wait(&ctl.cvt_empty[c], ((i / kTcCvt) - 1) & 1, kTcWait);
+            if (!w) give_up();
+            // warp-uniform: every lane leaves together
+            if (__any_sync(0xffffffffu, !w || aborted())) {
+                ok = false;
+                break;
+            }
+            const unsigned char* rs = raw + r * S::kRawBytes;
+            unsigned char* cs = cvt + c * S::kCvtBytes;
+            // activations: 128 rows x 4 runs of 16 codes
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int task = tid + u * 256, row = task >> 2, c16 = task & 3;
+                const uint4 v = *reinterpret_cast<const uint4*>(rs + row * kTcKB + c16 * 16);
+                uint4 h0, h1;
+                i8x4_to_half2x2(v.x, h0.x, h0.y);
+                i8x4_to_half2x2(v.y, h0.z, h0.w);
+                i8x4_to_half2x2(v.z, h1.x, h1.y);
+                i8x4_to_half2x2(v.w, h1.z, h1.w);
+                *reinterpret_cast<uint4*>(cs + tc_swz(row, 2 * c16)) = h0;
+                *reinterpret_cast<uint4*>(cs + tc_swz(row, 2 * c16 + 1)) = h1;
+            }
+            // weights: 8 chunks of 16 rows x 64 columns, one lane slot each
+            {
+                const int gg = warp >> 2, rr = warp & 3;
+                const int gq = lane >> 2, tq = lane & 3;
+                const int nl0 = gg * 64 + rr * 16 + gq, nl1 = nl0 + 8;
+                unsigned char* bt = cs + S::kA;
+                const bool valid = nt * (kTcN / 64) + gg < ngroups_n;
+                if (kHead) {
+                    uint4 r0[2], r1[2];  // [gi]: rows gq, gq + 8
+                    if (valid) {
+                        const unsigned char* ch = rs + kTcM * kTcKB + gg * kI8Super + rr * kI8Chunk + lane * 32;
+                        const uint4 w0 = *reinterpret_cast<const uint4*>(ch);
+                        const uint4 w1 = *reinterpret_cast<const uint4*>(ch + 16);
+                        // word (gi, s, up) at index (gi * 2 + s) * 2 + up: four codes of row gq + 8 up
+                        // at columns 32 gi + 8 tq + 4 s + 0..3
+                        const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                        for (int gi = 0; gi < 2; ++gi) {
+                            i8x4_to_half2x2(wd[(gi * 2 + 0) * 2 + 0], r0[gi].x, r0[gi].y);
+                            i8x4_to_half2x2(wd[(gi * 2 + 1) * 2 + 0], r0[gi].z, r0[gi].w);
+                            i8x4_to_half2x2(wd[(gi * 2 + 0) * 2 + 1], r1[gi].x, r1[gi].y);
+                            i8x4_to_half2x2(wd[(gi * 2 + 1) * 2 + 1], r1[gi].z, r1[gi].w);
+                        }
+                    } else {
+                        r0[0] = r0[1] = r1[0] = r1[1] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+#pragma unroll
+                    for (int gi = 0; gi < 2; ++gi) {
+                        *reinterpret_cast<uint4*>(bt + tc_swz(nl0, 4 * gi + tq)) = r0[gi];
+                        *reinterpret_cast<uint4*>(bt + tc_swz(nl1, 4 * gi + tq)) = r1[gi];
+                    }
+                } else {
+                    unsigned char* blo = bt + S::kB;
+                    if (valid) {
+                        const unsigned char* ch = rs + kTcM * kTcKB + gg * 4 * kQ4Chunk + rr * kQ4Chunk;
+                        const uint4 wv = *reinterpret_cast<const uint4*>(ch + lane * 16);
+                        const uint2 sv = *reinterpret_cast<const uint2*>(ch + 512 + gq * 8);
+                        const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                        for (int gi = 0; gi < 2; ++gi) {
+                            uint32_t a0[4], a1[4];
+                            unpack_q4_word(wd[gi * 2 + 0], a0);  // columns 8 tq + 0..3
+                            unpack_q4_word(wd[gi * 2 + 1], a1);  // columns 8 tq + 4..7
+                            const uint32_t sw = gi ? sv.y : sv.x;  // (s[gq][g], s[gq+8][g])
+                            const uint32_t s0 = __byte_perm(sw, 0, 0x1010), s1 = __byte_perm(sw, 0, 0x3232);
+                            const uint32_t q0[4] = {a0[0], a0[2], a1[0], a1[2]};  // row gq
+                            const uint32_t q1[4] = {a0[1], a0[3], a1[1], a1[3]};  // row gq + 8
+                            uint4 hi, lo;
+                            split_scaled(q0, s0, hi, lo);
+                            *reinterpret_cast<uint4*>(bt + tc_swz(nl0, 4 * gi + tq)) = hi;
+                            *reinterpret_cast<uint4*>(blo + tc_swz(nl0, 4 * gi + tq)) = lo;
+                            split_scaled(q1, s1, hi, lo);
+                            *reinterpret_cast<uint4*>(bt + tc_swz(nl1, 4 * gi + tq)) = hi;
+                            *reinterpret_cast<uint4*>(blo + tc_swz(nl1, 4 * gi + tq)) = lo;
+                        }
+                    } else {
+                        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                        for (int gi = 0; gi < 2; ++gi) {
+                            *reinterpret_cast<uint4*>(bt + tc_swz(nl0, 4 * gi + tq)) = z;
+                            *reinterpret_cast<uint4*>(blo + tc_swz(nl0, 4 * gi + tq)) = z;
+                            *reinterpret_cast<uint4*>(bt + tc_swz(nl1, 4 * gi + tq)) = z;
+                            *reinterpret_cast<uint4*>(blo + tc_swz(nl1, 4 * gi + tq)) = z;
+                        }
+                    }
+                }
+            }
+            // the converted tiles are read by the tensor cores (async proxy)
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&ctl.raw_empty[r]);
+                mbar_arrive(&ctl.cvt_full[c]);
+            }
+            // chunk ch - 1 is finished by now or soon (its last MMAs went out
+            // before k-block i - 2 was converted): drain it while the tensor
+            // cores run chunk ch
+            if (i % kTcChunk == 2 && i >= kTcChunk) {
+                drain(i / kTcChunk - 1);
+                ++drained;
+            }
+        }
+        while (ok && drained < nchunks) drain(drained++);
+
+        // ---------------------------------------------------------------- epilogue
+        if (ok) {
+            const int t = m0 + 32 * sub + lane;
+            const int n0 = nt * kTcN + half * kTcCols;
+            if (kHead) {
+                unsigned long long best = 0ull;
+                if (t < a.T) {
+                    const float xs = a.xscale[t];
+                    const bool vec = a.y != nullptr && (a.ldy & 3) == 0;
+#pragma unroll
+                    for (int q = 0; q < kTcCols / 4; ++q) {
+                        const int n = n0 + 4 * q;
+                        if (n >= a.N) break;
+                        float l[4];
+                        if (n + 4 <= a.N) {
+                            // the head's row scales are padded to whole 64-row groups
+                            const float4 sw = *reinterpret_cast<const float4*>(a.wscale + n);
+                            l[0] = xs * sw.x * (float)iacc[4 * q];
+                            l[1] = xs * sw.y * (float)iacc[4 * q + 1];
+                            l[2] = xs * sw.z * (float)iacc[4 * q + 2];
+                            l[3] = xs * sw.w * (float)iacc[4 * q + 3];
+                            if (vec)
+                                *reinterpret_cast<float4*>(a.y + (int64_t)t * a.ldy + n) = make_float4(l[0], l[1], l[2], l[3]);
+                            else if (a.y)
+                                for (int e = 0; e < 4; ++e) a.y[(int64_t)t * a.ldy + n + e] = l[e];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) best = max(best, argmax_key(l[e], (uint32_t)(n + e)));
+                        } else {
+                            for (int e = 0; e < 4 && n + e < a.N; ++e) {
+                                const float le = xs * a.wscale[n + e] * (float)iacc[4 * q + e];
+                                if (a.y) a.y[(int64_t)t * a.ldy + n + e] = le;
+                                best = max(best, argmax_key(le, (uint32_t)(n + e)));
+                            }
+                        }
+                    }
+                    if (best) atomicMax(a.keys + t, best);
+                }
+            } else if (t < a.T && n0 < a.N) {
+                const float xs = a.xscale[t];
+                float* dst = a.y + (int64_t)t * a.ldy + n0;
+                const bool red = a.accumulate != 0 || gridDim.z > 1;
+#pragma unroll
+                for (int q = 0; q < kTcCols / 4; ++q) {
+                    const float v0 = facc[4 * q] * xs, v1 = facc[4 * q + 1] * xs, v2 = facc[4 * q + 2] * xs,
+                                v3 = facc[4 * q + 3] * xs;
+                    if (red)
+                        red_add_v4(dst + 4 * q, v0, v1, v2, v3);
+                    else
+                        *reinterpret_cast<float4*>(dst + 4 * q) = make_float4(v0, v1, v2, v3);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kTcMmaWarp) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * kTcN) : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        else
+            cudaGetLastError();
+    }
+    return fn;
+}
+
+// the tensor map of the int8 activation codes [T][K] (row stride ld bytes): 64 x 128 boxes
+static bool act_map(CUtensorMap* map, const int8_t* codes, int K, int T, int ld) {
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)T};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld};
+    const cuuint32_t box[2] = {(cuuint32_t)kTcKB, (cuuint32_t)kTcM};
+    const cuuint32_t estr[2] = {1, 1};
+    return encode_fn()(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(codes), dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool kHead>
+static cudaError_t tc_set_smem() {
+    static bool done = false;
+    if (done) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<kHead>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)TcShape<kHead>::kSmem);
+    if (e == cudaSuccess) done = true;
+    return e;
+}
+
+bool q4_tc_supported(Q4Layout L, int tile0, int N, int K, QAct x) {
+    return encode_fn() != nullptr && tile0 % 4 == 0 && N % 64 == 0 && N > 0 && K == L.ksteps * kQ4KStep &&
+           x.ld % 16 == 0 && (reinterpret_cast<uintptr_t>(x.codes) & 15) == 0;
+}
+
+int q4_tc(const uint8_t* packed, Q4Layout L, int tile0, int N, QAct x, int T, float* y, int ldy, bool accumulate,
+          int num_sms, int* err_flag, cudaStream_t st) {
+    if (T <= 0 || N <= 0) return 0;
+    const int K = L.ksteps * kQ4KStep;
+    if (!q4_tc_supported(L, tile0, N, K, x) || ldy % 4 || (reinterpret_cast<uintptr_t>(y) & 15))
+        return (int)cudaErrorInvalidValue;
+    CUtensorMap map;
+    if (!act_map(&map, x.codes, K, T, x.ld)) return (int)cudaErrorInvalidValue;
+    cudaError_t e = tc_set_smem<false>();
+    if (e != cudaSuccess) return (int)e;
+    const int mt = (T + kTcM - 1) / kTcM, ntl = (N + kTcN - 1) / kTcN;
+    // split K over CTAs when the tiles alone leave most SMs idle
+    int splits = 1;
+    if (mt * ntl * 2 <= num_sms) splits = std::min(std::max(1, num_sms / (mt * ntl)), std::max(1, L.ksteps / 8));
+    const int kps = (L.ksteps + splits - 1) / splits;
+    splits = (L.ksteps + kps - 1) / kps;
+    if (splits > 1 && !accumulate) {
+        e = cudaMemset2DAsync(y, (size_t)ldy * sizeof(float), 0, (size_t)N * sizeof(float), T, st);
+        if (e != cudaSuccess) return (int)e;
+    }
+    TcArgs args{packed, L, tile0 / 4, N, x.scale, T, y, ldy, accumulate ? 1 : 0, kps, nullptr, nullptr, err_flag};
+    return (int)launch(tc_gemm_kernel<false>, dim3(mt, ntl, splits), dim3(kTcThreads), TcShape<false>::kSmem, st, map,
+                       args);
+}
+
+bool head_tc_supported(int ksteps, QAct x) {
+    return encode_fn() != nullptr && ksteps > 0 && x.ld % 16 == 0 && (reinterpret_cast<uintptr_t>(x.codes) & 15) == 0;
+}
+
+int head_tc(const int8_t* packed, const float* row_scale, int V, int ksteps, QAct x, int T, float* logits, int ldl,
+            unsigned long long* keys, int* err_flag, cudaStream_t st) {
+    if (T <= 0 || V <= 0) return 0;
+    if (!head_tc_supported(ksteps, x)) return (int)cudaErrorInvalidValue;
+    CUtensorMap map;
+    if (!act_map(&map, x.codes, ksteps * kI8KStep, T, x.ld)) return (int)cudaErrorInvalidValue;
+    cudaError_t e = tc_set_smem<true>();
+    if (e != cudaSuccess) return (int)e;
+    const int mt = (T + kTcM - 1) / kTcM, ntl = (V + kTcN - 1) / kTcN;
+    Q4Layout L{0, ksteps, 1};
+    TcArgs args{reinterpret_cast<const uint8_t*>(packed), L, 0, V, x.scale, T, logits, ldl, 0, ksteps, row_scale,
+                keys, err_flag};
+    return (int)launch(tc_gemm_kernel<true>, dim3(mt, ntl, 1), dim3(kTcThreads), TcShape<true>::kSmem, st, map, args);
+}
+
+}  // namespace dflash

@@ -63,6 +63,21 @@ int q4_gemm(const uint8_t* packed, Q4Layout L, int tile0, int N, QAct x, int T, 
 // The int32 group sums of the same inner loop (T <= 16): out[t][n][g].
 int q4_groupsums(const uint8_t* packed, Q4Layout L, int tile0, int N, QAct x, int T, int32_t* out, cudaStream_t st);
 
+// The same product for many rows on the tcgen05 tensor cores (k_tc.cu):
+// 128-row x 256-output tiles, the 4-bit weights dequantised in shared memory
+// to exact hi + lo f16 pairs, f32 accumulation in tensor memory.  Needs
+// tile0 % 4 == 0, N % 64 == 0, x.ld % 16 == 0, 16-byte aligned codes, y and
+// ldy (q4_tc_supported); err_flag is raised when a bounded wait expires.
+bool q4_tc_supported(Q4Layout L, int tile0, int N, int K, QAct x);
+int q4_tc(const uint8_t* packed, Q4Layout L, int tile0, int N, QAct x, int T, float* y, int ldy, bool accumulate,
+          int num_sms, int* err_flag, cudaStream_t st);
+// The head for many rows on the same kernel (exact int32 row sums, drained
+// from tensor memory every 512 columns): logits (may be nullptr) and the
+// argmax keys as head_stream.
+bool head_tc_supported(int ksteps, QAct x);
+int head_tc(const int8_t* packed, const float* row_scale, int V, int ksteps, QAct x, int T, float* logits, int ldl,
+            unsigned long long* keys, int* err_flag, cudaStream_t st);
+
 // The streaming form for up to 16 rows: every CTA streams a contiguous slice
 // of the matrix (tile0 and N multiples of 64 rows) through a bulk-copy ring
 // and ADDS its partial sums into y (which must hold zeros or the residual).

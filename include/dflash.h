@@ -277,6 +277,20 @@ DFLASH_API int dflash_debug_q4_groupsums(dflash_model* model, int32_t matrix_id,
                               void* stream);
 
 /*
+ * One 4-bit matmul of the library on given int8 activation codes, through
+ * the same dispatch the path uses (the streaming kernel for rows <= 16, the
+ * tcgen05 tensor-core kernel beyond, where its alignment rules hold):
+ * y[r][n] = xs[r] * sum_g s[n][g] * sum_{k in g} q[n][k] x[r][k]
+ * (page "cortiq-engine 0.8.75 -- src/gpu_wgpu/dflash_dev.rs", `Dev::q4`,
+ * with one activation scale per row).  x [rows][cols] int8 (|x| <= 127), xs
+ * [rows] f32, y [rows][rows_of_matrix] f32, all host memory; the call
+ * synchronises the stream.  Errors: EINVAL (f32 model, bad id, rows < 1,
+ * code -128), ECUDA.
+ */
+DFLASH_API int dflash_debug_q4_matmul(dflash_model* model, int32_t matrix_id, const int8_t* x, const float* xs,
+                                      int32_t rows, float* y, void* stream);
+
+/*
  * The stored keys and values of context positions [pos, pos + n) of one
  * layer: k and v [n][kv_heads][head_dim] f32 (either may be NULL).
  * Errors: EINVAL, ERANGE (positions not held), ECUDA.

@@ -191,7 +191,10 @@ class OracleSeq:
     per KV head, the keys (normed, rotated) and values of the positions the
     layer still holds (``dropped`` rows left its window)."""
 
-    ROWS_PER_PASS = 1024  # context rows projected at a time (rows are independent)
+    # context rows projected at a time.  Rows are independent, so this only
+    # groups the quantisation trace's records (one per pass and site); it is
+    # the library's append pass, so that traced decisions line up one to one.
+    ROWS_PER_PASS = 8192
 
     def __init__(self, model):
         self.m = model

@@ -133,6 +133,32 @@ def test_group_sums_bit_exact(rows):
         np.testing.assert_array_equal(got, Q.q4_group_sums(x, rq).astype(np.int32))
 
 
+@pytest.mark.parametrize("name,rows", [("small_q4", 300), ("small_q4", 17), ("small_q4", 128),
+                                       ("small_q4_hd64", 200), ("small_q4", 9)])
+def test_q4_matmul_matches_definition(name, rows):
+    """The library's 4-bit matmul on given int8 rows (streaming kernel up to
+    16 rows, tcgen05 kernel beyond: several 128-row tiles, ragged rows,
+    sub-matrices at a row offset inside fused matrices, a ragged 256-row
+    weight tile) against the quantised definition on the library's own codes:
+    every product is exact on both paths, only the f32 accumulation rounds."""
+    dfl = _dfl()
+    p = pair(name)
+    rng = np.random.default_rng(rows)
+    mats = [(dfl.MAT_FC, p.w["fc"])]
+    for which in ("q", "k", "up", "down"):
+        mats.append((dfl.mat_layer(1, which), p.w["layers"][1][which]))
+    for mid, w in mats:
+        x = rng.integers(-127, 128, size=(rows, w.shape[1]), dtype=np.int8)
+        x[0, :7] = 127
+        x[-1, -9:] = -127
+        xs = (rng.random(rows).astype(np.float32) + 0.5) / 127
+        got = p.gpu.q4_matmul(mid, x, xs, w.shape[0])
+        codes, scales = p.gpu.q4_codes(mid, *w.shape)
+        ref = Q.q4_matvec_by_definition(x, xs, codes, scales.view(np.float16))
+        err = float(np.max(np.abs(got - ref)))
+        assert err <= 2e-5 * float(np.max(np.abs(ref))), (mid, err, float(np.max(np.abs(ref))))
+
+
 # ---------------------------------------------------------------- context append
 @pytest.mark.parametrize("name", ["tiny_f32", "small_q4", "small_q4_hd64"])
 def test_kv_append_matches_oracle(name):
@@ -304,6 +330,22 @@ def test_batched_sequences(name):
     sc.block([0, 1, 2], [11, 12, 13], lens, g.block)
     sc.block([2, 0], [14, 15], [61, 7], 5)
     sc.run().check()
+
+
+@pytest.mark.parametrize("name", ["small_q4", "small_q4_hd64"])
+@pytest.mark.parametrize("forced", [True, False])
+def test_batched_many_sequences(name, forced):
+    """Ten sequences in one call: every matmul and the head run on the
+    tensor-core kernels with two 128-row tiles (the second ragged) and a
+    ragged last vocabulary tile."""
+    p = pair(name)
+    g = p.g
+    lens = [5, 0, 33, 44, 12, 1, 40, 27, 9, 44]
+    sc = Script(p, len(lens), 64)
+    for i, n in enumerate(lens):
+        sc.append(i, 0, W.make_taps(g, n, call_id=40 + i))
+    sc.block(list(range(len(lens))), [(37 * i + 5) % g.vocab for i in range(len(lens))], lens, g.block)
+    sc.run(forced).check(forced)
 
 
 def test_truncate_and_reappend():

@@ -97,6 +97,8 @@ WORKLOADS = {
     "qwen3_8b_batch32_ctx4096": Workload("qwen3_8b_batch32_ctx4096", Geometry(**QWEN3_8B_DRAFT), ctx=4096, n_seqs=32),
     # one append of 8192 target rows
     "qwen3_8b_prefill8192": Workload("qwen3_8b_prefill8192", Geometry(**QWEN3_8B_DRAFT), ctx=0, prefill=8192),
+    # the same kernels on 1024 rows: the small case for profiler captures
+    "qwen3_8b_prefill1024": Workload("qwen3_8b_prefill1024", Geometry(**QWEN3_8B_DRAFT), ctx=0, prefill=1024),
     # small quantised shapes the oracle finishes in seconds: several tiles and
     # ragged tails (vocab and context not multiples of any tile)
     "small_q4": Workload("small_q4", Geometry(hidden=512, intermediate=1536, layers=2, heads=8, kv_heads=2,
