@@ -112,6 +112,7 @@ struct dflash_model {
     // before it allocates; calls of the same sizes allocate nothing)
     DevBuf h, xq, xs, qkv, y, gu, logits, keys, toks, part, anchors, pos0, aseqs, rope;
     DevBuf a_taps, a_codes, a_scale, a_t, a_kv, a_pos;
+    DevBuf x16;  // activation codes as f16 for the tcgen05 kernels (matmuls of more than 16 rows)
     bool grown = false;  // a scratch buffer moved since the graphs were captured
 
     // CUDA graphs of the kernel sequences of a block and of a short append,
@@ -494,9 +495,11 @@ int q4_mm(dflash_model* m, const uint8_t* packed, Q4Layout L, int tile0, int N, 
         KL(m, "q4_stream", 1, q4_bytes_of(N, K, T, true), st,
            q4_stream(packed, L, tile0, N, x, T, y, ldy, m->num_sms, m->err_dev, st));
     } else if (m->use_tc && q4_tc_supported(L, tile0, N, K, x) && ldy % 4 == 0 &&
-               (reinterpret_cast<uintptr_t>(y) & 15) == 0) {
+               (reinterpret_cast<uintptr_t>(y) & 15) == 0 && m->x16.bytes >= (size_t)T * K * sizeof(__half)) {
+        __half* x16 = P<__half>(m->x16);
+        KL(m, "act_f16", 1, (double)T * K * 3, st, codes_to_f16(x.codes, x.ld, T, K, x16, m->num_sms, st));
         KL(m, "q4_tc", 1, q4_bytes_of(N, K, T, accumulate), st,
-           q4_tc(packed, L, tile0, N, x, T, y, ldy, accumulate, m->num_sms, m->err_dev, st));
+           q4_tc(packed, L, tile0, N, x, x16, T, y, ldy, accumulate, m->num_sms, m->err_dev, st));
     } else {
         KL(m, "q4_gemm", 1, q4_bytes_of(N, K, T, accumulate), st,
            q4_gemm(packed, L, tile0, N, x, T, y, ldy, accumulate, m->num_sms, st));
@@ -509,9 +512,13 @@ int q4_mm(dflash_model* m, const uint8_t* packed, Q4Layout L, int tile0, int N, 
 int run_head(dflash_model* m, QAct xh, int D, float* logit_out, unsigned long long* keys, double hb, cudaStream_t st) {
     const dflash_geometry& g = m->g;
     const int H = g.hidden;
-    if (D > 16 && m->use_tc && head_tc_supported(H / kI8KStep, xh)) {
+    if (D > 16 && m->use_tc && head_tc_supported(H / kI8KStep, xh) &&
+        m->x16.bytes >= (size_t)D * H * sizeof(__half)) {
+        __half* x16 = P<__half>(m->x16);
+        KL(m, "act_f16", 1, (double)D * H * 3, st, codes_to_f16(xh.codes, xh.ld, D, H, x16, m->num_sms, st));
         KL(m, "head_tc", 1, hb, st,
-           head_tc(m->head_p, m->head_scale, g.vocab, H / kI8KStep, xh, D, logit_out, g.vocab, keys, m->err_dev, st));
+           head_tc(m->head_p, m->head_scale, g.vocab, H / kI8KStep, xh, x16, D, logit_out, g.vocab, keys, m->err_dev,
+                   st));
     } else {
         KL(m, "head_stream", 1, hb, st,
            head_stream(m->head_p, m->head_scale, g.vocab, H / kI8KStep, xh, D, logit_out, g.vocab, keys, m->num_sms,
@@ -793,6 +800,8 @@ int ensure_append_scratch(dflash_model* m, int64_t rows) {
     CK(m, ensure_m(m, m->a_t, r * m->g.hidden * sizeof(float)));
     CK(m, ensure_m(m, m->a_kv, r * m->kvctx_w * sizeof(float)));
     CK(m, ensure_m(m, m->a_pos, 2 * sizeof(int64_t)));
+    if (quant && rows > 16)
+        CK(m, ensure_m(m, m->x16, r * std::max(m->tap_w, m->g.hidden) * sizeof(__half)));
     return 0;
 }
 
@@ -844,7 +853,8 @@ void dflash_free(dflash_model* m) {
     if (m->cap_stream) cudaStreamDestroy(m->cap_stream);
     for (void* p : m->owned) cudaFree(p);
     for (DevBuf* b : {&m->h, &m->xq, &m->xs, &m->qkv, &m->y, &m->gu, &m->logits, &m->keys, &m->toks, &m->part,
-                      &m->anchors, &m->pos0, &m->aseqs, &m->a_taps, &m->a_codes, &m->a_scale, &m->a_t, &m->a_kv})
+                      &m->anchors, &m->pos0, &m->aseqs, &m->rope, &m->a_taps, &m->a_codes, &m->a_scale, &m->a_t,
+                      &m->a_kv, &m->a_pos, &m->x16, &m->trace_buf})
         free_buf(*b);
     delete m;
 }
@@ -1022,6 +1032,7 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
     CK(m, ensure_m(m, m->pos0, (size_t)n_seqs * sizeof(int64_t)));
     CK(m, ensure_m(m, m->rope, (size_t)R * (hd / 2) * sizeof(float2)));
     CK(m, ensure_m(m, m->aseqs, (size_t)g.layers * n_seqs * sizeof(AttnSeq)));
+    if (quant && R > 16) CK(m, ensure_m(m, m->x16, (size_t)R * maxK * sizeof(__half)));
     float* logit_out = io_on_device ? logits : nullptr;
     if (!io_on_device && logits) {
         CK(m, ensure_m(m, m->logits, (size_t)D * g.vocab * sizeof(float)));
@@ -1465,6 +1476,7 @@ int dflash_debug_q4_matmul(dflash_model* m, int32_t id, const int8_t* x, const f
     if (!e) e = (int)cudaMemcpyAsync(dsc, xs, rows * sizeof(float), cudaMemcpyHostToDevice, st);
     // the streaming kernel adds into y: start from zeros on every path
     if (!e) e = (int)cudaMemsetAsync(dy, 0, outn * sizeof(float), st);
+    if (!e && rows > 16) e = ensure_m(m, m->x16, (size_t)rows * ldk * sizeof(__half));
     QAct qa{dx, dsc, ldk};
     int lib_rc = DFLASH_OK;
     if (!e) lib_rc = q4_mm(m, v.packed, v.L, v.tile0, v.N, v.K, qa, rows, dy, v.N, false, st);

@@ -27,15 +27,15 @@
 //
 // One CTA computes a 128-row x 128-output tile, D[t][n], in tensor memory
 // (128 lanes x 128 f32 columns per accumulator).  Roles:
-//   warp 8 (one lane): TMA -- the int8 activation tile of each 64-column
-//     k-block (cp.async.bulk.tensor over a tensor map of the codes) and the
-//     packed weights of the k-block's two 64-row groups (cp.async.bulk), into
-//     a ring of raw stages;
-//   warps 0-7: convert a raw stage into a converted stage (activations to
-//     f16; weights to f16, or to the hi and lo f16 tiles) in the K-major
-//     128-byte-swizzled layout the MMA descriptors name; drain finished
-//     chunks; run the epilogue (warp w reads tensor-memory lanes
-//     32 (w % 4) .., columns 64 (w / 4) ..);
+//   warp 8 (one lane): TMA -- the f16 activation tile of each 64-column
+//     k-block (cp.async.bulk.tensor over a tensor map of the activation
+//     codes as f16, 128-byte swizzle: it lands in the layout the MMA reads)
+//     into the activation ring, and the packed weights of the k-block's two
+//     64-row groups (cp.async.bulk) into the raw ring;
+//   warps 0-7: convert a raw stage into a converted stage (weights to f16,
+//     or to the hi and lo f16 tiles) in the K-major 128-byte-swizzled layout
+//     the MMA descriptors name; drain finished chunks; run the epilogue
+//     (warp w reads tensor-memory lanes 32 (w % 4) .., columns 64 (w / 4) ..);
 //   warp 9: allocates the tensor memory; one lane issues the MMAs
 //     (tcgen05.mma kind::f16, M 128, N 128, K 16) and commits every converted
 //     stage and every finished chunk.
@@ -55,7 +55,7 @@ constexpr int kTcM = 128;    // rows of a tile: MMA M, tensor-memory lanes
 constexpr int kTcN = 128;    // outputs of a tile: MMA N, tensor-memory columns of one accumulator
 constexpr int kTcKB = 64;    // columns of a k-block: one 128-byte swizzle row of f16
 constexpr int kTcChunk = 8;  // k-blocks accumulated in tensor memory before a drain
-constexpr int kTcCvt = 2;    // converted stages
+constexpr int kTcCvt = 3;    // converted stages
 constexpr int kTcCvtWarps = 8;
 constexpr int kTcThreads = (kTcCvtWarps + 2) * 32;
 constexpr int kTcTmaWarp = kTcCvtWarps, kTcMmaWarp = kTcCvtWarps + 1;
@@ -64,20 +64,20 @@ constexpr uint64_t kTcWait = 1000000000ull;  // ns a wait may take before the ke
 static_assert(kTcChunk >= 3, "a chunk is drained at the third k-block of the next one");
 static_assert(kTcCvtWarps * 32 * kTcCols == kTcM * kTcN, "drain split");
 
-constexpr int kTcMaxRaw = 9;  // raw stages at most (the control block's barrier arrays)
-// Raw stages are compact (int8 activations, packed weights), so the ring is
-// deep: enough bytes in flight to cover the load latency at the tensor cores'
-// pace; converted stages (f16) are double-buffered.
+constexpr int kTcMaxRaw = 12;  // raw stages at most (the control block's barrier arrays)
+constexpr int kTcAct = 4;      // activation stages
+constexpr int kTcA = kTcM * kTcKB * 2;  // f16 activation tile (swizzled by the TMA)
+// Raw stages are compact (packed weights), so the ring is deep: enough bytes
+// in flight to cover the load latency at the tensor cores' pace; converted
+// stages (f16) are double-buffered.
 template <bool kHead>
 struct TcShape {
-    static constexpr int kWRaw = kHead ? 2 * kI8Super : 2 * 4 * kQ4Chunk;  // two 64-row groups of one k-block
-    static constexpr int kRawBytes = kTcM * kTcKB + kWRaw;                   // + the int8 activation tile
-    static constexpr int kA = kTcM * kTcKB * 2;                              // f16 activation tile, swizzled
-    static constexpr int kB = kTcN * kTcKB * 2;                              // f16 weight tile, swizzled
-    static constexpr int kCvtBytes = kA + (kHead ? 1 : 2) * kB;
-    static constexpr int kRaw = kHead ? 9 : 8;                               // raw stages
-    static constexpr size_t kSmem = 1024 /*alignment slack*/ + 1024 /*control*/ + (size_t)kTcCvt * kCvtBytes +
-                                    (size_t)kRaw * kRawBytes;
+    static constexpr int kRawBytes = kHead ? 2 * kI8Super : 2 * 4 * kQ4Chunk;  // two 64-row groups of one k-block
+    static constexpr int kB = kTcN * kTcKB * 2;                                 // f16 weight tile, swizzled
+    static constexpr int kCvtBytes = (kHead ? 1 : 2) * kB;
+    static constexpr int kRaw = kHead ? 8 : 10;                                 // raw stages
+    static constexpr size_t kSmem = 1024 /*alignment slack*/ + 1024 /*control*/ + (size_t)kTcAct * kTcA +
+                                    (size_t)kTcCvt * kCvtBytes + (size_t)kRaw * kRawBytes;
     static_assert(kCvtBytes % 1024 == 0 && kRawBytes % 128 == 0, "stage alignment");
     static_assert(kRaw <= kTcMaxRaw && kSmem <= 227 * 1024, "shared memory");
 };
@@ -146,7 +146,8 @@ DF_DEV void split_scaled(const uint32_t (&q)[4], uint32_t s2, uint4& hi, uint4& 
 }
 
 struct TcCtl {
-    uint64_t raw_full[kTcMaxRaw], raw_empty[kTcMaxRaw], cvt_full[kTcCvt], cvt_empty[kTcCvt], dfull[2], dempty[2], fin;
+    uint64_t raw_full[kTcMaxRaw], raw_empty[kTcMaxRaw], act_full[kTcAct], act_empty[kTcAct], cvt_full[kTcCvt],
+        cvt_empty[kTcCvt], dfull[2], dempty[2], fin;
     uint32_t tmem;
     int abort;
 };
@@ -175,10 +176,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     // 1024-aligned base (the swizzled tiles need it)
     unsigned char* sm = sm_raw + ((1024 - (smem_addr(sm_raw) & 1023)) & 1023);
     TcCtl& ctl = *reinterpret_cast<TcCtl*>(sm);
-    unsigned char* cvt = sm + 1024;
+    unsigned char* act = sm + 1024;
+    unsigned char* cvt = act + kTcAct * kTcA;
     unsigned char* raw = cvt + kTcCvt * S::kCvtBytes;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * kTcM, nt = blockIdx.y;
+    // tile order: the 4-bit matmuls run the output tiles of one row tile
+    // together (x = output tile), so that its activations are read from HBM
+    // once and reused from L2 (the packed weights fit in L2); the head runs
+    // the row tiles of one output tile together (x = row tile): its weights
+    // are the large operand
+    const int m0 = (kHead ? blockIdx.x : blockIdx.y) * kTcM, nt = kHead ? blockIdx.y : blockIdx.x;
     const int ksteps = a.L.ksteps;
     const int kb_lo = blockIdx.z * a.kb_per_split, kb_hi = min(ksteps, kb_lo + a.kb_per_split);
     const int nkb = kb_hi - kb_lo;
@@ -190,6 +197,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         for (int i = 0; i < kTcRaw; ++i) {
             mbar_init(&ctl.raw_full[i], 1);
             mbar_init(&ctl.raw_empty[i], kTcCvtWarps);
+        }
+        for (int i = 0; i < kTcAct; ++i) {
+            mbar_init(&ctl.act_full[i], 1);
+            mbar_init(&ctl.act_empty[i], 1);
         }
         for (int i = 0; i < kTcCvt; ++i) {
             mbar_init(&ctl.cvt_full[i], kTcCvtWarps);
@@ -230,28 +241,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
             for (int gg = 0; gg < kTcN / 64; ++gg) ng += (nt * (kTcN / 64) + gg < ngroups_n) ? 1 : 0;
             const int wbytes = kHead ? kI8Super : 4 * kQ4Chunk;
             for (int i = 0; i < nkb; ++i) {
-                const int r = i % kTcRaw;
-                if (i >= kTcRaw && !mbar_wait(&ctl.raw_empty[r], ((i / kTcRaw) - 1) & 1, kTcWait)) {
-                    give_up();
-                    break;
-                }
-                if (aborted()) break;
+                const int r = i % kTcRaw, sa = i % kTcAct;
+                bool ok = true;
+                if (i >= kTcRaw) ok = mbar_wait(&ctl.raw_empty[r], ((i / kTcRaw) - 1) & 1, kTcWait);
+                if (ok && i >= kTcAct) ok = mbar_wait(&ctl.act_empty[sa], ((i / kTcAct) - 1) & 1, kTcWait);
+                if (!ok) give_up();
+                if (!ok || aborted()) break;
                 fence_proxy_async_smem();
                 const int kb = kb_lo + i;
+                mbar_arrive_expect_tx(&ctl.act_full[sa], (uint32_t)kTcA);
+                tma_load_2d(act + sa * kTcA, &xmap, kb * kTcKB, m0, &ctl.act_full[sa]);
                 unsigned char* dst = raw + r * S::kRawBytes;
-                mbar_arrive_expect_tx(&ctl.raw_full[r], (uint32_t)(kTcM * kTcKB + ng * wbytes));
-                tma_load_2d(dst, &xmap, kb * kTcKB, m0, &ctl.raw_full[r]);
+                mbar_arrive_expect_tx(&ctl.raw_full[r], (uint32_t)(ng * wbytes));
                 for (int gg = 0; gg < ng; ++gg) {
                     const int grp = nt * (kTcN / 64) + gg;
                     const uint8_t* src = kHead ? a.w + ((int64_t)grp * ksteps + kb) * kI8Super
                                                : a.w + q4_chunk_offset(a.L, 4 * (a.g0 + grp), kb);
-                    bulk_g2s(dst + kTcM * kTcKB + gg * wbytes, src, (uint32_t)wbytes, &ctl.raw_full[r]);
+                    bulk_g2s(dst + gg * wbytes, src, (uint32_t)wbytes, &ctl.raw_full[r]);
                 }
                 issued = i + 1;
             }
             // copies still in flight land before the CTA can leave
             for (int i = max(0, issued - kTcRaw); i < issued; ++i)
                 mbar_wait(&ctl.raw_full[i % kTcRaw], (i / kTcRaw) & 1, kTcWait);
+            for (int i = max(0, issued - kTcAct); i < issued; ++i)
+                mbar_wait(&ctl.act_full[i % kTcAct], (i / kTcAct) & 1, kTcWait);
         }
     } else if (warp == kTcMmaWarp) {
         if (lane == 0) {
@@ -259,20 +273,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
                 const int st = i % kTcCvt, ch = i / kTcChunk, buf = ch & 1;
                 const bool first = i % kTcChunk == 0;
                 bool ok = true;
+                const int sx = i % kTcAct;
                 if (first && ch >= 2) ok = mbar_wait(&ctl.dempty[buf], ((ch >> 1) - 1) & 1, kTcWait);
+                if (ok) ok = mbar_wait(&ctl.act_full[sx], (i / kTcAct) & 1, kTcWait);
                 if (ok) ok = mbar_wait(&ctl.cvt_full[st], (i / kTcCvt) & 1, kTcWait);
                 if (!ok) give_up();
                 if (!ok || aborted()) break;
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(buf * kTcN);
-                const uint32_t sa = smem_addr(cvt + st * S::kCvtBytes);
-                const uint32_t sb = sa + S::kA;
+                const uint32_t sa = smem_addr(act + sx * kTcA);
+                const uint32_t sb = smem_addr(cvt + st * S::kCvtBytes);
 #pragma unroll
                 for (int j = 0; j < kTcKB / 16; ++j) {
                     tc_mma(d, tc_desc_sw128(sa + 32 * j), tc_desc_sw128(sb + 32 * j), (first && j == 0) ? 0u : 1u);
                     if (!kHead) tc_mma(d, tc_desc_sw128(sa + 32 * j), tc_desc_sw128(sb + S::kB + 32 * j), 1u);
                 }
                 tc_commit(&ctl.cvt_empty[st]);
+                tc_commit(&ctl.act_empty[sx]);
                 if (i % kTcChunk == kTcChunk - 1 || i == nkb - 1) tc_commit(&ctl.dfull[buf]);
             }
             // arrives once every MMA issued so far has completed (the memory is freed after it)
@@ -281,8 +298,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         }
     } else {
         // ---------------------------------------------------------------- converters
-        const int tid = threadIdx.x;  // 0 .. 255
-        const int sub = warp & 3, half = warp >> 2;
+        const int sub = warp & 3, half = warp >> 2;  // tensor-memory lane quadrant, 64-column half
         const uint32_t lane_base = (uint32_t)(32 * sub) << 16;
         float facc[kTcCols];
         int32_t iacc[kTcCols];
@@ -334,55 +350,43 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
             }
             const unsigned char* rs = raw + r * S::kRawBytes;
             unsigned char* cs = cvt + c * S::kCvtBytes;
-            // activations: 128 rows x 4 runs of 16 codes
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int task = tid + u * 256, row = task >> 2, c16 = task & 3;
-                const uint4 v = *reinterpret_cast<const uint4*>(rs + row * kTcKB + c16 * 16);
-                uint4 h0, h1;
-                i8x4_to_half2x2(v.x, h0.x, h0.y);
-                i8x4_to_half2x2(v.y, h0.z, h0.w);
-                i8x4_to_half2x2(v.z, h1.x, h1.y);
-                i8x4_to_half2x2(v.w, h1.z, h1.w);
-                *reinterpret_cast<uint4*>(cs + tc_swz(row, 2 * c16)) = h0;
-                *reinterpret_cast<uint4*>(cs + tc_swz(row, 2 * c16 + 1)) = h1;
-            }
-            // weights: 8 chunks of 16 rows x 64 columns, one lane slot each
+            // weights: 8 chunks of 16 rows x 64 columns, chunk w to warp w, one
+            // lane slot a lane.  Lane L converts slot 4 gq + tq with, in
+            // quarter-warp q = L / 8, gq = 2q (L % 8 < 4) or 2q ^ 5: the eight
+            // 16-byte stores of a quarter then fall on eight distinct swizzled
+            // positions (their rows differ in bit 2).
             {
                 const int gg = warp >> 2, rr = warp & 3;
-                const int gq = lane >> 2, tq = lane & 3;
+                const int qw = lane >> 3, jw = lane & 7;
+                const int gq = (jw < 4) ? 2 * qw : ((2 * qw) ^ 5), tq = jw & 3;
+                const int slot = 4 * gq + tq;
                 const int nl0 = gg * 64 + rr * 16 + gq, nl1 = nl0 + 8;
-                unsigned char* bt = cs + S::kA;
+                unsigned char* bt = cs;
                 const bool valid = nt * (kTcN / 64) + gg < ngroups_n;
                 if (kHead) {
-                    uint4 r0[2], r1[2];  // [gi]: rows gq, gq + 8
+                    uint4 w[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
                     if (valid) {
-                        const unsigned char* ch = rs + kTcM * kTcKB + gg * kI8Super + rr * kI8Chunk + lane * 32;
-                        const uint4 w0 = *reinterpret_cast<const uint4*>(ch);
-                        const uint4 w1 = *reinterpret_cast<const uint4*>(ch + 16);
-                        // word (gi, s, up) at index (gi * 2 + s) * 2 + up: four codes of row gq + 8 up
-                        // at columns 32 gi + 8 tq + 4 s + 0..3
-                        const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-                        for (int gi = 0; gi < 2; ++gi) {
-                            i8x4_to_half2x2(wd[(gi * 2 + 0) * 2 + 0], r0[gi].x, r0[gi].y);
-                            i8x4_to_half2x2(wd[(gi * 2 + 1) * 2 + 0], r0[gi].z, r0[gi].w);
-                            i8x4_to_half2x2(wd[(gi * 2 + 0) * 2 + 1], r1[gi].x, r1[gi].y);
-                            i8x4_to_half2x2(wd[(gi * 2 + 1) * 2 + 1], r1[gi].z, r1[gi].w);
-                        }
-                    } else {
-                        r0[0] = r0[1] = r1[0] = r1[1] = make_uint4(0u, 0u, 0u, 0u);
+                        const unsigned char* ch = rs + gg * kI8Super + rr * kI8Chunk + slot * 32;
+                        w[0] = *reinterpret_cast<const uint4*>(ch);
+                        w[1] = *reinterpret_cast<const uint4*>(ch + 16);
                     }
 #pragma unroll
                     for (int gi = 0; gi < 2; ++gi) {
-                        *reinterpret_cast<uint4*>(bt + tc_swz(nl0, 4 * gi + tq)) = r0[gi];
-                        *reinterpret_cast<uint4*>(bt + tc_swz(nl1, 4 * gi + tq)) = r1[gi];
+                        // words (s, up) of group half gi: four codes of row gq + 8 up at
+                        // columns 32 gi + 8 tq + 4 s + 0..3
+                        uint4 r0, r1;  // rows gq, gq + 8
+                        i8x4_to_half2x2(w[gi].x, r0.x, r0.y);
+                        i8x4_to_half2x2(w[gi].z, r0.z, r0.w);
+                        i8x4_to_half2x2(w[gi].y, r1.x, r1.y);
+                        i8x4_to_half2x2(w[gi].w, r1.z, r1.w);
+                        *reinterpret_cast<uint4*>(bt + tc_swz(nl0, 4 * gi + tq)) = r0;
+                        *reinterpret_cast<uint4*>(bt + tc_swz(nl1, 4 * gi + tq)) = r1;
                     }
                 } else {
                     unsigned char* blo = bt + S::kB;
                     if (valid) {
-                        const unsigned char* ch = rs + kTcM * kTcKB + gg * 4 * kQ4Chunk + rr * kQ4Chunk;
-                        const uint4 wv = *reinterpret_cast<const uint4*>(ch + lane * 16);
+                        const unsigned char* ch = rs + gg * 4 * kQ4Chunk + rr * kQ4Chunk;
+                        const uint4 wv = *reinterpret_cast<const uint4*>(ch + slot * 16);
                         const uint2 sv = *reinterpret_cast<const uint2*>(ch + 512 + gq * 8);
                         const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
@@ -514,15 +518,45 @@ static EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// the tensor map of the int8 activation codes [T][K] (row stride ld bytes): 64 x 128 boxes
-static bool act_map(CUtensorMap* map, const int8_t* codes, int K, int T, int ld) {
+// the tensor map of the activation codes as f16 [T][K] (rows of K halves):
+// 64 x 128 boxes in the 128-byte swizzle, rows past T read as zeros
+static bool act_map(CUtensorMap* map, const __half* codes, int K, int T) {
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)T};
-    const cuuint64_t strides[1] = {(cuuint64_t)ld};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
     const cuuint32_t box[2] = {(cuuint32_t)kTcKB, (cuuint32_t)kTcM};
     const cuuint32_t estr[2] = {1, 1};
-    return encode_fn()(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(codes), dims, strides, box, estr,
-                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return encode_fn()(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(codes), dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// int8 codes [T][ld] -> f16 [T][K] (exact integers), 16 codes a thread
+__global__ void codes_to_f16_kernel(const int8_t* __restrict__ x, int ld, int T, int K, __half* __restrict__ out) {
+    pdl_trigger();
+    pdl_wait();
+    const int per_row = K / 16;
+    const int64_t n = (int64_t)T * per_row;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int r = (int)(i / per_row), c = (int)(i - (int64_t)r * per_row);
+        const uint4 v = *reinterpret_cast<const uint4*>(x + (int64_t)r * ld + c * 16);
+        uint4 h0, h1;
+        i8x4_to_half2x2(v.x, h0.x, h0.y);
+        i8x4_to_half2x2(v.y, h0.z, h0.w);
+        i8x4_to_half2x2(v.z, h1.x, h1.y);
+        i8x4_to_half2x2(v.w, h1.z, h1.w);
+        uint4* o = reinterpret_cast<uint4*>(out + (int64_t)r * K + c * 16);
+        o[0] = h0;
+        o[1] = h1;
+    }
+}
+
+int codes_to_f16(const int8_t* x, int ld, int T, int K, __half* out, int num_sms, cudaStream_t st) {
+    if (T <= 0) return 0;
+    if (K % 16 || ld % 16 || (reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
+        return (int)cudaErrorInvalidValue;
+    const int64_t n = (int64_t)T * (K / 16);
+    const int blocks = (int)std::min<int64_t>((n + 255) / 256, (int64_t)num_sms * 8);
+    return (int)launch(codes_to_f16_kernel, dim3(blocks), dim3(256), 0, st, x, ld, T, K, out);
 }
 
 template <bool kHead>
@@ -540,14 +574,15 @@ bool q4_tc_supported(Q4Layout L, int tile0, int N, int K, QAct x) {
            x.ld % 16 == 0 && (reinterpret_cast<uintptr_t>(x.codes) & 15) == 0;
 }
 
-int q4_tc(const uint8_t* packed, Q4Layout L, int tile0, int N, QAct x, int T, float* y, int ldy, bool accumulate,
-          int num_sms, int* err_flag, cudaStream_t st) {
+int q4_tc(const uint8_t* packed, Q4Layout L, int tile0, int N, QAct x, const __half* x16, int T, float* y, int ldy,
+          bool accumulate, int num_sms, int* err_flag, cudaStream_t st) {
     if (T <= 0 || N <= 0) return 0;
     const int K = L.ksteps * kQ4KStep;
-    if (!q4_tc_supported(L, tile0, N, K, x) || ldy % 4 || (reinterpret_cast<uintptr_t>(y) & 15))
+    if (!q4_tc_supported(L, tile0, N, K, x) || ldy % 4 || (reinterpret_cast<uintptr_t>(y) & 15) ||
+        (reinterpret_cast<uintptr_t>(x16) & 15))
         return (int)cudaErrorInvalidValue;
     CUtensorMap map;
-    if (!act_map(&map, x.codes, K, T, x.ld)) return (int)cudaErrorInvalidValue;
+    if (!act_map(&map, x16, K, T)) return (int)cudaErrorInvalidValue;
     cudaError_t e = tc_set_smem<false>();
     if (e != cudaSuccess) return (int)e;
     const int mt = (T + kTcM - 1) / kTcM, ntl = (N + kTcN - 1) / kTcN;
@@ -561,7 +596,7 @@ int q4_tc(const uint8_t* packed, Q4Layout L, int tile0, int N, QAct x, int T, fl
         if (e != cudaSuccess) return (int)e;
     }
     TcArgs args{packed, L, tile0 / 4, N, x.scale, T, y, ldy, accumulate ? 1 : 0, kps, nullptr, nullptr, err_flag};
-    return (int)launch(tc_gemm_kernel<false>, dim3(mt, ntl, splits), dim3(kTcThreads), TcShape<false>::kSmem, st, map,
+    return (int)launch(tc_gemm_kernel<false>, dim3(ntl, mt, splits), dim3(kTcThreads), TcShape<false>::kSmem, st, map,
                        args);
 }
 
@@ -569,12 +604,12 @@ bool head_tc_supported(int ksteps, QAct x) {
     return encode_fn() != nullptr && ksteps > 0 && x.ld % 16 == 0 && (reinterpret_cast<uintptr_t>(x.codes) & 15) == 0;
 }
 
-int head_tc(const int8_t* packed, const float* row_scale, int V, int ksteps, QAct x, int T, float* logits, int ldl,
-            unsigned long long* keys, int* err_flag, cudaStream_t st) {
+int head_tc(const int8_t* packed, const float* row_scale, int V, int ksteps, QAct x, const __half* x16, int T,
+            float* logits, int ldl, unsigned long long* keys, int* err_flag, cudaStream_t st) {
     if (T <= 0 || V <= 0) return 0;
-    if (!head_tc_supported(ksteps, x)) return (int)cudaErrorInvalidValue;
+    if (!head_tc_supported(ksteps, x) || (reinterpret_cast<uintptr_t>(x16) & 15)) return (int)cudaErrorInvalidValue;
     CUtensorMap map;
-    if (!act_map(&map, x.codes, ksteps * kI8KStep, T, x.ld)) return (int)cudaErrorInvalidValue;
+    if (!act_map(&map, x16, ksteps * kI8KStep, T)) return (int)cudaErrorInvalidValue;
     cudaError_t e = tc_set_smem<true>();
     if (e != cudaSuccess) return (int)e;
     const int mt = (T + kTcM - 1) / kTcM, ntl = (V + kTcN - 1) / kTcN;

@@ -68,15 +68,19 @@ int q4_groupsums(const uint8_t* packed, Q4Layout L, int tile0, int N, QAct x, in
 // to exact hi + lo f16 pairs, f32 accumulation in tensor memory.  Needs
 // tile0 % 4 == 0, N % 64 == 0, x.ld % 16 == 0, 16-byte aligned codes, y and
 // ldy (q4_tc_supported); err_flag is raised when a bounded wait expires.
+// x16: the same codes as f16 [T][K] (codes_to_f16), which the kernel's TMA
+// reads; x.scale the rows' scales.
 bool q4_tc_supported(Q4Layout L, int tile0, int N, int K, QAct x);
-int q4_tc(const uint8_t* packed, Q4Layout L, int tile0, int N, QAct x, int T, float* y, int ldy, bool accumulate,
-          int num_sms, int* err_flag, cudaStream_t st);
+int q4_tc(const uint8_t* packed, Q4Layout L, int tile0, int N, QAct x, const __half* x16, int T, float* y, int ldy,
+          bool accumulate, int num_sms, int* err_flag, cudaStream_t st);
 // The head for many rows on the same kernel (exact int32 row sums, drained
 // from tensor memory every 512 columns): logits (may be nullptr) and the
 // argmax keys as head_stream.
 bool head_tc_supported(int ksteps, QAct x);
-int head_tc(const int8_t* packed, const float* row_scale, int V, int ksteps, QAct x, int T, float* logits, int ldl,
-            unsigned long long* keys, int* err_flag, cudaStream_t st);
+int head_tc(const int8_t* packed, const float* row_scale, int V, int ksteps, QAct x, const __half* x16, int T,
+            float* logits, int ldl, unsigned long long* keys, int* err_flag, cudaStream_t st);
+// int8 activation codes [T][ld] -> f16 [T][K] (exact), for the tcgen05 kernels' TMA.
+int codes_to_f16(const int8_t* x, int ld, int T, int K, __half* out, int num_sms, cudaStream_t st);
 
 // The streaming form for up to 16 rows: every CTA streams a contiguous slice
 // of the matrix (tile0 and N multiples of 64 rows) through a bulk-copy ring
