@@ -131,9 +131,11 @@ struct dflash_model {
 struct dflash_seq {
     dflash_model* m = nullptr;
     int64_t cap = 0, first = 0, len = 0;
-    std::vector<float*> k, v;          // per layer [nkv][cap][hd]
-    float** k_dev = nullptr;           // device arrays of the per-layer pointers
-    float** v_dev = nullptr;
+    // per layer, each value as its (hi, lo) f16 pair: plane hi [nkv][cap][hd]
+    // then plane lo [nkv][cap][hd] (the 4 bytes of an f32 a value)
+    std::vector<__half*> k, v;
+    __half** k_dev = nullptr;  // device arrays of the per-layer pointers
+    __half** v_dev = nullptr;
 };
 
 namespace {
@@ -883,13 +885,13 @@ int dflash_seq_new(dflash_model* m, int64_t max_ctx_rows, dflash_seq** out) {
     s->v.assign(L, nullptr);
     cudaError_t e = cudaSuccess;
     for (int l = 0; l < L && e == cudaSuccess; ++l) {
-        e = cudaMalloc(&s->k[l], per * sizeof(float));
-        if (e == cudaSuccess) e = cudaMalloc(&s->v[l], per * sizeof(float));
+        e = cudaMalloc(&s->k[l], 2 * per * sizeof(__half));
+        if (e == cudaSuccess) e = cudaMalloc(&s->v[l], 2 * per * sizeof(__half));
     }
-    if (e == cudaSuccess) e = cudaMalloc(&s->k_dev, L * sizeof(float*));
-    if (e == cudaSuccess) e = cudaMalloc(&s->v_dev, L * sizeof(float*));
-    if (e == cudaSuccess) e = cudaMemcpy(s->k_dev, s->k.data(), L * sizeof(float*), cudaMemcpyHostToDevice);
-    if (e == cudaSuccess) e = cudaMemcpy(s->v_dev, s->v.data(), L * sizeof(float*), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMalloc(&s->k_dev, L * sizeof(__half*));
+    if (e == cudaSuccess) e = cudaMalloc(&s->v_dev, L * sizeof(__half*));
+    if (e == cudaSuccess) e = cudaMemcpy(s->k_dev, s->k.data(), L * sizeof(__half*), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(s->v_dev, s->v.data(), L * sizeof(__half*), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) {
         cudaGetLastError();
         dflash_seq_free(s);
@@ -904,8 +906,8 @@ int dflash_seq_new(dflash_model* m, int64_t max_ctx_rows, dflash_seq** out) {
 void dflash_seq_free(dflash_seq* s) {
     if (!s) return;
     if (s->m) cudaSetDevice(s->m->device);
-    for (float* p : s->k) if (p) cudaFree(p);
-    for (float* p : s->v) if (p) cudaFree(p);
+    for (__half* p : s->k) if (p) cudaFree(p);
+    for (__half* p : s->v) if (p) cudaFree(p);
     if (s->k_dev) cudaFree(s->k_dev);
     if (s->v_dev) cudaFree(s->v_dev);
     if (s->m && s->m->live_seqs > 0) s->m->live_seqs--;
@@ -1103,7 +1105,7 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
         for (int l = 0; l < g.layers; ++l) {
             const Layer& Ly = m->layers[l];
             const AttnSeq* aseq_dev = P<AttnSeq>(m->aseqs) + (size_t)l * n_seqs;
-            KL(m, "attention", 1, attn_bytes, st,
+            KL(m, "attention", attn_kernels(n_seqs, B, max_ctx, g.heads, g.kv_heads, hd, m->num_sms), attn_bytes, st,
                attention(qkv, m->qkv_w, n_seqs, B, aseq_dev, max_ctx, g.heads, g.kv_heads, hd, scale, P<float>(m->part),
                          part_floats, y, m->num_sms, st, Ly.q_norm, Ly.k_norm, rope, g.eps));
             c.add(row_stage(kChainRows, y, m->qd, ident, R, m->qd, nullptr, g.eps, xq, xs, maxK), (double)R * m->qd * 5,
@@ -1161,7 +1163,7 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
         }
         // q/k norms and rotation run inside the attention, as it loads them
         const AttnSeq* aseq_dev = P<AttnSeq>(m->aseqs) + (size_t)l * n_seqs;
-        KL(m, "attention", 1, attn_bytes, st,
+        KL(m, "attention", attn_kernels(n_seqs, B, max_ctx, g.heads, g.kv_heads, hd, m->num_sms), attn_bytes, st,
            attention(qkv, m->qkv_w, n_seqs, B, aseq_dev, max_ctx, g.heads, g.kv_heads, hd, scale, P<float>(m->part),
                      part_floats, y, m->num_sms, st, Ly.q_norm, Ly.k_norm, rope, g.eps));
         if (quant) {
@@ -1279,7 +1281,7 @@ int dflash_debug_attention(dflash_model* m, dflash_seq* const* seqs, int32_t n_s
     CK(m, ensure_m(m, m->part, (size_t)part_floats * sizeof(float)));
     CK(m, ensure_m(m, m->aseqs, (size_t)n_seqs * sizeof(AttnSeq)));
     CK(m, cudaMemcpyAsync(m->aseqs.p, views.data(), views.size() * sizeof(AttnSeq), cudaMemcpyHostToDevice, st));
-    KL(m, "attention", 1, 0.0, st,
+    KL(m, "attention", attn_kernels(n_seqs, block_len, max_ctx, g.heads, g.kv_heads, g.head_dim, m->num_sms), 0.0, st,
        attention(qkv, m->qkv_w, n_seqs, block_len, P<AttnSeq>(m->aseqs), max_ctx, g.heads, g.kv_heads, g.head_dim,
                  1.0f / sqrtf((float)g.head_dim), P<float>(m->part), part_floats, y, m->num_sms, st));
     return DFLASH_OK;
@@ -1503,14 +1505,24 @@ int dflash_debug_read_kv(dflash_model* m, const dflash_seq* s, int32_t layer, in
     cudaStream_t st = (cudaStream_t)stream;
     const int hd = m->g.head_dim, kv = m->g.kv_heads;
     const int64_t idx = pos - s->first;
+    const size_t plane = (size_t)kv * s->cap * hd;
+    // each stored value is the pair (hi, lo): the value read back is hi + lo,
+    // summed in f32 (exact: the two halves' bits fit one f32 significand)
+    std::vector<__half> hh((size_t)n * kv * hd), hl((size_t)n * kv * hd);
     for (int which = 0; which < 2; ++which) {
         float* dst = which ? v : k;
-        const float* src = which ? s->v[layer] : s->k[layer];
+        const __half* src = which ? s->v[layer] : s->k[layer];
         if (!dst || n == 0) continue;
-        for (int gq = 0; gq < kv; ++gq)
-            CK(m, cudaMemcpy2DAsync(dst + (size_t)gq * hd, (size_t)kv * hd * sizeof(float),
-                                    src + ((size_t)gq * s->cap + idx) * hd, (size_t)hd * sizeof(float),
-                                    (size_t)hd * sizeof(float), (size_t)n, cudaMemcpyDeviceToHost, st));
+        for (int part = 0; part < 2; ++part) {
+            __half* h = part ? hl.data() : hh.data();
+            for (int gq = 0; gq < kv; ++gq)
+                CK(m, cudaMemcpy2DAsync(h + (size_t)gq * hd, (size_t)kv * hd * sizeof(__half),
+                                        src + part * plane + ((size_t)gq * s->cap + idx) * hd,
+                                        (size_t)hd * sizeof(__half), (size_t)hd * sizeof(__half), (size_t)n,
+                                        cudaMemcpyDeviceToHost, st));
+        }
+        CK(m, cudaStreamSynchronize(st));
+        for (size_t i = 0; i < hh.size(); ++i) dst[i] = __half2float(hh[i]) + __half2float(hl[i]);
     }
     CK(m, cudaStreamSynchronize(st));
     return DFLASH_OK;
@@ -1588,14 +1600,15 @@ int dflash_attention_noalloc(dflash_model* m, dflash_seq* const* seqs, int32_t n
     CK(m, noalloc_base(m->device, &base));
     cudaStream_t st = (cudaStream_t)stream;
     AttnSeq* views_dev = reinterpret_cast<AttnSeq*>(base);
-    // the array's head holds the context views; the key splits merge their
-    // partial results in distributed shared memory, so the rest of the array
-    // (kept for kernels that need scratch) is not read, and nothing in it
-    // needs to start at zero
+    // the array's head holds the context views; the rest holds the key
+    // splits' partial rows when a long context splits the keys over more
+    // CTAs than clusters place (each launch writes them before the merge
+    // reads them, so nothing in it needs to start at zero); otherwise the
+    // splits merge in distributed shared memory and the rest is not read
     CK(m, cudaMemcpyAsync(views_dev, views.data(), views.size() * sizeof(AttnSeq), cudaMemcpyHostToDevice, st));
     CK(m, attention(qkv, m->qkv_w, n_seqs, block_len, views_dev, max_ctx, g.heads, g.kv_heads, g.head_dim,
                     1.0f / sqrtf((float)g.head_dim), base + kNoAllocViewFloats, part_floats, y, m->num_sms, st));
-    m->launches += 1;
+    m->launches += attn_kernels(n_seqs, block_len, max_ctx, g.heads, g.kv_heads, g.head_dim, m->num_sms);
     return DFLASH_OK;
 }
 

@@ -251,11 +251,18 @@ DF_DEV void norm_rope_head(float (&v)[E], const float* __restrict__ gain, const 
     }
 }
 
+// f32 -> (hi, lo) f16 pair with hi + lo = x to about 2^-22 relative (the form
+// the attention's tensor-core products take their operands in)
+DF_DEV void split_f16(float x, __half& hi, __half& lo) {
+    hi = __float2half_rn(x);
+    lo = __float2half_rn(x - __half2float(hi));
+}
+
 template <int E>
 __global__ void kv_append_kernel(const float* __restrict__ kv, int n, int L, int nkv,
                                  const float* const* __restrict__ k_norm, const float* __restrict__ inv_freq,
-                                 float eps, const int64_t* __restrict__ pos, float* const* __restrict__ kstore,
-                                 float* const* __restrict__ vstore, int64_t cap) {
+                                 float eps, const int64_t* __restrict__ pos, __half* const* __restrict__ kstore,
+                                 __half* const* __restrict__ vstore, int64_t cap) {
     constexpr int HD = 32 * E;
     const int64_t wid = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
     pdl_trigger();
@@ -273,17 +280,24 @@ __global__ void kv_append_kernel(const float* __restrict__ kv, int n, int L, int
         vv[j] = src[(nkv + g) * HD + lane + 32 * j];
     }
     norm_rope_head<E>(kvv, k_norm[l], inv_freq, eps, pos0 + r, true);
-    float* kd = kstore[l] + ((int64_t)g * cap + idx0 + r) * HD;
-    float* vd = vstore[l] + ((int64_t)g * cap + idx0 + r) * HD;
+    // the store keeps each value as its (hi, lo) f16 pair: plane hi then plane lo
+    const int64_t plane = (int64_t)nkv * cap * HD;
+    __half* kd = kstore[l] + ((int64_t)g * cap + idx0 + r) * HD;
+    __half* vd = vstore[l] + ((int64_t)g * cap + idx0 + r) * HD;
 #pragma unroll
     for (int j = 0; j < E; ++j) {
-        kd[lane + 32 * j] = kvv[j];
-        vd[lane + 32 * j] = vv[j];
+        __half h, lo;
+        split_f16(kvv[j], h, lo);
+        kd[lane + 32 * j] = h;
+        kd[plane + lane + 32 * j] = lo;
+        split_f16(vv[j], h, lo);
+        vd[lane + 32 * j] = h;
+        vd[plane + lane + 32 * j] = lo;
     }
 }
 
 int kv_append(const float* kv, int n, int L, int nkv, int hd, const float* const* k_norm_dev, const float* inv_freq,
-              float eps, const int64_t* pos_dev, float* const* kstore_dev, float* const* vstore_dev, int64_t cap,
+              float eps, const int64_t* pos_dev, __half* const* kstore_dev, __half* const* vstore_dev, int64_t cap,
               cudaStream_t st) {
     if (n <= 0) return 0;
     const int64_t warps = (int64_t)n * L * nkv;
@@ -443,11 +457,6 @@ constexpr int kAttnStep = kAttnKH * kAttnK;    // keys per step of the CTA
 constexpr int kAttnWarps = kAttnQW * kAttnKH;
 constexpr int kAttnMaxCluster = 32 / kAttnKH < 16 ? 32 / kAttnKH : 16;  // CTAs of a cluster (non-portable above 8)
 
-// f32 -> (hi, lo) f16 pair with hi + lo = x to about 2^-22 relative
-DF_DEV void split_f16(float x, __half& hi, __half& lo) {
-    hi = __float2half_rn(x);
-    lo = __float2half_rn(x - __half2float(hi));
-}
 
 DF_DEV void ldsm_x4(uint32_t (&r)[4], const __half* p) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -544,7 +553,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const flo
                                                                        float scale_log2, float* __restrict__ y,
                                                                        const float* __restrict__ q_norm,
                                                                        const float* __restrict__ k_norm,
-                                                                       const float2* __restrict__ rope, float eps) {
+                                                                       const float2* __restrict__ rope, float eps,
+                                                                       float* __restrict__ gpart) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     AttnSmem<HD>& sm = *reinterpret_cast<AttnSmem<HD>*>(smem_raw);
     constexpr int PART = AttnSmem<HD>::PART;
@@ -552,7 +562,10 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const flo
     constexpr int KS = HD / 16;  // k16 steps of the scores
     constexpr int kThreads = kAttnWarps * 32;
     cg::cluster_group cluster = cg::this_cluster();
-    const int sp = (int)cluster.block_rank(), g = blockIdx.y / qtiles, qt = blockIdx.y % qtiles, s = blockIdx.z;
+    // the key split: the CTA's rank in its cluster, or, when the splits merge
+    // through global memory (gpart), its x index in a launch without clusters
+    const int sp = gpart ? (int)blockIdx.x : (int)cluster.block_rank();
+    const int g = blockIdx.y / qtiles, qt = blockIdx.y % qtiles, s = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
     const int qw = warp % kAttnQW, half = warp / kAttnQW;  // query warp, key lane
     pdl_trigger();
@@ -571,7 +584,11 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const flo
     constexpr int D4 = HD / 4;
     constexpr int NQ4 = kAttnQ * D4 / kThreads, NK4 = kAttnStep * D4 / kThreads;
     static_assert(NQ4 * kThreads == kAttnQ * D4 && NK4 * kThreads == kAttnStep * D4, "tile split");
+    // context keys and values arrive as stored: the bits of their (hi, lo) f16
+    // pairs, four dimensions as (hi01, hi23, lo01, lo23) in a float4's words;
+    // the block's own rows arrive as f32 and are split on the way to shared memory
     float4 pk[NK4], pv[NK4];
+    const int64_t plane = (int64_t)nkv * sq.cap * HD;
     auto load_kv = [&](int jt) {
 #pragma unroll
         for (int u = 0; u < NK4; ++u) {
@@ -580,8 +597,14 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const flo
             if (j < j1) {
                 if (j < sq.n) {
                     const int64_t off = ((int64_t)g * sq.cap + sq.lo + j) * HD + d;
-                    kk = *reinterpret_cast<const float4*>(sq.kc + off);
-                    vv = *reinterpret_cast<const float4*>(sq.vc + off);
+                    const uint2 kh = *reinterpret_cast<const uint2*>(sq.kc + off);
+                    const uint2 kl = *reinterpret_cast<const uint2*>(sq.kc + plane + off);
+                    const uint2 vh = *reinterpret_cast<const uint2*>(sq.vc + off);
+                    const uint2 vl = *reinterpret_cast<const uint2*>(sq.vc + plane + off);
+                    kk = make_float4(__uint_as_float(kh.x), __uint_as_float(kh.y), __uint_as_float(kl.x),
+                                     __uint_as_float(kl.y));
+                    vv = make_float4(__uint_as_float(vh.x), __uint_as_float(vh.y), __uint_as_float(vl.x),
+                                     __uint_as_float(vl.y));
                 } else {
                     const int64_t off = (row0 + (j - sq.n)) * ld + d;
                     kk = *reinterpret_cast<const float4*>(qkv + off + (int64_t)(nq + g) * HD);
@@ -661,8 +684,16 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const flo
         for (int u = 0; u < NK4; ++u) {
             const int i = tid + u * kThreads, kr = i / D4, d = (i % D4) * 4;
             const int hf = kr / kAttnK, k = kr % kAttnK;
-            split_store4(pk[u], &sm.kh[hf][k][d], &sm.kl[hf][k][d]);
-            split_store4(pv[u], &sm.vh[hf][k][d], &sm.vl[hf][k][d]);
+            if (jt + kr < sq.n) {
+                // stored pairs: the bits go to shared memory as they are
+                *reinterpret_cast<uint2*>(&sm.kh[hf][k][d]) = make_uint2(__float_as_uint(pk[u].x), __float_as_uint(pk[u].y));
+                *reinterpret_cast<uint2*>(&sm.kl[hf][k][d]) = make_uint2(__float_as_uint(pk[u].z), __float_as_uint(pk[u].w));
+                *reinterpret_cast<uint2*>(&sm.vh[hf][k][d]) = make_uint2(__float_as_uint(pv[u].x), __float_as_uint(pv[u].y));
+                *reinterpret_cast<uint2*>(&sm.vl[hf][k][d]) = make_uint2(__float_as_uint(pv[u].z), __float_as_uint(pv[u].w));
+            } else {
+                split_store4(pk[u], &sm.kh[hf][k][d], &sm.kl[hf][k][d]);
+                split_store4(pv[u], &sm.vh[hf][k][d], &sm.vl[hf][k][d]);
+            }
         }
         __syncthreads();
         if (jt + kAttnStep < j1) load_kv(jt + kAttnStep);
@@ -780,6 +811,25 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const flo
             }
         }
     }
+    if (gpart) {
+        // this split's partial rows (running max in the log2 domain, sum,
+        // unnormalised output) to global memory, for attn_merge_kernel:
+        // [unit][split][key lane][query row][PART]
+        const int unit = blockIdx.z * gridDim.y + blockIdx.y;
+        float* gp = gpart + ((int64_t)(unit * nsplit + sp) * kAttnKH + half) * kAttnQ * PART;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float* out = gp + (int64_t)(qbase + gq + 8 * h) * PART;
+            if (tq == 0) {
+                out[0] = m_run[h];
+                out[1] = l_run[h];
+            }
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+                *reinterpret_cast<float2*>(out + 4 + j * 8 + 2 * tq) = make_float2(o[j][2 * h], o[j][2 * h + 1]);
+        }
+        return;
+    }
     __syncthreads();  // every warp is done with the key/value tiles: their area takes the partial rows
     float* part = sm.part();
 #pragma unroll
@@ -840,14 +890,63 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const flo
     cluster.sync();  // no CTA leaves while another may still read its partial rows
 }
 
+// The global-memory merge of the key splits (long contexts): warp w of CTA
+// (x, unit) merges query row 8 x + w of the unit's tile from its
+// kAttnKH * nsplit partial rows, as the cluster merge does.
+template <int HD>
+__global__ void __launch_bounds__(256) attn_merge_kernel(const float* __restrict__ gpart, int nsplit, int qtiles,
+                                                         int nkv, int nq, int block_len, float* __restrict__ y) {
+    constexpr int PART = HD + 4, VEC = HD / 32;
+    pdl_trigger();
+    pdl_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int unit = blockIdx.y, qr = blockIdx.x * 8 + warp;
+    const int qt = unit % qtiles, g = (unit / qtiles) % nkv, s = unit / (qtiles * nkv);
+    const int rep = nq / nkv, mq = rep * block_len;
+    const int ii = qt * kAttnQ + qr;
+    if (qr >= kAttnQ || ii >= mq) return;
+    const int nparts = kAttnKH * nsplit;
+    const float* base = gpart + (int64_t)unit * nparts * kAttnQ * PART + (int64_t)qr * PART;
+    float M = -INFINITY;
+    for (int p = lane; p < nparts; p += 32) M = fmaxf(M, base[(int64_t)p * kAttnQ * PART]);
+    M = warp_max(M);
+    float L = 0.f, acc[VEC];
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) acc[j] = 0.f;
+    for (int p = 0; p < nparts; ++p) {
+        const float* src = base + (int64_t)p * kAttnQ * PART;
+        const float mk = src[0];
+        const float w = (mk == -INFINITY) ? 0.f : exp2f(mk - M);
+        L = fmaf(src[1], w, L);
+        if constexpr (VEC == 4) {
+            const float4 a = *reinterpret_cast<const float4*>(src + 4 + 4 * lane);
+            acc[0] = fmaf(a.x, w, acc[0]);
+            acc[1] = fmaf(a.y, w, acc[1]);
+            acc[2] = fmaf(a.z, w, acc[2]);
+            acc[3] = fmaf(a.w, w, acc[3]);
+        } else {
+            const float2 a = *reinterpret_cast<const float2*>(src + 4 + 2 * lane);
+            acc[0] = fmaf(a.x, w, acc[0]);
+            acc[1] = fmaf(a.y, w, acc[1]);
+        }
+    }
+    const int head = g * rep + ii / block_len, r = ii % block_len;
+    float* dst = y + ((int64_t)s * block_len + r) * ((int64_t)nq * HD) + (int64_t)head * HD + VEC * lane;
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) dst[j] = acc[j] / L;
+}
+
 // Cluster size (the key splits).  max_active[c]: clusters of c CTAs the
 // device holds at once.  With few (sequence, kv head, query tile) units the
 // largest cluster whose units all run in one wave, capped by the key steps
 // of the longest context `max_ctx` (callers pass the sequences' capacity, so
 // that the launch does not change as contexts grow); with many units, enough
 // splits to cover the SMs.
+// With long contexts, when the clusters leave a quarter of the SMs idle, the
+// keys are split over plain CTAs instead (every SM busy, each with at least
+// 4 key steps) that merge through global memory (*gmerge).
 static void attn_plan(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int num_sms, const int* max_active,
-                      int* qtiles, int* nsplit) {
+                      int* qtiles, int* nsplit, bool* gmerge) {
     const int mq = (nq / nkv) * block_len;
     *qtiles = (mq + kAttnQ - 1) / kAttnQ;
     const int total = max_ctx + block_len;
@@ -859,9 +958,29 @@ static void attn_plan(int n_seqs, int block_len, int max_ctx, int nq, int nkv, i
     for (int c = 1; c <= std::min(want, kAttnMaxCluster); ++c)
         if (max_active[c] >= std::min(units, max_active[1])) best = c;
     *nsplit = best;
+    *gmerge = false;
+    const int gsplit = std::min(max_split, std::max(1, (num_sms + units - 1) / units));
+    if (units * best * 4 < num_sms * 3 && gsplit > best && total >= 4 * kAttnStep * gsplit) {
+        *nsplit = gsplit;
+        *gmerge = true;
+    }
 }
 
-int64_t attn_scratch_floats(int, int, int, int, int, int, int) { return 0; }
+template <int HD>
+static const int* attn_cluster_table(cudaStream_t st);
+
+int64_t attn_scratch_floats(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int hd, int num_sms) {
+    const int* table = hd == 128 ? attn_cluster_table<128>(0) : attn_cluster_table<64>(0);
+    int qtiles, nsplit;
+    bool gmerge;
+    attn_plan(n_seqs, block_len, max_ctx, nq, nkv, num_sms, table, &qtiles, &nsplit, &gmerge);
+    if (!gmerge) return 0;
+    return (int64_t)nkv * qtiles * n_seqs * nsplit * kAttnKH * kAttnQ * (hd + 4);
+}
+
+int attn_kernels(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int hd, int num_sms) {
+    return attn_scratch_floats(n_seqs, block_len, max_ctx, nq, nkv, hd, num_sms) > 0 ? 2 : 1;
+}
 
 // How many clusters of c = 1..16 CTAs of attn_cluster_kernel<HD> the device
 // holds at once (0 where it cannot place one), found once per process.
@@ -900,28 +1019,39 @@ static const int* attn_cluster_table(cudaStream_t st) {
 
 template <int HD>
 static int attention_hd(const float* qkv, int ld, int n_seqs, int block_len, const AttnSeq* seqs_dev, int max_ctx,
-                        int nq, int nkv, float scale, float* y, int num_sms, cudaStream_t st, const float* q_norm,
-                        const float* k_norm, const float2* rope, float eps) {
+                        int nq, int nkv, float scale, float* part, int64_t part_floats, float* y, int num_sms,
+                        cudaStream_t st, const float* q_norm, const float* k_norm, const float2* rope, float eps) {
     const int* table = attn_cluster_table<HD>(st);
     int qtiles, nsplit;
-    attn_plan(n_seqs, block_len, max_ctx, nq, nkv, num_sms, table, &qtiles, &nsplit);
+    bool gmerge;
+    attn_plan(n_seqs, block_len, max_ctx, nq, nkv, num_sms, table, &qtiles, &nsplit, &gmerge);
     const float scale_log2 = scale * 1.4426950408889634f;
+    const int64_t need = (int64_t)nkv * qtiles * n_seqs * nsplit * kAttnKH * kAttnQ * (HD + 4);
+    if (gmerge && (part == nullptr || part_floats < need)) return (int)cudaErrorInvalidValue;
     dim3 grid(nsplit, nkv * qtiles, n_seqs);
+    if (gmerge) {
+        cudaError_t e = launch(attn_cluster_kernel<HD>, grid, dim3(kAttnWarps * 32), sizeof(AttnSmem<HD>), st, qkv, ld,
+                               block_len, seqs_dev, nq, nkv, qtiles, nsplit, scale_log2, y, q_norm, k_norm, rope, eps,
+                               part);
+        if (e != cudaSuccess) return (int)e;
+        return (int)launch(attn_merge_kernel<HD>, dim3(kAttnQ / 8, nkv * qtiles * n_seqs), dim3(256), 0, st,
+                           (const float*)part, nsplit, qtiles, nkv, nq, block_len, y);
+    }
     return (int)launch_cluster(attn_cluster_kernel<HD>, grid, dim3(kAttnWarps * 32), sizeof(AttnSmem<HD>), st, nsplit,
                                qkv, ld, block_len, seqs_dev, nq, nkv, qtiles, nsplit, scale_log2, y, q_norm, k_norm,
-                               rope, eps);
+                               rope, eps, (float*)nullptr);
 }
 
 int attention(const float* qkv, int ld, int n_seqs, int block_len, const AttnSeq* seqs_dev, int max_ctx, int nq,
-              int nkv, int hd, float scale, float*, int64_t, float* y, int num_sms, cudaStream_t st,
+              int nkv, int hd, float scale, float* part, int64_t part_floats, float* y, int num_sms, cudaStream_t st,
               const float* q_norm, const float* k_norm, const float2* rope, float eps) {
     if ((q_norm == nullptr) != (k_norm == nullptr) || (q_norm != nullptr && rope == nullptr))
         return (int)cudaErrorInvalidValue;
     if (hd == 128)
-        return attention_hd<128>(qkv, ld, n_seqs, block_len, seqs_dev, max_ctx, nq, nkv, scale, y, num_sms, st, q_norm,
-                                 k_norm, rope, eps);
-    return attention_hd<64>(qkv, ld, n_seqs, block_len, seqs_dev, max_ctx, nq, nkv, scale, y, num_sms, st, q_norm,
-                            k_norm, rope, eps);
+        return attention_hd<128>(qkv, ld, n_seqs, block_len, seqs_dev, max_ctx, nq, nkv, scale, part, part_floats, y,
+                                 num_sms, st, q_norm, k_norm, rope, eps);
+    return attention_hd<64>(qkv, ld, n_seqs, block_len, seqs_dev, max_ctx, nq, nkv, scale, part, part_floats, y,
+                            num_sms, st, q_norm, k_norm, rope, eps);
 }
 
 }  // namespace dflash

@@ -165,10 +165,11 @@ int embed_rows(const float* embed, int H, int vocab, const uint32_t* anchor_tok,
                const float* inv_freq = nullptr, int hd = 0, float2* rope = nullptr);
 // Context rows: kv [n][L * 2 * nkv * hd] (per layer k then v) -> the
 // sequence's store: K rows normed (k_norm_l) and rotated at position
-// pos0 + r, V rows as they are; stored at index idx0 + r, where
-// pos_dev = {pos0, idx0} lives in device memory (set per call).
+// pos0 + r, V rows as they are; stored at index idx0 + r as (hi, lo) f16
+// pairs (plane hi [nkv][cap][hd], then plane lo), where pos_dev = {pos0,
+// idx0} lives in device memory (set per call).
 int kv_append(const float* kv, int n, int L, int nkv, int hd, const float* const* k_norm_dev, const float* inv_freq,
-              float eps, const int64_t* pos_dev, float* const* kstore_dev, float* const* vstore_dev, int64_t cap,
+              float eps, const int64_t* pos_dev, __half* const* kstore_dev, __half* const* vstore_dev, int64_t cap,
               cudaStream_t st);
 // a = silu(g) * u for gu [rows][2I] (gate then up); f32 out or int8 codes.
 // The same with the grid in clusters of cluster_x CTAs along x.
@@ -197,8 +198,11 @@ int silu_mul(const float* gu, int ld_gu, int rows, int I, float* out_f32, int ld
 
 // Attention of a block over its sequence's context and its own rows.
 struct AttnSeq {
-    const float* kc;  // layer's key store   [nkv][cap][hd]
-    const float* vc;  // layer's value store [nkv][cap][hd]
+    // The layer's key and value stores, each value as its (hi, lo) f16 pair
+    // (hi = f16(x), lo = f16(x - hi)): plane hi [nkv][cap][hd], then plane lo
+    // [nkv][cap][hd].
+    const __half* kc;
+    const __half* vc;
     int64_t cap;
     int64_t lo;  // first context index read (position - first)
     int n;       // context rows read
@@ -207,8 +211,10 @@ struct AttnSeq {
 // the kernel applies the per-head RMSNorm (q_norm / k_norm) and the rotation
 // (table `rope` of embed_rows) to q and to the block's k as it loads them,
 // otherwise q and k arrive normed and rotated.  y [n_seqs*block_len][nq*hd].  `part` / part_floats: scratch of
-// attn_scratch_floats() floats (none at present: the key splits merge in
-// distributed shared memory).
+// attn_scratch_floats() floats: none when the key splits merge in
+// distributed shared memory (clusters), the splits' partial rows when long
+// contexts split the keys over more CTAs than the clusters place and merge
+// through global memory (nothing in it needs to start at zero).
 // max_ctx: the largest context any sequence of the call may hold (its
 // capacity); the launch depends on it, each CTA's key range on the actual n.
 int attention(const float* qkv, int ld, int n_seqs, int block_len, const AttnSeq* seqs_dev, int max_ctx, int nq,
@@ -216,5 +222,8 @@ int attention(const float* qkv, int ld, int n_seqs, int block_len, const AttnSeq
               const float* q_norm = nullptr, const float* k_norm = nullptr, const float2* rope = nullptr,
               float eps = 0.f);
 int64_t attn_scratch_floats(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int hd, int num_sms);
+// Kernels one attention call launches (2 when the key splits merge through
+// global memory: the split kernel, then the merge).
+int attn_kernels(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int hd, int num_sms);
 
 }  // namespace dflash

@@ -348,6 +348,19 @@ def test_batched_many_sequences(name, forced):
     sc.run(forced).check(forced)
 
 
+def test_long_context_split_merge():
+    """A context long enough that the attention splits its keys over plain
+    CTAs (every SM busy) whose partial rows merge through global memory, not
+    in a cluster: identical decisions, values and logits to 1e-5."""
+    p = pair("small_q4")
+    g = p.g
+    n = 20000
+    sc = Script(p, 1, n + 16)
+    sc.append(0, 0, W.make_taps(g, n, call_id=90))
+    sc.block([0], [123], [n], g.block)
+    sc.run(True).check(True)
+
+
 def test_truncate_and_reappend():
     p = pair("small_q4")
     g = p.g
