@@ -1105,7 +1105,7 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
         for (int l = 0; l < g.layers; ++l) {
             const Layer& Ly = m->layers[l];
             const AttnSeq* aseq_dev = P<AttnSeq>(m->aseqs) + (size_t)l * n_seqs;
-            KL(m, "attention", attn_kernels(n_seqs, B, max_ctx, g.heads, g.kv_heads, hd, m->num_sms), attn_bytes, st,
+            KL(m, "attention", attn_kernels(n_seqs, B, max_ctx, g.heads, g.kv_heads, hd, m->num_sms, part_floats), attn_bytes, st,
                attention(qkv, m->qkv_w, n_seqs, B, aseq_dev, max_ctx, g.heads, g.kv_heads, hd, scale, P<float>(m->part),
                          part_floats, y, m->num_sms, st, Ly.q_norm, Ly.k_norm, rope, g.eps));
             c.add(row_stage(kChainRows, y, m->qd, ident, R, m->qd, nullptr, g.eps, xq, xs, maxK), (double)R * m->qd * 5,
@@ -1163,7 +1163,7 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
         }
         // q/k norms and rotation run inside the attention, as it loads them
         const AttnSeq* aseq_dev = P<AttnSeq>(m->aseqs) + (size_t)l * n_seqs;
-        KL(m, "attention", attn_kernels(n_seqs, B, max_ctx, g.heads, g.kv_heads, hd, m->num_sms), attn_bytes, st,
+        KL(m, "attention", attn_kernels(n_seqs, B, max_ctx, g.heads, g.kv_heads, hd, m->num_sms, part_floats), attn_bytes, st,
            attention(qkv, m->qkv_w, n_seqs, B, aseq_dev, max_ctx, g.heads, g.kv_heads, hd, scale, P<float>(m->part),
                      part_floats, y, m->num_sms, st, Ly.q_norm, Ly.k_norm, rope, g.eps));
         if (quant) {
@@ -1281,7 +1281,7 @@ int dflash_debug_attention(dflash_model* m, dflash_seq* const* seqs, int32_t n_s
     CK(m, ensure_m(m, m->part, (size_t)part_floats * sizeof(float)));
     CK(m, ensure_m(m, m->aseqs, (size_t)n_seqs * sizeof(AttnSeq)));
     CK(m, cudaMemcpyAsync(m->aseqs.p, views.data(), views.size() * sizeof(AttnSeq), cudaMemcpyHostToDevice, st));
-    KL(m, "attention", attn_kernels(n_seqs, block_len, max_ctx, g.heads, g.kv_heads, g.head_dim, m->num_sms), 0.0, st,
+    KL(m, "attention", attn_kernels(n_seqs, block_len, max_ctx, g.heads, g.kv_heads, g.head_dim, m->num_sms, part_floats), 0.0, st,
        attention(qkv, m->qkv_w, n_seqs, block_len, P<AttnSeq>(m->aseqs), max_ctx, g.heads, g.kv_heads, g.head_dim,
                  1.0f / sqrtf((float)g.head_dim), P<float>(m->part), part_floats, y, m->num_sms, st));
     return DFLASH_OK;
@@ -1590,12 +1590,9 @@ int dflash_attention_noalloc(dflash_model* m, dflash_seq* const* seqs, int32_t n
         return set_err(m, DFLASH_ERANGE, "attention without allocation: " + std::to_string(n_seqs) +
                                              " sequences, at most " + std::to_string(kNoAllocMaxSeqs));
     const dflash_geometry& g = m->g;
-    const int64_t part_floats =
-        attn_scratch_floats(n_seqs, block_len, max_ctx, g.heads, g.kv_heads, g.head_dim, m->num_sms);
-    if (part_floats > kNoAllocFloats - kNoAllocViewFloats)
-        return set_err(m, DFLASH_ERANGE, "attention without allocation needs " + std::to_string(part_floats) +
-                                             " floats of scratch; the fixed array holds " +
-                                             std::to_string(kNoAllocFloats - kNoAllocViewFloats));
+    // the fixed array's room for the key splits' partial rows: a call whose
+    // rows do not fit runs the cluster merge, which needs none
+    const int64_t part_floats = kNoAllocFloats - kNoAllocViewFloats;
     float* base = nullptr;
     CK(m, noalloc_base(m->device, &base));
     cudaStream_t st = (cudaStream_t)stream;
@@ -1608,7 +1605,7 @@ int dflash_attention_noalloc(dflash_model* m, dflash_seq* const* seqs, int32_t n
     CK(m, cudaMemcpyAsync(views_dev, views.data(), views.size() * sizeof(AttnSeq), cudaMemcpyHostToDevice, st));
     CK(m, attention(qkv, m->qkv_w, n_seqs, block_len, views_dev, max_ctx, g.heads, g.kv_heads, g.head_dim,
                     1.0f / sqrtf((float)g.head_dim), base + kNoAllocViewFloats, part_floats, y, m->num_sms, st));
-    m->launches += attn_kernels(n_seqs, block_len, max_ctx, g.heads, g.kv_heads, g.head_dim, m->num_sms);
+    m->launches += attn_kernels(n_seqs, block_len, max_ctx, g.heads, g.kv_heads, g.head_dim, m->num_sms, part_floats);
     return DFLASH_OK;
 }
 

@@ -942,11 +942,15 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const float* __restrict
 // of the longest context `max_ctx` (callers pass the sequences' capacity, so
 // that the launch does not change as contexts grow); with many units, enough
 // splits to cover the SMs.
-// With long contexts, when the clusters leave a quarter of the SMs idle, the
-// keys are split over plain CTAs instead (every SM busy, each with at least
-// 4 key steps) that merge through global memory (*gmerge).
+// Global-memory merge (*gmerge): when the clusters leave a quarter of the SMs
+// idle, the keys are split over plain CTAs instead (every SM busy, each with
+// at least kAttnMinSteps key steps).  (Splitting the units of a batch that
+// outnumber the SMs, to even out the waves, measured slower: the merge
+// kernels cost more than the waves gain.)
+constexpr int kAttnMinSteps = 2;  // key steps a CTA gets at least when the splits merge through global memory
+
 static void attn_plan(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int num_sms, const int* max_active,
-                      int* qtiles, int* nsplit, bool* gmerge) {
+                      int* qtiles, int* nsplit, bool* gmerge, bool allow_gmerge = true) {
     const int mq = (nq / nkv) * block_len;
     *qtiles = (mq + kAttnQ - 1) / kAttnQ;
     const int total = max_ctx + block_len;
@@ -959,10 +963,13 @@ static void attn_plan(int n_seqs, int block_len, int max_ctx, int nq, int nkv, i
         if (max_active[c] >= std::min(units, max_active[1])) best = c;
     *nsplit = best;
     *gmerge = false;
-    const int gsplit = std::min(max_split, std::max(1, (num_sms + units - 1) / units));
-    if (units * best * 4 < num_sms * 3 && gsplit > best && total >= 4 * kAttnStep * gsplit) {
-        *nsplit = gsplit;
-        *gmerge = true;
+    if (!allow_gmerge) return;
+    if (units * best * 4 < num_sms * 3) {
+        const int gsplit = std::min(max_split, std::max(1, (num_sms + units - 1) / units));
+        if (gsplit > best && total >= kAttnMinSteps * kAttnStep * gsplit) {
+            *nsplit = gsplit;
+            *gmerge = true;
+        }
     }
 }
 
@@ -978,8 +985,9 @@ int64_t attn_scratch_floats(int n_seqs, int block_len, int max_ctx, int nq, int 
     return (int64_t)nkv * qtiles * n_seqs * nsplit * kAttnKH * kAttnQ * (hd + 4);
 }
 
-int attn_kernels(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int hd, int num_sms) {
-    return attn_scratch_floats(n_seqs, block_len, max_ctx, nq, nkv, hd, num_sms) > 0 ? 2 : 1;
+int attn_kernels(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int hd, int num_sms, int64_t part_floats) {
+    const int64_t need = attn_scratch_floats(n_seqs, block_len, max_ctx, nq, nkv, hd, num_sms);
+    return (need > 0 && part_floats >= need) ? 2 : 1;
 }
 
 // How many clusters of c = 1..16 CTAs of attn_cluster_kernel<HD> the device
@@ -1027,7 +1035,8 @@ static int attention_hd(const float* qkv, int ld, int n_seqs, int block_len, con
     attn_plan(n_seqs, block_len, max_ctx, nq, nkv, num_sms, table, &qtiles, &nsplit, &gmerge);
     const float scale_log2 = scale * 1.4426950408889634f;
     const int64_t need = (int64_t)nkv * qtiles * n_seqs * nsplit * kAttnKH * kAttnQ * (HD + 4);
-    if (gmerge && (part == nullptr || part_floats < need)) return (int)cudaErrorInvalidValue;
+    if (gmerge && (part == nullptr || part_floats < need))  // no room for the partial rows: clusters
+        attn_plan(n_seqs, block_len, max_ctx, nq, nkv, num_sms, table, &qtiles, &nsplit, &gmerge, false);
     dim3 grid(nsplit, nkv * qtiles, n_seqs);
     if (gmerge) {
         cudaError_t e = launch(attn_cluster_kernel<HD>, grid, dim3(kAttnWarps * 32), sizeof(AttnSmem<HD>), st, qkv, ld,

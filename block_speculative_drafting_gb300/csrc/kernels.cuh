@@ -222,8 +222,10 @@ int attention(const float* qkv, int ld, int n_seqs, int block_len, const AttnSeq
               const float* q_norm = nullptr, const float* k_norm = nullptr, const float2* rope = nullptr,
               float eps = 0.f);
 int64_t attn_scratch_floats(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int hd, int num_sms);
-// Kernels one attention call launches (2 when the key splits merge through
-// global memory: the split kernel, then the merge).
-int attn_kernels(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int hd, int num_sms);
+// Kernels one attention call with part_floats of scratch launches (2 when
+// the key splits merge through global memory: the split kernel, then the
+// merge; with less scratch than attn_scratch_floats() the call falls back to
+// the cluster merge).
+int attn_kernels(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int hd, int num_sms, int64_t part_floats);
 
 }  // namespace dflash
