@@ -145,10 +145,13 @@ DFLASH_API int dflash_geometry_of(const dflash_model* model, dflash_geometry* ou
 
 /*
  * A sequence: device K/V storage for up to `max_ctx_rows` context positions
- * in every layer, f32, laid out per layer [kv_heads][max_ctx_rows][head_dim]
- * for keys and the same for values (page "cortiq-engine 0.8.71 —
+ * in every layer, laid out per layer [kv_heads][max_ctx_rows][head_dim] for
+ * keys and the same for values (page "cortiq-engine 0.8.71 —
  * src/dflash.rs", `Ctx`: per layer, per KV head, a row of head_dim per
- * position).  The context starts empty at position 0.
+ * position).  Each f32 value is held as the f16 pair the attention's
+ * tensor-core products take, hi = f16(x) and lo = f16(x - hi) (hi + lo = x to
+ * about 2^-22 relative), in two planes of the 4 bytes an f32 would take.
+ * The context starts empty at position 0.
  * Errors: EINVAL (null, max_ctx_rows < 1), ENOMEM, ECUDA.
  */
 DFLASH_API int dflash_seq_new(dflash_model* model, int64_t max_ctx_rows, dflash_seq** out);
@@ -292,8 +295,8 @@ DFLASH_API int dflash_debug_q4_matmul(dflash_model* model, int32_t matrix_id, co
 
 /*
  * The stored keys and values of context positions [pos, pos + n) of one
- * layer: k and v [n][kv_heads][head_dim] f32 (either may be NULL).
- * Errors: EINVAL, ERANGE (positions not held), ECUDA.
+ * layer: k and v [n][kv_heads][head_dim] f32 (either may be NULL), each the
+ * stored pair's hi + lo.  Errors: EINVAL, ERANGE (positions not held), ECUDA.
  */
 DFLASH_API int dflash_debug_read_kv(dflash_model* model, const dflash_seq* seq, int32_t layer, int64_t pos, int64_t n, float* k,
                          float* v, void* stream);
@@ -344,17 +347,20 @@ DFLASH_API int dflash_debug_attention(dflash_model* model, dflash_seq* const* se
  * capture, under a framework that owns all device memory through its own
  * pool, or in a loop that must never block in the allocator).
  * Same arguments, layouts and result as dflash_debug_attention.  Its scratch
- * (the context views; the key splits merge in distributed shared memory and
- * need no partials in global memory) is a fixed 16 MiB device array
- * inside this library, held by every GPU that loads the library until the
- * process exits; the call makes no cudaMalloc / cudaFree.  The first call on
- * a device looks up that array's device address (cudaGetSymbolAddress) and
+ * is a fixed 16 MiB device array inside this library, held by every GPU that
+ * loads the library until the process exits; the call makes no cudaMalloc /
+ * cudaFree.  The array holds the context views and, for a long context whose
+ * keys split over more CTAs than clusters place, the splits' partial rows
+ * (written before they are read: nothing needs to start at zero); when those
+ * rows do not fit, the call runs the cluster merge (distributed shared
+ * memory), which needs no partials in global memory.  The first call on a
+ * device looks up that array's device address (cudaGetSymbolAddress) and
  * keeps it: make that first call before any stream capture.  Every call shares
  * the one array and overwrites what the previous call left there, so calls
  * whose work overlaps on the GPU (other streams, other threads) race: order
  * them on one stream.  Errors: as dflash_debug_attention, and ERANGE when the
- * call needs more scratch than the array holds (more than 256 sequences) --
- * nothing is launched then.
+ * context views do not fit the array (more than 256 sequences) -- nothing is
+ * launched then.
  */
 DFLASH_API int dflash_attention_noalloc(dflash_model* model, dflash_seq* const* seqs, int32_t n_seqs, int32_t layer,
                                         const int64_t* anchor_pos, int32_t block_len, const float* qkv, float* y,
