@@ -241,6 +241,11 @@ class Model:
                                                  _stream(stream)))
         return out
 
+    def wait_expiry(self, limit_ns: int, stream=None):
+        """Run the library's bounded wait on an mbarrier that nothing arrives on
+        (raises DFlashError ECUDA when the wait gives up, as it must)."""
+        self._check(lib().dflash_debug_wait_expiry(self.handle, int(limit_ns), _stream(stream)))
+
     def trace(self, enable: bool = True):
         self._check(lib().dflash_debug_trace(self.handle, 1 if enable else 0))
 

@@ -69,6 +69,7 @@ _SIGS = {
     "dflash_debug_head_codes": (C.c_int, [_VP, _VP, _VP, _VP]),
     "dflash_debug_q4_groupsums": (C.c_int, [_VP, C.c_int32, _VP, C.c_int32, _VP, _VP]),
     "dflash_debug_q4_matmul": (C.c_int, [_VP, C.c_int32, _VP, _VP, C.c_int32, _VP, _VP]),
+    "dflash_debug_wait_expiry": (C.c_int, [_VP, C.c_int64, _VP]),
     "dflash_debug_read_kv": (C.c_int, [_VP, _VP, C.c_int32, C.c_int64, C.c_int64, _VP, _VP, _VP]),
     "dflash_debug_trace": (C.c_int, [_VP, C.c_int32]),
     "dflash_debug_trace_force": (C.c_int, [_VP, C.c_int32, C.c_int32, _VP, _VP]),

@@ -1495,6 +1495,19 @@ int dflash_debug_q4_matmul(dflash_model* m, int32_t id, const int8_t* x, const f
     return DFLASH_OK;
 }
 
+int dflash_debug_wait_expiry(dflash_model* m, int64_t limit_ns, void* stream) {
+    int rc = check_model(m);
+    if (rc) return rc;
+    if (limit_ns < 1000 || limit_ns > 10000000000ll)
+        return set_err(m, DFLASH_EINVAL, "limit_ns outside [1 us, 10 s]");
+    cudaStream_t st = (cudaStream_t)stream;
+    KL(m, "wait_expiry", 1, 0.0, st, wait_expiry(m->err_dev, (uint64_t)limit_ns, st));
+    CK(m, cudaMemcpyAsync(m->err_host, m->err_dev, sizeof(int), cudaMemcpyDeviceToHost, st));
+    CK(m, cudaStreamSynchronize(st));
+    if (*m->err_host) return device_wait_expired(m);
+    return DFLASH_OK;
+}
+
 int dflash_debug_read_kv(dflash_model* m, const dflash_seq* s, int32_t layer, int64_t pos, int64_t n, float* k,
                          float* v, void* stream) {
     int rc = check_model(m);

@@ -1063,4 +1063,24 @@ int attention(const float* qkv, int ld, int n_seqs, int block_len, const AttnSeq
                             num_sms, st, q_norm, k_norm, rope, eps);
 }
 
+// ------------------------------------------------------------------ wait expiry
+// One warp waits, with the bounded wait every kernel of the library uses, on an
+// mbarrier that nothing arrives on: the wait gives up after limit_ns, and the
+// kernel raises *err exactly as a kernel whose data never arrived does.
+__global__ void wait_expiry_kernel(int* __restrict__ err, unsigned long long limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    bool ok = true;
+    if (threadIdx.x == 0) ok = mbar_wait(&bar, 0, limit_ns);
+    if (!__all_sync(0xffffffffu, ok) && threadIdx.x == 0) atomicExch(err, 1);
+}
+
+int wait_expiry(int* err_flag, uint64_t limit_ns, cudaStream_t st) {
+    return (int)launch(wait_expiry_kernel, dim3(1), dim3(32), 0, st, err_flag, (unsigned long long)limit_ns);
+}
+
 }  // namespace dflash

@@ -228,4 +228,8 @@ int64_t attn_scratch_floats(int n_seqs, int block_len, int max_ctx, int nq, int 
 // the cluster merge).
 int attn_kernels(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int hd, int num_sms, int64_t part_floats);
 
+// Failure detection without a fault: one warp's bounded wait on an mbarrier
+// that nothing arrives on runs out after limit_ns and raises *err_flag.
+int wait_expiry(int* err_flag, uint64_t limit_ns, cudaStream_t st);
+
 }  // namespace dflash

@@ -294,6 +294,18 @@ DFLASH_API int dflash_debug_q4_matmul(dflash_model* model, int32_t matrix_id, co
                                       int32_t rows, float* y, void* stream);
 
 /*
+ * Failure detection without a GPU fault: one warp waits, with the bounded
+ * wait (a %globaltimer limit) that every kernel of the library uses for its
+ * data, on an mbarrier that nothing ever arrives on.  The wait gives up after
+ * limit_ns, the kernel raises the model's error flag and returns, and the call
+ * reports it exactly as a call whose kernel's data never arrived: ECUDA, and
+ * the model is poisoned (every later call on it returns ECUDA); the CUDA
+ * context stays usable.  The pages have no counterpart.
+ * Errors: EINVAL (limit_ns outside [1 us, 10 s]), ECUDA.
+ */
+DFLASH_API int dflash_debug_wait_expiry(dflash_model* model, int64_t limit_ns, void* stream);
+
+/*
  * The stored keys and values of context positions [pos, pos + n) of one
  * layer: k and v [n][kv_heads][head_dim] f32 (either may be NULL), each the
  * stored pair's hi + lo.  Errors: EINVAL, ERANGE (positions not held), ECUDA.

@@ -420,6 +420,32 @@ def test_device_io_matches_host_io():
     seq.close()
 
 
+def test_bounded_wait_expiry_is_reported():
+    """A kernel whose data never arrives gives up its bounded wait, raises the
+    model's error flag and returns: the call reports ECUDA, the model stays
+    poisoned, and the CUDA context still serves a fresh model."""
+    dfl = _dfl()
+    g = W.WORKLOADS["small_q4"].geom
+    w = W.make_weights(g)
+    m = dfl.Model(g, w)
+    try:
+        with pytest.raises(dfl.DFlashError) as ei:
+            m.wait_expiry(50_000_000)  # 50 ms
+        assert ei.value.code == dfl._abi.DFLASH_ECUDA
+        assert "bounded wait" in str(ei.value)
+        with pytest.raises(dfl.DFlashError):
+            m.new_sequence(8)
+    finally:
+        m.close()
+    m2 = dfl.Model(g, w)
+    seq = m2.new_sequence(40)
+    m2.ctx_append(seq, 0, W.make_taps(g, 20, call_id=5))
+    logits, toks = m2.block([seq], [3], [20], g.block)
+    assert np.isfinite(logits).all()
+    seq.close()
+    m2.close()
+
+
 def test_error_codes():
     dfl = _dfl()
     p = pair("tiny_f32")
