@@ -496,6 +496,244 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     }
 }
 
+// ---------------------------------------------------------------- 4-bit, 256 rows a CTA
+// The 4-bit matmuls of many rows: a CTA runs two 128-row tiles (256 rows)
+// against each converted 128-row weight tile, so that every dequantised
+// weight feeds 2 x 128 rows of MMAs (the converters' work per multiply-add
+// is half that of one tile a CTA), and K is split over CTAs in slices of at
+// most kT2MaxKb k-blocks (2048 columns): tensor memory accumulates no more
+// than that (its truncating f32 accumulation stays at the f32 level), and the
+// slices' partial sums meet in y through round-to-nearest vector reductions.
+// Measured against the quantised definition (relative rms error): K = 20480
+// in ten slices 1.4e-6, K = 4096 4.3e-7 (the chunk-draining kernel before
+// it: 1.6e-7, at 1.2 - 1.4x the time; 1024-column slices: 4.4e-7 at K =
+// 20480, at 1.15x the time of these).
+// Roles as tc_gemm_kernel: one TMA lane (the 256-row f16 activation box and
+// the packed weights), eight converter warps (which also run the epilogue),
+// one MMA lane.
+constexpr int kT2Tiles = 2;               // 128-row tiles a CTA
+constexpr int kT2MaxKb = 32;              // k-blocks a CTA at most
+constexpr int kT2Act = 3, kT2Cvt = 2, kT2Raw = 8;
+constexpr int kT2A = kT2Tiles * kTcA;     // one 256-row f16 activation box, 128-byte swizzle
+constexpr int kT2B = 2 * kTcN * kTcKB * 2;  // hi and lo weight tiles
+constexpr int kT2Raw_ = 2 * 4 * kQ4Chunk;   // two 64-row groups of packed weights
+constexpr size_t kT2Smem = 1024 + 1024 + (size_t)kT2Act * kT2A + (size_t)kT2Cvt * kT2B + (size_t)kT2Raw * kT2Raw_;
+static_assert(kT2Smem <= 227 * 1024, "shared memory");
+
+struct T2Ctl {
+    uint64_t raw_full[kT2Raw], raw_empty[kT2Raw], act_full[kT2Act], act_empty[kT2Act], cvt_full[kT2Cvt],
+        cvt_empty[kT2Cvt], acc_full;
+    uint32_t tmem;
+    int abort;
+};
+static_assert(sizeof(T2Ctl) <= 1024, "control block");
+
+// hi / lo f16 tiles of one 16-row chunk's lane slot (both 32-column groups),
+// the lane-slot permutation of tc_gemm_kernel (conflict-free stores)
+DF_DEV void t2_convert_q4(const unsigned char* rs, unsigned char* bt, int warp, int lane, bool valid) {
+    unsigned char* blo = bt + kTcN * kTcKB * 2;
+    const int gg = warp >> 2, rr = warp & 3;
+    const int qw = lane >> 3, jw = lane & 7;
+    const int gq = (jw < 4) ? 2 * qw : ((2 * qw) ^ 5), tq = jw & 3;
+    const int slot = 4 * gq + tq;
+    const int nl0 = gg * 64 + rr * 16 + gq, nl1 = nl0 + 8;
+    if (valid) {
+        const unsigned char* ch = rs + gg * 4 * kQ4Chunk + rr * kQ4Chunk;
+        const uint4 wv = *reinterpret_cast<const uint4*>(ch + slot * 16);
+        const uint2 sv = *reinterpret_cast<const uint2*>(ch + 512 + gq * 8);
+        const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+        for (int gi = 0; gi < 2; ++gi) {
+            uint32_t a0[4], a1[4];
+            unpack_q4_word(wd[gi * 2 + 0], a0);  // columns 8 tq + 0..3
+            unpack_q4_word(wd[gi * 2 + 1], a1);  // columns 8 tq + 4..7
+            const uint32_t sw = gi ? sv.y : sv.x;  // (s[gq][g], s[gq+8][g])
+            const uint32_t s0 = __byte_perm(sw, 0, 0x1010), s1 = __byte_perm(sw, 0, 0x3232);
+            const uint32_t q0[4] = {a0[0], a0[2], a1[0], a1[2]};  // row gq
+            const uint32_t q1[4] = {a0[1], a0[3], a1[1], a1[3]};  // row gq + 8
+            uint4 hi, lo;
+            split_scaled(q0, s0, hi, lo);
+            *reinterpret_cast<uint4*>(bt + tc_swz(nl0, 4 * gi + tq)) = hi;
+            *reinterpret_cast<uint4*>(blo + tc_swz(nl0, 4 * gi + tq)) = lo;
+            split_scaled(q1, s1, hi, lo);
+            *reinterpret_cast<uint4*>(bt + tc_swz(nl1, 4 * gi + tq)) = hi;
+            *reinterpret_cast<uint4*>(blo + tc_swz(nl1, 4 * gi + tq)) = lo;
+        }
+    } else {
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int gi = 0; gi < 2; ++gi) {
+            *reinterpret_cast<uint4*>(bt + tc_swz(nl0, 4 * gi + tq)) = z;
+            *reinterpret_cast<uint4*>(blo + tc_swz(nl0, 4 * gi + tq)) = z;
+            *reinterpret_cast<uint4*>(bt + tc_swz(nl1, 4 * gi + tq)) = z;
+            *reinterpret_cast<uint4*>(blo + tc_swz(nl1, 4 * gi + tq)) = z;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) q4_tc2_kernel(const __grid_constant__ CUtensorMap xmap, TcArgs a) {
+    extern __shared__ __align__(1024) unsigned char sm_raw[];
+    unsigned char* sm = sm_raw + ((1024 - (smem_addr(sm_raw) & 1023)) & 1023);
+    T2Ctl& ctl = *reinterpret_cast<T2Ctl*>(sm);
+    unsigned char* act = sm + 1024;
+    unsigned char* cvt = act + kT2Act * kT2A;
+    unsigned char* raw = cvt + kT2Cvt * kT2B;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nt = blockIdx.x, m0 = blockIdx.y * (kT2Tiles * kTcM);
+    const int tiles = min(kT2Tiles, (a.T - m0 + kTcM - 1) / kTcM);  // row tiles holding rows
+    const int kb_lo = blockIdx.z * a.kb_per_split, kb_hi = min(a.L.ksteps, kb_lo + a.kb_per_split);
+    const int nkb = kb_hi - kb_lo;
+    const int ngroups_n = a.N / 64;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kT2Raw; ++i) {
+            mbar_init(&ctl.raw_full[i], 1);
+            mbar_init(&ctl.raw_empty[i], kTcCvtWarps);
+        }
+        for (int i = 0; i < kT2Act; ++i) {
+            mbar_init(&ctl.act_full[i], 1);
+            mbar_init(&ctl.act_empty[i], 1);
+        }
+        for (int i = 0; i < kT2Cvt; ++i) {
+            mbar_init(&ctl.cvt_full[i], kTcCvtWarps);
+            mbar_init(&ctl.cvt_empty[i], 1);
+        }
+        mbar_init(&ctl.acc_full, 1);
+        ctl.abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kTcMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&ctl.tmem)),
+                     "r"(kT2Tiles * kTcN)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl.tmem;
+    pdl_trigger();
+    pdl_wait();
+
+    auto give_up = [&]() {
+        atomicExch(a.err, 1);
+        *reinterpret_cast<volatile int*>(&ctl.abort) = 1;
+    };
+    auto aborted = [&]() { return *reinterpret_cast<volatile int*>(&ctl.abort) != 0; };
+
+    if (warp == kTcTmaWarp) {
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&xmap) : "memory");
+            int issued = 0, ng = 0;
+            for (int gg = 0; gg < kTcN / 64; ++gg) ng += (nt * (kTcN / 64) + gg < ngroups_n) ? 1 : 0;
+            for (int i = 0; i < nkb; ++i) {
+                const int r = i % kT2Raw, sa = i % kT2Act;
+                bool ok = true;
+                if (i >= kT2Raw) ok = mbar_wait(&ctl.raw_empty[r], ((i / kT2Raw) - 1) & 1, kTcWait);
+                if (ok && i >= kT2Act) ok = mbar_wait(&ctl.act_empty[sa], ((i / kT2Act) - 1) & 1, kTcWait);
+                if (!ok) give_up();
+                if (!ok || aborted()) break;
+                fence_proxy_async_smem();
+                const int kb = kb_lo + i;
+                // the whole 256-row box: rows past T read as zeros and count toward the bytes
+                mbar_arrive_expect_tx(&ctl.act_full[sa], (uint32_t)kT2A);
+                tma_load_2d(act + sa * kT2A, &xmap, kb * kTcKB, m0, &ctl.act_full[sa]);
+                unsigned char* dst = raw + r * kT2Raw_;
+                mbar_arrive_expect_tx(&ctl.raw_full[r], (uint32_t)(ng * 4 * kQ4Chunk));
+                for (int gg = 0; gg < ng; ++gg)
+                    bulk_g2s(dst + gg * 4 * kQ4Chunk, a.w + q4_chunk_offset(a.L, 4 * (a.g0 + nt * (kTcN / 64) + gg), kb),
+                             4 * kQ4Chunk, &ctl.raw_full[r]);
+                issued = i + 1;
+            }
+            for (int i = max(0, issued - kT2Raw); i < issued; ++i)
+                mbar_wait(&ctl.raw_full[i % kT2Raw], (i / kT2Raw) & 1, kTcWait);
+            for (int i = max(0, issued - kT2Act); i < issued; ++i)
+                mbar_wait(&ctl.act_full[i % kT2Act], (i / kT2Act) & 1, kTcWait);
+        }
+    } else if (warp == kTcMmaWarp) {
+        if (lane == 0) {
+            for (int i = 0; i < nkb; ++i) {
+                const int sx = i % kT2Act, sc = i % kT2Cvt;
+                bool ok = mbar_wait(&ctl.act_full[sx], (i / kT2Act) & 1, kTcWait);
+                if (ok) ok = mbar_wait(&ctl.cvt_full[sc], (i / kT2Cvt) & 1, kTcWait);
+                if (!ok) give_up();
+                if (!ok || aborted()) break;
+                tc_fence_after();
+                const uint32_t sa = smem_addr(act + sx * kT2A);
+                const uint32_t sb = smem_addr(cvt + sc * kT2B);
+#pragma unroll
+                for (int j = 0; j < kTcKB / 16; ++j) {
+                    const uint64_t bh = tc_desc_sw128(sb + 32 * j), bl = tc_desc_sw128(sb + kTcN * kTcKB * 2 + 32 * j);
+                    for (int t = 0; t < tiles; ++t) {
+                        const uint64_t ad = tc_desc_sw128(sa + t * kTcA + 32 * j);
+                        const uint32_t d = tmem + (uint32_t)(t * kTcN);
+                        tc_mma(d, ad, bh, (i > 0 || j > 0) ? 1u : 0u);
+                        tc_mma(d, ad, bl, 1u);
+                    }
+                }
+                tc_commit(&ctl.cvt_empty[sc]);
+                tc_commit(&ctl.act_empty[sx]);
+            }
+            // arrives once every MMA issued so far has completed
+            tc_commit(&ctl.acc_full);
+        }
+    } else {
+        // ---------------------------------------------------------------- converters
+        for (int i = 0; i < nkb; ++i) {
+            const int r = i % kT2Raw, c = i % kT2Cvt;
+            bool w = mbar_wait(&ctl.raw_full[r], (i / kT2Raw) & 1, kTcWait);
+            if (w && i >= kT2Cvt) w = mbar_wait(&ctl.cvt_empty[c], ((i / kT2Cvt) - 1) & 1, kTcWait);
+            if (!w) give_up();
+            if (__any_sync(0xffffffffu, !w || aborted())) break;
+            t2_convert_q4(raw + r * kT2Raw_, cvt + c * kT2B, warp, lane, nt * (kTcN / 64) + (warp >> 2) < ngroups_n);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&ctl.raw_empty[r]);
+                mbar_arrive(&ctl.cvt_full[c]);
+            }
+        }
+        // ---------------------------------------------------------------- epilogue
+        const bool ok = mbar_wait(&ctl.acc_full, 0, kTcWait);
+        if (!ok) give_up();
+        tc_fence_after();
+        if (__all_sync(0xffffffffu, ok && !aborted()) && nkb > 0) {
+            const int sub = warp & 3, half = warp >> 2;
+            const bool red = a.accumulate != 0 || gridDim.z > 1;
+            for (int t = 0; t < tiles; ++t) {
+                const int row = m0 + t * kTcM + 32 * sub + lane;
+                const int n0 = nt * kTcN + half * 64;
+                const float xs = row < a.T ? a.xscale[row] : 0.f;
+#pragma unroll 1
+                for (int cc = 0; cc < 64; cc += 16) {
+                    uint32_t v[16];
+                    tc_ld16(tmem + ((uint32_t)(32 * sub) << 16) + (uint32_t)(t * kTcN + half * 64 + cc), v);
+                    tc_wait_ld();
+                    if (row < a.T && n0 + cc < a.N) {
+                        float* dst = a.y + (int64_t)row * a.ldy + n0 + cc;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float f0 = __uint_as_float(v[4 * q]) * xs, f1 = __uint_as_float(v[4 * q + 1]) * xs,
+                                        f2 = __uint_as_float(v[4 * q + 2]) * xs, f3 = __uint_as_float(v[4 * q + 3]) * xs;
+                            if (red)
+                                red_add_v4(dst + 4 * q, f0, f1, f2, f3);
+                            else
+                                *reinterpret_cast<float4*>(dst + 4 * q) = make_float4(f0, f1, f2, f3);
+                        }
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kTcMmaWarp) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kT2Tiles * kTcN)
+                     : "memory");
+    }
+}
+
 // ---------------------------------------------------------------- host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -520,10 +758,10 @@ static EncodeTiledFn encode_fn() {
 
 // the tensor map of the activation codes as f16 [T][K] (rows of K halves):
 // 64 x 128 boxes in the 128-byte swizzle, rows past T read as zeros
-static bool act_map(CUtensorMap* map, const __half* codes, int K, int T) {
+static bool act_map(CUtensorMap* map, const __half* codes, int K, int T, int box_rows = kTcM) {
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)T};
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kTcKB, (cuuint32_t)kTcM};
+    const cuuint32_t box[2] = {(cuuint32_t)kTcKB, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return encode_fn()(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(codes), dims, strides, box, estr,
                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -582,22 +820,26 @@ int q4_tc(const uint8_t* packed, Q4Layout L, int tile0, int N, QAct x, const __h
         (reinterpret_cast<uintptr_t>(x16) & 15))
         return (int)cudaErrorInvalidValue;
     CUtensorMap map;
-    if (!act_map(&map, x16, K, T)) return (int)cudaErrorInvalidValue;
-    cudaError_t e = tc_set_smem<false>();
-    if (e != cudaSuccess) return (int)e;
-    const int mt = (T + kTcM - 1) / kTcM, ntl = (N + kTcN - 1) / kTcN;
-    // split K over CTAs when the tiles alone leave most SMs idle
-    int splits = 1;
-    if (mt * ntl * 2 <= num_sms) splits = std::min(std::max(1, num_sms / (mt * ntl)), std::max(1, L.ksteps / 8));
+    if (!act_map(&map, x16, K, T, kT2Tiles * kTcM)) return (int)cudaErrorInvalidValue;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(q4_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kT2Smem);
+        if (e != cudaSuccess) return (int)e;
+        attr = true;
+    }
+    const int mt = (T + kT2Tiles * kTcM - 1) / (kT2Tiles * kTcM), ntl = (N + kTcN - 1) / kTcN;
+    // K slices of at most kT2MaxKb k-blocks (the accumulation bound); more
+    // slices while the tiles alone leave more than a third of the SMs idle
+    int splits = (L.ksteps + kT2MaxKb - 1) / kT2MaxKb;
+    while (mt * ntl * splits * 3 < num_sms * 2 && splits * 2 <= L.ksteps) splits *= 2;
     const int kps = (L.ksteps + splits - 1) / splits;
     splits = (L.ksteps + kps - 1) / kps;
     if (splits > 1 && !accumulate) {
-        e = cudaMemset2DAsync(y, (size_t)ldy * sizeof(float), 0, (size_t)N * sizeof(float), T, st);
+        cudaError_t e = cudaMemset2DAsync(y, (size_t)ldy * sizeof(float), 0, (size_t)N * sizeof(float), T, st);
         if (e != cudaSuccess) return (int)e;
     }
     TcArgs args{packed, L, tile0 / 4, N, x.scale, T, y, ldy, accumulate ? 1 : 0, kps, nullptr, nullptr, err_flag};
-    return (int)launch(tc_gemm_kernel<false>, dim3(ntl, mt, splits), dim3(kTcThreads), TcShape<false>::kSmem, st, map,
-                       args);
+    return (int)launch(q4_tc2_kernel, dim3(ntl, mt, splits), dim3(kTcThreads), kT2Smem, st, map, args);
 }
 
 bool head_tc_supported(int ksteps, QAct x) {
