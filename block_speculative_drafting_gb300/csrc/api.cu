@@ -74,6 +74,17 @@ struct dflash_model {
     unsigned* chain_bar = nullptr;  // the chain kernel's barrier counter (zero between launches)
     bool use_chain = false;         // run a block's (and a short append's) steps as chain programs
     bool use_tc = true;             // matmuls of more than 16 rows on the tcgen05 kernel (DFLASH_TC=0: mma.sync)
+    bool use_dense = true;          // ... from dense f16 weight copies (DFLASH_DENSE=0: dequantise in the kernel)
+    // dense f16 copies of the matrices for the many-row path, built on first need:
+    // the 4-bit matrices as (hi, lo) planes [N][K], the head's codes [vocab][hidden]
+    struct DenseMat {
+        const uint8_t* packed;
+        int N, K;
+        __half *hi, *lo;
+    };
+    std::vector<DenseMat> dense;
+    __half* head16 = nullptr;
+    bool dense_ready = false;
     int* err_host = nullptr;  // pinned copy, read after a synchronising call
 
     // launch accounting and the optional per-launch event profile
@@ -338,6 +349,8 @@ int build_model(dflash_model* m, const dflash_weights* w, bool on_dev, cudaStrea
         m->use_chain = ev && ev[0] == '1';
         const char* tv = getenv("DFLASH_TC");
         m->use_tc = !(tv && tv[0] == '0');
+        const char* dv = getenv("DFLASH_DENSE");
+        m->use_dense = !(dv && dv[0] == '0');
     }
     CK(m, cudaMallocHost(&m->err_host, sizeof(int)));
     *m->err_host = 0;
@@ -488,6 +501,72 @@ double f32_bytes_of(int N, int K, int T, bool accumulate) {
     return (double)N * K * 4 + (double)T * K * 4 + (double)T * N * 4 * (accumulate ? 2 : 1);
 }
 
+// The dense f16 copies of every 4-bit matrix and of the head, for the
+// tensor-core kernels of the many-row path (about 5.6 GB at the Qwen3-8B
+// shapes), built once on the first call that needs them -- never inside a
+// graph capture (callers run it before any).
+int ensure_dense(dflash_model* m, cudaStream_t st) {
+    if (m->dense_ready || !m->use_tc || !m->use_dense || m->g.quant != DFLASH_QUANT_Q4G32) return 0;
+    const dflash_geometry& g = m->g;
+    const int H = g.hidden, I = g.intermediate;
+    struct Src {
+        const uint8_t* p;
+        Q4Layout L;
+        int N, K;
+    };
+    std::vector<Src> srcs = {{m->fc_p, m->L_fc, H, m->tap_w}, {m->kvctx_p, m->L_kvctx, m->kvctx_w, H}};
+    for (const Layer& Ly : m->layers) {
+        srcs.push_back({Ly.qkv_p, m->L_qkv, m->qkv_w, H});
+        srcs.push_back({Ly.o_p, m->L_o, H, m->qd});
+        srcs.push_back({Ly.gu_p, m->L_gu, 2 * I, H});
+        srcs.push_back({Ly.down_p, m->L_down, H, I});
+    }
+    size_t most = (size_t)g.vocab * H;
+    for (const Src& q : srcs) most = std::max(most, (size_t)q.N * q.K);
+    int8_t* codes = nullptr;
+    uint16_t* scales = nullptr;
+    CK(m, cudaMalloc(&codes, most));
+    cudaError_t e = cudaMalloc(&scales, most / 32 * sizeof(uint16_t));
+    int rc = 0;
+    if (e != cudaSuccess) rc = (int)e;
+    std::vector<dflash_model::DenseMat> made;
+    for (const Src& q : srcs) {
+        if (rc) break;
+        dflash_model::DenseMat d{q.p, q.N, q.K, nullptr, nullptr};
+        rc = dalloc(m, &d.hi, (size_t)q.N * q.K);
+        if (!rc) rc = dalloc(m, &d.lo, (size_t)q.N * q.K);
+        if (!rc) rc = q4_unpack(q.p, q.L, 0, q.N, q.K, codes, scales, st);
+        if (!rc) rc = dequant_hilo(codes, scales, q.N, q.K, d.hi, d.lo, st);
+        if (!rc) made.push_back(d);
+        if (!rc) rc = (int)cudaStreamSynchronize(st);  // the temporaries are reused
+    }
+    __half* h16 = nullptr;
+    if (!rc) rc = dalloc(m, &h16, (size_t)g.vocab * H);
+    if (!rc) rc = i8_unpack(m->head_p, g.vocab, H, H / kI8KStep, codes, st);
+    if (!rc) rc = codes_to_f16(codes, H, g.vocab, H, h16, m->num_sms, st);
+    if (!rc) rc = (int)cudaStreamSynchronize(st);
+    cudaFree(codes);
+    cudaFree(scales);
+    CK(m, (cudaError_t)rc);
+    m->dense = made;
+    m->head16 = h16;
+    m->dense_ready = true;
+    return 0;
+}
+
+// The dense copy of a packed 4-bit matrix's rows [row0, row0 + N), or null.
+bool dense_of(const dflash_model* m, const uint8_t* packed, int row0, int N, int K, const __half** hi,
+              const __half** lo) {
+    if (!m->dense_ready) return false;
+    for (const auto& d : m->dense)
+        if (d.packed == packed && d.K == K && row0 + N <= d.N) {
+            *hi = d.hi + (size_t)row0 * K;
+            *lo = d.lo + (size_t)row0 * K;
+            return true;
+        }
+    return false;
+}
+
 // A 4-bit matmul on int8 codes: the streaming kernel for up to 16 rows (it
 // ADDS into y, which an earlier kernel cleared or which holds the residual),
 // the general one beyond.
@@ -500,8 +579,15 @@ int q4_mm(dflash_model* m, const uint8_t* packed, Q4Layout L, int tile0, int N, 
                (reinterpret_cast<uintptr_t>(y) & 15) == 0 && m->x16.bytes >= (size_t)T * K * sizeof(__half)) {
         __half* x16 = P<__half>(m->x16);
         KL(m, "act_f16", 1, (double)T * K * 3, st, codes_to_f16(x.codes, x.ld, T, K, x16, m->num_sms, st));
-        KL(m, "q4_tc", 1, q4_bytes_of(N, K, T, accumulate), st,
-           q4_tc(packed, L, tile0, N, x, x16, T, y, ldy, accumulate, m->num_sms, m->err_dev, st));
+        const __half *hi = nullptr, *lo = nullptr;
+        if (dense_of(m, packed, tile0 * 16, N, K, &hi, &lo)) {
+            // dense weight bytes: 4 a weight
+            KL(m, "q4_tc", 1, (double)N * K * 4 + (double)T * K * 2 + (double)T * N * 4 * (accumulate ? 2 : 1), st,
+               q4_tc_dense(hi, lo, N, K, x, x16, T, y, ldy, accumulate, m->num_sms, m->err_dev, st));
+        } else {
+            KL(m, "q4_tc", 1, q4_bytes_of(N, K, T, accumulate), st,
+               q4_tc(packed, L, tile0, N, x, x16, T, y, ldy, accumulate, m->num_sms, m->err_dev, st));
+        }
     } else {
         KL(m, "q4_gemm", 1, q4_bytes_of(N, K, T, accumulate), st,
            q4_gemm(packed, L, tile0, N, x, T, y, ldy, accumulate, m->num_sms, st));
@@ -518,9 +604,15 @@ int run_head(dflash_model* m, QAct xh, int D, float* logit_out, unsigned long lo
         m->x16.bytes >= (size_t)D * H * sizeof(__half)) {
         __half* x16 = P<__half>(m->x16);
         KL(m, "act_f16", 1, (double)D * H * 3, st, codes_to_f16(xh.codes, xh.ld, D, H, x16, m->num_sms, st));
-        KL(m, "head_tc", 1, hb, st,
-           head_tc(m->head_p, m->head_scale, g.vocab, H / kI8KStep, xh, x16, D, logit_out, g.vocab, keys, m->err_dev,
-                   st));
+        if (m->dense_ready && m->head16) {
+            KL(m, "head_tc", 1, hb + (double)g.vocab * H, st,
+               head_tc_dense(m->head16, m->head_scale, g.vocab, H, xh, x16, D, logit_out, g.vocab, keys, m->err_dev,
+                             st));
+        } else {
+            KL(m, "head_tc", 1, hb, st,
+               head_tc(m->head_p, m->head_scale, g.vocab, H / kI8KStep, xh, x16, D, logit_out, g.vocab, keys,
+                       m->err_dev, st));
+        }
     } else {
         KL(m, "head_stream", 1, hb, st,
            head_stream(m->head_p, m->head_scale, g.vocab, H / kI8KStep, xh, D, logit_out, g.vocab, keys, m->num_sms,
@@ -959,6 +1051,7 @@ int dflash_ctx_append(dflash_model* m, dflash_seq* s, int64_t pos, const float* 
     if (n_rows == 0) return DFLASH_OK;
     const int64_t chunk = std::min<int64_t>(n_rows, kAppendRows);
     rc = ensure_append_scratch(m, chunk);
+    if (!rc && chunk > 16) rc = ensure_dense(m, st);
     if (rc) return rc;
     for (int64_t r0 = 0; r0 < n_rows; r0 += chunk) {
         const int64_t n = std::min(chunk, n_rows - r0);
@@ -1034,7 +1127,11 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
     CK(m, ensure_m(m, m->pos0, (size_t)n_seqs * sizeof(int64_t)));
     CK(m, ensure_m(m, m->rope, (size_t)R * (hd / 2) * sizeof(float2)));
     CK(m, ensure_m(m, m->aseqs, (size_t)g.layers * n_seqs * sizeof(AttnSeq)));
-    if (quant && R > 16) CK(m, ensure_m(m, m->x16, (size_t)R * maxK * sizeof(__half)));
+    if (quant && R > 16) {
+        CK(m, ensure_m(m, m->x16, (size_t)R * maxK * sizeof(__half)));
+        rc = ensure_dense(m, st);
+        if (rc) return rc;
+    }
     float* logit_out = io_on_device ? logits : nullptr;
     if (!io_on_device && logits) {
         CK(m, ensure_m(m, m->logits, (size_t)D * g.vocab * sizeof(float)));
@@ -1479,6 +1576,15 @@ int dflash_debug_q4_matmul(dflash_model* m, int32_t id, const int8_t* x, const f
     // the streaming kernel adds into y: start from zeros on every path
     if (!e) e = (int)cudaMemsetAsync(dy, 0, outn * sizeof(float), st);
     if (!e && rows > 16) e = ensure_m(m, m->x16, (size_t)rows * ldk * sizeof(__half));
+    if (!e && rows > 16) {
+        const int drc = ensure_dense(m, st);
+        if (drc) {
+            cudaFree(dx);
+            cudaFree(dsc);
+            cudaFree(dy);
+            return drc;
+        }
+    }
     QAct qa{dx, dsc, ldk};
     int lib_rc = DFLASH_OK;
     if (!e) lib_rc = q4_mm(m, v.packed, v.L, v.tile0, v.N, v.K, qa, rows, dy, v.N, false, st);

@@ -734,6 +734,357 @@ __global__ void __launch_bounds__(kTcThreads, 1) q4_tc2_kernel(const __grid_cons
     }
 }
 
+// ---------------------------------------------------------------- dense weight copies
+// For the many-row path the library can hold a second copy of each matrix as
+// dense f16: the 4-bit matrices as the exact pair hi = f16(s q), lo =
+// f16(s q - hi) (two planes [N][K]), the head as its int8 codes in f16
+// ([V][K]).  With those the tensor-core kernels take every operand tile by
+// TMA and convert nothing (HBM is plentiful; conversion was their limit).
+__global__ void dequant_hilo_kernel(const int8_t* __restrict__ codes, const uint16_t* __restrict__ scales, int N,
+                                    int K, __half* __restrict__ hi, __half* __restrict__ lo) {
+    const int64_t n = (int64_t)N * K;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / K;
+        const int c = (int)(i - r * K);
+        const float sf = __half2float(__ushort_as_half(scales[r * (K / 32) + c / 32]));
+        const float p = sf * (float)codes[i];  // exact: 11 x 4 significant bits
+        const __half h = __float2half_rn(p);
+        hi[i] = h;
+        lo[i] = __float2half_rn(p - __half2float(h));  // exact remainder
+    }
+}
+
+int dequant_hilo(const int8_t* codes, const uint16_t* scales, int N, int K, __half* hi, __half* lo, cudaStream_t st) {
+    if (N <= 0 || K <= 0 || K % 32) return (int)cudaErrorInvalidValue;
+    dequant_hilo_kernel<<<1024, 256, 0, st>>>(codes, scales, N, K, hi, lo);
+    return (int)cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- 4-bit, dense copies
+// q4_tc2_kernel's tiling (two 128-row tiles a CTA, K slices of at most
+// kT2MaxKb k-blocks) with the weight tiles' hi and lo planes loaded by TMA
+// from the dense copy: one TMA lane, one MMA lane, eight epilogue warps.
+constexpr int kT3Stages = 3;
+constexpr int kT3Bt = kTcN * kTcKB * 2;              // one 128 x 64 f16 weight tile (16 KB)
+constexpr int kT3Stage = kT2Tiles * kTcA + 2 * kT3Bt;  // 256-row activation box + hi + lo (64 KB)
+constexpr size_t kT3Smem = 1024 + 1024 + (size_t)kT3Stages * kT3Stage;
+static_assert(kT3Smem <= 227 * 1024, "shared memory");
+
+struct T3Ctl {
+    uint64_t full[kT3Stages], empty[kT3Stages], acc_full;
+    uint32_t tmem;
+    int abort;
+};
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    q4_tc3_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap hmap,
+                  const __grid_constant__ CUtensorMap lmap, TcArgs a) {
+    extern __shared__ __align__(1024) unsigned char sm_raw[];
+    unsigned char* sm = sm_raw + ((1024 - (smem_addr(sm_raw) & 1023)) & 1023);
+    T3Ctl& ctl = *reinterpret_cast<T3Ctl*>(sm);
+    unsigned char* stages = sm + 1024;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nt = blockIdx.x, m0 = blockIdx.y * (kT2Tiles * kTcM);
+    const int tiles = min(kT2Tiles, (a.T - m0 + kTcM - 1) / kTcM);
+    const int kb_lo = blockIdx.z * a.kb_per_split, kb_hi = min(a.L.ksteps, kb_lo + a.kb_per_split);
+    const int nkb = kb_hi - kb_lo;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kT3Stages; ++i) {
+            mbar_init(&ctl.full[i], 1);
+            mbar_init(&ctl.empty[i], 1);
+        }
+        mbar_init(&ctl.acc_full, 1);
+        ctl.abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kTcMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&ctl.tmem)),
+                     "r"(kT2Tiles * kTcN)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl.tmem;
+    pdl_trigger();
+    pdl_wait();
+
+    auto give_up = [&]() {
+        atomicExch(a.err, 1);
+        *reinterpret_cast<volatile int*>(&ctl.abort) = 1;
+    };
+    auto aborted = [&]() { return *reinterpret_cast<volatile int*>(&ctl.abort) != 0; };
+
+    if (warp == kTcTmaWarp) {
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&xmap) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&hmap) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&lmap) : "memory");
+            int issued = 0;
+            for (int i = 0; i < nkb; ++i) {
+                const int st = i % kT3Stages;
+                if (i >= kT3Stages && !mbar_wait(&ctl.empty[st], ((i / kT3Stages) - 1) & 1, kTcWait)) {
+                    give_up();
+                    break;
+                }
+                if (aborted()) break;
+                const int kb = kb_lo + i;
+                unsigned char* dst = stages + st * kT3Stage;
+                // whole boxes: rows past T or past N read as zeros and count toward the bytes
+                mbar_arrive_expect_tx(&ctl.full[st], (uint32_t)kT3Stage);
+                tma_load_2d(dst, &xmap, kb * kTcKB, m0, &ctl.full[st]);
+                tma_load_2d(dst + kT2Tiles * kTcA, &hmap, kb * kTcKB, nt * kTcN, &ctl.full[st]);
+                tma_load_2d(dst + kT2Tiles * kTcA + kT3Bt, &lmap, kb * kTcKB, nt * kTcN, &ctl.full[st]);
+                issued = i + 1;
+            }
+            for (int i = max(0, issued - kT3Stages); i < issued; ++i)
+                mbar_wait(&ctl.full[i % kT3Stages], (i / kT3Stages) & 1, kTcWait);
+        }
+    } else if (warp == kTcMmaWarp) {
+        if (lane == 0) {
+            for (int i = 0; i < nkb; ++i) {
+                const int st = i % kT3Stages;
+                const bool ok = mbar_wait(&ctl.full[st], (i / kT3Stages) & 1, kTcWait);
+                if (!ok) give_up();
+                if (!ok || aborted()) break;
+                tc_fence_after();
+                const uint32_t sa = smem_addr(stages + st * kT3Stage);
+                const uint32_t sb = sa + kT2Tiles * kTcA;
+#pragma unroll
+                for (int j = 0; j < kTcKB / 16; ++j) {
+                    const uint64_t bh = tc_desc_sw128(sb + 32 * j), bl = tc_desc_sw128(sb + kT3Bt + 32 * j);
+                    for (int t = 0; t < tiles; ++t) {
+                        const uint64_t ad = tc_desc_sw128(sa + t * kTcA + 32 * j);
+                        const uint32_t d = tmem + (uint32_t)(t * kTcN);
+                        tc_mma(d, ad, bh, (i > 0 || j > 0) ? 1u : 0u);
+                        tc_mma(d, ad, bl, 1u);
+                    }
+                }
+                tc_commit(&ctl.empty[st]);
+            }
+            // arrives once every MMA issued so far has completed
+            tc_commit(&ctl.acc_full);
+        }
+    } else {
+        // ---------------------------------------------------------------- epilogue
+        const bool ok = mbar_wait(&ctl.acc_full, 0, kTcWait);
+        if (!ok) give_up();
+        tc_fence_after();
+        if (__all_sync(0xffffffffu, ok && !aborted()) && nkb > 0) {
+            const int sub = warp & 3, half = warp >> 2;
+            const bool red = a.accumulate != 0 || gridDim.z > 1;
+            for (int t = 0; t < tiles; ++t) {
+                const int row = m0 + t * kTcM + 32 * sub + lane;
+                const int n0 = nt * kTcN + half * 64;
+                const float xs = row < a.T ? a.xscale[row] : 0.f;
+#pragma unroll 1
+                for (int cc = 0; cc < 64; cc += 16) {
+                    uint32_t v[16];
+                    tc_ld16(tmem + ((uint32_t)(32 * sub) << 16) + (uint32_t)(t * kTcN + half * 64 + cc), v);
+                    tc_wait_ld();
+                    if (row < a.T && n0 + cc < a.N) {
+                        float* dst = a.y + (int64_t)row * a.ldy + n0 + cc;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float f0 = __uint_as_float(v[4 * q]) * xs, f1 = __uint_as_float(v[4 * q + 1]) * xs,
+                                        f2 = __uint_as_float(v[4 * q + 2]) * xs, f3 = __uint_as_float(v[4 * q + 3]) * xs;
+                            if (red)
+                                red_add_v4(dst + 4 * q, f0, f1, f2, f3);
+                            else
+                                *reinterpret_cast<float4*>(dst + 4 * q) = make_float4(f0, f1, f2, f3);
+                        }
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kTcMmaWarp) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kT2Tiles * kTcN)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- head, dense copy
+// The head over many rows with its codes from the dense f16 copy by TMA: a
+// CTA's 128-row x 128-logit tile, 512-column chunks in two alternating
+// tensor-memory accumulators drained by eight warps into exact int32 sums
+// (a chunk's sum is an integer below 2^24), then the logits and the argmax.
+constexpr int kH2Stages = 5;
+constexpr int kH2Stage = kTcA + kT3Bt;  // 128-row activation box + 128-row code tile (32 KB)
+constexpr size_t kH2Smem = 1024 + 1024 + (size_t)kH2Stages * kH2Stage;
+static_assert(kH2Smem <= 227 * 1024, "shared memory");
+
+struct H2Ctl {
+    uint64_t full[kH2Stages], empty[kH2Stages], dfull[2], dempty[2];
+    uint32_t tmem;
+    int abort;
+};
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    head_tc2_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap, TcArgs a) {
+    extern __shared__ __align__(1024) unsigned char sm_raw[];
+    unsigned char* sm = sm_raw + ((1024 - (smem_addr(sm_raw) & 1023)) & 1023);
+    H2Ctl& ctl = *reinterpret_cast<H2Ctl*>(sm);
+    unsigned char* stages = sm + 1024;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * kTcM, nt = blockIdx.y;
+    const int nkb = a.L.ksteps;
+    const int nchunks = (nkb + kTcChunk - 1) / kTcChunk;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kH2Stages; ++i) {
+            mbar_init(&ctl.full[i], 1);
+            mbar_init(&ctl.empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ctl.dfull[i], 1);
+            mbar_init(&ctl.dempty[i], kTcCvtWarps);
+        }
+        ctl.abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kTcMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&ctl.tmem)),
+                     "r"(2 * kTcN)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl.tmem;
+    pdl_trigger();
+    pdl_wait();
+
+    auto give_up = [&]() {
+        atomicExch(a.err, 1);
+        *reinterpret_cast<volatile int*>(&ctl.abort) = 1;
+    };
+    auto aborted = [&]() { return *reinterpret_cast<volatile int*>(&ctl.abort) != 0; };
+
+    if (warp == kTcTmaWarp) {
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&xmap) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&wmap) : "memory");
+            int issued = 0;
+            for (int i = 0; i < nkb; ++i) {
+                const int st = i % kH2Stages;
+                if (i >= kH2Stages && !mbar_wait(&ctl.empty[st], ((i / kH2Stages) - 1) & 1, kTcWait)) {
+                    give_up();
+                    break;
+                }
+                if (aborted()) break;
+                unsigned char* dst = stages + st * kH2Stage;
+                mbar_arrive_expect_tx(&ctl.full[st], (uint32_t)kH2Stage);
+                tma_load_2d(dst, &xmap, i * kTcKB, m0, &ctl.full[st]);
+                tma_load_2d(dst + kTcA, &wmap, i * kTcKB, nt * kTcN, &ctl.full[st]);
+                issued = i + 1;
+            }
+            for (int i = max(0, issued - kH2Stages); i < issued; ++i)
+                mbar_wait(&ctl.full[i % kH2Stages], (i / kH2Stages) & 1, kTcWait);
+        }
+    } else if (warp == kTcMmaWarp) {
+        if (lane == 0) {
+            for (int i = 0; i < nkb; ++i) {
+                const int st = i % kH2Stages, ch = i / kTcChunk, buf = ch & 1;
+                const bool first = i % kTcChunk == 0;
+                bool ok = true;
+                if (first && ch >= 2) ok = mbar_wait(&ctl.dempty[buf], ((ch >> 1) - 1) & 1, kTcWait);
+                if (ok) ok = mbar_wait(&ctl.full[st], (i / kH2Stages) & 1, kTcWait);
+                if (!ok) give_up();
+                if (!ok || aborted()) break;
+                tc_fence_after();
+                const uint32_t sa = smem_addr(stages + st * kH2Stage), sb = sa + kTcA;
+                const uint32_t d = tmem + (uint32_t)(buf * kTcN);
+#pragma unroll
+                for (int j = 0; j < kTcKB / 16; ++j)
+                    tc_mma(d, tc_desc_sw128(sa + 32 * j), tc_desc_sw128(sb + 32 * j), (first && j == 0) ? 0u : 1u);
+                tc_commit(&ctl.empty[st]);
+                if (i % kTcChunk == kTcChunk - 1 || i == nkb - 1) tc_commit(&ctl.dfull[buf]);
+            }
+        }
+    } else {
+        // ---------------------------------------------------------------- drains and epilogue
+        const int sub = warp & 3, half = warp >> 2;
+        const uint32_t lane_base = (uint32_t)(32 * sub) << 16;
+        int32_t iacc[kTcCols];
+#pragma unroll
+        for (int j = 0; j < kTcCols; ++j) iacc[j] = 0;
+        bool ok = true;
+        for (int ch = 0; ch < nchunks && ok; ++ch) {
+            const int buf = ch & 1;
+            const bool w = mbar_wait(&ctl.dfull[buf], (ch >> 1) & 1, kTcWait);
+            if (!w) give_up();
+            if (__any_sync(0xffffffffu, !w || aborted())) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t base = tmem + lane_base + (uint32_t)(buf * kTcN + half * kTcCols);
+#pragma unroll
+            for (int c = 0; c < kTcCols; c += 16) {
+                uint32_t r[16];
+                tc_ld16(base + (uint32_t)c, r);
+                tc_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 16; ++q) iacc[c + q] += (int32_t)__uint_as_float(r[q]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl.dempty[buf]);
+        }
+        if (ok) {
+            const int t = m0 + 32 * sub + lane;
+            const int n0 = nt * kTcN + half * kTcCols;
+            unsigned long long best = 0ull;
+            if (t < a.T) {
+                const float xs = a.xscale[t];
+                const bool vec = a.y != nullptr && (a.ldy & 3) == 0;
+#pragma unroll
+                for (int q = 0; q < kTcCols / 4; ++q) {
+                    const int n = n0 + 4 * q;
+                    if (n >= a.N) break;
+                    if (n + 4 <= a.N) {
+                        const float4 sw = *reinterpret_cast<const float4*>(a.wscale + n);
+                        const float l0 = xs * sw.x * (float)iacc[4 * q], l1 = xs * sw.y * (float)iacc[4 * q + 1];
+                        const float l2 = xs * sw.z * (float)iacc[4 * q + 2], l3 = xs * sw.w * (float)iacc[4 * q + 3];
+                        if (vec)
+                            *reinterpret_cast<float4*>(a.y + (int64_t)t * a.ldy + n) = make_float4(l0, l1, l2, l3);
+                        else if (a.y) {
+                            a.y[(int64_t)t * a.ldy + n] = l0;
+                            a.y[(int64_t)t * a.ldy + n + 1] = l1;
+                            a.y[(int64_t)t * a.ldy + n + 2] = l2;
+                            a.y[(int64_t)t * a.ldy + n + 3] = l3;
+                        }
+                        best = max(best, argmax_key(l0, (uint32_t)n));
+                        best = max(best, argmax_key(l1, (uint32_t)(n + 1)));
+                        best = max(best, argmax_key(l2, (uint32_t)(n + 2)));
+                        best = max(best, argmax_key(l3, (uint32_t)(n + 3)));
+                    } else {
+                        for (int e = 0; e < 4 && n + e < a.N; ++e) {
+                            const float le = xs * a.wscale[n + e] * (float)iacc[4 * q + e];
+                            if (a.y) a.y[(int64_t)t * a.ldy + n + e] = le;
+                            best = max(best, argmax_key(le, (uint32_t)(n + e)));
+                        }
+                    }
+                }
+                if (best) atomicMax(a.keys + t, best);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kTcMmaWarp) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * kTcN) : "memory");
+    }
+}
+
 // ---------------------------------------------------------------- host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -859,6 +1210,68 @@ int head_tc(const int8_t* packed, const float* row_scale, int V, int ksteps, QAc
     TcArgs args{reinterpret_cast<const uint8_t*>(packed), L, 0, V, x.scale, T, logits, ldl, 0, ksteps, row_scale,
                 keys, err_flag};
     return (int)launch(tc_gemm_kernel<true>, dim3(mt, ntl, 1), dim3(kTcThreads), TcShape<true>::kSmem, st, map, args);
+}
+
+// a dense f16 weight copy [N][K] as a TMA tensor map: 64 x 128 boxes, 128-byte swizzle
+static bool dense_map(CUtensorMap* map, const __half* w, int K, int N) {
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kTcKB, (cuuint32_t)kTcN};
+    const cuuint32_t estr[2] = {1, 1};
+    return encode_fn()(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(w), dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int q4_tc_dense(const __half* hi, const __half* lo, int N, int K, QAct x, const __half* x16, int T, float* y, int ldy,
+                bool accumulate, int num_sms, int* err_flag, cudaStream_t st) {
+    if (T <= 0 || N <= 0) return 0;
+    if (encode_fn() == nullptr || K % kTcKB || N % 64 || ldy % 4 || (reinterpret_cast<uintptr_t>(y) & 15) ||
+        (reinterpret_cast<uintptr_t>(x16) & 15) || (reinterpret_cast<uintptr_t>(hi) & 15) ||
+        (reinterpret_cast<uintptr_t>(lo) & 15))
+        return (int)cudaErrorInvalidValue;
+    CUtensorMap xm, hm, lm;
+    if (!act_map(&xm, x16, K, T, kT2Tiles * kTcM) || !dense_map(&hm, hi, K, N) || !dense_map(&lm, lo, K, N))
+        return (int)cudaErrorInvalidValue;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(q4_tc3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kT3Smem);
+        if (e != cudaSuccess) return (int)e;
+        attr = true;
+    }
+    const int ksteps = K / kTcKB;
+    const int mt = (T + kT2Tiles * kTcM - 1) / (kT2Tiles * kTcM), ntl = (N + kTcN - 1) / kTcN;
+    int splits = (ksteps + kT2MaxKb - 1) / kT2MaxKb;
+    while (mt * ntl * splits * 3 < num_sms * 2 && splits * 2 <= ksteps) splits *= 2;
+    const int kps = (ksteps + splits - 1) / splits;
+    splits = (ksteps + kps - 1) / kps;
+    if (splits > 1 && !accumulate) {
+        cudaError_t e = cudaMemset2DAsync(y, (size_t)ldy * sizeof(float), 0, (size_t)N * sizeof(float), T, st);
+        if (e != cudaSuccess) return (int)e;
+    }
+    Q4Layout L{0, ksteps, 1};
+    TcArgs args{nullptr, L, 0, N, x.scale, T, y, ldy, accumulate ? 1 : 0, kps, nullptr, nullptr, err_flag};
+    return (int)launch(q4_tc3_kernel, dim3(ntl, mt, splits), dim3(kTcThreads), kT3Smem, st, xm, hm, lm, args);
+}
+
+int head_tc_dense(const __half* w16, const float* row_scale, int V, int K, QAct x, const __half* x16, int T,
+                  float* logits, int ldl, unsigned long long* keys, int* err_flag, cudaStream_t st) {
+    if (T <= 0 || V <= 0) return 0;
+    if (encode_fn() == nullptr || K % kTcKB || (reinterpret_cast<uintptr_t>(x16) & 15) ||
+        (reinterpret_cast<uintptr_t>(w16) & 15))
+        return (int)cudaErrorInvalidValue;
+    CUtensorMap xm, wm;
+    if (!act_map(&xm, x16, K, T) || !dense_map(&wm, w16, K, V)) return (int)cudaErrorInvalidValue;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(head_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kH2Smem);
+        if (e != cudaSuccess) return (int)e;
+        attr = true;
+    }
+    const int mt = (T + kTcM - 1) / kTcM, ntl = (V + kTcN - 1) / kTcN;
+    Q4Layout L{0, K / kTcKB, 1};
+    TcArgs args{nullptr, L, 0, V, x.scale, T, logits, ldl, 0, K / kTcKB, row_scale, keys, err_flag};
+    return (int)launch(head_tc2_kernel, dim3(mt, ntl, 1), dim3(kTcThreads), kH2Smem, st, xm, wm, args);
 }
 
 }  // namespace dflash

@@ -79,6 +79,15 @@ int q4_tc(const uint8_t* packed, Q4Layout L, int tile0, int N, QAct x, const __h
 bool head_tc_supported(int ksteps, QAct x);
 int head_tc(const int8_t* packed, const float* row_scale, int V, int ksteps, QAct x, const __half* x16, int T,
             float* logits, int ldl, unsigned long long* keys, int* err_flag, cudaStream_t st);
+// Dense f16 weight copies for the many-row path (k_tc.cu): hi = f16(s q),
+// lo = f16(s q - hi) [N][K] from a 4-bit matrix's codes and f16 scales; the
+// 4-bit matmul and the head on those copies (every operand tile by TMA, no
+// conversion in the kernel).
+int dequant_hilo(const int8_t* codes, const uint16_t* scales, int N, int K, __half* hi, __half* lo, cudaStream_t st);
+int q4_tc_dense(const __half* hi, const __half* lo, int N, int K, QAct x, const __half* x16, int T, float* y, int ldy,
+                bool accumulate, int num_sms, int* err_flag, cudaStream_t st);
+int head_tc_dense(const __half* w16, const float* row_scale, int V, int K, QAct x, const __half* x16, int T,
+                  float* logits, int ldl, unsigned long long* keys, int* err_flag, cudaStream_t st);
 // int8 activation codes [T][ld] -> f16 [T][K] (exact), for the tcgen05 kernels' TMA.
 int codes_to_f16(const int8_t* x, int ld, int T, int K, __half* out, int num_sms, cudaStream_t st);
 

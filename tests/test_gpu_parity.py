@@ -159,6 +159,32 @@ def test_q4_matmul_matches_definition(name, rows):
         assert err <= 2e-5 * float(np.max(np.abs(ref))), (mid, err, float(np.max(np.abs(ref))))
 
 
+def test_converter_path_matches(monkeypatch):
+    """With DFLASH_DENSE=0 at model creation the many-row matmuls and the head
+    dequantise their weights in the tensor-core kernels instead of reading the
+    dense f16 copies: the matmul against the quantised definition, and a
+    batched block (matmuls and head) with identical decisions, to the same
+    bounds as the default path."""
+    monkeypatch.setenv("DFLASH_DENSE", "0")
+    dfl = _dfl()
+    p = Pair("small_q4")
+    rng = np.random.default_rng(11)
+    for mid, w in [(dfl.MAT_FC, p.w["fc"]), (dfl.mat_layer(0, "up"), p.w["layers"][0]["up"])]:
+        x = rng.integers(-127, 128, size=(300, w.shape[1]), dtype=np.int8)
+        xs = (rng.random(300).astype(np.float32) + 0.5) / 127
+        got = p.gpu.q4_matmul(mid, x, xs, w.shape[0])
+        codes, scales = p.gpu.q4_codes(mid, *w.shape)
+        ref = Q.q4_matvec_by_definition(x, xs, codes, scales.view(np.float16))
+        assert float(np.max(np.abs(got - ref))) <= 2e-5 * float(np.max(np.abs(ref)))
+    g = p.g
+    lens = [7, 0, 33, 12]
+    sc = Script(p, len(lens), 48)
+    for i, n in enumerate(lens):
+        sc.append(i, 0, W.make_taps(g, n, call_id=60 + i))
+    sc.block(list(range(len(lens))), [11, 12, 13, 14], lens, g.block)
+    sc.run(True).check(True)
+
+
 # ---------------------------------------------------------------- context append
 @pytest.mark.parametrize("name", ["tiny_f32", "small_q4", "small_q4_hd64"])
 def test_kv_append_matches_oracle(name):
