@@ -458,6 +458,13 @@ constexpr int kAttnWarps = kAttnQW * kAttnKH;
 constexpr int kAttnMaxCluster = 32 / kAttnKH < 16 ? 32 / kAttnKH : 16;  // CTAs of a cluster (non-portable above 8)
 
 
+DF_DEV void cp_async16(void* dst_smem, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst_smem)), "l"(src) : "memory");
+}
+DF_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+DF_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+DF_DEV void cp_async_wait_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
 DF_DEV void ldsm_x4(uint32_t (&r)[4], const __half* p) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -523,16 +530,16 @@ DF_DEV void rope_pairs(const float2* __restrict__ rope, int64_t row, int d4, flo
     t23 = t[1];
 }
 
-template <int HD>
+template <int HD, int ST>
 struct AttnSmem {
     static constexpr int LD = HD + 8;  // halves: 16-byte row pad, conflict-free ldmatrix
     static constexpr int PART = HD + 4;  // floats of a partial row: m, l, -, -, acc[HD]
     __half qh[kAttnQ][LD], ql[kAttnQ][LD];
-    // [key lane][key][dim]; after the key loop this area holds the partial
-    // rows [key lane][query][PART] that the cluster merges
-    __half kh[kAttnKH][kAttnK][LD], kl[kAttnKH][kAttnK][LD];
-    __half vh[kAttnKH][kAttnK][LD], vl[kAttnKH][kAttnK][LD];
-    DF_DEV float* part() { return reinterpret_cast<float*>(&kh[0][0][0]); }
+    // [stage][key lane][key][dim]; after the key loop this area holds the
+    // partial rows [key lane][query][PART] that the cluster merges
+    __half kh[ST][kAttnKH][kAttnK][LD], kl[ST][kAttnKH][kAttnK][LD];
+    __half vh[ST][kAttnKH][kAttnK][LD], vl[ST][kAttnKH][kAttnK][LD];
+    DF_DEV float* part() { return reinterpret_cast<float*>(&kh[0][0][0][0]); }
 };
 static_assert(kAttnQW <= 4, "the partial rows must fit the key/value area");
 
@@ -546,8 +553,12 @@ static_assert(kAttnQW <= 4, "the partial rows must fit the key/value area");
 // domain, running sum, unnormalised output).  At the end every query row has
 // kAttnKH x nsplit partial results in the cluster's shared memory; CTA sp merges
 // rows sp, sp + nsplit, ... and writes them to y.
-template <int HD>
-__global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const float* __restrict__ qkv, int ld,
+// ST key-step stages in shared memory: 2 (double-buffered copies, the next
+// step in flight while the current one is multiplied; one CTA an SM) or 1 (two
+// CTAs an SM at 128 registers a thread, each one's copies overlapping the
+// other's products).
+template <int HD, int ST>
+__global__ void __launch_bounds__(kAttnWarps * 32, ST == 1 ? 2 : 1) attn_cluster_kernel(const float* __restrict__ qkv, int ld,
                                                                        int block_len, const AttnSeq* __restrict__ seqs,
                                                                        int nq, int nkv, int qtiles, int nsplit,
                                                                        float scale_log2, float* __restrict__ y,
@@ -556,8 +567,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const flo
                                                                        const float2* __restrict__ rope, float eps,
                                                                        float* __restrict__ gpart) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    AttnSmem<HD>& sm = *reinterpret_cast<AttnSmem<HD>*>(smem_raw);
-    constexpr int PART = AttnSmem<HD>::PART;
+    AttnSmem<HD, ST>& sm = *reinterpret_cast<AttnSmem<HD, ST>*>(smem_raw);
+    constexpr int PART = AttnSmem<HD, ST>::PART;
     constexpr int NT = HD / 8;   // n8 tiles of the output
     constexpr int KS = HD / 16;  // k16 steps of the scores
     constexpr int kThreads = kAttnWarps * 32;
@@ -578,43 +589,70 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const flo
     const int j0 = sp * kps, j1 = min(total, j0 + kps);
     const int64_t row0 = (int64_t)s * block_len;
 
-    // Operands move as float4: the query tile and each key step are read
-    // with all of a thread's loads in flight at once, and the next step is
-    // fetched into registers while the current one is multiplied.
+    // The query tile is read as float4 (all of a thread's loads in flight at
+    // once), normed, rotated and split into (hi, lo) f16 halves.  Context keys
+    // and values arrive as stored -- their (hi, lo) f16 pairs -- and go to
+    // shared memory by 16-byte cp.async copies, with no registers held; the
+    // block's own rows (f32, normed and rotated here) are split on the way.
+    // Two CTAs share an SM (128 registers a thread), so one's loads overlap
+    // the other's products.
     constexpr int D4 = HD / 4;
     constexpr int NQ4 = kAttnQ * D4 / kThreads, NK4 = kAttnStep * D4 / kThreads;
+    constexpr int C8 = HD / 8, NC8 = kAttnStep * C8 / kThreads;  // 16-byte chunks of a key step, per thread
     static_assert(NQ4 * kThreads == kAttnQ * D4 && NK4 * kThreads == kAttnStep * D4, "tile split");
-    // context keys and values arrive as stored: the bits of their (hi, lo) f16
-    // pairs, four dimensions as (hi01, hi23, lo01, lo23) in a float4's words;
-    // the block's own rows arrive as f32 and are split on the way to shared memory
-    float4 pk[NK4], pv[NK4];
+    static_assert(NC8 * kThreads == kAttnStep * C8, "chunk split");
     const int64_t plane = (int64_t)nkv * sq.cap * HD;
-    auto load_kv = [&](int jt) {
+    // context rows of step jt: cp.async from the store (zeros past the split)
+    auto issue_ctx = [&](int jt, int st) {
 #pragma unroll
+        for (int u = 0; u < NC8; ++u) {
+            const int i = tid + u * kThreads, kr = i / C8, c = (i % C8) * 8, j = jt + kr;
+            const int hf = kr / kAttnK, k = kr % kAttnK;
+            if (j < sq.n && j < j1) {
+                const int64_t off = ((int64_t)g * sq.cap + sq.lo + j) * HD + c;
+                cp_async16(&sm.kh[st][hf][k][c], sq.kc + off);
+                cp_async16(&sm.kl[st][hf][k][c], sq.kc + plane + off);
+                cp_async16(&sm.vh[st][hf][k][c], sq.vc + off);
+                cp_async16(&sm.vl[st][hf][k][c], sq.vc + plane + off);
+            } else if (j >= j1) {
+                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(&sm.kh[st][hf][k][c]) = z;
+                *reinterpret_cast<uint4*>(&sm.kl[st][hf][k][c]) = z;
+                *reinterpret_cast<uint4*>(&sm.vh[st][hf][k][c]) = z;
+                *reinterpret_cast<uint4*>(&sm.vl[st][hf][k][c]) = z;
+            }
+        }
+        cp_async_commit();
+    };
+    // block rows of step jt (j in [n, j1)): f32 from qkv; keys normed and
+    // rotated; split into shared memory -- a float4 at a time, few registers
+    auto store_block_rows = [&](int jt, int st) {
+        const int d4 = tid % D4;
+        float4 gk = make_float4(1.f, 1.f, 1.f, 1.f);
+        if (k_norm != nullptr) gk = *reinterpret_cast<const float4*>(k_norm + 4 * d4);
+#pragma unroll 1
         for (int u = 0; u < NK4; ++u) {
             const int i = tid + u * kThreads, kr = i / D4, d = (i % D4) * 4, j = jt + kr;
+            const int hf = kr / kAttnK, k = kr % kAttnK;
+            const bool mine = j >= sq.n && j < j1;  // uniform over the 32 lanes of a row
             float4 kk = make_float4(0.f, 0.f, 0.f, 0.f), vv = kk;
-            if (j < j1) {
-                if (j < sq.n) {
-                    const int64_t off = ((int64_t)g * sq.cap + sq.lo + j) * HD + d;
-                    const uint2 kh = *reinterpret_cast<const uint2*>(sq.kc + off);
-                    const uint2 kl = *reinterpret_cast<const uint2*>(sq.kc + plane + off);
-                    const uint2 vh = *reinterpret_cast<const uint2*>(sq.vc + off);
-                    const uint2 vl = *reinterpret_cast<const uint2*>(sq.vc + plane + off);
-                    kk = make_float4(__uint_as_float(kh.x), __uint_as_float(kh.y), __uint_as_float(kl.x),
-                                     __uint_as_float(kl.y));
-                    vv = make_float4(__uint_as_float(vh.x), __uint_as_float(vh.y), __uint_as_float(vl.x),
-                                     __uint_as_float(vl.y));
-                } else {
-                    const int64_t off = (row0 + (j - sq.n)) * ld + d;
-                    kk = *reinterpret_cast<const float4*>(qkv + off + (int64_t)(nq + g) * HD);
-                    vv = *reinterpret_cast<const float4*>(qkv + off + (int64_t)(nq + nkv + g) * HD);
-                }
+            if (mine) {
+                const int64_t off = (row0 + (j - sq.n)) * ld + d;
+                kk = *reinterpret_cast<const float4*>(qkv + off + (int64_t)(nq + g) * HD);
+                vv = *reinterpret_cast<const float4*>(qkv + off + (int64_t)(nq + nkv + g) * HD);
             }
-            pk[u] = kk;
-            pv[u] = vv;
+            if (k_norm != nullptr) {
+                float4 t01, t23;
+                rope_pairs<HD>(rope, row0 + min(max(j - sq.n, 0), block_len - 1), d4, t01, t23);
+                norm_rope4<HD>(kk, mine, gk, t01, t23, d4, eps);
+            }
+            if (mine) {
+                split_store4(kk, &sm.kh[st][hf][k][d], &sm.kl[st][hf][k][d]);
+                split_store4(vv, &sm.vh[st][hf][k][d], &sm.vl[st][hf][k][d]);
+            }
         }
     };
+    if (j0 < j1) issue_ctx(j0, 0);  // in flight while the queries are prepared
     {
         float4 qv[NQ4];
 #pragma unroll
@@ -627,23 +665,15 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const flo
             }
         }
         if (q_norm != nullptr) {
-            // gains and rotation pairs in flight with the loads above and below
             const int d4 = tid % D4;
             const float4 gq = *reinterpret_cast<const float4*>(q_norm + 4 * d4);
-            float4 tq[NQ4][2];
 #pragma unroll
             for (int u = 0; u < NQ4; ++u) {
                 const int ii = qt * kAttnQ + (tid + u * kThreads) / D4;
-                rope_pairs<HD>(rope, row0 + ii % block_len, d4, tq[u][0], tq[u][1]);
+                float4 t01, t23;
+                rope_pairs<HD>(rope, row0 + ii % block_len, d4, t01, t23);
+                norm_rope4<HD>(qv[u], ii < mq, gq, t01, t23, d4, eps);
             }
-            if (j0 < j1) load_kv(j0);
-#pragma unroll
-            for (int u = 0; u < NQ4; ++u) {
-                const int ii = qt * kAttnQ + (tid + u * kThreads) / D4;
-                norm_rope4<HD>(qv[u], ii < mq, gq, tq[u][0], tq[u][1], d4, eps);
-            }
-        } else if (j0 < j1) {
-            load_kv(j0);
         }
 #pragma unroll
         for (int u = 0; u < NQ4; ++u) {
@@ -660,43 +690,21 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const flo
     // ldmatrix row addresses: A (queries x dims) and B (keys x dims) operands
     const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8, lcol = (lane >> 4) * 8;
 
-    for (int jt = j0; jt < j1; jt += kAttnStep) {
-        __syncthreads();  // the previous step's keys and values are no longer read
-        if (k_norm != nullptr && jt + kAttnStep > sq.n) {
-            // this step holds block rows (j >= n): their keys get the norm and
-            // rotation here, as they go to shared memory (uniform over the
-            // CTA; all lanes run the shuffles)
-            const int d4 = tid % D4;
-            const float4 gk = *reinterpret_cast<const float4*>(k_norm + 4 * d4);
-            float4 tk[NK4][2];
-#pragma unroll
-            for (int u = 0; u < NK4; ++u) {
-                const int j = jt + (tid + u * kThreads) / D4;
-                rope_pairs<HD>(rope, row0 + min(max(j - sq.n, 0), block_len - 1), d4, tk[u][0], tk[u][1]);
-            }
-#pragma unroll
-            for (int u = 0; u < NK4; ++u) {
-                const int j = jt + (tid + u * kThreads) / D4;
-                norm_rope4<HD>(pk[u], j < j1 && j >= sq.n, gk, tk[u][0], tk[u][1], d4, eps);
-            }
+    int it = 0;
+    for (int jt = j0; jt < j1; jt += kAttnStep, ++it) {
+        const int st = ST == 1 ? 0 : (it & 1);
+        if (it > 0) __syncthreads();  // the stage refilled below is no longer read
+        if (ST == 1) {
+            if (it > 0) issue_ctx(jt, 0);
+        } else if (jt + kAttnStep < j1) {
+            issue_ctx(jt + kAttnStep, st ^ 1);  // the next step's copies, in flight during this one
         }
-#pragma unroll
-        for (int u = 0; u < NK4; ++u) {
-            const int i = tid + u * kThreads, kr = i / D4, d = (i % D4) * 4;
-            const int hf = kr / kAttnK, k = kr % kAttnK;
-            if (jt + kr < sq.n) {
-                // stored pairs: the bits go to shared memory as they are
-                *reinterpret_cast<uint2*>(&sm.kh[hf][k][d]) = make_uint2(__float_as_uint(pk[u].x), __float_as_uint(pk[u].y));
-                *reinterpret_cast<uint2*>(&sm.kl[hf][k][d]) = make_uint2(__float_as_uint(pk[u].z), __float_as_uint(pk[u].w));
-                *reinterpret_cast<uint2*>(&sm.vh[hf][k][d]) = make_uint2(__float_as_uint(pv[u].x), __float_as_uint(pv[u].y));
-                *reinterpret_cast<uint2*>(&sm.vl[hf][k][d]) = make_uint2(__float_as_uint(pv[u].z), __float_as_uint(pv[u].w));
-            } else {
-                split_store4(pk[u], &sm.kh[hf][k][d], &sm.kl[hf][k][d]);
-                split_store4(pv[u], &sm.vh[hf][k][d], &sm.vl[hf][k][d]);
-            }
-        }
+        if (jt + kAttnStep > sq.n) store_block_rows(jt, st);
+        if (ST == 2 && jt + kAttnStep < j1)
+            cp_async_wait_one();  // this step's copies done; the next step's may still fly
+        else
+            cp_async_wait_all();
         __syncthreads();
-        if (jt + kAttnStep < j1) load_kv(jt + kAttnStep);
         const int kt = jt + half * kAttnK;  // first key of this warp's tile
         if (kt >= j1) continue;              // warp-uniform: nothing of this lane in the last step
         // scores: 16 queries x 32 keys per warp
@@ -713,8 +721,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const flo
                 uint32_t bh[4], bl[4];
                 // matrices: (keys +0..7, dims +0..7), (keys +0..7, dims +8..15), (keys +8..15, ...), ...
                 const int brow = nb * 16 + (lane & 7) + (lane >> 4) * 8, bcol = k * 16 + ((lane >> 3) & 1) * 8;
-                ldsm_x4(bh, &sm.kh[half][brow][bcol]);
-                ldsm_x4(bl, &sm.kl[half][brow][bcol]);
+                ldsm_x4(bh, &sm.kh[st][half][brow][bcol]);
+                ldsm_x4(bl, &sm.kl[st][half][brow][bcol]);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     float* c = sc[nb * 2 + h];
@@ -794,8 +802,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_cluster_kernel(const flo
                 uint32_t bh[4], bl[4];
                 // .trans matrices: (keys +0..7, dims +0..7), (keys +8..15, dims +0..7), (keys +0..7, dims +8..15), ...
                 const int vrow = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, vcol = jb * 16 + (lane >> 4) * 8;
-                ldsm_x4_t(bh, &sm.vh[half][vrow][vcol]);
-                ldsm_x4_t(bl, &sm.vl[half][vrow][vcol]);
+                ldsm_x4_t(bh, &sm.vh[st][half][vrow][vcol]);
+                ldsm_x4_t(bl, &sm.vl[st][half][vrow][vcol]);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     float* c = o[jb * 2 + h];
@@ -950,7 +958,7 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const float* __restrict
 constexpr int kAttnMinSteps = 2;  // key steps a CTA gets at least when the splits merge through global memory
 
 static void attn_plan(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int num_sms, const int* max_active,
-                      int* qtiles, int* nsplit, bool* gmerge, bool allow_gmerge = true) {
+                      int* qtiles, int* nsplit, bool* gmerge, bool allow_gmerge) {
     const int mq = (nq / nkv) * block_len;
     *qtiles = (mq + kAttnQ - 1) / kAttnQ;
     const int total = max_ctx + block_len;
@@ -965,7 +973,7 @@ static void attn_plan(int n_seqs, int block_len, int max_ctx, int nq, int nkv, i
     *gmerge = false;
     if (!allow_gmerge) return;
     if (units * best * 4 < num_sms * 3) {
-        const int gsplit = std::min(max_split, std::max(1, (num_sms + units - 1) / units));
+        const int gsplit = std::min(max_split, std::max(1, (slots + units - 1) / units));
         if (gsplit > best && total >= kAttnMinSteps * kAttnStep * gsplit) {
             *nsplit = gsplit;
             *gmerge = true;
@@ -973,16 +981,36 @@ static void attn_plan(int n_seqs, int block_len, int max_ctx, int nq, int nkv, i
     }
 }
 
-template <int HD>
+template <int HD, int ST>
 static const int* attn_cluster_table(cudaStream_t st);
 
-int64_t attn_scratch_floats(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int hd, int num_sms) {
-    const int* table = hd == 128 ? attn_cluster_table<128>(0) : attn_cluster_table<64>(0);
-    int qtiles, nsplit;
+// The whole launch plan: stages (2: one CTA an SM with double-buffered key
+// steps, for few units; 1: two CTAs an SM, when the units alone fill the
+// SMs), query tiles, key splits, and whether they merge through global memory.
+struct AttnPlan {
+    int stages, qtiles, nsplit;
     bool gmerge;
-    attn_plan(n_seqs, block_len, max_ctx, nq, nkv, num_sms, table, &qtiles, &nsplit, &gmerge);
-    if (!gmerge) return 0;
-    return (int64_t)nkv * qtiles * n_seqs * nsplit * kAttnKH * kAttnQ * (hd + 4);
+};
+template <int HD>
+static AttnPlan attn_plan_hd(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int num_sms, bool allow_gmerge) {
+    AttnPlan p;
+    const int mq = (nq / nkv) * block_len;
+    const int units = nkv * ((mq + kAttnQ - 1) / kAttnQ) * n_seqs;
+    p.stages = units >= num_sms ? 1 : 2;
+    const int* table = p.stages == 1 ? attn_cluster_table<HD, 1>(0) : attn_cluster_table<HD, 2>(0);
+    attn_plan(n_seqs, block_len, max_ctx, nq, nkv, num_sms, table, &p.qtiles, &p.nsplit, &p.gmerge, allow_gmerge);
+    return p;
+}
+static AttnPlan attn_plan_any(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int hd, int num_sms,
+                              bool allow_gmerge) {
+    return hd == 128 ? attn_plan_hd<128>(n_seqs, block_len, max_ctx, nq, nkv, num_sms, allow_gmerge)
+                     : attn_plan_hd<64>(n_seqs, block_len, max_ctx, nq, nkv, num_sms, allow_gmerge);
+}
+
+int64_t attn_scratch_floats(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int hd, int num_sms) {
+    const AttnPlan p = attn_plan_any(n_seqs, block_len, max_ctx, nq, nkv, hd, num_sms, true);
+    if (!p.gmerge) return 0;
+    return (int64_t)nkv * p.qtiles * n_seqs * p.nsplit * kAttnKH * kAttnQ * (hd + 4);
 }
 
 int attn_kernels(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int hd, int num_sms, int64_t part_floats) {
@@ -990,21 +1018,21 @@ int attn_kernels(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int hd
     return (need > 0 && part_floats >= need) ? 2 : 1;
 }
 
-// How many clusters of c = 1..16 CTAs of attn_cluster_kernel<HD> the device
-// holds at once (0 where it cannot place one), found once per process.
-template <int HD>
+// How many clusters of c = 1..16 CTAs of attn_cluster_kernel<HD, ST> the
+// device holds at once (0 where it cannot place one), found once per process.
+template <int HD, int ST>
 static const int* attn_cluster_table(cudaStream_t st) {
     static int table[kAttnMaxCluster + 1] = {0};
     static bool done = false;
     if (done) return table;
-    cudaFuncSetAttribute(attn_cluster_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)sizeof(AttnSmem<HD>));
-    cudaFuncSetAttribute(attn_cluster_kernel<HD>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    cudaFuncSetAttribute(attn_cluster_kernel<HD, ST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)sizeof(AttnSmem<HD, ST>));
+    cudaFuncSetAttribute(attn_cluster_kernel<HD, ST>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     for (int c = 1; c <= kAttnMaxCluster; ++c) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(c, 1, 1);
         cfg.blockDim = dim3(kAttnWarps * 32);
-        cfg.dynamicSmemBytes = sizeof(AttnSmem<HD>);
+        cfg.dynamicSmemBytes = sizeof(AttnSmem<HD, ST>);
         cfg.stream = st;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1014,7 +1042,7 @@ static const int* attn_cluster_table(cudaStream_t st) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, attn_cluster_kernel<HD>, &cfg) != cudaSuccess) {
+        if (cudaOccupancyMaxActiveClusters(&n, attn_cluster_kernel<HD, ST>, &cfg) != cudaSuccess) {
             cudaGetLastError();
             n = 0;
         }
@@ -1025,30 +1053,38 @@ static const int* attn_cluster_table(cudaStream_t st) {
     return table;
 }
 
+template <int HD, int ST>
+static int attention_run(const AttnPlan& p, const float* qkv, int ld, int n_seqs, int block_len,
+                         const AttnSeq* seqs_dev, int nq, int nkv, float scale_log2, float* part, float* y,
+                         cudaStream_t st, const float* q_norm, const float* k_norm, const float2* rope, float eps) {
+    dim3 grid(p.nsplit, nkv * p.qtiles, n_seqs);
+    if (p.gmerge) {
+        cudaError_t e = launch(attn_cluster_kernel<HD, ST>, grid, dim3(kAttnWarps * 32), sizeof(AttnSmem<HD, ST>), st,
+                               qkv, ld, block_len, seqs_dev, nq, nkv, p.qtiles, p.nsplit, scale_log2, y, q_norm,
+                               k_norm, rope, eps, part);
+        if (e != cudaSuccess) return (int)e;
+        return (int)launch(attn_merge_kernel<HD>, dim3(kAttnQ / 8, nkv * p.qtiles * n_seqs), dim3(256), 0, st,
+                           (const float*)part, p.nsplit, p.qtiles, nkv, nq, block_len, y);
+    }
+    return (int)launch_cluster(attn_cluster_kernel<HD, ST>, grid, dim3(kAttnWarps * 32), sizeof(AttnSmem<HD, ST>), st,
+                               p.nsplit, qkv, ld, block_len, seqs_dev, nq, nkv, p.qtiles, p.nsplit, scale_log2, y,
+                               q_norm, k_norm, rope, eps, (float*)nullptr);
+}
+
 template <int HD>
 static int attention_hd(const float* qkv, int ld, int n_seqs, int block_len, const AttnSeq* seqs_dev, int max_ctx,
                         int nq, int nkv, float scale, float* part, int64_t part_floats, float* y, int num_sms,
                         cudaStream_t st, const float* q_norm, const float* k_norm, const float2* rope, float eps) {
-    const int* table = attn_cluster_table<HD>(st);
-    int qtiles, nsplit;
-    bool gmerge;
-    attn_plan(n_seqs, block_len, max_ctx, nq, nkv, num_sms, table, &qtiles, &nsplit, &gmerge);
+    AttnPlan p = attn_plan_hd<HD>(n_seqs, block_len, max_ctx, nq, nkv, num_sms, true);
+    const int64_t need = (int64_t)nkv * p.qtiles * n_seqs * p.nsplit * kAttnKH * kAttnQ * (HD + 4);
+    if (p.gmerge && (part == nullptr || part_floats < need))  // no room for the partial rows: clusters
+        p = attn_plan_hd<HD>(n_seqs, block_len, max_ctx, nq, nkv, num_sms, false);
     const float scale_log2 = scale * 1.4426950408889634f;
-    const int64_t need = (int64_t)nkv * qtiles * n_seqs * nsplit * kAttnKH * kAttnQ * (HD + 4);
-    if (gmerge && (part == nullptr || part_floats < need))  // no room for the partial rows: clusters
-        attn_plan(n_seqs, block_len, max_ctx, nq, nkv, num_sms, table, &qtiles, &nsplit, &gmerge, false);
-    dim3 grid(nsplit, nkv * qtiles, n_seqs);
-    if (gmerge) {
-        cudaError_t e = launch(attn_cluster_kernel<HD>, grid, dim3(kAttnWarps * 32), sizeof(AttnSmem<HD>), st, qkv, ld,
-                               block_len, seqs_dev, nq, nkv, qtiles, nsplit, scale_log2, y, q_norm, k_norm, rope, eps,
-                               part);
-        if (e != cudaSuccess) return (int)e;
-        return (int)launch(attn_merge_kernel<HD>, dim3(kAttnQ / 8, nkv * qtiles * n_seqs), dim3(256), 0, st,
-                           (const float*)part, nsplit, qtiles, nkv, nq, block_len, y);
-    }
-    return (int)launch_cluster(attn_cluster_kernel<HD>, grid, dim3(kAttnWarps * 32), sizeof(AttnSmem<HD>), st, nsplit,
-                               qkv, ld, block_len, seqs_dev, nq, nkv, qtiles, nsplit, scale_log2, y, q_norm, k_norm,
-                               rope, eps, (float*)nullptr);
+    if (p.stages == 1)
+        return attention_run<HD, 1>(p, qkv, ld, n_seqs, block_len, seqs_dev, nq, nkv, scale_log2, part, y, st, q_norm,
+                                    k_norm, rope, eps);
+    return attention_run<HD, 2>(p, qkv, ld, n_seqs, block_len, seqs_dev, nq, nkv, scale_log2, part, y, st, q_norm,
+                                k_norm, rope, eps);
 }
 
 int attention(const float* qkv, int ld, int n_seqs, int block_len, const AttnSeq* seqs_dev, int max_ctx, int nq,
