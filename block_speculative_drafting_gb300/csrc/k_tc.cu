@@ -761,14 +761,29 @@ int dequant_hilo(const int8_t* codes, const uint16_t* scales, int N, int K, __ha
 }
 
 // ---------------------------------------------------------------- 4-bit, dense copies
-// q4_tc2_kernel's tiling (two 128-row tiles a CTA, K slices of at most
-// kT2MaxKb k-blocks) with the weight tiles' hi and lo planes loaded by TMA
-// from the dense copy: one TMA lane, one MMA lane, eight epilogue warps.
-constexpr int kT3Stages = 3;
-constexpr int kT3Bt = kTcN * kTcKB * 2;              // one 128 x 64 f16 weight tile (16 KB)
-constexpr int kT3Stage = kT2Tiles * kTcA + 2 * kT3Bt;  // 256-row activation box + hi + lo (64 KB)
+// q4_tc2_kernel's row tiling (two 128-row tiles a CTA, K slices of at most
+// kT2MaxKb k-blocks), 256 outputs a CTA (M 128 x N 256 MMAs), the weight
+// tiles' hi and lo planes loaded by TMA from the dense copy: one TMA lane, one
+// MMA lane, eight epilogue warps.
+// A CTA computes 256 rows x kT3N outputs: the wide N halves the activation
+// bytes a multiply-add takes from L2 (the operand feed, not the MMAs, bounded
+// the 128-output form).
+constexpr int kT3N = 256;                             // outputs of a CTA: MMA N
+constexpr int kT3Stages = 2;
+constexpr int kT3Bt = kT3N * kTcKB * 2;               // one 256 x 64 f16 weight tile (32 KB)
+constexpr int kT3Stage = kT2Tiles * kTcA + 2 * kT3Bt;  // 256-row activation box + hi + lo (96 KB)
 constexpr size_t kT3Smem = 1024 + 1024 + (size_t)kT3Stages * kT3Stage;
 static_assert(kT3Smem <= 227 * 1024, "shared memory");
+static_assert(kT2Tiles * kT3N <= 512, "tensor memory");
+constexpr uint32_t kT3Idesc = (1u << 4) | ((uint32_t)(kT3N >> 3) << 17) | ((uint32_t)(kTcM >> 4) << 24);
+
+DF_DEV void tc_mma_n256(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(kT3Idesc), "r"(accumulate)
+        : "memory");
+}
 
 struct T3Ctl {
     uint64_t full[kT3Stages], empty[kT3Stages], acc_full;
@@ -800,7 +815,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     if (warp == kTcMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&ctl.tmem)),
-                     "r"(kT2Tiles * kTcN)
+                     "r"(kT2Tiles * kT3N)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -835,8 +850,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // whole boxes: rows past T or past N read as zeros and count toward the bytes
                 mbar_arrive_expect_tx(&ctl.full[st], (uint32_t)kT3Stage);
                 tma_load_2d(dst, &xmap, kb * kTcKB, m0, &ctl.full[st]);
-                tma_load_2d(dst + kT2Tiles * kTcA, &hmap, kb * kTcKB, nt * kTcN, &ctl.full[st]);
-                tma_load_2d(dst + kT2Tiles * kTcA + kT3Bt, &lmap, kb * kTcKB, nt * kTcN, &ctl.full[st]);
+                tma_load_2d(dst + kT2Tiles * kTcA, &hmap, kb * kTcKB, nt * kT3N, &ctl.full[st]);
+                tma_load_2d(dst + kT2Tiles * kTcA + kT3Bt, &lmap, kb * kTcKB, nt * kT3N, &ctl.full[st]);
                 issued = i + 1;
             }
             for (int i = max(0, issued - kT3Stages); i < issued; ++i)
@@ -857,9 +872,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const uint64_t bh = tc_desc_sw128(sb + 32 * j), bl = tc_desc_sw128(sb + kT3Bt + 32 * j);
                     for (int t = 0; t < tiles; ++t) {
                         const uint64_t ad = tc_desc_sw128(sa + t * kTcA + 32 * j);
-                        const uint32_t d = tmem + (uint32_t)(t * kTcN);
-                        tc_mma(d, ad, bh, (i > 0 || j > 0) ? 1u : 0u);
-                        tc_mma(d, ad, bl, 1u);
+                        const uint32_t d = tmem + (uint32_t)(t * kT3N);
+                        tc_mma_n256(d, ad, bh, (i > 0 || j > 0) ? 1u : 0u);
+                        tc_mma_n256(d, ad, bl, 1u);
                     }
                 }
                 tc_commit(&ctl.empty[st]);
@@ -877,12 +892,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const bool red = a.accumulate != 0 || gridDim.z > 1;
             for (int t = 0; t < tiles; ++t) {
                 const int row = m0 + t * kTcM + 32 * sub + lane;
-                const int n0 = nt * kTcN + half * 64;
+                const int n0 = nt * kT3N + half * (kT3N / 2);
                 const float xs = row < a.T ? a.xscale[row] : 0.f;
 #pragma unroll 1
-                for (int cc = 0; cc < 64; cc += 16) {
+                for (int cc = 0; cc < kT3N / 2; cc += 16) {
                     uint32_t v[16];
-                    tc_ld16(tmem + ((uint32_t)(32 * sub) << 16) + (uint32_t)(t * kTcN + half * 64 + cc), v);
+                    tc_ld16(tmem + ((uint32_t)(32 * sub) << 16) + (uint32_t)(t * kT3N + half * (kT3N / 2) + cc), v);
                     tc_wait_ld();
                     if (row < a.T && n0 + cc < a.N) {
                         float* dst = a.y + (int64_t)row * a.ldy + n0 + cc;
@@ -904,7 +919,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     if (warp == kTcMmaWarp) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kT2Tiles * kTcN)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kT2Tiles * kT3N)
                      : "memory");
     }
 }
@@ -915,7 +930,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // tensor-memory accumulators drained by eight warps into exact int32 sums
 // (a chunk's sum is an integer below 2^24), then the logits and the argmax.
 constexpr int kH2Stages = 5;
-constexpr int kH2Stage = kTcA + kT3Bt;  // 128-row activation box + 128-row code tile (32 KB)
+constexpr int kH2Bt = kTcN * kTcKB * 2;  // one 128 x 64 f16 code tile (16 KB)
+constexpr int kH2Stage = kTcA + kH2Bt;   // 128-row activation box + 128-row code tile (32 KB)
 constexpr size_t kH2Smem = 1024 + 1024 + (size_t)kH2Stages * kH2Stage;
 static_assert(kH2Smem <= 227 * 1024, "shared memory");
 
@@ -1213,10 +1229,10 @@ int head_tc(const int8_t* packed, const float* row_scale, int V, int ksteps, QAc
 }
 
 // a dense f16 weight copy [N][K] as a TMA tensor map: 64 x 128 boxes, 128-byte swizzle
-static bool dense_map(CUtensorMap* map, const __half* w, int K, int N) {
+static bool dense_map(CUtensorMap* map, const __half* w, int K, int N, int box_rows = kTcN) {
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kTcKB, (cuuint32_t)kTcN};
+    const cuuint32_t box[2] = {(cuuint32_t)kTcKB, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return encode_fn()(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(w), dims, strides, box, estr,
                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1231,7 +1247,7 @@ int q4_tc_dense(const __half* hi, const __half* lo, int N, int K, QAct x, const 
         (reinterpret_cast<uintptr_t>(lo) & 15))
         return (int)cudaErrorInvalidValue;
     CUtensorMap xm, hm, lm;
-    if (!act_map(&xm, x16, K, T, kT2Tiles * kTcM) || !dense_map(&hm, hi, K, N) || !dense_map(&lm, lo, K, N))
+    if (!act_map(&xm, x16, K, T, kT2Tiles * kTcM) || !dense_map(&hm, hi, K, N, kT3N) || !dense_map(&lm, lo, K, N, kT3N))
         return (int)cudaErrorInvalidValue;
     static bool attr = false;
     if (!attr) {
@@ -1240,7 +1256,7 @@ int q4_tc_dense(const __half* hi, const __half* lo, int N, int K, QAct x, const 
         attr = true;
     }
     const int ksteps = K / kTcKB;
-    const int mt = (T + kT2Tiles * kTcM - 1) / (kT2Tiles * kTcM), ntl = (N + kTcN - 1) / kTcN;
+    const int mt = (T + kT2Tiles * kTcM - 1) / (kT2Tiles * kTcM), ntl = (N + kT3N - 1) / kT3N;
     int splits = (ksteps + kT2MaxKb - 1) / kT2MaxKb;
     while (mt * ntl * splits * 3 < num_sms * 2 && splits * 2 <= ksteps) splits *= 2;
     const int kps = (ksteps + splits - 1) / splits;
