@@ -84,6 +84,12 @@ struct dflash_model {
     };
     std::vector<DenseMat> dense;
     __half* head16 = nullptr;
+    int* head_norm2 = nullptr;  // squared code norm of each vocabulary row (the dense head's guard)
+    unsigned long long head_norm2_max = 0;
+    // the dense head trusts its f32 sums while |x|^2 |w|^2 <= this (2^48:
+    // every partial sum within 2^24); DFLASH_HEAD_BOUND sets it (0 recomputes
+    // every element as an integer dot product)
+    unsigned long long head_bound = 1ull << 48;
     bool dense_ready = false;
     int* err_host = nullptr;  // pinned copy, read after a synchronising call
 
@@ -351,6 +357,8 @@ int build_model(dflash_model* m, const dflash_weights* w, bool on_dev, cudaStrea
         m->use_tc = !(tv && tv[0] == '0');
         const char* dv = getenv("DFLASH_DENSE");
         m->use_dense = !(dv && dv[0] == '0');
+        const char* bv = getenv("DFLASH_HEAD_BOUND");
+        if (bv && bv[0]) m->head_bound = std::min(strtoull(bv, nullptr, 10), 1ull << 48);
     }
     CK(m, cudaMallocHost(&m->err_host, sizeof(int)));
     *m->err_host = 0;
@@ -541,15 +549,23 @@ int ensure_dense(dflash_model* m, cudaStream_t st) {
         if (!rc) rc = (int)cudaStreamSynchronize(st);  // the temporaries are reused
     }
     __half* h16 = nullptr;
+    int* hn2 = nullptr;
     if (!rc) rc = dalloc(m, &h16, (size_t)g.vocab * H);
+    if (!rc) rc = dalloc(m, &hn2, (size_t)g.vocab);
     if (!rc) rc = i8_unpack(m->head_p, g.vocab, H, H / kI8KStep, codes, st);
-    if (!rc) rc = codes_to_f16(codes, H, g.vocab, H, h16, m->num_sms, st);
+    if (!rc) rc = codes_to_f16(codes, H, g.vocab, H, h16, hn2, m->num_sms, st);
+    std::vector<int> hn2_host(g.vocab);
+    if (!rc) rc = (int)cudaMemcpyAsync(hn2_host.data(), hn2, (size_t)g.vocab * sizeof(int), cudaMemcpyDeviceToHost, st);
     if (!rc) rc = (int)cudaStreamSynchronize(st);
+    unsigned long long hn2_max = 0;
+    for (int v : hn2_host) hn2_max = std::max(hn2_max, (unsigned long long)(uint32_t)v);
     cudaFree(codes);
     cudaFree(scales);
     CK(m, (cudaError_t)rc);
     m->dense = made;
     m->head16 = h16;
+    m->head_norm2 = hn2;
+    m->head_norm2_max = hn2_max;
     m->dense_ready = true;
     return 0;
 }
@@ -578,7 +594,7 @@ int q4_mm(dflash_model* m, const uint8_t* packed, Q4Layout L, int tile0, int N, 
     } else if (m->use_tc && q4_tc_supported(L, tile0, N, K, x) && ldy % 4 == 0 &&
                (reinterpret_cast<uintptr_t>(y) & 15) == 0 && m->x16.bytes >= (size_t)T * K * sizeof(__half)) {
         __half* x16 = P<__half>(m->x16);
-        KL(m, "act_f16", 1, (double)T * K * 3, st, codes_to_f16(x.codes, x.ld, T, K, x16, m->num_sms, st));
+        KL(m, "act_f16", 1, (double)T * K * 3, st, codes_to_f16(x.codes, x.ld, T, K, x16, nullptr, m->num_sms, st));
         const __half *hi = nullptr, *lo = nullptr;
         if (dense_of(m, packed, tile0 * 16, N, K, &hi, &lo)) {
             // dense weight bytes: 4 a weight
@@ -603,12 +619,17 @@ int run_head(dflash_model* m, QAct xh, int D, float* logit_out, unsigned long lo
     if (D > 16 && m->use_tc && head_tc_supported(H / kI8KStep, xh) &&
         m->x16.bytes >= (size_t)D * H * sizeof(__half)) {
         __half* x16 = P<__half>(m->x16);
-        KL(m, "act_f16", 1, (double)D * H * 3, st, codes_to_f16(xh.codes, xh.ld, D, H, x16, m->num_sms, st));
-        if (m->dense_ready && m->head16) {
-            KL(m, "head_tc", 1, hb + (double)g.vocab * H, st,
-               head_tc_dense(m->head16, m->head_scale, g.vocab, H, xh, x16, D, logit_out, g.vocab, keys, m->err_dev,
-                             st));
+        // the rows' squared code norms sit after their f16 codes
+        int* xn2 = reinterpret_cast<int*>(x16 + (size_t)D * H);
+        if (m->dense_ready && m->head16 && m->x16.bytes >= (size_t)D * (H * sizeof(__half) + sizeof(int))) {
+            KL(m, "act_f16", 1, (double)D * H * 3 + (double)D * 4, st,
+               codes_to_f16(xh.codes, xh.ld, D, H, x16, xn2, m->num_sms, st));
+            KL(m, "head_tc", 1, hb + (double)g.vocab * H + (double)g.vocab * 4, st,
+               head_tc_dense(m->head16, m->head_norm2, m->head_scale, g.vocab, H, xh, x16, xn2, D, logit_out, g.vocab,
+                             keys, m->head_bound, m->head_norm2_max, m->err_dev, st));
         } else {
+            KL(m, "act_f16", 1, (double)D * H * 3, st,
+               codes_to_f16(xh.codes, xh.ld, D, H, x16, nullptr, m->num_sms, st));
             KL(m, "head_tc", 1, hb, st,
                head_tc(m->head_p, m->head_scale, g.vocab, H / kI8KStep, xh, x16, D, logit_out, g.vocab, keys,
                        m->err_dev, st));
@@ -1128,7 +1149,8 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
     CK(m, ensure_m(m, m->rope, (size_t)R * (hd / 2) * sizeof(float2)));
     CK(m, ensure_m(m, m->aseqs, (size_t)g.layers * n_seqs * sizeof(AttnSeq)));
     if (quant && R > 16) {
-        CK(m, ensure_m(m, m->x16, (size_t)R * maxK * sizeof(__half)));
+        // f16 codes of the widest matmul input, then the head rows' code norms
+        CK(m, ensure_m(m, m->x16, (size_t)R * (maxK * sizeof(__half) + sizeof(int))));
         rc = ensure_dense(m, st);
         if (rc) return rc;
     }

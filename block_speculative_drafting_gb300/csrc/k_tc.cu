@@ -167,6 +167,16 @@ struct TcArgs {
     const float* wscale;       // head: row scales [>= N]
     unsigned long long* keys;  // head: argmax keys [T]
     int* err;
+    // dense head: the exactness guard -- squared code norms of the rows [T]
+    // and of the vocabulary rows [N], the f16 codes of both, the row length K
+    // and the largest norm product the f32 sums are trusted under
+    const int* xn2;
+    const int* wn2;
+    const __half* xf;
+    const __half* wf;
+    int K;
+    unsigned long long bound;
+    unsigned long long wn2_max;  // the largest of wn2: rows under the bound against it skip the check
 };
 
 template <bool kHead>
@@ -700,6 +710,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) q4_tc2_kernel(const __grid_cons
         if (__all_sync(0xffffffffu, ok && !aborted()) && nkb > 0) {
             const int sub = warp & 3, half = warp >> 2;
             const bool red = a.accumulate != 0 || gridDim.z > 1;
+            const bool vec_out = a.y && a.ldy % 4 == 0 && (reinterpret_cast<uintptr_t>(a.y) & 15) == 0;
             for (int t = 0; t < tiles; ++t) {
                 const int row = m0 + t * kTcM + 32 * sub + lane;
                 const int n0 = nt * kTcN + half * 64;
@@ -760,20 +771,27 @@ int dequant_hilo(const int8_t* codes, const uint16_t* scales, int N, int K, __ha
     return (int)cudaGetLastError();
 }
 
-// ---------------------------------------------------------------- 4-bit, dense copies
+// ---------------------------------------------------------------- 4-bit and head, dense copies
 // q4_tc2_kernel's row tiling (two 128-row tiles a CTA, K slices of at most
 // kT2MaxKb k-blocks), 256 outputs a CTA (M 128 x N 256 MMAs), the weight
-// tiles' hi and lo planes loaded by TMA from the dense copy: one TMA lane, one
-// MMA lane, eight epilogue warps.
+// tiles' hi and lo planes (the head: its one plane of codes) loaded by TMA
+// from the dense copy: one TMA lane, one MMA lane, eight epilogue warps.
 // A CTA computes 256 rows x kT3N outputs: the wide N halves the activation
 // bytes a multiply-add takes from L2 (the operand feed, not the MMAs, bounded
 // the 128-output form).
 constexpr int kT3N = 256;                             // outputs of a CTA: MMA N
-constexpr int kT3Stages = 2;
 constexpr int kT3Bt = kT3N * kTcKB * 2;               // one 256 x 64 f16 weight tile (32 KB)
-constexpr int kT3Stage = kT2Tiles * kTcA + 2 * kT3Bt;  // 256-row activation box + hi + lo (96 KB)
-constexpr size_t kT3Smem = 1024 + 1024 + (size_t)kT3Stages * kT3Stage;
-static_assert(kT3Smem <= 227 * 1024, "shared memory");
+// per variant: the 4-bit matrices take a 256-row activation box and the hi
+// and lo weight tiles a stage (96 KB, two stages), the head the box and one
+// code tile (64 KB, three stages)
+template <bool kHead>
+struct T3Shape {
+    static constexpr int kStages = kHead ? 3 : 2;
+    static constexpr int kStage = kT2Tiles * kTcA + (kHead ? 1 : 2) * kT3Bt;
+    static constexpr size_t kSmem = 1024 + 1024 + (size_t)kStages * kStage;
+    static_assert(kSmem <= 227 * 1024, "shared memory");
+};
+constexpr int kT3MaxStages = 3;
 static_assert(kT2Tiles * kT3N <= 512, "tensor memory");
 constexpr uint32_t kT3Idesc = (1u << 4) | ((uint32_t)(kT3N >> 3) << 17) | ((uint32_t)(kTcM >> 4) << 24);
 
@@ -786,20 +804,46 @@ DF_DEV void tc_mma_n256(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_
 }
 
 struct T3Ctl {
-    uint64_t full[kT3Stages], empty[kT3Stages], acc_full;
+    uint64_t full[kT3MaxStages], empty[kT3MaxStages], acc_full;
     uint32_t tmem;
     int abort;
 };
 
+// The exact integer dot product of two rows of f16 codes (|code| <= 127: every
+// product is exact in f32), for the head elements the norm guard rejects.
+__device__ __noinline__ int exact_dot_f16(const __half* __restrict__ x, const __half* __restrict__ w, int K) {
+    int s = 0;
+    for (int k = 0; k < K; k += 8) {
+        const uint4 a = *reinterpret_cast<const uint4*>(x + k), b = *reinterpret_cast<const uint4*>(w + k);
+        const __half2* ah = reinterpret_cast<const __half2*>(&a);
+        const __half2* bh = reinterpret_cast<const __half2*>(&b);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 fa = __half22float2(ah[j]), fb = __half22float2(bh[j]);
+            s += (int)(fa.x * fb.x) + (int)(fa.y * fb.y);
+        }
+    }
+    return s;
+}
+
+// kHead: the head's codes (one plane) against the rows, the logits and the
+// argmax in the epilogue, the whole K in tensor memory. Its products are
+// integers, so a sum is exact in f32 while every partial sum stays within
+// 2^24 in magnitude; by Cauchy-Schwarz each is at most |x|*|w| (code norms),
+// so an element whose norm product passes the bound is recomputed as an
+// integer dot product instead. The row tiles of one output tile run together
+// (x = row tile pair) so the weight tile is read from HBM once.
+template <bool kHead>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    q4_tc3_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap hmap,
-                  const __grid_constant__ CUtensorMap lmap, TcArgs a) {
+    dense_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap hmap,
+                    const __grid_constant__ CUtensorMap lmap, TcArgs a) {
+    constexpr int kT3Stages = T3Shape<kHead>::kStages, kT3Stage = T3Shape<kHead>::kStage;
     extern __shared__ __align__(1024) unsigned char sm_raw[];
     unsigned char* sm = sm_raw + ((1024 - (smem_addr(sm_raw) & 1023)) & 1023);
     T3Ctl& ctl = *reinterpret_cast<T3Ctl*>(sm);
     unsigned char* stages = sm + 1024;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nt = blockIdx.x, m0 = blockIdx.y * (kT2Tiles * kTcM);
+    const int nt = kHead ? blockIdx.y : blockIdx.x, m0 = (kHead ? blockIdx.x : blockIdx.y) * (kT2Tiles * kTcM);
     const int tiles = min(kT2Tiles, (a.T - m0 + kTcM - 1) / kTcM);
     const int kb_lo = blockIdx.z * a.kb_per_split, kb_hi = min(a.L.ksteps, kb_lo + a.kb_per_split);
     const int nkb = kb_hi - kb_lo;
@@ -836,7 +880,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(&xmap) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(&hmap) : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"(&lmap) : "memory");
+            if (!kHead) asm volatile("prefetch.tensormap [%0];" ::"l"(&lmap) : "memory");
             int issued = 0;
             for (int i = 0; i < nkb; ++i) {
                 const int st = i % kT3Stages;
@@ -851,7 +895,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 mbar_arrive_expect_tx(&ctl.full[st], (uint32_t)kT3Stage);
                 tma_load_2d(dst, &xmap, kb * kTcKB, m0, &ctl.full[st]);
                 tma_load_2d(dst + kT2Tiles * kTcA, &hmap, kb * kTcKB, nt * kT3N, &ctl.full[st]);
-                tma_load_2d(dst + kT2Tiles * kTcA + kT3Bt, &lmap, kb * kTcKB, nt * kT3N, &ctl.full[st]);
+                if (!kHead) tma_load_2d(dst + kT2Tiles * kTcA + kT3Bt, &lmap, kb * kTcKB, nt * kT3N, &ctl.full[st]);
                 issued = i + 1;
             }
             for (int i = max(0, issued - kT3Stages); i < issued; ++i)
@@ -874,7 +918,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         const uint64_t ad = tc_desc_sw128(sa + t * kTcA + 32 * j);
                         const uint32_t d = tmem + (uint32_t)(t * kT3N);
                         tc_mma_n256(d, ad, bh, (i > 0 || j > 0) ? 1u : 0u);
-                        tc_mma_n256(d, ad, bl, 1u);
+                        if (!kHead) tc_mma_n256(d, ad, bl, 1u);
                     }
                 }
                 tc_commit(&ctl.empty[st]);
@@ -890,28 +934,61 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (__all_sync(0xffffffffu, ok && !aborted()) && nkb > 0) {
             const int sub = warp & 3, half = warp >> 2;
             const bool red = a.accumulate != 0 || gridDim.z > 1;
+            const bool vec_out = a.y && a.ldy % 4 == 0 && (reinterpret_cast<uintptr_t>(a.y) & 15) == 0;
             for (int t = 0; t < tiles; ++t) {
                 const int row = m0 + t * kTcM + 32 * sub + lane;
                 const int n0 = nt * kT3N + half * (kT3N / 2);
                 const float xs = row < a.T ? a.xscale[row] : 0.f;
+                const unsigned long long xn = kHead && row < a.T ? (uint32_t)a.xn2[row] : 0ull;
+                const bool guard = kHead && xn * a.wn2_max > a.bound;
+                unsigned long long best = 0ull;
 #pragma unroll 1
                 for (int cc = 0; cc < kT3N / 2; cc += 16) {
                     uint32_t v[16];
                     tc_ld16(tmem + ((uint32_t)(32 * sub) << 16) + (uint32_t)(t * kT3N + half * (kT3N / 2) + cc), v);
                     tc_wait_ld();
                     if (row < a.T && n0 + cc < a.N) {
-                        float* dst = a.y + (int64_t)row * a.ldy + n0 + cc;
+                        if (kHead) {
+                            // logits = xs * sw[n] * (integer row sum), as the streaming head
+                            float l[16];
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float f0 = __uint_as_float(v[4 * q]) * xs, f1 = __uint_as_float(v[4 * q + 1]) * xs,
-                                        f2 = __uint_as_float(v[4 * q + 2]) * xs, f3 = __uint_as_float(v[4 * q + 3]) * xs;
-                            if (red)
-                                red_add_v4(dst + 4 * q, f0, f1, f2, f3);
-                            else
-                                *reinterpret_cast<float4*>(dst + 4 * q) = make_float4(f0, f1, f2, f3);
+                            for (int q = 0; q < 16; ++q) {
+                                const int n = n0 + cc + q;
+                                float acc = __uint_as_float(v[q]);
+                                if (guard && n < a.N && xn * (uint32_t)a.wn2[n] > a.bound)
+                                    acc = (float)exact_dot_f16(a.xf + (int64_t)row * a.K, a.wf + (int64_t)n * a.K, a.K);
+                                l[q] = n < a.N ? xs * a.wscale[n] * acc : 0.f;
+                                if (n < a.N) best = max(best, argmax_key(l[q], (uint32_t)n));
+                            }
+                            if (a.y) {
+                                float* dst = a.y + (int64_t)row * a.ldy + n0 + cc;
+                                if (vec_out && n0 + cc + 16 <= a.N) {
+#pragma unroll
+                                    for (int q = 0; q < 4; ++q)
+                                        *reinterpret_cast<float4*>(dst + 4 * q) =
+                                            make_float4(l[4 * q], l[4 * q + 1], l[4 * q + 2], l[4 * q + 3]);
+                                } else {
+#pragma unroll
+                                    for (int q = 0; q < 16; ++q)
+                                        if (n0 + cc + q < a.N) dst[q] = l[q];
+                                }
+                            }
+                        } else {
+                            float* dst = a.y + (int64_t)row * a.ldy + n0 + cc;
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const float f0 = __uint_as_float(v[4 * q]) * xs, f1 = __uint_as_float(v[4 * q + 1]) * xs,
+                                            f2 = __uint_as_float(v[4 * q + 2]) * xs,
+                                            f3 = __uint_as_float(v[4 * q + 3]) * xs;
+                                if (red)
+                                    red_add_v4(dst + 4 * q, f0, f1, f2, f3);
+                                else
+                                    *reinterpret_cast<float4*>(dst + 4 * q) = make_float4(f0, f1, f2, f3);
+                            }
                         }
                     }
                 }
+                if (kHead && row < a.T && best) atomicMax(a.keys + row, best);
             }
         }
     }
@@ -921,183 +998,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kT2Tiles * kT3N)
                      : "memory");
-    }
-}
-
-// ---------------------------------------------------------------- head, dense copy
-// The head over many rows with its codes from the dense f16 copy by TMA: a
-// CTA's 128-row x 128-logit tile, 512-column chunks in two alternating
-// tensor-memory accumulators drained by eight warps into exact int32 sums
-// (a chunk's sum is an integer below 2^24), then the logits and the argmax.
-constexpr int kH2Stages = 5;
-constexpr int kH2Bt = kTcN * kTcKB * 2;  // one 128 x 64 f16 code tile (16 KB)
-constexpr int kH2Stage = kTcA + kH2Bt;   // 128-row activation box + 128-row code tile (32 KB)
-constexpr size_t kH2Smem = 1024 + 1024 + (size_t)kH2Stages * kH2Stage;
-static_assert(kH2Smem <= 227 * 1024, "shared memory");
-
-struct H2Ctl {
-    uint64_t full[kH2Stages], empty[kH2Stages], dfull[2], dempty[2];
-    uint32_t tmem;
-    int abort;
-};
-
-__global__ void __launch_bounds__(kTcThreads, 1)
-    head_tc2_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap, TcArgs a) {
-    extern __shared__ __align__(1024) unsigned char sm_raw[];
-    unsigned char* sm = sm_raw + ((1024 - (smem_addr(sm_raw) & 1023)) & 1023);
-    H2Ctl& ctl = *reinterpret_cast<H2Ctl*>(sm);
-    unsigned char* stages = sm + 1024;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * kTcM, nt = blockIdx.y;
-    const int nkb = a.L.ksteps;
-    const int nchunks = (nkb + kTcChunk - 1) / kTcChunk;
-
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kH2Stages; ++i) {
-            mbar_init(&ctl.full[i], 1);
-            mbar_init(&ctl.empty[i], 1);
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&ctl.dfull[i], 1);
-            mbar_init(&ctl.dempty[i], kTcCvtWarps);
-        }
-        ctl.abort = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    if (warp == kTcMmaWarp) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&ctl.tmem)),
-                     "r"(2 * kTcN)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = ctl.tmem;
-    pdl_trigger();
-    pdl_wait();
-
-    auto give_up = [&]() {
-        atomicExch(a.err, 1);
-        *reinterpret_cast<volatile int*>(&ctl.abort) = 1;
-    };
-    auto aborted = [&]() { return *reinterpret_cast<volatile int*>(&ctl.abort) != 0; };
-
-    if (warp == kTcTmaWarp) {
-        if (lane == 0) {
-            asm volatile("prefetch.tensormap [%0];" ::"l"(&xmap) : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"(&wmap) : "memory");
-            int issued = 0;
-            for (int i = 0; i < nkb; ++i) {
-                const int st = i % kH2Stages;
-                if (i >= kH2Stages && !mbar_wait(&ctl.empty[st], ((i / kH2Stages) - 1) & 1, kTcWait)) {
-                    give_up();
-                    break;
-                }
-                if (aborted()) break;
-                unsigned char* dst = stages + st * kH2Stage;
-                mbar_arrive_expect_tx(&ctl.full[st], (uint32_t)kH2Stage);
-                tma_load_2d(dst, &xmap, i * kTcKB, m0, &ctl.full[st]);
-                tma_load_2d(dst + kTcA, &wmap, i * kTcKB, nt * kTcN, &ctl.full[st]);
-                issued = i + 1;
-            }
-            for (int i = max(0, issued - kH2Stages); i < issued; ++i)
-                mbar_wait(&ctl.full[i % kH2Stages], (i / kH2Stages) & 1, kTcWait);
-        }
-    } else if (warp == kTcMmaWarp) {
-        if (lane == 0) {
-            for (int i = 0; i < nkb; ++i) {
-                const int st = i % kH2Stages, ch = i / kTcChunk, buf = ch & 1;
-                const bool first = i % kTcChunk == 0;
-                bool ok = true;
-                if (first && ch >= 2) ok = mbar_wait(&ctl.dempty[buf], ((ch >> 1) - 1) & 1, kTcWait);
-                if (ok) ok = mbar_wait(&ctl.full[st], (i / kH2Stages) & 1, kTcWait);
-                if (!ok) give_up();
-                if (!ok || aborted()) break;
-                tc_fence_after();
-                const uint32_t sa = smem_addr(stages + st * kH2Stage), sb = sa + kTcA;
-                const uint32_t d = tmem + (uint32_t)(buf * kTcN);
-#pragma unroll
-                for (int j = 0; j < kTcKB / 16; ++j)
-                    tc_mma(d, tc_desc_sw128(sa + 32 * j), tc_desc_sw128(sb + 32 * j), (first && j == 0) ? 0u : 1u);
-                tc_commit(&ctl.empty[st]);
-                if (i % kTcChunk == kTcChunk - 1 || i == nkb - 1) tc_commit(&ctl.dfull[buf]);
-            }
-        }
-    } else {
-        // ---------------------------------------------------------------- drains and epilogue
-        const int sub = warp & 3, half = warp >> 2;
-        const uint32_t lane_base = (uint32_t)(32 * sub) << 16;
-        int32_t iacc[kTcCols];
-#pragma unroll
-        for (int j = 0; j < kTcCols; ++j) iacc[j] = 0;
-        bool ok = true;
-        for (int ch = 0; ch < nchunks && ok; ++ch) {
-            const int buf = ch & 1;
-            const bool w = mbar_wait(&ctl.dfull[buf], (ch >> 1) & 1, kTcWait);
-            if (!w) give_up();
-            if (__any_sync(0xffffffffu, !w || aborted())) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t base = tmem + lane_base + (uint32_t)(buf * kTcN + half * kTcCols);
-#pragma unroll
-            for (int c = 0; c < kTcCols; c += 16) {
-                uint32_t r[16];
-                tc_ld16(base + (uint32_t)c, r);
-                tc_wait_ld();
-#pragma unroll
-                for (int q = 0; q < 16; ++q) iacc[c + q] += (int32_t)__uint_as_float(r[q]);
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl.dempty[buf]);
-        }
-        if (ok) {
-            const int t = m0 + 32 * sub + lane;
-            const int n0 = nt * kTcN + half * kTcCols;
-            unsigned long long best = 0ull;
-            if (t < a.T) {
-                const float xs = a.xscale[t];
-                const bool vec = a.y != nullptr && (a.ldy & 3) == 0;
-#pragma unroll
-                for (int q = 0; q < kTcCols / 4; ++q) {
-                    const int n = n0 + 4 * q;
-                    if (n >= a.N) break;
-                    if (n + 4 <= a.N) {
-                        const float4 sw = *reinterpret_cast<const float4*>(a.wscale + n);
-                        const float l0 = xs * sw.x * (float)iacc[4 * q], l1 = xs * sw.y * (float)iacc[4 * q + 1];
-                        const float l2 = xs * sw.z * (float)iacc[4 * q + 2], l3 = xs * sw.w * (float)iacc[4 * q + 3];
-                        if (vec)
-                            *reinterpret_cast<float4*>(a.y + (int64_t)t * a.ldy + n) = make_float4(l0, l1, l2, l3);
-                        else if (a.y) {
-                            a.y[(int64_t)t * a.ldy + n] = l0;
-                            a.y[(int64_t)t * a.ldy + n + 1] = l1;
-                            a.y[(int64_t)t * a.ldy + n + 2] = l2;
-                            a.y[(int64_t)t * a.ldy + n + 3] = l3;
-                        }
-                        best = max(best, argmax_key(l0, (uint32_t)n));
-                        best = max(best, argmax_key(l1, (uint32_t)(n + 1)));
-                        best = max(best, argmax_key(l2, (uint32_t)(n + 2)));
-                        best = max(best, argmax_key(l3, (uint32_t)(n + 3)));
-                    } else {
-                        for (int e = 0; e < 4 && n + e < a.N; ++e) {
-                            const float le = xs * a.wscale[n + e] * (float)iacc[4 * q + e];
-                            if (a.y) a.y[(int64_t)t * a.ldy + n + e] = le;
-                            best = max(best, argmax_key(le, (uint32_t)(n + e)));
-                        }
-                    }
-                }
-                if (best) atomicMax(a.keys + t, best);
-            }
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == kTcMmaWarp) {
-        tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * kTcN) : "memory");
     }
 }
 
@@ -1155,10 +1055,51 @@ __global__ void codes_to_f16_kernel(const int8_t* __restrict__ x, int ld, int T,
     }
 }
 
-int codes_to_f16(const int8_t* x, int ld, int T, int K, __half* out, int num_sms, cudaStream_t st) {
+// ... and the squared norm of each row's codes (exact in int32 for K < 2^17),
+// a block per row
+__global__ void __launch_bounds__(256) codes_to_f16_norm_kernel(const int8_t* __restrict__ x, int ld, int T, int K,
+                                                                __half* __restrict__ out, int* __restrict__ norm2) {
+    pdl_trigger();
+    pdl_wait();
+    __shared__ int part[8];
+    for (int r = blockIdx.x; r < T; r += gridDim.x) {
+        int s = 0;
+        for (int c = threadIdx.x; c < K / 16; c += blockDim.x) {
+            const uint4 v = *reinterpret_cast<const uint4*>(x + (int64_t)r * ld + c * 16);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) s = __dp4a((int)w[j], (int)w[j], s);
+            uint4 h0, h1;
+            i8x4_to_half2x2(v.x, h0.x, h0.y);
+            i8x4_to_half2x2(v.y, h0.z, h0.w);
+            i8x4_to_half2x2(v.z, h1.x, h1.y);
+            i8x4_to_half2x2(v.w, h1.z, h1.w);
+            uint4* o = reinterpret_cast<uint4*>(out + (int64_t)r * K + c * 16);
+            o[0] = h0;
+            o[1] = h1;
+        }
+#pragma unroll
+        for (int d = 16; d; d >>= 1) s += __shfl_xor_sync(0xffffffffu, s, d);
+        if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = s;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int t = 0;
+            for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += part[w];
+            norm2[r] = t;
+        }
+        __syncthreads();
+    }
+}
+
+int codes_to_f16(const int8_t* x, int ld, int T, int K, __half* out, int* norm2, int num_sms, cudaStream_t st) {
     if (T <= 0) return 0;
     if (K % 16 || ld % 16 || (reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
         return (int)cudaErrorInvalidValue;
+    if (norm2) {
+        if (K >= (1 << 17)) return (int)cudaErrorInvalidValue;
+        const int blocks = std::min(T, num_sms * 8);
+        return (int)launch(codes_to_f16_norm_kernel, dim3(blocks), dim3(256), 0, st, x, ld, T, K, out, norm2);
+    }
     const int64_t n = (int64_t)T * (K / 16);
     const int blocks = (int)std::min<int64_t>((n + 255) / 256, (int64_t)num_sms * 8);
     return (int)launch(codes_to_f16_kernel, dim3(blocks), dim3(256), 0, st, x, ld, T, K, out);
@@ -1251,7 +1192,8 @@ int q4_tc_dense(const __half* hi, const __half* lo, int N, int K, QAct x, const 
         return (int)cudaErrorInvalidValue;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(q4_tc3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kT3Smem);
+        cudaError_t e = cudaFuncSetAttribute(dense_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)T3Shape<false>::kSmem);
         if (e != cudaSuccess) return (int)e;
         attr = true;
     }
@@ -1267,27 +1209,33 @@ int q4_tc_dense(const __half* hi, const __half* lo, int N, int K, QAct x, const 
     }
     Q4Layout L{0, ksteps, 1};
     TcArgs args{nullptr, L, 0, N, x.scale, T, y, ldy, accumulate ? 1 : 0, kps, nullptr, nullptr, err_flag};
-    return (int)launch(q4_tc3_kernel, dim3(ntl, mt, splits), dim3(kTcThreads), kT3Smem, st, xm, hm, lm, args);
+    return (int)launch(dense_tc_kernel<false>, dim3(ntl, mt, splits), dim3(kTcThreads), T3Shape<false>::kSmem, st, xm,
+                       hm, lm, args);
 }
 
-int head_tc_dense(const __half* w16, const float* row_scale, int V, int K, QAct x, const __half* x16, int T,
-                  float* logits, int ldl, unsigned long long* keys, int* err_flag, cudaStream_t st) {
+int head_tc_dense(const __half* w16, const int* w_norm2, const float* row_scale, int V, int K, QAct x,
+                  const __half* x16, const int* x_norm2, int T, float* logits, int ldl, unsigned long long* keys,
+                  unsigned long long bound, unsigned long long w_norm2_max, int* err_flag, cudaStream_t st) {
     if (T <= 0 || V <= 0) return 0;
     if (encode_fn() == nullptr || K % kTcKB || (reinterpret_cast<uintptr_t>(x16) & 15) ||
-        (reinterpret_cast<uintptr_t>(w16) & 15))
+        (reinterpret_cast<uintptr_t>(w16) & 15) || !w_norm2 || !x_norm2)
         return (int)cudaErrorInvalidValue;
     CUtensorMap xm, wm;
-    if (!act_map(&xm, x16, K, T) || !dense_map(&wm, w16, K, V)) return (int)cudaErrorInvalidValue;
+    if (!act_map(&xm, x16, K, T, kT2Tiles * kTcM) || !dense_map(&wm, w16, K, V, kT3N))
+        return (int)cudaErrorInvalidValue;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(head_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kH2Smem);
+        cudaError_t e = cudaFuncSetAttribute(dense_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)T3Shape<true>::kSmem);
         if (e != cudaSuccess) return (int)e;
         attr = true;
     }
-    const int mt = (T + kTcM - 1) / kTcM, ntl = (V + kTcN - 1) / kTcN;
+    const int mt = (T + kT2Tiles * kTcM - 1) / (kT2Tiles * kTcM), ntl = (V + kT3N - 1) / kT3N;
     Q4Layout L{0, K / kTcKB, 1};
-    TcArgs args{nullptr, L, 0, V, x.scale, T, logits, ldl, 0, K / kTcKB, row_scale, keys, err_flag};
-    return (int)launch(head_tc2_kernel, dim3(mt, ntl, 1), dim3(kTcThreads), kH2Smem, st, xm, wm, args);
+    TcArgs args{nullptr, L,        0,       V,   x.scale, T,   logits, ldl, 0, K / kTcKB, row_scale,
+                keys,    err_flag, x_norm2, w_norm2, x16,     w16, K,      bound,  w_norm2_max};
+    return (int)launch(dense_tc_kernel<true>, dim3(mt, ntl, 1), dim3(kTcThreads), T3Shape<true>::kSmem, st, xm, wm, wm,
+                       args);
 }
 
 }  // namespace dflash

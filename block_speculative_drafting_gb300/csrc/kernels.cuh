@@ -86,10 +86,17 @@ int head_tc(const int8_t* packed, const float* row_scale, int V, int ksteps, QAc
 int dequant_hilo(const int8_t* codes, const uint16_t* scales, int N, int K, __half* hi, __half* lo, cudaStream_t st);
 int q4_tc_dense(const __half* hi, const __half* lo, int N, int K, QAct x, const __half* x16, int T, float* y, int ldy,
                 bool accumulate, int num_sms, int* err_flag, cudaStream_t st);
-int head_tc_dense(const __half* w16, const float* row_scale, int V, int K, QAct x, const __half* x16, int T,
-                  float* logits, int ldl, unsigned long long* keys, int* err_flag, cudaStream_t st);
-// int8 activation codes [T][ld] -> f16 [T][K] (exact), for the tcgen05 kernels' TMA.
-int codes_to_f16(const int8_t* x, int ld, int T, int K, __half* out, int num_sms, cudaStream_t st);
+// The head takes the squared code norms of its vocabulary rows (w_norm2 [V],
+// largest w_norm2_max) and of the activation rows (x_norm2 [T]): an element
+// whose norm product passes `bound` (2^48: a partial sum could leave the
+// exact f32 integers) is recomputed as an integer dot product; logits (may
+// be nullptr) and the argmax keys as head_stream.
+int head_tc_dense(const __half* w16, const int* w_norm2, const float* row_scale, int V, int K, QAct x,
+                  const __half* x16, const int* x_norm2, int T, float* logits, int ldl, unsigned long long* keys,
+                  unsigned long long bound, unsigned long long w_norm2_max, int* err_flag, cudaStream_t st);
+// int8 activation codes [T][ld] -> f16 [T][K] (exact), for the tcgen05 kernels'
+// TMA; with norm2 non-null also each row's squared code norm (K < 2^17).
+int codes_to_f16(const int8_t* x, int ld, int T, int K, __half* out, int* norm2, int num_sms, cudaStream_t st);
 
 // The streaming form for up to 16 rows: every CTA streams a contiguous slice
 // of the matrix (tile0 and N multiples of 64 rows) through a bulk-copy ring

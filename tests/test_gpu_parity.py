@@ -185,6 +185,22 @@ def test_converter_path_matches(monkeypatch):
     sc.run(True).check(True)
 
 
+def test_head_norm_guard_recompute_matches(monkeypatch):
+    """The dense head trusts its f32 tensor-memory sums only while the product
+    of the two rows' code norms keeps every partial sum within 2^24 (Cauchy-
+    Schwarz); past it an element is recomputed as an integer dot product.
+    DFLASH_HEAD_BOUND=0 sends every element down that path: a batched block
+    must still give the oracle's logits and identical decisions."""
+    monkeypatch.setenv("DFLASH_HEAD_BOUND", "0")
+    p = Pair("small_q4")
+    lens = [5, 40, 0, 21]
+    sc = Script(p, len(lens), 48)
+    for i, n in enumerate(lens):
+        sc.append(i, 0, W.make_taps(p.g, n, call_id=80 + i))
+    sc.block(list(range(len(lens))), [21, 22, 23, 24], lens, p.g.block)
+    sc.run(True).check(True)
+
+
 # ---------------------------------------------------------------- context append
 @pytest.mark.parametrize("name", ["tiny_f32", "small_q4", "small_q4_hd64"])
 def test_kv_append_matches_oracle(name):
