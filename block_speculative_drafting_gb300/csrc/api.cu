@@ -91,6 +91,9 @@ struct dflash_model {
     // every element as an integer dot product)
     unsigned long long head_bound = 1ull << 48;
     bool dense_ready = false;
+    // set while run_enqueue captures a graph of the library's own: the
+    // context stores are then final for every kernel of a block
+    bool own_capture = false;
     int* err_host = nullptr;  // pinned copy, read after a synchronising call
 
     // launch accounting and the optional per-launch event profile
@@ -812,7 +815,11 @@ int run_enqueue(dflash_model* m, const std::vector<int64_t>& key, cudaStream_t s
     if (!m->cap_stream) CK(m, cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking));
     const int64_t before = m->launches;
     CK(m, cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeThreadLocal));
+    // a graph of its own runs after all earlier work on the stream, whatever
+    // its kernels' programmatic dependencies inside it
+    m->own_capture = true;
     int rc = enqueue(m->cap_stream);
+    m->own_capture = false;
     cudaGraph_t graph = nullptr;
     cudaError_t e2 = cudaStreamEndCapture(m->cap_stream, &graph);
     const int64_t kernels = m->launches - before;
@@ -1226,7 +1233,7 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
             const AttnSeq* aseq_dev = P<AttnSeq>(m->aseqs) + (size_t)l * n_seqs;
             KL(m, "attention", attn_kernels(n_seqs, B, max_ctx, g.heads, g.kv_heads, hd, m->num_sms, part_floats), attn_bytes, st,
                attention(qkv, m->qkv_w, n_seqs, B, aseq_dev, max_ctx, g.heads, g.kv_heads, hd, scale, P<float>(m->part),
-                         part_floats, y, m->num_sms, st, Ly.q_norm, Ly.k_norm, rope, g.eps));
+                         part_floats, y, m->num_sms, st, Ly.q_norm, Ly.k_norm, rope, g.eps, m->own_capture));
             c.add(row_stage(kChainRows, y, m->qd, ident, R, m->qd, nullptr, g.eps, xq, xs, maxK), (double)R * m->qd * 5,
                   [&]() {
                       return trace_site(m, st, R, m->qd, xq, maxK, xs, [&](float* v) {
@@ -1284,7 +1291,7 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
         const AttnSeq* aseq_dev = P<AttnSeq>(m->aseqs) + (size_t)l * n_seqs;
         KL(m, "attention", attn_kernels(n_seqs, B, max_ctx, g.heads, g.kv_heads, hd, m->num_sms, part_floats), attn_bytes, st,
            attention(qkv, m->qkv_w, n_seqs, B, aseq_dev, max_ctx, g.heads, g.kv_heads, hd, scale, P<float>(m->part),
-                     part_floats, y, m->num_sms, st, Ly.q_norm, Ly.k_norm, rope, g.eps));
+                     part_floats, y, m->num_sms, st, Ly.q_norm, Ly.k_norm, rope, g.eps, m->own_capture));
         if (quant) {
             KL(m, "rms_quant", 1, (double)R * m->qd * 5, st, rms_rows(y, m->qd, ident, R, m->qd, nullptr, g.eps, nullptr, 0, xq, xs, maxK, st));
             TRACE(trace_site(m, st, R, m->qd, xq, maxK, xs, [&](float* v) {

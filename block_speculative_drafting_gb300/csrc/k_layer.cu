@@ -565,7 +565,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, ST == 1 ? 2 : 1) attn_cluster
                                                                        const float* __restrict__ q_norm,
                                                                        const float* __restrict__ k_norm,
                                                                        const float2* __restrict__ rope, float eps,
-                                                                       float* __restrict__ gpart) {
+                                                                       float* __restrict__ gpart, int kv_ready) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     AttnSmem<HD, ST>& sm = *reinterpret_cast<AttnSmem<HD, ST>*>(smem_raw);
     constexpr int PART = AttnSmem<HD, ST>::PART;
@@ -580,11 +580,14 @@ __global__ void __launch_bounds__(kAttnWarps * 32, ST == 1 ? 2 : 1) attn_cluster
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
     const int qw = warp % kAttnQW, half = warp / kAttnQW;  // query warp, key lane
     pdl_trigger();
-    pdl_wait();
+    // the views are uploaded before the launch sequence: read ahead of the wait
     const AttnSeq sq = seqs[s];
     const int rep = nq / nkv, mq = rep * block_len;
     const int total = sq.n + block_len;
-    // this sequence's keys in nsplit equal shares (the last step of a share may be partial)
+    // this sequence's keys, the block's rows first (keys 0 .. block_len - 1)
+    // then its context rows, in nsplit equal shares (the last step of a share
+    // may be partial); the softmax sees the keys as a set, so their order
+    // only moves the f32 rounding
     const int kps = (total + nsplit - 1) / nsplit;
     const int j0 = sp * kps, j1 = min(total, j0 + kps);
     const int64_t row0 = (int64_t)s * block_len;
@@ -608,8 +611,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32, ST == 1 ? 2 : 1) attn_cluster
         for (int u = 0; u < NC8; ++u) {
             const int i = tid + u * kThreads, kr = i / C8, c = (i % C8) * 8, j = jt + kr;
             const int hf = kr / kAttnK, k = kr % kAttnK;
-            if (j < sq.n && j < j1) {
-                const int64_t off = ((int64_t)g * sq.cap + sq.lo + j) * HD + c;
+            if (j >= block_len && j < j1) {
+                const int64_t off = ((int64_t)g * sq.cap + sq.lo + (j - block_len)) * HD + c;
                 cp_async16(&sm.kh[st][hf][k][c], sq.kc + off);
                 cp_async16(&sm.kl[st][hf][k][c], sq.kc + plane + off);
                 cp_async16(&sm.vh[st][hf][k][c], sq.vc + off);
@@ -624,37 +627,61 @@ __global__ void __launch_bounds__(kAttnWarps * 32, ST == 1 ? 2 : 1) attn_cluster
         }
         cp_async_commit();
     };
-    // block rows of step jt (j in [n, j1)): f32 from qkv; keys normed and
-    // rotated; split into shared memory -- a float4 at a time, few registers
+    // block rows of step jt (keys j < min(block_len, j1)): f32 from qkv; keys
+    // normed and rotated; split into shared memory.  Two float4 of a thread
+    // at a time, all their loads issued before any is used.
     auto store_block_rows = [&](int jt, int st) {
         const int d4 = tid % D4;
         float4 gk = make_float4(1.f, 1.f, 1.f, 1.f);
         if (k_norm != nullptr) gk = *reinterpret_cast<const float4*>(k_norm + 4 * d4);
+        const int lim = min(block_len, j1);
 #pragma unroll 1
-        for (int u = 0; u < NK4; ++u) {
-            const int i = tid + u * kThreads, kr = i / D4, d = (i % D4) * 4, j = jt + kr;
-            const int hf = kr / kAttnK, k = kr % kAttnK;
-            const bool mine = j >= sq.n && j < j1;  // uniform over the 32 lanes of a row
-            float4 kk = make_float4(0.f, 0.f, 0.f, 0.f), vv = kk;
-            if (mine) {
-                const int64_t off = (row0 + (j - sq.n)) * ld + d;
-                kk = *reinterpret_cast<const float4*>(qkv + off + (int64_t)(nq + g) * HD);
-                vv = *reinterpret_cast<const float4*>(qkv + off + (int64_t)(nq + nkv + g) * HD);
+        for (int u0 = 0; u0 < NK4; u0 += 2) {
+            if (jt + (u0 * kThreads) / D4 >= lim) break;  // no block row in this pair or later (CTA-uniform)
+            float4 kk[2], vv[2], t01[2], t23[2];
+            bool mine[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int i = tid + (u0 + e) * kThreads, kr = i / D4, d = (i % D4) * 4, j = jt + kr;
+                mine[e] = j < lim;  // uniform over the lanes of a row
+                kk[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+                vv[e] = kk[e];
+                if (mine[e]) {
+                    const int64_t off = (row0 + j) * ld + d;
+                    kk[e] = *reinterpret_cast<const float4*>(qkv + off + (int64_t)(nq + g) * HD);
+                    vv[e] = *reinterpret_cast<const float4*>(qkv + off + (int64_t)(nq + nkv + g) * HD);
+                }
+                if (k_norm != nullptr) rope_pairs<HD>(rope, row0 + min(j, block_len - 1), d4, t01[e], t23[e]);
             }
-            if (k_norm != nullptr) {
-                float4 t01, t23;
-                rope_pairs<HD>(rope, row0 + min(max(j - sq.n, 0), block_len - 1), d4, t01, t23);
-                norm_rope4<HD>(kk, mine, gk, t01, t23, d4, eps);
-            }
-            if (mine) {
-                split_store4(kk, &sm.kh[st][hf][k][d], &sm.kl[st][hf][k][d]);
-                split_store4(vv, &sm.vh[st][hf][k][d], &sm.vl[st][hf][k][d]);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int i = tid + (u0 + e) * kThreads, kr = i / D4, d = (i % D4) * 4;
+                const int hf = kr / kAttnK, k = kr % kAttnK;
+                if (k_norm != nullptr) norm_rope4<HD>(kk[e], mine[e], gk, t01[e], t23[e], d4, eps);
+                if (mine[e]) {
+                    split_store4(kk[e], &sm.kh[st][hf][k][d], &sm.kl[st][hf][k][d]);
+                    split_store4(vv[e], &sm.vh[st][hf][k][d], &sm.vl[st][hf][k][d]);
+                }
             }
         }
     };
-    if (j0 < j1) issue_ctx(j0, 0);  // in flight while the queries are prepared
+    // The context copies of the first steps go out before the wait when the
+    // caller vouches that no kernel of the dependency chain writes the store
+    // (kv_ready); otherwise just after it.
+    auto issue_first = [&]() {
+        if (j0 < j1) issue_ctx(j0, 0);
+        if (ST == 2 && j0 + kAttnStep < j1) issue_ctx(j0 + kAttnStep, 1);
+    };
+    if (kv_ready) issue_first();
+    pdl_wait();
+    if (!kv_ready) issue_first();
     {
-        float4 qv[NQ4];
+        // the query tile (and, one CTA an SM, its rotation pairs), then the
+        // block rows of this split's first step: their loads all in flight
+        // before the first is used
+        constexpr int NR = ST == 2 ? NQ4 : 1;  // two CTAs an SM: the pairs are loaded as used
+        float4 qv[NQ4], qt01[NR], qt23[NR];
+        const int d4 = tid % D4;
 #pragma unroll
         for (int u = 0; u < NQ4; ++u) {
             const int i = tid + u * kThreads, qr = i / D4, d = (i % D4) * 4, ii = qt * kAttnQ + qr;
@@ -663,16 +690,22 @@ __global__ void __launch_bounds__(kAttnWarps * 32, ST == 1 ? 2 : 1) attn_cluster
                 const int head = g * rep + ii / block_len, r = ii % block_len;
                 qv[u] = *reinterpret_cast<const float4*>(qkv + (row0 + r) * ld + (int64_t)head * HD + d);
             }
+            if constexpr (ST == 2)
+                if (q_norm != nullptr) rope_pairs<HD>(rope, row0 + ii % block_len, d4, qt01[u], qt23[u]);
         }
+        if (j0 < j1 && j0 < block_len) store_block_rows(j0, 0);
         if (q_norm != nullptr) {
-            const int d4 = tid % D4;
             const float4 gq = *reinterpret_cast<const float4*>(q_norm + 4 * d4);
 #pragma unroll
             for (int u = 0; u < NQ4; ++u) {
                 const int ii = qt * kAttnQ + (tid + u * kThreads) / D4;
-                float4 t01, t23;
-                rope_pairs<HD>(rope, row0 + ii % block_len, d4, t01, t23);
-                norm_rope4<HD>(qv[u], ii < mq, gq, t01, t23, d4, eps);
+                if constexpr (ST == 2) {
+                    norm_rope4<HD>(qv[u], ii < mq, gq, qt01[u], qt23[u], d4, eps);
+                } else {
+                    float4 t01, t23;
+                    rope_pairs<HD>(rope, row0 + ii % block_len, d4, t01, t23);
+                    norm_rope4<HD>(qv[u], ii < mq, gq, t01, t23, d4, eps);
+                }
             }
         }
 #pragma unroll
@@ -696,10 +729,10 @@ __global__ void __launch_bounds__(kAttnWarps * 32, ST == 1 ? 2 : 1) attn_cluster
         if (it > 0) __syncthreads();  // the stage refilled below is no longer read
         if (ST == 1) {
             if (it > 0) issue_ctx(jt, 0);
-        } else if (jt + kAttnStep < j1) {
+        } else if (it > 0 && jt + kAttnStep < j1) {
             issue_ctx(jt + kAttnStep, st ^ 1);  // the next step's copies, in flight during this one
         }
-        if (jt + kAttnStep > sq.n) store_block_rows(jt, st);
+        if (it > 0 && jt < block_len) store_block_rows(jt, st);  // the first step's went with the queries
         if (ST == 2 && jt + kAttnStep < j1)
             cp_async_wait_one();  // this step's copies done; the next step's may still fly
         else
@@ -898,50 +931,73 @@ __global__ void __launch_bounds__(kAttnWarps * 32, ST == 1 ? 2 : 1) attn_cluster
     cluster.sync();  // no CTA leaves while another may still read its partial rows
 }
 
-// The global-memory merge of the key splits (long contexts): warp w of CTA
-// (x, unit) merges query row 8 x + w of the unit's tile from its
-// kAttnKH * nsplit partial rows, as the cluster merge does.
+// The global-memory merge of the key splits (long contexts): CTA (x, unit)
+// merges query rows 2 x and 2 x + 1 of the unit's tile from their
+// kAttnKH * nsplit partial rows, as the cluster merge does; four warps share
+// a row, each taking every fourth partial row (four times the loads in flight
+// of one warp a row), and meet in shared memory.
+constexpr int kMergeWays = 4;
 template <int HD>
 __global__ void __launch_bounds__(256) attn_merge_kernel(const float* __restrict__ gpart, int nsplit, int qtiles,
                                                          int nkv, int nq, int block_len, float* __restrict__ y) {
     constexpr int PART = HD + 4, VEC = HD / 32;
+    __shared__ float red[8][HD + 4];  // per warp: its share's sum and unnormalised output
     pdl_trigger();
     pdl_wait();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int unit = blockIdx.y, qr = blockIdx.x * 8 + warp;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, way = warp % kMergeWays;
+    const int unit = blockIdx.y, qr = blockIdx.x * (8 / kMergeWays) + warp / kMergeWays;
     const int qt = unit % qtiles, g = (unit / qtiles) % nkv, s = unit / (qtiles * nkv);
     const int rep = nq / nkv, mq = rep * block_len;
     const int ii = qt * kAttnQ + qr;
-    if (qr >= kAttnQ || ii >= mq) return;
+    const bool live = qr < kAttnQ && ii < mq;  // warp-uniform
     const int nparts = kAttnKH * nsplit;
-    const float* base = gpart + (int64_t)unit * nparts * kAttnQ * PART + (int64_t)qr * PART;
-    float M = -INFINITY;
-    for (int p = lane; p < nparts; p += 32) M = fmaxf(M, base[(int64_t)p * kAttnQ * PART]);
-    M = warp_max(M);
+    const float* base = gpart + (int64_t)unit * nparts * kAttnQ * PART + (int64_t)min(qr, kAttnQ - 1) * PART;
     float L = 0.f, acc[VEC];
 #pragma unroll
     for (int j = 0; j < VEC; ++j) acc[j] = 0.f;
-    for (int p = 0; p < nparts; ++p) {
-        const float* src = base + (int64_t)p * kAttnQ * PART;
-        const float mk = src[0];
-        const float w = (mk == -INFINITY) ? 0.f : exp2f(mk - M);
-        L = fmaf(src[1], w, L);
-        if constexpr (VEC == 4) {
-            const float4 a = *reinterpret_cast<const float4*>(src + 4 + 4 * lane);
-            acc[0] = fmaf(a.x, w, acc[0]);
-            acc[1] = fmaf(a.y, w, acc[1]);
-            acc[2] = fmaf(a.z, w, acc[2]);
-            acc[3] = fmaf(a.w, w, acc[3]);
-        } else {
-            const float2 a = *reinterpret_cast<const float2*>(src + 4 + 2 * lane);
-            acc[0] = fmaf(a.x, w, acc[0]);
-            acc[1] = fmaf(a.y, w, acc[1]);
+    if (live) {
+        float M = -INFINITY;
+        for (int p = lane; p < nparts; p += 32) M = fmaxf(M, base[(int64_t)p * kAttnQ * PART]);
+        M = warp_max(M);
+#pragma unroll 4
+        for (int p = way; p < nparts; p += kMergeWays) {
+            const float* src = base + (int64_t)p * kAttnQ * PART;
+            const float2 ml = *reinterpret_cast<const float2*>(src);
+            float a[VEC];
+            if constexpr (VEC == 4) {
+                const float4 v = *reinterpret_cast<const float4*>(src + 4 + 4 * lane);
+                a[0] = v.x;
+                a[1] = v.y;
+                a[2] = v.z;
+                a[3] = v.w;
+            } else {
+                const float2 v = *reinterpret_cast<const float2*>(src + 4 + 2 * lane);
+                a[0] = v.x;
+                a[1] = v.y;
+            }
+            const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+            L = fmaf(ml.y, w, L);
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) acc[j] = fmaf(a[j], w, acc[j]);
         }
     }
+    if (lane == 0) red[warp][0] = L;
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) red[warp][4 + VEC * lane + j] = acc[j];
+    __syncthreads();
+    if (!live || way != 0) return;
+    float Lt = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMergeWays; ++w) Lt += red[warp + w][0];
     const int head = g * rep + ii / block_len, r = ii % block_len;
     float* dst = y + ((int64_t)s * block_len + r) * ((int64_t)nq * HD) + (int64_t)head * HD + VEC * lane;
 #pragma unroll
-    for (int j = 0; j < VEC; ++j) dst[j] = acc[j] / L;
+    for (int j = 0; j < VEC; ++j) {
+        float t = 0.f;
+#pragma unroll
+        for (int w = 0; w < kMergeWays; ++w) t += red[warp + w][4 + VEC * lane + j];
+        dst[j] = t / Lt;
+    }
 }
 
 // Cluster size (the key splits).  max_active[c]: clusters of c CTAs the
@@ -1056,25 +1112,27 @@ static const int* attn_cluster_table(cudaStream_t st) {
 template <int HD, int ST>
 static int attention_run(const AttnPlan& p, const float* qkv, int ld, int n_seqs, int block_len,
                          const AttnSeq* seqs_dev, int nq, int nkv, float scale_log2, float* part, float* y,
-                         cudaStream_t st, const float* q_norm, const float* k_norm, const float2* rope, float eps) {
+                         cudaStream_t st, const float* q_norm, const float* k_norm, const float2* rope, float eps,
+                         int kv_ready) {
     dim3 grid(p.nsplit, nkv * p.qtiles, n_seqs);
     if (p.gmerge) {
         cudaError_t e = launch(attn_cluster_kernel<HD, ST>, grid, dim3(kAttnWarps * 32), sizeof(AttnSmem<HD, ST>), st,
                                qkv, ld, block_len, seqs_dev, nq, nkv, p.qtiles, p.nsplit, scale_log2, y, q_norm,
-                               k_norm, rope, eps, part);
+                               k_norm, rope, eps, part, kv_ready);
         if (e != cudaSuccess) return (int)e;
-        return (int)launch(attn_merge_kernel<HD>, dim3(kAttnQ / 8, nkv * p.qtiles * n_seqs), dim3(256), 0, st,
+        return (int)launch(attn_merge_kernel<HD>, dim3(kAttnQ / (8 / kMergeWays), nkv * p.qtiles * n_seqs), dim3(256), 0, st,
                            (const float*)part, p.nsplit, p.qtiles, nkv, nq, block_len, y);
     }
     return (int)launch_cluster(attn_cluster_kernel<HD, ST>, grid, dim3(kAttnWarps * 32), sizeof(AttnSmem<HD, ST>), st,
                                p.nsplit, qkv, ld, block_len, seqs_dev, nq, nkv, p.qtiles, p.nsplit, scale_log2, y,
-                               q_norm, k_norm, rope, eps, (float*)nullptr);
+                               q_norm, k_norm, rope, eps, (float*)nullptr, kv_ready);
 }
 
 template <int HD>
 static int attention_hd(const float* qkv, int ld, int n_seqs, int block_len, const AttnSeq* seqs_dev, int max_ctx,
                         int nq, int nkv, float scale, float* part, int64_t part_floats, float* y, int num_sms,
-                        cudaStream_t st, const float* q_norm, const float* k_norm, const float2* rope, float eps) {
+                        cudaStream_t st, const float* q_norm, const float* k_norm, const float2* rope, float eps,
+                        int kv_ready) {
     AttnPlan p = attn_plan_hd<HD>(n_seqs, block_len, max_ctx, nq, nkv, num_sms, true);
     const int64_t need = (int64_t)nkv * p.qtiles * n_seqs * p.nsplit * kAttnKH * kAttnQ * (HD + 4);
     if (p.gmerge && (part == nullptr || part_floats < need))  // no room for the partial rows: clusters
@@ -1082,21 +1140,21 @@ static int attention_hd(const float* qkv, int ld, int n_seqs, int block_len, con
     const float scale_log2 = scale * 1.4426950408889634f;
     if (p.stages == 1)
         return attention_run<HD, 1>(p, qkv, ld, n_seqs, block_len, seqs_dev, nq, nkv, scale_log2, part, y, st, q_norm,
-                                    k_norm, rope, eps);
+                                    k_norm, rope, eps, kv_ready);
     return attention_run<HD, 2>(p, qkv, ld, n_seqs, block_len, seqs_dev, nq, nkv, scale_log2, part, y, st, q_norm,
-                                k_norm, rope, eps);
+                                k_norm, rope, eps, kv_ready);
 }
 
 int attention(const float* qkv, int ld, int n_seqs, int block_len, const AttnSeq* seqs_dev, int max_ctx, int nq,
               int nkv, int hd, float scale, float* part, int64_t part_floats, float* y, int num_sms, cudaStream_t st,
-              const float* q_norm, const float* k_norm, const float2* rope, float eps) {
+              const float* q_norm, const float* k_norm, const float2* rope, float eps, bool kv_ready) {
     if ((q_norm == nullptr) != (k_norm == nullptr) || (q_norm != nullptr && rope == nullptr))
         return (int)cudaErrorInvalidValue;
     if (hd == 128)
         return attention_hd<128>(qkv, ld, n_seqs, block_len, seqs_dev, max_ctx, nq, nkv, scale, part, part_floats, y,
-                                 num_sms, st, q_norm, k_norm, rope, eps);
+                                 num_sms, st, q_norm, k_norm, rope, eps, kv_ready ? 1 : 0);
     return attention_hd<64>(qkv, ld, n_seqs, block_len, seqs_dev, max_ctx, nq, nkv, scale, part, part_floats, y,
-                            num_sms, st, q_norm, k_norm, rope, eps);
+                            num_sms, st, q_norm, k_norm, rope, eps, kv_ready ? 1 : 0);
 }
 
 // ------------------------------------------------------------------ wait expiry

@@ -233,10 +233,13 @@ struct AttnSeq {
 // through global memory (nothing in it needs to start at zero).
 // max_ctx: the largest context any sequence of the call may hold (its
 // capacity); the launch depends on it, each CTA's key range on the actual n.
+// kv_ready: no kernel that may still run when this one starts (the chain of
+// programmatic dependent launches before it) writes the context stores, so
+// their copies may go out before the kernel's dependency wait.
 int attention(const float* qkv, int ld, int n_seqs, int block_len, const AttnSeq* seqs_dev, int max_ctx, int nq,
               int nkv, int hd, float scale, float* part, int64_t part_floats, float* y, int num_sms, cudaStream_t st,
               const float* q_norm = nullptr, const float* k_norm = nullptr, const float2* rope = nullptr,
-              float eps = 0.f);
+              float eps = 0.f, bool kv_ready = false);
 int64_t attn_scratch_floats(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int hd, int num_sms);
 // Kernels one attention call with part_floats of scratch launches (2 when
 // the key splits merge through global memory: the split kernel, then the
