@@ -13,6 +13,11 @@ documentation; ``rms``; ``Drafter::rotate``; ``Drafter::mlp``;
 * in the quantised format (``quant=1``), every matrix input row quantised to
   int8 before its matvec (``oracle.quant``); the draft-layer matrices, ``fc``
   and the per-layer Wk/Wv 4-bit g32; the head int8 per row;
+* the geometry's attention variants: per-layer windows (``window`` for
+  every layer, or the ``windows`` list; 0 is the whole context) with the
+  row-dependent mask of ``block`` and the drop of context rows no block row
+  of a layer can see any more (``settle_rows``), and layers whose queries
+  and keys carry no rotary position (``no_rope``);
 * continuous arithmetic in float64; the decisions that pick an integer (the
   quantised codes, the draft token's argmax) taken in float32; the RoPE angle
   rounded to float32 before its cosine and sine, as the page's ``rotate``
@@ -183,7 +188,18 @@ class OracleModel:
         self.inv_f = inv_freq(g.head_dim, g.rope_theta)
 
     def window_of(self, layer):
-        return self.g.window
+        """Positions a block row of layer `layer` sees back (0: all): the
+        per-layer list where the geometry gives one, else the one window
+        (page "cortiq-engine 0.8.71 — src/dflash.rs", `Geometry`: `window`,
+        `windows`)."""
+        g = self.g
+        ws = getattr(g, "windows", ())
+        return ws[layer] if ws else g.window
+
+    def rotary(self, layer):
+        """Whether layer `layer`'s queries and keys carry the rotary
+        position (`Geometry::no_rope` lists the layers that do not)."""
+        return layer not in getattr(self.g, "no_rope", ())
 
 
 class OracleSeq:
@@ -245,9 +261,11 @@ class OracleSeq:
         t = rms(m.fc.apply(taps), m.hidden_norm, g.eps)
         ks, vs = [], []
         positions = np.arange(pos, pos + n)
-        for L in m.layers:
+        for li, L in enumerate(m.layers):
             k = L["k"].apply(t).reshape(n, g.kv_heads, g.head_dim)
-            k = rope(rms(k, L["k_norm"], g.eps), positions, m.inv_f)
+            k = rms(k, L["k_norm"], g.eps)
+            if m.rotary(li):
+                k = rope(k, positions, m.inv_f)
             v = L["v"].apply(t).reshape(n, g.kv_heads, g.head_dim)
             ks.append(k)
             vs.append(v)
@@ -333,8 +351,11 @@ def block(model, seq, anchor_tok, anchor_pos, block_len=None, return_hidden=Fals
         q = L["q"].apply(x).reshape(rows, nh, hd)
         k = L["k"].apply(x).reshape(rows, kv, hd)
         v = L["v"].apply(x).reshape(rows, kv, hd)
-        q = rope(rms(q, L["q_norm"], g.eps), positions, m.inv_f)
-        k = rope(rms(k, L["k_norm"], g.eps), positions, m.inv_f)
+        q = rms(q, L["q_norm"], g.eps)
+        k = rms(k, L["k_norm"], g.eps)
+        if m.rotary(li):
+            q = rope(q, positions, m.inv_f)
+            k = rope(k, positions, m.inv_f)
         w = m.window_of(li)
         row_from = [max(anchor_pos + r + 1 - w, 0) for r in range(rows)] if w > 0 else None
         y = attention(q, k, v, kc, vc, g.rep, scale, row_from, lo)

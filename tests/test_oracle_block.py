@@ -117,3 +117,91 @@ def test_block_shapes_and_shorter_block(model):
         block(m, s, 5, 12, block_len=1)
     with pytest.raises(ValueError):
         block(m, s, 5, 12, block_len=m.g.block + 1)
+
+
+# ------------------------------------------------------------ attention variants
+def _one_layer(m, **kw):
+    g1 = dataclasses.replace(m.g, layers=1, **kw)
+    return g1, W.make_weights(g1)
+
+
+def test_window_row_equals_a_shorter_context(model):
+    """With one layer a draft row's logits depend on its own attention only,
+    so row r under a window w equals row r of an unwindowed block whose
+    context holds only the positions that row may see (>= anchor + r + 1 - w):
+    the row-dependent mask of page "cortiq-engine 0.8.71 — src/dflash.rs",
+    `Drafter::block`, checked against plain truncation."""
+    m, _ = model
+    w_ = 5
+    g1, wts = _one_layer(m)
+    gw = dataclasses.replace(g1, window=w_)
+    m_all, m_win = OracleModel(g1, wts), OracleModel(gw, wts)
+    n = 20
+    taps = W.make_taps(g1, n)
+    sw = OracleSeq(m_win)
+    sw.append(0, taps)
+    lw, _ = block(m_win, sw, 7, n)
+    for r in range(1, g1.block):
+        start = n + r + 1 - w_
+        s = OracleSeq(m_all)
+        if start < n:
+            s.append(start, taps[start:])
+        lr, _ = block(m_all, s, 7, n)
+        np.testing.assert_allclose(lw[r - 1], lr[r - 1], rtol=1e-12, atol=1e-13)
+
+
+def test_windows_list_equals_one_window(model):
+    """The per-layer list with every entry w is the one window w; entries
+    that cover the whole context are no window."""
+    m, _ = model
+    g = m.g
+    wts = W.make_weights(g)
+    taps = W.make_taps(g, 24)
+    outs = []
+    for kw in ({"window": 6}, {"windows": (6,) * g.layers}, {"windows": (10 ** 6,) * g.layers}, {}):
+        mm = OracleModel(dataclasses.replace(g, **kw), wts)
+        s = OracleSeq(mm)
+        s.append(0, taps)
+        outs.append(block(mm, s, 5, 24)[0])
+    np.testing.assert_array_equal(outs[0], outs[1])
+    np.testing.assert_array_equal(outs[2], outs[3])
+    assert not np.allclose(outs[0], outs[3])  # the window does cut something
+
+
+def test_drop_keeps_what_the_window_sees(model):
+    """Rows that fell out of every window are dropped as the context grows
+    (`settle_rows`); appending in small chunks drops at other moments than
+    one append does, and a block at the end reads the same rows either way."""
+    m, _ = model
+    g = dataclasses.replace(m.g, window=5)
+    mm = OracleModel(g, W.make_weights(m.g))
+    taps = W.make_taps(g, 60)
+    one, chunked = OracleSeq(mm), OracleSeq(mm)
+    one.append(0, taps)
+    for r0 in range(0, 60, 7):
+        chunked.append(r0, taps[r0:r0 + 7])
+    assert one.dropped[0] == 55 and chunked.dropped[0] != one.dropped[0]
+    assert all(one.len - d <= 2 * 5 for d in chunked.dropped)
+    # (the projections of a row differ between the passes only in the order of the sums)
+    np.testing.assert_allclose(block(mm, one, 9, 60)[0], block(mm, chunked, 9, 60)[0], rtol=1e-12, atol=1e-13)
+
+
+def test_no_rope_layers_see_the_context_as_a_set(model):
+    """Without the rotary position a layer's attention cannot tell the order
+    of its context rows: reversing the context leaves every logit (up to the
+    order of the sums); with it, reversing changes them."""
+    m, _ = model
+    g = m.g
+    wts = W.make_weights(g)
+    taps = W.make_taps(g, 16)
+    res = {}
+    for name, kw in (("plain", {}), ("no_rope", {"no_rope": tuple(range(g.layers))})):
+        mm = OracleModel(dataclasses.replace(g, **kw), wts)
+        a, b = OracleSeq(mm), OracleSeq(mm)
+        a.append(0, taps)
+        b.append(0, taps[::-1].copy())
+        res[name] = (block(mm, a, 3, 16)[0], block(mm, b, 3, 16)[0])
+    la, lb = res["no_rope"]
+    np.testing.assert_allclose(la, lb, rtol=1e-9, atol=1e-10 * np.max(np.abs(la)))
+    pa, pb = res["plain"]
+    assert np.max(np.abs(pa - pb)) > 1e-6 * np.max(np.abs(pa))

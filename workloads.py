@@ -59,6 +59,14 @@ class Geometry:
     quant: int = 0  # 0: all f32; 1: 4-bit g32 matrices, int8 head, int8 activations
     mask_token: int | None = None  # None: vocab - 1
     window: int = 0  # positions a block row sees back; 0 = all
+    windows: tuple = ()  # the same per layer where layers differ (0: all); empty: `window` for every layer
+    no_rope: tuple = ()  # layers whose queries and keys carry no rotary position
+
+    def window_of(self, layer: int) -> int:
+        return self.windows[layer] if self.windows else self.window
+
+    def rotary(self, layer: int) -> bool:
+        return layer not in self.no_rope
 
     @property
     def mask(self) -> int:
