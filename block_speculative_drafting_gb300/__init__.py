@@ -77,6 +77,20 @@ def geometry_struct(g) -> _abi.Geometry:
     s.quant = int(getattr(g, "quant", 0))
     s.eps = float(getattr(g, "eps", 1e-6))
     s.rope_theta = float(getattr(g, "rope_theta", 1e6))
+    # per-layer lists: arrays kept alive on the struct until dflash_init has copied them
+    L = int(g.layers)
+    wins = tuple(getattr(g, "windows", ()) or ())
+    if wins:
+        if len(wins) != L:
+            raise ValueError(f"windows has {len(wins)} entries for {L} layers")
+        s._windows = (C.c_int32 * L)(*[int(w) for w in wins])
+        s.windows = C.cast(s._windows, C.POINTER(C.c_int32))
+    nr = tuple(getattr(g, "no_rope", ()) or ())
+    if nr:
+        if any(not 0 <= int(l) < L for l in nr):
+            raise ValueError(f"no_rope lists a layer outside [0, {L})")
+        s._no_rope = (C.c_int32 * L)(*[1 if l in nr else 0 for l in range(L)])
+        s.no_rope = C.cast(s._no_rope, C.POINTER(C.c_int32))
     return s
 
 

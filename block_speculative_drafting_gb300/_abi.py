@@ -33,7 +33,8 @@ class Geometry(C.Structure):
     _fields_ = [("hidden", C.c_int32), ("intermediate", C.c_int32), ("layers", C.c_int32), ("heads", C.c_int32),
                 ("kv_heads", C.c_int32), ("head_dim", C.c_int32), ("vocab", C.c_int32), ("block", C.c_int32),
                 ("n_taps", C.c_int32), ("mask_token", C.c_int32), ("window", C.c_int32), ("quant", C.c_int32),
-                ("eps", C.c_float), ("rope_theta", C.c_double)]
+                ("eps", C.c_float), ("rope_theta", C.c_double), ("windows", C.POINTER(C.c_int32)),
+                ("no_rope", C.POINTER(C.c_int32))]
 
 
 _FP = C.POINTER(C.c_float)

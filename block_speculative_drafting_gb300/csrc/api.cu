@@ -72,6 +72,11 @@ struct dflash_model {
     Q4Layout L_fc{}, L_kvctx{}, L_qkv{}, L_o{}, L_gu{}, L_down{};
     int* err_dev = nullptr;   // raised by a kernel whose bounded wait expired
     unsigned* chain_bar = nullptr;  // the chain kernel's barrier counter (zero between launches)
+    // per layer: the window (positions a block row sees back, 0 = all) and
+    // whether queries and keys carry the rotary position; rot_dev: the
+    // latter on the device (kv_append)
+    std::vector<int32_t> win, norope;
+    int* rot_dev = nullptr;
     bool use_chain = false;         // run a block's (and a short append's) steps as chain programs
     bool use_tc = true;             // matmuls of more than 16 rows on the tcgen05 kernel (DFLASH_TC=0: mma.sync)
     bool use_dense = true;          // ... from dense f16 weight copies (DFLASH_DENSE=0: dequantise in the kernel)
@@ -156,6 +161,9 @@ struct dflash_seq {
     std::vector<__half*> k, v;
     __half** k_dev = nullptr;  // device arrays of the per-layer pointers
     __half** v_dev = nullptr;
+    // per layer: context rows no block row of the layer can see any more
+    // (its window), dropped for good; the layer reads from first + dropped
+    std::vector<int64_t> dropped;
 };
 
 namespace {
@@ -258,6 +266,27 @@ T* P(const DevBuf& b) {
     return static_cast<T*>(b.p);
 }
 
+// The context view of layer `l` of sequence `q` for a block anchored at
+// `anchor`: positions [lo, hi) with hi = min(anchor, first + len) and lo the
+// first held position (first + the rows the layer dropped), raised under a
+// window w > 0 to anchor + 1 - w, the first position block row 0 sees; row i
+// sees from anchor + i + 1 - w on (page "cortiq-engine 0.8.71 —
+// src/dflash.rs", `Drafter::block`).
+AttnSeq layer_view(const dflash_model* m, const dflash_seq* q, int l, int64_t anchor) {
+    const int64_t w = m->win[l];
+    const int64_t base = q->first + q->dropped[l];
+    const int64_t hi = std::max(std::min(anchor, q->first + q->len), base);
+    const int64_t lo = w > 0 ? std::min(std::max(anchor + 1 - w, base), hi) : base;
+    AttnSeq a{};
+    a.kc = q->k[l];
+    a.vc = q->v[l];
+    a.cap = q->cap;
+    a.lo = lo - q->first;
+    a.n = (int)(hi - lo);
+    a.cut = w > 0 ? (int)std::max<int64_t>(anchor + 1 - w - lo, kNoCut) : kNoCut;
+    return a;
+}
+
 std::string geometry_problem(const dflash_geometry& g) {
     char buf[256];
     if (g.layers < 1) return "layers < 1";
@@ -269,7 +298,10 @@ std::string geometry_problem(const dflash_geometry& g) {
     if (g.intermediate < 64 || g.intermediate % 64) return "intermediate must be a positive multiple of 64";
     if (g.vocab < 1) return "vocab < 1";
     if (g.mask_token < 0 || g.mask_token >= g.vocab) return "mask_token outside [0, vocab)";
-    if (g.window != 0) return "window != 0 (per-layer windows are not supported)";
+    if (g.window < 0) return "window < 0";
+    if (g.windows)
+        for (int l = 0; l < g.layers; ++l)
+            if (g.windows[l] < 0) return "windows[" + std::to_string(l) + "] < 0";
     if (!(g.eps > 0.f)) return "eps must be > 0";
     if (!(g.rope_theta > 0.0)) return "rope_theta must be > 0";
     if (g.quant != DFLASH_QUANT_F32 && g.quant != DFLASH_QUANT_Q4G32) return "unknown quant";
@@ -350,6 +382,12 @@ int build_model(dflash_model* m, const dflash_weights* w, bool on_dev, cudaStrea
     CK(m, cudaMemset(m->err_dev, 0, sizeof(int)));
     CK(m, dalloc(m, &m->chain_bar, 1));
     CK(m, cudaMemset(m->chain_bar, 0, sizeof(unsigned)));
+    {
+        std::vector<int> rot(g.layers);
+        for (int l = 0; l < g.layers; ++l) rot[l] = m->norope[l] ? 0 : 1;
+        CK(m, dalloc(m, &m->rot_dev, (size_t)g.layers));
+        CK(m, cudaMemcpy(m->rot_dev, rot.data(), rot.size() * sizeof(int), cudaMemcpyHostToDevice));
+    }
     {
         // DFLASH_CHAIN=1 runs the steps between two attentions as one persistent
         // chain kernel each (measured slower than one kernel per step on the
@@ -909,7 +947,7 @@ int append_rows(dflash_model* m, dflash_seq* s, const float* taps_dev, int64_t n
     }
     KL(m, "kv_append", 1, (double)rows * m->kvctx_w * 8, st,
        kv_append(kv, rows, g.layers, g.kv_heads, g.head_dim, m->k_norm_dev, m->inv_freq, g.eps, P<int64_t>(m->a_pos),
-                 s->k_dev, s->v_dev, s->cap, st));
+                 s->k_dev, s->v_dev, s->cap, st, m->rot_dev));
     return DFLASH_OK;
 }
 
@@ -944,6 +982,15 @@ int dflash_init(const dflash_geometry* geom, const dflash_weights* weights, int 
     dflash_model* m = new (std::nothrow) dflash_model();
     if (!m) return set_err(nullptr, DFLASH_ENOMEM, "host allocation failed");
     m->g = *geom;
+    // the per-layer lists as the model's own copies (what geometry_of returns)
+    m->win.assign(geom->layers, geom->window);
+    m->norope.assign(geom->layers, 0);
+    for (int l = 0; l < geom->layers; ++l) {
+        if (geom->windows) m->win[l] = geom->windows[l];
+        if (geom->no_rope) m->norope[l] = geom->no_rope[l] != 0;
+    }
+    m->g.windows = geom->windows ? m->win.data() : nullptr;
+    m->g.no_rope = geom->no_rope ? m->norope.data() : nullptr;
     cudaStream_t st = (cudaStream_t)stream;
     int rc = DFLASH_OK;
     cudaError_t e = cudaGetDevice(&m->device);
@@ -1002,6 +1049,7 @@ int dflash_seq_new(dflash_model* m, int64_t max_ctx_rows, dflash_seq** out) {
     const int L = m->g.layers;
     const size_t per = (size_t)m->g.kv_heads * (size_t)max_ctx_rows * m->g.head_dim;
     s->k.assign(L, nullptr);
+    s->dropped.assign(L, 0);
     s->v.assign(L, nullptr);
     cudaError_t e = cudaSuccess;
     for (int l = 0; l < L && e == cudaSuccess; ++l) {
@@ -1045,6 +1093,7 @@ int dflash_truncate(dflash_seq* s, int64_t pos) {
     if (!s) return DFLASH_EINVAL;
     int64_t keep = std::min(std::max<int64_t>(pos - s->first, 0), s->len);
     s->len = keep;
+    for (auto& d : s->dropped) d = std::min(d, keep);
     return DFLASH_OK;
 }
 
@@ -1052,6 +1101,7 @@ int dflash_reset(dflash_seq* s) {
     if (!s) return DFLASH_EINVAL;
     s->len = 0;
     s->first = 0;
+    for (auto& d : s->dropped) d = 0;
     return DFLASH_OK;
 }
 
@@ -1076,6 +1126,7 @@ int dflash_ctx_append(dflash_model* m, dflash_seq* s, int64_t pos, const float* 
                                                 std::to_string(s->cap));
     s->first = first;
     s->len = len;
+    for (auto& d : s->dropped) d = std::min(d, len);  // a restart holds nothing: 0
     if (n_rows == 0) return DFLASH_OK;
     const int64_t chunk = std::min<int64_t>(n_rows, kAppendRows);
     rc = ensure_append_scratch(m, chunk);
@@ -1097,6 +1148,13 @@ int dflash_ctx_append(dflash_model* m, dflash_seq* s, int64_t pos, const float* 
         if (!taps_on_device && r0 + chunk < n_rows) CK(m, cudaStreamSynchronize(st));  // staging reused
     }
     s->len = len + n_rows;
+    // no row of a layer sees further back than its window: once a layer holds
+    // more than twice its window, all but the last window of rows are dropped
+    // (page "cortiq-engine 0.8.71 — src/dflash.rs", `settle_rows`)
+    for (int l = 0; l < m->g.layers; ++l) {
+        const int64_t w = m->win[l], held = s->len - s->dropped[l];
+        if (w > 0 && held > 2 * w) s->dropped[l] += held - w;
+    }
     if (!taps_on_device) {
         CK(m, cudaMemcpyAsync(m->err_host, m->err_dev, sizeof(int), cudaMemcpyDeviceToHost, st));
         CK(m, cudaStreamSynchronize(st));
@@ -1127,20 +1185,17 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
     const int R = n_seqs * B, D = n_seqs * (B - 1);
     const int maxK = std::max({H, I, m->qd});
 
-    // context rows each sequence reads: [first, min(anchor, first + len))
-    std::vector<AttnSeq> as(n_seqs);
     std::vector<int64_t> p0(anchor_pos, anchor_pos + n_seqs);
     int max_ctx = 0;  // the launch is planned for the largest capacity, so that it stays as contexts grow
-    for (int s = 0; s < n_seqs; ++s) {
-        const dflash_seq* q = seqs[s];
-        const int64_t hi = std::max(std::min(anchor_pos[s], q->first + q->len), q->first);
-        as[s].cap = q->cap;
-        as[s].lo = 0;
-        as[s].n = (int)(hi - q->first);
-        max_ctx = (int)std::max<int64_t>(max_ctx, q->cap);
-    }
-    double attn_bytes = (double)R * m->qkv_w * 4 + (double)R * m->qd * 4;
-    for (int s = 0; s < n_seqs; ++s) attn_bytes += (double)as[s].n * m->kd * 8;
+    for (int s = 0; s < n_seqs; ++s) max_ctx = (int)std::max<int64_t>(max_ctx, seqs[s]->cap);
+    // every layer's context views: [layer][sequence], and each layer's attention bytes
+    std::vector<AttnSeq> as_all((size_t)g.layers * n_seqs);
+    std::vector<double> attn_bytes_l(g.layers, (double)R * m->qkv_w * 4 + (double)R * m->qd * 4);
+    for (int l = 0; l < g.layers; ++l)
+        for (int s = 0; s < n_seqs; ++s) {
+            as_all[(size_t)l * n_seqs + s] = layer_view(m, seqs[s], l, anchor_pos[s]);
+            attn_bytes_l[l] += (double)as_all[(size_t)l * n_seqs + s].n * m->kd * 8;
+        }
     const int64_t part_floats = attn_scratch_floats(n_seqs, B, max_ctx, g.heads, g.kv_heads, hd, m->num_sms);
     CK(m, ensure_m(m, m->h, (size_t)R * H * sizeof(float)));
     CK(m, ensure_m(m, m->xq, (size_t)R * (quant ? maxK : maxK * sizeof(float))));
@@ -1177,15 +1232,7 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
         anchors_dev = P<uint32_t>(m->anchors);
     }
     CK(m, cudaMemcpyAsync(m->pos0.p, p0.data(), n_seqs * sizeof(int64_t), cudaMemcpyHostToDevice, st));
-    // every layer's context views in one upload: [layer][sequence]
-    std::vector<AttnSeq> as_all((size_t)g.layers * n_seqs);
-    for (int l = 0; l < g.layers; ++l)
-        for (int s = 0; s < n_seqs; ++s) {
-            AttnSeq a = as[s];
-            a.kc = seqs[s]->k[l];
-            a.vc = seqs[s]->v[l];
-            as_all[(size_t)l * n_seqs + s] = a;
-        }
+    // every layer's context views in one upload
     CK(m, cudaMemcpyAsync(m->aseqs.p, as_all.data(), as_all.size() * sizeof(AttnSeq), cudaMemcpyHostToDevice, st));
 
     auto enqueue = [&](cudaStream_t st) -> int {
@@ -1231,9 +1278,10 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
         for (int l = 0; l < g.layers; ++l) {
             const Layer& Ly = m->layers[l];
             const AttnSeq* aseq_dev = P<AttnSeq>(m->aseqs) + (size_t)l * n_seqs;
-            KL(m, "attention", attn_kernels(n_seqs, B, max_ctx, g.heads, g.kv_heads, hd, m->num_sms, part_floats), attn_bytes, st,
+            KL(m, "attention", attn_kernels(n_seqs, B, max_ctx, g.heads, g.kv_heads, hd, m->num_sms, part_floats), attn_bytes_l[l], st,
                attention(qkv, m->qkv_w, n_seqs, B, aseq_dev, max_ctx, g.heads, g.kv_heads, hd, scale, P<float>(m->part),
-                         part_floats, y, m->num_sms, st, Ly.q_norm, Ly.k_norm, rope, g.eps, m->own_capture));
+                         part_floats, y, m->num_sms, st, Ly.q_norm, Ly.k_norm, m->norope[l] ? nullptr : rope, g.eps,
+                         m->own_capture));
             c.add(row_stage(kChainRows, y, m->qd, ident, R, m->qd, nullptr, g.eps, xq, xs, maxK), (double)R * m->qd * 5,
                   [&]() {
                       return trace_site(m, st, R, m->qd, xq, maxK, xs, [&](float* v) {
@@ -1289,9 +1337,10 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
         }
         // q/k norms and rotation run inside the attention, as it loads them
         const AttnSeq* aseq_dev = P<AttnSeq>(m->aseqs) + (size_t)l * n_seqs;
-        KL(m, "attention", attn_kernels(n_seqs, B, max_ctx, g.heads, g.kv_heads, hd, m->num_sms, part_floats), attn_bytes, st,
+        KL(m, "attention", attn_kernels(n_seqs, B, max_ctx, g.heads, g.kv_heads, hd, m->num_sms, part_floats), attn_bytes_l[l], st,
            attention(qkv, m->qkv_w, n_seqs, B, aseq_dev, max_ctx, g.heads, g.kv_heads, hd, scale, P<float>(m->part),
-                     part_floats, y, m->num_sms, st, Ly.q_norm, Ly.k_norm, rope, g.eps, m->own_capture));
+                     part_floats, y, m->num_sms, st, Ly.q_norm, Ly.k_norm, m->norope[l] ? nullptr : rope, g.eps,
+                         m->own_capture));
         if (quant) {
             KL(m, "rms_quant", 1, (double)R * m->qd * 5, st, rms_rows(y, m->qd, ident, R, m->qd, nullptr, g.eps, nullptr, 0, xq, xs, maxK, st));
             TRACE(trace_site(m, st, R, m->qd, xq, maxK, xs, [&](float* v) {
@@ -1379,12 +1428,7 @@ int attention_views(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, in
         const dflash_seq* q = seqs[s];
         if (!q || q->m != m) return set_err(m, DFLASH_EINVAL, "attention: a sequence is NULL or of another model");
         if (anchor_pos[s] < 0) return set_err(m, DFLASH_EINVAL, "attention: anchor_pos < 0");
-        const int64_t hi = std::max(std::min(anchor_pos[s], q->first + q->len), q->first);
-        views[s].kc = q->k[layer];
-        views[s].vc = q->v[layer];
-        views[s].cap = q->cap;
-        views[s].lo = 0;
-        views[s].n = (int)(hi - q->first);
+        views[s] = layer_view(m, q, layer, anchor_pos[s]);
         *max_ctx = std::max(*max_ctx, views[s].n);
     }
     return DFLASH_OK;

@@ -262,7 +262,7 @@ template <int E>
 __global__ void kv_append_kernel(const float* __restrict__ kv, int n, int L, int nkv,
                                  const float* const* __restrict__ k_norm, const float* __restrict__ inv_freq,
                                  float eps, const int64_t* __restrict__ pos, __half* const* __restrict__ kstore,
-                                 __half* const* __restrict__ vstore, int64_t cap) {
+                                 __half* const* __restrict__ vstore, int64_t cap, const int* __restrict__ rotary) {
     constexpr int HD = 32 * E;
     const int64_t wid = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
     pdl_trigger();
@@ -279,7 +279,7 @@ __global__ void kv_append_kernel(const float* __restrict__ kv, int n, int L, int
         kvv[j] = src[g * HD + lane + 32 * j];
         vv[j] = src[(nkv + g) * HD + lane + 32 * j];
     }
-    norm_rope_head<E>(kvv, k_norm[l], inv_freq, eps, pos0 + r, true);
+    norm_rope_head<E>(kvv, k_norm[l], inv_freq, eps, pos0 + r, rotary == nullptr || rotary[l] != 0);
     // the store keeps each value as its (hi, lo) f16 pair: plane hi then plane lo
     const int64_t plane = (int64_t)nkv * cap * HD;
     __half* kd = kstore[l] + ((int64_t)g * cap + idx0 + r) * HD;
@@ -298,15 +298,15 @@ __global__ void kv_append_kernel(const float* __restrict__ kv, int n, int L, int
 
 int kv_append(const float* kv, int n, int L, int nkv, int hd, const float* const* k_norm_dev, const float* inv_freq,
               float eps, const int64_t* pos_dev, __half* const* kstore_dev, __half* const* vstore_dev, int64_t cap,
-              cudaStream_t st) {
+              cudaStream_t st, const int* rotary_dev) {
     if (n <= 0) return 0;
     const int64_t warps = (int64_t)n * L * nkv;
     const unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
     if (hd == 128)
         return (int)launch(kv_append_kernel<4>, dim3(blocks), dim3(256), 0, st, kv, n, L, nkv, k_norm_dev, inv_freq,
-                           eps, pos_dev, kstore_dev, vstore_dev, cap);
+                           eps, pos_dev, kstore_dev, vstore_dev, cap, rotary_dev);
     return (int)launch(kv_append_kernel<2>, dim3(blocks), dim3(256), 0, st, kv, n, L, nkv, k_norm_dev, inv_freq, eps,
-                       pos_dev, kstore_dev, vstore_dev, cap);
+                       pos_dev, kstore_dev, vstore_dev, cap, rotary_dev);
 }
 
 
@@ -496,15 +496,20 @@ DF_DEV void split_store4(float4 v, __half* hi, __half* lo) {
 // i +- HD/2 sit at lane d4 ^ HD/8).  Every lane runs the shuffles; the result
 // replaces v where `apply`.  g: the gains of the lane's dims; t01 / t23: the
 // (cos, sin) pairs of its frequencies i0 .. i0 + 3, i0 = 4 d4 mod HD/2
-// (loaded by the caller, ahead of time).
+// (loaded by the caller, ahead of time).  rot false (a layer without the
+// rotary position; the same for every thread): the norm alone.
 template <int HD>
-DF_DEV void norm_rope4(float4& v, bool apply, float4 g, float4 t01, float4 t23, int d4, float eps) {
+DF_DEV void norm_rope4(float4& v, bool apply, float4 g, float4 t01, float4 t23, int d4, float eps, bool rot = true) {
     constexpr int D4 = HD / 4;
     float ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, v.w * v.w)));
 #pragma unroll
     for (int o = D4 / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     const float s = 1.0f / sqrtf(ss / (float)HD + eps);
     const float4 n = make_float4(v.x * s * g.x, v.y * s * g.y, v.z * s * g.z, v.w * s * g.w);
+    if (!rot) {
+        if (apply) v = n;
+        return;
+    }
     float4 pn;  // the partner lane's normed dims
     pn.x = __shfl_xor_sync(0xffffffffu, n.x, D4 / 2);
     pn.y = __shfl_xor_sync(0xffffffffu, n.y, D4 / 2);
@@ -651,13 +656,15 @@ __global__ void __launch_bounds__(kAttnWarps * 32, ST == 1 ? 2 : 1) attn_cluster
                     kk[e] = *reinterpret_cast<const float4*>(qkv + off + (int64_t)(nq + g) * HD);
                     vv[e] = *reinterpret_cast<const float4*>(qkv + off + (int64_t)(nq + nkv + g) * HD);
                 }
-                if (k_norm != nullptr) rope_pairs<HD>(rope, row0 + min(j, block_len - 1), d4, t01[e], t23[e]);
+                t01[e] = t23[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (k_norm != nullptr && rope != nullptr)
+                    rope_pairs<HD>(rope, row0 + min(j, block_len - 1), d4, t01[e], t23[e]);
             }
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int i = tid + (u0 + e) * kThreads, kr = i / D4, d = (i % D4) * 4;
                 const int hf = kr / kAttnK, k = kr % kAttnK;
-                if (k_norm != nullptr) norm_rope4<HD>(kk[e], mine[e], gk, t01[e], t23[e], d4, eps);
+                if (k_norm != nullptr) norm_rope4<HD>(kk[e], mine[e], gk, t01[e], t23[e], d4, eps, rope != nullptr);
                 if (mine[e]) {
                     split_store4(kk[e], &sm.kh[st][hf][k][d], &sm.kl[st][hf][k][d]);
                     split_store4(vv[e], &sm.vh[st][hf][k][d], &sm.vl[st][hf][k][d]);
@@ -691,7 +698,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, ST == 1 ? 2 : 1) attn_cluster
                 qv[u] = *reinterpret_cast<const float4*>(qkv + (row0 + r) * ld + (int64_t)head * HD + d);
             }
             if constexpr (ST == 2)
-                if (q_norm != nullptr) rope_pairs<HD>(rope, row0 + ii % block_len, d4, qt01[u], qt23[u]);
+                if (q_norm != nullptr && rope != nullptr) rope_pairs<HD>(rope, row0 + ii % block_len, d4, qt01[u], qt23[u]);
         }
         if (j0 < j1 && j0 < block_len) store_block_rows(j0, 0);
         if (q_norm != nullptr) {
@@ -700,11 +707,11 @@ __global__ void __launch_bounds__(kAttnWarps * 32, ST == 1 ? 2 : 1) attn_cluster
             for (int u = 0; u < NQ4; ++u) {
                 const int ii = qt * kAttnQ + (tid + u * kThreads) / D4;
                 if constexpr (ST == 2) {
-                    norm_rope4<HD>(qv[u], ii < mq, gq, qt01[u], qt23[u], d4, eps);
+                    norm_rope4<HD>(qv[u], ii < mq, gq, qt01[u], qt23[u], d4, eps, rope != nullptr);
                 } else {
-                    float4 t01, t23;
-                    rope_pairs<HD>(rope, row0 + ii % block_len, d4, t01, t23);
-                    norm_rope4<HD>(qv[u], ii < mq, gq, t01, t23, d4, eps);
+                    float4 t01 = make_float4(0.f, 0.f, 0.f, 0.f), t23 = t01;
+                    if (rope != nullptr) rope_pairs<HD>(rope, row0 + ii % block_len, d4, t01, t23);
+                    norm_rope4<HD>(qv[u], ii < mq, gq, t01, t23, d4, eps, rope != nullptr);
                 }
             }
         }
@@ -720,6 +727,11 @@ __global__ void __launch_bounds__(kAttnWarps * 32, ST == 1 ? 2 : 1) attn_cluster
     for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     const int qbase = qw * 16;
+    // the leading context rows each of this lane's two query rows does not
+    // see (block row i of a windowed layer: sq.cut + i)
+    int cutr[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) cutr[h] = sq.cut + (qt * kAttnQ + qbase + gq + 8 * h) % block_len;
     // ldmatrix row addresses: A (queries x dims) and B (keys x dims) operands
     const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8, lcol = (lane >> 4) * 8;
 
@@ -777,7 +789,9 @@ __global__ void __launch_bounds__(kAttnWarps * 32, ST == 1 ? 2 : 1) attn_cluster
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int key = kt + n * 8 + 2 * tq + (e & 1);
-                const float v = key < j1 ? sc[n][e] * scale_log2 : -INFINITY;
+                // past the split, or a context row before the query row's window
+                const bool seen = key < j1 && (key < block_len || key - block_len >= cutr[e >> 1]);
+                const float v = seen ? sc[n][e] * scale_log2 : -INFINITY;
                 sc[n][e] = v;
                 tmax[e >> 1] = fmaxf(tmax[e >> 1], v);
             }
@@ -1148,8 +1162,7 @@ static int attention_hd(const float* qkv, int ld, int n_seqs, int block_len, con
 int attention(const float* qkv, int ld, int n_seqs, int block_len, const AttnSeq* seqs_dev, int max_ctx, int nq,
               int nkv, int hd, float scale, float* part, int64_t part_floats, float* y, int num_sms, cudaStream_t st,
               const float* q_norm, const float* k_norm, const float2* rope, float eps, bool kv_ready) {
-    if ((q_norm == nullptr) != (k_norm == nullptr) || (q_norm != nullptr && rope == nullptr))
-        return (int)cudaErrorInvalidValue;
+    if ((q_norm == nullptr) != (k_norm == nullptr)) return (int)cudaErrorInvalidValue;
     if (hd == 128)
         return attention_hd<128>(qkv, ld, n_seqs, block_len, seqs_dev, max_ctx, nq, nkv, scale, part, part_floats, y,
                                  num_sms, st, q_norm, k_norm, rope, eps, kv_ready ? 1 : 0);

@@ -184,9 +184,11 @@ int embed_rows(const float* embed, int H, int vocab, const uint32_t* anchor_tok,
 // pos0 + r, V rows as they are; stored at index idx0 + r as (hi, lo) f16
 // pairs (plane hi [nkv][cap][hd], then plane lo), where pos_dev = {pos0,
 // idx0} lives in device memory (set per call).
+// rotary_dev: per layer, 0 where the layer's keys carry no rotary position
+// (nullptr: every layer rotary).
 int kv_append(const float* kv, int n, int L, int nkv, int hd, const float* const* k_norm_dev, const float* inv_freq,
               float eps, const int64_t* pos_dev, __half* const* kstore_dev, __half* const* vstore_dev, int64_t cap,
-              cudaStream_t st);
+              cudaStream_t st, const int* rotary_dev = nullptr);
 // a = silu(g) * u for gu [rows][2I] (gate then up); f32 out or int8 codes.
 // The same with the grid in clusters of cluster_x CTAs along x.
 template <typename... KArgs, typename... Args>
@@ -222,11 +224,18 @@ struct AttnSeq {
     int64_t cap;
     int64_t lo;  // first context index read (position - first)
     int n;       // context rows read
+    // context rows (of the n) block row 0 does not see, row i: cut + i
+    // (a layer's window; kNoCut: every row sees all n)
+    int cut;
 };
+constexpr int kNoCut = -(1 << 30);
 // qkv [n_seqs*block_len][ld] (q, k, v of the block); with q_norm != nullptr
 // the kernel applies the per-head RMSNorm (q_norm / k_norm) and the rotation
 // (table `rope` of embed_rows) to q and to the block's k as it loads them,
-// otherwise q and k arrive normed and rotated.  y [n_seqs*block_len][nq*hd].  `part` / part_floats: scratch of
+// otherwise q and k arrive normed and rotated; rope == nullptr with the
+// norms: normed, not rotated (a layer without the rotary position).  Each
+// view's `cut` masks the leading context rows a windowed layer's block row
+// does not see.  y [n_seqs*block_len][nq*hd].  `part` / part_floats: scratch of
 // attn_scratch_floats() floats: none when the key splits merge in
 // distributed shared memory (clusters), the splits' partial rows when long
 // contexts split the keys over more CTAs than the clusters place and merge

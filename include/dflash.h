@@ -68,8 +68,18 @@ typedef struct dflash_seq dflash_seq;     /* one sequence's context K/V */
  * Rules (DFLASH_EGEOM otherwise): layers >= 1; block >= 2; n_taps >= 1;
  * kv_heads >= 1; heads % kv_heads == 0 (the page's rules); and the kernels'
  * limits: head_dim 64 or 128; hidden and intermediate multiples of 64;
- * 0 <= mask_token < vocab; window == 0 (every layer reads its whole
- * context); eps > 0; rope_theta > 0; quant one of DFLASH_QUANT_*.
+ * 0 <= mask_token < vocab; window >= 0 and every windows[l] >= 0;
+ * eps > 0; rope_theta > 0; quant one of DFLASH_QUANT_*.
+ * Windows (page "cortiq-engine 0.8.71 — src/dflash.rs", `Geometry`:
+ * `window`, `windows`; `Drafter::block`, `settle_rows`): block row i of a
+ * layer with window w > 0 sees the context positions >= anchor_pos + i + 1
+ * - w (and every row of the block); once a layer holds more than 2 w
+ * context rows, all but its last w are dropped for good (a later block of
+ * that layer reads from the first row still held).
+ * windows / no_rope point to `layers` entries each, or are NULL (windows:
+ * `window` for every layer; no_rope: every layer rotary).  dflash_init
+ * copies them; dflash_geometry_of returns pointers to the model's copies
+ * (valid until dflash_free).
  */
 typedef struct {
     int32_t hidden;       /* H */
@@ -82,10 +92,12 @@ typedef struct {
     int32_t block;        /* rows of a block: the anchor and block - 1 drafts */
     int32_t n_taps;       /* target layers a context row joins; a row is n_taps * H wide */
     int32_t mask_token;   /* token whose embedding fills rows 1.. of a block */
-    int32_t window;       /* positions a block row sees back; 0 = all (the only value accepted) */
+    int32_t window;       /* positions a block row sees back; 0 = all */
     int32_t quant;        /* DFLASH_QUANT_F32 or DFLASH_QUANT_Q4G32 */
     float eps;            /* RMSNorm epsilon */
     double rope_theta;    /* RoPE base: inv_freq[i] = theta^(-2i/hd) */
+    const int32_t* windows; /* per layer, where the layers differ (0 = all); NULL: `window` everywhere */
+    const int32_t* no_rope; /* per layer, nonzero: no rotary position on its queries and keys; NULL: none */
 } dflash_geometry;
 
 /*

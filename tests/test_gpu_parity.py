@@ -342,6 +342,40 @@ def test_block_matches_oracle(name, forced):
 
 
 @pytest.mark.parametrize("name", ["tiny_f32", "small_q4"])
+@pytest.mark.parametrize("forced", [True, False])
+def test_windows_and_no_rope_match_oracle(name, forced):
+    """Page 1's geometry variants: a windowed layer among whole-context ones,
+    a layer without the rotary position, and the drop of context rows that
+    fell out of every window (appends in chunks that cross it), in blocks of
+    two sequences at the end of their contexts and one anchored inside the
+    rows still held."""
+    L = W.WORKLOADS[name].geom.layers
+    p = Pair(name, windows=(9,) + (0,) * (L - 1), no_rope=(L - 1,))
+    g = p.g
+    sc = Script(p, 2, 64)
+    taps = W.make_taps(g, 40)
+    for r0 in range(0, 40, 13):
+        sc.append(0, r0, taps[r0:r0 + 13])
+    sc.append(1, 0, W.make_taps(g, 25, call_id=3))
+    anchors = [int(a) for a in W.make_anchors(g, 2)]
+    sc.block([0, 1], anchors, [40, 25], g.block)
+    sc.block([0], [anchors[1]], [34], g.block)
+    sc.run(forced).check(forced)
+
+
+def test_geometry_lists_round_trip():
+    """dflash_geometry_of gives back the per-layer windows and no-rope flags
+    the model was made with."""
+    dfl = _dfl()
+    L = W.WORKLOADS["small_q4"].geom.layers
+    p = Pair("small_q4", windows=(5,) + (0,) * (L - 1), no_rope=(0,))
+    gs = dfl._abi.Geometry()
+    assert dfl.lib().dflash_geometry_of(p.gpu.handle, dfl._abi.C.byref(gs)) == 0
+    assert [gs.windows[i] for i in range(L)] == list(p.g.windows)
+    assert [gs.no_rope[i] for i in range(L)] == [1 if i == 0 else 0 for i in range(L)]
+
+
+@pytest.mark.parametrize("name", ["tiny_f32", "small_q4"])
 def test_block_edge_cases(name):
     """Shorter blocks, an empty context, an anchor inside the held context, a
     block reading a context that starts past position 0."""
