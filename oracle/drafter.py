@@ -5,8 +5,11 @@ documentation; ``rms``; ``Drafter::rotate``; ``Drafter::mlp``;
 ``Drafter::push_context`` / ``queue_context`` / ``truncate`` / ``reset``;
 ``Drafter::settle_rows``; ``Drafter::block``; ``top_k``), with:
 
-* the DFlash 2 row convolution bypassed (x and the sub-layer outputs pass
-  unchanged), the reading this path takes because its workloads fix no
+* the DFlash 2 row convolution (``conv_in`` / ``conv`` / ``conv_out``:
+  stage 0 on the normed rows before a sub-layer, stage 1 on its output before
+  the residual add, both with the dynamic kernels projected from the normed
+  rows) where the geometry has one (``conv_kernel > 0``); without one the
+  sub-layers are unwrapped, the reading the workloads take since they fix no
   convolution geometry;
 * rows queued for later settling not modelled: every append settles at once
   (the values are the same, only the time they are computed moves);
@@ -39,6 +42,29 @@ def rms(x, w, eps):
     x = np.asarray(x, dtype=F64)
     ms = np.mean(x * x, axis=-1, keepdims=True)
     return x / np.sqrt(ms + eps) * np.asarray(w, dtype=F64)
+
+
+def row_conv(base, d, x, stage, kn, gs):
+    """One stage of the DFlash 2 row convolution over a block's rows (page
+    "cortiq-engine 0.8.71 — src/dflash.rs", `conv`): output row r is the sum
+    over row offsets o < min(kn, r + 1) of (base[stage][o] + the row's
+    dynamic kernel value of its column group) times input row r - o.
+
+    base: [2, kn, hidden]; d: [rows, 2 * kn * groups], row r's dynamic
+    kernels in the order (stage, offset, group); x: [rows, hidden];
+    gs: columns per group.  Returns [rows, hidden] (float64).
+    """
+    x = np.asarray(x, dtype=F64)
+    rows, hs = x.shape
+    groups = hs // gs
+    dyn = np.asarray(d, dtype=F64).reshape(rows, 2, kn, groups)
+    base = np.asarray(base, dtype=F64).reshape(2, kn, hs)
+    y = np.zeros((rows, hs), dtype=F64)
+    for r in range(rows):
+        for o in range(min(kn, r + 1)):
+            kernel = base[stage, o] + np.repeat(dyn[r, stage, o], gs)
+            y[r] += kernel * x[r - o]
+    return y
 
 
 def silu(a):
@@ -178,13 +204,19 @@ class OracleModel:
         self.head = Matrix(weights["head"], hfmt)
         self.layers = []
         for lw in weights["layers"]:
-            self.layers.append({
+            layer = {
                 "in_norm": np.asarray(lw["in_norm"], dtype=F64),
                 "post_norm": np.asarray(lw["post_norm"], dtype=F64),
                 "q_norm": np.asarray(lw["q_norm"], dtype=F64),
                 "k_norm": np.asarray(lw["k_norm"], dtype=F64),
                 **{name: Matrix(lw[name], mfmt) for name in ("q", "k", "v", "o", "gate", "up", "down")},
-            })
+            }
+            if getattr(g, "conv_kernel", 0):
+                # the row convolutions: base kernels and the f32 kernel projections
+                for c in ("attn_conv", "mlp_conv"):
+                    layer[c + "_base"] = np.asarray(lw[c + "_base"], dtype=F64)
+                    layer[c + "_proj"] = np.asarray(lw[c + "_proj"], dtype=F64)
+            self.layers.append(layer)
         self.inv_f = inv_freq(g.head_dim, g.rope_theta)
 
     def window_of(self, layer):
@@ -347,7 +379,13 @@ def block(model, seq, anchor_tok, anchor_pos, block_len=None, return_hidden=Fals
         base = seq.first + seq.dropped[li]
         kc = seq.k[li][:, lo - base:hi - base]
         vc = seq.v[li][:, lo - base:hi - base]
+        conv = getattr(g, "conv_kernel", 0)
+        kn, gs = conv, getattr(g, "conv_group", 0)
         x = rms(h, L["in_norm"], g.eps)
+        if conv:
+            # x, d = conv_in(x): the row's dynamic kernels from the normed rows, then stage 0
+            da = x @ L["attn_conv_proj"].T
+            x = row_conv(L["attn_conv_base"], da, x, 0, kn, gs)
         q = L["q"].apply(x).reshape(rows, nh, hd)
         k = L["k"].apply(x).reshape(rows, kv, hd)
         v = L["v"].apply(x).reshape(rows, kv, hd)
@@ -359,10 +397,19 @@ def block(model, seq, anchor_tok, anchor_pos, block_len=None, return_hidden=Fals
         w = m.window_of(li)
         row_from = [max(anchor_pos + r + 1 - w, 0) for r in range(rows)] if w > 0 else None
         y = attention(q, k, v, kc, vc, g.rep, scale, row_from, lo)
-        h = h + L["o"].apply(y.reshape(rows, nh * hd))
+        o = L["o"].apply(y.reshape(rows, nh * hd))
+        if conv:
+            o = row_conv(L["attn_conv_base"], da, o, 1, kn, gs)  # conv_out(O y, d)
+        h = h + o
         x = rms(h, L["post_norm"], g.eps)
+        if conv:
+            dm = x @ L["mlp_conv_proj"].T
+            x = row_conv(L["mlp_conv_base"], dm, x, 0, kn, gs)
         a = silu(L["gate"].apply(x)) * L["up"].apply(x)
-        h = h + L["down"].apply(a)
+        dn = L["down"].apply(a)
+        if conv:
+            dn = row_conv(L["mlp_conv_base"], dm, dn, 1, kn, gs)
+        h = h + dn
     hn = rms(h, m.norm, g.eps)
     logits = m.head.apply(hn[1:])
     toks = argmax_first(logits)

@@ -205,3 +205,113 @@ def test_no_rope_layers_see_the_context_as_a_set(model):
     np.testing.assert_allclose(la, lb, rtol=1e-9, atol=1e-10 * np.max(np.abs(la)))
     pa, pb = res["plain"]
     assert np.max(np.abs(pa - pb)) > 1e-6 * np.max(np.abs(pa))
+
+
+# ------------------------------------------------------------ row convolution
+def test_row_conv_shift_closed_form():
+    """Kernels of two rows with no dynamic part: output = (I + c S) x with S
+    the one-row shift, as a matrix product."""
+    from oracle import row_conv
+    rng = np.random.default_rng(5)
+    rows, hs, gs = 7, 12, 4
+    x = rng.standard_normal((rows, hs))
+    c = rng.standard_normal(hs)
+    base = np.zeros((2, 2, hs))
+    base[1, 0] = 1.0
+    base[1, 1] = c
+    d = np.zeros((rows, 2 * 2 * (hs // gs)))
+    y = row_conv(base, d, x, 1, 2, gs)
+    shift = np.eye(rows, k=-1)
+    np.testing.assert_allclose(y, x + (shift @ x) * c, rtol=1e-14, atol=1e-15)
+    # stage 0 of the same base is all zeros here
+    np.testing.assert_array_equal(row_conv(base, d, x, 0, 2, gs), np.zeros_like(x))
+
+
+def test_row_conv_dynamic_kernel_indexing():
+    """A projection whose (stage 1, offset 0, group g) row picks column j_g of
+    the row and a zero base: output column i = x[r, j_{g(i)}] * x[r, i],
+    by fancy indexing -- the dynamic kernels' (stage, offset, group) order."""
+    from oracle import row_conv
+    rng = np.random.default_rng(6)
+    rows, hs, gs, kn = 5, 16, 4, 3
+    groups = hs // gs
+    x = rng.standard_normal((rows, hs))
+    pick = rng.integers(0, hs, size=groups)
+    proj = np.zeros((2 * kn * groups, hs))
+    for g_ in range(groups):
+        proj[(1 * kn + 0) * groups + g_, pick[g_]] = 1.0
+    d = x @ proj.T
+    y = row_conv(np.zeros((2, kn, hs)), d, x, 1, kn, gs)
+    ref = x * x[:, pick][:, np.arange(hs) // gs]
+    np.testing.assert_allclose(y, ref, rtol=1e-14, atol=1e-15)
+
+
+def test_bypass_convolution_is_no_convolution(model):
+    """kn = 1, base 1, projection 0: the convolution passes every row
+    unchanged, so the block equals the unwrapped one exactly."""
+    m, _ = model
+    g = m.g
+    gc = dataclasses.replace(g, conv_kernel=1, conv_group=g.hidden // 4)
+    w = W.make_weights(gc)
+    for lw in w["layers"]:
+        for c in ("attn_conv", "mlp_conv"):
+            lw[c + "_base"][:] = 1
+            lw[c + "_proj"][:] = 0
+    plain = {k: v for k, v in w.items() if k != "layers"}
+    plain["layers"] = [{k: v for k, v in lw.items() if "conv" not in k} for lw in w["layers"]]
+    mc, mp = OracleModel(gc, w), OracleModel(g, plain)
+    taps = W.make_taps(g, 12)
+    sc, sp = OracleSeq(mc), OracleSeq(mp)
+    sc.append(0, taps)
+    sp.append(0, taps)
+    np.testing.assert_array_equal(block(mc, sc, 4, 12)[0], block(mp, sp, 4, 12)[0])
+
+
+def test_single_row_kernel_folds_into_weights():
+    """kn = 1 with no dynamic part scales columns: stage 0 of the attention
+    convolution is a factor on in_norm's gains, its stage 1 one on O's output
+    rows; the MLP's likewise on post_norm and on down's rows (all-f32 drafter,
+    so the folded weights are exact)."""
+    g = dataclasses.replace(W.WORKLOADS["tiny_f32"].geom, conv_kernel=1, conv_group=64)
+    w = W.make_weights(g)
+    rng = np.random.default_rng(8)
+    for lw in w["layers"]:
+        for c in ("attn_conv", "mlp_conv"):
+            lw[c + "_proj"][:] = 0
+            # powers of two: the folded float32 weights are exact
+            lw[c + "_base"][:] = 2.0 ** rng.integers(-2, 3, size=lw[c + "_base"].shape)
+    folded = {k: v for k, v in w.items() if k != "layers"}
+    folded["layers"] = []
+    for lw in w["layers"]:
+        f = {k: v.copy() for k, v in lw.items() if "conv" not in k}
+        f["in_norm"] = (lw["in_norm"].astype(np.float64) * lw["attn_conv_base"][0, 0]).astype(np.float64)
+        f["o"] = lw["o"].astype(np.float64) * lw["attn_conv_base"][1, 0][:, None]
+        f["post_norm"] = lw["post_norm"].astype(np.float64) * lw["mlp_conv_base"][0, 0]
+        f["down"] = lw["down"].astype(np.float64) * lw["mlp_conv_base"][1, 0][:, None]
+        folded["layers"].append(f)
+    g0 = dataclasses.replace(g, conv_kernel=0, conv_group=0)
+    mc, mf = OracleModel(g, w), OracleModel(g0, folded)
+    taps = W.make_taps(g, 10)
+    sc, sf = OracleSeq(mc), OracleSeq(mf)
+    sc.append(0, taps)
+    sf.append(0, taps)
+    lc, lf = block(mc, sc, 2, 10)[0], block(mf, sf, 2, 10)[0]
+    np.testing.assert_allclose(lc, lf, rtol=1e-10, atol=1e-12 * np.max(np.abs(lf)))
+
+
+def test_convolution_is_causal_over_the_block_rows(model):
+    """Row r's draft depends on rows <= r only: a longer block's first rows
+    equal a shorter block's (a convolution looking ahead would change them
+    through the later rows).  Attention mixes every block row, so it is taken
+    out (Wo = 0) and the rows meet only in the convolutions."""
+    m, _ = model
+    g = dataclasses.replace(m.g, conv_kernel=3, conv_group=m.g.hidden // 4)
+    w = W.make_weights(g)
+    for lw in w["layers"]:
+        lw["o"][:] = 0  # attention mixes all block rows; take it out
+    mc = OracleModel(g, w)
+    s = OracleSeq(mc)
+    s.append(0, W.make_taps(g, 9))
+    long_, _ = block(mc, s, 6, 9, block_len=g.block)
+    short, _ = block(mc, s, 6, 9, block_len=4)
+    np.testing.assert_allclose(long_[:3], short, rtol=1e-12, atol=1e-13 * np.max(np.abs(short)))

@@ -10,6 +10,8 @@ Recipe (all draws float32, all seeded, no dataset):
 * every weight matrix and the embedding: N(0, 0.02);
 * every norm gain (hidden_norm, norm, in_norm, post_norm, q_norm, k_norm):
   1 + N(0, 0.02), so the gain multiply is exercised;
+* a row convolution's base kernels (when the geometry has one): N(0, 0.02),
+  plus 1 at row offset 0; its kernel projections N(0, 0.02);
 * context taps: N(0, 1);
 * anchor tokens: uniform over the vocabulary.
 
@@ -36,7 +38,9 @@ ANCHOR_SEED = 2
 # LAYER_BASE + LAYER_STRIDE * l + (offset in LAYER_TENSORS)
 TID_FC, TID_HIDDEN_NORM, TID_NORM, TID_EMBED, TID_HEAD = 0, 1, 2, 3, 4
 LAYER_BASE, LAYER_STRIDE = 16, 16
-LAYER_TENSORS = ("in_norm", "post_norm", "q_norm", "k_norm", "q", "k", "v", "o", "gate", "up", "down")
+LAYER_TENSORS = ("in_norm", "post_norm", "q_norm", "k_norm", "q", "k", "v", "o", "gate", "up", "down",
+                 "attn_conv_base", "attn_conv_proj", "mlp_conv_base", "mlp_conv_proj")
+CONV_TENSORS = LAYER_TENSORS[11:]  # drawn only for a geometry with a row convolution
 GAINS = {"in_norm", "post_norm", "q_norm", "k_norm", "hidden_norm", "norm"}
 
 
@@ -59,6 +63,8 @@ class Geometry:
     quant: int = 0  # 0: all f32; 1: 4-bit g32 matrices, int8 head, int8 activations
     mask_token: int | None = None  # None: vocab - 1
     window: int = 0  # positions a block row sees back; 0 = all
+    conv_kernel: int = 0  # rows of the DFlash 2 row convolution; 0: none (the sub-layers unwrapped)
+    conv_group: int = 0  # hidden columns that share one dynamic kernel value
     windows: tuple = ()  # the same per layer where layers differ (0: all); empty: `window` for every layer
     no_rope: tuple = ()  # layers whose queries and keys carry no rotary position
 
@@ -152,11 +158,17 @@ def normal(seed: int, tensor_id: int, shape, std: float = 1.0, mean: float = 0.0
 
 def weight_shapes(g: Geometry) -> dict:
     hs, ffn, qd, kd = g.hidden, g.intermediate, g.heads * g.head_dim, g.kv_heads * g.head_dim
-    return {
+    shapes = {
         "in_norm": (hs,), "post_norm": (hs,), "q_norm": (g.head_dim,), "k_norm": (g.head_dim,),
         "q": (qd, hs), "k": (kd, hs), "v": (kd, hs), "o": (hs, qd),
         "gate": (ffn, hs), "up": (ffn, hs), "down": (hs, ffn),
     }
+    if g.conv_kernel:
+        kn, groups = g.conv_kernel, hs // g.conv_group
+        for c in ("attn_conv", "mlp_conv"):
+            shapes[c + "_base"] = (2, kn, hs)  # [stage][row offset][column]
+            shapes[c + "_proj"] = (2 * kn * groups, hs)  # the dynamic kernels [stage][offset][group] of a row
+    return shapes
 
 
 def make_weights(g: Geometry, seed: int = WEIGHT_SEED, std: float = 0.02) -> dict:
@@ -179,8 +191,13 @@ def make_weights(g: Geometry, seed: int = WEIGHT_SEED, std: float = 0.02) -> dic
         "head": draw(TID_HEAD, "head", (g.vocab, hs)),
     }
     shapes = weight_shapes(g)
-    w["layers"] = [{name: draw(layer_tid(l, name), name, shapes[name]) for name in LAYER_TENSORS}
+    w["layers"] = [{name: draw(layer_tid(l, name), name, shapes[name]) for name in LAYER_TENSORS if name in shapes}
                    for l in range(g.layers)]
+    for lw in w["layers"]:
+        # a convolution's base kernel: 1 + N(0, 0.02) at row offset 0, N(0, 0.02) further back
+        for c in ("attn_conv_base", "mlp_conv_base"):
+            if c in lw:
+                lw[c][:, 0, :] += np.float32(1.0)
     return w
 
 
