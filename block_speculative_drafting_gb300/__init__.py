@@ -23,6 +23,7 @@ _lib = None
 
 GEOM_FIELDS = ("hidden", "intermediate", "layers", "heads", "kv_heads", "head_dim", "vocab", "block", "n_taps")
 LAYER_TENSORS = ("in_norm", "post_norm", "q_norm", "k_norm", "q", "k", "v", "o", "gate", "up", "down")
+CONV_TENSORS = ("attn_conv_base", "attn_conv_proj", "mlp_conv_base", "mlp_conv_proj")  # with a row convolution
 
 
 def lib():
@@ -77,6 +78,8 @@ def geometry_struct(g) -> _abi.Geometry:
     s.quant = int(getattr(g, "quant", 0))
     s.eps = float(getattr(g, "eps", 1e-6))
     s.rope_theta = float(getattr(g, "rope_theta", 1e6))
+    s.conv_kernel = int(getattr(g, "conv_kernel", 0))
+    s.conv_group = int(getattr(g, "conv_group", 0))
     # per-layer lists: arrays kept alive on the struct until dflash_init has copied them
     L = int(g.layers)
     wins = tuple(getattr(g, "windows", ()) or ())
@@ -146,7 +149,10 @@ class Model:
         for k in ("fc", "hidden_norm", "norm", "embed", "head"):
             setattr(w, k, C.cast(C.c_void_p(_ptr(weights[k])), FP))
         arrays = []
-        for name in LAYER_TENSORS:
+        names = LAYER_TENSORS + (CONV_TENSORS if self.gs.conv_kernel > 0 else ())
+        for name in names:
+            if any(name not in lw for lw in weights["layers"]):
+                continue  # left NULL: the library names what is missing
             arr = (FP * L)(*[C.cast(C.c_void_p(_ptr(weights["layers"][l][name])), FP) for l in range(L)])
             arrays.append(arr)
             setattr(w, name, C.cast(arr, C.POINTER(FP)))

@@ -32,6 +32,9 @@ struct Layer {
     float *in_norm = nullptr, *post_norm = nullptr, *q_norm = nullptr, *k_norm = nullptr;
     uint8_t *qkv_p = nullptr, *o_p = nullptr, *gu_p = nullptr, *down_p = nullptr;  // 4-bit packed
     float *qkv_f = nullptr, *o_f = nullptr, *gu_f = nullptr, *down_f = nullptr;    // f32
+    // the row convolutions around attention (a) and the MLP (m): base
+    // [2][kn][H], kernel projection [2 kn G][H] (f32)
+    float *a_base = nullptr, *a_proj = nullptr, *m_base = nullptr, *m_proj = nullptr;
 };
 
 struct MatView {
@@ -138,6 +141,7 @@ struct dflash_model {
     DevBuf h, xq, xs, qkv, y, gu, logits, keys, toks, part, anchors, pos0, aseqs, rope;
     DevBuf a_taps, a_codes, a_scale, a_t, a_kv, a_pos;
     DevBuf x16;  // activation codes as f16 for the tcgen05 kernels (matmuls of more than 16 rows)
+    DevBuf cx, cd, co;  // the row convolution: normed rows, their dynamic kernels, a sub-layer's output
     bool grown = false;  // a scratch buffer moved since the graphs were captured
 
     // CUDA graphs of the kernel sequences of a block and of a short append,
@@ -299,6 +303,9 @@ std::string geometry_problem(const dflash_geometry& g) {
     if (g.vocab < 1) return "vocab < 1";
     if (g.mask_token < 0 || g.mask_token >= g.vocab) return "mask_token outside [0, vocab)";
     if (g.window < 0) return "window < 0";
+    if (g.conv_kernel < 0 || g.conv_kernel > 64) return "conv_kernel outside [0, 64]";
+    if (g.conv_kernel > 0 && (g.conv_group < 4 || g.conv_group % 4 || g.hidden % g.conv_group))
+        return "conv_group must be a multiple of 4 dividing hidden";
     if (g.windows)
         for (int l = 0; l < g.layers; ++l)
             if (g.windows[l] < 0) return "windows[" + std::to_string(l) + "] < 0";
@@ -482,6 +489,17 @@ int build_model(dflash_model* m, const dflash_weights* w, bool on_dev, cudaStrea
         CK(m, dalloc(m, &Ly.k_norm, hd));
         CK(m, copy_f32(m, Ly.k_norm, w->k_norm[l], hd, on_dev));
         knorm_ptrs[l] = Ly.k_norm;
+        if (g.conv_kernel > 0) {
+            const size_t nb = (size_t)2 * g.conv_kernel * H, np = nb / g.conv_group * H;
+            CK(m, dalloc(m, &Ly.a_base, nb));
+            CK(m, copy_f32(m, Ly.a_base, w->attn_conv_base[l], nb, on_dev));
+            CK(m, dalloc(m, &Ly.a_proj, np));
+            CK(m, copy_f32(m, Ly.a_proj, w->attn_conv_proj[l], np, on_dev));
+            CK(m, dalloc(m, &Ly.m_base, nb));
+            CK(m, copy_f32(m, Ly.m_base, w->mlp_conv_base[l], nb, on_dev));
+            CK(m, dalloc(m, &Ly.m_proj, np));
+            CK(m, copy_f32(m, Ly.m_proj, w->mlp_conv_proj[l], np, on_dev));
+        }
         if (quant) {
             CK(m, dalloc(m, &Ly.qkv_p, q4_bytes(m->L_qkv)));
             CK(m, pack(w->q[l], m->qd, H, Ly.qkv_p, 0, m->L_qkv));
@@ -522,7 +540,7 @@ int build_model(dflash_model* m, const dflash_weights* w, bool on_dev, cudaStrea
     return DFLASH_OK;
 }
 
-bool weights_complete(const dflash_weights* w, int L) {
+bool weights_complete(const dflash_weights* w, int L, bool conv) {
     if (!w->fc || !w->hidden_norm || !w->norm || !w->embed || !w->head) return false;
     const float* const* per[] = {w->in_norm, w->post_norm, w->q_norm, w->k_norm, w->q, w->k,
                                  w->v,       w->o,         w->gate,   w->up,     w->down};
@@ -530,6 +548,14 @@ bool weights_complete(const dflash_weights* w, int L) {
         if (!a) return false;
         for (int l = 0; l < L; ++l)
             if (!a[l]) return false;
+    }
+    if (conv) {
+        const float* const* cv[] = {w->attn_conv_base, w->attn_conv_proj, w->mlp_conv_base, w->mlp_conv_proj};
+        for (auto a : cv) {
+            if (!a) return false;
+            for (int l = 0; l < L; ++l)
+                if (!a[l]) return false;
+        }
     }
     return true;
 }
@@ -978,7 +1004,8 @@ int dflash_init(const dflash_geometry* geom, const dflash_weights* weights, int 
     if (!geom || !weights) return set_err(nullptr, DFLASH_EINVAL, "geometry or weights is NULL");
     std::string why = geometry_problem(*geom);
     if (!why.empty()) return set_err(nullptr, DFLASH_EGEOM, "unsupported geometry: " + why);
-    if (!weights_complete(weights, geom->layers)) return set_err(nullptr, DFLASH_EINVAL, "a weight pointer is NULL");
+    if (!weights_complete(weights, geom->layers, geom->conv_kernel > 0))
+        return set_err(nullptr, DFLASH_EINVAL, "a weight pointer is NULL");
     dflash_model* m = new (std::nothrow) dflash_model();
     if (!m) return set_err(nullptr, DFLASH_ENOMEM, "host allocation failed");
     m->g = *geom;
@@ -1023,7 +1050,7 @@ void dflash_free(dflash_model* m) {
     for (void* p : m->owned) cudaFree(p);
     for (DevBuf* b : {&m->h, &m->xq, &m->xs, &m->qkv, &m->y, &m->gu, &m->logits, &m->keys, &m->toks, &m->part,
                       &m->anchors, &m->pos0, &m->aseqs, &m->rope, &m->a_taps, &m->a_codes, &m->a_scale, &m->a_t,
-                      &m->a_kv, &m->a_pos, &m->x16, &m->trace_buf})
+                      &m->a_kv, &m->a_pos, &m->x16, &m->trace_buf, &m->cx, &m->cd, &m->co})
         free_buf(*b);
     delete m;
 }
@@ -1210,6 +1237,11 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
     CK(m, ensure_m(m, m->pos0, (size_t)n_seqs * sizeof(int64_t)));
     CK(m, ensure_m(m, m->rope, (size_t)R * (hd / 2) * sizeof(float2)));
     CK(m, ensure_m(m, m->aseqs, (size_t)g.layers * n_seqs * sizeof(AttnSeq)));
+    if (g.conv_kernel > 0) {
+        CK(m, ensure_m(m, m->cx, (size_t)R * H * sizeof(float)));
+        CK(m, ensure_m(m, m->cd, (size_t)R * 2 * g.conv_kernel * (H / g.conv_group) * sizeof(float)));
+        CK(m, ensure_m(m, m->co, (size_t)R * H * sizeof(float)));
+    }
     if (quant && R > 16) {
         // f16 codes of the widest matmul input, then the head rows' code norms
         CK(m, ensure_m(m, m->x16, (size_t)R * (maxK * sizeof(__half) + sizeof(int))));
@@ -1255,7 +1287,7 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
     RowMap drafts{B - 1, B, 1};
     unsigned long long* keys = P<unsigned long long>(m->keys);
     uint32_t* tok_out = (io_on_device && draft_tok) ? draft_tok : P<uint32_t>(m->toks);
-    if (quant && chain_ok(m, R)) {
+    if (quant && chain_ok(m, R) && g.conv_kernel == 0) {
         // the steps between two attentions as one chain program each:
         // [x = Q(rms(h, in_norm)); qkv = W x] before the first attention, then per
         // layer [Q(y); h += O y; x = Q(rms(h, post_norm)); gu = [G; U] x;
@@ -1321,7 +1353,87 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
         KL(m, "keys_to_tokens", 1, (double)D * 12, st, keys_to_tokens(keys, D, tok_out, st));
         return DFLASH_OK;
     }
-    for (int l = 0; l < g.layers; ++l) {
+    // with a row convolution: x = conv_in(rms(h, norm)) before each
+    // sub-layer, h += conv_out(its output) after it (a separate sequence of
+    // launches; the sub-layers' own kernels are the same)
+    for (int l = 0; l < g.layers && g.conv_kernel > 0; ++l) {
+        const Layer& Ly = m->layers[l];
+        const int kn = g.conv_kernel, gs = g.conv_group, nd = 2 * kn * (H / gs);
+        float* cx = P<float>(m->cx);
+        float* cd = P<float>(m->cd);
+        float* co = P<float>(m->co);
+        // cx = rms(h, w); cd = proj . cx; then stage 0 of cx: the codes of the
+        // next matmul (quantised) or its f32 rows; `zero` cleared on the side
+        // of the norm's launch, `zero2` of stage 0's
+        auto conv_in = [&](const float* w, const float* base, const float* proj, float* zero, int64_t zero_n,
+                           float* zero2, int64_t zero2_n) -> int {
+            KL(m, "rms_f32", 1, (double)R * H * 8, st,
+               rms_rows(h, H, ident, R, H, w, g.eps, cx, H, nullptr, nullptr, 0, st, zero, zero_n));
+            KL(m, "linear_f32", 1, f32_bytes_of(nd, H, R, false), st,
+               linear_f32(proj, nd, H, cx, H, R, cd, nd, false, st));
+            if (quant) {
+                KL(m, "conv_rows", 1, (double)R * H * 4 * (kn + 1), st,
+                   conv_rows(cx, H, cd, nd, base, 0, kn, gs, H, R, B, nullptr, 0, nullptr, 0, xq, xs, maxK, st, zero2,
+                             zero2_n));
+                TRACE(trace_site(m, st, R, H, xq, maxK, xs, [&](float* v) {
+                    return conv_rows(cx, H, cd, nd, base, 0, kn, gs, H, R, B, nullptr, 0, v, H, nullptr, nullptr, 0,
+                                     st);
+                }));
+            } else {
+                KL(m, "conv_rows", 1, (double)R * H * 4 * (kn + 1), st,
+                   conv_rows(cx, H, cd, nd, base, 0, kn, gs, H, R, B, nullptr, 0, xf, maxK, nullptr, nullptr, 0, st, zero2,
+                             zero2_n));
+            }
+            return DFLASH_OK;
+        };
+        // h += stage 1 of the sub-layer's output co
+        auto conv_out = [&](const float* base) -> int {
+            KL(m, "conv_rows", 1, (double)R * H * 4 * (kn + 2), st,
+               conv_rows(co, H, cd, nd, base, 1, kn, gs, H, R, B, h, H, nullptr, 0, nullptr, nullptr, 0, st));
+            return DFLASH_OK;
+        };
+        APPLY(conv_in(Ly.in_norm, Ly.a_base, Ly.a_proj, quant ? qkv : nullptr, quant ? (int64_t)R * m->qkv_w : 0,
+                      nullptr, 0));
+        if (quant)
+            APPLY(apply(m, Ly.qkv_p, nullptr, m->L_qkv, 0, m->qkv_w, H, nullptr, 0, R, qkv, m->qkv_w, false, maxK, st));
+        else
+            APPLY(apply(m, nullptr, Ly.qkv_f, Q4Layout{}, 0, m->qkv_w, H, xf, maxK, R, qkv, m->qkv_w, false, 0, st));
+        const AttnSeq* aseq_dev = P<AttnSeq>(m->aseqs) + (size_t)l * n_seqs;
+        KL(m, "attention", attn_kernels(n_seqs, B, max_ctx, g.heads, g.kv_heads, hd, m->num_sms, part_floats),
+           attn_bytes_l[l], st,
+           attention(qkv, m->qkv_w, n_seqs, B, aseq_dev, max_ctx, g.heads, g.kv_heads, hd, scale, P<float>(m->part),
+                     part_floats, y, m->num_sms, st, Ly.q_norm, Ly.k_norm, m->norope[l] ? nullptr : rope, g.eps,
+                     m->own_capture));
+        // co = O y (the streaming matvec adds: co cleared by the quantisation of y)
+        if (quant) {
+            KL(m, "rms_quant", 1, (double)R * m->qd * 5, st,
+               rms_rows(y, m->qd, ident, R, m->qd, nullptr, g.eps, nullptr, 0, xq, xs, maxK, st, co, (int64_t)R * H));
+            TRACE(trace_site(m, st, R, m->qd, xq, maxK, xs, [&](float* v) {
+                return rms_rows(y, m->qd, ident, R, m->qd, nullptr, g.eps, v, m->qd, nullptr, nullptr, 0, st);
+            }));
+            APPLY(apply(m, Ly.o_p, nullptr, m->L_o, 0, H, m->qd, nullptr, 0, R, co, H, false, maxK, st));
+        } else {
+            APPLY(apply(m, nullptr, Ly.o_f, Q4Layout{}, 0, H, m->qd, y, m->qd, R, co, H, false, 0, st));
+        }
+        APPLY(conv_out(Ly.a_base));
+        // the MLP the same way (gu cleared by the norm's launch, co by stage 0's)
+        APPLY(conv_in(Ly.post_norm, Ly.m_base, Ly.m_proj, quant ? gu : nullptr, quant ? (int64_t)R * 2 * I : 0,
+                      quant ? co : nullptr, quant ? (int64_t)R * H : 0));
+        if (quant) {
+            APPLY(apply(m, Ly.gu_p, nullptr, m->L_gu, 0, 2 * I, H, nullptr, 0, R, gu, 2 * I, false, maxK, st));
+            KL(m, "silu_quant", 1, (double)R * I * 9, st, silu_mul(gu, 2 * I, R, I, nullptr, 0, xq, xs, maxK, st));
+            TRACE(trace_site(m, st, R, I, xq, maxK, xs, [&](float* v) {
+                return silu_mul(gu, 2 * I, R, I, v, I, nullptr, nullptr, 0, st);
+            }));
+            APPLY(apply(m, Ly.down_p, nullptr, m->L_down, 0, H, I, nullptr, 0, R, co, H, false, maxK, st));
+        } else {
+            APPLY(apply(m, nullptr, Ly.gu_f, Q4Layout{}, 0, 2 * I, H, xf, maxK, R, gu, 2 * I, false, 0, st));
+            KL(m, "silu_f32", 1, (double)R * I * 12, st, silu_mul(gu, 2 * I, R, I, xf, maxK, nullptr, nullptr, 0, st));
+            APPLY(apply(m, nullptr, Ly.down_f, Q4Layout{}, 0, H, I, xf, maxK, R, co, H, false, 0, st));
+        }
+        APPLY(conv_out(Ly.m_base));
+    }
+    for (int l = 0; l < g.layers && g.conv_kernel == 0; ++l) {
         const Layer& Ly = m->layers[l];
         // attention half: x = rms(h, in_norm); q, k, v; norms and rotation; attention; h += O y
         if (quant) {

@@ -189,6 +189,104 @@ int rms_rows(const float* src, int ld_src, RowMap map, int rows, int n, const fl
                        ld_out, out_codes, out_scale, ld_codes, zero_buf, zero_n);
 }
 
+// ------------------------------------------------------------------ row convolution
+// One stage of the DFlash 2 row convolution (page "cortiq-engine 0.8.71 —
+// src/dflash.rs", `conv`), a CTA per row r of the block rows: with i = r %
+// block_len the row's index in its sequence's block,
+//   y[r] = sum_{o < min(kn, i + 1)} (base[stage][o] + d[r][(stage kn + o) G + group]) * x[r - o]
+// (G = n / gs groups of gs columns; every float4 of a thread in one group).
+// Then, as asked: h[r] += y (stage 1: the sub-layer output into the residual),
+// y as f32, and / or y as int8 codes with one f32 scale (stage 0: a matmul
+// input).  CTAs past the rows clear the side buffer.
+template <int NV>
+__global__ void __launch_bounds__(kRowThreads) conv_rows_kernel(
+    const float* __restrict__ x, int ldx, const float* __restrict__ d, int ldd, const float* __restrict__ base,
+    int stage, int kn, int gs, int n, int block_len, float* __restrict__ h_add, int ldh, float* __restrict__ out_f32,
+    int ld_out, int8_t* __restrict__ out_codes, float* __restrict__ out_scale, int ld_codes, float* zero_buf,
+    int64_t zero_n, int rows) {
+    __shared__ float red[33];
+    pdl_trigger();
+    pdl_wait();
+    if ((int)blockIdx.x >= rows) {
+        const int64_t stride = (int64_t)(gridDim.x - rows) * blockDim.x;
+        const int64_t first = (int64_t)(blockIdx.x - rows) * blockDim.x + threadIdx.x;
+        float4* p4 = reinterpret_cast<float4*>(zero_buf);
+        for (int64_t k = first; k < zero_n / 4; k += stride) p4[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (first < zero_n % 4) zero_buf[zero_n / 4 * 4 + first] = 0.f;
+        return;
+    }
+    const int r = blockIdx.x, i = r % block_len, groups = n / gs, n4 = n / 4;
+    const int taps = min(kn, i + 1);
+    float4 y[NV];
+#pragma unroll
+    for (int u = 0; u < NV; ++u) y[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int o = 0; o < taps; ++o) {
+        const float4* x4 = reinterpret_cast<const float4*>(x + (int64_t)(r - o) * ldx);
+        const float4* b4 = reinterpret_cast<const float4*>(base + (int64_t)(stage * kn + o) * n);
+        const float* dyn = d + (int64_t)r * ldd + (int64_t)(stage * kn + o) * groups;
+#pragma unroll
+        for (int u = 0; u < NV; ++u) {
+            const int c = threadIdx.x + u * kRowThreads;
+            if (c < n4) {
+                const float4 xv = x4[c], bv = b4[c];
+                const float k = dyn[(4 * c) / gs];
+                y[u].x = fmaf(bv.x + k, xv.x, y[u].x);
+                y[u].y = fmaf(bv.y + k, xv.y, y[u].y);
+                y[u].z = fmaf(bv.z + k, xv.z, y[u].z);
+                y[u].w = fmaf(bv.w + k, xv.w, y[u].w);
+            }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < NV; ++u) {
+        const int c = threadIdx.x + u * kRowThreads;
+        if (c < n4) {
+            if (h_add) {
+                float4* h4 = reinterpret_cast<float4*>(h_add + (int64_t)r * ldh) + c;
+                const float4 hv = *h4;
+                *h4 = make_float4(hv.x + y[u].x, hv.y + y[u].y, hv.z + y[u].z, hv.w + y[u].w);
+            }
+            if (out_f32) reinterpret_cast<float4*>(out_f32 + (int64_t)r * ld_out)[c] = y[u];
+        }
+    }
+    if (!out_codes) return;
+    float amax = 0.f;
+#pragma unroll
+    for (int u = 0; u < NV; ++u) amax = fmaxf(amax, amax4(y[u]));  // lanes past n hold zeros
+    amax = row_reduce<true>(amax, red);
+    const float sx = __fdiv_rn(amax, 127.0f);
+    uint32_t* q4 = reinterpret_cast<uint32_t*>(out_codes + (int64_t)r * ld_codes);
+#pragma unroll
+    for (int u = 0; u < NV; ++u) {
+        const int c = threadIdx.x + u * kRowThreads;
+        if (c < n4) q4[c] = codes4(y[u], sx);
+    }
+    if (threadIdx.x == 0) out_scale[r] = sx;
+}
+
+int conv_rows(const float* x, int ldx, const float* d, int ldd, const float* base, int stage, int kn, int gs, int n,
+              int rows, int block_len, float* h_add, int ldh, float* out_f32, int ld_out, int8_t* out_codes,
+              float* out_scale, int ld_codes, cudaStream_t st, float* zero_buf, int64_t zero_n) {
+    if (rows <= 0) return 0;
+    auto al = [](const void* p, int a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; };
+    if (kn < 1 || gs < 4 || gs % 4 || n % gs || block_len < 1 || rows % block_len || stage < 0 || stage > 1 ||
+        n > 8 * 4 * kRowThreads || ldx % 4 || !al(x, 16) || !al(base, 16) || (h_add && (ldh % 4 || !al(h_add, 16))) ||
+        (out_f32 && (ld_out % 4 || !al(out_f32, 16))) || (out_codes && (ld_codes % 4 || !al(out_codes, 4))) ||
+        (zero_buf && !al(zero_buf, 16)))
+        return (int)cudaErrorInvalidValue;
+    const int nv = (n + 4 * kRowThreads - 1) / (4 * kRowThreads);
+    const int extra = zero_buf && zero_n > 0 ? (int)std::min<int64_t>(128, zero_n / 4 / (kRowThreads * 4) + 1) : 0;
+    auto go = [&](auto kern) {
+        return (int)launch(kern, dim3(rows + extra), dim3(kRowThreads), 0, st, x, ldx, d, ldd, base, stage, kn, gs, n,
+                           block_len, h_add, ldh, out_f32, ld_out, out_codes, out_scale, ld_codes, zero_buf, zero_n,
+                           rows);
+    };
+    if (nv <= 1) return go(conv_rows_kernel<1>);
+    if (nv <= 2) return go(conv_rows_kernel<2>);
+    if (nv <= 4) return go(conv_rows_kernel<4>);
+    return go(conv_rows_kernel<8>);
+}
+
 // A token outside [0, vocab) (only possible for anchors already on the
 // device, which the host cannot check) embeds as a row of zeros.
 __global__ void embed_rows_kernel(const float* __restrict__ embed, int H, int vocab,

@@ -213,6 +213,15 @@ cudaError_t launch_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size
 
 int silu_mul(const float* gu, int ld_gu, int rows, int I, float* out_f32, int ld_out, int8_t* out_codes,
              float* out_scale, int ld_codes, cudaStream_t st);
+// One stage of the row convolution over `rows` block rows (block_len rows a
+// sequence) of n columns: y[r] = sum_{o < min(kn, r % block_len + 1)}
+// (base[stage][o] + d[r][(stage kn + o) (n / gs) + group]) * x[r - o], base
+// [2][kn][n], d [rows][ldd] (2 kn n / gs used); then h_add[r] += y, y as f32
+// (out_f32) and / or as int8 codes + scale (out_codes), each where non-null.
+// gs % 4 == 0, n % gs == 0, n <= 32768; zero_buf / zero_n cleared on the side.
+int conv_rows(const float* x, int ldx, const float* d, int ldd, const float* base, int stage, int kn, int gs, int n,
+              int rows, int block_len, float* h_add, int ldh, float* out_f32, int ld_out, int8_t* out_codes,
+              float* out_scale, int ld_codes, cudaStream_t st, float* zero_buf = nullptr, int64_t zero_n = 0);
 
 // Attention of a block over its sequence's context and its own rows.
 struct AttnSeq {

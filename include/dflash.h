@@ -76,6 +76,15 @@ typedef struct dflash_seq dflash_seq;     /* one sequence's context K/V */
  * - w (and every row of the block); once a layer holds more than 2 w
  * context rows, all but its last w are dropped for good (a later block of
  * that layer reads from the first row still held).
+ * Row convolution (page "cortiq-engine 0.8.71 — src/dflash.rs", module
+ * documentation, `conv_in` / `conv`, `Drafter::block`): with conv_kernel =
+ * kn > 0, each layer wraps attention and the MLP alike: with x the normed
+ * rows, d = proj . x (f32; per row 2 kn G values, G = hidden / conv_group,
+ * order [stage][offset][group]); the sub-layer reads stage 0 of x and its
+ * output passes stage 1 (with the same d) before the residual add, where
+ * stage s of rows z is y[i] = sum_{o < min(kn, i + 1)} (base[s][o] +
+ * d[i][s][o][group]) * z[i - o] over a block's rows i.  conv_kernel = 0: the
+ * sub-layers unwrapped (the same as kn = 1, base 1, proj 0).
  * windows / no_rope point to `layers` entries each, or are NULL (windows:
  * `window` for every layer; no_rope: every layer rotary).  dflash_init
  * copies them; dflash_geometry_of returns pointers to the model's copies
@@ -98,6 +107,9 @@ typedef struct {
     double rope_theta;    /* RoPE base: inv_freq[i] = theta^(-2i/hd) */
     const int32_t* windows; /* per layer, where the layers differ (0 = all); NULL: `window` everywhere */
     const int32_t* no_rope; /* per layer, nonzero: no rotary position on its queries and keys; NULL: none */
+    int32_t conv_kernel;    /* rows of the row convolution around each sub-layer; 0 = none */
+    int32_t conv_group;     /* columns sharing a dynamic kernel value (conv_kernel > 0: a multiple of 4
+                               dividing hidden) */
 } dflash_geometry;
 
 /*
@@ -130,6 +142,13 @@ typedef struct {
     const float* const* gate;
     const float* const* up;
     const float* const* down;
+    /* the row convolutions (conv_kernel > 0; NULL otherwise): per layer, for
+     * attention and for the MLP, base [2][conv_kernel][H] and the kernel
+     * projection [2 * conv_kernel * (H / conv_group)][H] */
+    const float* const* attn_conv_base;
+    const float* const* attn_conv_proj;
+    const float* const* mlp_conv_base;
+    const float* const* mlp_conv_proj;
 } dflash_weights;
 
 /*

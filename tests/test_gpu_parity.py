@@ -363,6 +363,27 @@ def test_windows_and_no_rope_match_oracle(name, forced):
     sc.run(forced).check(forced)
 
 
+@pytest.mark.parametrize("name", ["tiny_f32", "small_q4"])
+@pytest.mark.parametrize("forced", [True, False])
+@pytest.mark.parametrize("variants", [False, True])
+def test_row_convolution_matches_oracle(name, forced, variants):
+    """The DFlash 2 row convolution around attention and the MLP (page 1's
+    conv_in / conv_out), in a block of two sequences (the many-row matmuls
+    at small_q4) and a shorter block of one (the streaming ones); with
+    `variants` also a windowed layer and a layer without the rotary position."""
+    L = W.WORKLOADS[name].geom.layers
+    extra = dict(windows=(9,) + (0,) * (L - 1), no_rope=(L - 1,)) if variants else {}
+    p = Pair(name, conv_kernel=4, conv_group=64, **extra)
+    g = p.g
+    sc = Script(p, 2, 64)
+    sc.append(0, 0, W.make_taps(g, 30))
+    sc.append(1, 0, W.make_taps(g, 17, call_id=5))
+    anchors = [int(a) for a in W.make_anchors(g, 2)]
+    sc.block([0, 1], anchors, [30, 17], g.block)
+    sc.block([0], [anchors[1]], [30], 5)
+    sc.run(forced).check(forced)
+
+
 def test_geometry_lists_round_trip():
     """dflash_geometry_of gives back the per-layer windows and no-rope flags
     the model was made with."""
