@@ -19,4 +19,4 @@ the pages: its composition is pinned only through those parts.
 """
 from . import quant  # noqa: F401
 from .drafter import (OracleModel, OracleSeq, Matrix, argmax_first, attention, block, inv_freq,  # noqa: F401
-                      rms, rope, silu, softmax, top_k, row_conv)
+                      rms, rope, silu, softmax, top_k, row_conv, select)

@@ -21,6 +21,8 @@ documentation; ``rms``; ``Drafter::rotate``; ``Drafter::mlp``;
   row-dependent mask of ``block`` and the drop of context rows no block row
   of a layer can see any more (``settle_rows``), and layers whose queries
   and keys carry no rotary position (``no_rope``);
+* the candidate selector after the head where the geometry has one
+  (``selector_rank > 0``): the draft tokens are then its choices;
 * continuous arithmetic in float64; the decisions that pick an integer (the
   quantised codes, the draft token's argmax) taken in float32; the RoPE angle
   rounded to float32 before its cosine and sine, as the page's ``rotate``
@@ -202,6 +204,12 @@ class OracleModel:
         self.norm = np.asarray(weights["norm"], dtype=F64)
         self.embed = weights["embed"]  # float32 [vocab][hidden], the target's
         self.head = Matrix(weights["head"], hfmt)
+        if getattr(g, "selector_rank", 0):
+            # the candidate selector: the rows' projection (f32 on the page)
+            # and the predecessor / successor codebooks (f16 [vocab][rank])
+            self.sel = np.asarray(weights["selector_projection"], dtype=F64)
+            self.book_p = np.asarray(weights["predecessor_codebook"], dtype=np.float16).astype(F64)
+            self.book_c = np.asarray(weights["successor_codebook"], dtype=np.float16).astype(F64)
         self.layers = []
         for lw in weights["layers"]:
             layer = {
@@ -413,6 +421,36 @@ def block(model, seq, anchor_tok, anchor_pos, block_len=None, return_hidden=Fals
     hn = rms(h, m.norm, g.eps)
     logits = m.head.apply(hn[1:])
     toks = argmax_first(logits)
+    if getattr(g, "selector_rank", 0):
+        toks, _ = select(m, hn[1:], logits, anchor_tok)
     if return_hidden:
         return logits, toks, hn
     return logits, toks
+
+
+def select(model, hn, logits, anchor):
+    """The candidate selector (page "cortiq-engine 0.8.71 — src/dflash.rs",
+    `select` / `select_with`): row by row, its `selector_top` candidates by
+    logit (``top_k`` on the float32 logits) re-scored as logit + (P[prev] ⊙
+    S·h) · C[candidate], the best (the first of equals, in candidate order)
+    taken and fed to the next row as prev; the anchor is the first row's prev.
+
+    hn: [n, hidden] the rows after the last norm; logits: [n, vocab].
+    Returns (chosen, plain) uint32 [n]: the selected tokens and each row's own
+    top token.
+    """
+    g = model.g
+    hp = np.asarray(hn, dtype=F64) @ model.sel.T  # S . h: [n, rank]
+    prev, chosen, plain = int(anchor), [], []
+    for j in range(hp.shape[0]):
+        cand = top_k(np.asarray(logits[j], dtype=np.float32), g.selector_top)
+        plain.append(cand[0][1])
+        pc = model.book_p[prev] * hp[j]
+        best_s, best_t = -math.inf, cand[0][1]
+        for unary, tok in cand:
+            s = unary + float(pc @ model.book_c[tok])
+            if s > best_s:
+                best_s, best_t = s, tok
+        prev = best_t
+        chosen.append(prev)
+    return np.array(chosen, dtype=np.uint32), np.array(plain, dtype=np.uint32)

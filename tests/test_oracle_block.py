@@ -315,3 +315,50 @@ def test_convolution_is_causal_over_the_block_rows(model):
     long_, _ = block(mc, s, 6, 9, block_len=g.block)
     short, _ = block(mc, s, 6, 9, block_len=4)
     np.testing.assert_allclose(long_[:3], short, rtol=1e-12, atol=1e-13 * np.max(np.abs(short)))
+
+
+# ------------------------------------------------------------ candidate selector
+def _sel_model(top, rank=2):
+    g = dataclasses.replace(W.WORKLOADS["tiny_f32"].geom, selector_rank=rank, selector_top=top)
+    return g, W.make_weights(g)
+
+
+def test_selector_with_a_zero_codebook_keeps_each_rows_top():
+    """C = 0: every candidate scores its own logit, so the selector returns
+    each row's top token (the plain argmax, first of equals)."""
+    g, w = _sel_model(top=8)
+    w["successor_codebook"][:] = 0
+    m = OracleModel(g, w)
+    s = OracleSeq(m)
+    s.append(0, W.make_taps(g, 12))
+    logits, toks = block(m, s, 7, 12)
+    np.testing.assert_array_equal(toks, np.argmax(logits.astype(np.float32), axis=1))
+
+
+def test_selector_chains_the_previous_choice():
+    """Codebooks built so that the anchor's predecessor row points every
+    candidate score at token t1 and t1's at t2 (C rows one-hot, other P rows
+    zero): the first two rows choose t1 then t2 over any logit, the rest keep
+    their own top token -- the anchor feeds row 0 and each choice the next."""
+    g_vocab = W.WORKLOADS["tiny_f32"].geom.vocab
+    g, w = _sel_model(top=g_vocab)
+    m0 = OracleModel(g, w)
+    s0 = OracleSeq(m0)
+    s0.append(0, W.make_taps(g, 12))
+    anchor = 7
+    logits, _, hn = block(m0, s0, anchor, 12, return_hidden=True)
+    hp = hn[1:] @ w["selector_projection"].astype(np.float64).T
+    plain = np.argmax(logits.astype(np.float32), axis=1)
+    t1, t2 = [t for t in range(g_vocab) if t not in set(plain.tolist()) | {anchor}][:2]
+    P = np.zeros((g.vocab, 2), dtype=np.float16)
+    C = np.zeros((g.vocab, 2), dtype=np.float16)
+    C[t1, 0] = C[t2, 1] = 1
+    P[anchor, 0] = np.float16(1e4 * np.sign(hp[0, 0]))
+    P[t1, 1] = np.float16(1e4 * np.sign(hp[1, 1]))
+    w["predecessor_codebook"], w["successor_codebook"] = P, C
+    m = OracleModel(g, w)
+    s = OracleSeq(m)
+    s.append(0, W.make_taps(g, 12))
+    _, toks = block(m, s, anchor, 12)
+    assert toks[0] == t1 and toks[1] == t2
+    np.testing.assert_array_equal(toks[2:], plain[2:])

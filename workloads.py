@@ -12,6 +12,8 @@ Recipe (all draws float32, all seeded, no dataset):
   1 + N(0, 0.02), so the gain multiply is exercised;
 * a row convolution's base kernels (when the geometry has one): N(0, 0.02),
   plus 1 at row offset 0; its kernel projections N(0, 0.02);
+* the candidate selector (when the geometry has one): its projection
+  N(0, 0.02), its two codebooks N(0, 1) stored as float16;
 * context taps: N(0, 1);
 * anchor tokens: uniform over the vocabulary.
 
@@ -37,6 +39,7 @@ ANCHOR_SEED = 2
 # tensor ids of the model-wide tensors; layer l's tensors are
 # LAYER_BASE + LAYER_STRIDE * l + (offset in LAYER_TENSORS)
 TID_FC, TID_HIDDEN_NORM, TID_NORM, TID_EMBED, TID_HEAD = 0, 1, 2, 3, 4
+TID_SELECTOR, TID_BOOK_P, TID_BOOK_C = 5, 6, 7
 LAYER_BASE, LAYER_STRIDE = 16, 16
 LAYER_TENSORS = ("in_norm", "post_norm", "q_norm", "k_norm", "q", "k", "v", "o", "gate", "up", "down",
                  "attn_conv_base", "attn_conv_proj", "mlp_conv_base", "mlp_conv_proj")
@@ -63,6 +66,8 @@ class Geometry:
     quant: int = 0  # 0: all f32; 1: 4-bit g32 matrices, int8 head, int8 activations
     mask_token: int | None = None  # None: vocab - 1
     window: int = 0  # positions a block row sees back; 0 = all
+    selector_rank: int = 0  # the candidate selector's rank; 0: none (each row's own top token)
+    selector_top: int = 0  # candidates a row's selector re-scores
     conv_kernel: int = 0  # rows of the DFlash 2 row convolution; 0: none (the sub-layers unwrapped)
     conv_group: int = 0  # hidden columns that share one dynamic kernel value
     windows: tuple = ()  # the same per layer where layers differ (0: all); empty: `window` for every layer
@@ -195,6 +200,11 @@ def make_weights(g: Geometry, seed: int = WEIGHT_SEED, std: float = 0.02) -> dic
         "embed": draw(TID_EMBED, "embed", (g.vocab, hs)),
         "head": draw(TID_HEAD, "head", (g.vocab, hs)),
     }
+    if g.selector_rank:
+        w["selector_projection"] = draw(TID_SELECTOR, "selector_projection", (g.selector_rank, hs))
+        # the codebooks as the page stores them: f16 [vocab][rank], N(0, 1)
+        for tid, name in ((TID_BOOK_P, "predecessor_codebook"), (TID_BOOK_C, "successor_codebook")):
+            w[name] = normal(seed, tid, (g.vocab, g.selector_rank)).astype(np.float16)
     shapes = weight_shapes(g)
     w["layers"] = [{name: draw(layer_tid(l, name), name, shapes[name]) for name in LAYER_TENSORS if name in shapes}
                    for l in range(g.layers)]
