@@ -78,6 +78,8 @@ def geometry_struct(g) -> _abi.Geometry:
     s.quant = int(getattr(g, "quant", 0))
     s.eps = float(getattr(g, "eps", 1e-6))
     s.rope_theta = float(getattr(g, "rope_theta", 1e6))
+    s.selector_rank = int(getattr(g, "selector_rank", 0))
+    s.selector_top = int(getattr(g, "selector_top", 0))
     s.conv_kernel = int(getattr(g, "conv_kernel", 0))
     s.conv_group = int(getattr(g, "conv_group", 0))
     # per-layer lists: arrays kept alive on the struct until dflash_init has copied them
@@ -141,13 +143,23 @@ class Model:
         if not on_device:
             weights = {**weights, "layers": [{k: np.ascontiguousarray(v, dtype=np.float32) for k, v in lw.items()}
                                              for lw in weights["layers"]]}
-            for k in ("fc", "hidden_norm", "norm", "embed", "head"):
-                weights[k] = np.ascontiguousarray(weights[k], dtype=np.float32)
+            for k in ("fc", "hidden_norm", "norm", "embed", "head", "selector_projection"):
+                if k in weights:
+                    weights[k] = np.ascontiguousarray(weights[k], dtype=np.float32)
+            for k in ("predecessor_codebook", "successor_codebook"):
+                if k in weights:
+                    weights[k] = np.ascontiguousarray(weights[k], dtype=np.float16)
         self._keep = weights  # alive during init
         w = _abi.Weights()
         FP = C.POINTER(C.c_float)
         for k in ("fc", "hidden_norm", "norm", "embed", "head"):
             setattr(w, k, C.cast(C.c_void_p(_ptr(weights[k])), FP))
+        if self.gs.selector_rank > 0:
+            if "selector_projection" in weights:
+                w.selector_projection = C.cast(C.c_void_p(_ptr(weights["selector_projection"])), FP)
+            for k in ("predecessor_codebook", "successor_codebook"):
+                if k in weights:
+                    setattr(w, k, _ptr(weights[k]))
         arrays = []
         names = LAYER_TENSORS + (CONV_TENSORS if self.gs.conv_kernel > 0 else ())
         for name in names:

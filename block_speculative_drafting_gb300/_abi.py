@@ -34,7 +34,8 @@ class Geometry(C.Structure):
                 ("kv_heads", C.c_int32), ("head_dim", C.c_int32), ("vocab", C.c_int32), ("block", C.c_int32),
                 ("n_taps", C.c_int32), ("mask_token", C.c_int32), ("window", C.c_int32), ("quant", C.c_int32),
                 ("eps", C.c_float), ("rope_theta", C.c_double), ("windows", C.POINTER(C.c_int32)),
-                ("no_rope", C.POINTER(C.c_int32)), ("conv_kernel", C.c_int32), ("conv_group", C.c_int32)]
+                ("no_rope", C.POINTER(C.c_int32)), ("conv_kernel", C.c_int32), ("conv_group", C.c_int32),
+                ("selector_rank", C.c_int32), ("selector_top", C.c_int32)]
 
 
 _FP = C.POINTER(C.c_float)
@@ -45,7 +46,9 @@ class Weights(C.Structure):
     _fields_ = [("fc", _FP), ("hidden_norm", _FP), ("norm", _FP), ("embed", _FP), ("head", _FP),
                 ("in_norm", _FPP), ("post_norm", _FPP), ("q_norm", _FPP), ("k_norm", _FPP), ("q", _FPP),
                 ("k", _FPP), ("v", _FPP), ("o", _FPP), ("gate", _FPP), ("up", _FPP), ("down", _FPP),
-                ("attn_conv_base", _FPP), ("attn_conv_proj", _FPP), ("mlp_conv_base", _FPP), ("mlp_conv_proj", _FPP)]
+                ("attn_conv_base", _FPP), ("attn_conv_proj", _FPP), ("mlp_conv_base", _FPP), ("mlp_conv_proj", _FPP),
+                ("selector_projection", _FP), ("predecessor_codebook", C.c_void_p),
+                ("successor_codebook", C.c_void_p)]
 
 
 _VP = C.c_void_p

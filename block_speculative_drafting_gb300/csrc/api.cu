@@ -80,6 +80,10 @@ struct dflash_model {
     // latter on the device (kv_append)
     std::vector<int32_t> win, norope;
     int* rot_dev = nullptr;
+    // the candidate selector: S [rank][H] f32, codebooks P, C [V][rank] f16
+    float* sel = nullptr;
+    __half *book_p = nullptr, *book_c = nullptr;
+    DevBuf hn, hp, cand, plain;  // its scratch: normed rows, their projection, candidates, own top tokens
     bool use_chain = false;         // run a block's (and a short append's) steps as chain programs
     bool use_tc = true;             // matmuls of more than 16 rows on the tcgen05 kernel (DFLASH_TC=0: mma.sync)
     bool use_dense = true;          // ... from dense f16 weight copies (DFLASH_DENSE=0: dequantise in the kernel)
@@ -304,6 +308,9 @@ std::string geometry_problem(const dflash_geometry& g) {
     if (g.mask_token < 0 || g.mask_token >= g.vocab) return "mask_token outside [0, vocab)";
     if (g.window < 0) return "window < 0";
     if (g.conv_kernel < 0 || g.conv_kernel > 64) return "conv_kernel outside [0, 64]";
+    if (g.selector_rank < 0 || g.selector_rank > 4096) return "selector_rank outside [0, 4096]";
+    if (g.selector_rank > 0 && (g.selector_top < 1 || g.selector_top > 32 || g.selector_top > g.vocab))
+        return "selector_top outside [1, min(32, vocab)]";
     if (g.conv_kernel > 0 && (g.conv_group < 4 || g.conv_group % 4 || g.hidden % g.conv_group))
         return "conv_group must be a multiple of 4 dividing hidden";
     if (g.windows)
@@ -475,6 +482,16 @@ int build_model(dflash_model* m, const dflash_weights* w, bool on_dev, cudaStrea
         CK(m, dalloc(m, &m->head_f, (size_t)g.vocab * H));
         CK(m, copy_f32(m, m->head_f, w->head, (size_t)g.vocab * H, on_dev));
     }
+    if (g.selector_rank > 0) {
+        const size_t rk = (size_t)g.selector_rank, nb = (size_t)g.vocab * rk;
+        CK(m, dalloc(m, &m->sel, rk * H));
+        CK(m, copy_f32(m, m->sel, w->selector_projection, rk * H, on_dev));
+        const cudaMemcpyKind kind = on_dev ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
+        CK(m, dalloc(m, &m->book_p, nb));
+        CK(m, cudaMemcpy(m->book_p, w->predecessor_codebook, nb * sizeof(__half), kind));
+        CK(m, dalloc(m, &m->book_c, nb));
+        CK(m, cudaMemcpy(m->book_c, w->successor_codebook, nb * sizeof(__half), kind));
+    }
     // layers
     m->layers.resize(L);
     std::vector<const float*> knorm_ptrs(L);
@@ -540,7 +557,7 @@ int build_model(dflash_model* m, const dflash_weights* w, bool on_dev, cudaStrea
     return DFLASH_OK;
 }
 
-bool weights_complete(const dflash_weights* w, int L, bool conv) {
+bool weights_complete(const dflash_weights* w, int L, bool conv, bool sel) {
     if (!w->fc || !w->hidden_norm || !w->norm || !w->embed || !w->head) return false;
     const float* const* per[] = {w->in_norm, w->post_norm, w->q_norm, w->k_norm, w->q, w->k,
                                  w->v,       w->o,         w->gate,   w->up,     w->down};
@@ -549,6 +566,7 @@ bool weights_complete(const dflash_weights* w, int L, bool conv) {
         for (int l = 0; l < L; ++l)
             if (!a[l]) return false;
     }
+    if (sel && (!w->selector_projection || !w->predecessor_codebook || !w->successor_codebook)) return false;
     if (conv) {
         const float* const* cv[] = {w->attn_conv_base, w->attn_conv_proj, w->mlp_conv_base, w->mlp_conv_proj};
         for (auto a : cv) {
@@ -706,6 +724,26 @@ int run_head(dflash_model* m, QAct xh, int D, float* logit_out, unsigned long lo
            head_stream(m->head_p, m->head_scale, g.vocab, H / kI8KStep, xh, D, logit_out, g.vocab, keys, m->num_sms,
                        m->err_dev, st));
     }
+    return DFLASH_OK;
+}
+
+// The candidate selector after the head: the rows after the last norm (f32),
+// their projection S . hn, each row's top candidates from its logits, then
+// the choices row by row per sequence (into tok_out).
+int run_selector(dflash_model* m, cudaStream_t st, const float* h, RowMap drafts, int D, int n_seqs, int B,
+                 const float* logits, const uint32_t* anchors, uint32_t* tok_out) {
+    const dflash_geometry& g = m->g;
+    const int H = g.hidden, rank = g.selector_rank, top = g.selector_top;
+    float* hn = P<float>(m->hn);
+    float* hp = P<float>(m->hp);
+    unsigned long long* cand = P<unsigned long long>(m->cand);
+    KL(m, "rms_f32", 1, (double)D * H * 8, st,
+       rms_rows(h, H, drafts, D, H, m->norm, g.eps, hn, H, nullptr, nullptr, 0, st));
+    KL(m, "linear_f32", 1, f32_bytes_of(rank, H, D, false), st, linear_f32(m->sel, rank, H, hn, H, D, hp, rank, false, st));
+    KL(m, "topk_rows", 1, (double)D * g.vocab * 4, st, topk_rows(logits, g.vocab, g.vocab, D, top, cand, st));
+    KL(m, "select", 1, (double)D * top * rank * 4, st,
+       select_tokens(cand, top, hp, rank, m->book_p, m->book_c, g.vocab, anchors, n_seqs, B - 1, tok_out,
+                     P<uint32_t>(m->plain), st));
     return DFLASH_OK;
 }
 
@@ -1004,7 +1042,7 @@ int dflash_init(const dflash_geometry* geom, const dflash_weights* weights, int 
     if (!geom || !weights) return set_err(nullptr, DFLASH_EINVAL, "geometry or weights is NULL");
     std::string why = geometry_problem(*geom);
     if (!why.empty()) return set_err(nullptr, DFLASH_EGEOM, "unsupported geometry: " + why);
-    if (!weights_complete(weights, geom->layers, geom->conv_kernel > 0))
+    if (!weights_complete(weights, geom->layers, geom->conv_kernel > 0, geom->selector_rank > 0))
         return set_err(nullptr, DFLASH_EINVAL, "a weight pointer is NULL");
     dflash_model* m = new (std::nothrow) dflash_model();
     if (!m) return set_err(nullptr, DFLASH_ENOMEM, "host allocation failed");
@@ -1050,7 +1088,8 @@ void dflash_free(dflash_model* m) {
     for (void* p : m->owned) cudaFree(p);
     for (DevBuf* b : {&m->h, &m->xq, &m->xs, &m->qkv, &m->y, &m->gu, &m->logits, &m->keys, &m->toks, &m->part,
                       &m->anchors, &m->pos0, &m->aseqs, &m->rope, &m->a_taps, &m->a_codes, &m->a_scale, &m->a_t,
-                      &m->a_kv, &m->a_pos, &m->x16, &m->trace_buf, &m->cx, &m->cd, &m->co})
+                      &m->a_kv, &m->a_pos, &m->x16, &m->trace_buf, &m->cx, &m->cd, &m->co, &m->hn, &m->hp,
+                      &m->cand, &m->plain})
         free_buf(*b);
     delete m;
 }
@@ -1237,6 +1276,12 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
     CK(m, ensure_m(m, m->pos0, (size_t)n_seqs * sizeof(int64_t)));
     CK(m, ensure_m(m, m->rope, (size_t)R * (hd / 2) * sizeof(float2)));
     CK(m, ensure_m(m, m->aseqs, (size_t)g.layers * n_seqs * sizeof(AttnSeq)));
+    if (g.selector_rank > 0) {
+        CK(m, ensure_m(m, m->hn, (size_t)D * H * sizeof(float)));
+        CK(m, ensure_m(m, m->hp, (size_t)D * g.selector_rank * sizeof(float)));
+        CK(m, ensure_m(m, m->cand, (size_t)D * g.selector_top * sizeof(unsigned long long)));
+        CK(m, ensure_m(m, m->plain, (size_t)D * sizeof(uint32_t)));
+    }
     if (g.conv_kernel > 0) {
         CK(m, ensure_m(m, m->cx, (size_t)R * H * sizeof(float)));
         CK(m, ensure_m(m, m->cd, (size_t)R * 2 * g.conv_kernel * (H / g.conv_group) * sizeof(float)));
@@ -1253,7 +1298,7 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
         CK(m, ensure_m(m, m->logits, (size_t)D * g.vocab * sizeof(float)));
         logit_out = P<float>(m->logits);
     }
-    if (!quant && !logit_out) {  // the f32 head needs its logits for the argmax
+    if ((!quant || g.selector_rank > 0) && !logit_out) {  // the f32 head's argmax and the selector read the logits
         CK(m, ensure_m(m, m->logits, (size_t)D * g.vocab * sizeof(float)));
         logit_out = P<float>(m->logits);
     }
@@ -1287,7 +1332,7 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
     RowMap drafts{B - 1, B, 1};
     unsigned long long* keys = P<unsigned long long>(m->keys);
     uint32_t* tok_out = (io_on_device && draft_tok) ? draft_tok : P<uint32_t>(m->toks);
-    if (quant && chain_ok(m, R) && g.conv_kernel == 0) {
+    if (quant && chain_ok(m, R) && g.conv_kernel == 0 && g.selector_rank == 0) {
         // the steps between two attentions as one chain program each:
         // [x = Q(rms(h, in_norm)); qkv = W x] before the first attention, then per
         // layer [Q(y); h += O y; x = Q(rms(h, post_norm)); gu = [G; U] x;
@@ -1501,7 +1546,10 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
            linear_f32(m->head_f, g.vocab, H, xf, maxK, D, logit_out, g.vocab, false, st));
         KL(m, "argmax_rows", 1, (double)D * g.vocab * 4, st, argmax_rows(logit_out, g.vocab, g.vocab, D, keys, st));
     }
-    KL(m, "keys_to_tokens", 1, (double)D * 12, st, keys_to_tokens(keys, D, tok_out, st));
+    if (g.selector_rank > 0)
+        APPLY(run_selector(m, st, h, drafts, D, n_seqs, B, logit_out, anchors_dev, tok_out));
+    else
+        KL(m, "keys_to_tokens", 1, (double)D * 12, st, keys_to_tokens(keys, D, tok_out, st));
     return DFLASH_OK;
     };
     uint32_t* tok_out = (io_on_device && draft_tok) ? draft_tok : P<uint32_t>(m->toks);

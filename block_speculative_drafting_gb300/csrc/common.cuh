@@ -308,6 +308,8 @@ DF_DEV uint32_t float_order_key(float f) {
     uint32_t b = __float_as_uint(f);
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
+// The inverse of float_order_key.
+DF_DEV float float_of_order_key(uint32_t k) { return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k); }
 // (value, index) -> u64 key: larger value wins, then the lower index.
 DF_DEV unsigned long long argmax_key(float f, uint32_t idx) {
     return ((unsigned long long)float_order_key(f) << 32) | (unsigned long long)(0xFFFFFFFFu - idx);

@@ -262,4 +262,154 @@ int keys_to_tokens(const unsigned long long* keys, int T, uint32_t* tokens, cuda
     return (int)launch(keys_to_tokens_kernel, dim3((T + 255) / 256), dim3(256), 0, st, keys, T, tokens);
 }
 
+// ------------------------------------------------------------------ candidate selector
+// Per row, its K largest logits as argmax keys, largest first (the lower
+// index first among equal values: page "cortiq-engine 0.8.71 — src/dflash.rs",
+// `top_k`).  A CTA a row: each thread keeps the K best of its strided share
+// (a compare-exchange pass a candidate), which holds every row-wide top-K
+// element of that share; then k rounds of a CTA-wide maximum over the
+// threads' lists, each round taking out its winner.
+template <int K>
+struct TopShape {
+    static constexpr int kThreads = K >= 32 ? 128 : 256;  // the lists in 32 KB of shared memory at most
+};
+template <int K>
+__global__ void __launch_bounds__(TopShape<K>::kThreads) topk_rows_kernel(const float* __restrict__ logits, int ldl,
+                                                                           int V, int k,
+                                                                           unsigned long long* __restrict__ out) {
+    constexpr int kTopThreads = TopShape<K>::kThreads;
+    __shared__ unsigned long long cand[kTopThreads * K];
+    __shared__ unsigned long long red[kTopThreads / 32];
+    const int t = blockIdx.x, tid = threadIdx.x;
+    pdl_trigger();
+    pdl_wait();
+    unsigned long long mine[K];
+#pragma unroll
+    for (int i = 0; i < K; ++i) mine[i] = 0ull;  // no real key is 0 (its index part is below 2^32 - 1 - V)
+    const float* row = logits + (int64_t)t * ldl;
+    for (int n = tid; n < V; n += kTopThreads) {
+        unsigned long long x = argmax_key(row[n], (uint32_t)n);
+        if (x <= mine[K - 1]) continue;
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+            const unsigned long long hi = max(x, mine[i]), lo = min(x, mine[i]);
+            mine[i] = hi;
+            x = lo;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < K; ++i) cand[tid * K + i] = mine[i];
+    __syncthreads();
+    for (int r = 0; r < k; ++r) {
+        unsigned long long b = 0ull;
+#pragma unroll
+        for (int i = 0; i < K; ++i) b = max(b, cand[tid * K + i]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) b = max(b, __shfl_xor_sync(0xffffffffu, b, o));
+        if ((tid & 31) == 0) red[tid >> 5] = b;
+        __syncthreads();
+        b = 0ull;
+#pragma unroll
+        for (int w = 0; w < kTopThreads / 32; ++w) b = max(b, red[w]);
+        if (tid == 0) out[(int64_t)t * k + r] = b;
+#pragma unroll
+        for (int i = 0; i < K; ++i)
+            if (cand[tid * K + i] == b) cand[tid * K + i] = 0ull;  // keys are unique: its one owner
+        __syncthreads();
+    }
+}
+
+int topk_rows(const float* logits, int ldl, int V, int T, int k, unsigned long long* out, cudaStream_t st) {
+    if (T <= 0) return 0;
+    if (k < 1 || k > 32 || k > V) return (int)cudaErrorInvalidValue;
+    if (k <= 8)
+        return (int)launch(topk_rows_kernel<8>, dim3(T), dim3(TopShape<8>::kThreads), 0, st, logits, ldl, V, k, out);
+    if (k <= 16)
+        return (int)launch(topk_rows_kernel<16>, dim3(T), dim3(TopShape<16>::kThreads), 0, st, logits, ldl, V, k, out);
+    return (int)launch(topk_rows_kernel<32>, dim3(T), dim3(TopShape<32>::kThreads), 0, st, logits, ldl, V, k, out);
+}
+
+// The selector's choices, a warp a sequence (its rows one after another):
+// row j's candidates (lane c: the c-th) scored unary + sum_i (P[prev][i] *
+// hp[j][i]) * C[tok][i] in f32 as the page sums (products rounded, added in
+// order i), the best taken (the first candidate among equals) and fed to the
+// next row; the anchor is the first row's prev.
+// (An anchor outside [0, V), possible only for anchors already on the device,
+// has a predecessor row of zeros.)
+__global__ void select_kernel(const unsigned long long* __restrict__ cand, int k, const float* __restrict__ hp,
+                              int rank, const __half* __restrict__ book_p, const __half* __restrict__ book_c, int V,
+                              const uint32_t* __restrict__ anchors, int n_seqs, int rows, uint32_t* __restrict__ chosen,
+                              uint32_t* __restrict__ plain) {
+    const int s = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    pdl_trigger();
+    pdl_wait();
+    if (s >= n_seqs) return;
+    uint32_t prev = anchors[s];
+    for (int j = 0; j < rows; ++j) {
+        const int r = s * rows + j;
+        float best = -INFINITY;
+        int best_c = 0;
+        uint32_t best_t = 0;
+        for (int c0 = 0; c0 < k; c0 += 32) {
+            const int c = c0 + lane;
+            float sc = -INFINITY;
+            uint32_t tok = 0;
+            if (c < k) {
+                const unsigned long long key = cand[(int64_t)r * k + c];
+                tok = 0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull);
+                const float unary = float_of_order_key((uint32_t)(key >> 32));
+                const __half* pp = book_p + (int64_t)prev * rank;
+                const __half* cc = book_c + (int64_t)tok * rank;
+                const float* hh = hp + (int64_t)r * rank;
+                float acc = 0.f;
+                if (prev < (uint32_t)V)
+                    for (int i = 0; i < rank; ++i)
+                        acc = __fadd_rn(acc, __fmul_rn(__fmul_rn(__half2float(pp[i]), hh[i]), __half2float(cc[i])));
+                sc = __fadd_rn(unary, acc);
+            }
+            // the best of these 32 (the lowest candidate among equals), then against the earlier ones
+            float v = sc;
+            int vc = c < k ? c : 0x7FFFFFFF;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+                const int oc = __shfl_xor_sync(0xffffffffu, vc, o);
+                if (ov > v || (ov == v && oc < vc)) {
+                    v = ov;
+                    vc = oc;
+                }
+            }
+            const uint32_t vt = __shfl_sync(0xffffffffu, tok, vc & 31);
+            if (c0 == 0) {
+                // the first candidate stands unless one scores strictly higher
+                best_t = __shfl_sync(0xffffffffu, tok, 0);
+                best_c = 0;
+                if (v > -INFINITY) {
+                    best = v;
+                    best_c = vc;
+                    best_t = vt;
+                }
+            } else if (v > best) {
+                best = v;
+                best_c = vc;
+                best_t = vt;
+            }
+            if (c0 == 0 && lane == 0) plain[r] = tok;
+        }
+        (void)best_c;
+        prev = best_t;
+        if (lane == 0) chosen[r] = prev;
+    }
+}
+
+int select_tokens(const unsigned long long* cand, int k, const float* hp, int rank, const __half* book_p,
+                  const __half* book_c, int V, const uint32_t* anchors, int n_seqs, int rows, uint32_t* chosen,
+                  uint32_t* plain, cudaStream_t st) {
+    if (n_seqs <= 0 || rows <= 0) return 0;
+    if (k < 1 || k > 32 || rank < 1) return (int)cudaErrorInvalidValue;
+    const int warps = 4;
+    return (int)launch(select_kernel, dim3((n_seqs + warps - 1) / warps), dim3(32 * warps), 0, st, cand, k, hp, rank,
+                       book_p, book_c, V, anchors, n_seqs, rows, chosen, plain);
+}
+
 }  // namespace dflash

@@ -118,6 +118,15 @@ int linear_f32(const float* W, int N, int K, const float* x, int ldx, int T, flo
 int argmax_rows(const float* logits, int ldl, int V, int T, unsigned long long* keys, cudaStream_t st);
 // tokens[t] = index encoded in keys[t].
 int keys_to_tokens(const unsigned long long* keys, int T, uint32_t* tokens, cudaStream_t st);
+// The candidate selector: per row the k (<= 32, <= V) largest logits as
+// argmax keys, largest first (out [T][k]); then per sequence, its `rows` rows
+// in order, the choices (chosen) and each row's own top token (plain) from
+// the candidates, hp [n_seqs*rows][rank] (the rows' projection) and the f16
+// codebooks [V][rank].
+int topk_rows(const float* logits, int ldl, int V, int T, int k, unsigned long long* out, cudaStream_t st);
+int select_tokens(const unsigned long long* cand, int k, const float* hp, int rank, const __half* book_p,
+                  const __half* book_c, int V, const uint32_t* anchors, int n_seqs, int rows, uint32_t* chosen,
+                  uint32_t* plain, cudaStream_t st);
 
 // ---- the chain: a persistent kernel (one CTA per SM) that runs a short
 // program of dependent stages of the block's rows, with a grid-wide barrier

@@ -85,6 +85,13 @@ typedef struct dflash_seq dflash_seq;     /* one sequence's context K/V */
  * stage s of rows z is y[i] = sum_{o < min(kn, i + 1)} (base[s][o] +
  * d[i][s][o][group]) * z[i - o] over a block's rows i.  conv_kernel = 0: the
  * sub-layers unwrapped (the same as kn = 1, base 1, proj 0).
+ * Candidate selector (page "cortiq-engine 0.8.71 — src/dflash.rs", `select`,
+ * `top_k`): with selector_rank > 0 the draft tokens are chosen row by row:
+ * row j's selector_top largest logits (the lower index first among equals)
+ * scored logit + (P[prev] * (S . hn_j)) . C[candidate] in f32 (products
+ * rounded, summed in order), the first best taken; prev is the anchor for
+ * row 1 and the previous row's choice after it (hn: the rows after the last
+ * norm, f32).
  * windows / no_rope point to `layers` entries each, or are NULL (windows:
  * `window` for every layer; no_rope: every layer rotary).  dflash_init
  * copies them; dflash_geometry_of returns pointers to the model's copies
@@ -110,6 +117,8 @@ typedef struct {
     int32_t conv_kernel;    /* rows of the row convolution around each sub-layer; 0 = none */
     int32_t conv_group;     /* columns sharing a dynamic kernel value (conv_kernel > 0: a multiple of 4
                                dividing hidden) */
+    int32_t selector_rank;  /* the candidate selector's rank; 0 = none (draft tokens: each row's argmax) */
+    int32_t selector_top;   /* candidates it re-scores a row (selector_rank > 0: 1 .. 32, <= vocab) */
 } dflash_geometry;
 
 /*
@@ -149,6 +158,12 @@ typedef struct {
     const float* const* attn_conv_proj;
     const float* const* mlp_conv_base;
     const float* const* mlp_conv_proj;
+    /* the candidate selector (selector_rank > 0; NULL otherwise): S
+     * [selector_rank][H] f32, and the predecessor (P) and successor (C)
+     * codebooks [V][selector_rank] as IEEE half bit patterns */
+    const float* selector_projection;
+    const uint16_t* predecessor_codebook;
+    const uint16_t* successor_codebook;
 } dflash_weights;
 
 /*

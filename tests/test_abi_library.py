@@ -45,7 +45,8 @@ def test_geometry_rejected_before_any_device_work():
     import block_speculative_drafting_gb300 as dfl
     import workloads as W
     bad = [dict(head_dim=96), dict(hidden=200), dict(heads=6, kv_heads=4), dict(window=-1), dict(windows=(4, -2)),
-           dict(block=1), dict(conv_kernel=-1), dict(conv_kernel=2, conv_group=6), dict(conv_kernel=2, conv_group=96)]
+           dict(block=1), dict(conv_kernel=-1), dict(conv_kernel=2, conv_group=6), dict(conv_kernel=2, conv_group=96),
+           dict(selector_rank=4, selector_top=0), dict(selector_rank=4, selector_top=33)]
     base = W.WORKLOADS["tiny_f32"].geom
     import dataclasses
     w = W.make_weights(base)

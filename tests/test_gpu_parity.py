@@ -384,6 +384,43 @@ def test_row_convolution_matches_oracle(name, forced, variants):
     sc.run(forced).check(forced)
 
 
+def test_selector_matches_oracle_forced():
+    """The candidate selector after the head (page 1's select): with the
+    oracle's quantisation decisions taken, the library's choices equal the
+    oracle's, in a block of two sequences and a shorter block of one."""
+    p = Pair("small_q4", selector_rank=16, selector_top=8)
+    g = p.g
+    sc = Script(p, 2, 64)
+    sc.append(0, 0, W.make_taps(g, 30))
+    sc.append(1, 0, W.make_taps(g, 17, call_id=5))
+    anchors = [int(a) for a in W.make_anchors(g, 2)]
+    sc.block([0, 1], anchors, [30, 17], g.block)
+    sc.block([0], [anchors[1]], [30], 6)
+    sc.run(True).check(True)
+
+
+@pytest.mark.parametrize("top", [1, 8, 32])
+def test_selector_choices_from_the_librarys_logits(top):
+    """All-f32 drafter: the library's choices equal the oracle's selection run
+    on the library's own logits and the oracle's normed rows (what remains
+    is the f32 scoring against the oracle's f64: far from any tie here)."""
+    from oracle import select
+    p = Pair("tiny_f32", selector_rank=24, selector_top=top)
+    g = p.g
+    seq = p.gpu.new_sequence(64)
+    taps = W.make_taps(g, 20)
+    p.gpu.ctx_append(seq, 0, taps)
+    osq = OracleSeq(p.ora)
+    osq.append(0, taps)
+    for anchor, bl in ((11, g.block), (3, 4)):
+        logits, toks = p.gpu.block([seq], [anchor], [20], bl)
+        ref_logits, _, hn = block(p.ora, osq, anchor, 20, bl, return_hidden=True)
+        assert np.max(np.abs(logits[0] - ref_logits)) <= 1e-4 * np.max(np.abs(ref_logits))
+        chosen, plain = select(p.ora, hn[1:], logits[0], anchor)
+        np.testing.assert_array_equal(toks[0], chosen)
+    seq.close()
+
+
 def test_geometry_lists_round_trip():
     """dflash_geometry_of gives back the per-layer windows and no-rope flags
     the model was made with."""

@@ -114,11 +114,13 @@ WORKLOADS = {
     "qwen3_8b_ctx32768": Workload("qwen3_8b_ctx32768", Geometry(**QWEN3_8B_DRAFT), ctx=32768),
     # 32 independent sequences, context 4096 each
     "qwen3_8b_batch32_ctx4096": Workload("qwen3_8b_batch32_ctx4096", Geometry(**QWEN3_8B_DRAFT), ctx=4096, n_seqs=32),
-    # the single-sequence block with a DFlash 2 row convolution around every
-    # sub-layer (4 rows, 32 groups of 128 columns: no config fixes one, so
-    # this geometry is this build's choice)
-    "qwen3_8b_ctx2048_conv": Workload("qwen3_8b_ctx2048_conv", Geometry(**QWEN3_8B_DRAFT, conv_kernel=4,
-                                                                        conv_group=128), ctx=2048),
+    # the single-sequence block with the DFlash 2 pieces no config fixes: a
+    # row convolution around every sub-layer (4 rows, 32 groups of 128
+    # columns) and the candidate selector (rank 64, 8 candidates) -- sizes of
+    # this build's choosing
+    "qwen3_8b_ctx2048_dflash2": Workload("qwen3_8b_ctx2048_dflash2",
+                                         Geometry(**QWEN3_8B_DRAFT, conv_kernel=4, conv_group=128, selector_rank=64,
+                                                  selector_top=8), ctx=2048),
     # one append of 8192 target rows
     "qwen3_8b_prefill8192": Workload("qwen3_8b_prefill8192", Geometry(**QWEN3_8B_DRAFT), ctx=0, prefill=8192),
     # the same kernels on 1024 rows: the small case for profiler captures
