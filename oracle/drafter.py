@@ -252,6 +252,13 @@ class OracleSeq:
     # the library's append pass, so that traced decisions line up one to one.
     ROWS_PER_PASS = 8192
 
+    # rows that may wait in the queue before the oldest are settled, and the
+    # granule they are settled in (page "cortiq-engine 0.8.71 —
+    # src/dflash.rs": `PENDING_ROWS`, `CONTEXT_CHUNK`, `BLOCK_SLACK`)
+    PENDING_ROWS = 512
+    CONTEXT_CHUNK = 64
+    BLOCK_SLACK = 256
+
     def __init__(self, model):
         self.m = model
         g = model.g
@@ -260,12 +267,15 @@ class OracleSeq:
         self.k = [np.zeros((g.kv_heads, 0, g.head_dim)) for _ in range(g.layers)]
         self.v = [np.zeros((g.kv_heads, 0, g.head_dim)) for _ in range(g.layers)]
         self.dropped = [0] * g.layers
+        self.pending = np.zeros((0, g.tap_width), dtype=np.float32)  # queued rows, not yet context
 
     # -- positions (``Drafter::next_position``, ``truncate``, ``reset``) --
     def next_position(self):
-        return self.first + self.len
+        return self.first + self.len + self.pending.shape[0]
 
     def truncate(self, pos):
+        held = self.first + self.len
+        self.pending = self.pending[:max(pos - held, 0)]
         keep = min(max(pos - self.first, 0), self.len)
         for li in range(self.m.g.layers):
             rows = max(keep - self.dropped[li], 0)
@@ -290,7 +300,11 @@ class OracleSeq:
             self.first = pos
         else:
             self.truncate(pos)
-        self._settle(self.first + self.len, taps)
+        # queued rows still held go first, all in one settle (`push_context`
+        # is the queue then a settle; the queue's limit would only split the
+        # same rows into two settles)
+        rows, self.pending = np.concatenate([self.pending, taps]), self.pending[:0]
+        self._settle(self.first + self.len, rows)
 
     def project(self, pos, taps):
         """The context rows' keys and values: t = rms(fc . taps, hidden_norm);
@@ -310,6 +324,36 @@ class OracleSeq:
             ks.append(k)
             vs.append(v)
         return ks, vs
+
+    def queue(self, pos, taps):
+        """``append`` put off (`queue_context`): the rows wait until a block
+        reads the context (``settle``); past the queue's limit the oldest go
+        through at once, a multiple of the chunk granule.  The limit is the
+        page's device one: with every layer windowed, the widest window plus
+        a slack when that is more than PENDING_ROWS."""
+        g = self.m.g
+        taps = np.asarray(taps, dtype=np.float32).reshape(-1, g.tap_width)
+        if pos > self.next_position() or pos < self.first:
+            self.truncate(0)
+            self.first = pos
+        else:
+            self.truncate(pos)
+        self.pending = np.concatenate([self.pending, taps])
+        wins = [self.m.window_of(li) for li in range(g.layers)]
+        limit = self.PENDING_ROWS
+        if all(w > 0 for w in wins):
+            limit = max(self.PENDING_ROWS, max(wins) + self.BLOCK_SLACK)
+        held = self.pending.shape[0]
+        if held > limit:
+            over = min(-(-(held - limit) // self.CONTEXT_CHUNK) * self.CONTEXT_CHUNK, held)
+            rows, self.pending = self.pending[:over], self.pending[over:]
+            self._settle(self.first + self.len, rows)
+
+    def settle(self):
+        """Make every queued row context (`settle`)."""
+        if self.pending.shape[0]:
+            rows, self.pending = self.pending, self.pending[:0]
+            self._settle(self.first + self.len, rows)
 
     def _settle(self, pos, taps):
         g = self.m.g
@@ -377,6 +421,7 @@ def block(model, seq, anchor_tok, anchor_pos, block_len=None, return_hidden=Fals
     rows = g.block if block_len is None else block_len
     if not 2 <= rows <= g.block:
         raise ValueError(f"block_len {rows} outside [2, {g.block}]")
+    seq.settle()  # the queued rows become context before a block reads it
     hd, nh, kv = g.head_dim, g.heads, g.kv_heads
     scale = 1.0 / math.sqrt(hd)
     toks = [int(anchor_tok)] + [g.mask] * (rows - 1)

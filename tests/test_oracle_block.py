@@ -362,3 +362,57 @@ def test_selector_chains_the_previous_choice():
     _, toks = block(m, s, anchor, 12)
     assert toks[0] == t1 and toks[1] == t2
     np.testing.assert_array_equal(toks[2:], plain[2:])
+
+
+# ------------------------------------------------------------ context queue
+def test_queue_then_settle_equals_append(model):
+    """Rows queued in several calls and settled by the block read the same
+    context as one append (page 1's queue_context / settle): the same keys
+    and values, the same block."""
+    m, _ = model
+    taps = W.make_taps(m.g, 40)
+    a, q = OracleSeq(m), OracleSeq(m)
+    a.append(0, taps)
+    for r0 in (0, 9, 23):
+        q.queue(r0, taps[r0:r0 + (9 if r0 == 0 else 14 if r0 == 9 else 17)])
+    assert q.len == 0 and q.next_position() == 40 and q.pending.shape[0] == 40
+    la, _ = block(m, a, 3, 40)
+    lq, _ = block(m, q, 3, 40)
+    assert q.len == 40 and q.pending.shape[0] == 0
+    for x, y in zip(_kv(a), _kv(q)):
+        np.testing.assert_allclose(x, y, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(la, lq, rtol=1e-12, atol=1e-13)
+
+
+def test_queue_limit_settles_the_oldest_in_chunks(model):
+    """Past PENDING_ROWS waiting rows the oldest are settled, a multiple of 64
+    of them; with every layer windowed the limit is the widest window plus
+    the slack where that is larger."""
+    m, _ = model
+    s = OracleSeq(m)
+    s.queue(0, W.make_taps(m.g, 500))
+    assert (s.len, s.pending.shape[0]) == (0, 500)
+    s.queue(500, W.make_taps(m.g, 100, call_id=2))      # 600 waiting: 88 over -> 128 settle
+    assert (s.len, s.pending.shape[0], s.next_position()) == (128, 472, 600)
+    gw = dataclasses.replace(m.g, window=700)
+    mw = OracleModel(gw, W.make_weights(m.g))
+    sw = OracleSeq(mw)
+    sw.queue(0, W.make_taps(gw, 900))                     # limit 700 + 256 = 956: nothing settles
+    assert (sw.len, sw.pending.shape[0]) == (0, 900)
+
+
+def test_truncate_cuts_queued_rows_first(model):
+    m, _ = model
+    s = OracleSeq(m)
+    taps = W.make_taps(m.g, 30)
+    s.append(0, taps[:10])
+    s.queue(10, taps[10:30])
+    s.truncate(25)
+    assert (s.len, s.pending.shape[0], s.next_position()) == (10, 15, 25)
+    s.truncate(6)
+    assert (s.len, s.pending.shape[0], s.next_position()) == (6, 0, 6)
+    s.queue(4, taps[4:9])                                 # a held position: replaces from 4 on
+    assert (s.len, s.pending.shape[0], s.next_position()) == (4, 5, 9)
+    fresh = OracleSeq(m)
+    fresh.append(0, taps[:9])
+    np.testing.assert_allclose(block(m, s, 1, 9)[0], block(m, fresh, 1, 9)[0], rtol=1e-12, atol=1e-13)
