@@ -203,6 +203,19 @@ class Model:
         self._check(lib().dflash_ctx_append(self.handle, seq.handle, int(pos), _ptr(taps), n, 1 if on_dev else 0,
                                             _stream(stream)))
 
+    def ctx_queue(self, seq: Sequence, pos: int, taps, stream=None):
+        """ctx_append put off: the rows wait until a block (or settle) reads them."""
+        n = 0 if taps is None else int(taps.shape[0])
+        on_dev = taps is not None and _is_torch(taps)
+        if taps is not None and not on_dev:
+            taps = np.ascontiguousarray(taps, dtype=np.float32)
+        self._check(lib().dflash_ctx_queue(self.handle, seq.handle, int(pos), _ptr(taps), n, 1 if on_dev else 0,
+                                           _stream(stream)))
+
+    def settle(self, seq: Sequence, stream=None):
+        """Make every queued row of `seq` context."""
+        self._check(lib().dflash_settle(self.handle, seq.handle, _stream(stream)))
+
     def block(self, seqs, anchor_tok, anchor_pos, block_len=None, logits=None, tokens=None, want_logits=True,
               stream=None):
         """One block per sequence.  Host mode (numpy or lists): returns

@@ -61,6 +61,8 @@ _SIGS = {
     "dflash_seq_free": (None, [_VP]),
     "dflash_seq_span": (C.c_int, [_VP, C.POINTER(C.c_int64), C.POINTER(C.c_int64)]),
     "dflash_ctx_append": (C.c_int, [_VP, _VP, C.c_int64, _VP, C.c_int64, C.c_int, _VP]),
+    "dflash_ctx_queue": (C.c_int, [_VP, _VP, C.c_int64, _VP, C.c_int64, C.c_int, _VP]),
+    "dflash_settle": (C.c_int, [_VP, _VP, _VP]),
     "dflash_truncate": (C.c_int, [_VP, C.c_int64]),
     "dflash_reset": (C.c_int, [_VP]),
     "dflash_block": (C.c_int, [_VP, C.POINTER(_VP), C.c_int32, _VP, C.POINTER(C.c_int64), C.c_int32, _VP, _VP,

@@ -172,6 +172,10 @@ struct dflash_seq {
     // per layer: context rows no block row of the layer can see any more
     // (its window), dropped for good; the layer reads from first + dropped
     std::vector<int64_t> dropped;
+    // queued tap rows (positions first + len ..): rows [pend_off, pend_off +
+    // pending) of a device buffer of pend_cap rows
+    float* pend = nullptr;
+    int64_t pend_cap = 0, pend_off = 0, pending = 0;
 };
 
 namespace {
@@ -1096,6 +1100,117 @@ void dflash_free(dflash_model* m) {
 
 const char* dflash_last_error(const dflash_model* m) { return m ? m->err.c_str() : g_init_error.c_str(); }
 
+namespace {
+
+// the context queue's limits (page "cortiq-engine 0.8.71 — src/dflash.rs",
+// `queue_context`: PENDING_ROWS, CONTEXT_CHUNK, BLOCK_SLACK)
+constexpr int64_t kPendingRows = 512, kContextChunk = 64, kBlockSlack = 256;
+
+// Forget the positions from pos on, queued rows first (`truncate`).
+void seq_truncate(dflash_seq* s, int64_t pos) {
+    const int64_t held = s->first + s->len;
+    s->pending = std::min(s->pending, std::max<int64_t>(pos - held, 0));
+    if (s->pending == 0) s->pend_off = 0;
+    const int64_t keep = std::min(std::max<int64_t>(pos - s->first, 0), s->len);
+    s->len = keep;
+    for (auto& d : s->dropped) d = std::min(d, keep);
+}
+
+// The position rule of an append or a queue of n rows at pos: a held position
+// replaces it and what follows, a gap (or a position before the first) starts
+// the context over; ECAPACITY (nothing changed) when the rows would not fit.
+int seq_place(dflash_model* m, dflash_seq* s, int64_t pos, int64_t n) {
+    const int64_t held = s->first + s->len, next = held + s->pending;
+    const bool restart = pos > next || pos < s->first;
+    const int64_t keep = restart ? 0 : std::min(pos - s->first, s->len);
+    const int64_t pend = restart ? 0 : std::min(s->pending, std::max<int64_t>(pos - held, 0));
+    if (keep + pend + n > s->cap)
+        return set_err(m, DFLASH_ECAPACITY, "context of " + std::to_string(keep + pend + n) +
+                                                " rows exceeds capacity " + std::to_string(s->cap));
+    if (restart) {
+        seq_truncate(s, 0);
+        s->first = pos;
+    } else {
+        seq_truncate(s, pos);
+    }
+    return DFLASH_OK;
+}
+
+// n tap rows (host or device) onto the end of the queue.
+int queue_rows(dflash_model* m, dflash_seq* s, const float* taps, int64_t n, bool on_device, cudaStream_t st) {
+    if (n <= 0) return DFLASH_OK;
+    const int64_t tw = m->tap_w;
+    if (s->pend_off + s->pending + n > s->pend_cap) {
+        // a larger buffer, the queued rows at its start
+        const int64_t cap = std::max<int64_t>({2 * s->pend_cap, s->pending + n, kContextChunk});
+        float* q = nullptr;
+        CK(m, cudaMalloc(&q, (size_t)cap * tw * sizeof(float)));
+        if (s->pending > 0)
+            CK(m, cudaMemcpyAsync(q, s->pend + s->pend_off * tw, (size_t)s->pending * tw * sizeof(float),
+                                  cudaMemcpyDeviceToDevice, st));
+        if (s->pend) {
+            CK(m, cudaStreamSynchronize(st));
+            cudaFree(s->pend);
+        }
+        s->pend = q;
+        s->pend_cap = cap;
+        s->pend_off = 0;
+    }
+    CK(m, cudaMemcpyAsync(s->pend + (s->pend_off + s->pending) * tw, taps, (size_t)n * tw * sizeof(float),
+                          on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, st));
+    s->pending += n;
+    return DFLASH_OK;
+}
+
+// Make n rows of taps (host or device) context at position first + len
+// (`settle_rows`): the projection passes, then the window drop.
+int settle_rows(dflash_model* m, dflash_seq* s, const float* taps, int64_t n_rows, bool taps_on_device,
+                cudaStream_t st) {
+    if (n_rows <= 0) return DFLASH_OK;
+    const int64_t first = s->first, len = s->len;
+    const int64_t chunk = std::min<int64_t>(n_rows, kAppendRows);
+    int rc = ensure_append_scratch(m, chunk);
+    if (!rc && chunk > 16) rc = ensure_dense(m, st);
+    if (rc) return rc;
+    for (int64_t r0 = 0; r0 < n_rows; r0 += chunk) {
+        const int64_t n = std::min(chunk, n_rows - r0);
+        const float* src = taps + r0 * m->tap_w;
+        if (!taps_on_device) {
+            CK(m, cudaMemcpyAsync(m->a_taps.p, src, (size_t)n * m->tap_w * sizeof(float), cudaMemcpyHostToDevice, st));
+            src = P<float>(m->a_taps);
+        }
+        const int64_t pos2[2] = {first + len + r0, len + r0};
+        CK(m, cudaMemcpyAsync(m->a_pos.p, pos2, sizeof(pos2), cudaMemcpyHostToDevice, st));
+        const std::vector<int64_t> key = {1, (int64_t)(intptr_t)s, (int64_t)(intptr_t)s->k_dev, n,
+                                          (int64_t)(intptr_t)src};
+        rc = run_enqueue(m, key, st, [&](cudaStream_t q) { return append_rows(m, s, src, n, q); });
+        if (rc) return rc;
+        if (!taps_on_device && r0 + chunk < n_rows) CK(m, cudaStreamSynchronize(st));  // staging reused
+    }
+    s->len = len + n_rows;
+    // no row of a layer sees further back than its window: once a layer holds
+    // more than twice its window, all but the last window of rows are dropped
+    // (page "cortiq-engine 0.8.71 — src/dflash.rs", `settle_rows`)
+    for (int l = 0; l < m->g.layers; ++l) {
+        const int64_t w = m->win[l], held = s->len - s->dropped[l];
+        if (w > 0 && held > 2 * w) s->dropped[l] += held - w;
+    }
+    return DFLASH_OK;
+}
+
+// Every queued row made context (`settle`).
+int settle_pending(dflash_model* m, dflash_seq* s, cudaStream_t st) {
+    if (s->pending == 0) return DFLASH_OK;
+    const int64_t n = s->pending;
+    int rc = settle_rows(m, s, s->pend + s->pend_off * m->tap_w, n, true, st);
+    if (rc) return rc;
+    s->pending = 0;
+    s->pend_off = 0;
+    return DFLASH_OK;
+}
+
+}  // namespace
+
 int dflash_geometry_of(const dflash_model* m, dflash_geometry* out) {
     if (!m || !out) return DFLASH_EINVAL;
     *out = m->g;
@@ -1144,6 +1259,7 @@ void dflash_seq_free(dflash_seq* s) {
     for (__half* p : s->v) if (p) cudaFree(p);
     if (s->k_dev) cudaFree(s->k_dev);
     if (s->v_dev) cudaFree(s->v_dev);
+    if (s->pend) cudaFree(s->pend);
     if (s->m && s->m->live_seqs > 0) s->m->live_seqs--;
     delete s;
 }
@@ -1151,23 +1267,20 @@ void dflash_seq_free(dflash_seq* s) {
 int dflash_seq_span(const dflash_seq* s, int64_t* first, int64_t* next) {
     if (!s || !first || !next) return DFLASH_EINVAL;
     *first = s->first;
-    *next = s->first + s->len;
+    *next = s->first + s->len + s->pending;
     return DFLASH_OK;
 }
 
 int dflash_truncate(dflash_seq* s, int64_t pos) {
     if (!s) return DFLASH_EINVAL;
-    int64_t keep = std::min(std::max<int64_t>(pos - s->first, 0), s->len);
-    s->len = keep;
-    for (auto& d : s->dropped) d = std::min(d, keep);
+    seq_truncate(s, pos);
     return DFLASH_OK;
 }
 
 int dflash_reset(dflash_seq* s) {
     if (!s) return DFLASH_EINVAL;
-    s->len = 0;
+    seq_truncate(s, 0);
     s->first = 0;
-    for (auto& d : s->dropped) d = 0;
     return DFLASH_OK;
 }
 
@@ -1179,54 +1292,60 @@ int dflash_ctx_append(dflash_model* m, dflash_seq* s, int64_t pos, const float* 
     if (n_rows < 0 || pos < 0) return set_err(m, DFLASH_EINVAL, "n_rows < 0 or pos < 0");
     if (n_rows > 0 && !taps) return set_err(m, DFLASH_EINVAL, "taps is NULL");
     cudaStream_t st = (cudaStream_t)stream;
-    // position rule: replace from pos, or start over at pos
-    int64_t first = s->first, len = s->len;
-    if (pos > first + len || pos < first) {
-        first = pos;
-        len = 0;
-    } else {
-        len = pos - first;
-    }
-    if (len + n_rows > s->cap)
-        return set_err(m, DFLASH_ECAPACITY, "context of " + std::to_string(len + n_rows) + " rows exceeds capacity " +
-                                                std::to_string(s->cap));
-    s->first = first;
-    s->len = len;
-    for (auto& d : s->dropped) d = std::min(d, len);  // a restart holds nothing: 0
-    if (n_rows == 0) return DFLASH_OK;
-    const int64_t chunk = std::min<int64_t>(n_rows, kAppendRows);
-    rc = ensure_append_scratch(m, chunk);
-    if (!rc && chunk > 16) rc = ensure_dense(m, st);
+    rc = seq_place(m, s, pos, n_rows);
     if (rc) return rc;
-    for (int64_t r0 = 0; r0 < n_rows; r0 += chunk) {
-        const int64_t n = std::min(chunk, n_rows - r0);
-        const float* src = taps + r0 * m->tap_w;
-        if (!taps_on_device) {
-            CK(m, cudaMemcpyAsync(m->a_taps.p, src, (size_t)n * m->tap_w * sizeof(float), cudaMemcpyHostToDevice, st));
-            src = P<float>(m->a_taps);
-        }
-        const int64_t pos2[2] = {first + len + r0, len + r0};
-        CK(m, cudaMemcpyAsync(m->a_pos.p, pos2, sizeof(pos2), cudaMemcpyHostToDevice, st));
-        const std::vector<int64_t> key = {1, (int64_t)(intptr_t)s, (int64_t)(intptr_t)s->k_dev, n,
-                                          (int64_t)(intptr_t)src};
-        rc = run_enqueue(m, key, st, [&](cudaStream_t q) { return append_rows(m, s, src, n, q); });
-        if (rc) return rc;
-        if (!taps_on_device && r0 + chunk < n_rows) CK(m, cudaStreamSynchronize(st));  // staging reused
+    if (s->pending > 0) {
+        // queued rows still held go first, in the same settle
+        rc = queue_rows(m, s, taps, n_rows, taps_on_device != 0, st);
+        if (!rc) rc = settle_pending(m, s, st);
+    } else {
+        rc = settle_rows(m, s, taps, n_rows, taps_on_device != 0, st);
     }
-    s->len = len + n_rows;
-    // no row of a layer sees further back than its window: once a layer holds
-    // more than twice its window, all but the last window of rows are dropped
-    // (page "cortiq-engine 0.8.71 — src/dflash.rs", `settle_rows`)
-    for (int l = 0; l < m->g.layers; ++l) {
-        const int64_t w = m->win[l], held = s->len - s->dropped[l];
-        if (w > 0 && held > 2 * w) s->dropped[l] += held - w;
-    }
-    if (!taps_on_device) {
+    if (rc) return rc;
+    if (!taps_on_device && n_rows > 0) {
         CK(m, cudaMemcpyAsync(m->err_host, m->err_dev, sizeof(int), cudaMemcpyDeviceToHost, st));
         CK(m, cudaStreamSynchronize(st));
         if (*m->err_host) return device_wait_expired(m);
     }
     return DFLASH_OK;
+}
+
+int dflash_ctx_queue(dflash_model* m, dflash_seq* s, int64_t pos, const float* taps, int64_t n_rows,
+                     int taps_on_device, void* stream) {
+    int rc = check_model(m);
+    if (rc) return rc;
+    if (!s || s->m != m) return set_err(m, DFLASH_EINVAL, "sequence is NULL or belongs to another model");
+    if (n_rows < 0 || pos < 0) return set_err(m, DFLASH_EINVAL, "n_rows < 0 or pos < 0");
+    if (n_rows > 0 && !taps) return set_err(m, DFLASH_EINVAL, "taps is NULL");
+    cudaStream_t st = (cudaStream_t)stream;
+    rc = seq_place(m, s, pos, n_rows);
+    if (!rc) rc = queue_rows(m, s, taps, n_rows, taps_on_device != 0, st);
+    if (rc) return rc;
+    // past the queue's limit the oldest rows go through, a multiple of the granule
+    int64_t limit = kPendingRows;
+    bool all_windowed = true;
+    int64_t widest = 0;
+    for (int l = 0; l < m->g.layers; ++l) {
+        all_windowed = all_windowed && m->win[l] > 0;
+        widest = std::max<int64_t>(widest, m->win[l]);
+    }
+    if (all_windowed) limit = std::max<int64_t>(kPendingRows, widest + kBlockSlack);
+    if (s->pending > limit) {
+        const int64_t over = std::min((s->pending - limit + kContextChunk - 1) / kContextChunk * kContextChunk, s->pending);
+        rc = settle_rows(m, s, s->pend + s->pend_off * m->tap_w, over, true, st);
+        if (rc) return rc;
+        s->pend_off += over;
+        s->pending -= over;
+        if (s->pending == 0) s->pend_off = 0;
+    }
+    return DFLASH_OK;
+}
+
+int dflash_settle(dflash_model* m, dflash_seq* s, void* stream) {
+    int rc = check_model(m);
+    if (rc) return rc;
+    if (!s || s->m != m) return set_err(m, DFLASH_EINVAL, "sequence is NULL or belongs to another model");
+    return settle_pending(m, s, (cudaStream_t)stream);
 }
 
 int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const uint32_t* anchor_tok,
@@ -1246,6 +1365,11 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
             return set_err(m, DFLASH_EINVAL, "anchor token outside the vocabulary");
     }
     cudaStream_t st = (cudaStream_t)stream;
+    // the queued rows become context before the block reads it
+    for (int s = 0; s < n_seqs; ++s) {
+        rc = settle_pending(m, seqs[s], st);
+        if (rc) return rc;
+    }
     const bool quant = g.quant == DFLASH_QUANT_Q4G32;
     const int H = g.hidden, I = g.intermediate, hd = g.head_dim, B = block_len;
     const int R = n_seqs * B, D = n_seqs * (B - 1);

@@ -205,7 +205,8 @@ DFLASH_API int dflash_seq_new(dflash_model* model, int64_t max_ctx_rows, dflash_
 /* Free a sequence. NULL is a no-op. */
 DFLASH_API void dflash_seq_free(dflash_seq* seq);
 
-/* The positions the context covers: [*first, *next) (`Drafter::span`). */
+/* The positions the context covers: [*first, *next), queued rows included
+ * (`Drafter::span`). */
 DFLASH_API int dflash_seq_span(const dflash_seq* seq, int64_t* first, int64_t* next);
 
 /*
@@ -219,14 +220,32 @@ DFLASH_API int dflash_seq_span(const dflash_seq* seq, int64_t* first, int64_t* n
  * layers' outputs joined in tap order; a host pointer, or a device pointer
  * when taps_on_device is 1.  Positions: with first <= pos <= next the rows
  * replace position pos and everything after it; pos < first or pos > next
- * starts the context over at pos.  The rows are settled at once (no queue).
- * n_rows == 0 applies only the position rule.  Host taps: the call returns
- * after the rows are copied; device taps: the work is queued on `stream`.
+ * starts the context over at pos (next counts queued rows, see
+ * dflash_ctx_queue).  The rows are settled at once, after the queued rows
+ * still held (`push_context`: queue, then settle).  n_rows == 0 applies the
+ * position rule and settles the queue.  Host taps: the call returns after
+ * the rows are copied; device taps: the work is queued on `stream`.
  * Errors: EINVAL (null taps with n_rows > 0, n_rows < 0, pos < 0),
  * ECAPACITY (the context would exceed max_ctx_rows), ECUDA.
  */
 DFLASH_API int dflash_ctx_append(dflash_model* model, dflash_seq* seq, int64_t pos, const float* taps, int64_t n_rows,
                       int taps_on_device, void* stream);
+
+/*
+ * `dflash_ctx_append` put off (page "cortiq-engine 0.8.71 — src/dflash.rs",
+ * `queue_context`, `settle`): the position rule as for an append, then the
+ * rows wait, copied into the sequence's device queue, until a block reads
+ * the context (dflash_block settles every queued row of its sequences first)
+ * or dflash_settle / dflash_ctx_append settle them.  At most 512 rows wait
+ * (with every layer windowed: the widest window + 256, if more); past that
+ * the oldest are settled now, a multiple of 64 of them.  A truncation cuts
+ * queued rows first.  Errors as dflash_ctx_append.
+ */
+DFLASH_API int dflash_ctx_queue(dflash_model* model, dflash_seq* seq, int64_t pos, const float* taps,
+                                int64_t n_rows, int taps_on_device, void* stream);
+
+/* Settle every queued row of `seq` (`settle`).  Errors: EINVAL, ECUDA. */
+DFLASH_API int dflash_settle(dflash_model* model, dflash_seq* seq, void* stream);
 
 /* Forget the context from position `pos` on (`Drafter::truncate`). */
 DFLASH_API int dflash_truncate(dflash_seq* seq, int64_t pos);

@@ -257,6 +257,12 @@ class Script:
     def append(self, i, pos, taps):
         self.actions.append(("append", i, pos, taps))
 
+    def queue(self, i, pos, taps):
+        self.actions.append(("queue", i, pos, taps))
+
+    def truncate(self, i, pos):
+        self.actions.append(("truncate", i, pos))
+
     def block(self, seqs, anchors, positions, bl):
         self.actions.append(("block", list(seqs), list(anchors), list(positions), bl))
 
@@ -268,12 +274,20 @@ class Script:
         oracle_out, sites = [], []
         try:
             for a in self.actions:
-                if a[0] == "append":
-                    osq[a[1]].append(a[2], a[3])
+                if a[0] in ("append", "queue"):
+                    getattr(osq[a[1]], a[0])(a[2], a[3])
                     if D.TRACE is not None:
                         sites += D.TRACE.sites
                         D.TRACE.sites = []
+                elif a[0] == "truncate":
+                    osq[a[1]].truncate(a[2])
                 else:
+                    # a block settles its sequences' queued rows first, in sequence order
+                    for i in a[1]:
+                        osq[i].settle()
+                        if D.TRACE is not None:
+                            sites += D.TRACE.sites
+                            D.TRACE.sites = []
                     _, ids, anchors, positions, bl = a
                     per_seq = []
                     res = []
@@ -298,6 +312,10 @@ class Script:
             for a in self.actions:
                 if a[0] == "append":
                     p.gpu.ctx_append(gseq[a[1]], a[2], a[3])
+                elif a[0] == "queue":
+                    p.gpu.ctx_queue(gseq[a[1]], a[2], a[3])
+                elif a[0] == "truncate":
+                    gseq[a[1]].truncate(a[2])
                 else:
                     _, ids, anchors, positions, bl = a
                     gpu_out.append(p.gpu.block([gseq[i] for i in ids], anchors, positions, bl))
@@ -418,6 +436,49 @@ def test_selector_choices_from_the_librarys_logits(top):
         assert np.max(np.abs(logits[0] - ref_logits)) <= 1e-4 * np.max(np.abs(ref_logits))
         chosen, plain = select(p.ora, hn[1:], logits[0], anchor)
         np.testing.assert_array_equal(toks[0], chosen)
+    seq.close()
+
+
+@pytest.mark.parametrize("name", ["tiny_f32", "small_q4"])
+@pytest.mark.parametrize("forced", [True, False])
+def test_context_queue_matches_oracle(name, forced):
+    """Page 1's context queue: rows queued over several calls and settled by
+    the block that reads them; a truncation that cuts queued rows; a queue
+    past its limit (the oldest settled in 64-row granules)."""
+    p = Pair(name)
+    g = p.g
+    sc = Script(p, 2, 700)
+    taps = W.make_taps(g, 40)
+    sc.append(0, 0, taps[:10])
+    sc.queue(0, 10, taps[10:25])
+    sc.queue(0, 25, taps[25:40])
+    sc.truncate(0, 33)
+    sc.queue(0, 33, taps[33:40])
+    sc.queue(1, 0, W.make_taps(g, 600, call_id=4))
+    anchors = [int(a) for a in W.make_anchors(g, 2)]
+    sc.block([0, 1], anchors, [40, 600], g.block)
+    sc.queue(0, 40, W.make_taps(g, 16, call_id=6))
+    sc.block([0], [anchors[1]], [56], g.block)
+    sc.run(forced).check(forced)
+
+
+def test_queue_span_and_settle():
+    """The span counts queued rows; settle makes them context; the capacity
+    counts them too."""
+    dfl = _dfl()
+    p = pair("tiny_f32")
+    g = p.g
+    seq = p.gpu.new_sequence(50)
+    p.gpu.ctx_queue(seq, 0, W.make_taps(g, 30))
+    assert seq.span() == (0, 30)
+    with pytest.raises(dfl.DFlashError) as e:
+        p.gpu.ctx_queue(seq, 30, W.make_taps(g, 21))
+    assert e.value.code == dfl._abi.DFLASH_ECAPACITY
+    assert seq.span() == (0, 30)
+    p.gpu.settle(seq)
+    assert seq.span() == (0, 30)
+    seq.truncate(12)
+    assert seq.span() == (0, 12)
     seq.close()
 
 
