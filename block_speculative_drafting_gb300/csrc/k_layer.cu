@@ -738,13 +738,17 @@ __global__ void __launch_bounds__(kAttnWarps * 32, ST == 1 ? 2 : 1) attn_cluster
         float4 gk = make_float4(1.f, 1.f, 1.f, 1.f);
         if (k_norm != nullptr) gk = *reinterpret_cast<const float4*>(k_norm + 4 * d4);
         const int lim = min(block_len, j1);
+        // one CTA an SM: two float4 a thread per round, every load of the
+        // round issued before any is used; two CTAs an SM (registers short):
+        // one
+        constexpr int CH = ST == 2 ? 2 : 1;
 #pragma unroll 1
-        for (int u0 = 0; u0 < NK4; u0 += 2) {
-            if (jt + (u0 * kThreads) / D4 >= lim) break;  // no block row in this pair or later (CTA-uniform)
-            float4 kk[2], vv[2], t01[2], t23[2];
-            bool mine[2];
+        for (int u0 = 0; u0 < NK4; u0 += CH) {
+            if (jt + (u0 * kThreads) / D4 >= lim) break;  // no block row in this round or later (CTA-uniform)
+            float4 kk[CH], vv[CH], t01[CH], t23[CH];
+            bool mine[CH];
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
+            for (int e = 0; e < CH; ++e) {
                 const int i = tid + (u0 + e) * kThreads, kr = i / D4, d = (i % D4) * 4, j = jt + kr;
                 mine[e] = j < lim;  // uniform over the lanes of a row
                 kk[e] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -759,7 +763,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, ST == 1 ? 2 : 1) attn_cluster
                     rope_pairs<HD>(rope, row0 + min(j, block_len - 1), d4, t01[e], t23[e]);
             }
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
+            for (int e = 0; e < CH; ++e) {
                 const int i = tid + (u0 + e) * kThreads, kr = i / D4, d = (i % D4) * 4;
                 const int hf = kr / kAttnK, k = kr % kAttnK;
                 if (k_norm != nullptr) norm_rope4<HD>(kk[e], mine[e], gk, t01[e], t23[e], d4, eps, rope != nullptr);

@@ -1199,10 +1199,22 @@ int q4_tc_dense(const __half* hi, const __half* lo, int N, int K, QAct x, const 
     }
     const int ksteps = K / kTcKB;
     const int mt = (T + kT2Tiles * kTcM - 1) / (kT2Tiles * kTcM), ntl = (N + kT3N - 1) / kT3N;
-    int splits = (ksteps + kT2MaxKb - 1) / kT2MaxKb;
-    while (mt * ntl * splits * 3 < num_sms * 2 && splits * 2 <= ksteps) splits *= 2;
-    const int kps = (ksteps + splits - 1) / splits;
-    splits = (ksteps + kps - 1) / kps;
+    // K slices: at most kT2MaxKb k-blocks each; of those, the count whose
+    // waves of CTAs (one an SM) times a CTA's k-blocks, plus about two
+    // k-blocks' worth of epilogue (its reductions into y), is least
+    const int s_min = (ksteps + kT2MaxKb - 1) / kT2MaxKb;
+    int splits = s_min, kps = (ksteps + s_min - 1) / s_min;
+    int64_t best = INT64_MAX;
+    for (int sp = s_min; sp <= std::min(ksteps, 8 * s_min); ++sp) {
+        const int k = (ksteps + sp - 1) / sp, real = (ksteps + k - 1) / k;
+        const int64_t waves = ((int64_t)mt * ntl * real + num_sms - 1) / num_sms;
+        const int64_t cost = waves * (k + 2);
+        if (cost < best) {
+            best = cost;
+            splits = real;
+            kps = k;
+        }
+    }
     if (splits > 1 && !accumulate) {
         cudaError_t e = cudaMemset2DAsync(y, (size_t)ldy * sizeof(float), 0, (size_t)N * sizeof(float), T, st);
         if (e != cudaSuccess) return (int)e;
