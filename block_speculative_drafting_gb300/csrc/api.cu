@@ -744,7 +744,8 @@ int run_selector(dflash_model* m, cudaStream_t st, const float* h, RowMap drafts
     KL(m, "rms_f32", 1, (double)D * H * 8, st,
        rms_rows(h, H, drafts, D, H, m->norm, g.eps, hn, H, nullptr, nullptr, 0, st));
     KL(m, "linear_f32", 1, f32_bytes_of(rank, H, D, false), st, linear_f32(m->sel, rank, H, hn, H, D, hp, rank, false, st));
-    KL(m, "topk_rows", 1, (double)D * g.vocab * 4, st, topk_rows(logits, g.vocab, g.vocab, D, top, cand, st));
+    unsigned long long* parts = cand + (size_t)D * top;  // the first phase's keys, after the candidates
+    KL(m, "topk_rows", 2, (double)D * g.vocab * 4, st, topk_rows(logits, g.vocab, g.vocab, D, top, parts, cand, st));
     KL(m, "select", 1, (double)D * top * rank * 4, st,
        select_tokens(cand, top, hp, rank, m->book_p, m->book_c, g.vocab, anchors, n_seqs, B - 1, tok_out,
                      P<uint32_t>(m->plain), st));
@@ -1403,7 +1404,8 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
     if (g.selector_rank > 0) {
         CK(m, ensure_m(m, m->hn, (size_t)D * H * sizeof(float)));
         CK(m, ensure_m(m, m->hp, (size_t)D * g.selector_rank * sizeof(float)));
-        CK(m, ensure_m(m, m->cand, (size_t)D * g.selector_top * sizeof(unsigned long long)));
+        CK(m, ensure_m(m, m->cand, (size_t)D * g.selector_top * (1 + topk_parts(g.vocab, g.selector_top)) *
+                                       sizeof(unsigned long long)));
         CK(m, ensure_m(m, m->plain, (size_t)D * sizeof(uint32_t)));
     }
     if (g.conv_kernel > 0) {
@@ -1482,7 +1484,7 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
             KL(m, "attention", attn_kernels(n_seqs, B, max_ctx, g.heads, g.kv_heads, hd, m->num_sms, part_floats), attn_bytes_l[l], st,
                attention(qkv, m->qkv_w, n_seqs, B, aseq_dev, max_ctx, g.heads, g.kv_heads, hd, scale, P<float>(m->part),
                          part_floats, y, m->num_sms, st, Ly.q_norm, Ly.k_norm, m->norope[l] ? nullptr : rope, g.eps,
-                         m->own_capture));
+                         m->own_capture, m->win[l] > 0));
             c.add(row_stage(kChainRows, y, m->qd, ident, R, m->qd, nullptr, g.eps, xq, xs, maxK), (double)R * m->qd * 5,
                   [&]() {
                       return trace_site(m, st, R, m->qd, xq, maxK, xs, [&](float* v) {
@@ -1572,7 +1574,7 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
            attn_bytes_l[l], st,
            attention(qkv, m->qkv_w, n_seqs, B, aseq_dev, max_ctx, g.heads, g.kv_heads, hd, scale, P<float>(m->part),
                      part_floats, y, m->num_sms, st, Ly.q_norm, Ly.k_norm, m->norope[l] ? nullptr : rope, g.eps,
-                     m->own_capture));
+                     m->own_capture, m->win[l] > 0));
         // co = O y (the streaming matvec adds: co cleared by the quantisation of y)
         if (quant) {
             KL(m, "rms_quant", 1, (double)R * m->qd * 5, st,
@@ -1621,7 +1623,7 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
         KL(m, "attention", attn_kernels(n_seqs, B, max_ctx, g.heads, g.kv_heads, hd, m->num_sms, part_floats), attn_bytes_l[l], st,
            attention(qkv, m->qkv_w, n_seqs, B, aseq_dev, max_ctx, g.heads, g.kv_heads, hd, scale, P<float>(m->part),
                      part_floats, y, m->num_sms, st, Ly.q_norm, Ly.k_norm, m->norope[l] ? nullptr : rope, g.eps,
-                         m->own_capture));
+                         m->own_capture, m->win[l] > 0));
         if (quant) {
             KL(m, "rms_quant", 1, (double)R * m->qd * 5, st, rms_rows(y, m->qd, ident, R, m->qd, nullptr, g.eps, nullptr, 0, xq, xs, maxK, st));
             TRACE(trace_site(m, st, R, m->qd, xq, maxK, xs, [&](float* v) {
@@ -1737,7 +1739,8 @@ int dflash_debug_attention(dflash_model* m, dflash_seq* const* seqs, int32_t n_s
     CK(m, cudaMemcpyAsync(m->aseqs.p, views.data(), views.size() * sizeof(AttnSeq), cudaMemcpyHostToDevice, st));
     KL(m, "attention", attn_kernels(n_seqs, block_len, max_ctx, g.heads, g.kv_heads, g.head_dim, m->num_sms, part_floats), 0.0, st,
        attention(qkv, m->qkv_w, n_seqs, block_len, P<AttnSeq>(m->aseqs), max_ctx, g.heads, g.kv_heads, g.head_dim,
-                 1.0f / sqrtf((float)g.head_dim), P<float>(m->part), part_floats, y, m->num_sms, st));
+                 1.0f / sqrtf((float)g.head_dim), P<float>(m->part), part_floats, y, m->num_sms, st, nullptr, nullptr,
+                 nullptr, 0.f, false, m->win[layer] > 0));
     return DFLASH_OK;
 }
 
@@ -2080,7 +2083,8 @@ int dflash_attention_noalloc(dflash_model* m, dflash_seq* const* seqs, int32_t n
     // splits merge in distributed shared memory and the rest is not read
     CK(m, cudaMemcpyAsync(views_dev, views.data(), views.size() * sizeof(AttnSeq), cudaMemcpyHostToDevice, st));
     CK(m, attention(qkv, m->qkv_w, n_seqs, block_len, views_dev, max_ctx, g.heads, g.kv_heads, g.head_dim,
-                    1.0f / sqrtf((float)g.head_dim), base + kNoAllocViewFloats, part_floats, y, m->num_sms, st));
+                    1.0f / sqrtf((float)g.head_dim), base + kNoAllocViewFloats, part_floats, y, m->num_sms, st,
+                    nullptr, nullptr, nullptr, 0.f, false, m->win[layer] > 0));
     m->launches += attn_kernels(n_seqs, block_len, max_ctx, g.heads, g.kv_heads, g.head_dim, m->num_sms, part_floats);
     return DFLASH_OK;
 }

@@ -185,25 +185,27 @@ int q4_groupsums(const uint8_t* packed, Q4Layout L, int tile0, int N, QAct x, in
 // ------------------------------------------------------------------ f32 path
 constexpr int kLinTok = 8;
 
+// A CTA an output n and up to kLinTok rows: its eight warps take eighths of
+// K (float4 a lane), and the CTA adds the warps' sums.
 __global__ void __launch_bounds__(256) linear_f32_kernel(const float* __restrict__ W, int N, int K,
                                                          const float* __restrict__ x, int ldx, int T,
                                                          float* __restrict__ y, int ldy, int accumulate) {
-    const int n = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
-    const int lane = threadIdx.x & 31;
+    __shared__ float part[8][kLinTok];
+    const int n = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_trigger();
     pdl_wait();
-    if (n >= N) return;
     const int t0 = blockIdx.y * kLinTok;
     float acc[kLinTok];
 #pragma unroll
     for (int i = 0; i < kLinTok; ++i) acc[i] = 0.f;
     const float* wr = W + (int64_t)n * K;
-    for (int k = lane * 4; k < K; k += 128) {
-        const float4 w = *reinterpret_cast<const float4*>(wr + k);
+    const int k4 = K / 4, per = (k4 + 7) / 8, lo = warp * per, hi = min(k4, lo + per);
+    for (int c = lo + lane; c < hi; c += 32) {
+        const float4 w = reinterpret_cast<const float4*>(wr)[c];
 #pragma unroll
         for (int i = 0; i < kLinTok; ++i) {
             if (t0 + i < T) {
-                const float4 v = *reinterpret_cast<const float4*>(x + (int64_t)(t0 + i) * ldx + k);
+                const float4 v = reinterpret_cast<const float4*>(x + (int64_t)(t0 + i) * ldx)[c];
                 acc[i] = fmaf(w.x, v.x, fmaf(w.y, v.y, fmaf(w.z, v.z, fmaf(w.w, v.w, acc[i]))));
             }
         }
@@ -211,17 +213,24 @@ __global__ void __launch_bounds__(256) linear_f32_kernel(const float* __restrict
 #pragma unroll
     for (int i = 0; i < kLinTok; ++i) {
         const float s = warp_sum(acc[i]);
-        if (lane == 0 && t0 + i < T) {
-            float* p = y + (int64_t)(t0 + i) * ldy + n;
-            *p = accumulate ? *p + s : s;
-        }
+        if (lane == 0) part[warp][i] = s;
+    }
+    __syncthreads();
+    if (threadIdx.x < kLinTok && t0 + (int)threadIdx.x < T) {
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) s += part[w][threadIdx.x];
+        float* p = y + (int64_t)(t0 + threadIdx.x) * ldy + n;
+        *p = accumulate ? *p + s : s;
     }
 }
 
 int linear_f32(const float* W, int N, int K, const float* x, int ldx, int T, float* y, int ldy, bool accumulate,
                cudaStream_t st) {
     if (T <= 0 || N <= 0) return 0;
-    dim3 grid((N * 32 + 255) / 256, (T + kLinTok - 1) / kLinTok);
+    if (K % 4 || ldx % 4 || (reinterpret_cast<uintptr_t>(W) & 15) || (reinterpret_cast<uintptr_t>(x) & 15))
+        return (int)cudaErrorInvalidValue;
+    dim3 grid(N, (T + kLinTok - 1) / kLinTok);
     return (int)launch(linear_f32_kernel, grid, dim3(256), 0, st, W, N, K, x, ldx, T, y, ldy, accumulate ? 1 : 0);
 }
 
@@ -273,9 +282,15 @@ template <int K>
 struct TopShape {
     static constexpr int kThreads = K >= 32 ? 128 : 256;  // the lists in 32 KB of shared memory at most
 };
+// Phase 1 (logits != nullptr): CTA (t, part) over the part-th of row t's
+// columns, its k best into out[(t * parts + part) * k ..].  Phase 2 (logits
+// == nullptr): CTA t over the parts * k keys of phase 1 (`keys`), the row's
+// k best into out[t * k ..].  Either keeps the exact top k: a key among the
+// row's best k is among its part's best k.
 template <int K>
 __global__ void __launch_bounds__(TopShape<K>::kThreads) topk_rows_kernel(const float* __restrict__ logits, int ldl,
-                                                                           int V, int k,
+                                                                           int V, int k, int parts,
+                                                                           const unsigned long long* __restrict__ keys,
                                                                            unsigned long long* __restrict__ out) {
     constexpr int kTopThreads = TopShape<K>::kThreads;
     __shared__ unsigned long long cand[kTopThreads * K];
@@ -286,9 +301,11 @@ __global__ void __launch_bounds__(TopShape<K>::kThreads) topk_rows_kernel(const 
     unsigned long long mine[K];
 #pragma unroll
     for (int i = 0; i < K; ++i) mine[i] = 0ull;  // no real key is 0 (its index part is below 2^32 - 1 - V)
-    const float* row = logits + (int64_t)t * ldl;
-    for (int n = tid; n < V; n += kTopThreads) {
-        unsigned long long x = argmax_key(row[n], (uint32_t)n);
+    const float* row = logits ? logits + (int64_t)t * ldl : nullptr;
+    const int chunk = logits ? (V + parts - 1) / parts : parts * k;
+    const int c0 = logits ? blockIdx.y * chunk : 0, c1 = logits ? min(V, c0 + chunk) : parts * k;
+    for (int n = c0 + tid; n < c1; n += kTopThreads) {
+        unsigned long long x = logits ? argmax_key(row[n], (uint32_t)n) : keys[(int64_t)t * parts * k + n];
         if (x <= mine[K - 1]) continue;
 #pragma unroll
         for (int i = 0; i < K; ++i) {
@@ -311,7 +328,7 @@ __global__ void __launch_bounds__(TopShape<K>::kThreads) topk_rows_kernel(const 
         b = 0ull;
 #pragma unroll
         for (int w = 0; w < kTopThreads / 32; ++w) b = max(b, red[w]);
-        if (tid == 0) out[(int64_t)t * k + r] = b;
+        if (tid == 0) out[((int64_t)t * gridDim.y + blockIdx.y) * k + r] = b;
 #pragma unroll
         for (int i = 0; i < K; ++i)
             if (cand[tid * K + i] == b) cand[tid * K + i] = 0ull;  // keys are unique: its one owner
@@ -319,14 +336,27 @@ __global__ void __launch_bounds__(TopShape<K>::kThreads) topk_rows_kernel(const 
     }
 }
 
-int topk_rows(const float* logits, int ldl, int V, int T, int k, unsigned long long* out, cudaStream_t st) {
+template <int K>
+static int topk_two_phase(const float* logits, int ldl, int V, int T, int k, int parts, unsigned long long* scratch,
+                          unsigned long long* out, cudaStream_t st) {
+    constexpr int nt = TopShape<K>::kThreads;
+    cudaError_t e = launch(topk_rows_kernel<K>, dim3(T, parts), dim3(nt), 0, st, logits, ldl, V, k, parts,
+                           (const unsigned long long*)nullptr, scratch);
+    if (e != cudaSuccess) return (int)e;
+    return (int)launch(topk_rows_kernel<K>, dim3(T, 1), dim3(nt), 0, st, (const float*)nullptr, 0, V, k, parts,
+                       (const unsigned long long*)scratch, out);
+}
+
+int topk_parts(int V, int k) { return std::max(1, std::min(32, V / (8 * k))); }
+
+int topk_rows(const float* logits, int ldl, int V, int T, int k, unsigned long long* scratch, unsigned long long* out,
+              cudaStream_t st) {
     if (T <= 0) return 0;
     if (k < 1 || k > 32 || k > V) return (int)cudaErrorInvalidValue;
-    if (k <= 8)
-        return (int)launch(topk_rows_kernel<8>, dim3(T), dim3(TopShape<8>::kThreads), 0, st, logits, ldl, V, k, out);
-    if (k <= 16)
-        return (int)launch(topk_rows_kernel<16>, dim3(T), dim3(TopShape<16>::kThreads), 0, st, logits, ldl, V, k, out);
-    return (int)launch(topk_rows_kernel<32>, dim3(T), dim3(TopShape<32>::kThreads), 0, st, logits, ldl, V, k, out);
+    const int parts = topk_parts(V, k);
+    if (k <= 8) return topk_two_phase<8>(logits, ldl, V, T, k, parts, scratch, out, st);
+    if (k <= 16) return topk_two_phase<16>(logits, ldl, V, T, k, parts, scratch, out, st);
+    return topk_two_phase<32>(logits, ldl, V, T, k, parts, scratch, out, st);
 }
 
 // The selector's choices, a warp a sequence (its rows one after another):

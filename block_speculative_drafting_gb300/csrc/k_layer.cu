@@ -660,7 +660,7 @@ static_assert(kAttnQW <= 4, "the partial rows must fit the key/value area");
 // step in flight while the current one is multiplied; one CTA an SM) or 1 (two
 // CTAs an SM at 128 registers a thread, each one's copies overlapping the
 // other's products).
-template <int HD, int ST>
+template <int HD, int ST, bool WIN>
 __global__ void __launch_bounds__(kAttnWarps * 32, ST == 1 ? 2 : 1) attn_cluster_kernel(const float* __restrict__ qkv, int ld,
                                                                        int block_len, const AttnSeq* __restrict__ seqs,
                                                                        int nq, int nkv, int qtiles, int nsplit,
@@ -830,10 +830,13 @@ __global__ void __launch_bounds__(kAttnWarps * 32, ST == 1 ? 2 : 1) attn_cluster
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     const int qbase = qw * 16;
     // the leading context rows each of this lane's two query rows does not
-    // see (block row i of a windowed layer: sq.cut + i)
-    int cutr[2];
+    // see (block row i of a windowed layer: sq.cut + i; WIN: some view of
+    // the launch has a window)
+    int cutr[2] = {kNoCut, kNoCut};
+    if constexpr (WIN) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) cutr[h] = sq.cut + (qt * kAttnQ + qbase + gq + 8 * h) % block_len;
+        for (int h = 0; h < 2; ++h) cutr[h] = sq.cut + (qt * kAttnQ + qbase + gq + 8 * h) % block_len;
+    }
     // ldmatrix row addresses: A (queries x dims) and B (keys x dims) operands
     const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8, lcol = (lane >> 4) * 8;
 
@@ -892,7 +895,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, ST == 1 ? 2 : 1) attn_cluster
             for (int e = 0; e < 4; ++e) {
                 const int key = kt + n * 8 + 2 * tq + (e & 1);
                 // past the split, or a context row before the query row's window
-                const bool seen = key < j1 && (key < block_len || key - block_len >= cutr[e >> 1]);
+                const bool seen = key < j1 && (!WIN || key < block_len || key - block_len >= cutr[e >> 1]);
                 const float v = seen ? sc[n][e] * scale_log2 : -INFINITY;
                 sc[n][e] = v;
                 tmax[e >> 1] = fmaxf(tmax[e >> 1], v);
@@ -1197,9 +1200,10 @@ static const int* attn_cluster_table(cudaStream_t st) {
     static int table[kAttnMaxCluster + 1] = {0};
     static bool done = false;
     if (done) return table;
-    cudaFuncSetAttribute(attn_cluster_kernel<HD, ST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)sizeof(AttnSmem<HD, ST>));
-    cudaFuncSetAttribute(attn_cluster_kernel<HD, ST>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    for (auto kern : {attn_cluster_kernel<HD, ST, false>, attn_cluster_kernel<HD, ST, true>}) {
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(AttnSmem<HD, ST>));
+        cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    }
     for (int c = 1; c <= kAttnMaxCluster; ++c) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(c, 1, 1);
@@ -1214,7 +1218,8 @@ static const int* attn_cluster_table(cudaStream_t st) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, attn_cluster_kernel<HD, ST>, &cfg) != cudaSuccess) {
+        // (the windowed variant takes the same resources within its launch bounds)
+        if (cudaOccupancyMaxActiveClusters(&n, attn_cluster_kernel<HD, ST, false>, &cfg) != cudaSuccess) {
             cudaGetLastError();
             n = 0;
         }
@@ -1225,30 +1230,42 @@ static const int* attn_cluster_table(cudaStream_t st) {
     return table;
 }
 
-template <int HD, int ST>
-static int attention_run(const AttnPlan& p, const float* qkv, int ld, int n_seqs, int block_len,
-                         const AttnSeq* seqs_dev, int nq, int nkv, float scale_log2, float* part, float* y,
-                         cudaStream_t st, const float* q_norm, const float* k_norm, const float2* rope, float eps,
-                         int kv_ready) {
+template <int HD, int ST, bool WIN>
+static int attention_launch(const AttnPlan& p, const float* qkv, int ld, int n_seqs, int block_len,
+                            const AttnSeq* seqs_dev, int nq, int nkv, float scale_log2, float* part, float* y,
+                            cudaStream_t st, const float* q_norm, const float* k_norm, const float2* rope, float eps,
+                            int kv_ready) {
     dim3 grid(p.nsplit, nkv * p.qtiles, n_seqs);
     if (p.gmerge) {
-        cudaError_t e = launch(attn_cluster_kernel<HD, ST>, grid, dim3(kAttnWarps * 32), sizeof(AttnSmem<HD, ST>), st,
-                               qkv, ld, block_len, seqs_dev, nq, nkv, p.qtiles, p.nsplit, scale_log2, y, q_norm,
+        cudaError_t e = launch(attn_cluster_kernel<HD, ST, WIN>, grid, dim3(kAttnWarps * 32), sizeof(AttnSmem<HD, ST>),
+                               st, qkv, ld, block_len, seqs_dev, nq, nkv, p.qtiles, p.nsplit, scale_log2, y, q_norm,
                                k_norm, rope, eps, part, kv_ready);
         if (e != cudaSuccess) return (int)e;
         return (int)launch(attn_merge_kernel<HD>, dim3(kAttnQ / (8 / kMergeWays), nkv * p.qtiles * n_seqs), dim3(256), 0, st,
                            (const float*)part, p.nsplit, p.qtiles, nkv, nq, block_len, y);
     }
-    return (int)launch_cluster(attn_cluster_kernel<HD, ST>, grid, dim3(kAttnWarps * 32), sizeof(AttnSmem<HD, ST>), st,
-                               p.nsplit, qkv, ld, block_len, seqs_dev, nq, nkv, p.qtiles, p.nsplit, scale_log2, y,
-                               q_norm, k_norm, rope, eps, (float*)nullptr, kv_ready);
+    return (int)launch_cluster(attn_cluster_kernel<HD, ST, WIN>, grid, dim3(kAttnWarps * 32),
+                               sizeof(AttnSmem<HD, ST>), st, p.nsplit, qkv, ld, block_len, seqs_dev, nq, nkv, p.qtiles,
+                               p.nsplit, scale_log2, y, q_norm, k_norm, rope, eps, (float*)nullptr, kv_ready);
+}
+
+template <int HD, int ST>
+static int attention_run(const AttnPlan& p, const float* qkv, int ld, int n_seqs, int block_len,
+                         const AttnSeq* seqs_dev, int nq, int nkv, float scale_log2, float* part, float* y,
+                         cudaStream_t st, const float* q_norm, const float* k_norm, const float2* rope, float eps,
+                         int kv_ready, bool windowed) {
+    if (windowed)
+        return attention_launch<HD, ST, true>(p, qkv, ld, n_seqs, block_len, seqs_dev, nq, nkv, scale_log2, part, y,
+                                              st, q_norm, k_norm, rope, eps, kv_ready);
+    return attention_launch<HD, ST, false>(p, qkv, ld, n_seqs, block_len, seqs_dev, nq, nkv, scale_log2, part, y, st,
+                                           q_norm, k_norm, rope, eps, kv_ready);
 }
 
 template <int HD>
 static int attention_hd(const float* qkv, int ld, int n_seqs, int block_len, const AttnSeq* seqs_dev, int max_ctx,
                         int nq, int nkv, float scale, float* part, int64_t part_floats, float* y, int num_sms,
                         cudaStream_t st, const float* q_norm, const float* k_norm, const float2* rope, float eps,
-                        int kv_ready) {
+                        int kv_ready, bool windowed) {
     AttnPlan p = attn_plan_hd<HD>(n_seqs, block_len, max_ctx, nq, nkv, num_sms, true);
     const int64_t need = (int64_t)nkv * p.qtiles * n_seqs * p.nsplit * kAttnKH * kAttnQ * (HD + 4);
     if (p.gmerge && (part == nullptr || part_floats < need))  // no room for the partial rows: clusters
@@ -1256,20 +1273,20 @@ static int attention_hd(const float* qkv, int ld, int n_seqs, int block_len, con
     const float scale_log2 = scale * 1.4426950408889634f;
     if (p.stages == 1)
         return attention_run<HD, 1>(p, qkv, ld, n_seqs, block_len, seqs_dev, nq, nkv, scale_log2, part, y, st, q_norm,
-                                    k_norm, rope, eps, kv_ready);
+                                    k_norm, rope, eps, kv_ready, windowed);
     return attention_run<HD, 2>(p, qkv, ld, n_seqs, block_len, seqs_dev, nq, nkv, scale_log2, part, y, st, q_norm,
-                                k_norm, rope, eps, kv_ready);
+                                k_norm, rope, eps, kv_ready, windowed);
 }
 
 int attention(const float* qkv, int ld, int n_seqs, int block_len, const AttnSeq* seqs_dev, int max_ctx, int nq,
               int nkv, int hd, float scale, float* part, int64_t part_floats, float* y, int num_sms, cudaStream_t st,
-              const float* q_norm, const float* k_norm, const float2* rope, float eps, bool kv_ready) {
+              const float* q_norm, const float* k_norm, const float2* rope, float eps, bool kv_ready, bool windowed) {
     if ((q_norm == nullptr) != (k_norm == nullptr)) return (int)cudaErrorInvalidValue;
     if (hd == 128)
         return attention_hd<128>(qkv, ld, n_seqs, block_len, seqs_dev, max_ctx, nq, nkv, scale, part, part_floats, y,
-                                 num_sms, st, q_norm, k_norm, rope, eps, kv_ready ? 1 : 0);
+                                 num_sms, st, q_norm, k_norm, rope, eps, kv_ready ? 1 : 0, windowed);
     return attention_hd<64>(qkv, ld, n_seqs, block_len, seqs_dev, max_ctx, nq, nkv, scale, part, part_floats, y,
-                            num_sms, st, q_norm, k_norm, rope, eps, kv_ready ? 1 : 0);
+                            num_sms, st, q_norm, k_norm, rope, eps, kv_ready ? 1 : 0, windowed);
 }
 
 // ------------------------------------------------------------------ wait expiry

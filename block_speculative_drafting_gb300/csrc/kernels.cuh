@@ -123,7 +123,11 @@ int keys_to_tokens(const unsigned long long* keys, int T, uint32_t* tokens, cuda
 // in order, the choices (chosen) and each row's own top token (plain) from
 // the candidates, hp [n_seqs*rows][rank] (the rows' projection) and the f16
 // codebooks [V][rank].
-int topk_rows(const float* logits, int ldl, int V, int T, int k, unsigned long long* out, cudaStream_t st);
+// (two launches: the rows' parts, then their merge; scratch holds
+// T * topk_parts(V, k) * k keys)
+int topk_parts(int V, int k);
+int topk_rows(const float* logits, int ldl, int V, int T, int k, unsigned long long* scratch, unsigned long long* out,
+              cudaStream_t st);
 int select_tokens(const unsigned long long* cand, int k, const float* hp, int rank, const __half* book_p,
                   const __half* book_c, int V, const uint32_t* anchors, int n_seqs, int rows, uint32_t* chosen,
                   uint32_t* plain, cudaStream_t st);
@@ -260,13 +264,15 @@ constexpr int kNoCut = -(1 << 30);
 // through global memory (nothing in it needs to start at zero).
 // max_ctx: the largest context any sequence of the call may hold (its
 // capacity); the launch depends on it, each CTA's key range on the actual n.
+// windowed: some view has a cut (kNoCut everywhere otherwise: the kernel
+// without the window mask runs).
 // kv_ready: no kernel that may still run when this one starts (the chain of
 // programmatic dependent launches before it) writes the context stores, so
 // their copies may go out before the kernel's dependency wait.
 int attention(const float* qkv, int ld, int n_seqs, int block_len, const AttnSeq* seqs_dev, int max_ctx, int nq,
               int nkv, int hd, float scale, float* part, int64_t part_floats, float* y, int num_sms, cudaStream_t st,
               const float* q_norm = nullptr, const float* k_norm = nullptr, const float2* rope = nullptr,
-              float eps = 0.f, bool kv_ready = false);
+              float eps = 0.f, bool kv_ready = false, bool windowed = false);
 int64_t attn_scratch_floats(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int hd, int num_sms);
 // Kernels one attention call with part_floats of scratch launches (2 when
 // the key splits merge through global memory: the split kernel, then the
