@@ -396,16 +396,19 @@ def run_ours(args, wl):
         step()
     barrier()
     n0 = model.launch_count()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # one event between steps as well: the per-step spread (p10 / p50 / p90)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     t_wall0 = time.time()
-    e0.record(stream)
-    for _ in range(args.steps):
+    evs[0].record(stream)
+    for i in range(args.steps):
         step()
-    e1.record(stream)
+        evs[i + 1].record(stream)
     barrier()
     t_wall1 = time.time()
     launches = model.launch_count() - n0
-    ms = e0.elapsed_time(e1) / args.steps
+    ms = evs[0].elapsed_time(evs[-1]) / args.steps
+    per_step = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps))
+    pct = {f"ms_p{q}": per_step[min(len(per_step) - 1, int(q / 100 * len(per_step)))] for q in (10, 50, 90)}
     clocks.stop()
     clk = clocks.summary(t_wall0, t_wall1)
     if dist:
@@ -483,7 +486,7 @@ def run_ours(args, wl):
             "config": {"workload": wl.name, "n_seqs": wl.n_seqs, "ctx": wl.ctx, "block": B,
                        "prefill": wl.prefill, "step": case["desc"], "parallelism": f"replicas x{world}",
                        "l2": case["l2"]},
-            "block_latency_ms": ms, "hbm_gbs_step": step_bytes / (ms * 1e-3) / 1e9,
+            "block_latency_ms": ms, **pct, "hbm_gbs_step": step_bytes / (ms * 1e-3) / 1e9,
             "algorithmic_bytes_per_step": step_bytes, "profiled_ms_per_step": prof_ms,
             "roofline": roofline, "kernels": kernels, "e2e": e2e, "cpu_baseline": cpu,
             "gpu_launches": launches, "clocks": clk, "setup_s": setup_s,

@@ -378,7 +378,6 @@ __global__ void select_kernel(const unsigned long long* __restrict__ cand, int k
     for (int j = 0; j < rows; ++j) {
         const int r = s * rows + j;
         float best = -INFINITY;
-        int best_c = 0;
         uint32_t best_t = 0;
         for (int c0 = 0; c0 < k; c0 += 32) {
             const int c = c0 + lane;
@@ -413,20 +412,16 @@ __global__ void select_kernel(const unsigned long long* __restrict__ cand, int k
             if (c0 == 0) {
                 // the first candidate stands unless one scores strictly higher
                 best_t = __shfl_sync(0xffffffffu, tok, 0);
-                best_c = 0;
                 if (v > -INFINITY) {
                     best = v;
-                    best_c = vc;
                     best_t = vt;
                 }
             } else if (v > best) {
                 best = v;
-                best_c = vc;
                 best_t = vt;
             }
             if (c0 == 0 && lane == 0) plain[r] = tok;
         }
-        (void)best_c;
         prev = best_t;
         if (lane == 0) chosen[r] = prev;
     }

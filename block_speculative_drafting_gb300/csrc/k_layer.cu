@@ -39,6 +39,23 @@ DF_DEV float row_reduce(float v, float* red) {
     return r;
 }
 
+// The same over NT threads (NT / 32 warps).
+template <bool kMax, int NT>
+DF_DEV float row_reduce_nt(float v, float* red) {
+    v = kMax ? warp_max(v) : warp_sum(v);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        float u = threadIdx.x < NT / 32 ? red[threadIdx.x] : 0.f;  // 0: the identity of both (the max is of |x|)
+        u = kMax ? warp_max(u) : warp_sum(u);
+        if (threadIdx.x == 0) red[32] = u;
+    }
+    __syncthreads();
+    float r = red[32];
+    __syncthreads();
+    return r;
+}
+
 // Zero `n` floats at `p`, spread over the grid (a side duty that clears the
 // buffer a later kernel accumulates into).
 DF_DEV void zero_side(float* p, int64_t n) {
@@ -88,8 +105,8 @@ __global__ void __launch_bounds__(kRowThreads) rms_rows_kernel(const float* __re
 // n <= 4 * NV * kRowThreads.
 DF_DEV bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-template <int NV>
-__global__ void __launch_bounds__(kRowThreads) rms_rows_reg_kernel(const float* __restrict__ src, int ld_src, RowMap map,
+template <int NV, int NT = kRowThreads>
+__global__ void __launch_bounds__(NT, NT == kRowThreads || NV > 12 ? 1 : 2) rms_rows_reg_kernel(const float* __restrict__ src, int ld_src, RowMap map,
                                                                    int n, const float* __restrict__ w, float eps,
                                                                    float* __restrict__ out_f32, int ld_out,
                                                                    int8_t* __restrict__ out_codes,
@@ -115,7 +132,7 @@ __global__ void __launch_bounds__(kRowThreads) rms_rows_reg_kernel(const float* 
     float ss = 0.f;
 #pragma unroll
     for (int u = 0; u < NV; ++u) {
-        const int c = threadIdx.x + u * kRowThreads;
+        const int c = threadIdx.x + u * NT;
         v[u] = c < n4 ? x4[c] : make_float4(0.f, 0.f, 0.f, 0.f);
         ss = fmaf(v[u].x, v[u].x, ss);
         ss = fmaf(v[u].y, v[u].y, ss);
@@ -123,12 +140,12 @@ __global__ void __launch_bounds__(kRowThreads) rms_rows_reg_kernel(const float* 
         ss = fmaf(v[u].w, v[u].w, ss);
     }
     if (w) {
-        ss = row_reduce<false>(ss, red);
+        ss = row_reduce_nt<false, NT>(ss, red);
         const float s = 1.f / sqrtf(ss / (float)n + eps);
         const float4* w4 = reinterpret_cast<const float4*>(w);
 #pragma unroll
         for (int u = 0; u < NV; ++u) {
-            const int c = threadIdx.x + u * kRowThreads;
+            const int c = threadIdx.x + u * NT;
             if (c < n4) {
                 const float4 g = w4[c];
                 v[u] = make_float4(v[u].x * s * g.x, v[u].y * s * g.y, v[u].z * s * g.z, v[u].w * s * g.w);
@@ -139,7 +156,7 @@ __global__ void __launch_bounds__(kRowThreads) rms_rows_reg_kernel(const float* 
         float4* o4 = reinterpret_cast<float4*>(out_f32 + (int64_t)i * ld_out);
 #pragma unroll
         for (int u = 0; u < NV; ++u) {
-            const int c = threadIdx.x + u * kRowThreads;
+            const int c = threadIdx.x + u * NT;
             if (c < n4) o4[c] = v[u];
         }
         return;
@@ -147,12 +164,12 @@ __global__ void __launch_bounds__(kRowThreads) rms_rows_reg_kernel(const float* 
     float amax = 0.f;
 #pragma unroll
     for (int u = 0; u < NV; ++u) amax = fmaxf(amax, amax4(v[u]));  // lanes past n hold zeros
-    amax = row_reduce<true>(amax, red);
+    amax = row_reduce_nt<true, NT>(amax, red);
     const float sx = __fdiv_rn(amax, 127.0f);
     uint32_t* q4 = reinterpret_cast<uint32_t*>(out_codes + (int64_t)i * ld_codes);
 #pragma unroll
     for (int u = 0; u < NV; ++u) {
-        const int c = threadIdx.x + u * kRowThreads;
+        const int c = threadIdx.x + u * NT;
         if (c < n4) q4[c] = codes4(v[u], sx);
     }
     if (threadIdx.x == 0) out_scale[i] = sx;
@@ -183,7 +200,15 @@ int rms_rows(const float* src, int ld_src, RowMap map, int rows, int n, const fl
         if (nv <= 1) return go(rms_rows_reg_kernel<1>);
         if (nv <= 2) return go(rms_rows_reg_kernel<2>);
         if (nv <= 4) return go(rms_rows_reg_kernel<4>);
-        return go(rms_rows_reg_kernel<8>);
+        // wider rows (the taps): 512 threads a row, so that two rows share an SM
+        const int nv512 = (n + 4 * 512 - 1) / (4 * 512);
+        auto go512 = [&](auto kern) {
+            const int extra512 = zero_buf && zero_n > 0 ? (int)std::min<int64_t>(256, zero_n / 4 / (512 * 4) + 1) : 0;
+            return (int)launch(kern, dim3(rows + extra512), dim3(512), 0, st, src, ld_src, map, n, w, eps, out_f32, ld_out,
+                               out_codes, out_scale, ld_codes, zero_buf, zero_n, rows);
+        };
+        if (nv512 <= 12) return go512(rms_rows_reg_kernel<12, 512>);
+        return go512(rms_rows_reg_kernel<16, 512>);
     }
     return (int)launch(rms_rows_kernel, dim3(rows), dim3(kRowThreads), 0, st, src, ld_src, map, n, w, eps, out_f32,
                        ld_out, out_codes, out_scale, ld_codes, zero_buf, zero_n);
