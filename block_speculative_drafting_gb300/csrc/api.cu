@@ -119,6 +119,9 @@ struct dflash_model {
     };
     std::vector<ProfRec> prof_open;
     std::vector<cudaEvent_t> ev_pool;
+    // recorded after a call's last copy from caller host memory: the call
+    // waits for it (the caller may reuse its buffer), not for the work after
+    cudaEvent_t copy_ev = nullptr;
     struct ProfSum {
         const char* name;
         int64_t launches = 0;
@@ -400,6 +403,7 @@ int build_model(dflash_model* m, const dflash_weights* w, bool on_dev, cudaStrea
     CK(m, cudaMemset(m->err_dev, 0, sizeof(int)));
     CK(m, dalloc(m, &m->chain_bar, 1));
     CK(m, cudaMemset(m->chain_bar, 0, sizeof(unsigned)));
+    CK(m, cudaEventCreateWithFlags(&m->copy_ev, cudaEventDisableTiming));
     {
         std::vector<int> rot(g.layers);
         for (int l = 0; l < g.layers; ++l) rot[l] = m->norope[l] ? 0 : 1;
@@ -1087,6 +1091,7 @@ void dflash_free(dflash_model* m) {
         cudaEventDestroy(r.e1);
     }
     for (cudaEvent_t e : m->ev_pool) cudaEventDestroy(e);
+    if (m->copy_ev) cudaEventDestroy(m->copy_ev);
     if (m->err_host) cudaFreeHost(m->err_host);
     clear_graphs(m);
     if (m->cap_stream) cudaStreamDestroy(m->cap_stream);
@@ -1159,6 +1164,7 @@ int queue_rows(dflash_model* m, dflash_seq* s, const float* taps, int64_t n, boo
     }
     CK(m, cudaMemcpyAsync(s->pend + (s->pend_off + s->pending) * tw, taps, (size_t)n * tw * sizeof(float),
                           on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, st));
+    if (!on_device) CK(m, cudaEventRecord(m->copy_ev, st));
     s->pending += n;
     return DFLASH_OK;
 }
@@ -1178,6 +1184,7 @@ int settle_rows(dflash_model* m, dflash_seq* s, const float* taps, int64_t n_row
         const float* src = taps + r0 * m->tap_w;
         if (!taps_on_device) {
             CK(m, cudaMemcpyAsync(m->a_taps.p, src, (size_t)n * m->tap_w * sizeof(float), cudaMemcpyHostToDevice, st));
+            CK(m, cudaEventRecord(m->copy_ev, st));
             src = P<float>(m->a_taps);
         }
         const int64_t pos2[2] = {first + len + r0, len + r0};
@@ -1303,11 +1310,10 @@ int dflash_ctx_append(dflash_model* m, dflash_seq* s, int64_t pos, const float* 
         rc = settle_rows(m, s, taps, n_rows, taps_on_device != 0, st);
     }
     if (rc) return rc;
-    if (!taps_on_device && n_rows > 0) {
-        CK(m, cudaMemcpyAsync(m->err_host, m->err_dev, sizeof(int), cudaMemcpyDeviceToHost, st));
-        CK(m, cudaStreamSynchronize(st));
-        if (*m->err_host) return device_wait_expired(m);
-    }
+    // host taps: back once they are copied; a wait that expires in this
+    // work is reported by the next call that reads the device (a block with
+    // host buffers)
+    if (!taps_on_device && n_rows > 0) CK(m, cudaEventSynchronize(m->copy_ev));
     return DFLASH_OK;
 }
 
@@ -1322,6 +1328,7 @@ int dflash_ctx_queue(dflash_model* m, dflash_seq* s, int64_t pos, const float* t
     rc = seq_place(m, s, pos, n_rows);
     if (!rc) rc = queue_rows(m, s, taps, n_rows, taps_on_device != 0, st);
     if (rc) return rc;
+    if (!taps_on_device && n_rows > 0) CK(m, cudaEventSynchronize(m->copy_ev));  // the caller's rows are copied
     // past the queue's limit the oldest rows go through, a multiple of the granule
     int64_t limit = kPendingRows;
     bool all_windowed = true;

@@ -223,8 +223,11 @@ DFLASH_API int dflash_seq_span(const dflash_seq* seq, int64_t* first, int64_t* n
  * starts the context over at pos (next counts queued rows, see
  * dflash_ctx_queue).  The rows are settled at once, after the queued rows
  * still held (`push_context`: queue, then settle).  n_rows == 0 applies the
- * position rule and settles the queue.  Host taps: the call returns after
- * the rows are copied; device taps: the work is queued on `stream`.
+ * position rule and settles the queue.  Host taps: the call returns once
+ * the rows are copied (the caller may reuse its buffer; the work itself may
+ * still run, and a device wait that expires in it is reported by the next
+ * call that reads the device back: a block with host buffers); device taps:
+ * the work is queued on `stream`.
  * Errors: EINVAL (null taps with n_rows > 0, n_rows < 0, pos < 0),
  * ECAPACITY (the context would exceed max_ctx_rows), ECUDA.
  */
