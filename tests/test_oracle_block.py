@@ -207,6 +207,74 @@ def test_no_rope_layers_see_the_context_as_a_set(model):
     assert np.max(np.abs(pa - pb)) > 1e-6 * np.max(np.abs(pa))
 
 
+@pytest.mark.parametrize("window", [0, 3, 5, 12, 40])
+def test_zero_queries_average_the_visible_values(window):
+    """With Wq = 0 every score is 0, so each query head's output is the plain
+    mean of its KV head's values over exactly the keys its row sees: the
+    context positions in the row's window plus every block row (the block is
+    not causal).  With Wd = 0 as well, each layer adds Wo . mean to the rows,
+    and the block reduces to sums and matrix products written out here,
+    with no softmax, key ordering or position bookkeeping of the oracle's."""
+    wl = W.WORKLOADS["tiny_f32"]
+    g = dataclasses.replace(wl.geom, window=window)
+    w = W.make_weights(g)
+    for lw in w["layers"]:
+        lw["q"][:] = 0
+        lw["down"][:] = 0
+    n, anchor, tok = 30, 30, 17
+    taps = W.make_taps(g, n)
+    mz = OracleModel(g, w)
+    s = OracleSeq(mz)
+    s.append(0, taps)
+    logits, _ = block(mz, s, tok, anchor)
+
+    f64 = lambda a: np.asarray(a, dtype=np.float64)
+
+    def norm_rows(x, gain):
+        return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + g.eps) * f64(gain)
+
+    rows, kv, hd, rep = g.block, g.kv_heads, g.head_dim, g.rep
+    t = norm_rows(f64(taps) @ f64(w["fc"]).T, w["hidden_norm"])
+    h = f64(w["embed"][[tok] + [g.mask] * (rows - 1)])
+    for lw in w["layers"]:
+        vc = (t @ f64(lw["v"]).T).reshape(n, kv, hd)
+        vb = (norm_rows(h, lw["in_norm"]) @ f64(lw["v"]).T).reshape(rows, kv, hd)
+        y = np.empty((rows, g.heads, hd))
+        for r in range(rows):
+            # row r sits at position anchor + r and sees the context from
+            # anchor + r + 1 - window on (none of it once that is past the end)
+            lo = min(max(anchor + r + 1 - window, 0), n) if window else 0
+            mean = (vc[lo:].sum(0) + vb.sum(0)) / (n - lo + rows)  # [kv, hd]
+            y[r] = mean[np.arange(g.heads) // rep]
+        h = h + y.reshape(rows, -1) @ f64(lw["o"]).T
+    ref = norm_rows(h[1:], w["norm"]) @ f64(w["head"]).T
+    np.testing.assert_allclose(logits, ref, rtol=1e-10, atol=1e-12 * np.max(np.abs(ref)))
+
+
+def test_block_depends_only_on_relative_positions(model):
+    """Rotary attention sees only position differences, so the same context
+    held from position 0 or from position 64, with the block anchored the
+    same distance after it, gives the same logits up to the rounding of the
+    angles: each is one f32 product position x inv_freq, off by at most
+    2^-24 of itself (under 1e-5 rad for positions below 110), which moves a
+    logit by far less than the 1e-4 of max|logit| allowed here.  A block
+    anchored one position later -- the off-by-one the test guards against --
+    moves the logits by over a tenth of max|logit|."""
+    m, _ = model
+    taps = W.make_taps(m.g, 21)
+    a, b = OracleSeq(m), OracleSeq(m)
+    a.append(0, taps)
+    b.append(64, taps)
+    assert (b.first, b.len) == (64, 21)
+    la, ta = block(m, a, 9, 21)
+    lb, tb = block(m, b, 9, 85)
+    top = np.max(np.abs(la))
+    np.testing.assert_allclose(la, lb, rtol=0, atol=1e-4 * top)
+    assert (ta == tb).all()
+    lc, _ = block(m, a, 9, 22)
+    assert np.max(np.abs(lc - la)) > 1e-2 * top
+
+
 # ------------------------------------------------------------ row convolution
 def test_row_conv_shift_closed_form():
     """Kernels of two rows with no dynamic part: output = (I + c S) x with S
