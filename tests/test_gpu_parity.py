@@ -29,11 +29,13 @@ def _dfl():
 class Pair:
     """A GPU model and an oracle model on the same weights."""
 
-    def __init__(self, name, **changes):
+    def __init__(self, name, edit=None, **changes):
         wl = W.WORKLOADS[name]
         self.wl = wl
         self.g = dataclasses.replace(wl.geom, **changes) if changes else wl.geom
         self.w = W.make_weights(self.g)
+        if edit is not None:
+            edit(self.w)  # a special case's weights, changed in place before either side sees them
         self.gpu = _dfl().Model(self.g, self.w)
         self.ora = OracleModel(self.g, self.w)
 
@@ -378,6 +380,32 @@ def test_windows_and_no_rope_match_oracle(name, forced):
     anchors = [int(a) for a in W.make_anchors(g, 2)]
     sc.block([0, 1], anchors, [40, 25], g.block)
     sc.block([0], [anchors[1]], [34], g.block)
+    sc.run(forced).check(forced)
+
+
+def _zero_queries_and_down(w):
+    for lw in w["layers"]:
+        lw["q"][:] = 0
+        lw["down"][:] = 0
+
+
+@pytest.mark.parametrize("name", ["tiny_f32", "small_q4"])
+@pytest.mark.parametrize("forced", [True, False])
+@pytest.mark.parametrize("window", [0, 3])
+def test_equal_scores_match_oracle(name, forced, window):
+    """Wq = 0 (and Wd = 0): every attention score is exactly 0, so each row's
+    softmax is uniform over the keys it sees -- the degenerate case of the
+    split-key online softmax, whose oracle side is pinned by a closed form.
+    A window of 3 (shorter than the block) leaves the later rows no context
+    key at all, only the block's rows."""
+    p = Pair(name, edit=_zero_queries_and_down, window=window)
+    g = p.g
+    n = p.wl.ctx
+    sc = Script(p, 1, n + 16)
+    sc.append(0, 0, W.make_taps(g, n))
+    anchor = int(W.make_anchors(g, 1)[0])
+    sc.block([0], [anchor], [n], g.block)
+    sc.block([0], [anchor], [n], 5)
     sc.run(forced).check(forced)
 
 
