@@ -35,6 +35,14 @@ import sys
 import threading
 import time
 
+# torchrun starts every rank with one OpenMP thread; the reference arm does its
+# work on rank 0 alone, so that rank takes the host's cores as a plain run does
+# (the BLAS reads the count when numpy loads)
+if (os.environ.get("TORCHELASTIC_RUN_ID") and os.environ.get("RANK", "0") == "0"
+        and ("--impl=reference" in sys.argv
+             or any(a == "--impl" and b == "reference" for a, b in zip(sys.argv, sys.argv[1:])))):
+    os.environ["OMP_NUM_THREADS"] = str(os.cpu_count() or 1)
+
 import numpy as np
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
