@@ -367,6 +367,23 @@ def build_case(model, wl, dev):
     }
 
 
+def max_over_ranks(x, dist=None, device="cpu"):
+    """The largest of every rank's `x` (a time of the timed region): the job
+    takes as long as its slowest rank.  Without a process group, x itself."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, units_per_rank, seconds):
+    """Units all ranks processed per second of the slowest rank (weak scaling:
+    each rank runs the same workload as an independent replica)."""
+    return world * units_per_rank / seconds
+
+
 def run_ours(args, wl):
     import torch
 
@@ -419,11 +436,8 @@ def run_ours(args, wl):
     pct = {f"ms_p{q}": per_step[min(len(per_step) - 1, int(q / 100 * len(per_step)))] for q in (10, 50, 90)}
     clocks.stop()
     clk = clocks.summary(t_wall0, t_wall1)
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * units / (ms * 1e-3)
+    ms = max_over_ranks(ms, dist, dev)
+    value = job_throughput(world, units, ms * 1e-3)
 
     # profiled pass: the same steps with every launch bracketed by events
     model.profile_start()
@@ -472,11 +486,8 @@ def run_ours(args, wl):
         step_host()
     barrier()
     e2e_s = (time.perf_counter() - t0) / k_e2e
-    if dist:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e = {"value": world * units / e2e_s, "unit": unit, "ms_per_step": e2e_s * 1e3,
+    e2e_s = max_over_ranks(e2e_s, dist, dev)
+    e2e = {"value": job_throughput(world, units, e2e_s), "unit": unit, "ms_per_step": e2e_s * 1e3,
            "h2d_bytes_per_step": case["h2d"], "d2h_bytes_per_step": case["d2h"]}
 
     cpu = None
