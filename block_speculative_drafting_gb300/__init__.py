@@ -256,6 +256,11 @@ class Model:
     def launch_count(self) -> int:
         return int(lib().dflash_launch_count(self.handle))
 
+    def option(self, name: str, value: int):
+        """Switch one of the model's kernel choices (test hook): "tc", "dense",
+        "head_bound" (include/dflash.h, dflash_debug_option)."""
+        self._check(lib().dflash_debug_option(self.handle, name.encode(), int(value)))
+
     # ---------------------------------------------------------------- test hooks
     def q4_codes(self, matrix_id: int, rows: int, cols: int, stream=None):
         codes = np.empty((rows, cols), dtype=np.int8)

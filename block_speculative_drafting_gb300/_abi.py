@@ -72,6 +72,7 @@ _SIGS = {
     "dflash_profile_entry": (C.c_int, [_VP, C.c_int32, C.POINTER(C.c_char_p), C.POINTER(C.c_int64),
                                        C.POINTER(C.c_double), C.POINTER(C.c_double)]),
     "dflash_launch_count": (C.c_int64, [_VP]),
+    "dflash_debug_option": (C.c_int, [_VP, C.c_char_p, C.c_int64]),
     "dflash_debug_q4_codes": (C.c_int, [_VP, C.c_int32, _VP, _VP, _VP]),
     "dflash_debug_head_codes": (C.c_int, [_VP, _VP, _VP, _VP]),
     "dflash_debug_q4_groupsums": (C.c_int, [_VP, C.c_int32, _VP, C.c_int32, _VP, _VP]),

@@ -5,7 +5,6 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
-#include <functional>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -74,19 +73,24 @@ struct dflash_model {
     // layouts of the packed 4-bit matrices (the same for every layer)
     Q4Layout L_fc{}, L_kvctx{}, L_qkv{}, L_o{}, L_gu{}, L_down{};
     int* err_dev = nullptr;   // raised by a kernel whose bounded wait expired
-    unsigned* chain_bar = nullptr;  // the chain kernel's barrier counter (zero between launches)
     // per layer: the window (positions a block row sees back, 0 = all) and
     // whether queries and keys carry the rotary position; rot_dev: the
     // latter on the device (kv_append)
     std::vector<int32_t> win, norope;
+    // per layer: the attention's accumulate-mode reference (log2 domain): a
+    // bound on every score the layer's normed queries and keys can make, or
+    // NaN when the gains are too large for the mode's f32 range
+    std::vector<float> attn_ref;
     int* rot_dev = nullptr;
     // the candidate selector: S [rank][H] f32, codebooks P, C [V][rank] f16
     float* sel = nullptr;
     __half *book_p = nullptr, *book_c = nullptr;
     DevBuf hn, hp, cand, plain;  // its scratch: normed rows, their projection, candidates, own top tokens
-    bool use_chain = false;         // run a block's (and a short append's) steps as chain programs
-    bool use_tc = true;             // matmuls of more than 16 rows on the tcgen05 kernel (DFLASH_TC=0: mma.sync)
-    bool use_dense = true;          // ... from dense f16 weight copies (DFLASH_DENSE=0: dequantise in the kernel)
+    // options (dflash_debug_option): matmuls of more than 16 rows on the
+    // tcgen05 kernels (off: the mma.sync kernel), from dense f16 weight copies
+    // (off: dequantised in the kernel)
+    bool use_tc = true;
+    bool use_dense = true;
     // dense f16 copies of the matrices for the many-row path, built on first need:
     // the 4-bit matrices as (hi, lo) planes [N][K], the head's codes [vocab][hidden]
     struct DenseMat {
@@ -99,8 +103,8 @@ struct dflash_model {
     int* head_norm2 = nullptr;  // squared code norm of each vocabulary row (the dense head's guard)
     unsigned long long head_norm2_max = 0;
     // the dense head trusts its f32 sums while |x|^2 |w|^2 <= this (2^48:
-    // every partial sum within 2^24); DFLASH_HEAD_BOUND sets it (0 recomputes
-    // every element as an integer dot product)
+    // every partial sum within 2^24); option "head_bound" lowers it (0
+    // recomputes every element as an integer dot product)
     unsigned long long head_bound = 1ull << 48;
     bool dense_ready = false;
     // set while run_enqueue captures a graph of the library's own: the
@@ -401,27 +405,12 @@ int build_model(dflash_model* m, const dflash_weights* w, bool on_dev, cudaStrea
     m->L_down = make_layout(H, I);
     CK(m, dalloc(m, &m->err_dev, 1));
     CK(m, cudaMemset(m->err_dev, 0, sizeof(int)));
-    CK(m, dalloc(m, &m->chain_bar, 1));
-    CK(m, cudaMemset(m->chain_bar, 0, sizeof(unsigned)));
     CK(m, cudaEventCreateWithFlags(&m->copy_ev, cudaEventDisableTiming));
     {
         std::vector<int> rot(g.layers);
         for (int l = 0; l < g.layers; ++l) rot[l] = m->norope[l] ? 0 : 1;
         CK(m, dalloc(m, &m->rot_dev, (size_t)g.layers));
         CK(m, cudaMemcpy(m->rot_dev, rot.data(), rot.size() * sizeof(int), cudaMemcpyHostToDevice));
-    }
-    {
-        // DFLASH_CHAIN=1 runs the steps between two attentions as one persistent
-        // chain kernel each (measured slower than one kernel per step on the
-        // context-2048 block: kept as an option for comparisons)
-        const char* ev = getenv("DFLASH_CHAIN");
-        m->use_chain = ev && ev[0] == '1';
-        const char* tv = getenv("DFLASH_TC");
-        m->use_tc = !(tv && tv[0] == '0');
-        const char* dv = getenv("DFLASH_DENSE");
-        m->use_dense = !(dv && dv[0] == '0');
-        const char* bv = getenv("DFLASH_HEAD_BOUND");
-        if (bv && bv[0]) m->head_bound = std::min(strtoull(bv, nullptr, 10), 1ull << 48);
     }
     CK(m, cudaMallocHost(&m->err_host, sizeof(int)));
     *m->err_host = 0;
@@ -551,6 +540,25 @@ int build_model(dflash_model* m, const dflash_weights* w, bool on_dev, cudaStrea
             CK(m, copy_f32(m, Ly.down_f, w->down[l], (size_t)H * I, on_dev));
         }
     }
+    // The attention's accumulate-mode reference per layer.  After the per-head
+    // RMSNorm a query has |q| <= sqrt(hd) * max|q_norm| (the normed row's
+    // squares sum to hd * ms / (ms + eps) < hd), likewise a key, so a score in
+    // the kernel's log2 domain obeys |s| <= sqrt(hd) * max|gq| * max|gk| *
+    // log2(e) (the 1/sqrt(hd) scale taken in).  Rescaled partial sums then
+    // stay within [2^(-2 ref), 1]: usable while 2 ref + 2 < 126.
+    m->attn_ref.assign(L, NAN);
+    for (int l = 0; l < L; ++l) {
+        std::vector<float> gq(hd), gk(hd);
+        CK(m, cudaMemcpy(gq.data(), m->layers[l].q_norm, hd * sizeof(float), cudaMemcpyDeviceToHost));
+        CK(m, cudaMemcpy(gk.data(), m->layers[l].k_norm, hd * sizeof(float), cudaMemcpyDeviceToHost));
+        double aq = 0, ak = 0;
+        for (int i = 0; i < hd; ++i) {
+            aq = std::max(aq, (double)std::fabs(gq[i]));
+            ak = std::max(ak, (double)std::fabs(gk[i]));
+        }
+        const double ref = std::sqrt((double)hd) * aq * ak * 1.4426950408889634 * (1.0 + 1e-3) + 0.5;
+        if (std::isfinite(ref) && 2 * ref + 2 < 126) m->attn_ref[l] = (float)ref;
+    }
     CK(m, dalloc(m, &m->k_norm_dev, L));
     CK(m, cudaMemcpy(m->k_norm_dev, knorm_ptrs.data(), L * sizeof(float*), cudaMemcpyHostToDevice));
     CK(m, cudaStreamSynchronize(st));
@@ -666,7 +674,7 @@ int ensure_dense(dflash_model* m, cudaStream_t st) {
 // The dense copy of a packed 4-bit matrix's rows [row0, row0 + N), or null.
 bool dense_of(const dflash_model* m, const uint8_t* packed, int row0, int N, int K, const __half** hi,
               const __half** lo) {
-    if (!m->dense_ready) return false;
+    if (!m->dense_ready || !m->use_dense) return false;
     for (const auto& d : m->dense)
         if (d.packed == packed && d.K == K && row0 + N <= d.N) {
             *hi = d.hi + (size_t)row0 * K;
@@ -714,7 +722,7 @@ int run_head(dflash_model* m, QAct xh, int D, float* logit_out, unsigned long lo
         __half* x16 = P<__half>(m->x16);
         // the rows' squared code norms sit after their f16 codes
         int* xn2 = reinterpret_cast<int*>(x16 + (size_t)D * H);
-        if (m->dense_ready && m->head16 && m->x16.bytes >= (size_t)D * (H * sizeof(__half) + sizeof(int))) {
+        if (m->dense_ready && m->use_dense && m->head16 && m->x16.bytes >= (size_t)D * (H * sizeof(__half) + sizeof(int))) {
             KL(m, "act_f16", 1, (double)D * H * 3 + (double)D * 4, st,
                codes_to_f16(xh.codes, xh.ld, D, H, x16, xn2, m->num_sms, st));
             KL(m, "head_tc", 1, hb + (double)g.vocab * H + (double)g.vocab * 4, st,
@@ -818,95 +826,7 @@ int trace_site(dflash_model* m, cudaStream_t st, int rows, int cols, int8_t* cod
         if (rc__) return rc__;     \
     } while (0)
 
-// ------------------------------------------------------------------ chain programs
-// A matvec stage over the whole (fused) matrix of N rows (N % 64 == 0).
-ChainStage mv_stage(const uint8_t* wp, Q4Layout L, int N, const int8_t* xc, const float* xs, int ldx, int T, float* y,
-                    int ldy) {
-    ChainStage c = {};
-    c.op = kChainMatvec;
-    c.wp = wp;
-    c.L = L;
-    c.g0 = 0;
-    c.ng = N / 64;
-    c.xc = xc;
-    c.xs = xs;
-    c.ldx = ldx;
-    c.T = T;
-    c.y = y;
-    c.ldy = ldy;
-    return c;
-}
-// A row stage (kChainRows: codes of rms(row, w), or of the row itself when
-// w is null; kChainSilu: codes of silu(g) * u of [g | u] rows of 2n).
-ChainStage row_stage(int op, const float* src, int ld_src, RowMap map, int rows, int n, const float* w, float eps,
-                     int8_t* codes, float* scale, int ld_codes, float* zero = nullptr, int64_t zero_n = 0) {
-    ChainStage c = {};
-    c.op = op;
-    c.src = src;
-    c.ld_src = ld_src;
-    c.map = map;
-    c.rows = rows;
-    c.n = n;
-    c.w = w;
-    c.eps = eps;
-    c.codes = codes;
-    c.scale = scale;
-    c.ld_codes = ld_codes;
-    c.zero = zero;
-    c.zero_n = zero_n;
-    return c;
-}
-
-// A chain program being built, with a hook after each stage (tracing: the
-// record of the quantisation site the stage wrote, and a forced decision).
-struct ChainBuild {
-    ChainProgram p{};
-    std::vector<std::function<int()>> hooks;
-    double bytes = 0;
-    void add(const ChainStage& st, double b, std::function<int()> hook = nullptr) {
-        p.s[p.n++] = st;
-        hooks.push_back(std::move(hook));
-        bytes += b;
-    }
-    void clear() {
-        p.n = 0;
-        hooks.clear();
-        bytes = 0;
-    }
-};
-
-// Launch a built program as one chain kernel; with tracing on, one launch
-// per stage with the stage's hook after it (the same device code).
-int run_chain(dflash_model* m, cudaStream_t st, ChainBuild& c) {
-    if (c.p.n == 0) return 0;
-    if (!m->tracing) {
-        KL(m, "chain", 1, c.bytes, st, chain_run(c.p, m->num_sms, m->chain_bar, m->err_dev, st));
-    } else {
-        for (int i = 0; i < c.p.n; ++i) {
-            ChainProgram one{};
-            one.n = 1;
-            one.s[0] = c.p.s[i];
-            KL(m, "chain", 1, 0.0, st, chain_run(one, m->num_sms, m->chain_bar, m->err_dev, st));
-            if (c.hooks[i]) {
-                const int rc = c.hooks[i]();
-                if (rc) return rc;
-            }
-        }
-    }
-    c.clear();
-    return 0;
-}
-
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
-
-// Whether rows of the block (or of an append) go through chain programs.
-bool chain_ok(const dflash_model* m, int rows) {
-    const dflash_geometry& g = m->g;
-    return m->use_chain && g.quant == DFLASH_QUANT_Q4G32 && rows >= 1 && rows <= 16 && rows < m->num_sms &&
-           m->num_sms >= 16 && g.hidden % 64 == 0 && m->qkv_w % 64 == 0 && (2 * g.intermediate) % 64 == 0 &&
-           m->kvctx_w % 64 == 0 && m->tap_w % 4 == 0 && m->tap_w <= kChainRowMax && g.hidden <= kChainRowMax &&
-           g.intermediate <= kChainRowMax && m->qd <= kChainRowMax && m->qd % 4 == 0 && g.intermediate % 4 == 0;
-}
 
 // Run `enqueue(stream)` (a fixed kernel sequence) on `st`: replayed from a
 // graph captured once per key, or directly when graphs are off (profiling,
@@ -964,31 +884,7 @@ int append_rows(dflash_model* m, dflash_seq* s, const float* taps_dev, int64_t n
     RowMap ident{1, 1, 0};
     float* t = P<float>(m->a_t);
     float* kv = P<float>(m->a_kv);
-    if (quant && chain_ok(m, rows) && al16(taps_dev)) {
-        // the same four steps as one chain program
-        int8_t* codes = P<int8_t>(m->a_codes);
-        float* sc = P<float>(m->a_scale);
-        ChainBuild c;
-        c.add(row_stage(kChainRows, taps_dev, m->tap_w, ident, rows, m->tap_w, nullptr, g.eps, codes, sc, m->tap_w, t,
-                        (int64_t)rows * H),
-              (double)rows * m->tap_w * 5, [&]() {
-                  return trace_site(m, st, rows, m->tap_w, codes, m->tap_w, sc, [&](float* v) {
-                      return rms_rows(taps_dev, m->tap_w, ident, rows, m->tap_w, nullptr, g.eps, v, m->tap_w, nullptr,
-                                      nullptr, 0, st);
-                  });
-              });
-        c.add(mv_stage(m->fc_p, m->L_fc, H, codes, sc, m->tap_w, rows, t, H), q4_bytes_of(H, m->tap_w, rows, true));
-        c.add(row_stage(kChainRows, t, H, ident, rows, H, m->hidden_norm, g.eps, codes, sc, H, kv,
-                        (int64_t)rows * m->kvctx_w),
-              (double)rows * H * 5, [&]() {
-                  return trace_site(m, st, rows, H, codes, H, sc, [&](float* v) {
-                      return rms_rows(t, H, ident, rows, H, m->hidden_norm, g.eps, v, H, nullptr, nullptr, 0, st);
-                  });
-              });
-        c.add(mv_stage(m->kvctx_p, m->L_kvctx, m->kvctx_w, codes, sc, H, rows, kv, m->kvctx_w),
-              q4_bytes_of(m->kvctx_w, H, rows, true));
-        APPLY(run_chain(m, st, c));
-    } else if (quant) {
+    if (quant) {
         // taps -> int8 rows (t cleared on the side); t = FC . Q(taps);
         // x = Q(rms(t, hidden_norm)) (kv cleared on the side); kv = [Wk;Wv]_all . x
         int8_t* codes = P<int8_t>(m->a_codes);
@@ -1395,10 +1291,22 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
             attn_bytes_l[l] += (double)as_all[(size_t)l * n_seqs + s].n * m->kd * 8;
         }
     const int64_t part_floats = attn_scratch_floats(n_seqs, B, max_ctx, g.heads, g.kv_heads, hd, m->num_sms);
+    // layers whose attention accumulates its key splits' rescaled partial
+    // rows (few units: a single sequence's 8 kv heads spread over every SM)
+    const int acc_split = quant ? attn_acc_plan(n_seqs, B, max_ctx, g.heads, g.kv_heads, hd, m->num_sms) : 0;
+    std::vector<char> acc_l(g.layers, 0);
+    bool any_acc = false;
+    for (int l = 0; l < g.layers; ++l) {
+        acc_l[l] = acc_split > 0 && !std::isnan(m->attn_ref[l]);
+        any_acc = any_acc || acc_l[l];
+    }
+    // qkv, then (accumulate mode) the attention's unnormalised output and its
+    // softmax sums: one buffer, cleared together before each layer's qkv
+    const int64_t qkv_zero = (int64_t)R * m->qkv_w + (any_acc ? (int64_t)R * (m->qd + g.heads) : 0);
     CK(m, ensure_m(m, m->h, (size_t)R * H * sizeof(float)));
     CK(m, ensure_m(m, m->xq, (size_t)R * (quant ? maxK : maxK * sizeof(float))));
     CK(m, ensure_m(m, m->xs, (size_t)R * sizeof(float)));
-    CK(m, ensure_m(m, m->qkv, (size_t)R * m->qkv_w * sizeof(float)));
+    CK(m, ensure_m(m, m->qkv, (size_t)qkv_zero * sizeof(float)));
     CK(m, ensure_m(m, m->y, (size_t)R * m->qd * sizeof(float)));
     CK(m, ensure_m(m, m->gu, (size_t)R * 2 * I * sizeof(float)));
     CK(m, ensure_m(m, m->part, (size_t)part_floats * sizeof(float)));
@@ -1449,12 +1357,33 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
     float* h = P<float>(m->h);
     float* qkv = P<float>(m->qkv);
     float* y = P<float>(m->y);
+    const float scale = 1.0f / sqrtf((float)hd);
+    float* yacc = qkv + (size_t)R * m->qkv_w;  // accumulate mode (any_acc)
+    float* lacc = yacc + (size_t)R * m->qd;
+    // the block's attention of layer l into y (or, accumulate mode, into
+    // yacc / lacc, which the clearing before the layer's qkv zeroed)
+    auto run_attention = [&](int l) -> int {
+        const Layer& Ly = m->layers[l];
+        const AttnSeq* aseq_dev = P<AttnSeq>(m->aseqs) + (size_t)l * n_seqs;
+        const float2* rl = m->norope[l] ? nullptr : P<float2>(m->rope);
+        if (acc_l[l]) {
+            KL(m, "attention", 1, attn_bytes_l[l] + (double)R * g.heads * (hd + 1) * 4, st,
+               attention_acc(qkv, m->qkv_w, n_seqs, B, aseq_dev, acc_split, g.heads, g.kv_heads, hd, scale, yacc, lacc,
+                             m->attn_ref[l], st, Ly.q_norm, Ly.k_norm, rl, g.eps, m->own_capture, m->win[l] > 0));
+        } else {
+            KL(m, "attention", attn_kernels(n_seqs, B, max_ctx, g.heads, g.kv_heads, hd, m->num_sms, part_floats),
+               attn_bytes_l[l], st,
+               attention(qkv, m->qkv_w, n_seqs, B, aseq_dev, max_ctx, g.heads, g.kv_heads, hd, scale,
+                         P<float>(m->part), part_floats, y, m->num_sms, st, Ly.q_norm, Ly.k_norm, rl, g.eps,
+                         m->own_capture, m->win[l] > 0));
+        }
+        return DFLASH_OK;
+    };
     float* gu = P<float>(m->gu);
     float* xf = P<float>(m->xq);  // the f32 path's normed rows
     int8_t* xq = P<int8_t>(m->xq);
     float* xs = P<float>(m->xs);
     RowMap ident{1, 1, 0};
-    const float scale = 1.0f / sqrtf((float)hd);
 
     // the embedding also writes the block rows' rotation table (cos, sin per
     // position and frequency) that the attention applies as it loads q and k
@@ -1465,72 +1394,6 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
     RowMap drafts{B - 1, B, 1};
     unsigned long long* keys = P<unsigned long long>(m->keys);
     uint32_t* tok_out = (io_on_device && draft_tok) ? draft_tok : P<uint32_t>(m->toks);
-    if (quant && chain_ok(m, R) && g.conv_kernel == 0 && g.selector_rank == 0) {
-        // the steps between two attentions as one chain program each:
-        // [x = Q(rms(h, in_norm)); qkv = W x] before the first attention, then per
-        // layer [Q(y); h += O y; x = Q(rms(h, post_norm)); gu = [G; U] x;
-        // a = Q(silu(g) u); h += D a; then the next layer's x and qkv, or the
-        // head's Q(rms(h, norm)) of the draft rows]
-        ChainBuild c;
-        auto add_in = [&](int l) {
-            const Layer& Ly = m->layers[l];
-            c.add(row_stage(kChainRows, h, H, ident, R, H, Ly.in_norm, g.eps, xq, xs, maxK, qkv, (int64_t)R * m->qkv_w),
-                  (double)R * H * 5, [&, l]() {
-                      return trace_site(m, st, R, H, xq, maxK, xs, [&, l](float* v) {
-                          return rms_rows(h, H, ident, R, H, m->layers[l].in_norm, g.eps, v, H, nullptr, nullptr, 0, st);
-                      });
-                  });
-            c.add(mv_stage(Ly.qkv_p, m->L_qkv, m->qkv_w, xq, xs, maxK, R, qkv, m->qkv_w),
-                  q4_bytes_of(m->qkv_w, H, R, true));
-        };
-        add_in(0);
-        APPLY(run_chain(m, st, c));
-        for (int l = 0; l < g.layers; ++l) {
-            const Layer& Ly = m->layers[l];
-            const AttnSeq* aseq_dev = P<AttnSeq>(m->aseqs) + (size_t)l * n_seqs;
-            KL(m, "attention", attn_kernels(n_seqs, B, max_ctx, g.heads, g.kv_heads, hd, m->num_sms, part_floats), attn_bytes_l[l], st,
-               attention(qkv, m->qkv_w, n_seqs, B, aseq_dev, max_ctx, g.heads, g.kv_heads, hd, scale, P<float>(m->part),
-                         part_floats, y, m->num_sms, st, Ly.q_norm, Ly.k_norm, m->norope[l] ? nullptr : rope, g.eps,
-                         m->own_capture, m->win[l] > 0));
-            c.add(row_stage(kChainRows, y, m->qd, ident, R, m->qd, nullptr, g.eps, xq, xs, maxK), (double)R * m->qd * 5,
-                  [&]() {
-                      return trace_site(m, st, R, m->qd, xq, maxK, xs, [&](float* v) {
-                          return rms_rows(y, m->qd, ident, R, m->qd, nullptr, g.eps, v, m->qd, nullptr, nullptr, 0, st);
-                      });
-                  });
-            c.add(mv_stage(Ly.o_p, m->L_o, H, xq, xs, maxK, R, h, H), q4_bytes_of(H, m->qd, R, true));
-            c.add(row_stage(kChainRows, h, H, ident, R, H, Ly.post_norm, g.eps, xq, xs, maxK, gu, (int64_t)R * 2 * I),
-                  (double)R * H * 5, [&]() {
-                      return trace_site(m, st, R, H, xq, maxK, xs, [&](float* v) {
-                          return rms_rows(h, H, ident, R, H, Ly.post_norm, g.eps, v, H, nullptr, nullptr, 0, st);
-                      });
-                  });
-            c.add(mv_stage(Ly.gu_p, m->L_gu, 2 * I, xq, xs, maxK, R, gu, 2 * I), q4_bytes_of(2 * I, H, R, true));
-            c.add(row_stage(kChainSilu, gu, 2 * I, ident, R, I, nullptr, g.eps, xq, xs, maxK), (double)R * I * 9, [&]() {
-                return trace_site(m, st, R, I, xq, maxK, xs, [&](float* v) {
-                    return silu_mul(gu, 2 * I, R, I, v, I, nullptr, nullptr, 0, st);
-                });
-            });
-            c.add(mv_stage(Ly.down_p, m->L_down, H, xq, xs, maxK, R, h, H), q4_bytes_of(H, I, R, true));
-            if (l + 1 < g.layers) {
-                add_in(l + 1);
-            } else {
-                c.add(row_stage(kChainRows, h, H, drafts, D, H, m->norm, g.eps, xq, xs, maxK,
-                                reinterpret_cast<float*>(keys), (int64_t)D * 2),
-                      (double)D * H * 5, [&]() {
-                          return trace_site(m, st, D, H, xq, maxK, xs, [&](float* v) {
-                              return rms_rows(h, H, drafts, D, H, m->norm, g.eps, v, H, nullptr, nullptr, 0, st);
-                          });
-                      });
-            }
-            APPLY(run_chain(m, st, c));
-        }
-        QAct xh{xq, xs, maxK};
-        const double hb = (double)g.vocab * H + (double)g.vocab * 4 + (double)D * H + (logit_out ? (double)D * g.vocab * 4 : 0.0);
-        APPLY(run_head(m, xh, D, logit_out, keys, hb, st));
-        KL(m, "keys_to_tokens", 1, (double)D * 12, st, keys_to_tokens(keys, D, tok_out, st));
-        return DFLASH_OK;
-    }
     // with a row convolution: x = conv_in(rms(h, norm)) before each
     // sub-layer, h += conv_out(its output) after it (a separate sequence of
     // launches; the sub-layers' own kernels are the same)
@@ -1570,24 +1433,22 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
                conv_rows(co, H, cd, nd, base, 1, kn, gs, H, R, B, h, H, nullptr, 0, nullptr, nullptr, 0, st));
             return DFLASH_OK;
         };
-        APPLY(conv_in(Ly.in_norm, Ly.a_base, Ly.a_proj, quant ? qkv : nullptr, quant ? (int64_t)R * m->qkv_w : 0,
-                      nullptr, 0));
+        APPLY(conv_in(Ly.in_norm, Ly.a_base, Ly.a_proj, quant ? qkv : nullptr, quant ? qkv_zero : 0, nullptr, 0));
         if (quant)
             APPLY(apply(m, Ly.qkv_p, nullptr, m->L_qkv, 0, m->qkv_w, H, nullptr, 0, R, qkv, m->qkv_w, false, maxK, st));
         else
             APPLY(apply(m, nullptr, Ly.qkv_f, Q4Layout{}, 0, m->qkv_w, H, xf, maxK, R, qkv, m->qkv_w, false, 0, st));
-        const AttnSeq* aseq_dev = P<AttnSeq>(m->aseqs) + (size_t)l * n_seqs;
-        KL(m, "attention", attn_kernels(n_seqs, B, max_ctx, g.heads, g.kv_heads, hd, m->num_sms, part_floats),
-           attn_bytes_l[l], st,
-           attention(qkv, m->qkv_w, n_seqs, B, aseq_dev, max_ctx, g.heads, g.kv_heads, hd, scale, P<float>(m->part),
-                     part_floats, y, m->num_sms, st, Ly.q_norm, Ly.k_norm, m->norope[l] ? nullptr : rope, g.eps,
-                     m->own_capture, m->win[l] > 0));
+        APPLY(run_attention(l));
         // co = O y (the streaming matvec adds: co cleared by the quantisation of y)
         if (quant) {
+            const float* ysrc = acc_l[l] ? yacc : y;
+            const float* ydiv = acc_l[l] ? lacc : nullptr;
             KL(m, "rms_quant", 1, (double)R * m->qd * 5, st,
-               rms_rows(y, m->qd, ident, R, m->qd, nullptr, g.eps, nullptr, 0, xq, xs, maxK, st, co, (int64_t)R * H));
+               rms_rows(ysrc, m->qd, ident, R, m->qd, nullptr, g.eps, nullptr, 0, xq, xs, maxK, st, co, (int64_t)R * H,
+                        ydiv, hd));
             TRACE(trace_site(m, st, R, m->qd, xq, maxK, xs, [&](float* v) {
-                return rms_rows(y, m->qd, ident, R, m->qd, nullptr, g.eps, v, m->qd, nullptr, nullptr, 0, st);
+                return rms_rows(ysrc, m->qd, ident, R, m->qd, nullptr, g.eps, v, m->qd, nullptr, nullptr, 0, st,
+                                nullptr, 0, ydiv, hd);
             }));
             APPLY(apply(m, Ly.o_p, nullptr, m->L_o, 0, H, m->qd, nullptr, 0, R, co, H, false, maxK, st));
         } else {
@@ -1616,7 +1477,7 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
         // attention half: x = rms(h, in_norm); q, k, v; norms and rotation; attention; h += O y
         if (quant) {
             KL(m, "rms_quant", 1, (double)R * H * 5, st,
-               rms_rows(h, H, ident, R, H, Ly.in_norm, g.eps, nullptr, 0, xq, xs, maxK, st, qkv, (int64_t)R * m->qkv_w));
+               rms_rows(h, H, ident, R, H, Ly.in_norm, g.eps, nullptr, 0, xq, xs, maxK, st, qkv, qkv_zero));
             TRACE(trace_site(m, st, R, H, xq, maxK, xs, [&](float* v) {
                 return rms_rows(h, H, ident, R, H, Ly.in_norm, g.eps, v, H, nullptr, nullptr, 0, st);
             }));
@@ -1626,15 +1487,17 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
             APPLY(apply(m, nullptr, Ly.qkv_f, Q4Layout{}, 0, m->qkv_w, H, xf, maxK, R, qkv, m->qkv_w, false, 0, st));
         }
         // q/k norms and rotation run inside the attention, as it loads them
-        const AttnSeq* aseq_dev = P<AttnSeq>(m->aseqs) + (size_t)l * n_seqs;
-        KL(m, "attention", attn_kernels(n_seqs, B, max_ctx, g.heads, g.kv_heads, hd, m->num_sms, part_floats), attn_bytes_l[l], st,
-           attention(qkv, m->qkv_w, n_seqs, B, aseq_dev, max_ctx, g.heads, g.kv_heads, hd, scale, P<float>(m->part),
-                     part_floats, y, m->num_sms, st, Ly.q_norm, Ly.k_norm, m->norope[l] ? nullptr : rope, g.eps,
-                         m->own_capture, m->win[l] > 0));
+        APPLY(run_attention(l));
         if (quant) {
-            KL(m, "rms_quant", 1, (double)R * m->qd * 5, st, rms_rows(y, m->qd, ident, R, m->qd, nullptr, g.eps, nullptr, 0, xq, xs, maxK, st));
+            // y (accumulate mode: yacc / lacc per head) -> int8 rows
+            const float* ysrc = acc_l[l] ? yacc : y;
+            const float* ydiv = acc_l[l] ? lacc : nullptr;
+            KL(m, "rms_quant", 1, (double)R * m->qd * 5, st,
+               rms_rows(ysrc, m->qd, ident, R, m->qd, nullptr, g.eps, nullptr, 0, xq, xs, maxK, st, nullptr, 0, ydiv,
+                        hd));
             TRACE(trace_site(m, st, R, m->qd, xq, maxK, xs, [&](float* v) {
-                return rms_rows(y, m->qd, ident, R, m->qd, nullptr, g.eps, v, m->qd, nullptr, nullptr, 0, st);
+                return rms_rows(ysrc, m->qd, ident, R, m->qd, nullptr, g.eps, v, m->qd, nullptr, nullptr, 0, st,
+                                nullptr, 0, ydiv, hd);
             }));
             APPLY(apply(m, Ly.o_p, nullptr, m->L_o, 0, H, m->qd, nullptr, 0, R, h, H, true, maxK, st));
         } else {
@@ -1837,6 +1700,23 @@ int dflash_profile_entry(const dflash_model* m, int32_t i, const char** name, in
 
 int64_t dflash_launch_count(const dflash_model* m) { return m ? m->launches : -1; }
 
+int dflash_debug_option(dflash_model* m, const char* name, int64_t value) {
+    if (!m || !name) return DFLASH_EINVAL;
+    const std::string opt(name);
+    if (opt == "tc") {
+        m->use_tc = value != 0;
+    } else if (opt == "dense") {
+        m->use_dense = value != 0;
+    } else if (opt == "head_bound") {
+        if (value < 0) return set_err(m, DFLASH_EINVAL, "head_bound < 0");
+        m->head_bound = std::min<unsigned long long>((unsigned long long)value, 1ull << 48);
+    } else {
+        return set_err(m, DFLASH_EINVAL, "unknown option " + opt);
+    }
+    clear_graphs(m);  // the captured kernel sequences may change
+    return DFLASH_OK;
+}
+
 // ------------------------------------------------------------------ test hooks
 int dflash_debug_q4_codes(dflash_model* m, int32_t id, int8_t* codes, uint16_t* scales, void* stream) {
     int rc = check_model(m);
@@ -2020,22 +1900,23 @@ int dflash_debug_read_kv(dflash_model* m, const dflash_seq* s, int32_t layer, in
 // The block's attention without any allocation.
 //
 // Some callers cannot allocate device memory at the moment they need the
-// attention: code running while another component captures a CUDA graph
-// (an allocation would break or be recorded into the capture), processes in
-// which a host framework owns every device byte through its own pool, or
-// latency-critical loops that must never block in the allocator.  For them,
-// dflash_attention_noalloc runs the same attention kernels as
-// dflash_debug_attention, but its scratch (the split partials and the
-// per-sequence context views) lives in the fixed array below, which is part of
-// this library's device image: every GPU that loads the library holds these
-// 16 MiB until the process exits.
+// attention: processes in which a host framework owns every device byte
+// through its own pool allocator (a cudaMalloc behind its back can fail, or
+// take memory the pool has already promised elsewhere), and latency-critical
+// loops that must never block in the allocator or synchronise the device, as
+// cudaMalloc and cudaFree can.  For them, dflash_attention_noalloc runs the
+// same attention kernels as dflash_debug_attention, but its scratch (the
+// per-sequence context views and the split partials) lives in the fixed
+// array below, which is part of this library's device image: every GPU that
+// loads the library holds these 16 MiB until the process exits.
 // ============================================================================
 namespace {
 
 constexpr int64_t kNoAllocFloats = int64_t(4) << 20;  // 16 MiB of f32 scratch
 constexpr int64_t kNoAllocViewFloats = 4096;           // the first 16 KiB hold the context views
-constexpr int kNoAllocMaxSeqs = 256;                   // 256 views * 40 B fit in those 16 KiB
+constexpr int kNoAllocMaxSeqs = kViewsMax;             // 256 views * 40 B fit in those 16 KiB
 constexpr int kNoAllocMaxDevices = 64;
+static_assert(kNoAllocMaxSeqs * sizeof(AttnSeq) <= kNoAllocViewFloats * sizeof(float), "view area");
 
 std::mutex g_noalloc_mutex;
 float* g_noalloc_base[kNoAllocMaxDevices] = {};
@@ -2077,22 +1958,28 @@ int dflash_attention_noalloc(dflash_model* m, dflash_seq* const* seqs, int32_t n
                                              " sequences, at most " + std::to_string(kNoAllocMaxSeqs));
     const dflash_geometry& g = m->g;
     // the fixed array's room for the key splits' partial rows: a call whose
-    // rows do not fit runs the cluster merge, which needs none
+    // rows do not fit runs the cluster merge, which needs none (on 152 SMs the
+    // split plan needs at most ~3.8 Mi floats, so it always fits there)
     const int64_t part_floats = kNoAllocFloats - kNoAllocViewFloats;
     float* base = nullptr;
     CK(m, noalloc_base(m->device, &base));
     cudaStream_t st = (cudaStream_t)stream;
     AttnSeq* views_dev = reinterpret_cast<AttnSeq*>(base);
-    // the array's head holds the context views; the rest holds the key
-    // splits' partial rows when a long context splits the keys over more
-    // CTAs than clusters place (each launch writes them before the merge
-    // reads them, so nothing in it needs to start at zero); otherwise the
-    // splits merge in distributed shared memory and the rest is not read
-    CK(m, cudaMemcpyAsync(views_dev, views.data(), views.size() * sizeof(AttnSeq), cudaMemcpyHostToDevice, st));
-    CK(m, attention(qkv, m->qkv_w, n_seqs, block_len, views_dev, max_ctx, g.heads, g.kv_heads, g.head_dim,
-                    1.0f / sqrtf((float)g.head_dim), base + kNoAllocViewFloats, part_floats, y, m->num_sms, st,
-                    nullptr, nullptr, nullptr, 0.f, false, m->win[layer] > 0));
-    m->launches += attn_kernels(n_seqs, block_len, max_ctx, g.heads, g.kv_heads, g.head_dim, m->num_sms, part_floats);
+    // The array's head takes the context views, passed by value to a small
+    // kernel (no host buffer has to outlive the call); the attention reads
+    // them after its dependency wait.  The rest holds the key splits' partial
+    // rows when a long context splits the keys over more CTAs than clusters
+    // place (each launch writes them before the merge reads them, so nothing
+    // in it needs to start at zero); otherwise the splits merge in
+    // distributed shared memory and the rest is not read.
+    AttnViews byval;
+    byval.n = n_seqs;
+    std::copy(views.begin(), views.end(), byval.v);
+    KL(m, "attn_views", 1, (double)n_seqs * sizeof(AttnSeq), st, attn_views_store(byval, views_dev, st));
+    KL(m, "attention_noalloc",
+       attn_kernels(n_seqs, block_len, max_ctx, g.heads, g.kv_heads, g.head_dim, m->num_sms, part_floats), 0.0, st,
+       attention(qkv, m->qkv_w, n_seqs, block_len, views_dev, max_ctx, g.heads, g.kv_heads, g.head_dim,
+                 1.0f / sqrtf((float)g.head_dim), base + kNoAllocViewFloats, part_floats, y, m->num_sms, st, nullptr,
+                 nullptr, nullptr, 0.f, false, m->win[layer] > 0));
     return DFLASH_OK;
 }
-

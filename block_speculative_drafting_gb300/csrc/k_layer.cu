@@ -12,6 +12,7 @@
 #include <cooperative_groups.h>
 
 #include <algorithm>
+#include <array>
 
 #include "common.cuh"
 #include "kernels.cuh"
@@ -69,7 +70,8 @@ __global__ void __launch_bounds__(kRowThreads) rms_rows_kernel(const float* __re
                                                                float* __restrict__ out_f32, int ld_out,
                                                                int8_t* __restrict__ out_codes,
                                                                float* __restrict__ out_scale, int ld_codes,
-                                                               float* zero_buf, int64_t zero_n) {
+                                                               float* zero_buf, int64_t zero_n,
+                                                               const float* __restrict__ div, int div_seg) {
     __shared__ float red[33];
     pdl_trigger();
     pdl_wait();
@@ -77,24 +79,28 @@ __global__ void __launch_bounds__(kRowThreads) rms_rows_kernel(const float* __re
     const int i = blockIdx.x;
     const int srow = (i / map.per) * map.stride + map.skip + (i % map.per);
     const float* x = src + (int64_t)srow * ld_src;
+    // with div: each div_seg-column segment of the source divided by its divisor first
+    const float* dv = div ? div + (int64_t)srow * (n / div_seg) : nullptr;
+    auto src_at = [&](int c) { return dv ? x[c] / dv[c / div_seg] : x[c]; };
     float s = 1.f;
     if (w) {
         float ss = 0.f;
-        for (int c = threadIdx.x; c < n; c += kRowThreads) ss = fmaf(x[c], x[c], ss);
+        for (int c = threadIdx.x; c < n; c += kRowThreads) ss = fmaf(src_at(c), src_at(c), ss);
         ss = row_reduce<false>(ss, red);
         s = 1.0f / sqrtf(ss / (float)n + eps);
     }
     if (out_f32) {
-        for (int c = threadIdx.x; c < n; c += kRowThreads) out_f32[(int64_t)i * ld_out + c] = w ? x[c] * s * w[c] : x[c];
+        for (int c = threadIdx.x; c < n; c += kRowThreads)
+            out_f32[(int64_t)i * ld_out + c] = w ? src_at(c) * s * w[c] : src_at(c);
         return;
     }
     float amax = 0.f;
-    for (int c = threadIdx.x; c < n; c += kRowThreads) amax = fmaxf(amax, fabsf(w ? x[c] * s * w[c] : x[c]));
+    for (int c = threadIdx.x; c < n; c += kRowThreads) amax = fmaxf(amax, fabsf(w ? src_at(c) * s * w[c] : src_at(c)));
     amax = row_reduce<true>(amax, red);
     const float sx = __fdiv_rn(amax, 127.0f);
     int8_t* q = out_codes + (int64_t)i * ld_codes;
     for (int c = threadIdx.x; c < n; c += kRowThreads) {
-        const float v = w ? x[c] * s * w[c] : x[c];
+        const float v = w ? src_at(c) * s * w[c] : src_at(c);
         q[c] = sx > 0.f ? code_of(v, sx) : (int8_t)0;
     }
     if (threadIdx.x == 0) out_scale[i] = sx;
@@ -111,7 +117,8 @@ __global__ void __launch_bounds__(NT, NT == kRowThreads || NV > 12 ? 1 : 2) rms_
                                                                    float* __restrict__ out_f32, int ld_out,
                                                                    int8_t* __restrict__ out_codes,
                                                                    float* __restrict__ out_scale, int ld_codes,
-                                                                   float* zero_buf, int64_t zero_n, int rows) {
+                                                                   float* zero_buf, int64_t zero_n, int rows,
+                                                                   const float* __restrict__ div, int div_seg) {
     __shared__ float red[33];
     pdl_trigger();
     pdl_wait();
@@ -134,6 +141,11 @@ __global__ void __launch_bounds__(NT, NT == kRowThreads || NV > 12 ? 1 : 2) rms_
     for (int u = 0; u < NV; ++u) {
         const int c = threadIdx.x + u * NT;
         v[u] = c < n4 ? x4[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (div != nullptr && c < n4) {
+            // a sum of parts: the float4's segment divided by its divisor (div_seg % 4 == 0)
+            const float d = div[(int64_t)srow * (n / div_seg) + (4 * c) / div_seg];
+            v[u] = make_float4(v[u].x / d, v[u].y / d, v[u].z / d, v[u].w / d);
+        }
         ss = fmaf(v[u].x, v[u].x, ss);
         ss = fmaf(v[u].y, v[u].y, ss);
         ss = fmaf(v[u].z, v[u].z, ss);
@@ -184,8 +196,9 @@ static bool rows_fit_reg(int n, const void* src, int ld_src, const void* out_f32
 
 int rms_rows(const float* src, int ld_src, RowMap map, int rows, int n, const float* w, float eps, float* out_f32,
              int ld_out, int8_t* out_codes, float* out_scale, int ld_codes, cudaStream_t st, float* zero_buf,
-             int64_t zero_n) {
+             int64_t zero_n, const float* div, int div_seg) {
     if (rows <= 0) return 0;
+    if (div && (div_seg <= 0 || div_seg % 4 || n % div_seg)) return (int)cudaErrorInvalidValue;
     const bool wal = !w || (reinterpret_cast<uintptr_t>(w) % 16) == 0;
     const bool zal = !zero_buf || (reinterpret_cast<uintptr_t>(zero_buf) % 16) == 0;
     if (wal && zal && rows_fit_reg(n, src, ld_src, out_f32, ld_out, out_codes, ld_codes, 8 * 4 * kRowThreads)) {
@@ -195,7 +208,7 @@ int rms_rows(const float* src, int ld_src, RowMap map, int rows, int n, const fl
             zero_buf && zero_n > 0 ? (int)std::min<int64_t>(128, zero_n / 4 / (kRowThreads * 4) + 1) : 0;
         auto go = [&](auto kern) {
             return (int)launch(kern, dim3(rows + extra), dim3(kRowThreads), 0, st, src, ld_src, map, n, w, eps, out_f32,
-                               ld_out, out_codes, out_scale, ld_codes, zero_buf, zero_n, rows);
+                               ld_out, out_codes, out_scale, ld_codes, zero_buf, zero_n, rows, div, div_seg);
         };
         if (nv <= 1) return go(rms_rows_reg_kernel<1>);
         if (nv <= 2) return go(rms_rows_reg_kernel<2>);
@@ -205,13 +218,13 @@ int rms_rows(const float* src, int ld_src, RowMap map, int rows, int n, const fl
         auto go512 = [&](auto kern) {
             const int extra512 = zero_buf && zero_n > 0 ? (int)std::min<int64_t>(256, zero_n / 4 / (512 * 4) + 1) : 0;
             return (int)launch(kern, dim3(rows + extra512), dim3(512), 0, st, src, ld_src, map, n, w, eps, out_f32, ld_out,
-                               out_codes, out_scale, ld_codes, zero_buf, zero_n, rows);
+                               out_codes, out_scale, ld_codes, zero_buf, zero_n, rows, div, div_seg);
         };
         if (nv512 <= 12) return go512(rms_rows_reg_kernel<12, 512>);
         return go512(rms_rows_reg_kernel<16, 512>);
     }
     return (int)launch(rms_rows_kernel, dim3(rows), dim3(kRowThreads), 0, st, src, ld_src, map, n, w, eps, out_f32,
-                       ld_out, out_codes, out_scale, ld_codes, zero_buf, zero_n);
+                       ld_out, out_codes, out_scale, ld_codes, zero_buf, zero_n, div, div_seg);
 }
 
 // ------------------------------------------------------------------ row convolution
@@ -693,7 +706,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32, ST == 1 ? 2 : 1) attn_cluster
                                                                        const float* __restrict__ q_norm,
                                                                        const float* __restrict__ k_norm,
                                                                        const float2* __restrict__ rope, float eps,
-                                                                       float* __restrict__ gpart, int kv_ready) {
+                                                                       float* __restrict__ gpart, int kv_ready,
+                                                                       float* __restrict__ lacc, float ref_log2) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     AttnSmem<HD, ST>& sm = *reinterpret_cast<AttnSmem<HD, ST>*>(smem_raw);
     constexpr int PART = AttnSmem<HD, ST>::PART;
@@ -702,13 +716,18 @@ __global__ void __launch_bounds__(kAttnWarps * 32, ST == 1 ? 2 : 1) attn_cluster
     constexpr int kThreads = kAttnWarps * 32;
     cg::cluster_group cluster = cg::this_cluster();
     // the key split: the CTA's rank in its cluster, or, when the splits merge
-    // through global memory (gpart), its x index in a launch without clusters
-    const int sp = gpart ? (int)blockIdx.x : (int)cluster.block_rank();
+    // through global memory (gpart) or add into accumulators (lacc), its x
+    // index in a launch without clusters
+    const int sp = (gpart || lacc) ? (int)blockIdx.x : (int)cluster.block_rank();
     const int g = blockIdx.y / qtiles, qt = blockIdx.y % qtiles, s = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
     const int qw = warp % kAttnQW, half = warp / kAttnQW;  // query warp, key lane
     pdl_trigger();
-    // the views are uploaded before the launch sequence: read ahead of the wait
+    // the context views: read ahead of the dependency wait when the caller
+    // vouches that the views and the stores were final before the launch
+    // sequence (kv_ready), after it otherwise (the kernel just before this one
+    // may have written them)
+    if (!kv_ready) pdl_wait();
     const AttnSeq sq = seqs[s];
     const int rep = nq / nkv, mq = rep * block_len;
     const int total = sq.n + block_len;
@@ -1027,6 +1046,40 @@ __global__ void __launch_bounds__(kAttnWarps * 32, ST == 1 ? 2 : 1) attn_cluster
 #pragma unroll
         for (int j = 0; j < NT; ++j) *reinterpret_cast<float2*>(out + 4 + j * 8 + 2 * tq) = make_float2(o[j][2 * h], o[j][2 * h + 1]);
     }
+    if (lacc) {
+        // Accumulate: the two key lanes' partial rows of each query row are
+        // rescaled to the fixed reference 2^ref_log2 (at least every score of
+        // the layer: its queries and keys are RMS-normed, so |q.k| is bounded
+        // by the norms' gains) and added into y (the unnormalised output)
+        // and lacc (the softmax sum); a later kernel divides.  Exactly the
+        // merge of the splits, in any order, with no second kernel.
+        constexpr int VEC = HD / 32;
+        __syncthreads();  // every warp's partial rows are written
+        for (int qr = warp; qr < kAttnQ; qr += kAttnWarps) {
+            const int ii = qt * kAttnQ + qr;
+            if (ii >= mq) break;  // rows grow with qr (warp-uniform)
+            const float* p0 = part + qr * PART;
+            const float* p1 = part + (kAttnQ + qr) * PART;
+            const float m0 = p0[0], m1 = p1[0];
+            const float f0 = (m0 == -INFINITY) ? 0.f : exp2f(m0 - ref_log2);
+            const float f1 = (m1 == -INFINITY) ? 0.f : exp2f(m1 - ref_log2);
+            const int head = g * rep + ii / block_len, r = ii % block_len;
+            float* dst = y + (row0 + r) * ((int64_t)nq * HD) + (int64_t)head * HD + VEC * lane;
+            if constexpr (VEC == 4) {
+                const float4 a = *reinterpret_cast<const float4*>(p0 + 4 + 4 * lane);
+                const float4 b = *reinterpret_cast<const float4*>(p1 + 4 + 4 * lane);
+                red_add_v4(dst, fmaf(a.x, f0, b.x * f1), fmaf(a.y, f0, b.y * f1), fmaf(a.z, f0, b.z * f1),
+                           fmaf(a.w, f0, b.w * f1));
+            } else {
+                const float2 a = *reinterpret_cast<const float2*>(p0 + 4 + 2 * lane);
+                const float2 b = *reinterpret_cast<const float2*>(p1 + 4 + 2 * lane);
+                atomicAdd(dst, fmaf(a.x, f0, b.x * f1));
+                atomicAdd(dst + 1, fmaf(a.y, f0, b.y * f1));
+            }
+            if (lane == 0) atomicAdd(lacc + (row0 + r) * nq + head, fmaf(p0[1], f0, p1[1] * f1));
+        }
+        return;
+    }
     cluster.sync();  // every CTA's partial rows are written
 
     // merge: one warp per query row; lane k < kAttnKH nsplit reads partial
@@ -1221,10 +1274,22 @@ int attn_kernels(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int hd
 // How many clusters of c = 1..16 CTAs of attn_cluster_kernel<HD, ST> the
 // device holds at once (0 where it cannot place one), found once per process.
 template <int HD, int ST>
+static void attn_cluster_fill(int* table, cudaStream_t st);
+
+template <int HD, int ST>
 static const int* attn_cluster_table(cudaStream_t st) {
-    static int table[kAttnMaxCluster + 1] = {0};
-    static bool done = false;
-    if (done) return table;
+    // built once, thread-safely (a function-local static's initialiser runs
+    // exactly once even when several host threads make their first call together)
+    static const std::array<int, kAttnMaxCluster + 1> table = [st] {
+        std::array<int, kAttnMaxCluster + 1> t{};
+        attn_cluster_fill<HD, ST>(t.data(), st);
+        return t;
+    }();
+    return table.data();
+}
+
+template <int HD, int ST>
+static void attn_cluster_fill(int* table, cudaStream_t st) {
     for (auto kern : {attn_cluster_kernel<HD, ST, false>, attn_cluster_kernel<HD, ST, true>}) {
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(AttnSmem<HD, ST>));
         cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -1251,8 +1316,6 @@ static const int* attn_cluster_table(cudaStream_t st) {
         table[c] = n;
     }
     if (table[1] < 1) table[1] = 1;
-    done = true;
-    return table;
 }
 
 template <int HD, int ST, bool WIN>
@@ -1264,14 +1327,15 @@ static int attention_launch(const AttnPlan& p, const float* qkv, int ld, int n_s
     if (p.gmerge) {
         cudaError_t e = launch(attn_cluster_kernel<HD, ST, WIN>, grid, dim3(kAttnWarps * 32), sizeof(AttnSmem<HD, ST>),
                                st, qkv, ld, block_len, seqs_dev, nq, nkv, p.qtiles, p.nsplit, scale_log2, y, q_norm,
-                               k_norm, rope, eps, part, kv_ready);
+                               k_norm, rope, eps, part, kv_ready, (float*)nullptr, 0.f);
         if (e != cudaSuccess) return (int)e;
         return (int)launch(attn_merge_kernel<HD>, dim3(kAttnQ / (8 / kMergeWays), nkv * p.qtiles * n_seqs), dim3(256), 0, st,
                            (const float*)part, p.nsplit, p.qtiles, nkv, nq, block_len, y);
     }
     return (int)launch_cluster(attn_cluster_kernel<HD, ST, WIN>, grid, dim3(kAttnWarps * 32),
                                sizeof(AttnSmem<HD, ST>), st, p.nsplit, qkv, ld, block_len, seqs_dev, nq, nkv, p.qtiles,
-                               p.nsplit, scale_log2, y, q_norm, k_norm, rope, eps, (float*)nullptr, kv_ready);
+                               p.nsplit, scale_log2, y, q_norm, k_norm, rope, eps, (float*)nullptr, kv_ready,
+                               (float*)nullptr, 0.f);
 }
 
 template <int HD, int ST>
@@ -1312,6 +1376,69 @@ int attention(const float* qkv, int ld, int n_seqs, int block_len, const AttnSeq
                                  num_sms, st, q_norm, k_norm, rope, eps, kv_ready ? 1 : 0, windowed);
     return attention_hd<64>(qkv, ld, n_seqs, block_len, seqs_dev, max_ctx, nq, nkv, scale, part, part_floats, y,
                             num_sms, st, q_norm, k_norm, rope, eps, kv_ready ? 1 : 0, windowed);
+}
+
+// ------------------------------------------------------------------ accumulate mode
+// Few units (fewer than the SMs): the keys of each unit split over
+// floor(SMs / units) plain CTAs (one wave, every SM busy for a single
+// sequence), each adding its rescaled partial rows into y and lacc.
+template <int HD>
+static int attn_acc_splits(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int num_sms) {
+    const int mq = (nq / nkv) * block_len;
+    const int units = nkv * ((mq + kAttnQ - 1) / kAttnQ) * n_seqs;
+    if (units >= num_sms) return 0;
+    const int* table = attn_cluster_table<HD, 2>(0);
+    const int slots = std::max(table[1], num_sms);
+    const int max_split = std::max(1, (max_ctx + block_len + kAttnStep - 1) / kAttnStep);
+    const int nsplit = std::min(max_split, slots / units);
+    return nsplit > 1 ? nsplit : 0;
+}
+
+int attn_acc_plan(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int hd, int num_sms) {
+    return hd == 128 ? attn_acc_splits<128>(n_seqs, block_len, max_ctx, nq, nkv, num_sms)
+                     : attn_acc_splits<64>(n_seqs, block_len, max_ctx, nq, nkv, num_sms);
+}
+
+template <int HD, bool WIN>
+static int attention_acc_hd(const float* qkv, int ld, int n_seqs, int block_len, const AttnSeq* seqs_dev, int nsplit,
+                            int nq, int nkv, float scale, float* yacc, float* lacc, float ref_log2, cudaStream_t st,
+                            const float* q_norm, const float* k_norm, const float2* rope, float eps, int kv_ready) {
+    const int mq = (nq / nkv) * block_len, qtiles = (mq + kAttnQ - 1) / kAttnQ;
+    attn_cluster_table<HD, 2>(0);  // the kernels' shared-memory attributes
+    const float scale_log2 = scale * 1.4426950408889634f;
+    return (int)launch(attn_cluster_kernel<HD, 2, WIN>, dim3(nsplit, nkv * qtiles, n_seqs), dim3(kAttnWarps * 32),
+                       sizeof(AttnSmem<HD, 2>), st, qkv, ld, block_len, seqs_dev, nq, nkv, qtiles, nsplit, scale_log2,
+                       yacc, q_norm, k_norm, rope, eps, (float*)nullptr, kv_ready, lacc, ref_log2);
+}
+
+int attention_acc(const float* qkv, int ld, int n_seqs, int block_len, const AttnSeq* seqs_dev, int nsplit, int nq,
+                  int nkv, int hd, float scale, float* yacc, float* lacc, float ref_log2, cudaStream_t st,
+                  const float* q_norm, const float* k_norm, const float2* rope, float eps, bool kv_ready,
+                  bool windowed) {
+    if (!q_norm || !k_norm || !yacc || !lacc || nsplit < 1 || (reinterpret_cast<uintptr_t>(yacc) & 15))
+        return (int)cudaErrorInvalidValue;
+    const int kr = kv_ready ? 1 : 0;
+    if (hd == 128)
+        return windowed ? attention_acc_hd<128, true>(qkv, ld, n_seqs, block_len, seqs_dev, nsplit, nq, nkv, scale,
+                                                      yacc, lacc, ref_log2, st, q_norm, k_norm, rope, eps, kr)
+                        : attention_acc_hd<128, false>(qkv, ld, n_seqs, block_len, seqs_dev, nsplit, nq, nkv, scale,
+                                                       yacc, lacc, ref_log2, st, q_norm, k_norm, rope, eps, kr);
+    return windowed ? attention_acc_hd<64, true>(qkv, ld, n_seqs, block_len, seqs_dev, nsplit, nq, nkv, scale, yacc,
+                                                 lacc, ref_log2, st, q_norm, k_norm, rope, eps, kr)
+                    : attention_acc_hd<64, false>(qkv, ld, n_seqs, block_len, seqs_dev, nsplit, nq, nkv, scale, yacc,
+                                                  lacc, ref_log2, st, q_norm, k_norm, rope, eps, kr);
+}
+
+// ------------------------------------------------------------------ views by value
+__global__ void __launch_bounds__(256) attn_views_store_kernel(const __grid_constant__ AttnViews views,
+                                                                AttnSeq* __restrict__ dst) {
+    pdl_wait();  // a kernel before this one may still read the views it replaces
+    for (int i = threadIdx.x; i < views.n; i += blockDim.x) dst[i] = views.v[i];
+}
+
+int attn_views_store(const AttnViews& views, AttnSeq* dst, cudaStream_t st) {
+    if (views.n < 0 || views.n > kViewsMax || dst == nullptr) return (int)cudaErrorInvalidValue;
+    return (int)launch(attn_views_store_kernel, dim3(1), dim3(256), 0, st, views, dst);
 }
 
 // ------------------------------------------------------------------ wait expiry

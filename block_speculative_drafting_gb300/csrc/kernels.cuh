@@ -132,59 +132,16 @@ int select_tokens(const unsigned long long* cand, int k, const float* hp, int ra
                   const __half* book_c, int V, const uint32_t* anchors, int n_seqs, int rows, uint32_t* chosen,
                   uint32_t* plain, cudaStream_t st);
 
-// ---- the chain: a persistent kernel (one CTA per SM) that runs a short
-// program of dependent stages of the block's rows, with a grid-wide barrier
-// between stages, and whose warps stream the 4-bit weights of every matvec
-// stage of the program through their rings in program order -- a stage's
-// first weights arrive while earlier stages still run (k_chain.cu).
-enum ChainOp : int {
-    kChainMatvec = 0,  // y[t][n] += xs[t] * sum_g s[n][g] * sum_k q[n][k] x[t][k] (t < T <= 16), as q4_stream
-    kChainRows = 1,    // codes of rms(src row, w) (w == nullptr: of the row itself), one f32 scale a row
-    kChainSilu = 2,    // codes of silu(g) * u, src rows [g (n) | u (n)]
-};
-struct ChainStage {
-    int op;
-    // matvec
-    const uint8_t* wp;
-    Q4Layout L;
-    int g0, ng;  // 64-row groups of the (fused) matrix
-    const int8_t* xc;
-    const float* xs;
-    int ldx, T;
-    float* y;
-    int ldy;
-    // row stages: `rows` rows (row i reads source row map(i)) of n columns
-    const float* src;
-    int ld_src;
-    RowMap map;
-    int rows, n;
-    const float* w;
-    float eps;
-    int8_t* codes;
-    float* scale;
-    int ld_codes;
-    float* zero;  // side duty of a row stage: clear zero_n floats here
-    int64_t zero_n;
-};
-constexpr int kChainMaxStages = 12;
-struct ChainProgram {
-    int n;
-    ChainStage s[kChainMaxStages];
-};
-// Launch a program on num_sms CTAs; bar: a device counter the launch resets
-// and uses for its barriers; err: the model's error flag (raised when a
-// bounded wait expires).  Row stages need rows <= num_sms, n % 4 == 0 and
-// n <= kChainRowMax, 16-byte aligned rows.
-constexpr int kChainRowMax = 4 * 12 * 512;
-int chain_run(const ChainProgram& p, int num_sms, unsigned* bar, int* err, cudaStream_t st);
-
 // ---- layer pieces (k_layer.cu)
 // x = rms(src, w) (w == nullptr: no norm, x = src); then either f32 out
 // (out_f32 != nullptr) or int8 codes + an f32 scale per row.
 // zero_buf / zero_n: a buffer the kernel clears on the side (nullptr: none).
+// div (nullptr: none): the source row is a sum of parts, and each div_seg
+// columns of source row r are first divided by div[r][segment] (the
+// attention's accumulate mode: y = yacc / lacc per head).
 int rms_rows(const float* src, int ld_src, RowMap map, int rows, int n, const float* w, float eps, float* out_f32,
              int ld_out, int8_t* out_codes, float* out_scale, int ld_codes, cudaStream_t st,
-             float* zero_buf = nullptr, int64_t zero_n = 0);
+             float* zero_buf = nullptr, int64_t zero_n = 0, const float* div = nullptr, int div_seg = 0);
 // h[r] = embed[tok(r)]: row r of sequence s = r / block_len is the anchor
 // (anchor_tok[s]) for r % block_len == 0, the mask token otherwise.  Side
 // duty (rope != nullptr): the block rows' rotation table rope[r][i] =
@@ -279,6 +236,34 @@ int64_t attn_scratch_floats(int n_seqs, int block_len, int max_ctx, int nq, int 
 // merge; with less scratch than attn_scratch_floats() the call falls back to
 // the cluster merge).
 int attn_kernels(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int hd, int num_sms, int64_t part_floats);
+
+// Accumulate mode of the attention, for layers whose queries and keys the
+// kernel RMS-norms (q_norm, k_norm): every score s of the layer then obeys
+// s * log2(e) * scale <= ref_log2 (the bound the gains give), so each CTA's
+// partial rows, rescaled by 2^(m - ref_log2), add into yacc [rows][nq * hd]
+// (unnormalised output) and lacc [rows][nq] (softmax sums) with atomics, in
+// any order: the merge of the key splits needs neither clusters nor a second
+// kernel.  Both must hold zeros before the launch; y = yacc / lacc per head
+// (rms_rows' divisor) finishes it.  attn_acc_plan: the key splits a unit
+// takes in this mode (0: not worth it -- as many units as SMs, or a single
+// key step -- use attention()).
+int attn_acc_plan(int n_seqs, int block_len, int max_ctx, int nq, int nkv, int hd, int num_sms);
+int attention_acc(const float* qkv, int ld, int n_seqs, int block_len, const AttnSeq* seqs_dev, int nsplit, int nq,
+                  int nkv, int hd, float scale, float* yacc, float* lacc, float ref_log2, cudaStream_t st,
+                  const float* q_norm, const float* k_norm, const float2* rope, float eps, bool kv_ready,
+                  bool windowed);
+
+// Up to kViewsMax context views passed by value (a kernel parameter of
+// about 10 KB), for a caller that must not keep a host buffer alive past its
+// call: attn_views_store writes them to dst (device memory) in stream order
+// -- it waits for the kernels before it, and an attention kernel after it
+// reads the views after its own dependency wait (kv_ready false).
+constexpr int kViewsMax = 256;
+struct AttnViews {
+    int n;
+    AttnSeq v[kViewsMax];
+};
+int attn_views_store(const AttnViews& views, AttnSeq* dst, cudaStream_t st);
 
 // Failure detection without a fault: one warp's bounded wait on an mbarrier
 // that nothing arrives on runs out after limit_ns and raises *err_flag.

@@ -307,6 +307,24 @@ DFLASH_API int dflash_profile_entry(const dflash_model* model, int32_t index, co
  * (-1 for NULL). */
 DFLASH_API int64_t dflash_launch_count(const dflash_model* model);
 
+/*
+ * Test hook (the pages have no counterpart): switch one of the model's
+ * kernel choices, for comparing the alternatives against the oracle.
+ *   "tc"         1 (default): matmuls and the head of more than 16 rows on
+ *                the tcgen05 kernels; 0: the warp-MMA kernel and the
+ *                streaming head.
+ *   "dense"      1 (default): the tcgen05 kernels read dense f16 copies of
+ *                the weights (built on the first call that needs them);
+ *                0: they dequantise the packed weights in shared memory.
+ *   "head_bound" the dense head trusts its tensor-memory f32 sums while a
+ *                row pair's squared code norms multiply to at most this
+ *                (default and maximum 2^48); 0 recomputes every element as
+ *                an integer dot product.
+ * Takes effect for calls after it (captured kernel sequences are dropped).
+ * Errors: EINVAL (NULL, unknown name, negative head_bound).
+ */
+DFLASH_API int dflash_debug_option(dflash_model* model, const char* name, int64_t value);
+
 /* ---------------------------------------------------------------------------
  * Test hooks: views of the library's internal state, for parity checks.
  * All pointers are host pointers; each call synchronises `stream`.
@@ -422,25 +440,28 @@ DFLASH_API int dflash_debug_attention(dflash_model* model, dflash_seq* const* se
 
 /*
  * dflash_debug_attention without allocating anything (the pages have no
- * counterpart: this entry point exists for callers that cannot allocate device
- * memory when they run the attention -- inside another component's CUDA graph
- * capture, under a framework that owns all device memory through its own
- * pool, or in a loop that must never block in the allocator).
+ * counterpart).  It exists for callers that cannot allocate device memory
+ * when they run the attention: a host framework that owns every device byte
+ * through its own pool allocator (a cudaMalloc behind its back can fail or
+ * take memory the pool has promised elsewhere), or a latency-critical loop
+ * that must never block in the allocator or synchronise the device, as
+ * cudaMalloc and cudaFree can.
  * Same arguments, layouts and result as dflash_debug_attention.  Its scratch
  * is a fixed 16 MiB device array inside this library, held by every GPU that
  * loads the library until the process exits; the call makes no cudaMalloc /
- * cudaFree.  The array holds the context views and, for a long context whose
+ * cudaFree and calls no allocating library routine.  The array's head takes
+ * the context views, which the call passes by value to a small kernel (no
+ * host buffer outlives the call); the rest holds, for a long context whose
  * keys split over more CTAs than clusters place, the splits' partial rows
  * (written before they are read: nothing needs to start at zero); when those
  * rows do not fit, the call runs the cluster merge (distributed shared
  * memory), which needs no partials in global memory.  The first call on a
- * device looks up that array's device address (cudaGetSymbolAddress) and
- * keeps it: make that first call before any stream capture.  Every call shares
- * the one array and overwrites what the previous call left there, so calls
- * whose work overlaps on the GPU (other streams, other threads) race: order
- * them on one stream.  Errors: as dflash_debug_attention, and ERANGE when the
- * context views do not fit the array (more than 256 sequences) -- nothing is
- * launched then.
+ * device looks up that array's device address (cudaGetSymbolAddress, with
+ * the device current) and keeps it.  Every call shares the one array and
+ * overwrites what the previous call left there, so calls whose work overlaps
+ * on the GPU (other streams, other threads) race: order them on one stream.
+ * Errors: as dflash_debug_attention, and ERANGE when the context views do not
+ * fit the array (more than 256 sequences) -- nothing is launched then.
  */
 DFLASH_API int dflash_attention_noalloc(dflash_model* model, dflash_seq* const* seqs, int32_t n_seqs, int32_t layer,
                                         const int64_t* anchor_pos, int32_t block_len, const float* qkv, float* y,

@@ -114,3 +114,53 @@ def test_full_size_free_running_within_decision_noise(full):
           f"oracle vs f32-perturbed oracle {devs}")
     assert gpu_dev <= 3 * max(devs) + 2e-3
     seq.close()
+
+
+def test_full_size_argmax_agreement_over_1005_rows(full):
+    """Draft tokens of 67 context-2048 blocks (1005 rows) against the
+    oracle's, binned by the oracle's top-2 margin: with identical decisions
+    (context and block) every row agrees; free running, every row whose
+    margin exceeds a tenth of max|logit| agrees, and the table reports the
+    rest."""
+    import oracle.drafter as D
+    from test_gpu_parity import agreement_table, print_agreement
+    wl, g, w, model, om = full
+    B, n = g.block, wl.ctx
+    taps = W.make_taps(g, n, call_id=500)
+    D.TRACE = D.QuantTrace()
+    try:
+        osq = OracleSeq(om)
+        osq.append(0, taps)
+        ctx_sites = D.TRACE.sites
+    finally:
+        D.TRACE = None
+    seq = model.new_sequence(n + B)
+    model.trace(True)
+    for _, q, s in ctx_sites:
+        model.trace_force(q, s)
+    try:
+        model.ctx_append(seq, 0, taps)
+    finally:
+        model.trace(False)
+    records = []
+    for a in W.make_anchors(g, 67, call_id=501):
+        D.TRACE = D.QuantTrace()
+        try:
+            ref, _ = block(om, osq, int(a), n, B)
+            sites = D.TRACE.sites
+        finally:
+            D.TRACE = None
+        model.trace(True)
+        for _, q, s in sites:
+            model.trace_force(q, s)
+        try:
+            _, tf = model.block([seq], [int(a)], [n], B, want_logits=False)
+        finally:
+            model.trace(False)
+        _, tr = model.block([seq], [int(a)], [n], B, want_logits=False)
+        records.append((ref, tf[0], tr[0]))
+    seq.close()
+    table, forced, free, m, er = agreement_table(records)
+    print_agreement(f"qwen3_8b_ctx2048, {len(records)} blocks, {sum(t[2] for t in table)} rows", table, forced, free)
+    assert forced == 1.0
+    assert er[m >= 0.1].all()

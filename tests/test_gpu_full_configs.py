@@ -117,6 +117,51 @@ def test_prefill_8192_rows_sampled(qwen):
     seq.close()
 
 
+def test_prefill_8192_rows_identical_decisions(qwen):
+    """The 8192-row append (the prefill configuration, the tcgen05 path) with
+    the oracle's quantisation decisions at both of its sites (the taps, and
+    the normed context rows feeding every layer's Wk/Wv): every stored K and
+    V row of every layer agrees with the oracle's at f32 level (5e-5 of the
+    largest value), and the GPU's own codes differ from the oracle's only at
+    rounding boundaries.  Rows are independent, so the oracle projects all of
+    them in one pass (float64, a few seconds of BLAS)."""
+    import oracle.drafter as D
+    from test_gpu_parity import check_sites
+    g, model, om = qwen
+    n = W.WORKLOADS["qwen3_8b_prefill8192"].prefill
+    taps = W.make_taps(g, n, call_id=80)
+    D.TRACE = D.QuantTrace()
+    try:
+        osq = OracleSeq(om)
+        osq.append(0, taps)
+        sites = D.TRACE.sites
+    finally:
+        D.TRACE = None
+    assert len(sites) == 2
+    seq = model.new_sequence(n)
+    model.trace(True)
+    for _, q, sc in sites:
+        model.trace_force(q, sc)
+    try:
+        model.ctx_append(seq, 0, taps)
+        own = model.trace_sites()
+    finally:
+        model.trace(False)
+    flips = check_sites(sites, own, 5e-5)
+    del sites, own
+    worst = 0.0
+    for l in range(g.layers):
+        k, v = model.read_kv(seq, l, 0, n)
+        rk, rv = osq.k[l].transpose(1, 0, 2), osq.v[l].transpose(1, 0, 2)
+        ek = float(np.max(np.abs(k - rk))) / float(np.max(np.abs(rk)))
+        ev = float(np.max(np.abs(v - rv))) / float(np.max(np.abs(rv)))
+        worst = max(worst, ek, ev)
+        assert ek <= 5e-5 and ev <= 5e-5, f"layer {l}: K {ek:.2e}, V {ev:.2e}"
+    print(f"prefill 8192, identical decisions: every row of {g.layers} layers within {worst:.2e} "
+          f"of max; {flips} own codes at boundaries")
+    seq.close()
+
+
 def test_batch32_ctx4096_sampled_sequences(qwen):
     """32 sequences of context 4096 in one batched block (the batched
     configuration); two of them against the oracle run whole."""

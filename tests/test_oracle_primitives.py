@@ -9,6 +9,7 @@ import pytest
 import torch
 
 from oracle import attention, inv_freq, rms, rope, silu, softmax, top_k
+from oracle.drafter import argmax_first
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -190,3 +191,52 @@ def test_top_k_page_example():
         k, rest = line.split(":", 1)
         want = [(float(p.split(",")[0]), int(p.split(",")[1])) for p in rest.split()]
         assert top_k(x, int(k)) == want
+
+
+# ---------------------------------------------------------------- argmax_first
+def _page_example_row():
+    with open(os.path.join(GOLDEN, "top_k_page_example.txt")) as fh:
+        lines = [l.strip() for l in fh if l.strip() and not l.startswith("#")]
+    return [float(v) for v in lines[0].split(":", 1)[1].split()]
+
+
+def test_argmax_first_keeps_the_first_of_equals_page_example():
+    # The page's `top_k` test (page "cortiq-engine 0.8.71 — src/dflash.rs",
+    # `top_k_orders_and_keeps_first_of_equals`) ranks the value 2.0 at index 1
+    # ahead of the equal 2.0 at index 3.  With the unique maximum 3.5 taken
+    # out of that row, the draft token's argmax must therefore be index 1.
+    x = np.array(_page_example_row())
+    assert argmax_first(x[None, :])[0] == 4
+    y = x.copy()
+    y[4] = -np.inf
+    assert argmax_first(y[None, :])[0] == 1
+    # the same row with the equal pair moved: the first of them wins wherever it sits
+    for a, b in [(0, 5), (2, 3), (1, 2), (0, 1)]:
+        z = np.full(6, -1.0)
+        z[a] = z[b] = 7.0
+        assert argmax_first(z[None, :])[0] == min(a, b)
+
+
+def test_argmax_first_ties_at_several_positions():
+    rng = np.random.default_rng(5)
+    rows, width = 64, 997
+    x = rng.uniform(-1.0, 1.0, size=(rows, width)).astype(np.float32)
+    want = np.empty(rows, dtype=np.uint32)
+    for r in range(rows):
+        pos = np.sort(rng.choice(width, size=1 + r % 5, replace=False))
+        x[r, pos] = 2.0
+        want[r] = pos[0]
+    assert np.array_equal(argmax_first(x), want)
+    # an all-equal row (a head of zeros gives one): index 0
+    assert argmax_first(np.zeros((3, 17), dtype=np.float32)).tolist() == [0, 0, 0]
+
+
+def test_argmax_first_decides_in_float32():
+    # two values distinct in float64 but the same float32 are equals: the first wins
+    a = 1.0 + 2.0 ** -30
+    x = np.array([[0.0, 1.0, a, 0.5]])
+    assert np.float32(a) == np.float32(1.0)
+    assert argmax_first(x)[0] == 1
+    # distinct in float32: the larger wins, wherever it sits
+    x = np.array([[0.0, 1.0, 1.0 + 2.0 ** -20, 0.5]])
+    assert argmax_first(x)[0] == 2
