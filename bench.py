@@ -21,7 +21,11 @@ host inputs in, outputs out, copies inside the timed region).  roofline: the
 kernel with the largest device time in a profiled pass of the same steps.
 cpu_baseline / --impl reference: the CPU oracle on a bounded sample.
 
-python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME] [--others auto|on|off]
+
+With the default workload on one GPU the line also carries "others": the
+context-32768, batch-32 and prefill-8192 workloads of the same drafter, each
+timed the same way (same steps and warm-up) on the same model.
 """
 from __future__ import annotations
 
@@ -384,25 +388,19 @@ def job_throughput(world, units_per_rank, seconds):
     return world * units_per_rank / seconds
 
 
-def run_ours(args, wl):
+OTHER_WORKLOADS = ("qwen3_8b_ctx32768", "qwen3_8b_batch32_ctx4096", "qwen3_8b_prefill8192")
+
+
+def measure(args, wl, model, dev, world, dist, clocks, weights, cpu_leg):
+    """One workload's numbers on an existing model (the workloads share one
+    geometry): the timed steps, the profiled pass, the host-buffer e2e and,
+    when asked, the CPU oracle leg.  Returns the JSON fields of its line."""
     import torch
 
-    import block_speculative_drafting_gb300 as dfl
-
-    rank, world, local = env_int("RANK", 0), env_int("WORLD_SIZE", 1), env_int("LOCAL_RANK", 0)
-    torch.cuda.set_device(local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist_mod
-        dist = dist_mod
-        dist.init_process_group("nccl")
     g = wl.geom
     B = g.block
     units, unit = step_units(wl)
     t_setup = time.perf_counter()
-    weights = W.make_weights(g)
-    model = dfl.Model(g, weights)
-    dev = torch.device("cuda", local)
     case = build_case(model, wl, dev)
     step, step_host = case["step"], case["step_host"]
     stream = torch.cuda.current_stream()
@@ -414,9 +412,6 @@ def run_ours(args, wl):
             dist.barrier()
         torch.cuda.synchronize()
 
-    clocks = ClockSampler(torch.cuda.current_device())
-    clocks.start()
-    time.sleep(0.3)
     for _ in range(args.warmup):
         step()
     barrier()
@@ -434,7 +429,6 @@ def run_ours(args, wl):
     ms = evs[0].elapsed_time(evs[-1]) / args.steps
     per_step = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps))
     pct = {f"ms_p{q}": per_step[min(len(per_step) - 1, int(q / 100 * len(per_step)))] for q in (10, 50, 90)}
-    clocks.stop()
     clk = clocks.summary(t_wall0, t_wall1)
     ms = max_over_ranks(ms, dist, dev)
     value = job_throughput(world, units, ms * 1e-3)
@@ -491,28 +485,70 @@ def run_ours(args, wl):
            "h2d_bytes_per_step": case["h2d"], "d2h_bytes_per_step": case["d2h"]}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if cpu_leg:
         sec, n, cores, what = oracle_step_timer(wl, weights, 3, budget_s=args.cpu_budget)
         cpu = {"value": units / sec, "unit": unit, "cores": cores, "kind": "oracle",
                "sample": f"median of {n} sample(s): {what}, of {wl.name}; oracle build and context prefill untimed"}
+    for sq in case["seqs"]:
+        sq.close()
+    return {
+        "value": value, "unit": unit, "ms_per_step": ms,
+        "config": {"workload": wl.name, "n_seqs": wl.n_seqs, "ctx": wl.ctx, "block": B,
+                   "prefill": wl.prefill, "step": case["desc"], "parallelism": f"replicas x{world}",
+                   "l2": case["l2"]},
+        "block_latency_ms": ms, **pct, "hbm_gbs_step": step_bytes / (ms * 1e-3) / 1e9,
+        "algorithmic_bytes_per_step": step_bytes, "profiled_ms_per_step": prof_ms,
+        "roofline": roofline, "kernels": kernels, "e2e": e2e, "cpu_baseline": cpu,
+        "gpu_launches": launches, "clocks": clk, "setup_s": setup_s,
+    }
 
+
+def run_ours(args, wl):
+    import torch
+
+    import block_speculative_drafting_gb300 as dfl
+
+    rank, world, local = env_int("RANK", 0), env_int("WORLD_SIZE", 1), env_int("LOCAL_RANK", 0)
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist = dist_mod
+        dist.init_process_group("nccl")
+    weights = W.make_weights(wl.geom)
+    model = dfl.Model(wl.geom, weights)
+    dev = torch.device("cuda", local)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    cpu_leg = rank == 0 and world == 1 and not args.no_cpu_baseline
+    main_line = measure(args, wl, model, dev, world, dist, clocks, weights, cpu_leg)
+    # the other full-size configurations of the same drafter, each timed the
+    # same way on the same model, reported beside the headline (one GPU)
+    others = {}
+    want_others = args.others == "on" or (args.others == "auto" and world == 1 and wl.name == "qwen3_8b_ctx2048")
+    if want_others:
+        for other in OTHER_WORKLOADS:
+            owl = W.WORKLOADS[other]
+            if owl.geom != wl.geom:
+                continue
+            r = measure(args, owl, model, dev, world, dist, clocks, weights, False)
+            others[other] = {k: r[k] for k in ("value", "unit", "ms_per_step", "ms_p10", "ms_p50", "ms_p90",
+                                               "config", "roofline", "kernels", "e2e", "hbm_gbs_step",
+                                               "gpu_launches", "clocks", "setup_s")}
+    clocks.stop()
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "int4xint8 (f32 accumulate)",
+            "metric": METRIC, "value": main_line["value"], "unit": main_line["unit"], "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": main_line["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int4xint8 (f32 accumulate)",
             "data": "synthetic (seeded Gaussian weights N(0,0.02), taps N(0,1))",
-            "config": {"workload": wl.name, "n_seqs": wl.n_seqs, "ctx": wl.ctx, "block": B,
-                       "prefill": wl.prefill, "step": case["desc"], "parallelism": f"replicas x{world}",
-                       "l2": case["l2"]},
-            "block_latency_ms": ms, **pct, "hbm_gbs_step": step_bytes / (ms * 1e-3) / 1e9,
-            "algorithmic_bytes_per_step": step_bytes, "profiled_ms_per_step": prof_ms,
-            "roofline": roofline, "kernels": kernels, "e2e": e2e, "cpu_baseline": cpu,
-            "gpu_launches": launches, "clocks": clk, "setup_s": setup_s,
+            **{k: v for k, v in main_line.items() if k not in ("value", "unit", "ms_per_step")},
         }
+        if others:
+            line["others"] = others
         print(json.dumps(line), flush=True)
-    for s in case["seqs"]:
-        s.close()
     model.close()
     if dist:
         dist.barrier()
@@ -528,6 +564,9 @@ def main():
     ap.add_argument("--workload", default="qwen3_8b_ctx2048", choices=sorted(W.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=60.0, help="seconds of CPU oracle steps at most")
+    ap.add_argument("--others", default="auto", choices=["auto", "on", "off"],
+                    help="also time the other full-size workloads of the same drafter (auto: with the default "
+                         "workload on one GPU)")
     args = ap.parse_args()
     wl = W.WORKLOADS[args.workload]
     if args.impl == "reference":
