@@ -21,6 +21,10 @@ thread_local std::string g_init_error;
 
 // Context rows projected per pass of an append (bounds the scratch buffers).
 constexpr int64_t kAppendRows = 8192;
+// Keys a CTA of the tcgen05 attention streams at least for it to be chosen
+// over the warp-MMA kernel (measured on GB300: the tcgen05 kernel wins from
+// about four 64-key steps a CTA; at context 2048 a split holds under two)
+constexpr int64_t kTcAttnMinKeys = 256;
 
 struct DevBuf {
     void* p = nullptr;
@@ -91,6 +95,7 @@ struct dflash_model {
     // (off: dequantised in the kernel)
     bool use_tc = true;
     bool use_dense = true;
+    int64_t tc_attn_min_keys = kTcAttnMinKeys;  // keys a CTA of the tcgen05 attention streams at least
     // dense f16 copies of the matrices for the many-row path, built on first need:
     // the 4-bit matrices as (hi, lo) planes [N][K], the head's codes [vocab][hidden]
     struct DenseMat {
@@ -176,6 +181,10 @@ struct dflash_seq {
     std::vector<__half*> k, v;
     __half** k_dev = nullptr;  // device arrays of the per-layer pointers
     __half** v_dev = nullptr;
+    // per layer, the tensor maps of its key and value stores for the tcgen05
+    // attention (device memory, 2 x 128 bytes a layer; null when the driver
+    // could not encode them: that attention is then not used)
+    void* maps_dev = nullptr;
     // per layer: context rows no block row of the layer can see any more
     // (its window), dropped for good; the layer reads from first + dropped
     std::vector<int64_t> dropped;
@@ -303,6 +312,7 @@ AttnSeq layer_view(const dflash_model* m, const dflash_seq* q, int l, int64_t an
     a.lo = lo - q->first;
     a.n = (int)(hi - lo);
     a.cut = w > 0 ? (int)std::max<int64_t>(anchor + 1 - w - lo, kNoCut) : kNoCut;
+    a.maps = q->maps_dev ? static_cast<const unsigned char*>(q->maps_dev) + (size_t)l * 256 : nullptr;
     return a;
 }
 
@@ -1145,6 +1155,26 @@ int dflash_seq_new(dflash_model* m, int64_t max_ctx_rows, dflash_seq** out) {
     if (e == cudaSuccess) e = cudaMalloc(&s->v_dev, L * sizeof(__half*));
     if (e == cudaSuccess) e = cudaMemcpy(s->k_dev, s->k.data(), L * sizeof(__half*), cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemcpy(s->v_dev, s->v.data(), L * sizeof(__half*), cudaMemcpyHostToDevice);
+    // every stored value finite from the start: the tcgen05 attention's
+    // tensor copies read whole 64-row boxes, rows past the context included
+    // (their weights are exactly zero, and 0 times a finite value is 0)
+    for (int l = 0; l < L && e == cudaSuccess; ++l) {
+        e = cudaMemset(s->k[l], 0, 2 * per * sizeof(__half));
+        if (e == cudaSuccess) e = cudaMemset(s->v[l], 0, 2 * per * sizeof(__half));
+    }
+    if (e == cudaSuccess) {
+        alignas(64) unsigned char maps[256];
+        std::vector<unsigned char> all((size_t)L * 256);
+        bool built = true;
+        for (int l = 0; l < L && built; ++l) {
+            built = kv_tensor_maps(s->k[l], s->v[l], m->g.kv_heads, max_ctx_rows, m->g.head_dim, maps);
+            if (built) std::memcpy(all.data() + (size_t)l * 256, maps, 256);
+        }
+        if (built) {
+            e = cudaMalloc(&s->maps_dev, all.size());
+            if (e == cudaSuccess) e = cudaMemcpy(s->maps_dev, all.data(), all.size(), cudaMemcpyHostToDevice);
+        }
+    }
     if (e != cudaSuccess) {
         cudaGetLastError();
         dflash_seq_free(s);
@@ -1163,6 +1193,7 @@ void dflash_seq_free(dflash_seq* s) {
     for (__half* p : s->v) if (p) cudaFree(p);
     if (s->k_dev) cudaFree(s->k_dev);
     if (s->v_dev) cudaFree(s->v_dev);
+    if (s->maps_dev) cudaFree(s->maps_dev);
     if (s->pend) cudaFree(s->pend);
     if (s->m && s->m->live_seqs > 0) s->m->live_seqs--;
     delete s;
@@ -1293,7 +1324,18 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
     const int64_t part_floats = attn_scratch_floats(n_seqs, B, max_ctx, g.heads, g.kv_heads, hd, m->num_sms);
     // layers whose attention accumulates its key splits' rescaled partial
     // rows (few units: a single sequence's 8 kv heads spread over every SM)
-    const int acc_split = quant ? attn_acc_plan(n_seqs, B, max_ctx, g.heads, g.kv_heads, hd, m->num_sms) : 0;
+    // (on the tcgen05 kernel when its single query tile holds a unit's rows:
+    // then every unit count, a batch filling the SMs included)
+    bool tc_attn = quant && m->use_tc && attention_tc_supported(g.heads, g.kv_heads, hd, B);
+    for (int s = 0; s < n_seqs; ++s) tc_attn = tc_attn && seqs[s]->maps_dev != nullptr;
+    int tc_split = tc_attn ? attn_tc_plan(n_seqs, B, max_ctx, g.kv_heads, m->num_sms) : 0;
+    // the tcgen05 kernel where each CTA has a few key steps to stream (its
+    // fixed cost -- queries, tensor memory, the pipeline's ramp -- then
+    // amortises: long contexts, batches); the warp-MMA kernel for short splits
+    if (tc_attn && tc_split > 1 && (int64_t)(max_ctx + B) / tc_split < m->tc_attn_min_keys) tc_attn = false;
+    const int acc_split = !quant    ? 0
+                          : tc_attn ? tc_split
+                                    : attn_acc_plan(n_seqs, B, max_ctx, g.heads, g.kv_heads, hd, m->num_sms);
     std::vector<char> acc_l(g.layers, 0);
     bool any_acc = false;
     for (int l = 0; l < g.layers; ++l) {
@@ -1366,7 +1408,12 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
         const Layer& Ly = m->layers[l];
         const AttnSeq* aseq_dev = P<AttnSeq>(m->aseqs) + (size_t)l * n_seqs;
         const float2* rl = m->norope[l] ? nullptr : P<float2>(m->rope);
-        if (acc_l[l]) {
+        if (acc_l[l] && tc_attn) {
+            KL(m, "attention", 1, attn_bytes_l[l] + (double)R * g.heads * (hd + 1) * 4, st,
+               attention_tc(qkv, m->qkv_w, n_seqs, B, aseq_dev, acc_split, g.heads, g.kv_heads, hd, scale, yacc, lacc,
+                            m->attn_ref[l], st, Ly.q_norm, Ly.k_norm, rl, g.eps, m->own_capture, m->win[l] > 0,
+                            m->err_dev));
+        } else if (acc_l[l]) {
             KL(m, "attention", 1, attn_bytes_l[l] + (double)R * g.heads * (hd + 1) * 4, st,
                attention_acc(qkv, m->qkv_w, n_seqs, B, aseq_dev, acc_split, g.heads, g.kv_heads, hd, scale, yacc, lacc,
                              m->attn_ref[l], st, Ly.q_norm, Ly.k_norm, rl, g.eps, m->own_capture, m->win[l] > 0));
@@ -1707,6 +1754,9 @@ int dflash_debug_option(dflash_model* m, const char* name, int64_t value) {
         m->use_tc = value != 0;
     } else if (opt == "dense") {
         m->use_dense = value != 0;
+    } else if (opt == "attn_tc_min_keys") {
+        if (value < 0) return set_err(m, DFLASH_EINVAL, "attn_tc_min_keys < 0");
+        m->tc_attn_min_keys = value;
     } else if (opt == "head_bound") {
         if (value < 0) return set_err(m, DFLASH_EINVAL, "head_bound < 0");
         m->head_bound = std::min<unsigned long long>((unsigned long long)value, 1ull << 48);

@@ -206,6 +206,9 @@ struct AttnSeq {
     // context rows (of the n) block row 0 does not see, row i: cut + i
     // (a layer's window; kNoCut: every row sees all n)
     int cut;
+    // the tcgen05 attention's tensor maps of the two stores (keys, then
+    // values: kv_tensor_maps), in device memory; nullptr where not built
+    const void* maps;
 };
 constexpr int kNoCut = -(1 << 30);
 // qkv [n_seqs*block_len][ld] (q, k, v of the block); with q_norm != nullptr
@@ -252,6 +255,24 @@ int attention_acc(const float* qkv, int ld, int n_seqs, int block_len, const Att
                   int nkv, int hd, float scale, float* yacc, float* lacc, float ref_log2, cudaStream_t st,
                   const float* q_norm, const float* k_norm, const float2* rope, float eps, bool kv_ready,
                   bool windowed);
+
+// The same accumulate mode on the tcgen05 tensor cores (k_attn_tc.cu): one
+// CTA takes all query rows of a (sequence, kv head) unit (rep * block_len <=
+// 128) against its share of the keys, 64 keys a step.  attn_tc_plan: the key
+// splits a unit takes (1 when the units fill the SMs).  err: raised when a
+// bounded wait expires.
+bool attention_tc_supported(int nq, int nkv, int hd, int block_len);
+// The two tensor maps (CUtensorMap, 128 bytes each: keys, then values) of a
+// layer's stores [2 planes][nkv][cap][hd] f16 that the tcgen05 attention
+// reads 64-row x 64-column boxes of, in the 128-byte swizzle.  out: host
+// memory of 256 bytes, 64-byte aligned.  false when the driver lacks the
+// encoder or rejects the shape.
+bool kv_tensor_maps(const __half* k, const __half* v, int nkv, int64_t cap, int hd, void* out);
+int attn_tc_plan(int n_seqs, int block_len, int max_ctx, int nkv, int num_sms);
+int attention_tc(const float* qkv, int ld, int n_seqs, int block_len, const AttnSeq* seqs_dev, int nsplit, int nq,
+                 int nkv, int hd, float scale, float* yacc, float* lacc, float ref_log2, cudaStream_t st,
+                 const float* q_norm, const float* k_norm, const float2* rope, float eps, bool kv_ready, bool windowed,
+                 int* err);
 
 // Up to kViewsMax context views passed by value (a kernel parameter of
 // about 10 KB), for a caller that must not keep a host buffer alive past its

@@ -316,6 +316,10 @@ DFLASH_API int64_t dflash_launch_count(const dflash_model* model);
  *   "dense"      1 (default): the tcgen05 kernels read dense f16 copies of
  *                the weights (built on the first call that needs them);
  *                0: they dequantise the packed weights in shared memory.
+ *   "attn_tc_min_keys"  the block attention runs on the tcgen05 kernel
+ *                when each of its CTAs streams at least this many keys
+ *                (default 256; 0: always where the geometry allows), on
+ *                the warp-MMA kernel otherwise.
  *   "head_bound" the dense head trusts its tensor-memory f32 sums while a
  *                row pair's squared code norms multiply to at most this
  *                (default and maximum 2^48); 0 recomputes every element as

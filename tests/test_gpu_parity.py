@@ -939,3 +939,56 @@ def test_argmax_agreement_over_3000_rows():
     assert sum(t[2] for t in table) >= 1000
     assert forced == 1.0
     assert er[m >= 0.1].all()
+
+
+# ---------------------------------------------------------------- the tcgen05 attention on small cases
+def _tc_pair(name, **changes):
+    """A fresh pair whose GPU model runs the block attention on the tcgen05
+    kernel whatever the split length (the default keeps it for splits of at
+    least 256 keys: long contexts and batches)."""
+    p = Pair(name, **changes)
+    p.gpu.option("attn_tc_min_keys", 0)
+    return p
+
+
+@pytest.mark.parametrize("name", ["small_q4", "small_q4_hd64"])
+@pytest.mark.parametrize("forced", [True, False])
+def test_tc_attention_block_matches_oracle(name, forced):
+    """The block (and a context starting at position 100) with the tcgen05
+    attention: a block step of the block's rows and tensor-copied context
+    steps, the splits added into the accumulators."""
+    p = _tc_pair(name)
+    g, n = p.g, p.wl.ctx
+    sc = Script(p, 1, n + 16)
+    sc.append(0, 0, W.make_taps(g, n))
+    sc.block([0], [int(W.make_anchors(g, 1)[0])], [n], g.block)
+    sc.block([0], [0], [150], g.block)
+    sc.run(forced).check(forced)
+
+
+@pytest.mark.parametrize("forced", [True, False])
+def test_tc_attention_windows_and_batches_match_oracle(forced):
+    """Windowed layers (the row-dependent mask of the context steps), a layer
+    without the rotary position, several sequences of different lengths (an
+    empty one included) and a context longer than one 64-key step."""
+    p = _tc_pair("small_q4", windows=(3, 0), no_rope=(1,))
+    g = p.g
+    lens = [77, 0, 200, 9]
+    sc = Script(p, len(lens), 224)
+    for i, n in enumerate(lens):
+        sc.append(i, 0, W.make_taps(g, n, call_id=110 + i))
+    sc.block(list(range(len(lens))), [(29 * i + 3) % g.vocab for i in range(len(lens))], lens, g.block)
+    sc.block([2], [17], [200], 9)
+    sc.run(forced).check(forced)
+
+
+@pytest.mark.parametrize("window", [0, 3])
+def test_tc_attention_equal_scores(window):
+    """All scores exactly 0 (Wq = Wd = 0): every row averages the values it
+    sees, through the tcgen05 kernel's online softmax."""
+    p = _tc_pair("small_q4", edit=_zero_queries_and_down, window=window)
+    g, n = p.g, p.wl.ctx
+    sc = Script(p, 1, n + 16)
+    sc.append(0, 0, W.make_taps(g, n))
+    sc.block([0], [5], [n], g.block)
+    sc.run(True).check(True)
