@@ -899,17 +899,20 @@ int append_rows(dflash_model* m, dflash_seq* s, const float* taps_dev, int64_t n
         // x = Q(rms(t, hidden_norm)) (kv cleared on the side); kv = [Wk;Wv]_all . x
         int8_t* codes = P<int8_t>(m->a_codes);
         float* sc = P<float>(m->a_scale);
+        // (the side duties clear the streaming matvecs' outputs; the many-row
+        // matmuls clear their own when they split K)
+        const bool stream = rows <= 16;
         KL(m, "rms_quant", 1, (double)rows * m->tap_w * 5, st,
-           rms_rows(taps_dev, m->tap_w, ident, rows, m->tap_w, nullptr, g.eps, nullptr, 0, codes, sc, m->tap_w, st, t,
-                    (int64_t)rows * H));
+           rms_rows(taps_dev, m->tap_w, ident, rows, m->tap_w, nullptr, g.eps, nullptr, 0, codes, sc, m->tap_w, st,
+                    stream ? t : nullptr, stream ? (int64_t)rows * H : 0));
         TRACE(trace_site(m, st, rows, m->tap_w, codes, m->tap_w, sc, [&](float* v) {
             return rms_rows(taps_dev, m->tap_w, ident, rows, m->tap_w, nullptr, g.eps, v, m->tap_w, nullptr, nullptr, 0, st);
         }));
         QAct xt{codes, sc, m->tap_w};
         APPLY(q4_mm(m, m->fc_p, m->L_fc, 0, H, m->tap_w, xt, rows, t, H, false, st));
         KL(m, "rms_quant", 1, (double)rows * H * 5, st,
-           rms_rows(t, H, ident, rows, H, m->hidden_norm, g.eps, nullptr, 0, codes, sc, H, st, kv,
-                    (int64_t)rows * m->kvctx_w));
+           rms_rows(t, H, ident, rows, H, m->hidden_norm, g.eps, nullptr, 0, codes, sc, H, st, stream ? kv : nullptr,
+                    stream ? (int64_t)rows * m->kvctx_w : 0));
         TRACE(trace_site(m, st, rows, H, codes, H, sc, [&](float* v) {
             return rms_rows(t, H, ident, rows, H, m->hidden_norm, g.eps, v, H, nullptr, nullptr, 0, st);
         }));
@@ -1402,6 +1405,12 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
     const float scale = 1.0f / sqrtf((float)hd);
     float* yacc = qkv + (size_t)R * m->qkv_w;  // accumulate mode (any_acc)
     float* lacc = yacc + (size_t)R * m->qd;
+    // what the in_norm quantisation clears on the side: the streaming matvec
+    // (up to 16 rows) adds into qkv, so qkv and the attention's accumulators;
+    // the many-row matmuls clear their own output when they split K, so only
+    // the accumulators
+    float* qz = R <= 16 ? qkv : yacc;
+    const int64_t qz_n = R <= 16 ? qkv_zero : (any_acc ? (int64_t)R * (m->qd + g.heads) : 0);
     // the block's attention of layer l into y (or, accumulate mode, into
     // yacc / lacc, which the clearing before the layer's qkv zeroed)
     auto run_attention = [&](int l) -> int {
@@ -1524,7 +1533,7 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
         // attention half: x = rms(h, in_norm); q, k, v; norms and rotation; attention; h += O y
         if (quant) {
             KL(m, "rms_quant", 1, (double)R * H * 5, st,
-               rms_rows(h, H, ident, R, H, Ly.in_norm, g.eps, nullptr, 0, xq, xs, maxK, st, qkv, qkv_zero));
+               rms_rows(h, H, ident, R, H, Ly.in_norm, g.eps, nullptr, 0, xq, xs, maxK, st, qz, qz_n));
             TRACE(trace_site(m, st, R, H, xq, maxK, xs, [&](float* v) {
                 return rms_rows(h, H, ident, R, H, Ly.in_norm, g.eps, v, H, nullptr, nullptr, 0, st);
             }));
@@ -1553,7 +1562,8 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
         // MLP half: x = rms(h, post_norm); h += down (silu(gate x) * up x)
         if (quant) {
             KL(m, "rms_quant", 1, (double)R * H * 5, st,
-               rms_rows(h, H, ident, R, H, Ly.post_norm, g.eps, nullptr, 0, xq, xs, maxK, st, gu, (int64_t)R * 2 * I));
+               rms_rows(h, H, ident, R, H, Ly.post_norm, g.eps, nullptr, 0, xq, xs, maxK, st, R <= 16 ? gu : nullptr,
+                        R <= 16 ? (int64_t)R * 2 * I : 0));
             TRACE(trace_site(m, st, R, H, xq, maxK, xs, [&](float* v) {
                 return rms_rows(h, H, ident, R, H, Ly.post_norm, g.eps, v, H, nullptr, nullptr, 0, st);
             }));
