@@ -698,14 +698,17 @@ bool dense_of(const dflash_model* m, const uint8_t* packed, int row0, int N, int
 // ADDS into y, which an earlier kernel cleared or which holds the residual),
 // the general one beyond.
 int q4_mm(dflash_model* m, const uint8_t* packed, Q4Layout L, int tile0, int N, int K, QAct x, int T, float* y,
-          int ldy, bool accumulate, cudaStream_t st) {
+          int ldy, bool accumulate, cudaStream_t st, bool x16_ready = false) {
     if (T <= 16) {
         KL(m, "q4_stream", 1, q4_bytes_of(N, K, T, true), st,
            q4_stream(packed, L, tile0, N, x, T, y, ldy, m->num_sms, m->err_dev, st));
     } else if (m->use_tc && q4_tc_supported(L, tile0, N, K, x) && ldy % 4 == 0 &&
                (reinterpret_cast<uintptr_t>(y) & 15) == 0 && m->x16.bytes >= (size_t)T * K * sizeof(__half)) {
         __half* x16 = P<__half>(m->x16);
-        KL(m, "act_f16", 1, (double)T * K * 3, st, codes_to_f16(x.codes, x.ld, T, K, x16, nullptr, m->num_sms, st));
+        // (x16_ready: the kernel that quantised x wrote these f16 codes already)
+        if (!x16_ready)
+            KL(m, "act_f16", 1, (double)T * K * 3, st,
+               codes_to_f16(x.codes, x.ld, T, K, x16, nullptr, m->num_sms, st));
         const __half *hi = nullptr, *lo = nullptr;
         if (dense_of(m, packed, tile0 * 16, N, K, &hi, &lo)) {
             // dense weight bytes: 4 a weight
@@ -779,10 +782,11 @@ int run_selector(dflash_model* m, cudaStream_t st, const float* h, RowMap drafts
 // a fresh output must have been cleared by an earlier kernel (the zeroing
 // side duty of the row kernel before it).  f32 format: the f32 rows `xf`.
 int apply(dflash_model* m, const uint8_t* packed, const float* f32w, Q4Layout L, int tile0, int N, int K,
-          const float* xf, int ldxf, int T, float* y, int ldy, bool accumulate, int ldq, cudaStream_t st) {
+          const float* xf, int ldxf, int T, float* y, int ldy, bool accumulate, int ldq, cudaStream_t st,
+          bool x16_ready = false) {
     if (m->g.quant == DFLASH_QUANT_Q4G32) {
         QAct x{P<int8_t>(m->xq), P<float>(m->xs), ldq};
-        return q4_mm(m, packed, L, tile0, N, K, x, T, y, ldy, accumulate, st);
+        return q4_mm(m, packed, L, tile0, N, K, x, T, y, ldy, accumulate, st, x16_ready);
     }
     KL(m, "linear_f32", 1, f32_bytes_of(N, K, T, accumulate), st,
        linear_f32(f32w, N, K, xf, ldxf, T, y, ldy, accumulate, st));
@@ -902,22 +906,24 @@ int append_rows(dflash_model* m, dflash_seq* s, const float* taps_dev, int64_t n
         // (the side duties clear the streaming matvecs' outputs; the many-row
         // matmuls clear their own when they split K)
         const bool stream = rows <= 16;
+        // (more rows: the f16 codes of the tcgen05 matmuls written beside the int8 ones)
+        __half* a16 = (!stream && !m->tracing && m->use_tc) ? P<__half>(m->x16) : nullptr;
         KL(m, "rms_quant", 1, (double)rows * m->tap_w * 5, st,
            rms_rows(taps_dev, m->tap_w, ident, rows, m->tap_w, nullptr, g.eps, nullptr, 0, codes, sc, m->tap_w, st,
-                    stream ? t : nullptr, stream ? (int64_t)rows * H : 0));
+                    stream ? t : nullptr, stream ? (int64_t)rows * H : 0, nullptr, 0, a16));
         TRACE(trace_site(m, st, rows, m->tap_w, codes, m->tap_w, sc, [&](float* v) {
             return rms_rows(taps_dev, m->tap_w, ident, rows, m->tap_w, nullptr, g.eps, v, m->tap_w, nullptr, nullptr, 0, st);
         }));
         QAct xt{codes, sc, m->tap_w};
-        APPLY(q4_mm(m, m->fc_p, m->L_fc, 0, H, m->tap_w, xt, rows, t, H, false, st));
+        APPLY(q4_mm(m, m->fc_p, m->L_fc, 0, H, m->tap_w, xt, rows, t, H, false, st, a16 != nullptr));
         KL(m, "rms_quant", 1, (double)rows * H * 5, st,
            rms_rows(t, H, ident, rows, H, m->hidden_norm, g.eps, nullptr, 0, codes, sc, H, st, stream ? kv : nullptr,
-                    stream ? (int64_t)rows * m->kvctx_w : 0));
+                    stream ? (int64_t)rows * m->kvctx_w : 0, nullptr, 0, a16));
         TRACE(trace_site(m, st, rows, H, codes, H, sc, [&](float* v) {
             return rms_rows(t, H, ident, rows, H, m->hidden_norm, g.eps, v, H, nullptr, nullptr, 0, st);
         }));
         QAct xh{codes, sc, H};
-        APPLY(q4_mm(m, m->kvctx_p, m->L_kvctx, 0, m->kvctx_w, H, xh, rows, kv, m->kvctx_w, false, st));
+        APPLY(q4_mm(m, m->kvctx_p, m->L_kvctx, 0, m->kvctx_w, H, xh, rows, kv, m->kvctx_w, false, st, a16 != nullptr));
     } else {
         KL(m, "linear_f32", 1, f32_bytes_of(H, m->tap_w, rows, false), st,
            linear_f32(m->fc_f, H, m->tap_w, taps_dev, m->tap_w, rows, t, H, false, st));
@@ -1405,6 +1411,11 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
     const float scale = 1.0f / sqrtf((float)hd);
     float* yacc = qkv + (size_t)R * m->qkv_w;  // accumulate mode (any_acc)
     float* lacc = yacc + (size_t)R * m->qd;
+    // the many-row matmuls' f16 activation codes, written by the kernels that
+    // quantise (not while tracing: a forced decision replaces the int8 codes
+    // after them, and the matmul converts those itself)
+    __half* o16 = (quant && R > 16 && !m->tracing && m->use_tc) ? P<__half>(m->x16) : nullptr;
+    const bool x16r = o16 != nullptr;
     // what the in_norm quantisation clears on the side: the streaming matvec
     // (up to 16 rows) adds into qkv, so qkv and the attention's accumulators;
     // the many-row matmuls clear their own output when they split K, so only
@@ -1533,11 +1544,13 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
         // attention half: x = rms(h, in_norm); q, k, v; norms and rotation; attention; h += O y
         if (quant) {
             KL(m, "rms_quant", 1, (double)R * H * 5, st,
-               rms_rows(h, H, ident, R, H, Ly.in_norm, g.eps, nullptr, 0, xq, xs, maxK, st, qz, qz_n));
+               rms_rows(h, H, ident, R, H, Ly.in_norm, g.eps, nullptr, 0, xq, xs, maxK, st, qz, qz_n, nullptr, 0,
+                        o16));
             TRACE(trace_site(m, st, R, H, xq, maxK, xs, [&](float* v) {
                 return rms_rows(h, H, ident, R, H, Ly.in_norm, g.eps, v, H, nullptr, nullptr, 0, st);
             }));
-            APPLY(apply(m, Ly.qkv_p, nullptr, m->L_qkv, 0, m->qkv_w, H, nullptr, 0, R, qkv, m->qkv_w, false, maxK, st));
+            APPLY(apply(m, Ly.qkv_p, nullptr, m->L_qkv, 0, m->qkv_w, H, nullptr, 0, R, qkv, m->qkv_w, false, maxK, st,
+                        x16r));
         } else {
             KL(m, "rms_f32", 1, (double)R * H * 8, st, rms_rows(h, H, ident, R, H, Ly.in_norm, g.eps, xf, maxK, nullptr, nullptr, 0, st));
             APPLY(apply(m, nullptr, Ly.qkv_f, Q4Layout{}, 0, m->qkv_w, H, xf, maxK, R, qkv, m->qkv_w, false, 0, st));
@@ -1550,12 +1563,12 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
             const float* ydiv = acc_l[l] ? lacc : nullptr;
             KL(m, "rms_quant", 1, (double)R * m->qd * 5, st,
                rms_rows(ysrc, m->qd, ident, R, m->qd, nullptr, g.eps, nullptr, 0, xq, xs, maxK, st, nullptr, 0, ydiv,
-                        hd));
+                        hd, o16));
             TRACE(trace_site(m, st, R, m->qd, xq, maxK, xs, [&](float* v) {
                 return rms_rows(ysrc, m->qd, ident, R, m->qd, nullptr, g.eps, v, m->qd, nullptr, nullptr, 0, st,
                                 nullptr, 0, ydiv, hd);
             }));
-            APPLY(apply(m, Ly.o_p, nullptr, m->L_o, 0, H, m->qd, nullptr, 0, R, h, H, true, maxK, st));
+            APPLY(apply(m, Ly.o_p, nullptr, m->L_o, 0, H, m->qd, nullptr, 0, R, h, H, true, maxK, st, x16r));
         } else {
             APPLY(apply(m, nullptr, Ly.o_f, Q4Layout{}, 0, H, m->qd, y, m->qd, R, h, H, true, 0, st));
         }
@@ -1563,16 +1576,16 @@ int dflash_block(dflash_model* m, dflash_seq* const* seqs, int32_t n_seqs, const
         if (quant) {
             KL(m, "rms_quant", 1, (double)R * H * 5, st,
                rms_rows(h, H, ident, R, H, Ly.post_norm, g.eps, nullptr, 0, xq, xs, maxK, st, R <= 16 ? gu : nullptr,
-                        R <= 16 ? (int64_t)R * 2 * I : 0));
+                        R <= 16 ? (int64_t)R * 2 * I : 0, nullptr, 0, o16));
             TRACE(trace_site(m, st, R, H, xq, maxK, xs, [&](float* v) {
                 return rms_rows(h, H, ident, R, H, Ly.post_norm, g.eps, v, H, nullptr, nullptr, 0, st);
             }));
-            APPLY(apply(m, Ly.gu_p, nullptr, m->L_gu, 0, 2 * I, H, nullptr, 0, R, gu, 2 * I, false, maxK, st));
-            KL(m, "silu_quant", 1, (double)R * I * 9, st, silu_mul(gu, 2 * I, R, I, nullptr, 0, xq, xs, maxK, st));
+            APPLY(apply(m, Ly.gu_p, nullptr, m->L_gu, 0, 2 * I, H, nullptr, 0, R, gu, 2 * I, false, maxK, st, x16r));
+            KL(m, "silu_quant", 1, (double)R * I * 9, st, silu_mul(gu, 2 * I, R, I, nullptr, 0, xq, xs, maxK, st, o16));
             TRACE(trace_site(m, st, R, I, xq, maxK, xs, [&](float* v) {
                 return silu_mul(gu, 2 * I, R, I, v, I, nullptr, nullptr, 0, st);
             }));
-            APPLY(apply(m, Ly.down_p, nullptr, m->L_down, 0, H, I, nullptr, 0, R, h, H, true, maxK, st));
+            APPLY(apply(m, Ly.down_p, nullptr, m->L_down, 0, H, I, nullptr, 0, R, h, H, true, maxK, st, x16r));
         } else {
             KL(m, "rms_f32", 1, (double)R * H * 8, st, rms_rows(h, H, ident, R, H, Ly.post_norm, g.eps, xf, maxK, nullptr, nullptr, 0, st));
             APPLY(apply(m, nullptr, Ly.gu_f, Q4Layout{}, 0, 2 * I, H, xf, maxK, R, gu, 2 * I, false, 0, st));

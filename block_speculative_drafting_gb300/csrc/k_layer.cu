@@ -58,6 +58,17 @@ DF_DEV float row_reduce_nt(float v, float* red) {
     return r;
 }
 
+// A word of four int8 codes, and (out16 != nullptr) the same codes as exact
+// f16 values at out16 + 4 c (the tcgen05 matmuls' activation operand).
+DF_DEV void put_codes4(uint32_t* q4, __half* out16, int c, uint32_t w) {
+    q4[c] = w;
+    if (out16 != nullptr) {
+        uint32_t lo, hi;
+        i8x4_to_half2x2(w, lo, hi);
+        *reinterpret_cast<uint2*>(out16 + 4 * c) = make_uint2(lo, hi);
+    }
+}
+
 // Zero `n` floats at `p`, spread over the grid (a side duty that clears the
 // buffer a later kernel accumulates into).
 DF_DEV void zero_side(float* p, int64_t n) {
@@ -72,7 +83,8 @@ __global__ void __launch_bounds__(kRowThreads) rms_rows_kernel(const float* __re
                                                                int8_t* __restrict__ out_codes,
                                                                float* __restrict__ out_scale, int ld_codes,
                                                                float* zero_buf, int64_t zero_n,
-                                                               const float* __restrict__ div, int div_seg) {
+                                                               const float* __restrict__ div, int div_seg,
+                                                               __half* __restrict__ out16) {
     __shared__ float red[33];
     pdl_trigger();
     pdl_wait();
@@ -103,6 +115,7 @@ __global__ void __launch_bounds__(kRowThreads) rms_rows_kernel(const float* __re
     for (int c = threadIdx.x; c < n; c += kRowThreads) {
         const float v = w ? src_at(c) * s * w[c] : src_at(c);
         q[c] = sx > 0.f ? code_of(v, sx) : (int8_t)0;
+        if (out16 != nullptr) out16[(int64_t)i * n + c] = __int2half_rn(q[c]);
     }
     if (threadIdx.x == 0) out_scale[i] = sx;
 }
@@ -119,7 +132,8 @@ __global__ void __launch_bounds__(NT, NT == kRowThreads || NV > 12 ? 1 : 2) rms_
                                                                    int8_t* __restrict__ out_codes,
                                                                    float* __restrict__ out_scale, int ld_codes,
                                                                    float* zero_buf, int64_t zero_n, int rows,
-                                                                   const float* __restrict__ div, int div_seg) {
+                                                                   const float* __restrict__ div, int div_seg,
+                                                                   __half* __restrict__ out16) {
     __shared__ float red[33];
     pdl_trigger();
     pdl_wait();
@@ -183,7 +197,7 @@ __global__ void __launch_bounds__(NT, NT == kRowThreads || NV > 12 ? 1 : 2) rms_
 #pragma unroll
     for (int u = 0; u < NV; ++u) {
         const int c = threadIdx.x + u * NT;
-        if (c < n4) q4[c] = codes4(v[u], sx);
+        if (c < n4) put_codes4(q4, out16 ? out16 + (int64_t)i * n : nullptr, c, codes4(v[u], sx));
     }
     if (threadIdx.x == 0) out_scale[i] = sx;
 }
@@ -197,9 +211,11 @@ static bool rows_fit_reg(int n, const void* src, int ld_src, const void* out_f32
 
 int rms_rows(const float* src, int ld_src, RowMap map, int rows, int n, const float* w, float eps, float* out_f32,
              int ld_out, int8_t* out_codes, float* out_scale, int ld_codes, cudaStream_t st, float* zero_buf,
-             int64_t zero_n, const float* div, int div_seg) {
+             int64_t zero_n, const float* div, int div_seg, __half* out16) {
     if (rows <= 0) return 0;
     if (div && (div_seg <= 0 || div_seg % 4 || n % div_seg)) return (int)cudaErrorInvalidValue;
+    if (out16 && (!out_codes || out_f32 || n % 4 || (reinterpret_cast<uintptr_t>(out16) & 7)))
+        return (int)cudaErrorInvalidValue;
     const bool wal = !w || (reinterpret_cast<uintptr_t>(w) % 16) == 0;
     const bool zal = !zero_buf || (reinterpret_cast<uintptr_t>(zero_buf) % 16) == 0;
     if (wal && zal && rows_fit_reg(n, src, ld_src, out_f32, ld_out, out_codes, ld_codes, 8 * 4 * kRowThreads)) {
@@ -209,7 +225,7 @@ int rms_rows(const float* src, int ld_src, RowMap map, int rows, int n, const fl
             zero_buf && zero_n > 0 ? (int)std::min<int64_t>(128, zero_n / 4 / (kRowThreads * 4) + 1) : 0;
         auto go = [&](auto kern) {
             return (int)launch(kern, dim3(rows + extra), dim3(kRowThreads), 0, st, src, ld_src, map, n, w, eps, out_f32,
-                               ld_out, out_codes, out_scale, ld_codes, zero_buf, zero_n, rows, div, div_seg);
+                               ld_out, out_codes, out_scale, ld_codes, zero_buf, zero_n, rows, div, div_seg, out16);
         };
         if (nv <= 1) return go(rms_rows_reg_kernel<1>);
         if (nv <= 2) return go(rms_rows_reg_kernel<2>);
@@ -219,13 +235,13 @@ int rms_rows(const float* src, int ld_src, RowMap map, int rows, int n, const fl
         auto go512 = [&](auto kern) {
             const int extra512 = zero_buf && zero_n > 0 ? (int)std::min<int64_t>(256, zero_n / 4 / (512 * 4) + 1) : 0;
             return (int)launch(kern, dim3(rows + extra512), dim3(512), 0, st, src, ld_src, map, n, w, eps, out_f32, ld_out,
-                               out_codes, out_scale, ld_codes, zero_buf, zero_n, rows, div, div_seg);
+                               out_codes, out_scale, ld_codes, zero_buf, zero_n, rows, div, div_seg, out16);
         };
         if (nv512 <= 12) return go512(rms_rows_reg_kernel<12, 512>);
         return go512(rms_rows_reg_kernel<16, 512>);
     }
     return (int)launch(rms_rows_kernel, dim3(rows), dim3(kRowThreads), 0, st, src, ld_src, map, n, w, eps, out_f32,
-                       ld_out, out_codes, out_scale, ld_codes, zero_buf, zero_n, div, div_seg);
+                       ld_out, out_codes, out_scale, ld_codes, zero_buf, zero_n, div, div_seg, out16);
 }
 
 // ------------------------------------------------------------------ row convolution
@@ -443,7 +459,8 @@ int kv_append(const float* kv, int n, int L, int nkv, int hd, const float* const
 __global__ void __launch_bounds__(kRowThreads) silu_mul_kernel(const float* __restrict__ gu, int ld_gu, int I,
                                                                float* __restrict__ out_f32, int ld_out,
                                                                int8_t* __restrict__ out_codes,
-                                                               float* __restrict__ out_scale, int ld_codes) {
+                                                               float* __restrict__ out_scale, int ld_codes,
+                                                               __half* __restrict__ out16) {
     __shared__ float red[33];
     pdl_trigger();
     pdl_wait();
@@ -462,6 +479,7 @@ __global__ void __launch_bounds__(kRowThreads) silu_mul_kernel(const float* __re
     for (int c = threadIdx.x; c < I; c += kRowThreads) {
         const float a = silu_f(g[c]) * u[c];
         q[c] = sx > 0.f ? code_of(a, sx) : (int8_t)0;
+        if (out16 != nullptr) out16[(int64_t)r * I + c] = __int2half_rn(q[c]);
     }
     if (threadIdx.x == 0) out_scale[r] = sx;
 }
@@ -471,7 +489,8 @@ template <int NV>
 __global__ void __launch_bounds__(kRowThreads) silu_mul_reg_kernel(const float* __restrict__ gu, int ld_gu, int I,
                                                                    float* __restrict__ out_f32, int ld_out,
                                                                    int8_t* __restrict__ out_codes,
-                                                                   float* __restrict__ out_scale, int ld_codes) {
+                                                                   float* __restrict__ out_scale, int ld_codes,
+                                                                   __half* __restrict__ out16) {
     __shared__ float red[33];
     pdl_trigger();
     pdl_wait();
@@ -509,7 +528,7 @@ __global__ void __launch_bounds__(kRowThreads) silu_mul_reg_kernel(const float* 
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
         const int c = threadIdx.x + k * kRowThreads;
-        if (c < n4) q4[c] = codes4(a[k], sx);
+        if (c < n4) put_codes4(q4, out16 ? out16 + (int64_t)r * I : nullptr, c, codes4(a[k], sx));
     }
     if (threadIdx.x == 0) out_scale[r] = sx;
 }
@@ -521,7 +540,8 @@ constexpr int kSiluSplit = 4;
 __global__ void __launch_bounds__(kRowThreads) silu_mul_cluster_kernel(const float* __restrict__ gu, int ld_gu, int I,
                                                                        float* __restrict__ out_f32, int ld_out,
                                                                        int8_t* __restrict__ out_codes,
-                                                                       float* __restrict__ out_scale, int ld_codes) {
+                                                                       float* __restrict__ out_scale, int ld_codes,
+                                                                       __half* __restrict__ out16) {
     __shared__ float red[33];
     cg::cluster_group cluster = cg::this_cluster();
     pdl_trigger();
@@ -547,31 +567,35 @@ __global__ void __launch_bounds__(kRowThreads) silu_mul_cluster_kernel(const flo
     for (int k = 0; k < kSiluSplit; ++k) amax = fmaxf(amax, cluster.map_shared_rank(red, k)[32]);
     cluster.sync();  // no CTA leaves while another may still read its max
     const float sx = __fdiv_rn(amax, 127.0f);
-    if (in) reinterpret_cast<uint32_t*>(out_codes + (int64_t)r * ld_codes)[c] = codes4(a, sx);
+    if (in)
+        put_codes4(reinterpret_cast<uint32_t*>(out_codes + (int64_t)r * ld_codes), out16 ? out16 + (int64_t)r * I : nullptr,
+                   c, codes4(a, sx));
     if (part == 0 && threadIdx.x == 0) out_scale[r] = sx;
 }
 
 int silu_mul(const float* gu, int ld_gu, int rows, int I, float* out_f32, int ld_out, int8_t* out_codes,
-             float* out_scale, int ld_codes, cudaStream_t st) {
+             float* out_scale, int ld_codes, cudaStream_t st, __half* out16) {
     if (rows <= 0) return 0;
+    if (out16 && (!out_codes || out_f32 || I % 4 || (reinterpret_cast<uintptr_t>(out16) & 7)))
+        return (int)cudaErrorInvalidValue;
     if (I % (4 * kSiluSplit) == 0 && I / 4 / kSiluSplit <= kRowThreads &&
         rows_fit_reg(I, gu, ld_gu, out_f32, ld_out, out_codes, ld_codes, 4 * kSiluSplit * kRowThreads) &&
         (reinterpret_cast<uintptr_t>(gu + I) % 16) == 0)
         return (int)launch_cluster(silu_mul_cluster_kernel, dim3(kSiluSplit, rows), dim3(kRowThreads), 0, st,
-                                   kSiluSplit, gu, ld_gu, I, out_f32, ld_out, out_codes, out_scale, ld_codes);
+                                   kSiluSplit, gu, ld_gu, I, out_f32, ld_out, out_codes, out_scale, ld_codes, out16);
     if (rows_fit_reg(I, gu, ld_gu, out_f32, ld_out, out_codes, ld_codes, 4 * 4 * kRowThreads) &&
         (reinterpret_cast<uintptr_t>(gu + I) % 16) == 0) {
         const int nv = (I + 4 * kRowThreads - 1) / (4 * kRowThreads);
         auto go = [&](auto kern) {
             return (int)launch(kern, dim3(rows), dim3(kRowThreads), 0, st, gu, ld_gu, I, out_f32, ld_out, out_codes,
-                               out_scale, ld_codes);
+                               out_scale, ld_codes, out16);
         };
         if (nv <= 1) return go(silu_mul_reg_kernel<1>);
         if (nv <= 2) return go(silu_mul_reg_kernel<2>);
         return go(silu_mul_reg_kernel<4>);
     }
     return (int)launch(silu_mul_kernel, dim3(rows), dim3(kRowThreads), 0, st, gu, ld_gu, I, out_f32, ld_out,
-                       out_codes, out_scale, ld_codes);
+                       out_codes, out_scale, ld_codes, out16);
 }
 
 // ------------------------------------------------------------------ attention

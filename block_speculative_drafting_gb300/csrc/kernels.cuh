@@ -136,12 +136,15 @@ int select_tokens(const unsigned long long* cand, int k, const float* hp, int ra
 // x = rms(src, w) (w == nullptr: no norm, x = src); then either f32 out
 // (out_f32 != nullptr) or int8 codes + an f32 scale per row.
 // zero_buf / zero_n: a buffer the kernel clears on the side (nullptr: none).
+// out16 (nullptr: none): the codes also as exact f16 values [rows][n] (the
+// tcgen05 matmuls' activation operand).
 // div (nullptr: none): the source row is a sum of parts, and each div_seg
 // columns of source row r are first divided by div[r][segment] (the
 // attention's accumulate mode: y = yacc / lacc per head).
 int rms_rows(const float* src, int ld_src, RowMap map, int rows, int n, const float* w, float eps, float* out_f32,
              int ld_out, int8_t* out_codes, float* out_scale, int ld_codes, cudaStream_t st,
-             float* zero_buf = nullptr, int64_t zero_n = 0, const float* div = nullptr, int div_seg = 0);
+             float* zero_buf = nullptr, int64_t zero_n = 0, const float* div = nullptr, int div_seg = 0,
+             __half* out16 = nullptr);
 // h[r] = embed[tok(r)]: row r of sequence s = r / block_len is the anchor
 // (anchor_tok[s]) for r % block_len == 0, the mask token otherwise.  Side
 // duty (rope != nullptr): the block rows' rotation table rope[r][i] =
@@ -182,7 +185,7 @@ cudaError_t launch_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size
 }
 
 int silu_mul(const float* gu, int ld_gu, int rows, int I, float* out_f32, int ld_out, int8_t* out_codes,
-             float* out_scale, int ld_codes, cudaStream_t st);
+             float* out_scale, int ld_codes, cudaStream_t st, __half* out16 = nullptr);
 // One stage of the row convolution over `rows` block rows (block_len rows a
 // sequence) of n columns: y[r] = sum_{o < min(kn, r % block_len + 1)}
 // (base[stage][o] + d[r][(stage kn + o) (n / gs) + group]) * x[r - o], base
