@@ -202,6 +202,9 @@ __global__ void __launch_bounds__(NT, NT == kRowThreads || NV > 12 ? 1 : 2) rms_
     if (threadIdx.x == 0) out_scale[i] = sx;
 }
 
+// Rows from which a row kernel takes the many-rows configuration.
+constexpr int kManyRows = 128;
+
 static bool rows_fit_reg(int n, const void* src, int ld_src, const void* out_f32, int ld_out, const void* codes,
                          int ld_codes, int max_n) {
     auto al = [](const void* p, int a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; };
@@ -227,16 +230,19 @@ int rms_rows(const float* src, int ld_src, RowMap map, int rows, int n, const fl
             return (int)launch(kern, dim3(rows + extra), dim3(kRowThreads), 0, st, src, ld_src, map, n, w, eps, out_f32,
                                ld_out, out_codes, out_scale, ld_codes, zero_buf, zero_n, rows, div, div_seg, out16);
         };
-        if (nv <= 1) return go(rms_rows_reg_kernel<1>);
-        if (nv <= 2) return go(rms_rows_reg_kernel<2>);
-        if (nv <= 4) return go(rms_rows_reg_kernel<4>);
-        // wider rows (the taps): 512 threads a row, so that two rows share an SM
         const int nv512 = (n + 4 * 512 - 1) / (4 * 512);
         auto go512 = [&](auto kern) {
             const int extra512 = zero_buf && zero_n > 0 ? (int)std::min<int64_t>(256, zero_n / 4 / (512 * 4) + 1) : 0;
             return (int)launch(kern, dim3(rows + extra512), dim3(512), 0, st, src, ld_src, map, n, w, eps, out_f32, ld_out,
                                out_codes, out_scale, ld_codes, zero_buf, zero_n, rows, div, div_seg, out16);
         };
+        // many rows (a batch, a prefill): 512 threads a row, so that more rows
+        // share an SM and the launch runs in fewer waves
+        if (rows >= kManyRows && nv512 <= 2) return go512(rms_rows_reg_kernel<2, 512>);
+        if (nv <= 1) return go(rms_rows_reg_kernel<1>);
+        if (nv <= 2) return go(rms_rows_reg_kernel<2>);
+        if (nv <= 4) return go(rms_rows_reg_kernel<4>);
+        // wider rows (the taps): 512 threads a row, so that two rows share an SM
         if (nv512 <= 12) return go512(rms_rows_reg_kernel<12, 512>);
         return go512(rms_rows_reg_kernel<16, 512>);
     }
@@ -578,7 +584,8 @@ int silu_mul(const float* gu, int ld_gu, int rows, int I, float* out_f32, int ld
     if (rows <= 0) return 0;
     if (out16 && (!out_codes || out_f32 || I % 4 || (reinterpret_cast<uintptr_t>(out16) & 7)))
         return (int)cudaErrorInvalidValue;
-    if (I % (4 * kSiluSplit) == 0 && I / 4 / kSiluSplit <= kRowThreads &&
+    // few rows: a row over a cluster of kSiluSplit CTAs; many rows: a CTA a row
+    if (rows < kManyRows && I % (4 * kSiluSplit) == 0 && I / 4 / kSiluSplit <= kRowThreads &&
         rows_fit_reg(I, gu, ld_gu, out_f32, ld_out, out_codes, ld_codes, 4 * kSiluSplit * kRowThreads) &&
         (reinterpret_cast<uintptr_t>(gu + I) % 16) == 0)
         return (int)launch_cluster(silu_mul_cluster_kernel, dim3(kSiluSplit, rows), dim3(kRowThreads), 0, st,
