@@ -45,6 +45,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <cstring>
 
 #include "common.cuh"
 #include "kernels.cuh"
@@ -121,6 +122,31 @@ DF_DEV void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 }
 DF_DEV void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// a box of a tensor map fetched into L2 only (no shared memory, no barrier)
+DF_DEV void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
+                 : "memory");
+}
+// shared -> global through a tensor map (elements outside the map's extents
+// are not written): a plain store, or an f32 add into what is there
+DF_DEV void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map), "r"(x),
+                 "r"(y), "r"(smem_addr(src))
+                 : "memory");
+}
+DF_DEV void tma_reduce_add_2d(const CUtensorMap* map, const void* src, int x, int y) {
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map),
+                 "r"(x), "r"(y), "r"(smem_addr(src))
+                 : "memory");
+}
+DF_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the issuing thread's bulk groups: at most N still reading shared memory / none outstanding
+template <int N>
+DF_DEV void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+DF_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 DF_DEV void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
@@ -177,6 +203,7 @@ struct TcArgs {
     int K;
     unsigned long long bound;
     unsigned long long wn2_max;  // the largest of wn2: rows under the bound against it skip the check
+    int y_tma;                   // dense kernels: y is written through the output tensor map
 };
 
 template <bool kHead>
@@ -710,7 +737,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) q4_tc2_kernel(const __grid_cons
         if (__all_sync(0xffffffffu, ok && !aborted()) && nkb > 0) {
             const int sub = warp & 3, half = warp >> 2;
             const bool red = a.accumulate != 0 || gridDim.z > 1;
-            const bool vec_out = a.y && a.ldy % 4 == 0 && (reinterpret_cast<uintptr_t>(a.y) & 15) == 0;
             for (int t = 0; t < tiles; ++t) {
                 const int row = m0 + t * kTcM + 32 * sub + lane;
                 const int n0 = nt * kTcN + half * 64;
@@ -787,11 +813,15 @@ constexpr int kT3Bt = kT3N * kTcKB * 2;               // one 256 x 64 f16 weight
 template <bool kHead>
 struct T3Shape {
     static constexpr int kStages = kHead ? 3 : 2;
+    static constexpr int kAhead = kHead ? 6 : 4;  // k-blocks of weights prefetched into L2 ahead of the ring
     static constexpr int kStage = kT2Tiles * kTcA + (kHead ? 1 : 2) * kT3Bt;
     static constexpr size_t kSmem = 1024 + 1024 + (size_t)kStages * kStage;
     static_assert(kSmem <= 227 * 1024, "shared memory");
 };
 constexpr int kT3MaxStages = 3;
+// the epilogue's staging: a warp's 32 rows x 32 f32 columns (4 KB, 128-byte
+// swizzle), kT3Boxes of them a warp, in the idle stage ring
+constexpr int kT3Box = 32 * 32 * 4, kT3Boxes = 4;
 static_assert(kT2Tiles * kT3N <= 512, "tensor memory");
 constexpr uint32_t kT3Idesc = (1u << 4) | ((uint32_t)(kT3N >> 3) << 17) | ((uint32_t)(kTcM >> 4) << 24);
 
@@ -836,14 +866,18 @@ __device__ __noinline__ int exact_dot_f16(const __half* __restrict__ x, const __
 template <bool kHead>
 __global__ void __launch_bounds__(kTcThreads, 1)
     dense_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap hmap,
-                    const __grid_constant__ CUtensorMap lmap, TcArgs a) {
-    constexpr int kT3Stages = T3Shape<kHead>::kStages, kT3Stage = T3Shape<kHead>::kStage;
+                    const __grid_constant__ CUtensorMap lmap, const __grid_constant__ CUtensorMap ymap, TcArgs a) {
+    constexpr int kT3Stages = T3Shape<kHead>::kStages, kT3Stage = T3Shape<kHead>::kStage,
+                  kT3Ahead = T3Shape<kHead>::kAhead;
+    static_assert(kT3Boxes * kT3Box * (kTcThreads / 32 - 2) <= kT3Stages * kT3Stage, "staging inside the stage ring");
     extern __shared__ __align__(1024) unsigned char sm_raw[];
     unsigned char* sm = sm_raw + ((1024 - (smem_addr(sm_raw) & 1023)) & 1023);
     T3Ctl& ctl = *reinterpret_cast<T3Ctl*>(sm);
     unsigned char* stages = sm + 1024;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nt = kHead ? blockIdx.y : blockIdx.x, m0 = (kHead ? blockIdx.x : blockIdx.y) * (kT2Tiles * kTcM);
+    // the row tiles of one output tile are neighbours in the launch order, so
+    // they stream the same weight tile at about the same time (one HBM read)
+    const int nt = blockIdx.y, m0 = blockIdx.x * (kT2Tiles * kTcM);
     const int tiles = min(kT2Tiles, (a.T - m0 + kTcM - 1) / kTcM);
     const int kb_lo = blockIdx.z * a.kb_per_split, kb_hi = min(a.L.ksteps, kb_lo + a.kb_per_split);
     const int nkb = kb_hi - kb_lo;
@@ -868,7 +902,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
     const uint32_t tmem = ctl.tmem;
     pdl_trigger();
-    pdl_wait();
 
     auto give_up = [&]() {
         atomicExch(a.err, 1);
@@ -881,21 +914,47 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             asm volatile("prefetch.tensormap [%0];" ::"l"(&xmap) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(&hmap) : "memory");
             if (!kHead) asm volatile("prefetch.tensormap [%0];" ::"l"(&lmap) : "memory");
-            int issued = 0;
-            for (int i = 0; i < nkb; ++i) {
+            // whole boxes: rows past T or past N read as zeros and count toward the bytes
+            auto load_w = [&](int i) {
+                const int kb = kb_lo + i;
+                unsigned char* dst = stages + (i % kT3Stages) * kT3Stage + kT2Tiles * kTcA;
+                tma_load_2d(dst, &hmap, kb * kTcKB, nt * kT3N, &ctl.full[i % kT3Stages]);
+                if (!kHead) tma_load_2d(dst + kT3Bt, &lmap, kb * kTcKB, nt * kT3N, &ctl.full[i % kT3Stages]);
+            };
+            auto prefetch_w = [&](int i) {
+                if (i >= nkb) return;
+                tma_prefetch_2d(&hmap, (kb_lo + i) * kTcKB, nt * kT3N);
+                if (!kHead) tma_prefetch_2d(&lmap, (kb_lo + i) * kTcKB, nt * kT3N);
+            };
+            auto load_x = [&](int i) {
+                tma_load_2d(stages + (i % kT3Stages) * kT3Stage, &xmap, (kb_lo + i) * kTcKB, m0,
+                            &ctl.full[i % kT3Stages]);
+            };
+            // The weights are written only when the model is built, so the
+            // first stages' weight tiles, and an L2 prefetch of the next
+            // ones, go out before the wait on the kernel before (which
+            // writes the activations); later weight tiles are fetched into L2
+            // kT3Ahead k-blocks before their stage is loaded.
+            const int pre = min(nkb, kT3Stages);
+            for (int i = 0; i < pre; ++i) {
+                mbar_arrive_expect_tx(&ctl.full[i], (uint32_t)kT3Stage);
+                load_w(i);
+            }
+            for (int i = pre; i < pre + kT3Ahead; ++i) prefetch_w(i);
+            pdl_wait();
+            for (int i = 0; i < pre; ++i) load_x(i);
+            int issued = pre;
+            for (int i = pre; i < nkb; ++i) {
                 const int st = i % kT3Stages;
-                if (i >= kT3Stages && !mbar_wait(&ctl.empty[st], ((i / kT3Stages) - 1) & 1, kTcWait)) {
+                if (!mbar_wait(&ctl.empty[st], ((i / kT3Stages) - 1) & 1, kTcWait)) {
                     give_up();
                     break;
                 }
                 if (aborted()) break;
-                const int kb = kb_lo + i;
-                unsigned char* dst = stages + st * kT3Stage;
-                // whole boxes: rows past T or past N read as zeros and count toward the bytes
+                prefetch_w(i + kT3Ahead);
                 mbar_arrive_expect_tx(&ctl.full[st], (uint32_t)kT3Stage);
-                tma_load_2d(dst, &xmap, kb * kTcKB, m0, &ctl.full[st]);
-                tma_load_2d(dst + kT2Tiles * kTcA, &hmap, kb * kTcKB, nt * kT3N, &ctl.full[st]);
-                if (!kHead) tma_load_2d(dst + kT2Tiles * kTcA + kT3Bt, &lmap, kb * kTcKB, nt * kT3N, &ctl.full[st]);
+                load_x(i);
+                load_w(i);
                 issued = i + 1;
             }
             for (int i = max(0, issued - kT3Stages); i < issued; ++i)
@@ -928,68 +987,94 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else {
         // ---------------------------------------------------------------- epilogue
+        pdl_wait();  // (the row scales and the outputs belong to the kernels before)
         const bool ok = mbar_wait(&ctl.acc_full, 0, kTcWait);
         if (!ok) give_up();
         tc_fence_after();
         if (__all_sync(0xffffffffu, ok && !aborted()) && nkb > 0) {
+            // Warp w reads tensor-memory lanes 32 (w % 4) .. (its 32 rows) and
+            // columns 128 (w / 4) .. of each tile, 32 columns at a time. Each
+            // 32 x 32 block goes through a 4 KB box of the stage ring (idle
+            // now: every MMA has completed) in the 128-byte swizzle and out by
+            // one TMA store, or reduce-add, of whole 128-byte row segments:
+            // a lane storing its own row's 16 bytes at a time kept the
+            // epilogue an order of magnitude longer than the copy.
             const int sub = warp & 3, half = warp >> 2;
             const bool red = a.accumulate != 0 || gridDim.z > 1;
-            const bool vec_out = a.y && a.ldy % 4 == 0 && (reinterpret_cast<uintptr_t>(a.y) & 15) == 0;
+            unsigned char* stg = stages + warp * (kT3Boxes * kT3Box);
+            int nbox = 0;
             for (int t = 0; t < tiles; ++t) {
-                const int row = m0 + t * kTcM + 32 * sub + lane;
-                const int n0 = nt * kT3N + half * (kT3N / 2);
+                const int r0 = m0 + t * kTcM + 32 * sub, row = r0 + lane;
+                if (r0 >= a.T) break;  // (uniform in the warp)
                 const float xs = row < a.T ? a.xscale[row] : 0.f;
                 const unsigned long long xn = kHead && row < a.T ? (uint32_t)a.xn2[row] : 0ull;
                 const bool guard = kHead && xn * a.wn2_max > a.bound;
+                const bool any_guard = __any_sync(0xffffffffu, guard);
                 unsigned long long best = 0ull;
 #pragma unroll 1
-                for (int cc = 0; cc < kT3N / 2; cc += 16) {
-                    uint32_t v[16];
-                    tc_ld16(tmem + ((uint32_t)(32 * sub) << 16) + (uint32_t)(t * kT3N + half * (kT3N / 2) + cc), v);
+                for (int cc = 0; cc < kT3N / 2; cc += 32) {
+                    const int n0 = nt * kT3N + half * (kT3N / 2) + cc;
+                    if (n0 >= a.N) break;  // (uniform)
+                    // per-column factors, one column a lane, shuffled to the rows
+                    const int nl = n0 + lane;
+                    const float ws_l = kHead && nl < a.N ? a.wscale[nl] : 0.f;
+                    const int wn_l = kHead && any_guard && nl < a.N ? a.wn2[nl] : 0;
+                    uint32_t v[32];
+                    const uint32_t ta = tmem + ((uint32_t)(32 * sub) << 16) + (uint32_t)(t * kT3N + half * (kT3N / 2) + cc);
+                    tc_ld16(ta, *reinterpret_cast<uint32_t(*)[16]>(v));
+                    tc_ld16(ta + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
                     tc_wait_ld();
-                    if (row < a.T && n0 + cc < a.N) {
+                    float f[32];
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) {
+                        float acc = __uint_as_float(v[q]);
                         if (kHead) {
                             // logits = xs * sw[n] * (integer row sum), as the streaming head
-                            float l[16];
-#pragma unroll
-                            for (int q = 0; q < 16; ++q) {
-                                const int n = n0 + cc + q;
-                                float acc = __uint_as_float(v[q]);
-                                if (guard && n < a.N && xn * (uint32_t)a.wn2[n] > a.bound)
+                            const int n = n0 + q;
+                            const float ws = __shfl_sync(0xffffffffu, ws_l, q);
+                            if (any_guard) {
+                                const int wn = __shfl_sync(0xffffffffu, wn_l, q);
+                                if (guard && n < a.N && xn * (uint32_t)wn > a.bound)
                                     acc = (float)exact_dot_f16(a.xf + (int64_t)row * a.K, a.wf + (int64_t)n * a.K, a.K);
-                                l[q] = n < a.N ? xs * a.wscale[n] * acc : 0.f;
-                                if (n < a.N) best = max(best, argmax_key(l[q], (uint32_t)n));
                             }
-                            if (a.y) {
-                                float* dst = a.y + (int64_t)row * a.ldy + n0 + cc;
-                                if (vec_out && n0 + cc + 16 <= a.N) {
-#pragma unroll
-                                    for (int q = 0; q < 4; ++q)
-                                        *reinterpret_cast<float4*>(dst + 4 * q) =
-                                            make_float4(l[4 * q], l[4 * q + 1], l[4 * q + 2], l[4 * q + 3]);
-                                } else {
-#pragma unroll
-                                    for (int q = 0; q < 16; ++q)
-                                        if (n0 + cc + q < a.N) dst[q] = l[q];
-                                }
-                            }
+                            f[q] = n < a.N ? xs * ws * acc : 0.f;
+                            if (n < a.N && row < a.T) best = max(best, argmax_key(f[q], (uint32_t)n));
                         } else {
-                            float* dst = a.y + (int64_t)row * a.ldy + n0 + cc;
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                const float f0 = __uint_as_float(v[4 * q]) * xs, f1 = __uint_as_float(v[4 * q + 1]) * xs,
-                                            f2 = __uint_as_float(v[4 * q + 2]) * xs,
-                                            f3 = __uint_as_float(v[4 * q + 3]) * xs;
-                                if (red)
-                                    red_add_v4(dst + 4 * q, f0, f1, f2, f3);
-                                else
-                                    *reinterpret_cast<float4*>(dst + 4 * q) = make_float4(f0, f1, f2, f3);
-                            }
+                            f[q] = acc * xs;
                         }
                     }
+                    if (!a.y) continue;  // (the head's argmax alone)
+                    if (!a.y_tma) {
+                        // (a head whose logit rows are not 16-byte multiples: plain stores)
+                        if (row < a.T)
+                            for (int q = 0; q < 32; ++q)
+                                if (n0 + q < a.N) a.y[(int64_t)row * a.ldy + n0 + q] = f[q];
+                        continue;
+                    }
+                    unsigned char* box = stg + (nbox % kT3Boxes) * kT3Box;
+                    if (nbox >= kT3Boxes) {
+                        if (lane == 0) bulk_wait_read<kT3Boxes - 1>();
+                        __syncwarp();
+                    }
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<float4*>(box + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                            make_float4(f[4 * c], f[4 * c + 1], f[4 * c + 2], f[4 * c + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (red)
+                            tma_reduce_add_2d(&ymap, box, n0, r0);
+                        else
+                            tma_store_2d(&ymap, box, n0, r0);
+                        bulk_commit();
+                    }
+                    ++nbox;
                 }
                 if (kHead && row < a.T && best) atomicMax(a.keys + row, best);
             }
+            if (lane == 0) bulk_wait_all();
+            __syncwarp();
         }
     }
     tc_fence_before();
@@ -1181,6 +1266,20 @@ static bool dense_map(CUtensorMap* map, const __half* w, int K, int N, int box_r
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// an f32 output [T][ldy] as a TMA tensor map of its first N columns: 32 x 32
+// boxes in the 128-byte swizzle (what the dense kernels' epilogue stages);
+// false where the rows are not 16-byte multiples or the base not 16-aligned
+static bool out_map(CUtensorMap* map, float* y, int ldy, int N, int T) {
+    if (!y || ldy % 4 || (reinterpret_cast<uintptr_t>(y) & 15)) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)T};
+    const cuuint64_t strides[1] = {(cuuint64_t)ldy * 4};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    return encode_fn()(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, y, dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int q4_tc_dense(const __half* hi, const __half* lo, int N, int K, QAct x, const __half* x16, int T, float* y, int ldy,
                 bool accumulate, int num_sms, int* err_flag, cudaStream_t st) {
     if (T <= 0 || N <= 0) return 0;
@@ -1188,8 +1287,9 @@ int q4_tc_dense(const __half* hi, const __half* lo, int N, int K, QAct x, const 
         (reinterpret_cast<uintptr_t>(x16) & 15) || (reinterpret_cast<uintptr_t>(hi) & 15) ||
         (reinterpret_cast<uintptr_t>(lo) & 15))
         return (int)cudaErrorInvalidValue;
-    CUtensorMap xm, hm, lm;
-    if (!act_map(&xm, x16, K, T, kT2Tiles * kTcM) || !dense_map(&hm, hi, K, N, kT3N) || !dense_map(&lm, lo, K, N, kT3N))
+    CUtensorMap xm, hm, lm, ym;
+    if (!act_map(&xm, x16, K, T, kT2Tiles * kTcM) || !dense_map(&hm, hi, K, N, kT3N) ||
+        !dense_map(&lm, lo, K, N, kT3N) || !out_map(&ym, y, ldy, N, T))
         return (int)cudaErrorInvalidValue;
     static bool attr = false;
     if (!attr) {
@@ -1222,8 +1322,9 @@ int q4_tc_dense(const __half* hi, const __half* lo, int N, int K, QAct x, const 
     }
     Q4Layout L{0, ksteps, 1};
     TcArgs args{nullptr, L, 0, N, x.scale, T, y, ldy, accumulate ? 1 : 0, kps, nullptr, nullptr, err_flag};
-    return (int)launch(dense_tc_kernel<false>, dim3(ntl, mt, splits), dim3(kTcThreads), T3Shape<false>::kSmem, st, xm,
-                       hm, lm, args);
+    args.y_tma = 1;
+    return (int)launch(dense_tc_kernel<false>, dim3(mt, ntl, splits), dim3(kTcThreads), T3Shape<false>::kSmem, st, xm,
+                       hm, lm, ym, args);
 }
 
 int head_tc_dense(const __half* w16, const int* w_norm2, const float* row_scale, int V, int K, QAct x,
@@ -1233,9 +1334,12 @@ int head_tc_dense(const __half* w16, const int* w_norm2, const float* row_scale,
     if (encode_fn() == nullptr || K % kTcKB || (reinterpret_cast<uintptr_t>(x16) & 15) ||
         (reinterpret_cast<uintptr_t>(w16) & 15) || !w_norm2 || !x_norm2)
         return (int)cudaErrorInvalidValue;
-    CUtensorMap xm, wm;
+    CUtensorMap xm, wm, ym;
     if (!act_map(&xm, x16, K, T, kT2Tiles * kTcM) || !dense_map(&wm, w16, K, V, kT3N))
         return (int)cudaErrorInvalidValue;
+    // the logits through the output map where their rows allow one, else plain stores
+    const bool y_tma = out_map(&ym, logits, ldl, V, T);
+    if (!y_tma) memset(&ym, 0, sizeof(ym));
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(dense_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1247,8 +1351,9 @@ int head_tc_dense(const __half* w16, const int* w_norm2, const float* row_scale,
     Q4Layout L{0, K / kTcKB, 1};
     TcArgs args{nullptr, L,        0,       V,   x.scale, T,   logits, ldl, 0, K / kTcKB, row_scale,
                 keys,    err_flag, x_norm2, w_norm2, x16,     w16, K,      bound,  w_norm2_max};
+    args.y_tma = y_tma ? 1 : 0;
     return (int)launch(dense_tc_kernel<true>, dim3(mt, ntl, 1), dim3(kTcThreads), T3Shape<true>::kSmem, st, xm, wm, wm,
-                       args);
+                       ym, args);
 }
 
 }  // namespace dflash
