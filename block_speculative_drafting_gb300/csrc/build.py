@@ -17,7 +17,8 @@ PKG = os.path.dirname(HERE)
 ROOT = os.path.dirname(PKG)
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdflash.so")
-SOURCES = ["api.cu", "k_quant.cu", "k_gemm.cu", "k_layer.cu", "k_stream.cu", "k_tc.cu", "k_attn_tc.cu"]
+SOURCES = ["api.cu", "k_quant.cu", "k_gemm.cu", "k_layer.cu", "k_stream.cu", "k_tc.cu", "k_tc_pair.cu",
+           "k_attn_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "-I", os.path.join(ROOT, "include")]

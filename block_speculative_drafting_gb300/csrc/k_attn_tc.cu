@@ -35,6 +35,7 @@
 #include "attn.cuh"
 #include "common.cuh"
 #include "kernels.cuh"
+#include "tc.cuh"
 
 namespace dflash {
 
@@ -560,10 +561,6 @@ int attn_tc_plan(int n_seqs, int block_len, int max_ctx, int nkv, int num_sms) {
     return std::max(1, std::min(max_split, num_sms / units));
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-EncodeTiledFn encode_fn();  // k_tc.cu
 
 bool kv_tensor_maps(const __half* k, const __half* v, int nkv, int64_t cap, int hd, void* out) {
     EncodeTiledFn enc = encode_fn();

@@ -49,6 +49,7 @@
 
 #include "common.cuh"
 #include "kernels.cuh"
+#include "tc.cuh"
 
 namespace dflash {
 
@@ -88,13 +89,6 @@ struct TcShape {
 // 17-22, M >> 4 at bits 24-28.
 constexpr uint32_t kTcIdesc = (1u << 4) | ((uint32_t)(kTcN >> 3) << 17) | ((uint32_t)(kTcM >> 4) << 24);
 
-// Shared-memory matrix descriptor: a K-major tile with 128-byte rows in the
-// 128-byte swizzle (eight-row atoms of 1024 bytes, stride 1024 bytes between
-// atoms), base 1024-aligned; the k16 slice j starts 32 j bytes into the rows.
-DF_DEV uint64_t tc_desc_sw128(uint32_t saddr) {
-    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
 // byte offset of the 16-byte chunk c (columns 8c .. 8c+7) of row r in such a tile
 DF_DEV uint32_t tc_swz(int r, int c) { return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4)); }
 
@@ -109,51 +103,9 @@ DF_DEV void tc_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
                  : "memory");
 }
-DF_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-DF_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 16 consecutive f32 columns of this thread's tensor-memory lane (whole warp)
-DF_DEV void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-}
-DF_DEV void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// a box of a tensor map fetched into L2 only (no shared memory, no barrier)
-DF_DEV void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
-                 : "memory");
-}
-// shared -> global through a tensor map (elements outside the map's extents
-// are not written): a plain store, or an f32 add into what is there
-DF_DEV void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map), "r"(x),
-                 "r"(y), "r"(smem_addr(src))
-                 : "memory");
-}
-DF_DEV void tma_reduce_add_2d(const CUtensorMap* map, const void* src, int x, int y) {
-    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map),
-                 "r"(x), "r"(y), "r"(smem_addr(src))
-                 : "memory");
-}
-DF_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// the issuing thread's bulk groups: at most N still reading shared memory / none outstanding
-template <int N>
-DF_DEV void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-DF_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-DF_DEV void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-        "[%4];" ::"r"(smem_addr(dst)),
-        "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar))
-        : "memory");
-}
 
 // hi / lo of s * q for four half2 of codes q
 DF_DEV void split_scaled(const uint32_t (&q)[4], uint32_t s2, uint4& hi, uint4& lo) {
@@ -832,6 +784,23 @@ DF_DEV void tc_mma_n256(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_
         "l"(adesc), "l"(bdesc), "r"(kT3Idesc), "r"(accumulate)
         : "memory");
 }
+// The hi and lo MMAs of a k16 slice share their A tile: the first fills the
+// tensor core's A collector, the second takes A from it instead of reading
+// the tile from shared memory again (shared-memory bandwidth, which the
+// MMAs' operand reads and the TMA's writes share, bounds this kernel).
+DF_DEV void tc_mma_n256_fill(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16.collector::a::fill [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(kT3Idesc), "r"(accumulate)
+        : "memory");
+}
+DF_DEV void tc_mma_n256_lastuse(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc) {
+    asm volatile(
+        "tcgen05.mma.cta_group::1.kind::f16.collector::a::lastuse [%0], %1, %2, %3, 1;\n" ::"r"(tmem_d), "l"(adesc),
+        "l"(bdesc), "r"(kT3Idesc)
+        : "memory");
+}
 
 struct T3Ctl {
     uint64_t full[kT3MaxStages], empty[kT3MaxStages], acc_full;
@@ -976,8 +945,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     for (int t = 0; t < tiles; ++t) {
                         const uint64_t ad = tc_desc_sw128(sa + t * kTcA + 32 * j);
                         const uint32_t d = tmem + (uint32_t)(t * kT3N);
-                        tc_mma_n256(d, ad, bh, (i > 0 || j > 0) ? 1u : 0u);
-                        if (!kHead) tc_mma_n256(d, ad, bl, 1u);
+                        if (kHead) {
+                            tc_mma_n256(d, ad, bh, (i > 0 || j > 0) ? 1u : 0u);
+                        } else {
+                            tc_mma_n256_fill(d, ad, bh, (i > 0 || j > 0) ? 1u : 0u);
+                            tc_mma_n256_lastuse(d, ad, bl);
+                        }
                     }
                 }
                 tc_commit(&ctl.empty[st]);
@@ -1088,9 +1061,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 // ---------------------------------------------------------------- host side
 // (shared with the tcgen05 attention's tensor maps)
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 EncodeTiledFn encode_fn() {
     static EncodeTiledFn fn = nullptr;
@@ -1111,7 +1081,7 @@ EncodeTiledFn encode_fn() {
 
 // the tensor map of the activation codes as f16 [T][K] (rows of K halves):
 // 64 x 128 boxes in the 128-byte swizzle, rows past T read as zeros
-static bool act_map(CUtensorMap* map, const __half* codes, int K, int T, int box_rows = kTcM) {
+bool act_map(CUtensorMap* map, const __half* codes, int K, int T, int box_rows) {
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)T};
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
     const cuuint32_t box[2] = {(cuuint32_t)kTcKB, (cuuint32_t)box_rows};
@@ -1245,7 +1215,7 @@ int head_tc(const int8_t* packed, const float* row_scale, int V, int ksteps, QAc
     if (T <= 0 || V <= 0) return 0;
     if (!head_tc_supported(ksteps, x) || (reinterpret_cast<uintptr_t>(x16) & 15)) return (int)cudaErrorInvalidValue;
     CUtensorMap map;
-    if (!act_map(&map, x16, ksteps * kI8KStep, T)) return (int)cudaErrorInvalidValue;
+    if (!act_map(&map, x16, ksteps * kI8KStep, T, kTcM)) return (int)cudaErrorInvalidValue;
     cudaError_t e = tc_set_smem<true>();
     if (e != cudaSuccess) return (int)e;
     const int mt = (T + kTcM - 1) / kTcM, ntl = (V + kTcN - 1) / kTcN;
@@ -1256,7 +1226,7 @@ int head_tc(const int8_t* packed, const float* row_scale, int V, int ksteps, QAc
 }
 
 // a dense f16 weight copy [N][K] as a TMA tensor map: 64 x 128 boxes, 128-byte swizzle
-static bool dense_map(CUtensorMap* map, const __half* w, int K, int N, int box_rows = kTcN) {
+bool dense_map(CUtensorMap* map, const __half* w, int K, int N, int box_rows) {
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
     const cuuint32_t box[2] = {(cuuint32_t)kTcKB, (cuuint32_t)box_rows};
@@ -1269,7 +1239,7 @@ static bool dense_map(CUtensorMap* map, const __half* w, int K, int N, int box_r
 // an f32 output [T][ldy] as a TMA tensor map of its first N columns: 32 x 32
 // boxes in the 128-byte swizzle (what the dense kernels' epilogue stages);
 // false where the rows are not 16-byte multiples or the base not 16-aligned
-static bool out_map(CUtensorMap* map, float* y, int ldy, int N, int T) {
+bool out_map(CUtensorMap* map, float* y, int ldy, int N, int T) {
     if (!y || ldy % 4 || (reinterpret_cast<uintptr_t>(y) & 15)) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)T};
     const cuuint64_t strides[1] = {(cuuint64_t)ldy * 4};

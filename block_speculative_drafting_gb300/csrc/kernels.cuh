@@ -94,6 +94,16 @@ int q4_tc_dense(const __half* hi, const __half* lo, int N, int K, QAct x, const 
 int head_tc_dense(const __half* w16, const int* w_norm2, const float* row_scale, int V, int K, QAct x,
                   const __half* x16, const int* x_norm2, int T, float* logits, int ldl, unsigned long long* keys,
                   unsigned long long bound, unsigned long long w_norm2_max, int* err_flag, cudaStream_t st);
+// The same two products on pairs of SMs (k_tc_pair.cu): 256-row x 256-output
+// units, tcgen05.mma cta_group::2, a persistent grid of one pair per two SMs
+// with two accumulators in tensor memory (the epilogue of one unit overlaps
+// the MMAs of the next).  Same arguments and results as q4_tc_dense /
+// head_tc_dense.
+int q4_tc_pair(const __half* hi, const __half* lo, int N, int K, QAct x, const __half* x16, int T, float* y, int ldy,
+               bool accumulate, int* err_flag, cudaStream_t st);
+int head_tc_pair(const __half* w16, const int* w_norm2, const float* row_scale, int V, int K, QAct x,
+                 const __half* x16, const int* x_norm2, int T, float* logits, int ldl, unsigned long long* keys,
+                 unsigned long long bound, unsigned long long w_norm2_max, int* err_flag, cudaStream_t st);
 // int8 activation codes [T][ld] -> f16 [T][K] (exact), for the tcgen05 kernels'
 // TMA; with norm2 non-null also each row's squared code norm (K < 2^17).
 int codes_to_f16(const int8_t* x, int ld, int T, int K, __half* out, int* norm2, int num_sms, cudaStream_t st);
