@@ -95,7 +95,6 @@ struct dflash_model {
     // (off: dequantised in the kernel)
     bool use_tc = true;
     bool use_dense = true;
-    bool use_pair = true;  // the dense copies' matmuls on SM pairs (off: one SM a tile)
     int64_t tc_attn_min_keys = kTcAttnMinKeys;  // keys a CTA of the tcgen05 attention streams at least
     // dense f16 copies of the matrices for the many-row path, built on first need:
     // the 4-bit matrices as (hi, lo) planes [N][K], the head's codes [vocab][hidden]
@@ -714,8 +713,7 @@ int q4_mm(dflash_model* m, const uint8_t* packed, Q4Layout L, int tile0, int N, 
         if (dense_of(m, packed, tile0 * 16, N, K, &hi, &lo)) {
             // dense weight bytes: 4 a weight
             KL(m, "q4_tc", 1, (double)N * K * 4 + (double)T * K * 2 + (double)T * N * 4 * (accumulate ? 2 : 1), st,
-               m->use_pair ? q4_tc_pair(hi, lo, N, K, x, x16, T, y, ldy, accumulate, m->err_dev, st)
-                           : q4_tc_dense(hi, lo, N, K, x, x16, T, y, ldy, accumulate, m->num_sms, m->err_dev, st));
+               q4_tc_dense(hi, lo, N, K, x, x16, T, y, ldy, accumulate, m->err_dev, st));
         } else {
             KL(m, "q4_tc", 1, q4_bytes_of(N, K, T, accumulate), st,
                q4_tc(packed, L, tile0, N, x, x16, T, y, ldy, accumulate, m->num_sms, m->err_dev, st));
@@ -741,10 +739,8 @@ int run_head(dflash_model* m, QAct xh, int D, float* logit_out, unsigned long lo
             KL(m, "act_f16", 1, (double)D * H * 3 + (double)D * 4, st,
                codes_to_f16(xh.codes, xh.ld, D, H, x16, xn2, m->num_sms, st));
             KL(m, "head_tc", 1, hb + (double)g.vocab * H + (double)g.vocab * 4, st,
-               m->use_pair ? head_tc_pair(m->head16, m->head_norm2, m->head_scale, g.vocab, H, xh, x16, xn2, D,
-                                          logit_out, g.vocab, keys, m->head_bound, m->head_norm2_max, m->err_dev, st)
-                           : head_tc_dense(m->head16, m->head_norm2, m->head_scale, g.vocab, H, xh, x16, xn2, D,
-                                           logit_out, g.vocab, keys, m->head_bound, m->head_norm2_max, m->err_dev, st));
+               head_tc_dense(m->head16, m->head_norm2, m->head_scale, g.vocab, H, xh, x16, xn2, D, logit_out, g.vocab,
+                             keys, m->head_bound, m->head_norm2_max, m->err_dev, st));
         } else {
             KL(m, "act_f16", 1, (double)D * H * 3, st,
                codes_to_f16(xh.codes, xh.ld, D, H, x16, nullptr, m->num_sms, st));
@@ -1781,8 +1777,7 @@ int dflash_debug_option(dflash_model* m, const char* name, int64_t value) {
         m->use_tc = value != 0;
     } else if (opt == "dense") {
         m->use_dense = value != 0;
-    } else if (opt == "pair") {
-        m->use_pair = value != 0;
+
     } else if (opt == "attn_tc_min_keys") {
         if (value < 0) return set_err(m, DFLASH_EINVAL, "attn_tc_min_keys < 0");
         m->tc_attn_min_keys = value;

@@ -749,316 +749,6 @@ int dequant_hilo(const int8_t* codes, const uint16_t* scales, int N, int K, __ha
     return (int)cudaGetLastError();
 }
 
-// ---------------------------------------------------------------- 4-bit and head, dense copies
-// q4_tc2_kernel's row tiling (two 128-row tiles a CTA, K slices of at most
-// kT2MaxKb k-blocks), 256 outputs a CTA (M 128 x N 256 MMAs), the weight
-// tiles' hi and lo planes (the head: its one plane of codes) loaded by TMA
-// from the dense copy: one TMA lane, one MMA lane, eight epilogue warps.
-// A CTA computes 256 rows x kT3N outputs: the wide N halves the activation
-// bytes a multiply-add takes from L2 (the operand feed, not the MMAs, bounded
-// the 128-output form).
-constexpr int kT3N = 256;                             // outputs of a CTA: MMA N
-constexpr int kT3Bt = kT3N * kTcKB * 2;               // one 256 x 64 f16 weight tile (32 KB)
-// per variant: the 4-bit matrices take a 256-row activation box and the hi
-// and lo weight tiles a stage (96 KB, two stages), the head the box and one
-// code tile (64 KB, three stages)
-template <bool kHead>
-struct T3Shape {
-    static constexpr int kStages = kHead ? 3 : 2;
-    static constexpr int kAhead = kHead ? 6 : 4;  // k-blocks of weights prefetched into L2 ahead of the ring
-    static constexpr int kStage = kT2Tiles * kTcA + (kHead ? 1 : 2) * kT3Bt;
-    static constexpr size_t kSmem = 1024 + 1024 + (size_t)kStages * kStage;
-    static_assert(kSmem <= 227 * 1024, "shared memory");
-};
-constexpr int kT3MaxStages = 3;
-// the epilogue's staging: a warp's 32 rows x 32 f32 columns (4 KB, 128-byte
-// swizzle), kT3Boxes of them a warp, in the idle stage ring
-constexpr int kT3Box = 32 * 32 * 4, kT3Boxes = 4;
-static_assert(kT2Tiles * kT3N <= 512, "tensor memory");
-constexpr uint32_t kT3Idesc = (1u << 4) | ((uint32_t)(kT3N >> 3) << 17) | ((uint32_t)(kTcM >> 4) << 24);
-
-DF_DEV void tc_mma_n256(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(kT3Idesc), "r"(accumulate)
-        : "memory");
-}
-// The hi and lo MMAs of a k16 slice share their A tile: the first fills the
-// tensor core's A collector, the second takes A from it instead of reading
-// the tile from shared memory again (shared-memory bandwidth, which the
-// MMAs' operand reads and the TMA's writes share, bounds this kernel).
-DF_DEV void tc_mma_n256_fill(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16.collector::a::fill [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(kT3Idesc), "r"(accumulate)
-        : "memory");
-}
-DF_DEV void tc_mma_n256_lastuse(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc) {
-    asm volatile(
-        "tcgen05.mma.cta_group::1.kind::f16.collector::a::lastuse [%0], %1, %2, %3, 1;\n" ::"r"(tmem_d), "l"(adesc),
-        "l"(bdesc), "r"(kT3Idesc)
-        : "memory");
-}
-
-struct T3Ctl {
-    uint64_t full[kT3MaxStages], empty[kT3MaxStages], acc_full;
-    uint32_t tmem;
-    int abort;
-};
-
-// The exact integer dot product of two rows of f16 codes (|code| <= 127: every
-// product is exact in f32), for the head elements the norm guard rejects.
-__device__ __noinline__ int exact_dot_f16(const __half* __restrict__ x, const __half* __restrict__ w, int K) {
-    int s = 0;
-    for (int k = 0; k < K; k += 8) {
-        const uint4 a = *reinterpret_cast<const uint4*>(x + k), b = *reinterpret_cast<const uint4*>(w + k);
-        const __half2* ah = reinterpret_cast<const __half2*>(&a);
-        const __half2* bh = reinterpret_cast<const __half2*>(&b);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float2 fa = __half22float2(ah[j]), fb = __half22float2(bh[j]);
-            s += (int)(fa.x * fb.x) + (int)(fa.y * fb.y);
-        }
-    }
-    return s;
-}
-
-// kHead: the head's codes (one plane) against the rows, the logits and the
-// argmax in the epilogue, the whole K in tensor memory. Its products are
-// integers, so a sum is exact in f32 while every partial sum stays within
-// 2^24 in magnitude; by Cauchy-Schwarz each is at most |x|*|w| (code norms),
-// so an element whose norm product passes the bound is recomputed as an
-// integer dot product instead. The row tiles of one output tile run together
-// (x = row tile pair) so the weight tile is read from HBM once.
-template <bool kHead>
-__global__ void __launch_bounds__(kTcThreads, 1)
-    dense_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap hmap,
-                    const __grid_constant__ CUtensorMap lmap, const __grid_constant__ CUtensorMap ymap, TcArgs a) {
-    constexpr int kT3Stages = T3Shape<kHead>::kStages, kT3Stage = T3Shape<kHead>::kStage,
-                  kT3Ahead = T3Shape<kHead>::kAhead;
-    static_assert(kT3Boxes * kT3Box * (kTcThreads / 32 - 2) <= kT3Stages * kT3Stage, "staging inside the stage ring");
-    extern __shared__ __align__(1024) unsigned char sm_raw[];
-    unsigned char* sm = sm_raw + ((1024 - (smem_addr(sm_raw) & 1023)) & 1023);
-    T3Ctl& ctl = *reinterpret_cast<T3Ctl*>(sm);
-    unsigned char* stages = sm + 1024;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // the row tiles of one output tile are neighbours in the launch order, so
-    // they stream the same weight tile at about the same time (one HBM read)
-    const int nt = blockIdx.y, m0 = blockIdx.x * (kT2Tiles * kTcM);
-    const int tiles = min(kT2Tiles, (a.T - m0 + kTcM - 1) / kTcM);
-    const int kb_lo = blockIdx.z * a.kb_per_split, kb_hi = min(a.L.ksteps, kb_lo + a.kb_per_split);
-    const int nkb = kb_hi - kb_lo;
-
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kT3Stages; ++i) {
-            mbar_init(&ctl.full[i], 1);
-            mbar_init(&ctl.empty[i], 1);
-        }
-        mbar_init(&ctl.acc_full, 1);
-        ctl.abort = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    if (warp == kTcMmaWarp) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&ctl.tmem)),
-                     "r"(kT2Tiles * kT3N)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = ctl.tmem;
-    pdl_trigger();
-
-    auto give_up = [&]() {
-        atomicExch(a.err, 1);
-        *reinterpret_cast<volatile int*>(&ctl.abort) = 1;
-    };
-    auto aborted = [&]() { return *reinterpret_cast<volatile int*>(&ctl.abort) != 0; };
-
-    if (warp == kTcTmaWarp) {
-        if (lane == 0) {
-            asm volatile("prefetch.tensormap [%0];" ::"l"(&xmap) : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"(&hmap) : "memory");
-            if (!kHead) asm volatile("prefetch.tensormap [%0];" ::"l"(&lmap) : "memory");
-            // whole boxes: rows past T or past N read as zeros and count toward the bytes
-            auto load_w = [&](int i) {
-                const int kb = kb_lo + i;
-                unsigned char* dst = stages + (i % kT3Stages) * kT3Stage + kT2Tiles * kTcA;
-                tma_load_2d(dst, &hmap, kb * kTcKB, nt * kT3N, &ctl.full[i % kT3Stages]);
-                if (!kHead) tma_load_2d(dst + kT3Bt, &lmap, kb * kTcKB, nt * kT3N, &ctl.full[i % kT3Stages]);
-            };
-            auto prefetch_w = [&](int i) {
-                if (i >= nkb) return;
-                tma_prefetch_2d(&hmap, (kb_lo + i) * kTcKB, nt * kT3N);
-                if (!kHead) tma_prefetch_2d(&lmap, (kb_lo + i) * kTcKB, nt * kT3N);
-            };
-            auto load_x = [&](int i) {
-                tma_load_2d(stages + (i % kT3Stages) * kT3Stage, &xmap, (kb_lo + i) * kTcKB, m0,
-                            &ctl.full[i % kT3Stages]);
-            };
-            // The weights are written only when the model is built, so the
-            // first stages' weight tiles, and an L2 prefetch of the next
-            // ones, go out before the wait on the kernel before (which
-            // writes the activations); later weight tiles are fetched into L2
-            // kT3Ahead k-blocks before their stage is loaded.
-            const int pre = min(nkb, kT3Stages);
-            for (int i = 0; i < pre; ++i) {
-                mbar_arrive_expect_tx(&ctl.full[i], (uint32_t)kT3Stage);
-                load_w(i);
-            }
-            for (int i = pre; i < pre + kT3Ahead; ++i) prefetch_w(i);
-            pdl_wait();
-            for (int i = 0; i < pre; ++i) load_x(i);
-            int issued = pre;
-            for (int i = pre; i < nkb; ++i) {
-                const int st = i % kT3Stages;
-                if (!mbar_wait(&ctl.empty[st], ((i / kT3Stages) - 1) & 1, kTcWait)) {
-                    give_up();
-                    break;
-                }
-                if (aborted()) break;
-                prefetch_w(i + kT3Ahead);
-                mbar_arrive_expect_tx(&ctl.full[st], (uint32_t)kT3Stage);
-                load_x(i);
-                load_w(i);
-                issued = i + 1;
-            }
-            for (int i = max(0, issued - kT3Stages); i < issued; ++i)
-                mbar_wait(&ctl.full[i % kT3Stages], (i / kT3Stages) & 1, kTcWait);
-        }
-    } else if (warp == kTcMmaWarp) {
-        if (lane == 0) {
-            for (int i = 0; i < nkb; ++i) {
-                const int st = i % kT3Stages;
-                const bool ok = mbar_wait(&ctl.full[st], (i / kT3Stages) & 1, kTcWait);
-                if (!ok) give_up();
-                if (!ok || aborted()) break;
-                tc_fence_after();
-                const uint32_t sa = smem_addr(stages + st * kT3Stage);
-                const uint32_t sb = sa + kT2Tiles * kTcA;
-#pragma unroll
-                for (int j = 0; j < kTcKB / 16; ++j) {
-                    const uint64_t bh = tc_desc_sw128(sb + 32 * j), bl = tc_desc_sw128(sb + kT3Bt + 32 * j);
-                    for (int t = 0; t < tiles; ++t) {
-                        const uint64_t ad = tc_desc_sw128(sa + t * kTcA + 32 * j);
-                        const uint32_t d = tmem + (uint32_t)(t * kT3N);
-                        if (kHead) {
-                            tc_mma_n256(d, ad, bh, (i > 0 || j > 0) ? 1u : 0u);
-                        } else {
-                            tc_mma_n256_fill(d, ad, bh, (i > 0 || j > 0) ? 1u : 0u);
-                            tc_mma_n256_lastuse(d, ad, bl);
-                        }
-                    }
-                }
-                tc_commit(&ctl.empty[st]);
-            }
-            // arrives once every MMA issued so far has completed
-            tc_commit(&ctl.acc_full);
-        }
-    } else {
-        // ---------------------------------------------------------------- epilogue
-        pdl_wait();  // (the row scales and the outputs belong to the kernels before)
-        const bool ok = mbar_wait(&ctl.acc_full, 0, kTcWait);
-        if (!ok) give_up();
-        tc_fence_after();
-        if (__all_sync(0xffffffffu, ok && !aborted()) && nkb > 0) {
-            // Warp w reads tensor-memory lanes 32 (w % 4) .. (its 32 rows) and
-            // columns 128 (w / 4) .. of each tile, 32 columns at a time. Each
-            // 32 x 32 block goes through a 4 KB box of the stage ring (idle
-            // now: every MMA has completed) in the 128-byte swizzle and out by
-            // one TMA store, or reduce-add, of whole 128-byte row segments:
-            // a lane storing its own row's 16 bytes at a time kept the
-            // epilogue an order of magnitude longer than the copy.
-            const int sub = warp & 3, half = warp >> 2;
-            const bool red = a.accumulate != 0 || gridDim.z > 1;
-            unsigned char* stg = stages + warp * (kT3Boxes * kT3Box);
-            int nbox = 0;
-            for (int t = 0; t < tiles; ++t) {
-                const int r0 = m0 + t * kTcM + 32 * sub, row = r0 + lane;
-                if (r0 >= a.T) break;  // (uniform in the warp)
-                const float xs = row < a.T ? a.xscale[row] : 0.f;
-                const unsigned long long xn = kHead && row < a.T ? (uint32_t)a.xn2[row] : 0ull;
-                const bool guard = kHead && xn * a.wn2_max > a.bound;
-                const bool any_guard = __any_sync(0xffffffffu, guard);
-                unsigned long long best = 0ull;
-#pragma unroll 1
-                for (int cc = 0; cc < kT3N / 2; cc += 32) {
-                    const int n0 = nt * kT3N + half * (kT3N / 2) + cc;
-                    if (n0 >= a.N) break;  // (uniform)
-                    // per-column factors, one column a lane, shuffled to the rows
-                    const int nl = n0 + lane;
-                    const float ws_l = kHead && nl < a.N ? a.wscale[nl] : 0.f;
-                    const int wn_l = kHead && any_guard && nl < a.N ? a.wn2[nl] : 0;
-                    uint32_t v[32];
-                    const uint32_t ta = tmem + ((uint32_t)(32 * sub) << 16) + (uint32_t)(t * kT3N + half * (kT3N / 2) + cc);
-                    tc_ld16(ta, *reinterpret_cast<uint32_t(*)[16]>(v));
-                    tc_ld16(ta + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
-                    tc_wait_ld();
-                    float f[32];
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) {
-                        float acc = __uint_as_float(v[q]);
-                        if (kHead) {
-                            // logits = xs * sw[n] * (integer row sum), as the streaming head
-                            const int n = n0 + q;
-                            const float ws = __shfl_sync(0xffffffffu, ws_l, q);
-                            if (any_guard) {
-                                const int wn = __shfl_sync(0xffffffffu, wn_l, q);
-                                if (guard && n < a.N && xn * (uint32_t)wn > a.bound)
-                                    acc = (float)exact_dot_f16(a.xf + (int64_t)row * a.K, a.wf + (int64_t)n * a.K, a.K);
-                            }
-                            f[q] = n < a.N ? xs * ws * acc : 0.f;
-                            if (n < a.N && row < a.T) best = max(best, argmax_key(f[q], (uint32_t)n));
-                        } else {
-                            f[q] = acc * xs;
-                        }
-                    }
-                    if (!a.y) continue;  // (the head's argmax alone)
-                    if (!a.y_tma) {
-                        // (a head whose logit rows are not 16-byte multiples: plain stores)
-                        if (row < a.T)
-                            for (int q = 0; q < 32; ++q)
-                                if (n0 + q < a.N) a.y[(int64_t)row * a.ldy + n0 + q] = f[q];
-                        continue;
-                    }
-                    unsigned char* box = stg + (nbox % kT3Boxes) * kT3Box;
-                    if (nbox >= kT3Boxes) {
-                        if (lane == 0) bulk_wait_read<kT3Boxes - 1>();
-                        __syncwarp();
-                    }
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<float4*>(box + lane * 128 + ((c ^ (lane & 7)) << 4)) =
-                            make_float4(f[4 * c], f[4 * c + 1], f[4 * c + 2], f[4 * c + 3]);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (red)
-                            tma_reduce_add_2d(&ymap, box, n0, r0);
-                        else
-                            tma_store_2d(&ymap, box, n0, r0);
-                        bulk_commit();
-                    }
-                    ++nbox;
-                }
-                if (kHead && row < a.T && best) atomicMax(a.keys + row, best);
-            }
-            if (lane == 0) bulk_wait_all();
-            __syncwarp();
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == kTcMmaWarp) {
-        tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kT2Tiles * kT3N)
-                     : "memory");
-    }
-}
-
 // ---------------------------------------------------------------- host side
 // (shared with the tcgen05 attention's tensor maps)
 
@@ -1236,9 +926,7 @@ bool dense_map(CUtensorMap* map, const __half* w, int K, int N, int box_rows) {
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// an f32 output [T][ldy] as a TMA tensor map of its first N columns: 32 x 32
-// boxes in the 128-byte swizzle (what the dense kernels' epilogue stages);
-// false where the rows are not 16-byte multiples or the base not 16-aligned
+// an f32 output [T][ldy] as a TMA tensor map of its first N columns
 bool out_map(CUtensorMap* map, float* y, int ldy, int N, int T) {
     if (!y || ldy % 4 || (reinterpret_cast<uintptr_t>(y) & 15)) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)T};
@@ -1248,82 +936,6 @@ bool out_map(CUtensorMap* map, float* y, int ldy, int N, int T) {
     return encode_fn()(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, y, dims, strides, box, estr,
                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-int q4_tc_dense(const __half* hi, const __half* lo, int N, int K, QAct x, const __half* x16, int T, float* y, int ldy,
-                bool accumulate, int num_sms, int* err_flag, cudaStream_t st) {
-    if (T <= 0 || N <= 0) return 0;
-    if (encode_fn() == nullptr || K % kTcKB || N % 64 || ldy % 4 || (reinterpret_cast<uintptr_t>(y) & 15) ||
-        (reinterpret_cast<uintptr_t>(x16) & 15) || (reinterpret_cast<uintptr_t>(hi) & 15) ||
-        (reinterpret_cast<uintptr_t>(lo) & 15))
-        return (int)cudaErrorInvalidValue;
-    CUtensorMap xm, hm, lm, ym;
-    if (!act_map(&xm, x16, K, T, kT2Tiles * kTcM) || !dense_map(&hm, hi, K, N, kT3N) ||
-        !dense_map(&lm, lo, K, N, kT3N) || !out_map(&ym, y, ldy, N, T))
-        return (int)cudaErrorInvalidValue;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(dense_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)T3Shape<false>::kSmem);
-        if (e != cudaSuccess) return (int)e;
-        attr = true;
-    }
-    const int ksteps = K / kTcKB;
-    const int mt = (T + kT2Tiles * kTcM - 1) / (kT2Tiles * kTcM), ntl = (N + kT3N - 1) / kT3N;
-    // K slices: at most kT2MaxKb k-blocks each; of those, the count whose
-    // waves of CTAs (one an SM) times a CTA's k-blocks, plus about two
-    // k-blocks' worth of epilogue (its reductions into y), is least
-    const int s_min = (ksteps + kT2MaxKb - 1) / kT2MaxKb;
-    int splits = s_min, kps = (ksteps + s_min - 1) / s_min;
-    int64_t best = INT64_MAX;
-    for (int sp = s_min; sp <= std::min(ksteps, 8 * s_min); ++sp) {
-        const int k = (ksteps + sp - 1) / sp, real = (ksteps + k - 1) / k;
-        const int64_t waves = ((int64_t)mt * ntl * real + num_sms - 1) / num_sms;
-        const int64_t cost = waves * (k + 2);
-        if (cost < best) {
-            best = cost;
-            splits = real;
-            kps = k;
-        }
-    }
-    if (splits > 1 && !accumulate) {
-        cudaError_t e = cudaMemset2DAsync(y, (size_t)ldy * sizeof(float), 0, (size_t)N * sizeof(float), T, st);
-        if (e != cudaSuccess) return (int)e;
-    }
-    Q4Layout L{0, ksteps, 1};
-    TcArgs args{nullptr, L, 0, N, x.scale, T, y, ldy, accumulate ? 1 : 0, kps, nullptr, nullptr, err_flag};
-    args.y_tma = 1;
-    return (int)launch(dense_tc_kernel<false>, dim3(mt, ntl, splits), dim3(kTcThreads), T3Shape<false>::kSmem, st, xm,
-                       hm, lm, ym, args);
-}
-
-int head_tc_dense(const __half* w16, const int* w_norm2, const float* row_scale, int V, int K, QAct x,
-                  const __half* x16, const int* x_norm2, int T, float* logits, int ldl, unsigned long long* keys,
-                  unsigned long long bound, unsigned long long w_norm2_max, int* err_flag, cudaStream_t st) {
-    if (T <= 0 || V <= 0) return 0;
-    if (encode_fn() == nullptr || K % kTcKB || (reinterpret_cast<uintptr_t>(x16) & 15) ||
-        (reinterpret_cast<uintptr_t>(w16) & 15) || !w_norm2 || !x_norm2)
-        return (int)cudaErrorInvalidValue;
-    CUtensorMap xm, wm, ym;
-    if (!act_map(&xm, x16, K, T, kT2Tiles * kTcM) || !dense_map(&wm, w16, K, V, kT3N))
-        return (int)cudaErrorInvalidValue;
-    // the logits through the output map where their rows allow one, else plain stores
-    const bool y_tma = out_map(&ym, logits, ldl, V, T);
-    if (!y_tma) memset(&ym, 0, sizeof(ym));
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(dense_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)T3Shape<true>::kSmem);
-        if (e != cudaSuccess) return (int)e;
-        attr = true;
-    }
-    const int mt = (T + kT2Tiles * kTcM - 1) / (kT2Tiles * kTcM), ntl = (V + kT3N - 1) / kT3N;
-    Q4Layout L{0, K / kTcKB, 1};
-    TcArgs args{nullptr, L,        0,       V,   x.scale, T,   logits, ldl, 0, K / kTcKB, row_scale,
-                keys,    err_flag, x_norm2, w_norm2, x16,     w16, K,      bound,  w_norm2_max};
-    args.y_tma = y_tma ? 1 : 0;
-    return (int)launch(dense_tc_kernel<true>, dim3(mt, ntl, 1), dim3(kTcThreads), T3Shape<true>::kSmem, st, xm, wm, wm,
-                       ym, args);
 }
 
 }  // namespace dflash

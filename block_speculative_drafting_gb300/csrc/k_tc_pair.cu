@@ -88,7 +88,8 @@ static_assert(sizeof(PCtl) <= 1024, "control block");
 
 struct PairArgs {
     int T, N, K;
-    int mt, ntl, splits, kps;  // units: mt x ntl x splits, 256-row tiles fastest; k-blocks of a unit
+    int mt, ntl, splits, kps;  // units: 256-row tiles x output tiles x K slices; k-blocks of a unit
+    int slices_inner;          // unit order: row tile, K slice, output tile (else row tile, output tile, K slice)
     const float* xscale;       // [T]
     int reduce;                // add into y (accumulate, or K split over units)
     int y_tma;                 // y through the output map; else plain stores (a head with odd rows)
@@ -187,11 +188,16 @@ __device__ __noinline__ int exact_dot_codes(const __half* __restrict__ x, const 
 // The sequence of k-blocks a pair runs: its units in order, each unit's k-blocks.
 struct PairWalk {
     int u, i, mi, ni, kb0, nkb;
+    // row tiles fastest; then, with few row tiles, the K slices of an output
+    // tile (their partial sums meet in y while its lines are still in L2) and
+    // the output tiles, or, with many, the output tiles and the K slices (the
+    // pairs at work share the activations of one K slice)
     DF_DEV void decode(const PairArgs& a) {
         mi = u % a.mt;
         const int r = u / a.mt;
-        ni = r % a.ntl;
-        kb0 = (r / a.ntl) * a.kps;
+        const int si = a.slices_inner ? r % a.splits : r / a.ntl;
+        ni = a.slices_inner ? r / a.splits : r % a.ntl;
+        kb0 = si * a.kps;
         nkb = min(a.K / kPKB, kb0 + a.kps) - kb0;
     }
     DF_DEV void start(int pair, const PairArgs& a) {
@@ -496,7 +502,7 @@ static cudaError_t pair_setup(int* max_pairs) {
     return cudaSuccess;
 }
 
-int q4_tc_pair(const __half* hi, const __half* lo, int N, int K, QAct x, const __half* x16, int T, float* y, int ldy,
+int q4_tc_dense(const __half* hi, const __half* lo, int N, int K, QAct x, const __half* x16, int T, float* y, int ldy,
                bool accumulate, int* err_flag, cudaStream_t st) {
     if (T <= 0 || N <= 0) return 0;
     if (encode_fn() == nullptr || K % kPKB || N % 64 || ldy % 4 || (reinterpret_cast<uintptr_t>(y) & 15) ||
@@ -541,6 +547,7 @@ int q4_tc_pair(const __half* hi, const __half* lo, int N, int K, QAct x, const _
     args.kps = kps;
     args.xscale = x.scale;
     args.reduce = (accumulate || splits > 1) ? 1 : 0;
+    args.slices_inner = mt < 8 ? 1 : 0;
     args.y_tma = 1;
     args.y = y;
     args.ldy = ldy;
@@ -551,7 +558,7 @@ int q4_tc_pair(const __half* hi, const __half* lo, int N, int K, QAct x, const _
                                hm, lm, ym, args);
 }
 
-int head_tc_pair(const __half* w16, const int* w_norm2, const float* row_scale, int V, int K, QAct x,
+int head_tc_dense(const __half* w16, const int* w_norm2, const float* row_scale, int V, int K, QAct x,
                  const __half* x16, const int* x_norm2, int T, float* logits, int ldl, unsigned long long* keys,
                  unsigned long long bound, unsigned long long w_norm2_max, int* err_flag, cudaStream_t st) {
     if (T <= 0 || V <= 0) return 0;

@@ -80,12 +80,16 @@ bool head_tc_supported(int ksteps, QAct x);
 int head_tc(const int8_t* packed, const float* row_scale, int V, int ksteps, QAct x, const __half* x16, int T,
             float* logits, int ldl, unsigned long long* keys, int* err_flag, cudaStream_t st);
 // Dense f16 weight copies for the many-row path (k_tc.cu): hi = f16(s q),
-// lo = f16(s q - hi) [N][K] from a 4-bit matrix's codes and f16 scales; the
-// 4-bit matmul and the head on those copies (every operand tile by TMA, no
-// conversion in the kernel).
+// lo = f16(s q - hi) [N][K] from a 4-bit matrix's codes and f16 scales.
 int dequant_hilo(const int8_t* codes, const uint16_t* scales, int N, int K, __half* hi, __half* lo, cudaStream_t st);
+// The 4-bit matmul and the head on those copies (k_tc_pair.cu): every operand
+// tile by TMA, no conversion in the kernel; 256-row x 256-output units on
+// pairs of SMs (tcgen05.mma cta_group::2), a persistent grid of at most one
+// pair per two SMs with two accumulators in tensor memory, so the epilogue of
+// one unit overlaps the MMAs of the next.  y as q4_tc (cleared first where K
+// is split over units and accumulate is off).
 int q4_tc_dense(const __half* hi, const __half* lo, int N, int K, QAct x, const __half* x16, int T, float* y, int ldy,
-                bool accumulate, int num_sms, int* err_flag, cudaStream_t st);
+                bool accumulate, int* err_flag, cudaStream_t st);
 // The head takes the squared code norms of its vocabulary rows (w_norm2 [V],
 // largest w_norm2_max) and of the activation rows (x_norm2 [T]): an element
 // whose norm product passes `bound` (2^48: a partial sum could leave the
@@ -94,16 +98,6 @@ int q4_tc_dense(const __half* hi, const __half* lo, int N, int K, QAct x, const 
 int head_tc_dense(const __half* w16, const int* w_norm2, const float* row_scale, int V, int K, QAct x,
                   const __half* x16, const int* x_norm2, int T, float* logits, int ldl, unsigned long long* keys,
                   unsigned long long bound, unsigned long long w_norm2_max, int* err_flag, cudaStream_t st);
-// The same two products on pairs of SMs (k_tc_pair.cu): 256-row x 256-output
-// units, tcgen05.mma cta_group::2, a persistent grid of one pair per two SMs
-// with two accumulators in tensor memory (the epilogue of one unit overlaps
-// the MMAs of the next).  Same arguments and results as q4_tc_dense /
-// head_tc_dense.
-int q4_tc_pair(const __half* hi, const __half* lo, int N, int K, QAct x, const __half* x16, int T, float* y, int ldy,
-               bool accumulate, int* err_flag, cudaStream_t st);
-int head_tc_pair(const __half* w16, const int* w_norm2, const float* row_scale, int V, int K, QAct x,
-                 const __half* x16, const int* x_norm2, int T, float* logits, int ldl, unsigned long long* keys,
-                 unsigned long long bound, unsigned long long w_norm2_max, int* err_flag, cudaStream_t st);
 // int8 activation codes [T][ld] -> f16 [T][K] (exact), for the tcgen05 kernels'
 // TMA; with norm2 non-null also each row's squared code norm (K < 2^17).
 int codes_to_f16(const int8_t* x, int ld, int T, int K, __half* out, int* norm2, int num_sms, cudaStream_t st);
