@@ -539,6 +539,38 @@ __global__ void __launch_bounds__(kRowThreads) silu_mul_reg_kernel(const float* 
     if (threadIdx.x == 0) out_scale[r] = sx;
 }
 
+// Many rows (a batch, a prefill): 512 threads a row and the row's products
+// staged in shared memory instead of registers, so that four rows share an SM
+// and a launch of a few hundred rows runs in one wave.  Same arithmetic as
+// silu_mul_reg_kernel.
+constexpr int kSiluSmemThreads = 512;
+__global__ void __launch_bounds__(kSiluSmemThreads, 4)
+    silu_mul_smem_kernel(const float* __restrict__ gu, int ld_gu, int I, int8_t* __restrict__ out_codes,
+                         float* __restrict__ out_scale, int ld_codes, __half* __restrict__ out16) {
+    extern __shared__ float4 arow[];
+    __shared__ float red[33];
+    pdl_trigger();
+    pdl_wait();
+    const int r = blockIdx.x;
+    const float4* g4 = reinterpret_cast<const float4*>(gu + (int64_t)r * ld_gu);
+    const float4* u4 = reinterpret_cast<const float4*>(gu + (int64_t)r * ld_gu + I);
+    const int n4 = I / 4;
+    float amax = 0.f;
+#pragma unroll 2
+    for (int c = threadIdx.x; c < n4; c += kSiluSmemThreads) {
+        const float4 g = g4[c], u = u4[c];
+        const float4 a = make_float4(silu_f(g.x) * u.x, silu_f(g.y) * u.y, silu_f(g.z) * u.z, silu_f(g.w) * u.w);
+        arow[c] = a;
+        amax = fmaxf(amax, amax4(a));
+    }
+    amax = row_reduce_nt<true, kSiluSmemThreads>(amax, red);  // (its barriers also publish arow)
+    const float sx = __fdiv_rn(amax, 127.0f);
+    uint32_t* q4 = reinterpret_cast<uint32_t*>(out_codes + (int64_t)r * ld_codes);
+    for (int c = threadIdx.x; c < n4; c += kSiluSmemThreads)
+        put_codes4(q4, out16 ? out16 + (int64_t)r * I : nullptr, c, codes4(arow[c], sx));
+    if (threadIdx.x == 0) out_scale[r] = sx;
+}
+
 // The same with a row split over the kSiluSplit CTAs of a cluster (one float4
 // of the row per thread): each CTA reduces its share's max|a|, the cluster
 // takes the row's max through distributed shared memory.
@@ -590,6 +622,19 @@ int silu_mul(const float* gu, int ld_gu, int rows, int I, float* out_f32, int ld
         (reinterpret_cast<uintptr_t>(gu + I) % 16) == 0)
         return (int)launch_cluster(silu_mul_cluster_kernel, dim3(kSiluSplit, rows), dim3(kRowThreads), 0, st,
                                    kSiluSplit, gu, ld_gu, I, out_f32, ld_out, out_codes, out_scale, ld_codes, out16);
+    if (rows >= kManyRows && out_codes && !out_f32 && rows_fit_reg(I, gu, ld_gu, nullptr, 0, out_codes, ld_codes, 16384) &&
+        (reinterpret_cast<uintptr_t>(gu + I) % 16) == 0) {
+        const size_t smem = (size_t)I * sizeof(float);
+        static size_t smem_set = 0;
+        if (smem > smem_set) {
+            cudaError_t e = cudaFuncSetAttribute(silu_mul_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)smem);
+            if (e != cudaSuccess) return (int)e;
+            smem_set = smem;
+        }
+        return (int)launch(silu_mul_smem_kernel, dim3(rows), dim3(kSiluSmemThreads), smem, st, gu, ld_gu, I, out_codes,
+                           out_scale, ld_codes, out16);
+    }
     if (rows_fit_reg(I, gu, ld_gu, out_f32, ld_out, out_codes, ld_codes, 4 * 4 * kRowThreads) &&
         (reinterpret_cast<uintptr_t>(gu + I) % 16) == 0) {
         const int nv = (I + 4 * kRowThreads - 1) / (4 * kRowThreads);
