@@ -125,6 +125,10 @@ WORKLOADS = {
     "qwen3_8b_prefill8192": Workload("qwen3_8b_prefill8192", Geometry(**QWEN3_8B_DRAFT), ctx=0, prefill=8192),
     # the same kernels on 1024 rows: the small case for profiler captures
     "qwen3_8b_prefill1024": Workload("qwen3_8b_prefill1024", Geometry(**QWEN3_8B_DRAFT), ctx=0, prefill=1024),
+    # the batched block's matmul and head shapes (32 blocks of 16 rows) with one
+    # layer and a 64-row context: a few GB on the device, for profiler captures
+    "qwen3_8b_l1_batch32_ctx64": Workload("qwen3_8b_l1_batch32_ctx64", Geometry(**dict(QWEN3_8B_DRAFT, layers=1)),
+                                          ctx=64, n_seqs=32),
     # small quantised shapes the oracle finishes in seconds: several tiles and
     # ragged tails (vocab and context not multiples of any tile)
     "small_q4": Workload("small_q4", Geometry(hidden=512, intermediate=1536, layers=2, heads=8, kv_heads=2,
