@@ -57,10 +57,12 @@ struct AtShape {
     static constexpr int kQ = kAtM * HD * 2;       // one plane of Q: KB blocks of 128 rows x 128 B
     static constexpr int kKV = kAtKeys * HD * 2;   // one plane of a K or V tile: KB blocks of 64 rows x 128 B
     static constexpr int kStage = 4 * kKV;         // kh, kl, vh, vl
-    static constexpr int kP = kAtM * kAtKeys * 2;  // one plane of P: 128 rows x 128 B
-    static constexpr size_t kSmem = 1024 /*alignment*/ + 2048 /*control*/ + 2 * (size_t)kQ + 2 * (size_t)kStage +
-                                    2 * (size_t)kP;
-    static constexpr int kCols = 256;  // tensor memory: S at columns 0 and 64, O at 128
+    static constexpr size_t kSmem = 1024 /*alignment*/ + 2048 /*control*/ + 2 * (size_t)kQ + 2 * (size_t)kStage;
+    // tensor memory: S at columns 0 and 64, O at 128, the A operands of the
+    // two products -- Q (hi, lo) and P (hi, lo), two f16 a column -- after it
+    static constexpr int kCols = 512;
+    static constexpr int kColQ = 256, kColQl = kColQ + HD / 2, kColP = 384, kColPl = kColP + kAtKeys / 2;
+    static_assert(kColQl + HD / 2 <= kColP && kColPl + kAtKeys / 2 <= kCols, "tensor memory");
     static_assert(kSmem <= 227 * 1024, "shared memory");
 };
 
@@ -95,6 +97,14 @@ DF_DEV void at_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t 
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
         "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// the same with the A operand in tensor memory (lane = row, two f16 a column)
+DF_DEV void at_mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 DF_DEV void at_commit(uint64_t* bar) {
@@ -177,8 +187,6 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     unsigned char* qh = sm + kAtCtl;
     unsigned char* ql = qh + S::kQ;
     unsigned char* stage0 = ql + S::kQ;
-    unsigned char* ph = stage0 + 2 * S::kStage;
-    unsigned char* pl = ph + S::kP;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int sp = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
     const int rep = nq / nkv, mq = rep * block_len;
@@ -315,8 +323,6 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             constexpr uint32_t idS = at_idesc(kAtM, kAtKeys, false), idO = at_idesc(kAtM, HD, true);
             // descriptors: built once; an operand's k16 slice is its base plus
             // the slice's byte offset / 16 (the start field never carries)
-            const uint64_t dqh = at_desc(smem_addr(qh), 16), dql = at_desc(smem_addr(ql), 16);
-            const uint64_t dph = at_desc(smem_addr(ph), 16), dpl = at_desc(smem_addr(pl), 16);
             const uint64_t dk0 = at_desc(smem_addr(stage0), 16);
             const uint64_t dv0 = at_desc(smem_addr(stage0) + 2 * S::kKV, kAtKeys * 128);
             constexpr uint64_t kStageD = S::kStage >> 4, kPlaneD = S::kKV >> 4;
@@ -329,11 +335,12 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                 const uint32_t d = tmem + (uint32_t)((u & 1) * kAtKeys);
 #pragma unroll
                 for (int j = 0; j < HD / 16; ++j) {
-                    const uint64_t qo = (uint64_t)(((j >> 2) * (kAtM * 128) + (j & 3) * 32) >> 4);
+                    // Q's k16 slice j: columns 8 j .. of its planes in tensor memory
+                    const uint32_t qh_t = tmem + (uint32_t)(S::kColQ + 8 * j), ql_t = tmem + (uint32_t)(S::kColQl + 8 * j);
                     const uint64_t ko = (uint64_t)(((j >> 2) * (kAtKeys * 128) + (j & 3) * 32) >> 4);
-                    at_mma(d, dqh + qo, kh + ko, idS, j > 0 ? 1u : 0u);
-                    at_mma(d, dqh + qo, kl + ko, idS, 1u);
-                    at_mma(d, dql + qo, kh + ko, idS, 1u);
+                    at_mma_ts(d, qh_t, kh + ko, idS, j > 0 ? 1u : 0u);
+                    at_mma_ts(d, qh_t, kl + ko, idS, 1u);
+                    at_mma_ts(d, ql_t, kh + ko, idS, 1u);
                 }
                 at_commit(&ctl.s_full[u & 1]);
                 at_commit(&ctl.k_empty[u & 1]);
@@ -350,11 +357,13 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                 const uint64_t vh = dv0 + (u & 1) * kStageD, vl = vh + kPlaneD;
 #pragma unroll
                 for (int j = 0; j < kAtKeys / 16; ++j) {
-                    const uint64_t po = (uint64_t)((j * 32) >> 4), vo = (uint64_t)((j * 2048) >> 4);
+                    // P's k16 slice j (keys 16 j ..): columns 8 j .. of its planes
+                    const uint32_t ph_t = tmem + (uint32_t)(S::kColP + 8 * j), pl_t = tmem + (uint32_t)(S::kColPl + 8 * j);
+                    const uint64_t vo = (uint64_t)((j * 2048) >> 4);
                     const uint32_t dO = tmem + 128;
-                    at_mma(dO, dph + po, vh + vo, idO, (u > 0 || j > 0) ? 1u : 0u);
-                    at_mma(dO, dph + po, vl + vo, idO, 1u);
-                    at_mma(dO, dpl + po, vh + vo, idO, 1u);
+                    at_mma_ts(dO, ph_t, vh + vo, idO, (u > 0 || j > 0) ? 1u : 0u);
+                    at_mma_ts(dO, ph_t, vl + vo, idO, 1u);
+                    at_mma_ts(dO, pl_t, vh + vo, idO, 1u);
                 }
                 at_commit(&ctl.v_empty[u & 1]);
                 at_commit(&ctl.p_empty);
@@ -398,7 +407,34 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                     split_store4(qv[e], reinterpret_cast<__half*>(qh + off), reinterpret_cast<__half*>(ql + off));
                 }
             }
-            fence_proxy_async_smem();
+            // Q to tensor memory, the scores' A operand (read there by every
+            // step's MMAs instead of from shared memory): thread (row tq,
+            // half hq) moves dims [hq HD/2, (hq + 1) HD/2) of its row, 8 dims
+            // a 16-byte chunk, 4 columns a chunk
+            asm volatile("bar.sync 1, %0;" ::"r"(kAtSoft) : "memory");  // every row written
+            const int tq = (warp & 3) * 32 + lane, hq = warp >> 2;
+            const uint32_t qlane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+#pragma unroll
+            for (int pl2 = 0; pl2 < 2; ++pl2) {
+                const unsigned char* src = pl2 ? ql : qh;
+#pragma unroll
+                for (int c4 = 0; c4 < HD / 64; ++c4) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int cq = hq * (HD / 16) + c4 * 4 + k;  // the row's 16-byte chunk
+                        const uint4 x = *reinterpret_cast<const uint4*>(src + (cq >> 3) * (kAtM * 128) + at_swz(tq, cq & 7));
+                        w[4 * k] = x.x;
+                        w[4 * k + 1] = x.y;
+                        w[4 * k + 2] = x.z;
+                        w[4 * k + 3] = x.w;
+                    }
+                    at_st16(qlane + (uint32_t)((pl2 ? S::kColQl : S::kColQ) + hq * (HD / 4) + c4 * 16),
+                            *reinterpret_cast<const float(*)[16]>(w));
+                }
+            }
+            at_wait_st();
+            at_fence_before();
             mbar_arrive(&ctl.q_ready);
         }
         // thread: query row t (tensor-memory lane t), key half h of each step
@@ -473,7 +509,9 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             }
             l *= f;
             m_ref = m_new;
-            // P of the row's key half: (hi, lo) f16 pairs, 8 keys a 16-byte chunk
+            // P of the row's key half: (hi, lo) f16 pairs, two keys a
+            // tensor-memory column (the A operand of O += P V)
+            uint32_t phw[KH / 2], plw[KH / 2];
 #pragma unroll
             for (int c8 = 0; c8 < KH / 8; ++c8) {
                 float p[8];
@@ -492,11 +530,16 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                     hw[i] = *reinterpret_cast<const uint32_t*>(&hh);
                     lw[i] = *reinterpret_cast<const uint32_t*>(&ll);
                 }
-                const uint32_t off = at_swz(t, h * (KH / 8) + c8);
-                *reinterpret_cast<uint4*>(ph + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4*>(pl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    phw[c8 * 4 + i] = hw[i];
+                    plw[c8 * 4 + i] = lw[i];
+                }
             }
-            fence_proxy_async_smem();
+            static_assert(KH / 2 == 16, "a key half is one 16-column store a plane");
+            at_st16(lane_addr + (uint32_t)(S::kColP + h * (KH / 2)), *reinterpret_cast<const float(*)[16]>(phw));
+            at_st16(lane_addr + (uint32_t)(S::kColPl + h * (KH / 2)), *reinterpret_cast<const float(*)[16]>(plw));
+            at_wait_st();
             at_fence_before();
             mbar_arrive(&ctl.p_full);
         }
