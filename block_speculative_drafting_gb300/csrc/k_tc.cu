@@ -1,41 +1,44 @@
 // Dense contractions of many rows on the fifth-generation tensor cores
-// (tcgen05): the 4-bit g32 matrices of page "cortiq-engine 0.8.75 —
-// src/gpu_wgpu/dflash_dev.rs" (`Dev::q4`: four-bit codes with one scale per
-// 32 columns against int8 activations) and the int8 head (`Dev::q8`, the
-// head of page "cortiq-engine 0.8.71 — src/dflash.rs", `block_dev`) applied
-// to a batch of rows: the prefill of many context rows
-// (`Drafter::settle_rows`) and the blocks of many sequences at once.
+// (tcgen05) with the weights converted in the kernel: the 4-bit g32 matrices
+// of page "cortiq-engine 0.8.75 — src/gpu_wgpu/dflash_dev.rs" (`Dev::q4`:
+// four-bit codes with one scale per 32 columns against int8 activations) and
+// the int8 head (`Dev::q8`, the head of page "cortiq-engine 0.8.71 —
+// src/dflash.rs", `block_dev`) applied to a batch of rows.  The library runs
+// the products from dense f16 weight copies (k_tc_pair.cu); these kernels
+// are the form without the copies (the model option "dense" at 0), and this
+// file also holds the host side the tensor-core kernels share: tensor maps,
+// the f16 activation codes, the dense copies' conversion.
 //
-// 4-bit: y[t][n] = xs[t] * sum_k (s[n][k/32] q[n][k]) x[t][k], the quantised
-// matvec with the group scale folded into the weight.  s (f16) times q
-// (-8..7) needs up to 14 significant bits, so the weight goes to the tensor
-// core as the exact sum of two f16 values, hi = f16(s q) and
+// 4-bit (q4_tc2_kernel): y[t][n] = xs[t] * sum_k (s[n][k/32] q[n][k]) x[t][k],
+// the quantised matvec with the group scale folded into the weight.  s (f16)
+// times q (-8..7) needs up to 14 significant bits, so the weight goes to the
+// tensor core as the exact sum of two f16 values, hi = f16(s q) and
 // lo = f16(s q - hi) (an fma; the remainder is representable), and every k
 // slice runs two MMAs (x . hi + x . lo).  The int8 codes of x are exact in
 // f16, so every product is exact.
-// Head: logits[t][n] = xs[t] * sw[n] * sum_k q[n][k] x[t][k], one MMA a k
-// slice on exact f16 integers, and the draft token's argmax (lowest index
-// among equal values) folded into the epilogue.
+// Head (tc_head_kernel): logits[t][n] = xs[t] * sw[n] * sum_k q[n][k] x[t][k],
+// one MMA a k slice on exact f16 integers, and the draft token's argmax
+// (lowest index among equal values) folded into the epilogue.
 //
 // Accumulation.  The tensor core's f32 accumulation truncates, which over
-// long K shrinks sums measurably; so tensor memory only ever holds a chunk of
-// kTcChunk k-blocks (512 columns), in two alternating accumulators, and the
-// converter warps drain each finished chunk into registers: round-to-nearest
-// f32 adds for the 4-bit matrices, exact int32 adds for the head (a chunk's
-// integer sum is below 512 * 127 * 127 < 2^24, so the f32 chunk value is the
-// exact integer).
+// long K shrinks sums measurably; so the head's tensor memory only ever holds
+// a chunk of kTcChunk k-blocks (512 columns), in two alternating
+// accumulators, and the converter warps drain each finished chunk into exact
+// int32 registers (a chunk's integer sum is below 512 * 127 * 127 < 2^24, so
+// the f32 chunk value is the exact integer).  The 4-bit kernel splits K over
+// CTAs in slices of at most 2048 columns instead.
 //
-// One CTA computes a 128-row x 128-output tile, D[t][n], in tensor memory
-// (128 lanes x 128 f32 columns per accumulator).  Roles:
+// The head's CTA computes a 128-row x 128-output tile, D[t][n], in tensor
+// memory (128 lanes x 128 f32 columns per accumulator).  Roles:
 //   warp 8 (one lane): TMA -- the f16 activation tile of each 64-column
 //     k-block (cp.async.bulk.tensor over a tensor map of the activation
 //     codes as f16, 128-byte swizzle: it lands in the layout the MMA reads)
-//     into the activation ring, and the packed weights of the k-block's two
+//     into the activation ring, and the packed codes of the k-block's two
 //     64-row groups (cp.async.bulk) into the raw ring;
-//   warps 0-7: convert a raw stage into a converted stage (weights to f16,
-//     or to the hi and lo f16 tiles) in the K-major 128-byte-swizzled layout
-//     the MMA descriptors name; drain finished chunks; run the epilogue
-//     (warp w reads tensor-memory lanes 32 (w % 4) .., columns 64 (w / 4) ..);
+//   warps 0-7: convert a raw stage into a converted stage (the codes as f16)
+//     in the K-major 128-byte-swizzled layout the MMA descriptors name; drain
+//     finished chunks; run the epilogue (warp w reads tensor-memory lanes
+//     32 (w % 4) .., columns 64 (w / 4) ..);
 //   warp 9: allocates the tensor memory; one lane issues the MMAs
 //     (tcgen05.mma kind::f16, M 128, N 128, K 16) and commits every converted
 //     stage and every finished chunk.
@@ -72,12 +75,11 @@ constexpr int kTcA = kTcM * kTcKB * 2;  // f16 activation tile (swizzled by the 
 // Raw stages are compact (packed weights), so the ring is deep: enough bytes
 // in flight to cover the load latency at the tensor cores' pace; converted
 // stages (f16) are double-buffered.
-template <bool kHead>
 struct TcShape {
-    static constexpr int kRawBytes = kHead ? 2 * kI8Super : 2 * 4 * kQ4Chunk;  // two 64-row groups of one k-block
-    static constexpr int kB = kTcN * kTcKB * 2;                                 // f16 weight tile, swizzled
-    static constexpr int kCvtBytes = (kHead ? 1 : 2) * kB;
-    static constexpr int kRaw = kHead ? 8 : 10;                                 // raw stages
+    static constexpr int kRawBytes = 2 * kI8Super;  // two 64-row groups of one k-block
+    static constexpr int kB = kTcN * kTcKB * 2;     // f16 weight tile, swizzled
+    static constexpr int kCvtBytes = kB;
+    static constexpr int kRaw = 8;                  // raw stages
     static constexpr size_t kSmem = 1024 /*alignment slack*/ + 1024 /*control*/ + (size_t)kTcAct * kTcA +
                                     (size_t)kTcCvt * kCvtBytes + (size_t)kRaw * kRawBytes;
     static_assert(kCvtBytes % 1024 == 0 && kRawBytes % 128 == 0, "stage alignment");
@@ -158,9 +160,8 @@ struct TcArgs {
     int y_tma;                   // dense kernels: y is written through the output tensor map
 };
 
-template <bool kHead>
-__global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_constant__ CUtensorMap xmap, TcArgs a) {
-    using S = TcShape<kHead>;
+__global__ void __launch_bounds__(kTcThreads, 1) tc_head_kernel(const __grid_constant__ CUtensorMap xmap, TcArgs a) {
+    using S = TcShape;
     extern __shared__ __align__(1024) unsigned char sm_raw[];
     // 1024-aligned base (the swizzled tiles need it)
     unsigned char* sm = sm_raw + ((1024 - (smem_addr(sm_raw) & 1023)) & 1023);
@@ -169,12 +170,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     unsigned char* cvt = act + kTcAct * kTcA;
     unsigned char* raw = cvt + kTcCvt * S::kCvtBytes;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // tile order: the 4-bit matmuls run the output tiles of one row tile
-    // together (x = output tile), so that its activations are read from HBM
-    // once and reused from L2 (the packed weights fit in L2); the head runs
-    // the row tiles of one output tile together (x = row tile): its weights
-    // are the large operand
-    const int m0 = (kHead ? blockIdx.x : blockIdx.y) * kTcM, nt = kHead ? blockIdx.y : blockIdx.x;
+    // the row tiles of one output tile run together (x = row tile): the
+    // weights are the large operand
+    const int m0 = blockIdx.x * kTcM, nt = blockIdx.y;
     const int ksteps = a.L.ksteps;
     const int kb_lo = blockIdx.z * a.kb_per_split, kb_hi = min(ksteps, kb_lo + a.kb_per_split);
     const int nkb = kb_hi - kb_lo;
@@ -228,7 +226,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
             int issued = 0;
             int ng = 0;  // valid 64-row groups of this tile
             for (int gg = 0; gg < kTcN / 64; ++gg) ng += (nt * (kTcN / 64) + gg < ngroups_n) ? 1 : 0;
-            const int wbytes = kHead ? kI8Super : 4 * kQ4Chunk;
+            const int wbytes = kI8Super;
             for (int i = 0; i < nkb; ++i) {
                 const int r = i % kTcRaw, sa = i % kTcAct;
                 bool ok = true;
@@ -244,8 +242,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
                 mbar_arrive_expect_tx(&ctl.raw_full[r], (uint32_t)(ng * wbytes));
                 for (int gg = 0; gg < ng; ++gg) {
                     const int grp = nt * (kTcN / 64) + gg;
-                    const uint8_t* src = kHead ? a.w + ((int64_t)grp * ksteps + kb) * kI8Super
-                                               : a.w + q4_chunk_offset(a.L, 4 * (a.g0 + grp), kb);
+                    const uint8_t* src = a.w + ((int64_t)grp * ksteps + kb) * kI8Super;
                     bulk_g2s(dst + gg * wbytes, src, (uint32_t)wbytes, &ctl.raw_full[r]);
                 }
                 issued = i + 1;
@@ -275,7 +272,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
 #pragma unroll
                 for (int j = 0; j < kTcKB / 16; ++j) {
                     tc_mma(d, tc_desc_sw128(sa + 32 * j), tc_desc_sw128(sb + 32 * j), (first && j == 0) ? 0u : 1u);
-                    if (!kHead) tc_mma(d, tc_desc_sw128(sa + 32 * j), tc_desc_sw128(sb + S::kB + 32 * j), 1u);
                 }
                 tc_commit(&ctl.cvt_empty[st]);
                 tc_commit(&ctl.act_empty[sx]);
@@ -289,13 +285,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         // ---------------------------------------------------------------- converters
         const int sub = warp & 3, half = warp >> 2;  // tensor-memory lane quadrant, 64-column half
         const uint32_t lane_base = (uint32_t)(32 * sub) << 16;
-        float facc[kTcCols];
         int32_t iacc[kTcCols];
 #pragma unroll
-        for (int j = 0; j < kTcCols; ++j) {
-            facc[j] = 0.f;
-            iacc[j] = 0;
-        }
+        for (int j = 0; j < kTcCols; ++j) iacc[j] = 0;
         bool ok = true;
         int drained = 0;
         // add finished chunk `ch` (tensor-memory accumulator ch & 1) into the registers
@@ -315,12 +307,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
                 tc_ld16(base + (uint32_t)c, r);
                 tc_wait_ld();
 #pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    if (kHead)
-                        iacc[c + q] += (int32_t)__uint_as_float(r[q]);
-                    else
-                        facc[c + q] += __uint_as_float(r[q]);
-                }
+                for (int q = 0; q < 16; ++q) iacc[c + q] += (int32_t)__uint_as_float(r[q]);
             }
             tc_fence_before();
             __syncwarp();
@@ -352,59 +339,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
                 const int nl0 = gg * 64 + rr * 16 + gq, nl1 = nl0 + 8;
                 unsigned char* bt = cs;
                 const bool valid = nt * (kTcN / 64) + gg < ngroups_n;
-                if (kHead) {
-                    uint4 w[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
-                    if (valid) {
-                        const unsigned char* ch = rs + gg * kI8Super + rr * kI8Chunk + slot * 32;
-                        w[0] = *reinterpret_cast<const uint4*>(ch);
-                        w[1] = *reinterpret_cast<const uint4*>(ch + 16);
-                    }
+                uint4 w[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+                if (valid) {
+                    const unsigned char* ch = rs + gg * kI8Super + rr * kI8Chunk + slot * 32;
+                    w[0] = *reinterpret_cast<const uint4*>(ch);
+                    w[1] = *reinterpret_cast<const uint4*>(ch + 16);
+                }
 #pragma unroll
-                    for (int gi = 0; gi < 2; ++gi) {
-                        // words (s, up) of group half gi: four codes of row gq + 8 up at
-                        // columns 32 gi + 8 tq + 4 s + 0..3
-                        uint4 r0, r1;  // rows gq, gq + 8
-                        i8x4_to_half2x2(w[gi].x, r0.x, r0.y);
-                        i8x4_to_half2x2(w[gi].z, r0.z, r0.w);
-                        i8x4_to_half2x2(w[gi].y, r1.x, r1.y);
-                        i8x4_to_half2x2(w[gi].w, r1.z, r1.w);
-                        *reinterpret_cast<uint4*>(bt + tc_swz(nl0, 4 * gi + tq)) = r0;
-                        *reinterpret_cast<uint4*>(bt + tc_swz(nl1, 4 * gi + tq)) = r1;
-                    }
-                } else {
-                    unsigned char* blo = bt + S::kB;
-                    if (valid) {
-                        const unsigned char* ch = rs + gg * 4 * kQ4Chunk + rr * kQ4Chunk;
-                        const uint4 wv = *reinterpret_cast<const uint4*>(ch + slot * 16);
-                        const uint2 sv = *reinterpret_cast<const uint2*>(ch + 512 + gq * 8);
-                        const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-                        for (int gi = 0; gi < 2; ++gi) {
-                            uint32_t a0[4], a1[4];
-                            unpack_q4_word(wd[gi * 2 + 0], a0);  // columns 8 tq + 0..3
-                            unpack_q4_word(wd[gi * 2 + 1], a1);  // columns 8 tq + 4..7
-                            const uint32_t sw = gi ? sv.y : sv.x;  // (s[gq][g], s[gq+8][g])
-                            const uint32_t s0 = __byte_perm(sw, 0, 0x1010), s1 = __byte_perm(sw, 0, 0x3232);
-                            const uint32_t q0[4] = {a0[0], a0[2], a1[0], a1[2]};  // row gq
-                            const uint32_t q1[4] = {a0[1], a0[3], a1[1], a1[3]};  // row gq + 8
-                            uint4 hi, lo;
-                            split_scaled(q0, s0, hi, lo);
-                            *reinterpret_cast<uint4*>(bt + tc_swz(nl0, 4 * gi + tq)) = hi;
-                            *reinterpret_cast<uint4*>(blo + tc_swz(nl0, 4 * gi + tq)) = lo;
-                            split_scaled(q1, s1, hi, lo);
-                            *reinterpret_cast<uint4*>(bt + tc_swz(nl1, 4 * gi + tq)) = hi;
-                            *reinterpret_cast<uint4*>(blo + tc_swz(nl1, 4 * gi + tq)) = lo;
-                        }
-                    } else {
-                        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-                        for (int gi = 0; gi < 2; ++gi) {
-                            *reinterpret_cast<uint4*>(bt + tc_swz(nl0, 4 * gi + tq)) = z;
-                            *reinterpret_cast<uint4*>(blo + tc_swz(nl0, 4 * gi + tq)) = z;
-                            *reinterpret_cast<uint4*>(bt + tc_swz(nl1, 4 * gi + tq)) = z;
-                            *reinterpret_cast<uint4*>(blo + tc_swz(nl1, 4 * gi + tq)) = z;
-                        }
-                    }
+                for (int gi = 0; gi < 2; ++gi) {
+                    // words (s, up) of group half gi: four codes of row gq + 8 up at
+                    // columns 32 gi + 8 tq + 4 s + 0..3
+                    uint4 r0, r1;  // rows gq, gq + 8
+                    i8x4_to_half2x2(w[gi].x, r0.x, r0.y);
+                    i8x4_to_half2x2(w[gi].z, r0.z, r0.w);
+                    i8x4_to_half2x2(w[gi].y, r1.x, r1.y);
+                    i8x4_to_half2x2(w[gi].w, r1.z, r1.w);
+                    *reinterpret_cast<uint4*>(bt + tc_swz(nl0, 4 * gi + tq)) = r0;
+                    *reinterpret_cast<uint4*>(bt + tc_swz(nl1, 4 * gi + tq)) = r1;
                 }
             }
             // the converted tiles are read by the tensor cores (async proxy)
@@ -428,52 +379,37 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         if (ok) {
             const int t = m0 + 32 * sub + lane;
             const int n0 = nt * kTcN + half * kTcCols;
-            if (kHead) {
-                unsigned long long best = 0ull;
-                if (t < a.T) {
-                    const float xs = a.xscale[t];
-                    const bool vec = a.y != nullptr && (a.ldy & 3) == 0;
-#pragma unroll
-                    for (int q = 0; q < kTcCols / 4; ++q) {
-                        const int n = n0 + 4 * q;
-                        if (n >= a.N) break;
-                        float l[4];
-                        if (n + 4 <= a.N) {
-                            // the head's row scales are padded to whole 64-row groups
-                            const float4 sw = *reinterpret_cast<const float4*>(a.wscale + n);
-                            l[0] = xs * sw.x * (float)iacc[4 * q];
-                            l[1] = xs * sw.y * (float)iacc[4 * q + 1];
-                            l[2] = xs * sw.z * (float)iacc[4 * q + 2];
-                            l[3] = xs * sw.w * (float)iacc[4 * q + 3];
-                            if (vec)
-                                *reinterpret_cast<float4*>(a.y + (int64_t)t * a.ldy + n) = make_float4(l[0], l[1], l[2], l[3]);
-                            else if (a.y)
-                                for (int e = 0; e < 4; ++e) a.y[(int64_t)t * a.ldy + n + e] = l[e];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) best = max(best, argmax_key(l[e], (uint32_t)(n + e)));
-                        } else {
-                            for (int e = 0; e < 4 && n + e < a.N; ++e) {
-                                const float le = xs * a.wscale[n + e] * (float)iacc[4 * q + e];
-                                if (a.y) a.y[(int64_t)t * a.ldy + n + e] = le;
-                                best = max(best, argmax_key(le, (uint32_t)(n + e)));
-                            }
-                        }
-                    }
-                    if (best) atomicMax(a.keys + t, best);
-                }
-            } else if (t < a.T && n0 < a.N) {
+            unsigned long long best = 0ull;
+            if (t < a.T) {
                 const float xs = a.xscale[t];
-                float* dst = a.y + (int64_t)t * a.ldy + n0;
-                const bool red = a.accumulate != 0 || gridDim.z > 1;
+                const bool vec = a.y != nullptr && (a.ldy & 3) == 0;
 #pragma unroll
                 for (int q = 0; q < kTcCols / 4; ++q) {
-                    const float v0 = facc[4 * q] * xs, v1 = facc[4 * q + 1] * xs, v2 = facc[4 * q + 2] * xs,
-                                v3 = facc[4 * q + 3] * xs;
-                    if (red)
-                        red_add_v4(dst + 4 * q, v0, v1, v2, v3);
-                    else
-                        *reinterpret_cast<float4*>(dst + 4 * q) = make_float4(v0, v1, v2, v3);
+                    const int n = n0 + 4 * q;
+                    if (n >= a.N) break;
+                    float l[4];
+                    if (n + 4 <= a.N) {
+                        // the head's row scales are padded to whole 64-row groups
+                        const float4 sw = *reinterpret_cast<const float4*>(a.wscale + n);
+                        l[0] = xs * sw.x * (float)iacc[4 * q];
+                        l[1] = xs * sw.y * (float)iacc[4 * q + 1];
+                        l[2] = xs * sw.z * (float)iacc[4 * q + 2];
+                        l[3] = xs * sw.w * (float)iacc[4 * q + 3];
+                        if (vec)
+                            *reinterpret_cast<float4*>(a.y + (int64_t)t * a.ldy + n) = make_float4(l[0], l[1], l[2], l[3]);
+                        else if (a.y)
+                            for (int e = 0; e < 4; ++e) a.y[(int64_t)t * a.ldy + n + e] = l[e];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) best = max(best, argmax_key(l[e], (uint32_t)(n + e)));
+                    } else {
+                        for (int e = 0; e < 4 && n + e < a.N; ++e) {
+                            const float le = xs * a.wscale[n + e] * (float)iacc[4 * q + e];
+                            if (a.y) a.y[(int64_t)t * a.ldy + n + e] = le;
+                            best = max(best, argmax_key(le, (uint32_t)(n + e)));
+                        }
+                    }
                 }
+                if (best) atomicMax(a.keys + t, best);
             }
         }
     }
@@ -497,7 +433,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
 // in ten slices 1.4e-6, K = 4096 4.3e-7 (the chunk-draining kernel before
 // it: 1.6e-7, at 1.2 - 1.4x the time; 1024-column slices: 4.4e-7 at K =
 // 20480, at 1.15x the time of these).
-// Roles as tc_gemm_kernel: one TMA lane (the 256-row f16 activation box and
+// Roles as tc_head_kernel: one TMA lane (the 256-row f16 activation box and
 // the packed weights), eight converter warps (which also run the epilogue),
 // one MMA lane.
 constexpr int kT2Tiles = 2;               // 128-row tiles a CTA
@@ -518,7 +454,7 @@ struct T2Ctl {
 static_assert(sizeof(T2Ctl) <= 1024, "control block");
 
 // hi / lo f16 tiles of one 16-row chunk's lane slot (both 32-column groups),
-// the lane-slot permutation of tc_gemm_kernel (conflict-free stores)
+// the lane-slot permutation of tc_head_kernel (conflict-free stores)
 DF_DEV void t2_convert_q4(const unsigned char* rs, unsigned char* bt, int warp, int lane, bool valid) {
     unsigned char* blo = bt + kTcN * kTcKB * 2;
     const int gg = warp >> 2, rr = warp & 3;
@@ -851,12 +787,11 @@ int codes_to_f16(const int8_t* x, int ld, int T, int K, __half* out, int* norm2,
     return (int)launch(codes_to_f16_kernel, dim3(blocks), dim3(256), 0, st, x, ld, T, K, out);
 }
 
-template <bool kHead>
 static cudaError_t tc_set_smem() {
     static bool done = false;
     if (done) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<kHead>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)TcShape<kHead>::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(tc_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)TcShape::kSmem);
     if (e == cudaSuccess) done = true;
     return e;
 }
@@ -906,13 +841,13 @@ int head_tc(const int8_t* packed, const float* row_scale, int V, int ksteps, QAc
     if (!head_tc_supported(ksteps, x) || (reinterpret_cast<uintptr_t>(x16) & 15)) return (int)cudaErrorInvalidValue;
     CUtensorMap map;
     if (!act_map(&map, x16, ksteps * kI8KStep, T, kTcM)) return (int)cudaErrorInvalidValue;
-    cudaError_t e = tc_set_smem<true>();
+    cudaError_t e = tc_set_smem();
     if (e != cudaSuccess) return (int)e;
     const int mt = (T + kTcM - 1) / kTcM, ntl = (V + kTcN - 1) / kTcN;
     Q4Layout L{0, ksteps, 1};
     TcArgs args{reinterpret_cast<const uint8_t*>(packed), L, 0, V, x.scale, T, logits, ldl, 0, ksteps, row_scale,
                 keys, err_flag};
-    return (int)launch(tc_gemm_kernel<true>, dim3(mt, ntl, 1), dim3(kTcThreads), TcShape<true>::kSmem, st, map, args);
+    return (int)launch(tc_head_kernel, dim3(mt, ntl, 1), dim3(kTcThreads), TcShape::kSmem, st, map, args);
 }
 
 // a dense f16 weight copy [N][K] as a TMA tensor map: 64 x 128 boxes, 128-byte swizzle
