@@ -137,12 +137,10 @@ __global__ void __launch_bounds__(256) q4_gemm16_kernel(const uint8_t* __restric
 static size_t q4_smem_bytes(int kps) { return (size_t)16 * (kps * kQ4KStep + kXPadHalves) * sizeof(__half); }
 
 static void q4_set_smem_limits() {
-    static bool done = false;
-    if (done) return;
-    const int bytes = (int)q4_smem_bytes(kMaxKstepsPerCta);
-    cudaFuncSetAttribute(q4_gemm16_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    cudaFuncSetAttribute(q4_gemm16_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    done = true;
+    static size_t limit0 = 0, limit1 = 0;
+    const size_t bytes = q4_smem_bytes(kMaxKstepsPerCta);
+    raise_smem_limit(q4_gemm16_kernel<false>, bytes, &limit0);
+    raise_smem_limit(q4_gemm16_kernel<true>, bytes, &limit1);
 }
 
 int q4_gemm(const uint8_t* packed, Q4Layout L, int tile0, int N, QAct x, int T, float* y, int ldy, bool accumulate,

@@ -625,13 +625,9 @@ int silu_mul(const float* gu, int ld_gu, int rows, int I, float* out_f32, int ld
     if (rows >= kManyRows && out_codes && !out_f32 && rows_fit_reg(I, gu, ld_gu, nullptr, 0, out_codes, ld_codes, 16384) &&
         (reinterpret_cast<uintptr_t>(gu + I) % 16) == 0) {
         const size_t smem = (size_t)I * sizeof(float);
-        static size_t smem_set = 0;
-        if (smem > smem_set) {
-            cudaError_t e = cudaFuncSetAttribute(silu_mul_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)smem);
-            if (e != cudaSuccess) return (int)e;
-            smem_set = smem;
-        }
+        static size_t limit = 0;
+        const cudaError_t e = raise_smem_limit(silu_mul_smem_kernel, smem, &limit);
+        if (e != cudaSuccess) return (int)e;
         return (int)launch(silu_mul_smem_kernel, dim3(rows), dim3(kSiluSmemThreads), smem, st, gu, ld_gu, I, out_codes,
                            out_scale, ld_codes, out16);
     }

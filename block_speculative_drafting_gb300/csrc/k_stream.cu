@@ -299,11 +299,8 @@ int q4_stream(const uint8_t* packed, Q4Layout L, int tile0, int N, QAct x, int T
     const size_t smem = q4_stream_bytes(L);
     if (smem > 227 * 1024) return (int)cudaErrorInvalidValue;
     static size_t limit = 0;
-    if (smem > limit) {
-        cudaError_t e = cudaFuncSetAttribute(q4_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return (int)e;
-        limit = smem;
-    }
+    const cudaError_t e = raise_smem_limit(q4_stream_kernel, smem, &limit);
+    if (e != cudaSuccess) return (int)e;
     return (int)launch(q4_stream_kernel, dim3(num_sms), dim3(kQ4Threads), smem, st, packed, L, tile0 / 4, N / 64, x, T,
                        y, ldy, err_flag);
 }
@@ -520,11 +517,8 @@ int head_stream(const int8_t* packed, const float* row_scale, int V, int ksteps,
     const size_t smem = 128 + (size_t)kHeadSlots * kHeadSlotSC * kI8Super + (size_t)kConsumers * 1024 * 4 +
                         (size_t)16 * (ksteps * kI8KStep + kActPad);
     static size_t limit = 0;
-    if (smem > limit) {
-        cudaError_t e = cudaFuncSetAttribute(head_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return (int)e;
-        limit = smem;
-    }
+    const cudaError_t e = raise_smem_limit(head_stream_kernel, smem, &limit);
+    if (e != cudaSuccess) return (int)e;
     dim3 grid(std::min(num_sms, ngroups), (T + 15) / 16);
     return (int)launch(head_stream_kernel, grid, dim3(kStreamThreads), smem, st, packed, row_scale, ngroups, ksteps, V,
                        x, T, logits, ldl, keys, err_flag);

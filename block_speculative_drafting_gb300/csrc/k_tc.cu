@@ -688,20 +688,23 @@ int dequant_hilo(const int8_t* codes, const uint16_t* scales, int N, int K, __ha
 // ---------------------------------------------------------------- host side
 // (shared with the tcgen05 attention's tensor maps)
 
+std::mutex& attr_mutex() {
+    static std::mutex m;
+    return m;
+}
+
 EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
+    // looked up once (a thread-safe static initialisation)
+    static const EncodeTiledFn fn = []() -> EncodeTiledFn {
         void* p = nullptr;
         cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-        else
-            cudaGetLastError();
-    }
+            return reinterpret_cast<EncodeTiledFn>(p);
+        cudaGetLastError();
+        return nullptr;
+    }();
     return fn;
 }
 
@@ -788,12 +791,8 @@ int codes_to_f16(const int8_t* x, int ld, int T, int K, __half* out, int* norm2,
 }
 
 static cudaError_t tc_set_smem() {
-    static bool done = false;
-    if (done) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(tc_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)TcShape::kSmem);
-    if (e == cudaSuccess) done = true;
-    return e;
+    static size_t limit = 0;
+    return raise_smem_limit(tc_head_kernel, TcShape::kSmem, &limit);
 }
 
 bool q4_tc_supported(Q4Layout L, int tile0, int N, int K, QAct x) {
@@ -810,12 +809,9 @@ int q4_tc(const uint8_t* packed, Q4Layout L, int tile0, int N, QAct x, const __h
         return (int)cudaErrorInvalidValue;
     CUtensorMap map;
     if (!act_map(&map, x16, K, T, kT2Tiles * kTcM)) return (int)cudaErrorInvalidValue;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(q4_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kT2Smem);
-        if (e != cudaSuccess) return (int)e;
-        attr = true;
-    }
+    static size_t limit = 0;
+    cudaError_t e = raise_smem_limit(q4_tc2_kernel, kT2Smem, &limit);
+    if (e != cudaSuccess) return (int)e;
     const int mt = (T + kT2Tiles * kTcM - 1) / (kT2Tiles * kTcM), ntl = (N + kTcN - 1) / kTcN;
     // K slices of at most kT2MaxKb k-blocks (the accumulation bound); more
     // slices while the tiles alone leave more than a third of the SMs idle

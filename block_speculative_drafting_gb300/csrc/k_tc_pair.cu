@@ -475,6 +475,7 @@ template <bool kHead>
 static cudaError_t pair_setup(int* max_pairs) {
     static bool done[2] = {false, false};
     static int pairs[2] = {0, 0};
+    std::lock_guard<std::mutex> lock(attr_mutex());
     if (!done[kHead]) {
         cudaError_t e = cudaFuncSetAttribute(pair_tc_kernel<kHead>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)PShape<kHead>::kSmem);

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace dflash {
@@ -39,6 +41,19 @@ cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// Raises a kernel's dynamic shared-memory limit to `bytes` where `*limit` (the
+// call site's record of what it set) is below it.  One lock guards every such
+// record and call, so host threads may run the library's entry points at once.
+std::mutex& attr_mutex();
+template <typename Kernel>
+cudaError_t raise_smem_limit(Kernel kernel, size_t bytes, size_t* limit) {
+    std::lock_guard<std::mutex> lock(attr_mutex());
+    if (bytes <= *limit) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) *limit = bytes;
+    return e;
 }
 
 // Row maps: output row i reads source row  (i / per) * stride + skip + i % per.
