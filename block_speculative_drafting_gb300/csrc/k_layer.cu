@@ -205,6 +205,93 @@ __global__ void __launch_bounds__(NT, NT == kRowThreads || NV > 12 ? 1 : 2) rms_
 // Rows from which a row kernel takes the many-rows configuration.
 constexpr int kManyRows = 128;
 
+// Many rows (a batch, a prefill) quantised: a CTA of kManyThreads threads a
+// row, NV float4 of the row a thread, held in registers.  Unlike the kernels
+// above, every load (the row's and the norm weights') is issued before the
+// first use, and each block-wide reduction takes one barrier: every thread
+// folds the warps' partials itself, in the same order, into the same value.
+constexpr int kManyThreads = 512;
+
+template <bool kMax>
+DF_DEV float block_fold(float v, float* part) {
+    v = kMax ? warp_max(v) : warp_sum(v);
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float r = part[0];
+#pragma unroll
+    for (int k = 1; k < kManyThreads / 32; ++k) r = kMax ? fmaxf(r, part[k]) : r + part[k];
+    return r;
+}
+
+template <int NV, bool kW, int kMinBlocks>
+__global__ void __launch_bounds__(kManyThreads, kMinBlocks)
+    rms_rows_many_kernel(const float* __restrict__ src, int ld_src, RowMap map, int n, const float* __restrict__ w,
+                         float eps, int8_t* __restrict__ out_codes, float* __restrict__ out_scale, int ld_codes,
+                         float* zero_buf, int64_t zero_n, int rows, const float* __restrict__ div, int div_seg,
+                         __half* __restrict__ out16) {
+    __shared__ float part[2][kManyThreads / 32];  // one array a reduction: no barrier between them
+    const int n4 = n / 4;
+    pdl_trigger();
+    pdl_wait();
+    if ((int)blockIdx.x >= rows) {
+        // the CTAs past the rows clear the side buffer, float4 at a time
+        const int64_t stride = (int64_t)(gridDim.x - rows) * blockDim.x;
+        const int64_t first = (int64_t)(blockIdx.x - rows) * blockDim.x + threadIdx.x;
+        float4* p4 = reinterpret_cast<float4*>(zero_buf);
+        for (int64_t k = first; k < zero_n / 4; k += stride) p4[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (first < zero_n % 4) zero_buf[zero_n / 4 * 4 + first] = 0.f;
+        return;
+    }
+    const int i = blockIdx.x;
+    const int srow = (i / map.per) * map.stride + map.skip + (i % map.per);
+    const float4* x4 = reinterpret_cast<const float4*>(src + (int64_t)srow * ld_src);
+    float4 v[NV], g[kW ? NV : 1];
+#pragma unroll
+    for (int u = 0; u < NV; ++u) {
+        const int c = threadIdx.x + u * kManyThreads;
+        v[u] = c < n4 ? x4[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (kW) g[u] = c < n4 ? reinterpret_cast<const float4*>(w)[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (div != nullptr) {
+#pragma unroll
+        for (int u = 0; u < NV; ++u) {
+            const int c = threadIdx.x + u * kManyThreads;
+            if (c < n4) {
+                // a sum of parts: the float4's segment divided by its divisor (div_seg % 4 == 0)
+                const float d = div[(int64_t)srow * (n / div_seg) + (4 * c) / div_seg];
+                v[u] = make_float4(v[u].x / d, v[u].y / d, v[u].z / d, v[u].w / d);
+            }
+        }
+    }
+    if (kW) {
+        float ss = 0.f;
+#pragma unroll
+        for (int u = 0; u < NV; ++u) {
+            ss = fmaf(v[u].x, v[u].x, ss);
+            ss = fmaf(v[u].y, v[u].y, ss);
+            ss = fmaf(v[u].z, v[u].z, ss);
+            ss = fmaf(v[u].w, v[u].w, ss);
+        }
+        ss = block_fold<false>(ss, part[0]);
+        const float s = 1.f / sqrtf(ss / (float)n + eps);
+#pragma unroll
+        for (int u = 0; u < NV; ++u)
+            v[u] = make_float4(v[u].x * s * g[u].x, v[u].y * s * g[u].y, v[u].z * s * g[u].z, v[u].w * s * g[u].w);
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int u = 0; u < NV; ++u) amax = fmaxf(amax, amax4(v[u]));  // lanes past n hold zeros
+    amax = block_fold<true>(amax, part[1]);
+    const float sx = __fdiv_rn(amax, 127.0f);
+    uint32_t* q4 = reinterpret_cast<uint32_t*>(out_codes + (int64_t)i * ld_codes);
+#pragma unroll
+    for (int u = 0; u < NV; ++u) {
+        const int c = threadIdx.x + u * kManyThreads;
+        if (c < n4) put_codes4(q4, out16 ? out16 + (int64_t)i * n : nullptr, c, codes4(v[u], sx));
+    }
+    if (threadIdx.x == 0) out_scale[i] = sx;
+}
+
 static bool rows_fit_reg(int n, const void* src, int ld_src, const void* out_f32, int ld_out, const void* codes,
                          int ld_codes, int max_n) {
     auto al = [](const void* p, int a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; };
@@ -236,8 +323,21 @@ int rms_rows(const float* src, int ld_src, RowMap map, int rows, int n, const fl
             return (int)launch(kern, dim3(rows + extra512), dim3(512), 0, st, src, ld_src, map, n, w, eps, out_f32, ld_out,
                                out_codes, out_scale, ld_codes, zero_buf, zero_n, rows, div, div_seg, out16);
         };
-        // many rows (a batch, a prefill): 512 threads a row, so that more rows
-        // share an SM and the launch runs in fewer waves
+        // many rows (a batch, a prefill) quantised: 512 threads a row, so that
+        // more rows share an SM and the launch runs in fewer waves
+        if (rows >= kManyRows && out_codes && !out_f32 && nv512 <= 12) {
+            auto many = [&](auto kern) {
+                // (few clearing CTAs, each with more to clear: a launch of 512 rows
+                // and its side duty stay one wave at four CTAs an SM)
+                const int extra512 =
+                    zero_buf && zero_n > 0 ? (int)std::min<int64_t>(96, zero_n / 4 / (512 * 4) + 1) : 0;
+                return (int)launch(kern, dim3(rows + extra512), dim3(kManyThreads), 0, st, src, ld_src, map, n, w, eps,
+                                   out_codes, out_scale, ld_codes, zero_buf, zero_n, rows, div, div_seg, out16);
+            };
+            if (nv512 <= 2) return w ? many(rms_rows_many_kernel<2, true, 4>) : many(rms_rows_many_kernel<2, false, 4>);
+            if (nv512 <= 4) return w ? many(rms_rows_many_kernel<4, true, 2>) : many(rms_rows_many_kernel<4, false, 2>);
+            if (!w) return many(rms_rows_many_kernel<12, false, 2>);
+        }
         if (rows >= kManyRows && nv512 <= 2) return go512(rms_rows_reg_kernel<2, 512>);
         if (nv <= 1) return go(rms_rows_reg_kernel<1>);
         if (nv <= 2) return go(rms_rows_reg_kernel<2>);
@@ -539,35 +639,43 @@ __global__ void __launch_bounds__(kRowThreads) silu_mul_reg_kernel(const float* 
     if (threadIdx.x == 0) out_scale[r] = sx;
 }
 
-// Many rows (a batch, a prefill): 512 threads a row and the row's products
-// staged in shared memory instead of registers, so that four rows share an SM
-// and a launch of a few hundred rows runs in one wave.  Same arithmetic as
-// silu_mul_reg_kernel.
-constexpr int kSiluSmemThreads = 512;
-__global__ void __launch_bounds__(kSiluSmemThreads, 4)
-    silu_mul_smem_kernel(const float* __restrict__ gu, int ld_gu, int I, int8_t* __restrict__ out_codes,
+// Many rows (a batch, a prefill): kManyThreads threads a row, NV float4 of
+// the gate and of the up half a thread, every load issued before the first
+// use and the products kept in registers (two rows an SM).  Same arithmetic
+// as silu_mul_reg_kernel.
+template <int NV>
+__global__ void __launch_bounds__(kManyThreads, 2)
+    silu_mul_many_kernel(const float* __restrict__ gu, int ld_gu, int I, int8_t* __restrict__ out_codes,
                          float* __restrict__ out_scale, int ld_codes, __half* __restrict__ out16) {
-    extern __shared__ float4 arow[];
-    __shared__ float red[33];
+    __shared__ float part[kManyThreads / 32];
     pdl_trigger();
     pdl_wait();
     const int r = blockIdx.x;
     const float4* g4 = reinterpret_cast<const float4*>(gu + (int64_t)r * ld_gu);
     const float4* u4 = reinterpret_cast<const float4*>(gu + (int64_t)r * ld_gu + I);
     const int n4 = I / 4;
-    float amax = 0.f;
-#pragma unroll 2
-    for (int c = threadIdx.x; c < n4; c += kSiluSmemThreads) {
-        const float4 g = g4[c], u = u4[c];
-        const float4 a = make_float4(silu_f(g.x) * u.x, silu_f(g.y) * u.y, silu_f(g.z) * u.z, silu_f(g.w) * u.w);
-        arow[c] = a;
-        amax = fmaxf(amax, amax4(a));
+    float4 gv[NV], uv[NV];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int c = threadIdx.x + k * kManyThreads;
+        gv[k] = c < n4 ? g4[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+        uv[k] = c < n4 ? u4[c] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    amax = row_reduce_nt<true, kSiluSmemThreads>(amax, red);  // (its barriers also publish arow)
+    float amax = 0.f;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        gv[k] = make_float4(silu_f(gv[k].x) * uv[k].x, silu_f(gv[k].y) * uv[k].y, silu_f(gv[k].z) * uv[k].z,
+                            silu_f(gv[k].w) * uv[k].w);
+        amax = fmaxf(amax, amax4(gv[k]));  // lanes past I: silu(0) * 0 = 0
+    }
+    amax = block_fold<true>(amax, part);
     const float sx = __fdiv_rn(amax, 127.0f);
     uint32_t* q4 = reinterpret_cast<uint32_t*>(out_codes + (int64_t)r * ld_codes);
-    for (int c = threadIdx.x; c < n4; c += kSiluSmemThreads)
-        put_codes4(q4, out16 ? out16 + (int64_t)r * I : nullptr, c, codes4(arow[c], sx));
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int c = threadIdx.x + k * kManyThreads;
+        if (c < n4) put_codes4(q4, out16 ? out16 + (int64_t)r * I : nullptr, c, codes4(gv[k], sx));
+    }
     if (threadIdx.x == 0) out_scale[r] = sx;
 }
 
@@ -617,19 +725,24 @@ int silu_mul(const float* gu, int ld_gu, int rows, int I, float* out_f32, int ld
     if (out16 && (!out_codes || out_f32 || I % 4 || (reinterpret_cast<uintptr_t>(out16) & 7)))
         return (int)cudaErrorInvalidValue;
     // few rows: a row over a cluster of kSiluSplit CTAs; many rows: a CTA a row
-    if (rows < kManyRows && I % (4 * kSiluSplit) == 0 && I / 4 / kSiluSplit <= kRowThreads &&
-        rows_fit_reg(I, gu, ld_gu, out_f32, ld_out, out_codes, ld_codes, 4 * kSiluSplit * kRowThreads) &&
-        (reinterpret_cast<uintptr_t>(gu + I) % 16) == 0)
+    const bool cluster_ok = rows < kManyRows && I % (4 * kSiluSplit) == 0 && I / 4 / kSiluSplit <= kRowThreads &&
+                            rows_fit_reg(I, gu, ld_gu, out_f32, ld_out, out_codes, ld_codes, 4 * kSiluSplit * kRowThreads) &&
+                            (reinterpret_cast<uintptr_t>(gu + I) % 16) == 0;
+    if (cluster_ok)
         return (int)launch_cluster(silu_mul_cluster_kernel, dim3(kSiluSplit, rows), dim3(kRowThreads), 0, st,
                                    kSiluSplit, gu, ld_gu, I, out_f32, ld_out, out_codes, out_scale, ld_codes, out16);
-    if (rows >= kManyRows && out_codes && !out_f32 && rows_fit_reg(I, gu, ld_gu, nullptr, 0, out_codes, ld_codes, 16384) &&
+    if (rows >= kManyRows && out_codes && !out_f32 &&
+        rows_fit_reg(I, gu, ld_gu, nullptr, 0, out_codes, ld_codes, 8 * 4 * kManyThreads) &&
         (reinterpret_cast<uintptr_t>(gu + I) % 16) == 0) {
-        const size_t smem = (size_t)I * sizeof(float);
-        static size_t limit = 0;
-        const cudaError_t e = raise_smem_limit(silu_mul_smem_kernel, smem, &limit);
-        if (e != cudaSuccess) return (int)e;
-        return (int)launch(silu_mul_smem_kernel, dim3(rows), dim3(kSiluSmemThreads), smem, st, gu, ld_gu, I, out_codes,
-                           out_scale, ld_codes, out16);
+        const int nv = (I / 4 + kManyThreads - 1) / kManyThreads;
+        auto go = [&](auto kern) {
+            return (int)launch(kern, dim3(rows), dim3(kManyThreads), 0, st, gu, ld_gu, I, out_codes, out_scale, ld_codes,
+                               out16);
+        };
+        if (nv <= 2) return go(silu_mul_many_kernel<2>);
+        if (nv <= 4) return go(silu_mul_many_kernel<4>);
+        if (nv <= 6) return go(silu_mul_many_kernel<6>);
+        return go(silu_mul_many_kernel<8>);
     }
     if (rows_fit_reg(I, gu, ld_gu, out_f32, ld_out, out_codes, ld_codes, 4 * 4 * kRowThreads) &&
         (reinterpret_cast<uintptr_t>(gu + I) % 16) == 0) {
