@@ -6,28 +6,34 @@
 //
 // One CTA takes the unit's query rows (the rep q heads of the kv head times
 // the block rows, at most 128: the MMA's M, zero-padded) against its share of
-// the unit's keys, in steps of 64 keys:
-//   S = Q K^T    (tcgen05.mma kind::f16, M 128, N 64: three products a k16
+// the unit's keys, in steps of 128 keys:
+//   S = Q K^T    (tcgen05.mma kind::f16, M 128, N 128: three products a k16
 //                 slice, qh.kh + qh.kl + ql.kh, f32 in tensor memory),
-//   P = 2^(S * scale * log2(e) - m)   (one thread a query row, f32, online:
+//   P = 2^(S * scale * log2(e) - m)   (two threads a query row, f32, online:
 //                 m moves only when a row's maximum passes it by more than
 //                 kAtLazy, so P stays within 2^kAtLazy, and the output rows in
 //                 tensor memory are then rescaled in place),
-//   O += P V     (M 128, N = head_dim, K 64: ph.vh + ph.vl + pl.vh).
+//   O += P V     (M 128, N = head_dim, K 128: ph.vh + ph.vl + pl.vh).
 // Every operand reaches the tensor cores as the f16 (hi, lo) pair of an f32
 // value (the context store keeps its keys and values in that form already);
-// the products hi*hi + hi*lo + lo*hi keep f32-level accuracy.  Q, K and P are
-// K-major tiles in the 128-byte swizzle; V is read as stored ([key][dim]),
-// the B operand in its MN-major form.
+// the products hi*hi + hi*lo + lo*hi keep f32-level accuracy.  Q and P sit in
+// tensor memory (the A operands); K is a K-major tile in the 128-byte swizzle
+// and V is read as stored ([key][dim]), the B operand in its MN-major form.
+// Steps of 128 keys, not 64: a scores MMA of N 64 runs at two thirds of the
+// pipe's rate (measured, chained M 128 x K 16 MMAs: 24.9 ns at N 64, 33.0 ns
+// at N 128), so the larger step takes a quarter less MMA time a key.
 //
-// Roles: warps 0-3 prepare the queries (RMSNorm, rotation, split) and run the
-// softmax and the epilogue, thread t owning query row t (tensor-memory lane
-// t); warp 4 allocates the tensor memory and one of its lanes issues the MMAs;
-// warps 5-7 load the keys and values (cp.async from the store, the block's
-// own rows normed, rotated and split from qkv) into a two-stage ring.  Every
-// wait is bounded (1 s of %globaltimer): on expiry the CTA raises the error
-// flag, the roles stop, work in flight is waited for and the tensor memory
-// is freed.
+// Roles: warps 0-7 prepare the queries (RMSNorm, rotation, split; staged 64
+// rows at a time on their way to tensor memory) and run the softmax and the
+// epilogue, threads t and t + 128 owning query row t (tensor-memory lane t),
+// each one half of a step's keys; warp 8 allocates the tensor memory and one
+// of its lanes issues the MMAs; warps 9-12 move the keys and values into a
+// ring of three slots (tensor copies of the store; the block's own rows
+// normed, rotated and split from qkv by threads).  S holds one step: the MMAs
+// of the next step's scores wait until the softmax has read this step's.
+// Every wait is bounded (1 s of %globaltimer): on expiry the CTA raises the
+// error flag, the roles stop, work in flight is waited for and the tensor
+// memory is freed.
 #include <cuda.h>
 
 #include <algorithm>
@@ -40,36 +46,41 @@
 namespace dflash {
 
 constexpr int kAtM = 128;        // MMA M: a unit's query rows, zero-padded
-constexpr int kAtKeys = 64;      // keys a step: the scores' N, the values' K
+constexpr int kAtKeys = 128;     // keys a step: the scores' N, the values' K
 constexpr int kAtSoftWarps = 8;  // two threads a query row: warps w and w + 4 share tensor-memory lanes
 constexpr int kAtSoft = kAtSoftWarps * 32;
 constexpr int kAtMmaWarp = kAtSoftWarps;
 constexpr int kAtLoadWarp0 = kAtSoftWarps + 1;
-constexpr int kAtLoadWarps = 4;                   // two for the keys, two for the values
+constexpr int kAtLoadWarps = 4;                    // the block step: two write the keys, two the values
 constexpr int kAtLoaders = kAtLoadWarps / 2 * 32;  // threads of one loader group
 constexpr int kAtThreads = (kAtSoftWarps + 1 + kAtLoadWarps) * 32;  // 416
+constexpr int kAtSlots = 3;      // ring slots, each one step's keys or values (hi and lo planes)
+constexpr int kAtQRows = 64;     // query rows staged at a time on their way to tensor memory
 constexpr float kAtLazy = 8.f;   // log2 units a row's maximum may pass its reference before a rescale
 constexpr uint64_t kAtWait = 1000000000ull;
 
 template <int HD>
 struct AtShape {
-    static constexpr int KB = HD / 64;             // 64-column (128-byte) blocks of a row
-    static constexpr int kQ = kAtM * HD * 2;       // one plane of Q: KB blocks of 128 rows x 128 B
-    static constexpr int kKV = kAtKeys * HD * 2;   // one plane of a K or V tile: KB blocks of 64 rows x 128 B
-    static constexpr int kStage = 4 * kKV;         // kh, kl, vh, vl
-    static constexpr size_t kSmem = 1024 /*alignment*/ + 2048 /*control*/ + 2 * (size_t)kQ + 2 * (size_t)kStage;
-    // tensor memory: S at columns 0 and 64, O at 128, the A operands of the
-    // two products -- Q (hi, lo) and P (hi, lo), two f16 a column -- after it
+    static constexpr int KB = HD / 64;                // 64-column (128-byte) blocks of a row
+    static constexpr int kPlane = kAtKeys * HD * 2;   // a K or V plane of a step: KB blocks of 128 rows x 128 B
+    static constexpr int kItem = 2 * kPlane;          // a ring slot: the step's hi and lo planes
+    static constexpr int kQStage = kAtQRows * HD * 2;  // a staged plane of Q: KB blocks of 64 rows x 128 B
+    static constexpr size_t kSmem =
+        1024 /*alignment*/ + 2048 /*control*/ + 2 * (size_t)kQStage + (size_t)kAtSlots * kItem;
+    // tensor memory: S (the step's 128 scores a row), O, then the A operands
+    // of the two products -- Q (hi, lo) and P (hi, lo), two f16 a column
     static constexpr int kCols = 512;
-    static constexpr int kColQ = 256, kColQl = kColQ + HD / 2, kColP = 384, kColPl = kColP + kAtKeys / 2;
-    static_assert(kColQl + HD / 2 <= kColP && kColPl + kAtKeys / 2 <= kCols, "tensor memory");
+    static constexpr int kColS = 0, kColO = kAtKeys, kColQ = 256, kColQl = kColQ + HD / 2, kColP = 384,
+                         kColPl = kColP + kAtKeys / 2;
+    static_assert(kColO + HD <= kColQ && kColQl + HD / 2 <= kColP && kColPl + kAtKeys / 2 <= kCols, "tensor memory");
     static_assert(kSmem <= 227 * 1024, "shared memory");
 };
 
 struct AtCtl {
-    // per stage: keys landed / free (after the scores' MMAs), values landed /
-    // free (after the output's MMAs)
-    uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], q_ready, p_full, p_empty, fin;
+    // per ring slot: its tile landed / its MMAs done; the scores landed /
+    // read out by the softmax; Q in tensor memory; P written / its MMAs
+    // done; every MMA done
+    uint64_t full[kAtSlots], empty[kAtSlots], s_full, s_free, q_ready, p_full, p_empty, fin;
     uint32_t tmem;
     int abort;
     float xch[2][kAtM];  // the two halves of each row's step maximum (then of its softmax sum)
@@ -185,21 +196,20 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     unsigned char* sm = sm_raw + ((1024 - (smem_addr(sm_raw) & 1023)) & 1023);
     AtCtl& ctl = *reinterpret_cast<AtCtl*>(sm);
     unsigned char* qh = sm + kAtCtl;
-    unsigned char* ql = qh + S::kQ;
-    unsigned char* stage0 = ql + S::kQ;
+    unsigned char* ql = qh + S::kQStage;
+    unsigned char* ring = ql + S::kQStage;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int sp = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
     const int rep = nq / nkv, mq = rep * block_len;
     const int64_t row0 = (int64_t)s * block_len;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&ctl.k_full[i], 1);
-            mbar_init(&ctl.k_empty[i], 1);
-            mbar_init(&ctl.v_full[i], 1);
-            mbar_init(&ctl.v_empty[i], 1);
-            mbar_init(&ctl.s_full[i], 1);
+        for (int i = 0; i < kAtSlots; ++i) {
+            mbar_init(&ctl.full[i], 1);
+            mbar_init(&ctl.empty[i], 1);
         }
+        mbar_init(&ctl.s_full, 1);
+        mbar_init(&ctl.s_free, kAtSoft);
         mbar_init(&ctl.q_ready, kAtSoft);
         mbar_init(&ctl.p_full, kAtSoft);
         mbar_init(&ctl.p_empty, 1);
@@ -232,7 +242,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     const int total = sq.n + block_len;
     // this sequence's keys, the block's rows first, in nsplit equal shares;
     // a share that holds block rows starts with a step of them alone (written
-    // by threads), then its context rows go by in 64-key steps (tensor copies)
+    // by threads), then its context rows go by in 128-key steps (tensor copies)
     const int kps = (total + nsplit - 1) / nsplit;
     const int j0 = sp * kps, j1 = min(total, j0 + kps);
     const int nb = (j0 < j1 && j0 < block_len) ? 1 : 0;
@@ -242,44 +252,54 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     // step u: tile row 0's key and the end of the step's valid keys
     auto key0 = [&](int u) { return u < nb ? j0 : block_len + c0 + (u - nb) * kAtKeys; };
     auto keyend = [&](int u) { return u < nb ? min(block_len, j1) : j1; };
+    // The ring's items in the order the MMAs take them: the keys of step 0,
+    // then per step u the next step's keys (while there is one) and step u's
+    // values -- K0, K1, V0, K2, V1, ..., V(n-1).  Item n goes to slot n % 3,
+    // which the MMAs of item n - 3 have released.
+    const int nitems = 2 * nsteps;
+    auto item_v = [&](int n) { return n != 0 && (n == nitems - 1 || (n & 1) == 0); };
+    auto item_u = [&](int n) {
+        return n == 0 ? 0 : n == nitems - 1 ? nsteps - 1 : (n & 1) ? ((n - 1) >> 1) + 1 : (n - 1) >> 1;
+    };
 
     if (warp >= kAtLoadWarp0) {
         // ------------------------------------------------------------ loads
-        // two groups of two warps: the keys (planes kh, kl of each stage) and
-        // the values (vh, vl).  Context steps: one thread issues the tensor
-        // copies (64 rows x 64 columns a box, both planes), up to two steps
-        // ahead, each as soon as its stage's MMAs have read it.  The block
-        // step: the group's threads write the block's rows (keys normed and
-        // rotated) and zeros past them.
-        const int grp = (warp - kAtLoadWarp0) / 2;                   // 0 keys, 1 values
+        // Context steps: one thread issues the tensor copies of each item (64
+        // rows x 64 columns a box, both planes) as soon as its slot is free.
+        // The block step: two groups of two warps write its keys (normed and
+        // rotated) and its values from qkv, zeros past the block's rows.
+        const int grp = (warp - kAtLoadWarp0) / 2;                   // block step: 0 keys, 1 values
         const int lt = threadIdx.x - (kAtLoadWarp0 + 2 * grp) * 32;  // 0 .. 63
-        uint64_t* full = grp ? ctl.v_full : ctl.k_full;
-        uint64_t* empty = grp ? ctl.v_empty : ctl.k_empty;
-        const CUtensorMap* map = reinterpret_cast<const CUtensorMap*>(sq.maps) + grp;
-        constexpr uint32_t kTx = 2u * S::kKV;  // bytes of a step's two planes
-        auto issue_ctx = [&](int u) {
-            unsigned char* st = stage0 + (u & 1) * S::kStage + grp * 2 * S::kKV;
-            const int row = (int)sq.lo + c0 + (u - nb) * kAtKeys;
-            mbar_arrive_expect_tx(&full[u & 1], kTx);
+        const bool issuer = threadIdx.x == kAtLoadWarp0 * 32;
+        auto is_block = [&](int n) { return item_u(n) < nb; };
+        auto issue = [&](int n) {
+            const CUtensorMap* map = reinterpret_cast<const CUtensorMap*>(sq.maps) + (item_v(n) ? 1 : 0);
+            unsigned char* st = ring + (n % kAtSlots) * S::kItem;
+            const int row = (int)sq.lo + c0 + (item_u(n) - nb) * kAtKeys;
+            uint64_t* bar = &ctl.full[n % kAtSlots];
+            mbar_arrive_expect_tx(bar, (uint32_t)S::kItem);
 #pragma unroll
             for (int pl2 = 0; pl2 < 2; ++pl2)
 #pragma unroll
                 for (int kb = 0; kb < S::KB; ++kb)
-                    at_tma_4d(st + pl2 * S::kKV + kb * (kAtKeys * 128), map, kb * 64, row, g, pl2, &full[u & 1]);
+                    at_tma_4d(st + pl2 * S::kPlane + kb * (kAtKeys * 128), map, kb * 64, row, g, pl2, bar);
         };
-        int issued = nb;  // context steps issued
-        if (lt == 0 && kv_ready)
-            for (; issued < min(2, nsteps); ++issued) issue_ctx(issued);
+        int next = 0;  // the issuer's next item
+        // the first items find their slots free
+        if (issuer && kv_ready)
+            for (; next < min(kAtSlots, nitems); ++next)
+                if (!is_block(next)) issue(next);
         pdl_wait();
         if (nb) {
-            // the block step (stage 0): the block's rows [j0, min(block_len, j1)), zeros past them
-            unsigned char* st = stage0 + grp * 2 * S::kKV;
+            // the block step: keys (item 0) or values (item 2, or 1 when it is the only step)
+            const int n = grp ? (nsteps == 1 ? 1 : 2) : 0;
+            unsigned char* st = ring + (n % kAtSlots) * S::kItem;
             const int lim = min(block_len, j1) - j0;
             for (int i = lt; i < (kAtKeys - lim) * (HD / 8); i += kAtLoaders) {
                 const int kk = lim + i / (HD / 8), c = i % (HD / 8);
                 const uint32_t off = (uint32_t)((c >> 3) * (kAtKeys * 128)) + at_swz(kk, c & 7);
                 *reinterpret_cast<uint4*>(st + off) = make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4*>(st + S::kKV + off) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(st + S::kPlane + off) = make_uint4(0u, 0u, 0u, 0u);
             }
             const int lw = (warp - kAtLoadWarp0) & 1, sub = lane / D4, d4 = lane % D4, d = 4 * d4;
             float4 gk = make_float4(1.f, 1.f, 1.f, 1.f);
@@ -296,26 +316,28 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                 if (!grp && k_norm != nullptr) norm_rope4<HD>(x, mine, gk, t01, t23, d4, eps, rope != nullptr);
                 if (mine) {
                     const uint32_t off = (uint32_t)((d >> 6) * (kAtKeys * 128)) + at_swz(kr, (d & 63) >> 3) + (d & 7) * 2;
-                    split_store4(x, reinterpret_cast<__half*>(st + off), reinterpret_cast<__half*>(st + S::kKV + off));
+                    split_store4(x, reinterpret_cast<__half*>(st + off), reinterpret_cast<__half*>(st + S::kPlane + off));
                 }
             }
             fence_proxy_async_smem();
             asm volatile("bar.sync %0, %1;" ::"r"(2 + grp), "r"(kAtLoaders) : "memory");
-            if (lt == 0) mbar_arrive(&full[0]);
+            if (lt == 0) mbar_arrive(&ctl.full[n % kAtSlots]);
         }
-        if (lt == 0) {
-            for (; issued < min(2, nsteps); ++issued) issue_ctx(issued);
-            for (; issued < nsteps; ++issued) {
+        if (issuer) {
+            for (; next < nitems; ++next) {
+                if (is_block(next)) continue;
                 if (aborted()) break;
-                // the stage is free once its MMAs of step issued - 2 are done
-                if (!mbar_wait(&empty[issued & 1], ((issued >> 1) - 1) & 1, kAtWait)) {
+                // the slot is free once the MMAs of item next - 3 are done
+                if (next >= kAtSlots &&
+                    !mbar_wait(&ctl.empty[next % kAtSlots], ((next / kAtSlots) - 1) & 1, kAtWait)) {
                     give_up();
                     break;
                 }
-                issue_ctx(issued);
+                issue(next);
             }
             // no copy may still land in this CTA's memory after it exits
-            for (int u = max(nb, issued - 2); u < issued; ++u) mbar_wait(&full[u & 1], (u >> 1) & 1, kAtWait);
+            for (int n = max(0, next - kAtSlots); n < next; ++n)
+                if (!is_block(n)) mbar_wait(&ctl.full[n % kAtSlots], (n / kAtSlots) & 1, kAtWait);
         }
     } else if (warp == kAtMmaWarp) {
         // ------------------------------------------------------------ MMAs
@@ -323,49 +345,55 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             constexpr uint32_t idS = at_idesc(kAtM, kAtKeys, false), idO = at_idesc(kAtM, HD, true);
             // descriptors: built once; an operand's k16 slice is its base plus
             // the slice's byte offset / 16 (the start field never carries)
-            const uint64_t dk0 = at_desc(smem_addr(stage0), 16);
-            const uint64_t dv0 = at_desc(smem_addr(stage0) + 2 * S::kKV, kAtKeys * 128);
-            constexpr uint64_t kStageD = S::kStage >> 4, kPlaneD = S::kKV >> 4;
+            const uint64_t dk0 = at_desc(smem_addr(ring), 16);
+            const uint64_t dv0 = at_desc(smem_addr(ring), kAtKeys * 128);
+            constexpr uint64_t kItemD = S::kItem >> 4, kPlaneD = S::kPlane >> 4;
             bool ok = mbar_wait(&ctl.q_ready, 0, kAtWait);
-            // S[b] = Q K^T of step u
-            auto scores = [&](int u) -> bool {
-                if (!mbar_wait(&ctl.k_full[u & 1], (u >> 1) & 1, kAtWait)) return false;
+            int it = 0;  // the next ring item
+            // S = Q K^T of the next item's keys
+            auto scores = [&]() -> bool {
+                const int n = it++;
+                if (!mbar_wait(&ctl.full[n % kAtSlots], (n / kAtSlots) & 1, kAtWait)) return false;
                 at_fence_after();
-                const uint64_t kh = dk0 + (u & 1) * kStageD, kl = kh + kPlaneD;
-                const uint32_t d = tmem + (uint32_t)((u & 1) * kAtKeys);
+                const uint64_t kh = dk0 + (uint64_t)(n % kAtSlots) * kItemD, kl = kh + kPlaneD;
 #pragma unroll
                 for (int j = 0; j < HD / 16; ++j) {
                     // Q's k16 slice j: columns 8 j .. of its planes in tensor memory
                     const uint32_t qh_t = tmem + (uint32_t)(S::kColQ + 8 * j), ql_t = tmem + (uint32_t)(S::kColQl + 8 * j);
                     const uint64_t ko = (uint64_t)(((j >> 2) * (kAtKeys * 128) + (j & 3) * 32) >> 4);
-                    at_mma_ts(d, qh_t, kh + ko, idS, j > 0 ? 1u : 0u);
-                    at_mma_ts(d, qh_t, kl + ko, idS, 1u);
-                    at_mma_ts(d, ql_t, kh + ko, idS, 1u);
+                    at_mma_ts(tmem + S::kColS, qh_t, kh + ko, idS, j > 0 ? 1u : 0u);
+                    at_mma_ts(tmem + S::kColS, qh_t, kl + ko, idS, 1u);
+                    at_mma_ts(tmem + S::kColS, ql_t, kh + ko, idS, 1u);
                 }
-                at_commit(&ctl.s_full[u & 1]);
-                at_commit(&ctl.k_empty[u & 1]);
+                at_commit(&ctl.empty[n % kAtSlots]);
+                at_commit(&ctl.s_full);
                 return true;
             };
-            if (ok) ok = scores(0);
+            if (ok) ok = scores();
             for (int u = 0; ok && u < nsteps; ++u) {
                 if (aborted()) break;
-                if (u + 1 < nsteps && !(ok = scores(u + 1))) break;
+                if (u + 1 < nsteps) {
+                    // S holds one step: the next one's scores once the softmax has read step u's
+                    if (!(ok = mbar_wait(&ctl.s_free, u & 1, kAtWait))) break;
+                    at_fence_after();
+                    if (!(ok = scores())) break;
+                }
                 if (!(ok = mbar_wait(&ctl.p_full, u & 1, kAtWait))) break;
-                if (!(ok = mbar_wait(&ctl.v_full[u & 1], (u >> 1) & 1, kAtWait))) break;
+                const int n = it++;
+                if (!(ok = mbar_wait(&ctl.full[n % kAtSlots], (n / kAtSlots) & 1, kAtWait))) break;
                 at_fence_after();
                 // O += P V of step u: V as stored, [key][dim], the MN-major B operand
-                const uint64_t vh = dv0 + (u & 1) * kStageD, vl = vh + kPlaneD;
+                const uint64_t vh = dv0 + (uint64_t)(n % kAtSlots) * kItemD, vl = vh + kPlaneD;
 #pragma unroll
                 for (int j = 0; j < kAtKeys / 16; ++j) {
                     // P's k16 slice j (keys 16 j ..): columns 8 j .. of its planes
                     const uint32_t ph_t = tmem + (uint32_t)(S::kColP + 8 * j), pl_t = tmem + (uint32_t)(S::kColPl + 8 * j);
                     const uint64_t vo = (uint64_t)((j * 2048) >> 4);
-                    const uint32_t dO = tmem + 128;
-                    at_mma_ts(dO, ph_t, vh + vo, idO, (u > 0 || j > 0) ? 1u : 0u);
-                    at_mma_ts(dO, ph_t, vl + vo, idO, 1u);
-                    at_mma_ts(dO, pl_t, vh + vo, idO, 1u);
+                    at_mma_ts(tmem + S::kColO, ph_t, vh + vo, idO, (u > 0 || j > 0) ? 1u : 0u);
+                    at_mma_ts(tmem + S::kColO, ph_t, vl + vo, idO, 1u);
+                    at_mma_ts(tmem + S::kColO, pl_t, vh + vo, idO, 1u);
                 }
-                at_commit(&ctl.v_empty[u & 1]);
+                at_commit(&ctl.empty[n % kAtSlots]);
                 at_commit(&ctl.p_empty);
             }
             if (!ok) give_up();
@@ -378,59 +406,81 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         // ------------------------------------------------------------ queries, softmax, epilogue
         pdl_wait();
         {
-            // the unit's query rows, normed, rotated and split into Q (rows
-            // past the unit's zero): a warp takes RPW rows at once, four such
-            // groups a round with all their loads issued first
+            // the unit's query rows, normed, rotated and split, staged kAtQRows
+            // at a time and moved to tensor memory (the scores' A operand):
+            // thread (row tq, half hq) moves dims [hq HD/2, (hq + 1) HD/2) of
+            // its row, 8 dims a 16-byte chunk, 4 columns a chunk; rows past
+            // the unit's are zeros
             const int sub = lane / D4, d4 = lane % D4, d = 4 * d4;
             float4 gq = make_float4(1.f, 1.f, 1.f, 1.f);
             if (q_norm != nullptr) gq = *reinterpret_cast<const float4*>(q_norm + d);
-            constexpr int kStride = kAtSoftWarps * RPW;  // rows between a warp's groups
-#pragma unroll 1
-            for (int rb = warp * RPW; rb < kAtM; rb += 4 * kStride) {
-                float4 qv[4], t01[4], t23[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int ii = rb + e * kStride + sub;
-                    qv[e] = t01[e] = t23[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (ii < mq) {
-                        const int head = g * rep + ii / block_len, r = ii % block_len;
-                        qv[e] = *reinterpret_cast<const float4*>(qkv + (row0 + r) * ld + (int64_t)head * HD + d);
-                        if (q_norm != nullptr && rope != nullptr) rope_pairs<HD>(rope, row0 + r, d4, t01[e], t23[e]);
-                    }
-                }
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int ii = rb + e * kStride + sub;
-                    if (ii >= kAtM) break;
-                    if (q_norm != nullptr) norm_rope4<HD>(qv[e], ii < mq, gq, t01[e], t23[e], d4, eps, rope != nullptr);
-                    const uint32_t off = (uint32_t)((d >> 6) * (kAtM * 128)) + at_swz(ii, (d & 63) >> 3) + (d & 7) * 2;
-                    split_store4(qv[e], reinterpret_cast<__half*>(qh + off), reinterpret_cast<__half*>(ql + off));
-                }
-            }
-            // Q to tensor memory, the scores' A operand (read there by every
-            // step's MMAs instead of from shared memory): thread (row tq,
-            // half hq) moves dims [hq HD/2, (hq + 1) HD/2) of its row, 8 dims
-            // a 16-byte chunk, 4 columns a chunk
-            asm volatile("bar.sync 1, %0;" ::"r"(kAtSoft) : "memory");  // every row written
             const int tq = (warp & 3) * 32 + lane, hq = warp >> 2;
             const uint32_t qlane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+            constexpr int kStride = kAtSoftWarps * RPW;  // rows between a warp's groups
+            const int passes = (mq + kAtQRows - 1) / kAtQRows;
+#pragma unroll 1
+            for (int ps = 0; ps < kAtM / kAtQRows; ++ps) {
+                const int rbase = ps * kAtQRows;
+                const bool mine = tq >= rbase && tq < rbase + kAtQRows;  // (whole warps)
+                if (ps < passes) {
+                    // a warp takes RPW rows at once, four such groups a round
+                    // with all their loads issued first
+#pragma unroll 1
+                    for (int rb = warp * RPW; rb < kAtQRows; rb += 4 * kStride) {
+                        float4 qv[4], t01[4], t23[4];
 #pragma unroll
-            for (int pl2 = 0; pl2 < 2; ++pl2) {
-                const unsigned char* src = pl2 ? ql : qh;
+                        for (int e = 0; e < 4; ++e) {
+                            const int ii = rbase + rb + e * kStride + sub;
+                            qv[e] = t01[e] = t23[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (ii < mq) {
+                                const int head = g * rep + ii / block_len, r = ii % block_len;
+                                qv[e] = *reinterpret_cast<const float4*>(qkv + (row0 + r) * ld + (int64_t)head * HD + d);
+                                if (q_norm != nullptr && rope != nullptr) rope_pairs<HD>(rope, row0 + r, d4, t01[e], t23[e]);
+                            }
+                        }
 #pragma unroll
-                for (int c4 = 0; c4 < HD / 64; ++c4) {
-                    uint32_t w[16];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int cq = hq * (HD / 16) + c4 * 4 + k;  // the row's 16-byte chunk
-                        const uint4 x = *reinterpret_cast<const uint4*>(src + (cq >> 3) * (kAtM * 128) + at_swz(tq, cq & 7));
-                        w[4 * k] = x.x;
-                        w[4 * k + 1] = x.y;
-                        w[4 * k + 2] = x.z;
-                        w[4 * k + 3] = x.w;
+                        for (int e = 0; e < 4; ++e) {
+                            const int li = rb + e * kStride + sub;
+                            if (li >= kAtQRows) break;
+                            if (q_norm != nullptr)
+                                norm_rope4<HD>(qv[e], rbase + li < mq, gq, t01[e], t23[e], d4, eps, rope != nullptr);
+                            const uint32_t off =
+                                (uint32_t)((d >> 6) * (kAtQRows * 128)) + at_swz(li, (d & 63) >> 3) + (d & 7) * 2;
+                            split_store4(qv[e], reinterpret_cast<__half*>(qh + off), reinterpret_cast<__half*>(ql + off));
+                        }
                     }
-                    at_st16(qlane + (uint32_t)((pl2 ? S::kColQl : S::kColQ) + hq * (HD / 4) + c4 * 16),
-                            *reinterpret_cast<const float(*)[16]>(w));
+                    asm volatile("bar.sync 1, %0;" ::"r"(kAtSoft) : "memory");  // the pass's rows written
+                    if (mine) {
+#pragma unroll
+                        for (int pl2 = 0; pl2 < 2; ++pl2) {
+                            const unsigned char* src = pl2 ? ql : qh;
+#pragma unroll
+                            for (int c4 = 0; c4 < HD / 64; ++c4) {
+                                uint32_t w[16];
+#pragma unroll
+                                for (int k = 0; k < 4; ++k) {
+                                    const int cq = hq * (HD / 16) + c4 * 4 + k;  // the row's 16-byte chunk
+                                    const uint4 x = *reinterpret_cast<const uint4*>(src + (cq >> 3) * (kAtQRows * 128) +
+                                                                                    at_swz(tq - rbase, cq & 7));
+                                    w[4 * k] = x.x;
+                                    w[4 * k + 1] = x.y;
+                                    w[4 * k + 2] = x.z;
+                                    w[4 * k + 3] = x.w;
+                                }
+                                at_st16(qlane + (uint32_t)((pl2 ? S::kColQl : S::kColQ) + hq * (HD / 4) + c4 * 16),
+                                        *reinterpret_cast<const float(*)[16]>(w));
+                            }
+                        }
+                    }
+                    asm volatile("bar.sync 1, %0;" ::"r"(kAtSoft) : "memory");  // the staging area is read
+                } else if (mine) {
+                    const float zero[16] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f,
+                                            0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int pl2 = 0; pl2 < 2; ++pl2)
+#pragma unroll
+                        for (int c4 = 0; c4 < HD / 64; ++c4)
+                            at_st16(qlane + (uint32_t)((pl2 ? S::kColQl : S::kColQ) + hq * (HD / 4) + c4 * 16), zero);
                 }
             }
             at_wait_st();
@@ -438,7 +488,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             mbar_arrive(&ctl.q_ready);
         }
         // thread: query row t (tensor-memory lane t), key half h of each step
-        // (keys 32 h .. 32 h + 31) and output columns h HD/2 .. of the row
+        // (keys 64 h .. 64 h + 63) and output columns h HD/2 .. of the row
         const int t = (warp & 3) * 32 + lane, h = warp >> 2;
         constexpr int KH = kAtKeys / 2, OH = HD / 2;
         const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
@@ -450,13 +500,16 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         for (int u = 0; u < nsteps; ++u) {
             // every exit below is decided by a barrier reduction over the
             // softmax warps: all of them leave the loop at the same step
-            const bool got = mbar_wait(&ctl.s_full[u & 1], (u >> 1) & 1, kAtWait);
+            const bool got = mbar_wait(&ctl.s_full, u & 1, kAtWait);
             at_fence_after();
             float v[KH];
 #pragma unroll
             for (int c = 0; c < KH; c += 16)
-                at_ld16(lane_addr + (uint32_t)((u & 1) * kAtKeys + h * KH + c), *reinterpret_cast<float(*)[16]>(v + c));
+                at_ld16(lane_addr + (uint32_t)(S::kColS + h * KH + c), *reinterpret_cast<float(*)[16]>(v + c));
             at_wait_ld();
+            // the scores are in registers: their columns may take the next step's
+            at_fence_before();
+            mbar_arrive(&ctl.s_free);
             const int jb = key0(u) + h * KH, jend = keyend(u);
             float rmax = -INFINITY;
             if (!WIN && jb + KH <= jend) {
@@ -499,46 +552,43 @@ __global__ void __launch_bounds__(kAtThreads, 1)
 #pragma unroll 1
                 for (int c = 0; c < OH; c += 16) {
                     float o[16];
-                    at_ld16(lane_addr + 128u + (uint32_t)(h * OH + c), o);
+                    at_ld16(lane_addr + (uint32_t)(S::kColO + h * OH + c), o);
                     at_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 16; ++i) o[i] *= fr;
-                    at_st16(lane_addr + 128u + (uint32_t)(h * OH + c), o);
+                    at_st16(lane_addr + (uint32_t)(S::kColO + h * OH + c), o);
                 }
                 at_wait_st();
             }
             l *= f;
             m_ref = m_new;
             // P of the row's key half: (hi, lo) f16 pairs, two keys a
-            // tensor-memory column (the A operand of O += P V)
-            uint32_t phw[KH / 2], plw[KH / 2];
+            // tensor-memory column (the A operand of O += P V), 32 keys a store
 #pragma unroll
-            for (int c8 = 0; c8 < KH / 8; ++c8) {
-                float p[8];
+            for (int c32 = 0; c32 < KH / 32; ++c32) {
+                uint32_t phw[16], plw[16];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float x = v[c8 * 8 + i];
-                    p[i] = (x == -INFINITY) ? 0.f : at_exp2(x - m_ref);
-                    l += p[i];
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    float p[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float x = v[c32 * 32 + c8 * 8 + i];
+                        p[i] = (x == -INFINITY) ? 0.f : at_exp2(x - m_ref);
+                        l += p[i];
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const __half2 hh = __floats2half2_rn(p[2 * i], p[2 * i + 1]);
+                        const float2 hf = __half22float2(hh);
+                        const __half2 lo2 = __floats2half2_rn(p[2 * i] - hf.x, p[2 * i + 1] - hf.y);
+                        phw[c8 * 4 + i] = *reinterpret_cast<const uint32_t*>(&hh);
+                        plw[c8 * 4 + i] = *reinterpret_cast<const uint32_t*>(&lo2);
+                    }
                 }
-                uint32_t hw[4], lw[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const __half2 hh = __floats2half2_rn(p[2 * i], p[2 * i + 1]);
-                    const float2 hf = __half22float2(hh);
-                    const __half2 ll = __floats2half2_rn(p[2 * i] - hf.x, p[2 * i + 1] - hf.y);
-                    hw[i] = *reinterpret_cast<const uint32_t*>(&hh);
-                    lw[i] = *reinterpret_cast<const uint32_t*>(&ll);
-                }
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    phw[c8 * 4 + i] = hw[i];
-                    plw[c8 * 4 + i] = lw[i];
-                }
+                at_st16(lane_addr + (uint32_t)(S::kColP + h * (KH / 2) + c32 * 16), *reinterpret_cast<const float(*)[16]>(phw));
+                at_st16(lane_addr + (uint32_t)(S::kColPl + h * (KH / 2) + c32 * 16),
+                        *reinterpret_cast<const float(*)[16]>(plw));
             }
-            static_assert(KH / 2 == 16, "a key half is one 16-column store a plane");
-            at_st16(lane_addr + (uint32_t)(S::kColP + h * (KH / 2)), *reinterpret_cast<const float(*)[16]>(phw));
-            at_st16(lane_addr + (uint32_t)(S::kColPl + h * (KH / 2)), *reinterpret_cast<const float(*)[16]>(plw));
             at_wait_st();
             at_fence_before();
             mbar_arrive(&ctl.p_full);
@@ -560,7 +610,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
 #pragma unroll 1
                 for (int c = 0; c < OH; c += 16) {
                     float o[16];
-                    at_ld16(lane_addr + 128u + (uint32_t)(h * OH + c), o);
+                    at_ld16(lane_addr + (uint32_t)(S::kColO + h * OH + c), o);
                     at_wait_ld();
                     if (live)
 #pragma unroll
