@@ -1165,7 +1165,7 @@ int dflash_seq_new(dflash_model* m, int64_t max_ctx_rows, dflash_seq** out) {
     if (e == cudaSuccess) e = cudaMemcpy(s->k_dev, s->k.data(), L * sizeof(__half*), cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemcpy(s->v_dev, s->v.data(), L * sizeof(__half*), cudaMemcpyHostToDevice);
     // every stored value finite from the start: the tcgen05 attention's
-    // tensor copies read whole 64-row boxes, rows past the context included
+    // tensor copies read whole 128-row boxes, rows past the context included
     // (their weights are exactly zero, and 0 times a finite value is 0)
     for (int l = 0; l < L && e == cudaSuccess; ++l) {
         e = cudaMemset(s->k[l], 0, 2 * per * sizeof(__half));

@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
 
     if (warp >= kAtLoadWarp0) {
         // ------------------------------------------------------------ loads
-        // Context steps: one thread issues the tensor copies of each item (64
+        // Context steps: one thread issues the tensor copies of each item (128
         // rows x 64 columns a box, both planes) as soon as its slot is free.
         // The block step: two groups of two warps write its keys (normed and
         // rotated) and its values from qkv, zeros past the block's rows.
@@ -658,7 +658,7 @@ int attn_tc_plan(int n_seqs, int block_len, int max_ctx, int nkv, int num_sms) {
 bool kv_tensor_maps(const __half* k, const __half* v, int nkv, int64_t cap, int hd, void* out) {
     EncodeTiledFn enc = encode_fn();
     if (!enc || (hd != 64 && hd != 128) || cap < 1 || (reinterpret_cast<uintptr_t>(out) & 63)) return false;
-    // [plane][kv][cap][hd]: 64 x 64 boxes of (head_dim, rows), one kv head and plane a box
+    // [plane][kv][cap][hd]: boxes of 64 head_dim columns x kAtKeys rows, one kv head and plane a box
     const cuuint64_t dims[4] = {(cuuint64_t)hd, (cuuint64_t)cap, (cuuint64_t)nkv, 2};
     const cuuint64_t strides[3] = {(cuuint64_t)hd * 2, (cuuint64_t)cap * hd * 2, (cuuint64_t)nkv * cap * hd * 2};
     const cuuint32_t box[4] = {64, (cuuint32_t)kAtKeys, 1, 1};
