@@ -970,7 +970,7 @@ def test_tc_attention_block_matches_oracle(name, forced):
 def test_tc_attention_windows_and_batches_match_oracle(forced):
     """Windowed layers (the row-dependent mask of the context steps), a layer
     without the rotary position, several sequences of different lengths (an
-    empty one included) and a context longer than one 64-key step."""
+    empty one included) and a context longer than one 128-key step."""
     p = _tc_pair("small_q4", windows=(3, 0), no_rope=(1,))
     g = p.g
     lens = [77, 0, 200, 9]
@@ -979,6 +979,22 @@ def test_tc_attention_windows_and_batches_match_oracle(forced):
         sc.append(i, 0, W.make_taps(g, n, call_id=110 + i))
     sc.block(list(range(len(lens))), [(29 * i + 3) % g.vocab for i in range(len(lens))], lens, g.block)
     sc.block([2], [17], [200], 9)
+    sc.run(forced).check(forced)
+
+
+@pytest.mark.parametrize("name,heads", [("small_q4", 12), ("small_q4", 16), ("small_q4_hd64", 27)])
+@pytest.mark.parametrize("forced", [True, False])
+def test_tc_attention_wide_query_tiles(name, heads, forced):
+    """More than 64 query rows a kv head (q heads a kv head times the block's
+    rows: 96, 128 and 72; the query tile reaches tensor memory in two staged
+    passes of 64 rows, and at 128 the MMA's M is full), with a context of
+    several 128-key steps and a second, shorter block."""
+    p = _tc_pair(name, heads=heads)
+    g, n = p.g, 300
+    sc = Script(p, 1, n + 16)
+    sc.append(0, 0, W.make_taps(g, n))
+    sc.block([0], [int(W.make_anchors(g, 1)[0])], [n], g.block)
+    sc.block([0], [9], [n], g.block - 5)
     sc.run(forced).check(forced)
 
 
