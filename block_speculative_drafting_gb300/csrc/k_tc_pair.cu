@@ -519,15 +519,17 @@ int q4_tc_dense(const __half* hi, const __half* lo, int N, int K, QAct x, const 
     if (e != cudaSuccess) return (int)e;
     const int ksteps = K / kPKB, mt = (T + 255) / 256, ntl = (N + kPN - 1) / kPN;
     // K slices of at most kPMaxKb k-blocks: of those, the count whose rounds
-    // of units over the pairs, times a unit's k-blocks (plus one for its
-    // accumulator hand-over), is least
+    // of units over the pairs, times a unit's k-blocks (plus three for its
+    // accumulator hand-over and the reduction of its partial tile into y:
+    // measured on the batched step, a charge of one chose five slices for the
+    // gate/up matrix where three run faster, and none many more), is least
     const int s_min = (ksteps + kPMaxKb - 1) / kPMaxKb;
     int splits = s_min, kps = (ksteps + s_min - 1) / s_min;
     int64_t best = INT64_MAX;
     for (int sp = s_min; sp <= std::min(ksteps, 8 * s_min); ++sp) {
         const int k = (ksteps + sp - 1) / sp, real = (ksteps + k - 1) / k;
         const int64_t rounds = ((int64_t)mt * ntl * real + max_pairs - 1) / max_pairs;
-        const int64_t cost = rounds * (k + 1);
+        const int64_t cost = rounds * (k + 3);
         if (cost < best) {
             best = cost;
             splits = real;
