@@ -251,15 +251,6 @@ DF_DEV void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, ui
           "f"(c[3]));
 }
 
-// D = A(16x32 s8) * B(32x8 s8) + C, s32 accumulate.
-DF_DEV void mma_s8_16832(int (&d)[4], const uint4& a, uint32_t b0, uint32_t b1) {
-    asm(
-        "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
-        : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
-}
-
 // Streaming 16-byte load that skips L1 (weights are read once per launch).
 DF_DEV uint4 ldg_stream_v4(const void* p) {
     uint4 v;

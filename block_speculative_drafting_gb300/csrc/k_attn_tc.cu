@@ -103,14 +103,8 @@ DF_DEV uint64_t at_desc(uint32_t saddr, uint32_t lbo) {
 // byte offset of the 16-byte chunk c of row r in a 128-byte-swizzled block
 DF_DEV uint32_t at_swz(int r, int c) { return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4)); }
 
-DF_DEV void at_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// the same with the A operand in tensor memory (lane = row, two f16 a column)
+// tcgen05.mma kind::f16 with the A operand in tensor memory (lane = row, two
+// f16 a column) and B in shared memory by its descriptor
 DF_DEV void at_mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
@@ -174,10 +168,6 @@ DF_DEV float at_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-// 16-byte cp.async that reads src_bytes (0 or 16) and zero-fills the rest
-DF_DEV void at_cp16(uint32_t dst, const void* src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
 
 // CTA (split sp, kv head g, sequence s).  yacc / lacc as the accumulate mode

@@ -123,8 +123,6 @@ __global__ void __launch_bounds__(kRowThreads) rms_rows_kernel(const float* __re
 // The same in one read: the row sits in registers (NV float4 per thread) from
 // the load to the codes.  Rows must be 16-byte aligned, n % 4 == 0 and
 // n <= 4 * NV * kRowThreads.
-DF_DEV bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
-
 template <int NV, int NT = kRowThreads>
 __global__ void __launch_bounds__(NT, NT == kRowThreads || NV > 12 ? 1 : 2) rms_rows_reg_kernel(const float* __restrict__ src, int ld_src, RowMap map,
                                                                    int n, const float* __restrict__ w, float eps,
