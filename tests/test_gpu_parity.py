@@ -972,19 +972,21 @@ def test_tc_attention_block_matches_oracle(name, forced):
     sc.run(forced).check(forced)
 
 
+@pytest.mark.parametrize("name", ["small_q4", "small_q4_hd64"])
 @pytest.mark.parametrize("forced", [True, False])
-def test_tc_attention_windows_and_batches_match_oracle(forced):
+def test_tc_attention_windows_and_batches_match_oracle(name, forced):
     """Windowed layers (the row-dependent mask of the context steps), a layer
     without the rotary position, several sequences of different lengths (an
-    empty one included) and a context longer than one 128-key step."""
-    p = _tc_pair("small_q4", windows=(3, 0), no_rope=(1,))
+    empty one included) and a context longer than one 128-key step; head_dim
+    128 and 64."""
+    p = _tc_pair(name, windows=(3, 0), no_rope=(1,))
     g = p.g
     lens = [77, 0, 200, 9]
     sc = Script(p, len(lens), 224)
     for i, n in enumerate(lens):
         sc.append(i, 0, W.make_taps(g, n, call_id=110 + i))
     sc.block(list(range(len(lens))), [(29 * i + 3) % g.vocab for i in range(len(lens))], lens, g.block)
-    sc.block([2], [17], [200], 9)
+    sc.block([2], [17], [200], min(9, g.block - 1))
     sc.run(forced).check(forced)
 
 
