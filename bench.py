@@ -138,7 +138,8 @@ def ncu_traffic(kernel, workload):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+    """nvidia-smi clocks and throttle reasons, sampled every 20 ms (a timed
+    region of a few hundred steps still holds several samples)."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -153,7 +154,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -163,6 +164,16 @@ class ClockSampler:
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append((time.time(), line.strip()))
+
+    def wait_first(self, limit_s=5.0):
+        """Until the first sample is in (nvidia-smi has initialised), at most
+        limit_s: its start-up, if it overlapped the timed steps, could hold
+        up this process's CUDA calls."""
+        t0 = time.time()
+        while self.proc is not None and not self.lines and time.time() - t0 < limit_s:
+            if self.proc.poll() is not None:
+                break
+            time.sleep(0.02)
 
     def stop(self):
         if self.proc:
@@ -186,7 +197,7 @@ class ClockSampler:
                 continue
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        inside = [r for r in rows if t0 - 0.15 <= r[0] <= t1 + 0.15] or rows
+        inside = [r for r in rows if t0 - 0.03 <= r[0] <= t1 + 0.03] or rows
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({n for r in inside for n, v in zip(names, r[3]) if v.lower().startswith("active")})
         return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
@@ -520,7 +531,7 @@ def run_ours(args, wl):
     dev = torch.device("cuda", local)
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
-    time.sleep(0.3)
+    clocks.wait_first()
     cpu_leg = rank == 0 and world == 1 and not args.no_cpu_baseline
     main_line = measure(args, wl, model, dev, world, dist, clocks, weights, cpu_leg)
     # the other full-size configurations of the same drafter, each timed the

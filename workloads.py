@@ -129,6 +129,10 @@ WORKLOADS = {
     # layer and a 64-row context: a few GB on the device, for profiler captures
     "qwen3_8b_l1_batch32_ctx64": Workload("qwen3_8b_l1_batch32_ctx64", Geometry(**dict(QWEN3_8B_DRAFT, layers=1)),
                                           ctx=64, n_seqs=32),
+    # the 1024-row prefill's FC (the same matrix at any layer count) with one
+    # layer: a few GB on the device, for profiler captures
+    "qwen3_8b_l1_prefill1024": Workload("qwen3_8b_l1_prefill1024", Geometry(**dict(QWEN3_8B_DRAFT, layers=1)),
+                                        ctx=0, prefill=1024),
     # small quantised shapes the oracle finishes in seconds: several tiles and
     # ragged tails (vocab and context not multiples of any tile)
     "small_q4": Workload("small_q4", Geometry(hidden=512, intermediate=1536, layers=2, heads=8, kv_heads=2,
